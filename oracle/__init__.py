@@ -1,0 +1,208 @@
+"""CPU oracle for the DARTree supertree build -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package.  The product library never
+does, and the oracle never imports the product library: the two share only
+the seeded inputs of ``speculative_decoding_draft_06_gb300.inputs``.
+
+The arithmetic lives in ``dartree_oracle.c`` (plain single-threaded C, built
+with ``-ffp-contract=off``); this module compiles it with gcc and marshals
+numpy arrays through ctypes.  See the C file for the method and citations.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dartree_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libdartree_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ORC_OK, ORC_ERR_ARG, ORC_ERR_CLOSURE, ORC_ERR_ORDER, ORC_ERR_MEM = 0, 1, 2, 3, 4
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (gcc, portable flags only)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-Wall", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, f32 = ctypes.c_int32, ctypes.c_float
+        lib.orc_version.restype = ctypes.c_int
+        lib.orc_round_bf16.argtypes = [f32]
+        lib.orc_round_bf16.restype = f32
+        lib.orc_state_step.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, i32, P]
+        lib.orc_state_step.restype = None
+        lib.orc_logits_row.argtypes = [ctypes.c_int] * 3 + [P] * 5
+        lib.orc_logits_row.restype = None
+        lib.orc_topk_row.argtypes = [ctypes.c_int, P, ctypes.c_int, P, P, P]
+        lib.orc_topk_row.restype = None
+        lib.orc_pool_size.argtypes = [ctypes.c_int] * 3
+        lib.orc_pool_size.restype = ctypes.c_int
+        lib.orc_build.argtypes = [ctypes.c_int] * 6 + [P] * 20
+        lib.orc_build.restype = ctypes.c_int
+        lib.orc_topb.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_int, f32] + [P] * 7
+        lib.orc_topb.restype = ctypes.c_int
+        lib.orc_heap_prune.argtypes = [ctypes.c_int, P, P, P, ctypes.c_int, f32, P]
+        lib.orc_heap_prune.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _weights(a: np.ndarray, bf16: bool) -> np.ndarray:
+    return _c(a, np.uint16 if bf16 else np.float32)
+
+
+def round_bf16(x: float) -> float:
+    return float(_load().orc_round_bf16(ctypes.c_float(x)))
+
+
+def pool_size(D: int, W: int, K: int) -> int:
+    return int(_load().orc_pool_size(D, W, K))
+
+
+def state_step(A, E, s_par, tok: int, bf16: bool) -> np.ndarray:
+    """One head state update q(tanh(A s_par + E[tok])) -> fp32 [H]."""
+    H = A.shape[0]
+    A, E = _weights(A, bf16), _weights(E, bf16)
+    s = _c(s_par, np.float32)
+    out = np.empty(H, np.float32)
+    _load().orc_state_step(H, int(bf16), _ptr(A), _ptr(E), _ptr(s), tok, _ptr(out))
+    return out
+
+
+def logits_row(z_d, Wout, s, bf16: bool):
+    """Corrected logits (fp32 [V]) and their log-sum-exp (float, fp64)."""
+    V, H = Wout.shape
+    z_d, Wout, s = _c(z_d, np.float32), _weights(Wout, bf16), _c(s, np.float32)
+    ell = np.empty(V, np.float32)
+    lse = np.zeros(1, np.float64)
+    _load().orc_logits_row(V, H, int(bf16), _ptr(z_d), _ptr(Wout), _ptr(s),
+                           _ptr(ell), _ptr(lse))
+    return ell, float(lse[0])
+
+
+def topk_row(ell, K: int):
+    """Top-K (tokens, values) by (value desc, token asc) and the K/K+1 gap."""
+    ell = _c(ell, np.float32)
+    tok = np.empty(K, np.int32)
+    val = np.empty(K, np.float32)
+    gap = np.zeros(1, np.float32)
+    _load().orc_topk_row(ell.shape[0], _ptr(ell), K, _ptr(tok), _ptr(val), _ptr(gap))
+    return tok, val, float(gap[0])
+
+
+def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
+               force_slot=None, force_tok=None) -> dict:
+    """Depth-wise supertree construction for request ``r`` of ``inp``.
+
+    ``force_slot`` / ``force_tok`` ([P] each, pool layout) force the kept
+    frontier at every depth (teacher forcing).  Returns the kept pool, the
+    oracle's own per-depth selection, per-row results and diagnostics.
+    """
+    z = _c(inp["z"][r, :D], np.float32)
+    V = z.shape[1]
+    H = inp["A"].shape[0]
+    s0 = _c(inp["state0"][r], np.float32)
+    A, E, Wo = (_weights(inp[k], bf16) for k in ("A", "E", "Wout"))
+    P = pool_size(D, W, K)
+    o = {k: np.empty(P, np.int32) for k in
+         ("pool_parent", "pool_token", "pool_depth", "own_slot", "own_tok")}
+    o.update({k: np.empty(P, np.float32) for k in
+              ("pool_score", "own_score", "force_margin")})
+    o["row_lse"] = np.full(D * W, np.nan, np.float64)
+    o["row_tok"] = np.full(D * W * K, -1, np.int32)
+    o["row_logp"] = np.full(D * W * K, np.nan, np.float32)
+    o["row_kgap"] = np.full(D * W, np.nan, np.float32)
+    o["w_cut"] = np.empty(2 * D, np.float32)
+    calls = np.zeros(1, np.int64)
+    fs = ft = None
+    if force_slot is not None:
+        fs, ft = _c(force_slot, np.int32), _c(force_tok, np.int32)
+    rc = _load().orc_build(
+        V, H, D, W, K, int(bf16), _ptr(z), _ptr(s0), _ptr(A), _ptr(E), _ptr(Wo),
+        _ptr(fs), _ptr(ft),
+        _ptr(o["pool_parent"]), _ptr(o["pool_token"]), _ptr(o["pool_depth"]),
+        _ptr(o["pool_score"]), _ptr(o["own_slot"]), _ptr(o["own_tok"]),
+        _ptr(o["own_score"]), _ptr(o["force_margin"]), _ptr(o["row_lse"]),
+        _ptr(o["row_tok"]), _ptr(o["row_logp"]), _ptr(o["row_kgap"]),
+        _ptr(o["w_cut"]), _ptr(calls))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_build failed with code {rc}")
+    o["row_lse"] = o["row_lse"].reshape(D, W)
+    o["row_tok"] = o["row_tok"].reshape(D, W, K)
+    o["row_logp"] = o["row_logp"].reshape(D, W, K)
+    o["row_kgap"] = o["row_kgap"].reshape(D, W)
+    o["w_cut"] = o["w_cut"].reshape(D, 2)
+    o["calls"] = int(calls[0])
+    return o
+
+
+def topb(pool_parent, pool_token, pool_depth, pool_score, B: int, beta: float) -> dict:
+    """Deferred Top-B, compaction and ancestor mask over one request's pool."""
+    pp, pt, pd = (_c(a, np.int32) for a in (pool_parent, pool_token, pool_depth))
+    ps = _c(pool_score, np.float32)
+    P = pp.shape[0]
+    words = (B + 31) // 32
+    o = {"parent": np.empty(B, np.int32), "token": np.empty(B, np.int32),
+         "depth": np.empty(B, np.int32), "score": np.empty(B, np.float32),
+         "mask": np.empty(B * words, np.uint32), "order": np.full(B, -1, np.int32)}
+    n = np.zeros(1, np.int32)
+    rc = _load().orc_topb(P, _ptr(pp), _ptr(pt), _ptr(pd), _ptr(ps), B,
+                          ctypes.c_float(beta), _ptr(o["parent"]), _ptr(o["token"]),
+                          _ptr(o["depth"]), _ptr(o["score"]), _ptr(o["mask"]),
+                          _ptr(n), _ptr(o["order"]))
+    o["n_out"] = int(n[0])
+    o["rc"] = rc
+    o["mask"] = o["mask"].reshape(B, words)
+    return o
+
+
+def heap_prune(pool_parent, pool_depth, pool_score, B: int, beta: float) -> np.ndarray:
+    """Sequential best-first max-heap pruning; returns the pop order."""
+    pp, pd = _c(pool_parent, np.int32), _c(pool_depth, np.int32)
+    ps = _c(pool_score, np.float32)
+    out = np.full(B, -1, np.int32)
+    n = _load().orc_heap_prune(pp.shape[0], _ptr(pp), _ptr(pd), _ptr(ps), B,
+                               ctypes.c_float(beta), _ptr(out))
+    if n < 0:
+        raise MemoryError("orc_heap_prune")
+    return out[:n]
+
+
+def build_request(inp: dict, r: int, D: int, W: int, K: int, B: int,
+                  beta: float, bf16: bool) -> dict:
+    """Full oracle pipeline for one request: construction then pruning."""
+    t = build_tree(inp, r, D, W, K, bf16)
+    t["tree"] = topb(t["pool_parent"], t["pool_token"], t["pool_depth"],
+                     t["pool_score"], B, beta)
+    return t

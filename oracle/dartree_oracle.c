@@ -1,0 +1,474 @@
+/*
+ * DARTree supertree oracle: a plain, slow, single-threaded CPU definition of
+ * what the GPU build computes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls this file.
+ * Only the tests, the package smoke check and the bench's CPU-baseline /
+ * reference leg load it.  It shares no code, header, table or constant with
+ * the CUDA path; both sides are fed the same seeded host arrays.
+ *
+ * Sources (page title -- section):
+ *   [P1] "DARTree: Teaching a Chain-Trained Corrector to Think in Trees"
+ *        -- Core Mechanism (level-by-level construction; best-first pruning
+ *        over cached scores), Key Concepts (marginal vs conditional),
+ *        Framework Shift (head calls = O(depth)).
+ *   [P2] "Technische Samenvatting: DARTree" -- Methodologie, 1. Depth-Wise
+ *        Parallel AR Expansie (batched correction, cumulative corrected
+ *        score, keep top-W and carry correction states) and 2. Deferred
+ *        Best-First Pruning (one global Top-B over all materialised prefixes;
+ *        Lemma 1: with a non-positive depth bonus it equals a sequential
+ *        best-first max-heap).
+ *   [P3] "Accelerating Language Models with Diffusion Draft Trees" -- Summary
+ *        & Methodology Analysis (global top-W child prefixes per depth, state
+ *        update, global top-B, prefix tree verified with a tree-attention
+ *        mask).
+ *
+ * The correction head's architecture is not given by the pages.  The fixed
+ * synthetic stand-in used throughout is
+ *      s'      = q(tanh(A s + E[tok]))          (state after committing tok)
+ *      logits  = z_d + s' Wout^T                 (corrected logits at depth d)
+ * with q() = round to bf16 (nearest, ties to even) when the weights are bf16
+ * and the identity when they are fp32.  The root state is q(state0).
+ *
+ * Precision (readings where the pages are silent): every dot product, the
+ * tanh and the log-sum-exp are evaluated in double; logits and log-probs are
+ * rounded to fp32 once; cumulative scores and Top-B keys are single fp32
+ * operations in the stated order.  Build with -ffp-contract=off so that no
+ * multiply-add is fused.
+ *
+ * Orders (readings; the pages give no tie-breaks):
+ *   top-K of a row      : (logit desc, token asc)
+ *   top-W of candidates : (score desc, candidate index i*K+j asc)
+ *   Top-B of the pool   : (key desc, pool index asc), key = score + beta*depth
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_CLOSURE 2
+#define ORC_ERR_ORDER 3
+#define ORC_ERR_MEM 4
+
+int orc_version(void) { return 1; }
+
+/* ---------------------------------------------------------------- helpers */
+
+/* bf16 bit pattern -> value: the 16 bits are the top half of an fp32. */
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double weight(const void *w, int bf16, size_t i) {
+    if (bf16) return bf16_to_double(((const uint16_t *)w)[i]);
+    return (double)((const float *)w)[i];
+}
+
+/* Round an fp32 value to bf16 precision, nearest with ties to even, by its
+ * definition: keep the top 16 bits, adding half an ulp of the kept part
+ * (minus one when the kept part is even, so that exact halves go to even). */
+float orc_round_bf16(float x) {
+    uint32_t u;
+    if (x != x) {                                    /* NaN stays a NaN */
+        u = 0x7FC00000u;
+    } else {                                         /* finite or inf */
+        memcpy(&u, &x, sizeof u);
+        uint32_t lsb = (u >> 16) & 1u;
+        u += 0x7FFFu + lsb;
+        u &= 0xFFFF0000u;
+    }
+    float r;
+    memcpy(&r, &u, sizeof r);
+    return r;
+}
+
+static float qstate(int bf16, float x) { return bf16 ? orc_round_bf16(x) : x; }
+
+/* "a is better than b" under (value desc, index asc). */
+static int better(float va, int64_t ia, float vb, int64_t ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+/* ------------------------------------------------------- head (stand-in) */
+
+/* State after committing token tok on top of the parent's state:
+ * s_out[h] = q( tanh( sum_j A[h,j] s_par[j] + E[tok,h] ) ).
+ * [P2] Methodologie 1 ("carries their correction states forward"),
+ * [P3] Summary ("updates their states"). */
+void orc_state_step(int H, int bf16, const void *A, const void *E,
+                    const float *s_par, int32_t tok, float *s_out) {
+    for (int h = 0; h < H; ++h) {
+        double u = 0.0;
+        for (int j = 0; j < H; ++j)
+            u += weight(A, bf16, (size_t)h * H + j) * (double)s_par[j];
+        u += weight(E, bf16, (size_t)tok * H + h);
+        s_out[h] = qstate(bf16, (float)tanh(u));
+    }
+}
+
+/* Corrected logits of one path and their log-sum-exp over the vocabulary.
+ * ell[v] = fp32( z_d[v] + sum_h s[h] Wout[v,h] );
+ * lse    = m + log sum_v exp(ell[v] - m), m = max ell, in double.
+ * [P1] Core Mechanism ("W corrected conditional distributions, each properly
+ * conditioned on the tokens along its own branch"). */
+void orc_logits_row(int V, int H, int bf16, const float *z_d, const void *Wout,
+                    const float *s, float *ell, double *lse) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double acc = (double)z_d[v];
+        for (int h = 0; h < H; ++h)
+            acc += (double)s[h] * weight(Wout, bf16, (size_t)v * H + h);
+        ell[v] = (float)acc;
+        if ((double)ell[v] > m) m = (double)ell[v];
+    }
+    if (m == -INFINITY) { *lse = -INFINITY; return; }
+    double sum = 0.0;
+    for (int v = 0; v < V; ++v) sum += exp((double)ell[v] - m);
+    *lse = m + log(sum);
+}
+
+/* Top-K of one row by (logit desc, token asc), by insertion into a sorted
+ * list.  gap = ell_(K) - ell_(K+1) (+inf when V == K).
+ * [P1] Core Mechanism ("Expand each node by its top-k children"). */
+void orc_topk_row(int V, const float *ell, int K, int32_t *tok, float *val,
+                  float *gap) {
+    int n = 0;
+    for (int v = 0; v < V; ++v) {
+        if (n == K && !better(ell[v], v, val[K - 1], tok[K - 1])) continue;
+        int p = (n < K) ? n : K - 1;
+        while (p > 0 && better(ell[v], v, val[p - 1], tok[p - 1])) {
+            val[p] = val[p - 1];
+            tok[p] = tok[p - 1];
+            --p;
+        }
+        val[p] = ell[v];
+        tok[p] = v;
+        if (n < K) ++n;
+    }
+    /* the (K+1)-th value: best entry not in the list */
+    float next = -INFINITY;
+    int32_t next_tok = -1;
+    for (int v = 0; v < V; ++v) {
+        int in = 0;
+        for (int j = 0; j < K; ++j)
+            if (tok[j] == v) { in = 1; break; }
+        if (in) continue;
+        if (next_tok < 0 || better(ell[v], v, next, next_tok)) {
+            next = ell[v];
+            next_tok = v;
+        }
+    }
+    *gap = (next_tok < 0) ? INFINITY : val[K - 1] - next;
+}
+
+/* --------------------------------------------------------- construction */
+
+typedef struct { float c; int32_t idx; } cand_t;
+
+static int cand_cmp(const void *a, const void *b) {
+    const cand_t *x = (const cand_t *)a, *y = (const cand_t *)b;
+    if (better(x->c, x->idx, y->c, y->idx)) return -1;
+    if (better(y->c, y->idx, x->c, x->idx)) return 1;
+    return 0;
+}
+
+/* Frontier sizes: |F_0| = 1, |F_d| = min(W, K |F_{d-1}|). */
+static int frontier(int d, int W, int K) {
+    int f = 1;
+    for (int i = 0; i < d; ++i) f = (K * f < W) ? K * f : W;
+    return f;
+}
+
+int orc_pool_size(int D, int W, int K) {
+    int p = 0;
+    for (int d = 1; d <= D; ++d) p += frontier(d, W, K);
+    return p;
+}
+
+/*
+ * Depth-wise batched construction of the supertree for one request.
+ * [P1] Core Mechanism: at depth d the W surviving paths go through the head
+ * in ONE call; each is expanded by its top-k children (W*k candidates),
+ * scored by accumulated path probability; the top W are kept; after D levels
+ * exactly D head calls have been made and a pool of scored nodes is held.
+ * [P2] Methodologie 1 and [P3] Summary: global top-W child prefixes per
+ * depth, correction states carried forward.
+ *
+ * Inputs: z [D,V] fp32, state0 [H] fp32, A [H,H], E [V,H], Wout [V,H]
+ * (bf16 bits or fp32).  Depth 1 has |F_1| = min(W, K) nodes.
+ *
+ * Teacher forcing: when force_slot/force_tok are given ([P] each, laid out
+ * like the pool), the frontier kept at each depth is the forced one (parent
+ * slot in F_{d-1}, token) instead of the oracle's own top-W; the oracle still
+ * records its own choice and scores the forced nodes in its own arithmetic.
+ *
+ * Outputs ([P] = pool size, rows = W per depth):
+ *   pool_parent/token/depth/score [P]: the pool that was kept, pool index =
+ *       depth-major, rank order within a depth; parent -1 at depth 1.
+ *   own_slot/own_tok/own_score [P]: the oracle's own top-W at each depth
+ *       given the kept previous frontier.
+ *   force_margin [P]: for kept nodes, ell(parent,tok) - ell_(K)(parent).
+ *   row_lse [D*W], row_tok/row_logp [D*W*K], row_kgap [D*W]: per head row.
+ *   w_cut [2*D]: own W-th and (W+1)-th candidate score (-inf if none).
+ *   calls: number of batched head calls made (== D).
+ */
+int orc_build(int V, int H, int D, int W, int K, int bf16,
+              const float *z, const float *state0,
+              const void *A, const void *E, const void *Wout,
+              const int32_t *force_slot, const int32_t *force_tok,
+              int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
+              float *pool_score,
+              int32_t *own_slot, int32_t *own_tok, float *own_score,
+              float *force_margin,
+              double *row_lse, int32_t *row_tok, float *row_logp,
+              float *row_kgap, float *w_cut, int64_t *calls) {
+    if (V < 1 || H < 1 || D < 1 || W < 1 || K < 1 || K > V) return ORC_ERR_ARG;
+    int rc = ORC_OK;
+    float *st = malloc(sizeof(float) * (size_t)W * H);      /* row states */
+    float *st_next = malloc(sizeof(float) * (size_t)W * H);
+    float *ell = malloc(sizeof(float) * (size_t)W * V);      /* full rows */
+    float *score = malloc(sizeof(float) * (size_t)W);        /* row scores */
+    int32_t *sel_slot = malloc(sizeof(int32_t) * (size_t)W);
+    int32_t *sel_tok = malloc(sizeof(int32_t) * (size_t)W);
+    float *sel_score = malloc(sizeof(float) * (size_t)W);
+    cand_t *cand = malloc(sizeof(cand_t) * (size_t)W * K);
+    float *kth = malloc(sizeof(float) * (size_t)W);          /* K-th logit */
+    int32_t *tk = malloc(sizeof(int32_t) * (size_t)K);
+    float *tv = malloc(sizeof(float) * (size_t)K);
+    if (!st || !st_next || !ell || !score || !sel_slot || !sel_tok ||
+        !sel_score || !cand || !kth || !tk || !tv) {
+        rc = ORC_ERR_MEM;
+        goto done;
+    }
+
+    *calls = 0;
+    int fp = 1, off_prev = 0, off = 0;
+    for (int h = 0; h < H; ++h) st[h] = qstate(bf16, state0[h]);  /* root */
+    score[0] = 0.0f;
+
+    for (int d = 1; d <= D; ++d) {
+        const float *zd = z + (size_t)(d - 1) * V;
+        int fd = (K * fp < W) ? K * fp : W;
+        /* one batched head call over every frontier row */
+        *calls += 1;
+        for (int i = 0; i < fp; ++i) {
+            double lse;
+            float kgap;
+            orc_logits_row(V, H, bf16, zd, Wout, st + (size_t)i * H,
+                           ell + (size_t)i * V, &lse);
+            orc_topk_row(V, ell + (size_t)i * V, K, tk, tv, &kgap);
+            size_t r = (size_t)(d - 1) * W + i;
+            row_lse[r] = lse;
+            row_kgap[r] = kgap;
+            kth[i] = tv[K - 1];
+            for (int j = 0; j < K; ++j) {
+                float logp = (float)((double)tv[j] - lse);
+                row_tok[r * K + j] = tk[j];
+                row_logp[r * K + j] = logp;
+                cand[i * K + j].c = score[i] + logp;       /* one fp32 add */
+                cand[i * K + j].idx = i * K + j;
+            }
+        }
+        /* own global top-W over the fp*K candidates */
+        qsort(cand, (size_t)fp * K, sizeof(cand_t), cand_cmp);
+        for (int q = 0; q < fd; ++q) {
+            own_slot[off + q] = cand[q].idx / K;
+            int j = cand[q].idx % K;
+            size_t r = (size_t)(d - 1) * W + own_slot[off + q];
+            own_tok[off + q] = row_tok[r * K + j];
+            own_score[off + q] = cand[q].c;
+        }
+        w_cut[2 * (d - 1)] = cand[fd - 1].c;
+        w_cut[2 * (d - 1) + 1] = (fp * K > fd) ? cand[fd].c : -INFINITY;
+
+        /* the frontier that is kept: forced or own */
+        for (int q = 0; q < fd; ++q) {
+            int32_t slot, tok;
+            if (force_slot) {
+                slot = force_slot[off + q];
+                tok = force_tok[off + q];
+                if (slot < 0 || slot >= fp || tok < 0 || tok >= V) {
+                    rc = ORC_ERR_ARG;
+                    goto done;
+                }
+                size_t r = (size_t)(d - 1) * W + slot;
+                float e = ell[(size_t)slot * V + tok];
+                float logp = (float)((double)e - row_lse[r]);
+                sel_score[q] = score[slot] + logp;
+                force_margin[off + q] = e - kth[slot];
+            } else {
+                slot = own_slot[off + q];
+                tok = own_tok[off + q];
+                sel_score[q] = own_score[off + q];
+                force_margin[off + q] = 0.0f;
+            }
+            sel_slot[q] = slot;
+            sel_tok[q] = tok;
+            pool_parent[off + q] = (d == 1) ? -1 : off_prev + slot;
+            pool_token[off + q] = tok;
+            pool_depth[off + q] = d;
+            pool_score[off + q] = sel_score[q];
+        }
+        /* carry the correction states forward to the kept nodes */
+        if (d < D) {
+            for (int q = 0; q < fd; ++q)
+                orc_state_step(H, bf16, A, E, st + (size_t)sel_slot[q] * H,
+                               sel_tok[q], st_next + (size_t)q * H);
+            float *t = st; st = st_next; st_next = t;
+        }
+        for (int q = 0; q < fd; ++q) score[q] = sel_score[q];
+        off_prev = off;
+        off += fd;
+        fp = fd;
+    }
+
+done:
+    free(st); free(st_next); free(ell); free(score); free(sel_slot);
+    free(sel_tok); free(sel_score); free(cand); free(kth); free(tk); free(tv);
+    return rc;
+}
+
+/* ------------------------------------------------------ deferred pruning */
+
+typedef struct { float key; int32_t idx; } key_t_;
+
+static int key_cmp(const void *a, const void *b) {
+    const key_t_ *x = (const key_t_ *)a, *y = (const key_t_ *)b;
+    if (better(x->key, x->idx, y->key, y->idx)) return -1;
+    if (better(y->key, y->idx, x->key, x->idx)) return 1;
+    return 0;
+}
+
+/* key = score + beta * depth, two fp32 operations in that order. */
+static float prune_key(float score, int32_t depth, float beta) {
+    float bd = beta * (float)depth;
+    return score + bd;
+}
+
+/*
+ * Deferred global Top-B, compaction and the tree-attention mask.
+ * [P2] Methodologie 2: one global Top-B over every materialised prefix of
+ * the supertree, with a non-positive depth bonus; [P1] Core Mechanism: the
+ * selected nodes form the verification tree plus the sparse attention mask
+ * that lets the target check every branch in one forward; [P3] Summary.
+ *
+ * Canonical output order = the selection order (key desc, pool index asc).
+ * out_parent = rank of the parent in that order (-1 at depth 1).
+ * out_mask: B rows of ceil(B/32) words; bit j%32 of word j/32 of row i is
+ * set iff node j is node i or one of its ancestors.  Rows at or beyond
+ * n_out are parent/token -1, depth 0, score 0, mask 0.
+ * order[r] = pool index of rank r.  Returns ORC_ERR_CLOSURE when a selected
+ * node's parent is not selected, ORC_ERR_ORDER when a parent ranks after its
+ * child (neither can happen for beta <= 0; see Lemma 1).
+ */
+int orc_topb(int P, const int32_t *pool_parent, const int32_t *pool_token,
+             const int32_t *pool_depth, const float *pool_score, int B,
+             float beta, int32_t *out_parent, int32_t *out_token,
+             int32_t *out_depth, float *out_score, uint32_t *out_mask,
+             int32_t *n_out, int32_t *order) {
+    if (P < 0 || B < 1) return ORC_ERR_ARG;
+    int rc = ORC_OK;
+    int words = (B + 31) / 32;
+    key_t_ *k = malloc(sizeof(key_t_) * (size_t)(P > 0 ? P : 1));
+    int32_t *map = malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+    if (!k || !map) { rc = ORC_ERR_MEM; goto done; }
+    for (int n = 0; n < P; ++n) {
+        k[n].key = prune_key(pool_score[n], pool_depth[n], beta);
+        k[n].idx = n;
+        map[n] = -1;
+    }
+    qsort(k, (size_t)P, sizeof(key_t_), key_cmp);
+    int n_sel = P < B ? P : B;
+    *n_out = n_sel;
+    for (int r = 0; r < n_sel; ++r) {
+        order[r] = k[r].idx;
+        map[k[r].idx] = r;
+    }
+    memset(out_mask, 0, sizeof(uint32_t) * (size_t)B * words);
+    for (int r = 0; r < B; ++r) {
+        if (r >= n_sel) {
+            out_parent[r] = -1; out_token[r] = -1; out_depth[r] = 0;
+            out_score[r] = 0.0f;
+            continue;
+        }
+        int n = order[r];
+        int32_t pp = pool_parent[n];
+        int32_t par = (pp < 0) ? -1 : map[pp];
+        if (pp >= 0 && par < 0) { rc = ORC_ERR_CLOSURE; par = -1; }
+        if (par >= r) { rc = ORC_ERR_ORDER; par = -1; }
+        out_parent[r] = par;
+        out_token[r] = pool_token[n];
+        out_depth[r] = pool_depth[n];
+        out_score[r] = pool_score[n];
+        uint32_t *row = out_mask + (size_t)r * words;
+        if (par >= 0) memcpy(row, out_mask + (size_t)par * words,
+                             sizeof(uint32_t) * (size_t)words);
+        row[r / 32] |= 1u << (r % 32);
+    }
+done:
+    free(k); free(map);
+    return rc;
+}
+
+/*
+ * Sequential best-first pruning over the cached scores with a max-heap:
+ * seed with the depth-1 nodes, then B times pop the best node and push its
+ * children from the pool.  [P1] Core Mechanism ("Best-first pruning runs
+ * over the cached scores ... The heap operations are still sequential, but
+ * they touch no neural network"); Expert Assessment (EAGLE-2's heap moved
+ * after the forwards).  Used to check Lemma 1 against orc_topb.
+ * pop_order[r] = pool index popped at step r; returns the number of pops.
+ */
+int orc_heap_prune(int P, const int32_t *pool_parent, const int32_t *pool_depth,
+                   const float *pool_score, int B, float beta,
+                   int32_t *pop_order) {
+    key_t_ *heap = malloc(sizeof(key_t_) * (size_t)(P > 0 ? P : 1));
+    if (!heap) return -ORC_ERR_MEM;
+    int hn = 0, pops = 0;
+    /* push = sift up; "max" under (key desc, idx asc) */
+#define ORC_PUSH(node)                                                        \
+    do {                                                                      \
+        key_t_ e_ = { prune_key(pool_score[node], pool_depth[node], beta),   \
+                      (int32_t)(node) };                                      \
+        int i_ = hn++;                                                        \
+        while (i_ > 0) {                                                      \
+            int p_ = (i_ - 1) / 2;                                            \
+            if (!better(e_.key, e_.idx, heap[p_].key, heap[p_].idx)) break;   \
+            heap[i_] = heap[p_];                                              \
+            i_ = p_;                                                          \
+        }                                                                     \
+        heap[i_] = e_;                                                        \
+    } while (0)
+    for (int n = 0; n < P; ++n)
+        if (pool_parent[n] < 0) ORC_PUSH(n);
+    while (pops < B && hn > 0) {
+        key_t_ top = heap[0];
+        key_t_ last = heap[--hn];
+        int i = 0;
+        for (;;) {                                    /* sift down */
+            int l = 2 * i + 1, r = l + 1, b = i;
+            key_t_ bv = last;
+            if (l < hn && better(heap[l].key, heap[l].idx, bv.key, bv.idx)) {
+                b = l; bv = heap[l];
+            }
+            if (r < hn && better(heap[r].key, heap[r].idx, bv.key, bv.idx)) {
+                b = r; bv = heap[r];
+            }
+            if (b == i) break;
+            heap[i] = heap[b];
+            i = b;
+        }
+        if (hn > 0) heap[i] = last;
+        pop_order[pops++] = top.idx;
+        for (int n = 0; n < P; ++n)
+            if (pool_parent[n] == top.idx) ORC_PUSH(n);
+    }
+#undef ORC_PUSH
+    free(heap);
+    return pops;
+}
