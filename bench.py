@@ -1,0 +1,378 @@
+#!/usr/bin/env python
+"""Benchmark of DARTree supertree builds on one GB300 (or N replicas).
+
+A step is one full build: D batched head calls (state step, fused corrected
+logits + log-softmax + top-K, row merge, top-W select) and the deferred
+Top-B + mask, over seeded synthetic inputs of the chosen workload.  Prints
+one JSON line (rank 0).
+
+  python bench.py [--config q8b] [--steps K] [--warmup W] [--gpus N]
+  python bench.py --impl reference ...    # the CPU oracle, timed as stated
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+from speculative_decoding_draft_06_gb300 import inputs as I  # noqa: E402
+
+DEFAULT_CONFIG = "q8b"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("speculative_decoding_draft_06_gb300/csrc/head_tc.cu",
+                  "speculative_decoding_draft_06_gb300/csrc/epilogue.cuh",
+                  "speculative_decoding_draft_06_gb300/csrc/ptx.cuh",
+                  "speculative_decoding_draft_06_gb300/csrc/common.cuh")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("dartree", "reference"), default="dartree")
+    ap.add_argument("--config", choices=sorted(I.CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------- bookkeeping
+
+def head_bytes_per_launch(w: I.Workload) -> float:
+    """Algorithmic bytes of one head call, averaged over the D calls:
+    the output projection once, the base logits of every request and the
+    head-row states (weights bf16/fp32, logits fp32)."""
+    wb = 2 if w.bf16 else 4
+    rows = w.head_rows()
+    per = [w.V * w.H * wb + w.R * w.V * 4 + m * w.H * wb for m in rows]
+    return sum(per) / len(per)
+
+
+def build_bytes(w: I.Workload) -> float:
+    """Algorithmic bytes of one build: D output projections, D-1 state
+    matrices, the gathered embedding rows and all base logits."""
+    wb = 2 if w.bf16 else 4
+    rows = w.head_rows()
+    return (w.D * w.V * w.H * wb + (w.D - 1) * w.H * w.H * wb + sum(rows[1:]) * w.H * wb
+            + w.R * w.D * w.V * 4)
+
+
+def kernels_per_build(w: I.Workload) -> int:
+    return 1 + w.D * 3 + (w.D - 1) + 1      # root, head+merge+select per depth, states, prune
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(_ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(config: str) -> float | None:
+    """DRAM bytes per head-call launch from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(_ROOT, "profiles", f"head_logits_{config}.md")
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def aggregate(ms_local: float, world: int) -> float:
+    """Max of the per-rank step time over all ranks (torch.distributed)."""
+    if world <= 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0"
+        self.idx = vis
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200",
+                                       "-i", self.idx],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                      text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict | None:
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0) -> dict:
+    """Time the CPU oracle on the first depths of one request's build, as
+    many as fit in about budget_s, and scale to a full build by head rows
+    (the dominant cost is one V x H fp64 pass per head row)."""
+    import oracle
+    rows = [m // w.R for m in w.head_rows()]       # head rows per request per depth
+    t0 = time.perf_counter()
+    oracle.build_tree(inp, request, 1, w.W, w.K, w.bf16)
+    t1 = time.perf_counter() - t0                  # one depth, one row
+    d_s, acc = 1, rows[0]
+    while d_s < w.D and (acc + rows[d_s]) * t1 <= budget_s:
+        acc += rows[d_s]
+        d_s += 1
+    if d_s > 1:
+        t0 = time.perf_counter()
+        oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16)
+        t = time.perf_counter() - t0
+    else:
+        t = t1
+    total_rows = sum(rows)
+    per_build = t * total_rows / acc
+    return {"builds_per_s": 1.0 / per_build, "seconds": t, "depths": d_s, "rows": acc,
+            "total_rows": total_rows,
+            "sample": (f"oracle (fp64, 1 thread) on depths 1..{d_s} of request {request} "
+                       f"({acc} of {total_rows} head rows, {t:.1f} s), scaled by head rows")}
+
+
+# -------------------------------------------------------------- reference arm
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = I.CONFIGS[args.config]
+    inp = I.make_inputs(w)
+    budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, budget)
+    vals = [oracle_sample(w, inp, budget) for _ in range(args.steps)]
+    per_build = statistics.mean(1.0 / v["builds_per_s"] for v in vals)
+    value = 1.0 / per_build
+    line = {
+        "impl": "reference", "metric": "supertree builds/s", "value": value,
+        "unit": "builds/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_build * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "builds/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[-1]["sample"]},
+        "e2e": {"value": value, "unit": "builds/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: I.Workload) -> dict:
+    return {"workload": (f"{w.name}: V={w.V} H={w.H} D={w.D} W={w.W} K={w.K} B={w.B} "
+                         f"beta={w.beta} R={w.R} {'bf16' if w.bf16 else 'fp32'} weights"),
+            "R": w.R, "V": w.V, "H": w.H, "D": w.D, "W": w.W, "K": w.K, "B": w.B,
+            "beta": w.beta, "weights": "bf16" if w.bf16 else "fp32",
+            "l2": ("inputs larger than L2: the output projection is streamed from HBM once per "
+                   "head call" if w.V * w.H * (2 if w.bf16 else 4) > 129e6 else
+                   "L2-resident (weights fit in L2); no flush between steps")}
+
+
+# -------------------------------------------------------------- GPU arm
+
+def run_gpu(args) -> None:
+    import torch
+
+    from speculative_decoding_draft_06_gb300 import dartree as dtl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    w = I.CONFIGS[args.config]
+    if world > 1:   # replicas: every rank builds its own requests
+        w = w.replace(seed=w.seed + 7919 * rank)
+    inp = I.make_inputs(w)
+    dev = dtl.weights_to_device(inp, w.bf16)
+    ctx = dtl.DARTree(w.V, w.H, max_D=w.D, max_W=w.W, max_K=w.K, max_B=w.B,
+                      max_requests=w.R, bf16=w.bf16)
+    stream = torch.cuda.Stream()
+    out = ctx.alloc_tree(w.R, w.B)
+    kw = dict(D=w.D, W=w.W, K=w.K, B=w.B, beta=w.beta, out=out, stream=stream)
+    args_t = (dev["z"], dev["state0"], dev["A"], dev["E"], dev["Wout"])
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up, then the timed region (device events on the build stream)
+    for _ in range(max(3, args.warmup)):
+        ctx.build(*args_t, **kw)
+    ctx.sync(stream)
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ctx.build(*args_t, **kw)
+    e1.record(stream)
+    e1.synchronize()
+    clock_info = clocks.stop()
+    ctx.sync(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = aggregate(ms_local, world)
+    value = world * w.R * 1e3 / ms
+
+    # per-kernel durations (events around each launch, same stream)
+    ctx.set_timing(True)
+    ctx.reset_timing()
+    for _ in range(min(args.steps, 50)):
+        ctx.build(*args_t, **kw)
+        ctx.sync(stream)
+    kt = ctx.timing()
+    ctx.set_timing(False)
+    head_ms, head_n = kt["head"]
+    head_avg_ms = head_ms / max(1, head_n)
+    peak, peak_kind = measured_peaks()
+    bytes_launch = head_bytes_per_launch(w)
+    achieved = bytes_launch / (head_avg_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.config)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        zh = torch.from_numpy(inp["z"]).pin_memory()
+        sh = torch.from_numpy(inp["state0"]).pin_memory()
+        oh = ctx.alloc_tree(w.R, w.B, device="cpu", pin=True)
+        for _ in range(max(3, args.warmup)):
+            ctx.build_host(zh, sh, dev["A"], dev["E"], dev["Wout"], D=w.D, W=w.W, K=w.K, B=w.B,
+                           beta=w.beta, out_host=oh, stream=stream)
+        barrier()
+        n_e2e = max(5, min(args.steps, 100))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            ctx.build_host(zh, sh, dev["A"], dev["E"], dev["Wout"], D=w.D, W=w.W, K=w.K,
+                           B=w.B, beta=w.beta, out_host=oh, stream=stream)
+        t_e2e = (time.perf_counter() - t0) / n_e2e * 1e3
+        t_e2e = aggregate(t_e2e, world)
+        e2e = {"value": world * w.R * 1e3 / t_e2e, "unit": "builds/s",
+               "h2d_bytes_per_step": int(zh.numel() * 4 + sh.numel() * 4),
+               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in oh.values())),
+               "ms_per_step": t_e2e}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        s = oracle_sample(w, inp, args.cpu_budget)
+        cpu = {"value": s["builds_per_s"], "unit": "builds/s", "cores": 1, "kind": "oracle",
+               "sample": s["sample"]}
+
+    if rank == 0:
+        line = {
+            "metric": "supertree builds/s", "value": value, "unit": "builds/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.bf16 else "f32", "data": "synthetic",
+            "config": workload_config(w),
+            "nodes_scored_per_s": value / w.R * w.candidates_per_build(),
+            "path_GBps_per_gpu": build_bytes(w) * (value / world / w.R) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "k_head_tc (head call: Wout stream, fused "
+                         "log-softmax + top-K)" if w.bf16 else "k_head_simt",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic, "bytes_per_launch": bytes_launch,
+                         "launch_ms": head_avg_ms},
+            "kernel_ms_per_build": {k: v[0] / max(1, min(args.steps, 50)) for k, v in kt.items()},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": kernels_per_build(w) * args.steps,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * dartree.h -- C ABI of the GB300 (sm_103a) DARTree supertree builder.
+ *
+ * What it computes.  DARTree builds a speculative draft tree with a causal
+ * correction head: level by level, ONE batched head call scores every kept
+ * path, each path is expanded by its top-k children, candidates are scored by
+ * accumulated (corrected) path log-probability and the best W are kept; after
+ * D levels exactly D head calls have been made and a pool of scored nodes is
+ * cached.  Pruning is deferred: one global Top-B over the pool (with a depth
+ * bonus beta <= 0, which by Lemma 1 equals sequential best-first max-heap
+ * pruning) selects the verification tree, emitted with its tree-attention
+ * (ancestor) mask.
+ *   Sources: "DARTree: Teaching a Chain-Trained Corrector to Think in Trees"
+ *   -- Core Mechanism; "Technische Samenvatting: DARTree" -- Methodologie
+ *   1 (Depth-Wise Parallel AR Expansie) and 2 (Deferred Best-First Pruning,
+ *   Lemma 1); "Accelerating Language Models with Diffusion Draft Trees" --
+ *   Summary & Methodology Analysis.
+ *
+ * The pages do not give the correction head's architecture; this library
+ * uses a fixed stand-in:
+ *     state after committing token t :  s' = q(tanh(A s + E[t]))
+ *     corrected logits at depth d    :  l  = z_d + s Wout^T
+ * where z_d are the drafter's base logits for depth d and q() rounds to bf16
+ * (nearest-even) when the weights are bf16.  The root state is q(state0).
+ *
+ * Conventions used by every entry point:
+ *   - All array pointers are DEVICE pointers unless a function says "host".
+ *     Matrices are row-major and densely packed.
+ *   - Weights (A [H,H], E [V,H], Wout [V,H]) have the context's dtype: fp32
+ *     or bf16 (raw 16-bit patterns).  Base logits and scores are fp32.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *     Calls are asynchronous on that stream unless stated otherwise; device
+ *     checks are collected by dartree_sync_status().
+ *   - Selections are total orders: top-K by (logit desc, token asc), top-W
+ *     by (score desc, candidate index i*K+j asc), Top-B by (key desc, pool
+ *     index asc) with key = score + beta*depth (fp32 ops in that order).
+ *   - The caller owns every input and output buffer; the context owns its
+ *     workspace.  No call except dartree_create allocates device memory.
+ *   - Thread safety: a context is used by one host thread at a time.
+ */
+#ifndef DARTREE_H
+#define DARTREE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dartree_status {
+  DARTREE_OK = 0,
+  DARTREE_ERR_INVALID_ARG = 1,  /* bad argument; nothing was launched */
+  DARTREE_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits */
+  DARTREE_ERR_CUDA = 3,         /* a CUDA runtime call failed (see last_error) */
+  DARTREE_ERR_DEVICE_CHECK = 4, /* a kernel flagged bad data (non-finite logits,
+                                   empty row, broken ancestor closure) */
+  DARTREE_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up */
+  DARTREE_ERR_OOM = 6           /* workspace allocation failed */
+} dartree_status;
+
+typedef enum dartree_wdtype { DARTREE_W_F32 = 0, DARTREE_W_BF16 = 1 } dartree_wdtype;
+
+/* Build limits of this library. */
+#define DARTREE_MAX_K 32     /* children per node */
+#define DARTREE_MAX_ROWS 256 /* R * W: head rows per call */
+#define DARTREE_MAX_D 32     /* depth */
+#define DARTREE_MAX_B 1024   /* verification budget */
+
+/* Fixed shape and capacity of a context.
+ *   V, H          vocabulary size, head width.  bf16: H % 64 == 0; fp32: H % 8 == 0.
+ *   max_D/W/K/B   largest per-call D, W, K, B (K <= 32, D <= 32, B <= 1024).
+ *   max_requests  largest R; R * max_W must stay <= 256.
+ *   wdtype        dartree_wdtype of A, E and Wout. */
+typedef struct dartree_config {
+  int32_t V, H, max_D, max_W, max_K, max_B, max_requests, wdtype;
+} dartree_config;
+
+/* Head weights (device, context dtype): A [H,H] (row h = output unit),
+ * E [V,H] (token embeddings), Wout [V,H] (output projection). */
+typedef struct dartree_head {
+  const void *A, *E, *Wout;
+} dartree_head;
+
+/* Verification trees of R requests (device or, for dartree_build_host, host).
+ * Request r uses parent/token/depth/score[r*B .. r*B+B), mask words
+ * [r*B*ceil(B/32) ..), n_out[r].  Node i (canonical order, parents first):
+ * parent rank (-1 at depth 1), token, depth (1-based), cumulative score
+ * (fp32 log-prob without beta); mask row i has bit j%32 of word j/32 set iff
+ * node j is i or an ancestor of i.  Rows >= n_out[r] = min(B, pool size) are
+ * parent/token -1, depth 0, score 0, mask 0. */
+typedef struct dartree_tree {
+  int32_t *parent, *token, *depth;
+  float *score;
+  uint32_t *mask;
+  int32_t *n_out;
+} dartree_tree;
+
+typedef struct dartree_ctx dartree_ctx;
+
+/* Pool size of one request: sum_{d=1..D} |F_d|, |F_0| = 1,
+ * |F_d| = min(W, K |F_{d-1}|).  Returns -1 on bad arguments. */
+int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
+
+/* Creates a context on the current CUDA device and allocates all workspace
+ * (the only allocating call).  Fails with UNSUPPORTED on a device other than
+ * compute capability 10.3. */
+dartree_status dartree_create(const dartree_config *cfg, dartree_ctx **out);
+
+/* Releases the context and its workspace (synchronises the device). */
+void dartree_destroy(dartree_ctx *ctx);
+
+/* One supertree build for R independent requests sharing one head.
+ *   base_logits [R, D, V] fp32 : drafter logits z_d per request and depth.
+ *   state0      [R, H]    fp32 : head state at each request's prefix.
+ *   Requires 1 <= D, W, K, B, R within the context's limits, K <= V,
+ *   beta <= 0 (Lemma 1 needs a non-positive depth bonus).
+ * Runs D batched head calls (dartree_head_calls() reports them), then the
+ * deferred Top-B and the mask; writes `out`.  Asynchronous; never allocates. */
+dartree_status dartree_build(dartree_ctx *ctx, const float *base_logits, const float *state0,
+                             const dartree_head *head, int32_t R, int32_t D, int32_t W, int32_t K,
+                             int32_t B, float beta, const dartree_tree *out, void *stream);
+
+/* Same as dartree_build with HOST base_logits, state0 and outputs (weights
+ * stay on the device): copies the inputs into the context's staging buffers,
+ * builds, copies the tree back and synchronises the stream.  Returns the
+ * folded device status like dartree_sync_status. */
+dartree_status dartree_build_host(dartree_ctx *ctx, const float *base_logits_host,
+                                  const float *state0_host, const dartree_head *head, int32_t R,
+                                  int32_t D, int32_t W, int32_t K, int32_t B, float beta,
+                                  const dartree_tree *out_host, void *stream);
+
+/* Synchronises `stream`, reads and clears the device check word and returns
+ * OK, DEVICE_CHECK or TIMEOUT (or CUDA if the synchronisation failed). */
+dartree_status dartree_sync_status(dartree_ctx *ctx, void *stream);
+
+/* Number of batched head calls made by the last build (== its D). */
+int64_t dartree_head_calls(const dartree_ctx *ctx);
+
+/* Text of the last error recorded by this context ("" if none). */
+const char *dartree_last_error(const dartree_ctx *ctx);
+
+/* Per-kernel timing.  When enabled, every launch of a build is bracketed by
+ * CUDA events on the build's stream; dartree_sync_status() adds the elapsed
+ * times to per-kind totals.  Kinds: 0 head call (fused logits + log-softmax
+ * + top-K partials), 1 state step, 2 row merge, 3 top-W select, 4 Top-B +
+ * mask, 5 root rows.  Enabling creates the events (no device memory). */
+#define DARTREE_KERNEL_KINDS 6
+dartree_status dartree_set_timing(dartree_ctx *ctx, int32_t enable);
+/* Totals since the last reset: milliseconds and launch count per kind. */
+dartree_status dartree_get_timing(const dartree_ctx *ctx, int32_t kind, double *total_ms,
+                                  int64_t *launches);
+dartree_status dartree_reset_timing(dartree_ctx *ctx);
+
+/* Debug: copy the last build's pool ([R, P] each, pool index depth-major,
+ * rank order within a depth, parent = pool index or -1) into any memory
+ * (host or device).  Asynchronous on `stream`. */
+dartree_status dartree_get_pool(dartree_ctx *ctx, int32_t *parent, int32_t *token,
+                                int32_t *depth, float *score, void *stream);
+
+/* Debug: the last build's per-row head results at depth d (1-based) for its
+ * R*|F_{d-1}| head rows: lse [rows] fp64, top-K tokens [rows, K] and their
+ * log-probs [rows, K].  Any memory; asynchronous. */
+dartree_status dartree_get_rows(dartree_ctx *ctx, int32_t d, double *lse, int32_t *tok,
+                                float *logp, void *stream);
+
+/* One batched head call (corrected logits fused with log-softmax and top-K)
+ * for M head rows with states S [M, H] (context dtype: bf16 bits or fp32).
+ * Row m belongs to request m / rows_per_req and uses base logits
+ * z + (m / rows_per_req) * z_req_stride (fp32 [V]).  Outputs: lse [M] fp64,
+ * tok [M, K] int32, logp [M, K] fp32 (= logit - lse), sorted by (logit desc,
+ * token asc).  M <= 256, K <= max_K, K <= V.  Asynchronous. */
+dartree_status dartree_head_topk(dartree_ctx *ctx, const void *S, const float *z,
+                                 int64_t z_req_stride, int32_t rows_per_req, const void *Wout,
+                                 int32_t M, int32_t K, double *lse, int32_t *tok, float *logp,
+                                 void *stream);
+
+/* Head state step for M rows: S_out[m] = q(tanh(A S_par[m] + E[tok[m]])).
+ * S_par, S_out [M, H] in the context dtype; tok [M] int32 in [0, V).
+ * M <= 256.  Asynchronous. */
+dartree_status dartree_state_step(dartree_ctx *ctx, const void *S_par, const int32_t *tok,
+                                  const void *A, const void *E, int32_t M, void *S_out,
+                                  void *stream);
+
+/* Deferred Top-B + compaction + mask over given pools (pool arrays [R, P],
+ * layout as dartree_get_pool).  R <= max_requests, P <= R-independent pool
+ * capacity of the context, B <= max_B, beta <= 0.  Asynchronous. */
+dartree_status dartree_prune(dartree_ctx *ctx, const int32_t *pool_parent,
+                             const int32_t *pool_token, const int32_t *pool_depth,
+                             const float *pool_score, int32_t R, int32_t P, int32_t B, float beta,
+                             const dartree_tree *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DARTREE_H */

@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -20,7 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dartree_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "_build", "libdartree_oracle.so")
+_LIB_PATH = os.path.join(_HERE, "_build", platform.machine(), "libdartree_oracle.so")
 _lock = threading.Lock()
 _lib = None
 

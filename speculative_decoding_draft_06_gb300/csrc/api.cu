@@ -1,0 +1,749 @@
+// C ABI of the DARTree supertree builder: context, argument checks, tensor
+// maps, and the depth loop that chains the kernels on the caller's stream.
+//
+// Per build (R requests, depth D):
+//   root rows -> for d = 1..D { [d >= 2] state step (A) ; head call (Wout,
+//   fused log-softmax + top-K partials) ; merge rows ; top-W select + pool
+//   append + state gather } -> Top-B + compaction + mask.
+// That is exactly D head calls ("DARTree: Teaching a Chain-Trained Corrector
+// to Think in Trees", Core Mechanism and Framework Shift: head calls =
+// O(depth), not O(nodes)).  Frontier sizes are a closed form, so every launch
+// shape is known on the host and no data-dependent control flow is needed.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/dartree.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using dt::pad_rows;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kNumPads = 5;  // N = 16, 32, 64, 128, 256
+int pad_index(int n) { return n == 16 ? 0 : n == 32 ? 1 : n == 64 ? 2 : n == 128 ? 3 : 4; }
+
+int frontier_after(int F, int W, int K) {
+  const long long f = static_cast<long long>(K) * F;
+  return f < W ? static_cast<int>(f) : W;
+}
+
+}  // namespace
+
+struct dartree_ctx {
+  dartree_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  bool bf16 = false;
+  size_t elem = 4;
+  int pool_cap = 0;   // pool entries per request
+  int max_cta = 0;    // partial slots per row
+  EncodeTiledFn encode = nullptr;
+
+  // workspace (device)
+  void* S_cur = nullptr;    // [256][H] states of the current head rows
+  void* S_in = nullptr;     // [256][H] parents' states for the next state step
+  float* score[2] = {nullptr, nullptr};
+  int32_t* tok_next = nullptr;
+  float* pm = nullptr;
+  float* ps = nullptr;
+  uint64_t* ptop = nullptr;
+  double* rows_lse = nullptr;   // [max_D][256]
+  int32_t* rows_tok = nullptr;  // [max_D][256][max_K]
+  float* rows_logp = nullptr;
+  int32_t* pool_parent = nullptr;
+  int32_t* pool_token = nullptr;
+  int32_t* pool_depth = nullptr;
+  float* pool_score = nullptr;
+  int* d_err = nullptr;
+  // staging for dartree_build_host
+  float* z_stage = nullptr;
+  float* s0_stage = nullptr;
+  int32_t* o_parent = nullptr;
+  int32_t* o_token = nullptr;
+  int32_t* o_depth = nullptr;
+  float* o_score = nullptr;
+  uint32_t* o_mask = nullptr;
+  int32_t* o_nout = nullptr;
+
+  CUtensorMap tm_cur[kNumPads];
+  CUtensorMap tm_in[kNumPads];
+  CUtensorMap tm_A{}, tm_Wout{};
+  const void* tm_A_ptr = nullptr;
+  const void* tm_Wout_ptr = nullptr;
+
+  // per-kernel timing (events around launches; see dartree_set_timing)
+  bool timing = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<std::pair<int, size_t>> ev_marks;  // (kind, index of start event)
+  double t_ms[DARTREE_KERNEL_KINDS] = {0};
+  int64_t t_n[DARTREE_KERNEL_KINDS] = {0};
+
+  // last build
+  int last_R = 0, last_D = 0, last_W = 0, last_K = 0, last_P = 0;
+  int64_t head_calls = 0;
+  std::string last_error;
+
+  dartree_status fail(dartree_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    last_error = buf;
+    return s;
+  }
+  dartree_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(DARTREE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
+};
+
+namespace {
+
+dartree_status encode_2d(dartree_ctx* c, CUtensorMap* m, const void* ptr, uint64_t rows,
+                         uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(dt::kTileH), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = c->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return c->fail(DARTREE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return DARTREE_OK;
+}
+
+// Launch bracketing for dartree_set_timing: start()/stop() record a pair of
+// events around one kernel launch of the given kind.
+struct KernelTimer {
+  dartree_ctx* c;
+  cudaStream_t st;
+  int kind;
+  size_t idx = 0;
+  bool on = false;
+  KernelTimer(dartree_ctx* c_, cudaStream_t st_, int kind_) : c(c_), st(st_), kind(kind_) {
+    if (c->timing && c->ev_used + 2 <= c->ev_pool.size()) {
+      idx = c->ev_used;
+      c->ev_used += 2;
+      on = cudaEventRecord(c->ev_pool[idx], st) == cudaSuccess;
+    }
+  }
+  ~KernelTimer() {
+    if (on && cudaEventRecord(c->ev_pool[idx + 1], st) == cudaSuccess)
+      c->ev_marks.emplace_back(kind, idx);
+  }
+};
+
+void flush_timing(dartree_ctx* c) {
+  for (auto& m : c->ev_marks) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, c->ev_pool[m.second], c->ev_pool[m.second + 1]) == cudaSuccess) {
+      c->t_ms[m.first] += ms;
+      c->t_n[m.first] += 1;
+    }
+  }
+  c->ev_marks.clear();
+  c->ev_used = 0;
+}
+
+template <typename T>
+cudaError_t alloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T) + 16);
+}
+
+// Head call for M rows whose states are in c->S_cur (rows >= M are zero or
+// finite): fused logits + partials, then the per-row merge into rows_*.
+dartree_status run_head(dartree_ctx* c, const float* z, long long z_req_stride, int rows_per_req,
+                        int M, int K, double* lse, int32_t* tok, float* logp, cudaStream_t st) {
+  const int V = c->cfg.V, H = c->cfg.H;
+  const int N = pad_rows(M);
+  dt::TcParams p{};
+  p.rows = V;
+  p.H = H;
+  p.M = M;
+  p.n_tiles = (V + dt::kTileV - 1) / dt::kTileV;
+  p.err = c->d_err;
+  p.z = z;
+  p.z_req_stride = z_req_stride;
+  p.rows_per_req = rows_per_req;
+  p.K = K;
+  p.pm = c->pm;
+  p.ps = c->ps;
+  p.ptop = c->ptop;
+  p.cta_stride = c->max_cta;
+  p.list_stride = c->max_cta * dt::kEpiWarps;
+  int grid;
+  cudaError_t e;
+  {
+    KernelTimer tk(c, st, 0);
+    if (c->bf16) {
+      grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
+      e = dt::launch_head_tc(N, true, c->tm_Wout, c->tm_cur[pad_index(N)], p, grid, st);
+    } else {
+      grid = p.n_tiles < c->max_cta ? p.n_tiles : c->max_cta;
+      p.W_f32 = static_cast<const float*>(c->tm_Wout_ptr);
+      p.S_f32 = static_cast<const float*>(c->S_cur);
+      e = dt::launch_head_simt(N, true, p, grid, st);
+    }
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "head logits launch");
+  dt::MergeParams mp{};
+  mp.pm = c->pm;
+  mp.ps = c->ps;
+  mp.ptop = c->ptop;
+  mp.n_cta = grid;
+  mp.cta_stride = c->max_cta;
+  mp.list_stride = c->max_cta * dt::kEpiWarps;
+  mp.K = K;
+  mp.M = M;
+  mp.row_lse = lse;
+  mp.row_tok = tok;
+  mp.row_logp = logp;
+  mp.err = c->d_err;
+  {
+    KernelTimer tk(c, st, 2);
+    e = dt::launch_merge_rows(mp, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "merge launch");
+  return DARTREE_OK;
+}
+
+// State step for M rows: c->S_cur = q(tanh(A c->S_in + E[tok])).
+dartree_status run_state(dartree_ctx* c, const void* A, const void* E, const int32_t* tok, int M,
+                         cudaStream_t st) {
+  const int H = c->cfg.H;
+  const int N = pad_rows(M);
+  dt::TcParams p{};
+  p.rows = H;
+  p.H = H;
+  p.M = M;
+  p.n_tiles = (H + dt::kTileV - 1) / dt::kTileV;
+  p.err = c->d_err;
+  p.tok = tok;
+  cudaError_t e;
+  KernelTimer tk(c, st, 1);
+  if (c->bf16) {
+    p.E_bf16 = static_cast<const uint16_t*>(E);
+    p.S_out_bf16 = static_cast<uint16_t*>(c->S_cur);
+    e = dt::launch_head_tc(N, false, c->tm_A, c->tm_in[pad_index(N)], p, p.n_tiles, st);
+  } else {
+    p.E_f32 = static_cast<const float*>(E);
+    p.S_out_f32 = static_cast<float*>(c->S_cur);
+    p.W_f32 = static_cast<const float*>(A);
+    p.S_f32 = static_cast<const float*>(c->S_in);
+    e = dt::launch_head_simt(N, false, p, p.n_tiles, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "state step launch");
+  return DARTREE_OK;
+}
+
+dartree_status bind_weights(dartree_ctx* c, const void* A, const void* Wout) {
+  if (!c->bf16) {
+    c->tm_A_ptr = A;
+    c->tm_Wout_ptr = Wout;
+    return DARTREE_OK;
+  }
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Wout)) & 15)
+    return c->fail(DARTREE_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
+  dartree_status s;
+  if (A != nullptr && A != c->tm_A_ptr) {
+    if ((s = encode_2d(c, &c->tm_A, A, c->cfg.H, c->cfg.H, dt::kTileV)) != DARTREE_OK) return s;
+    c->tm_A_ptr = A;
+  }
+  if (Wout != nullptr && Wout != c->tm_Wout_ptr) {
+    if ((s = encode_2d(c, &c->tm_Wout, Wout, c->cfg.V, c->cfg.H, dt::kTileV)) != DARTREE_OK)
+      return s;
+    c->tm_Wout_ptr = Wout;
+  }
+  return DARTREE_OK;
+}
+
+dartree_status check_build_args(dartree_ctx* c, const void* z, const void* s0,
+                                const dartree_head* head, int R, int D, int W, int K, int B,
+                                float beta, const dartree_tree* out) {
+  if (!z || !s0 || !head || !head->A || !head->E || !head->Wout || !out || !out->parent ||
+      !out->token || !out->depth || !out->score || !out->mask || !out->n_out)
+    return c->fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
+  const dartree_config& g = c->cfg;
+  if (R < 1 || R > g.max_requests) return c->fail(DARTREE_ERR_INVALID_ARG, "R=%d out of [1,%d]", R, g.max_requests);
+  if (D < 1 || D > g.max_D) return c->fail(DARTREE_ERR_INVALID_ARG, "D=%d out of [1,%d]", D, g.max_D);
+  if (W < 1 || W > g.max_W) return c->fail(DARTREE_ERR_INVALID_ARG, "W=%d out of [1,%d]", W, g.max_W);
+  if (K < 1 || K > g.max_K) return c->fail(DARTREE_ERR_INVALID_ARG, "K=%d out of [1,%d]", K, g.max_K);
+  if (K > g.V) return c->fail(DARTREE_ERR_INVALID_ARG, "K=%d exceeds V=%d", K, g.V);
+  if (B < 1 || B > g.max_B) return c->fail(DARTREE_ERR_INVALID_ARG, "B=%d out of [1,%d]", B, g.max_B);
+  if (!(beta <= 0.0f)) return c->fail(DARTREE_ERR_INVALID_ARG, "beta must be <= 0 (Lemma 1)");
+  if (R * W > dt::kMaxRows) return c->fail(DARTREE_ERR_UNSUPPORTED, "R*W=%d > 256", R * W);
+  if (c->bf16 && pad_rows(R * W) * K > 2048)
+    return c->fail(DARTREE_ERR_UNSUPPORTED, "padded rows x K = %d > 2048", pad_rows(R * W) * K);
+  return DARTREE_OK;
+}
+
+dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const dartree_head* head,
+                         int R, int D, int W, int K, int B, float beta, const dartree_tree* out,
+                         cudaStream_t st) {
+  dartree_status s = bind_weights(c, head->A, head->Wout);
+  if (s != DARTREE_OK) return s;
+  const int V = c->cfg.V, H = c->cfg.H;
+  const int P = dartree_pool_size(D, W, K);
+  dt::RootParams rp{};
+  rp.R = R;
+  rp.n_pad = pad_rows(R);
+  rp.H = H;
+  rp.bf16 = c->bf16;
+  rp.state0 = s0;
+  rp.S = c->S_cur;
+  rp.score = c->score[0];
+  cudaError_t e;
+  {
+    KernelTimer tk(c, st, 5);
+    e = dt::launch_root(rp, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "root launch");
+  int F = 1, off_prev = 0, off = 0, cur = 0;
+  int64_t calls = 0;
+  for (int d = 1; d <= D; ++d) {
+    const int M = R * F;
+    if (d >= 2) {
+      if ((s = run_state(c, head->A, head->E, c->tok_next, M, st)) != DARTREE_OK) return s;
+    }
+    const size_t ro = static_cast<size_t>(d - 1) * dt::kMaxRows;
+    s = run_head(c, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V, F, M, K,
+                 c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, st);
+    if (s != DARTREE_OK) return s;
+    ++calls;
+    const int Fd = frontier_after(F, W, K);
+    dt::SelectParams sp{};
+    sp.R = R;
+    sp.F = F;
+    sp.Fd = Fd;
+    sp.K = K;
+    sp.depth = d;
+    sp.off_prev = off_prev;
+    sp.off = off;
+    sp.pool_stride = P;
+    sp.row_tok = c->rows_tok + ro * K;
+    sp.row_logp = c->rows_logp + ro * K;
+    sp.score_in = c->score[cur];
+    sp.score_out = c->score[cur ^ 1];
+    sp.tok_next = c->tok_next;
+    sp.pool_parent = c->pool_parent;
+    sp.pool_token = c->pool_token;
+    sp.pool_depth = c->pool_depth;
+    sp.pool_score = c->pool_score;
+    sp.S_cur = c->S_cur;
+    sp.S_next_in = d < D ? c->S_in : nullptr;
+    sp.H = H;
+    sp.elem_bytes = static_cast<int>(c->elem);
+    {
+      KernelTimer tk(c, st, 3);
+      e = dt::launch_select(sp, st);
+    }
+    if (e != cudaSuccess) return c->cuda_fail(e, "select launch");
+    cur ^= 1;
+    off_prev = off;
+    off += Fd;
+    F = Fd;
+  }
+  dt::PruneParams pp{};
+  pp.R = R;
+  pp.P = P;
+  pp.pool_stride = P;
+  pp.B = B;
+  pp.words = (B + 31) / 32;
+  pp.beta = beta;
+  pp.pool_parent = c->pool_parent;
+  pp.pool_token = c->pool_token;
+  pp.pool_depth = c->pool_depth;
+  pp.pool_score = c->pool_score;
+  pp.parent = out->parent;
+  pp.token = out->token;
+  pp.depth = out->depth;
+  pp.score = out->score;
+  pp.mask = out->mask;
+  pp.n_out = out->n_out;
+  pp.err = c->d_err;
+  {
+    KernelTimer tk(c, st, 4);
+    e = dt::launch_prune(pp, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "prune launch");
+  c->last_R = R;
+  c->last_D = D;
+  c->last_W = W;
+  c->last_K = K;
+  c->last_P = P;
+  c->head_calls = calls;
+  return DARTREE_OK;
+}
+
+void free_events(dartree_ctx* c) {
+  for (cudaEvent_t ev : c->ev_pool) cudaEventDestroy(ev);
+  c->ev_pool.clear();
+  c->ev_marks.clear();
+  c->ev_used = 0;
+}
+
+void free_all(dartree_ctx* c) {
+  free_events(c);
+  void* ptrs[] = {c->S_cur,     c->S_in,       c->score[0],    c->score[1],   c->tok_next,
+                  c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
+                  c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
+                  c->d_err,     c->z_stage,    c->s0_stage,    c->o_parent,   c->o_token,
+                  c->o_depth,   c->o_score,    c->o_mask,      c->o_nout};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K) {
+  if (D < 1 || W < 1 || K < 1) return -1;
+  long long f = 1, p = 0;
+  for (int d = 0; d < D; ++d) {
+    f = f * K < W ? f * K : W;
+    p += f;
+  }
+  return p > 0x7FFFFFFF ? -1 : static_cast<int32_t>(p);
+}
+
+dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
+  if (!cfg || !out) return DARTREE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const dartree_config g = *cfg;
+  if (g.wdtype != DARTREE_W_F32 && g.wdtype != DARTREE_W_BF16) return DARTREE_ERR_INVALID_ARG;
+  if (g.V < 1 || g.H < 1 || g.max_D < 1 || g.max_W < 1 || g.max_K < 1 || g.max_B < 1 ||
+      g.max_requests < 1)
+    return DARTREE_ERR_INVALID_ARG;
+  if (g.max_K > DARTREE_MAX_K || g.max_D > DARTREE_MAX_D || g.max_B > DARTREE_MAX_B ||
+      g.max_W > DARTREE_MAX_ROWS || static_cast<long long>(g.max_requests) * g.max_W > DARTREE_MAX_ROWS)
+    return DARTREE_ERR_UNSUPPORTED;
+  if (g.wdtype == DARTREE_W_BF16 ? (g.H % 64 != 0) : (g.H % 8 != 0)) return DARTREE_ERR_UNSUPPORTED;
+
+  dartree_ctx* c = new (std::nothrow) dartree_ctx();
+  if (!c) return DARTREE_ERR_OOM;
+  c->cfg = g;
+  c->bf16 = g.wdtype == DARTREE_W_BF16;
+  c->elem = c->bf16 ? 2 : 4;
+  cudaError_t e = cudaGetDevice(&c->device);
+  cudaDeviceProp prop{};
+  if (e == cudaSuccess) e = cudaGetDeviceProperties(&prop, c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    return DARTREE_ERR_CUDA;
+  }
+  if (prop.major != 10 || prop.minor != 3) {
+    delete c;
+    return DARTREE_ERR_UNSUPPORTED;
+  }
+  c->num_sms = prop.multiProcessorCount;
+  c->max_cta = 2 * c->num_sms;
+  c->pool_cap = dartree_pool_size(g.max_D, g.max_W, g.max_K);
+
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    delete c;
+    return DARTREE_ERR_CUDA;
+  }
+  c->encode = reinterpret_cast<EncodeTiledFn>(fn);
+
+  const size_t rows = dt::kMaxRows;
+  const size_t Rc = static_cast<size_t>(g.max_requests);
+  const size_t B = static_cast<size_t>(g.max_B), words = (B + 31) / 32;
+  bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S_cur), rows * g.H * c->elem) == cudaSuccess &&
+            alloc(reinterpret_cast<uint8_t**>(&c->S_in), rows * g.H * c->elem) == cudaSuccess &&
+            alloc(&c->score[0], rows) == cudaSuccess && alloc(&c->score[1], rows) == cudaSuccess &&
+            alloc(&c->tok_next, rows) == cudaSuccess &&
+            alloc(&c->pm, rows * c->max_cta) == cudaSuccess &&
+            alloc(&c->ps, rows * c->max_cta) == cudaSuccess &&
+            alloc(&c->ptop, rows * c->max_cta * dt::kEpiWarps * g.max_K) == cudaSuccess &&
+            alloc(&c->rows_lse, static_cast<size_t>(g.max_D) * rows) == cudaSuccess &&
+            alloc(&c->rows_tok, static_cast<size_t>(g.max_D) * rows * g.max_K) == cudaSuccess &&
+            alloc(&c->rows_logp, static_cast<size_t>(g.max_D) * rows * g.max_K) == cudaSuccess &&
+            alloc(&c->pool_parent, Rc * c->pool_cap) == cudaSuccess &&
+            alloc(&c->pool_token, Rc * c->pool_cap) == cudaSuccess &&
+            alloc(&c->pool_depth, Rc * c->pool_cap) == cudaSuccess &&
+            alloc(&c->pool_score, Rc * c->pool_cap) == cudaSuccess &&
+            alloc(&c->d_err, 1) == cudaSuccess &&
+            alloc(&c->z_stage, Rc * g.max_D * static_cast<size_t>(g.V)) == cudaSuccess &&
+            alloc(&c->s0_stage, Rc * g.H) == cudaSuccess &&
+            alloc(&c->o_parent, Rc * B) == cudaSuccess && alloc(&c->o_token, Rc * B) == cudaSuccess &&
+            alloc(&c->o_depth, Rc * B) == cudaSuccess && alloc(&c->o_score, Rc * B) == cudaSuccess &&
+            alloc(&c->o_mask, Rc * B * words) == cudaSuccess &&
+            alloc(&c->o_nout, Rc) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return DARTREE_ERR_OOM;
+  }
+  e = cudaMemset(c->S_cur, 0, rows * g.H * c->elem);
+  if (e == cudaSuccess) e = cudaMemset(c->S_in, 0, rows * g.H * c->elem);
+  if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = dt::init_head_attrs();
+  if (e == cudaSuccess) e = dt::init_select_attrs();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(c);
+    delete c;
+    return DARTREE_ERR_CUDA;
+  }
+  if (c->bf16) {
+    for (int i = 0; i < kNumPads; ++i) {
+      const uint32_t n = 16u << i;
+      if (encode_2d(c, &c->tm_cur[i], c->S_cur, rows, g.H, n) != DARTREE_OK ||
+          encode_2d(c, &c->tm_in[i], c->S_in, rows, g.H, n) != DARTREE_OK) {
+        free_all(c);
+        delete c;
+        return DARTREE_ERR_CUDA;
+      }
+    }
+  }
+  *out = c;
+  return DARTREE_OK;
+}
+
+void dartree_destroy(dartree_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  free_all(ctx);
+  delete ctx;
+}
+
+dartree_status dartree_build(dartree_ctx* ctx, const float* base_logits, const float* state0,
+                             const dartree_head* head, int32_t R, int32_t D, int32_t W, int32_t K,
+                             int32_t B, float beta, const dartree_tree* out, void* stream) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  dartree_status s = check_build_args(ctx, base_logits, state0, head, R, D, W, K, B, beta, out);
+  if (s != DARTREE_OK) return s;
+  return run_build(ctx, base_logits, state0, head, R, D, W, K, B, beta, out,
+                   static_cast<cudaStream_t>(stream));
+}
+
+dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "stream synchronize");
+  flush_timing(ctx);
+  int h = 0;
+  e = cudaMemcpy(&h, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h != 0) e = cudaMemset(ctx->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "error word read");
+  if (h & dt::DT_ERR_TIMEOUT)
+    return ctx->fail(DARTREE_ERR_TIMEOUT, "device wait timed out (flags 0x%x)", h);
+  if (h != 0) return ctx->fail(DARTREE_ERR_DEVICE_CHECK, "device check failed (flags 0x%x)", h);
+  return DARTREE_OK;
+}
+
+dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float* s0h,
+                                  const dartree_head* head, int32_t R, int32_t D, int32_t W,
+                                  int32_t K, int32_t B, float beta, const dartree_tree* out_host,
+                                  void* stream) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  dartree_status s = check_build_args(ctx, zh, s0h, head, R, D, W, K, B, beta, out_host);
+  if (s != DARTREE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t zn = static_cast<size_t>(R) * D * ctx->cfg.V, sn = static_cast<size_t>(R) * ctx->cfg.H;
+  cudaError_t e = cudaMemcpyAsync(ctx->z_stage, zh, zn * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->s0_stage, s0h, sn * 4, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "input copy");
+  dartree_tree dev{ctx->o_parent, ctx->o_token, ctx->o_depth, ctx->o_score, ctx->o_mask, ctx->o_nout};
+  s = run_build(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta, &dev, st);
+  if (s != DARTREE_OK) return s;
+  const size_t nb = static_cast<size_t>(R) * B, nw = nb * ((B + 31) / 32);
+  struct {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } cp[] = {{out_host->parent, ctx->o_parent, nb * 4}, {out_host->token, ctx->o_token, nb * 4},
+            {out_host->depth, ctx->o_depth, nb * 4},   {out_host->score, ctx->o_score, nb * 4},
+            {out_host->mask, ctx->o_mask, nw * 4},     {out_host->n_out, ctx->o_nout, static_cast<size_t>(R) * 4}};
+  for (auto& x : cp) {
+    e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return ctx->cuda_fail(e, "output copy");
+  }
+  return dartree_sync_status(ctx, stream);
+}
+
+dartree_status dartree_set_timing(dartree_ctx* ctx, int32_t enable) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  if (!enable) {
+    cudaDeviceSynchronize();
+    free_events(ctx);
+    ctx->timing = false;
+    return DARTREE_OK;
+  }
+  if (ctx->ev_pool.empty()) {
+    const size_t n = 2 * (4 * static_cast<size_t>(ctx->cfg.max_D) + 8);
+    for (size_t i = 0; i < n; ++i) {
+      cudaEvent_t ev;
+      cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) {
+        free_events(ctx);
+        return ctx->cuda_fail(e, "event create");
+      }
+      ctx->ev_pool.push_back(ev);
+    }
+  }
+  ctx->timing = true;
+  return DARTREE_OK;
+}
+
+dartree_status dartree_get_timing(const dartree_ctx* ctx, int32_t kind, double* total_ms,
+                                  int64_t* launches) {
+  if (!ctx || !total_ms || !launches || kind < 0 || kind >= DARTREE_KERNEL_KINDS)
+    return DARTREE_ERR_INVALID_ARG;
+  *total_ms = ctx->t_ms[kind];
+  *launches = ctx->t_n[kind];
+  return DARTREE_OK;
+}
+
+dartree_status dartree_reset_timing(dartree_ctx* ctx) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  for (int k = 0; k < DARTREE_KERNEL_KINDS; ++k) {
+    ctx->t_ms[k] = 0.0;
+    ctx->t_n[k] = 0;
+  }
+  return DARTREE_OK;
+}
+
+int64_t dartree_head_calls(const dartree_ctx* ctx) { return ctx ? ctx->head_calls : -1; }
+
+const char* dartree_last_error(const dartree_ctx* ctx) {
+  return ctx ? ctx->last_error.c_str() : "null context";
+}
+
+dartree_status dartree_get_pool(dartree_ctx* ctx, int32_t* parent, int32_t* token, int32_t* depth,
+                                float* score, void* stream) {
+  if (!ctx || !parent || !token || !depth || !score) return DARTREE_ERR_INVALID_ARG;
+  if (ctx->last_P == 0) return ctx->fail(DARTREE_ERR_INVALID_ARG, "no build yet");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(ctx->last_R) * ctx->last_P * 4;
+  cudaError_t e = cudaMemcpyAsync(parent, ctx->pool_parent, n, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(token, ctx->pool_token, n, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(depth, ctx->pool_depth, n, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(score, ctx->pool_score, n, cudaMemcpyDefault, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "pool copy");
+  return DARTREE_OK;
+}
+
+dartree_status dartree_get_rows(dartree_ctx* ctx, int32_t d, double* lse, int32_t* tok, float* logp,
+                                void* stream) {
+  if (!ctx || !lse || !tok || !logp) return DARTREE_ERR_INVALID_ARG;
+  if (ctx->last_P == 0 || d < 1 || d > ctx->last_D)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "depth %d not in the last build", d);
+  int F = 1;
+  for (int i = 1; i < d; ++i) F = frontier_after(F, ctx->last_W, ctx->last_K);
+  const size_t rows = static_cast<size_t>(ctx->last_R) * F, K = ctx->last_K;
+  const size_t ro = static_cast<size_t>(d - 1) * dt::kMaxRows;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(lse, ctx->rows_lse + ro, rows * 8, cudaMemcpyDefault, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(tok, ctx->rows_tok + ro * K, rows * K * 4, cudaMemcpyDefault, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(logp, ctx->rows_logp + ro * K, rows * K * 4, cudaMemcpyDefault, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "rows copy");
+  return DARTREE_OK;
+}
+
+dartree_status dartree_head_topk(dartree_ctx* ctx, const void* S, const float* z,
+                                 int64_t z_req_stride, int32_t rows_per_req, const void* Wout,
+                                 int32_t M, int32_t K, double* lse, int32_t* tok, float* logp,
+                                 void* stream) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  if (!S || !z || !Wout || !lse || !tok || !logp)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
+  if (M < 1 || M > dt::kMaxRows || rows_per_req < 1 || K < 1 || K > ctx->cfg.max_K ||
+      K > ctx->cfg.V)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "bad M=%d, rows_per_req=%d or K=%d", M,
+                     rows_per_req, K);
+  if (ctx->bf16 && pad_rows(M) * K > 2048)
+    return ctx->fail(DARTREE_ERR_UNSUPPORTED, "padded rows x K > 2048");
+  dartree_status s = bind_weights(ctx, ctx->tm_A_ptr, Wout);
+  if (s != DARTREE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t rb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
+  cudaError_t e = cudaMemcpyAsync(ctx->S_cur, S, M * rb, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && pad_rows(M) > M)
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S_cur) + M * rb, 0, (pad_rows(M) - M) * rb, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy");
+  return run_head(ctx, z, z_req_stride, rows_per_req, M, K, lse, tok, logp, st);
+}
+
+dartree_status dartree_state_step(dartree_ctx* ctx, const void* S_par, const int32_t* tok,
+                                  const void* A, const void* E, int32_t M, void* S_out,
+                                  void* stream) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  if (!S_par || !tok || !A || !E || !S_out)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
+  if (M < 1 || M > dt::kMaxRows) return ctx->fail(DARTREE_ERR_INVALID_ARG, "bad M=%d", M);
+  dartree_status s = bind_weights(ctx, A, ctx->tm_Wout_ptr);
+  if (s != DARTREE_OK) return s;
+  if (!ctx->bf16) ctx->tm_A_ptr = A;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t rb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
+  cudaError_t e = cudaMemcpyAsync(ctx->S_in, S_par, M * rb, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && pad_rows(M) > M)
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S_in) + M * rb, 0, (pad_rows(M) - M) * rb, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy");
+  if ((s = run_state(ctx, A, E, tok, M, st)) != DARTREE_OK) return s;
+  e = cudaMemcpyAsync(S_out, ctx->S_cur, M * rb, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy back");
+  return DARTREE_OK;
+}
+
+dartree_status dartree_prune(dartree_ctx* ctx, const int32_t* pool_parent, const int32_t* pool_token,
+                             const int32_t* pool_depth, const float* pool_score, int32_t R,
+                             int32_t P, int32_t B, float beta, const dartree_tree* out,
+                             void* stream) {
+  if (!ctx) return DARTREE_ERR_INVALID_ARG;
+  if (!pool_parent || !pool_token || !pool_depth || !pool_score || !out || !out->parent ||
+      !out->token || !out->depth || !out->score || !out->mask || !out->n_out)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
+  if (R < 1 || R > ctx->cfg.max_requests || P < 1 || P > ctx->pool_cap || B < 1 ||
+      B > ctx->cfg.max_B || !(beta <= 0.0f))
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "bad R=%d, P=%d, B=%d or beta", R, P, B);
+  dt::PruneParams pp{};
+  pp.R = R;
+  pp.P = P;
+  pp.pool_stride = P;
+  pp.B = B;
+  pp.words = (B + 31) / 32;
+  pp.beta = beta;
+  pp.pool_parent = pool_parent;
+  pp.pool_token = pool_token;
+  pp.pool_depth = pool_depth;
+  pp.pool_score = pool_score;
+  pp.parent = out->parent;
+  pp.token = out->token;
+  pp.depth = out->depth;
+  pp.score = out->score;
+  pp.mask = out->mask;
+  pp.n_out = out->n_out;
+  pp.err = ctx->d_err;
+  cudaError_t e = dt::launch_prune(pp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "prune launch");
+  return DARTREE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+// Batched head contraction for fp32 weights on the CUDA cores.
+//
+// fp32 weights keep fp32 products: TF32 tensor cores round the operands to
+// 10 mantissa bits, which is far outside a 1e-5 score tolerance, so this
+// path uses FFMA.  Same two epilogues as the tensor-core kernel (fused
+// log-sum-exp + top-K of the corrected logits, or the tanh state step; see
+// "DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
+// Mechanism, and "Technische Samenvatting: DARTree", Methodologie 1).
+//
+// A CTA of 128 threads owns contiguous 128-row weight tiles; thread t owns
+// weight row tile*128 + t.  Weight and state slices of 32 columns are staged
+// through shared memory (coalesced loads, padded rows); each thread keeps 16
+// head-row accumulators in registers and runs over the columns in chunks.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace dt {
+
+constexpr int kSimtH = 32;  // contraction slice staged per step
+
+template <int N, bool kLogits>
+__global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  float* sW = reinterpret_cast<float*>(smem_raw);            // [128][33]
+  float* sS = sW + kTileV * (kSimtH + 1);                    // [16][32]
+  uint64_t* lists = reinterpret_cast<uint64_t*>(sS + 16 * kSimtH);
+  const int list_words = kLogits ? kEpiWarps * N * p.K : 0;
+  float2* red = reinterpret_cast<float2*>(lists + list_words);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
+  const int t_end =
+      static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
+
+  LogitsEpilogue<N> epi;
+  if (kLogits) epi.init(lists + warp * N * p.K, red + warp * N, p.K, p.M);
+  const int mcols = p.M < N ? p.M : N;  // columns that carry data
+
+  for (int t = t_begin; t < t_end; ++t) {
+    const int row = t * kTileV + tid;
+    const bool valid = row < p.rows;
+    // contraction of 16 head rows c0..c0+15 against this thread's weight row
+    auto dot16 = [&](float (&acc)[16], int c0) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+      for (int h0 = 0; h0 < p.H; h0 += kSimtH) {
+        __syncthreads();
+#pragma unroll 4
+        for (int i = 0; i < kSimtH; ++i) {
+          const int e = i * kTileV + tid;
+          const int r = e >> 5, c = e & 31;
+          const int gr = t * kTileV + r, gc = h0 + c;
+          sW[r * (kSimtH + 1) + c] =
+              (gr < p.rows && gc < p.H) ? __ldg(p.W_f32 + static_cast<size_t>(gr) * p.H + gc) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = i * kTileV + tid;
+          const int r = e >> 5, c = e & 31;
+          const int m = c0 + r, gc = h0 + c;
+          sS[r * kSimtH + c] =
+              (m < p.M && gc < p.H) ? __ldg(p.S_f32 + static_cast<size_t>(m) * p.H + gc) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int hh = 0; hh < kSimtH; ++hh) {
+          const float w = sW[tid * (kSimtH + 1) + hh];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf(w, sS[j * kSimtH + hh], acc[j]);
+        }
+      }
+    };
+    auto add_z = [&](float (&acc)[16], int c0) {
+      int req_prev = -1;
+      float zv = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j;
+        const int req = c / p.rows_per_req;
+        if (req != req_prev) {
+          req_prev = req;
+          zv = (valid && c < p.M) ? __ldg(p.z + static_cast<size_t>(req) * p.z_req_stride + row)
+                                  : 0.f;
+        }
+        acc[j] += zv;
+      }
+    };
+    if constexpr (kLogits) {
+      if constexpr (N <= 32) {
+        static_for<0, N / 16>([&](auto i) {
+          constexpr int C0 = decltype(i)::value * 16;
+          if (C0 < mcols) {
+            float acc[16];
+            dot16(acc, C0);
+            add_z(acc, C0);
+            epi.template consume_static<C0>(acc, valid, static_cast<uint32_t>(row));
+          }
+        });
+      } else {
+        for (int c0 = 0; c0 < mcols; c0 += 16) {
+          float acc[16];
+          dot16(acc, c0);
+          add_z(acc, c0);
+          epi.consume_dyn(acc, c0, valid, static_cast<uint32_t>(row));
+        }
+      }
+    } else {
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float acc[16];
+        if (c0 < mcols) {
+          dot16(acc, c0);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        }
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = c0 + j;
+            float out = 0.f;
+            if (m < p.M) {
+              const int tok = __ldg(p.tok + m);
+              out = tanhf(acc[j] + __ldg(p.E_f32 + static_cast<size_t>(tok) * p.H + row));
+            }
+            p.S_out_f32[static_cast<size_t>(m) * p.H + row] = out;
+          }
+        }
+      }
+    }
+    if constexpr (kLogits) epi.tile_done();
+  }
+  if constexpr (kLogits) {
+    epi.finish(red, warp, blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
+  }
+}
+
+template <int N, bool kLogits>
+static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(kTileV) * (kSimtH + 1) * 4 + 16 * kSimtH * 4 +
+                      static_cast<size_t>(kLogits ? kEpiWarps * N * p.K : 0) * 8 +
+                      static_cast<size_t>(kEpiWarps) * N * sizeof(float2);
+  k_head_simt<N, kLogits><<<grid, 128, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+#ifndef DT_N
+#error "compile head_simt.cu with -DDT_N=<16|32|64|128|256>"
+#endif
+
+#define DT_CAT2(a, b) a##b
+#define DT_CAT(a, b) DT_CAT2(a, b)
+
+cudaError_t DT_CAT(init_head_simt_attrs_, DT_N)() {
+  const int smem = 227 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_head_simt<DT_N, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_head_simt<DT_N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem);
+}
+
+cudaError_t DT_CAT(launch_head_simt_, DT_N)(bool logits, const TcParams& p, int grid,
+                                             cudaStream_t st) {
+  return logits ? launch_simt_n<DT_N, true>(p, grid, st) : launch_simt_n<DT_N, false>(p, grid, st);
+}
+
+}  // namespace dt

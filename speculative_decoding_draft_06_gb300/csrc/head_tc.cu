@@ -1,0 +1,302 @@
+// Batched head contraction on the 5th-generation tensor cores (bf16 weights).
+//
+// One kernel shape serves both dense steps of a DARTree head call:
+//   * corrected logits  ell[m, v] = z_d[v] + sum_h S[m, h] Wout[v, h]
+//     ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
+//     Mechanism: ONE batched head call on all W paths gives W corrected
+//     conditional distributions), fused with the online log-sum-exp and the
+//     per-row top-K (LogitsEpilogue) -- the logits never reach HBM;
+//   * state step        S'[m, h] = bf16(tanh(sum_j A[h, j] S[m, j] + E[tok_m, h]))
+//     ("Technische Samenvatting: DARTree", Methodologie 1: the kept branches
+//     carry their correction states forward).
+//
+// Swap-AB: the weight matrix supplies the 128-row MMA "M" side (vocabulary or
+// hidden rows) and the head rows are the MMA N (16..256), so tiny head
+// batches still fill the tensor core's M dimension.  Both operands are
+// K-major bf16 tiles of 128 B rows loaded by TMA with the 128-byte swizzle;
+// the fp32 accumulator lives in TMEM (two buffers, so the epilogue of tile i
+// overlaps the MMAs of tile i+1).
+//
+// Warp roles (192 threads): warps 0-3 epilogue (TMEM lane quarter = warp),
+// warp 4 TMA producer, warp 5 TMEM allocator + single-thread MMA issuer.
+// Each CTA owns a contiguous range of 128-row weight tiles (persistent, one
+// CTA per SM).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dt {
+
+template <int N>
+struct TcLayout {
+  static constexpr int kABytes = kTileV * kTileH * 2;  // 16 KB
+  static constexpr int kBBytes = N * kTileH * 2;       // N rows of 128 B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+};
+
+template <int N, bool kLogits>
+__global__ void __launch_bounds__(192, 1)
+    k_head_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+              const TcParams p) {
+  using L = TcLayout<N>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  uint8_t* stage_base = smem;
+  uint8_t* after = smem + static_cast<size_t>(S) * L::kStageBytes;
+  uint64_t* lists = reinterpret_cast<uint64_t*>(after);
+  const int list_words = kLogits ? kEpiWarps * N * p.K : 0;
+  float2* red = reinterpret_cast<float2*>(lists + list_words);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + kEpiWarps * N);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // contiguous, balanced tile range of this CTA
+  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
+  const int t_end =
+      static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
+  const int nk = p.H / kTileH;
+
+  if (warp == 5) tmem_alloc<L::kTmemCols>(tmem_slot);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_s);
+  }
+  LogitsEpilogue<N> epi;
+  if (kLogits && warp < kEpiWarps) epi.init(lists + warp * N * p.K, red + warp * N, p.K, p.M);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_s = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* a_dst = stage_base + static_cast<size_t>(stage) * L::kStageBytes;
+          uint8_t* b_dst = a_dst + L::kABytes;
+          mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+          tma_load_2d(a_dst, &tmap_w, &full[stage], kb * kTileH, t * kTileV, pol_w);
+          tma_load_2d(b_dst, &tmap_s, &full[stage], kb * kTileH, 0, pol_s);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: every issued copy must have landed before the CTA may exit
+      const long long first = issued > S ? issued - S : 0;
+      for (long long n = first; n < issued; ++n) {
+        const int s = static_cast<int>(n % S);
+        const uint32_t par = static_cast<uint32_t>((n / S) & 1);
+        if (!mbar_wait(&full[s], par, p.err)) break;
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_m128<N>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
+        const int a = it & 1;
+        if (!mbar_wait(&tempty[a], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * N);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.err)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr =
+              smem_u32(stage_base + static_cast<size_t>(stage) * L::kStageBytes);
+          const uint32_t b_addr = a_addr + L::kABytes;
+#pragma unroll
+          for (int k = 0; k < kTileH / 16; ++k) {
+            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
+                        idesc, (kb | k) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[a]);
+      }
+      // all issued MMAs complete before TMEM is released
+      tc_commit(done);
+      mbar_wait(done, 0, p.err);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    int it = 0;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int t = t_begin; t < t_end; ++t, ++it) {
+      const int a = it & 1;
+      if (*abort_flag) break;
+      if (!mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = t * kTileV + warp * 32 + lane;  // vocabulary (or hidden) index
+      const bool valid = row < p.rows;
+      const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(a * N);
+      if constexpr (kLogits) {
+        int req_prev = -1;
+        float zv = 0.f;
+        auto add_z = [&](float (&x)[16], int c0) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j;
+            const int req = c / p.rows_per_req;
+            if (req != req_prev) {
+              req_prev = req;
+              zv = (valid && c < p.M) ? __ldg(p.z + static_cast<size_t>(req) * p.z_req_stride + row)
+                                      : 0.f;
+            }
+            x[j] += zv;
+          }
+        };
+        if constexpr (N <= 32) {
+          static_for<0, N / 16>([&](auto i) {
+            constexpr int C0 = decltype(i)::value * 16;
+            float x[16];
+            tmem_ld16(tbase + C0, x);
+            add_z(x, C0);
+            epi.template consume_static<C0>(x, valid, static_cast<uint32_t>(row));
+          });
+        } else {
+          const int c_end = (p.M + 15) & ~15;
+          for (int c0 = 0; c0 < c_end; c0 += 16) {
+            float x[16];
+            tmem_ld16(tbase + c0, x);
+            add_z(x, c0);
+            epi.consume_dyn(x, c0, valid, static_cast<uint32_t>(row));
+          }
+        }
+        epi.tile_done();
+      } else {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float x[16];
+          tmem_ld16(tbase + c0, x);
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int m = c0 + j;
+              float out = 0.f;
+              if (m < p.M) {
+                const int tok = __ldg(p.tok + m);
+                const float e = bf16_bits_to_float(
+                    __ldg(p.E_bf16 + static_cast<size_t>(tok) * p.H + row));
+                out = tanhf(x[j] + e);
+              }
+              p.S_out_bf16[static_cast<size_t>(m) * p.H + row] = float_to_bf16_bits(out);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+    }
+    if constexpr (kLogits) {
+      epi.finish(red, warp, blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc<L::kTmemCols>(tmem_base);
+  }
+}
+
+template <int N, bool kLogits>
+static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p,
+                               int grid, cudaStream_t st) {
+  using L = TcLayout<N>;
+  size_t fixed = 1024 + static_cast<size_t>(kLogits ? kEpiWarps * N * p.K : 0) * 8 +
+                 static_cast<size_t>(kEpiWarps) * N * sizeof(float2) + 64 * 8 + 64;
+  const size_t budget = 227 * 1024;
+  int stages = static_cast<int>((budget - fixed) / L::kStageBytes);
+  if (stages > 8) stages = 8;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  TcParams q = p;
+  q.stages = stages;
+  const size_t smem = fixed + static_cast<size_t>(stages) * L::kStageBytes;
+  k_head_tc<N, kLogits><<<grid, 192, smem, st>>>(tw, ts, q);
+  return cudaGetLastError();
+}
+
+#ifndef DT_N
+#error "compile head_tc.cu with -DDT_N=<16|32|64|128|256>"
+#endif
+
+#define DT_CAT2(a, b) a##b
+#define DT_CAT(a, b) DT_CAT2(a, b)
+
+cudaError_t DT_CAT(init_head_tc_attrs_, DT_N)() {
+  const int smem = 227 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_head_tc<DT_N, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_head_tc<DT_N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem);
+}
+
+cudaError_t DT_CAT(launch_head_tc_, DT_N)(bool logits, const CUtensorMap& tw, const CUtensorMap& ts,
+                                           const TcParams& p, int grid, cudaStream_t st) {
+  return logits ? launch_tc_n<DT_N, true>(tw, ts, p, grid, st)
+                : launch_tc_n<DT_N, false>(tw, ts, p, grid, st);
+}
+
+}  // namespace dt

@@ -1,0 +1,158 @@
+// Kernel parameter blocks and launchers (host <-> device, internal).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dt {
+
+// Batched head contraction (tensor-core bf16 path and SIMT fp32 path).
+struct TcParams {
+  int rows;            // rows of the weight matrix: V (logits) or H (state)
+  int H;               // contraction length
+  int M;               // valid head rows (GEMM columns)
+  int n_tiles;         // ceil(rows / 128)
+  int stages;          // pipeline depth (set by the launcher)
+  int* err;            // device error word
+  // logits epilogue
+  const float* z;      // base logits of this depth, request 0
+  long long z_req_stride;
+  int rows_per_req;    // head rows per request (|F_{d-1}|)
+  int K;
+  float* pm;           // [rows_max][cta_stride] running max per CTA
+  float* ps;           // [rows_max][cta_stride] sum exp(x - max) per CTA
+  uint64_t* ptop;      // [rows_max][list_stride][K] per-warp top-K keys
+  int cta_stride;
+  int list_stride;
+  // state epilogue
+  const int32_t* tok;        // [M] committed token of each head row
+  const uint16_t* E_bf16;    // [V][H]
+  uint16_t* S_out_bf16;      // [rows_max][H]
+  const float* E_f32;
+  float* S_out_f32;
+  // SIMT operands (fp32 path)
+  const float* W_f32;        // [rows][H]
+  const float* S_f32;        // [rows_max][H]
+};
+
+// One object file per MMA N (16, 32, 64, 128, 256) defines these.
+#define DT_DECLARE_N(NN)                                                                    \
+  cudaError_t init_head_tc_attrs_##NN();                                                    \
+  cudaError_t launch_head_tc_##NN(bool logits, const CUtensorMap& tw, const CUtensorMap& ts, \
+                                  const TcParams& p, int grid, cudaStream_t st);            \
+  cudaError_t init_head_simt_attrs_##NN();                                                  \
+  cudaError_t launch_head_simt_##NN(bool logits, const TcParams& p, int grid, cudaStream_t st);
+DT_DECLARE_N(16)
+DT_DECLARE_N(32)
+DT_DECLARE_N(64)
+DT_DECLARE_N(128)
+DT_DECLARE_N(256)
+#undef DT_DECLARE_N
+
+inline cudaError_t launch_head_tc(int n_pad, bool logits, const CUtensorMap& tw,
+                                  const CUtensorMap& ts, const TcParams& p, int grid,
+                                  cudaStream_t st) {
+  switch (n_pad) {
+    case 16: return launch_head_tc_16(logits, tw, ts, p, grid, st);
+    case 32: return launch_head_tc_32(logits, tw, ts, p, grid, st);
+    case 64: return launch_head_tc_64(logits, tw, ts, p, grid, st);
+    case 128: return launch_head_tc_128(logits, tw, ts, p, grid, st);
+    case 256: return launch_head_tc_256(logits, tw, ts, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, int grid,
+                                    cudaStream_t st) {
+  switch (n_pad) {
+    case 16: return launch_head_simt_16(logits, p, grid, st);
+    case 32: return launch_head_simt_32(logits, p, grid, st);
+    case 64: return launch_head_simt_64(logits, p, grid, st);
+    case 128: return launch_head_simt_128(logits, p, grid, st);
+    case 256: return launch_head_simt_256(logits, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Merge of per-CTA partials into per-row lse and top-K (log-probs).
+struct MergeParams {
+  const float* pm;
+  const float* ps;
+  const uint64_t* ptop;
+  int n_cta;
+  int cta_stride;
+  int list_stride;
+  int K;
+  int M;
+  double* row_lse;     // [M]
+  int32_t* row_tok;    // [M][K]
+  float* row_logp;     // [M][K]
+  int* err;
+};
+cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
+
+// Global top-W of the candidates of each request + pool append + state gather.
+struct SelectParams {
+  int R, F, Fd, K, depth;    // depth is 1-based
+  int off_prev, off;         // pool offsets of depth-1 and depth
+  int pool_stride;           // pool entries per request
+  const int32_t* row_tok;    // [R*F][K]
+  const float* row_logp;     // [R*F][K]
+  const float* score_in;     // [R*F]
+  float* score_out;          // [R*Fd]
+  int32_t* tok_next;         // [R*Fd]
+  int32_t* pool_parent;
+  int32_t* pool_token;
+  int32_t* pool_depth;
+  float* pool_score;
+  const void* S_cur;         // [R*F][H] states of this depth's head rows
+  void* S_next_in;           // [R*Fd][H] parent states gathered for the next state step
+  int H;
+  int elem_bytes;
+};
+cudaError_t launch_select(const SelectParams& p, cudaStream_t st);
+
+// Deferred Top-B, compaction and the ancestor mask.
+struct PruneParams {
+  int R, P, pool_stride, B, words;
+  float beta;
+  const int32_t* pool_parent;
+  const int32_t* pool_token;
+  const int32_t* pool_depth;
+  const float* pool_score;
+  int32_t* parent;
+  int32_t* token;
+  int32_t* depth;
+  float* score;
+  uint32_t* mask;
+  int32_t* n_out;
+  int* err;
+};
+cudaError_t launch_prune(const PruneParams& p, cudaStream_t st);
+
+// Root rows: S[r] = q(state0[r]), zero padding rows, scores 0.
+struct RootParams {
+  int R, n_pad, H, bf16;
+  const float* state0;
+  void* S;
+  float* score;
+};
+cudaError_t launch_root(const RootParams& p, cudaStream_t st);
+
+// One-time kernel attribute setup (dynamic shared memory opt-in).
+cudaError_t init_select_attrs();
+inline cudaError_t init_head_attrs() {
+  cudaError_t e;
+  if ((e = init_head_tc_attrs_16()) != cudaSuccess) return e;
+  if ((e = init_head_tc_attrs_32()) != cudaSuccess) return e;
+  if ((e = init_head_tc_attrs_64()) != cudaSuccess) return e;
+  if ((e = init_head_tc_attrs_128()) != cudaSuccess) return e;
+  if ((e = init_head_tc_attrs_256()) != cudaSuccess) return e;
+  if ((e = init_head_simt_attrs_16()) != cudaSuccess) return e;
+  if ((e = init_head_simt_attrs_32()) != cudaSuccess) return e;
+  if ((e = init_head_simt_attrs_64()) != cudaSuccess) return e;
+  if ((e = init_head_simt_attrs_128()) != cudaSuccess) return e;
+  return init_head_simt_attrs_256();
+}
+
+}  // namespace dt

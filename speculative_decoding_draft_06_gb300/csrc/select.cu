@@ -1,0 +1,329 @@
+// Selection kernels of a DARTree build: merge of the head-call partials into
+// per-row log-probabilities and top-K, the per-depth global top-W with pool
+// append and state carry, the deferred global Top-B with compaction and the
+// ancestor (tree-attention) mask, and the root rows.
+//
+// Every selection sorts 64-bit keys (value desc, index asc; see common.cuh)
+// with a block-wide bitonic sort in shared memory, so results are a
+// deterministic total order and independent of thread timing.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dt {
+
+// ------------------------------------------------------------ block helpers
+
+// Sort keys[0..n) descending; n is a power of two.
+__device__ void block_sort_desc(uint64_t* keys, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = keys[i], b = keys[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+template <typename T, typename Op>
+__device__ T block_reduce(T v, Op op, T* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  T r = scratch[0];
+  for (int w = 1; w < nw; ++w) r = op(r, scratch[w]);
+  __syncthreads();
+  return r;
+}
+
+// ---------------------------------------------------------- merge of rows
+
+constexpr int kMergeThreads = 256;
+constexpr int kMergeCap = 4096;  // keys sorted at once
+
+// One block per head row.  lse = max + log(sum_cta s_cta exp(m_cta - max)) in
+// fp64; top-K = best K of all per-warp lists, after discarding every list
+// entry below the largest K-th entry of any list (that bound is <= the
+// row's true K-th key, because that list alone holds K keys at or above it).
+__global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams p) {
+  __shared__ uint64_t buf[kMergeCap];
+  __shared__ double dscr[32];
+  __shared__ float fscr[32];
+  __shared__ unsigned long long uscr[32];
+  __shared__ int iscr[32];
+  __shared__ int n_buf;
+  const int row = blockIdx.x;
+  const int K = p.K;
+
+  // ---- log-sum-exp
+  float mloc = -INFINITY;
+  for (int i = threadIdx.x; i < p.n_cta; i += blockDim.x)
+    mloc = fmaxf(mloc, p.pm[static_cast<size_t>(row) * p.cta_stride + i]);
+  const float mx = block_reduce(mloc, [](float a, float b) { return fmaxf(a, b); }, fscr);
+  double sloc = 0.0;
+  if (mx != -INFINITY) {
+    for (int i = threadIdx.x; i < p.n_cta; i += blockDim.x) {
+      const float m = p.pm[static_cast<size_t>(row) * p.cta_stride + i];
+      const float s = p.ps[static_cast<size_t>(row) * p.cta_stride + i];
+      if (m != -INFINITY) sloc += static_cast<double>(s) * exp(static_cast<double>(m) - mx);
+    }
+  }
+  const double ssum = block_reduce(sloc, [](double a, double b) { return a + b; }, dscr);
+  const double lse = (mx == -INFINITY) ? -INFINITY : static_cast<double>(mx) + log(ssum);
+  if (threadIdx.x == 0 && mx == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
+
+  // ---- top-K
+  const int n_lists = p.n_cta * kEpiWarps;
+  const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;
+  unsigned long long th = 0;
+  for (int l = threadIdx.x; l < n_lists; l += blockDim.x) {
+    const unsigned long long k = base[static_cast<size_t>(l) * K + K - 1];
+    th = k > th ? k : th;
+  }
+  th = block_reduce(th,
+                    [](unsigned long long a, unsigned long long b) { return a > b ? a : b; },
+                    uscr);
+
+  // lists per chunk so that one chunk's survivors plus the best K fit
+  const int lists_per_chunk = (kMergeCap - kMaxK) / K;
+  for (int i = threadIdx.x; i < kMergeCap; i += blockDim.x) buf[i] = 0ull;
+  if (threadIdx.x == 0) n_buf = 0;
+  __syncthreads();
+  bool have_best = false;
+  for (int l0 = 0; l0 < n_lists; l0 += lists_per_chunk) {
+    const int l1 = min(n_lists, l0 + lists_per_chunk);
+    if (threadIdx.x == 0) n_buf = have_best ? K : 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < (l1 - l0) * K; e += blockDim.x) {
+      const uint64_t k = base[static_cast<size_t>(l0) * K + e];
+      if (k >= th && k != 0ull) {
+        const int pos = atomicAdd(&n_buf, 1);
+        buf[pos] = k;
+      }
+    }
+    __syncthreads();
+    const int n = n_buf;
+    const int np2 = pow2_at_least(n < K ? K : n);
+    for (int i = n + threadIdx.x; i < np2; i += blockDim.x) buf[i] = 0ull;
+    __syncthreads();
+    block_sort_desc(buf, np2);
+    for (int i = K + threadIdx.x; i < np2; i += blockDim.x) buf[i] = 0ull;
+    __syncthreads();
+    have_best = true;
+  }
+  if (threadIdx.x < K) {
+    const uint64_t k = buf[threadIdx.x];
+    const float val = key_value(k);
+    p.row_tok[static_cast<size_t>(row) * K + threadIdx.x] = static_cast<int32_t>(key_index(k));
+    p.row_logp[static_cast<size_t>(row) * K + threadIdx.x] =
+        static_cast<float>(static_cast<double>(val) - lse);
+  }
+  if (threadIdx.x == 0) p.row_lse[row] = lse;
+  (void)iscr;
+}
+
+cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st) {
+  k_merge_rows<<<p.M, kMergeThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------- top-W per request
+
+constexpr int kSelectThreads = 1024;
+
+// One block per request.  Candidate (i, j) = child j of frontier slot i,
+// score c = score_i + logp_ij (one fp32 add), index i*K + j.  The best
+// |F_d| by (c desc, index asc) become the new frontier in rank order
+// ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
+// Mechanism: score by accumulated path probability, keep the top W;
+// "Accelerating Language Models with Diffusion Draft Trees", Summary: global
+// top-W child prefixes, states carried forward).
+__global__ void __launch_bounds__(kSelectThreads) k_select(const SelectParams p) {
+  extern __shared__ uint64_t keys[];
+  const int r = blockIdx.x;
+  const int n = p.F * p.K;
+  const int np2 = pow2_at_least(n);
+  for (int e = threadIdx.x; e < np2; e += blockDim.x) {
+    uint64_t k = 0ull;
+    if (e < n) {
+      const int i = e / p.K;
+      const int row = r * p.F + i;
+      const float c = __fadd_rn(p.score_in[row], p.row_logp[static_cast<size_t>(row) * p.K + (e % p.K)]);
+      k = make_key(c, static_cast<uint32_t>(e));
+    }
+    keys[e] = k;
+  }
+  __syncthreads();
+  block_sort_desc(keys, np2);
+  int32_t* slot_of = reinterpret_cast<int32_t*>(keys + np2);  // [Fd] parent slot
+  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) {
+    const uint64_t k = keys[q];
+    const int idx = static_cast<int>(key_index(k));
+    const int i = idx / p.K, j = idx % p.K;
+    const int row = r * p.F + i;
+    const float c = key_value(k);
+    const int32_t tok = p.row_tok[static_cast<size_t>(row) * p.K + j];
+    const size_t pi = static_cast<size_t>(r) * p.pool_stride + p.off + q;
+    p.pool_parent[pi] = (p.depth == 1) ? -1 : p.off_prev + i;
+    p.pool_token[pi] = tok;
+    p.pool_depth[pi] = p.depth;
+    p.pool_score[pi] = c;
+    const int m = r * p.Fd + q;
+    p.score_out[m] = c;
+    p.tok_next[m] = tok;
+    slot_of[q] = row;
+  }
+  __syncthreads();
+  if (p.S_next_in != nullptr) {
+    // gather the parents' states for the next state step (16-byte words)
+    const int words = p.H * p.elem_bytes / 16;
+    const uint4* src = reinterpret_cast<const uint4*>(p.S_cur);
+    uint4* dst = reinterpret_cast<uint4*>(p.S_next_in);
+    for (int e = threadIdx.x; e < p.Fd * words; e += blockDim.x) {
+      const int q = e / words, w = e % words;
+      dst[static_cast<size_t>(r * p.Fd + q) * words + w] =
+          src[static_cast<size_t>(slot_of[q]) * words + w];
+    }
+  }
+}
+
+cudaError_t launch_select(const SelectParams& p, cudaStream_t st) {
+  int np2 = 1;
+  while (np2 < p.F * p.K) np2 <<= 1;
+  const size_t smem = static_cast<size_t>(np2) * 8 + static_cast<size_t>(p.Fd) * 4;
+  k_select<<<p.R, kSelectThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------- Top-B, compaction, mask
+
+constexpr int kPruneThreads = 1024;
+
+// One block per request.  key = score + beta * depth (two fp32 operations);
+// the first min(B, P) nodes by (key desc, pool index asc) are the verification
+// tree, in that (canonical) order ("Technische Samenvatting: DARTree",
+// Methodologie 2: one global Top-B over all materialised prefixes with a
+// non-positive depth bonus).  parent_out = rank of the pool parent; the mask
+// row of node i has bit j set iff j is i or an ancestor of i ("DARTree:
+// Teaching a Chain-Trained Corrector to Think in Trees", Core Mechanism: the
+// sparse attention mask lets the target check every branch in one forward).
+__global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
+  extern __shared__ uint64_t keys[];
+  const int r = blockIdx.x;
+  const int np2 = pow2_at_least(p.P);
+  int32_t* map = reinterpret_cast<int32_t*>(keys + np2);  // [P] pool -> rank
+  int32_t* par = map + p.P;                               // [B] parent rank
+  const size_t pb = static_cast<size_t>(r) * p.pool_stride;
+  for (int e = threadIdx.x; e < np2; e += blockDim.x) {
+    uint64_t k = 0ull;
+    if (e < p.P) {
+      const float key = __fadd_rn(p.pool_score[pb + e],
+                                  __fmul_rn(p.beta, static_cast<float>(p.pool_depth[pb + e])));
+      k = make_key(key, static_cast<uint32_t>(e));
+    }
+    keys[e] = k;
+  }
+  for (int e = threadIdx.x; e < p.P; e += blockDim.x) map[e] = -1;
+  __syncthreads();
+  block_sort_desc(keys, np2);
+  const int n_sel = p.P < p.B ? p.P : p.B;
+  for (int q = threadIdx.x; q < n_sel; q += blockDim.x) map[key_index(keys[q])] = q;
+  __syncthreads();
+  const size_t ob = static_cast<size_t>(r) * p.B;
+  bool broken = false;
+  for (int q = threadIdx.x; q < p.B; q += blockDim.x) {
+    if (q < n_sel) {
+      const int n = static_cast<int>(key_index(keys[q]));
+      const int pp = p.pool_parent[pb + n];
+      int pr = pp < 0 ? -1 : map[pp];
+      if ((pp >= 0 && pr < 0) || pr >= q) {
+        broken = true;
+        pr = -1;
+      }
+      par[q] = pr;
+      p.parent[ob + q] = pr;
+      p.token[ob + q] = p.pool_token[pb + n];
+      p.depth[ob + q] = p.pool_depth[pb + n];
+      p.score[ob + q] = p.pool_score[pb + n];
+    } else {
+      par[q] = -1;
+      p.parent[ob + q] = -1;
+      p.token[ob + q] = -1;
+      p.depth[ob + q] = 0;
+      p.score[ob + q] = 0.f;
+    }
+  }
+  if (broken) atomicOr(p.err, DT_ERR_CLOSURE);
+  __syncthreads();
+  const size_t mb = static_cast<size_t>(r) * p.B * p.words;
+  for (int e = threadIdx.x; e < p.B * p.words; e += blockDim.x) {
+    const int q = e / p.words, w = e % p.words;
+    uint32_t bits = 0;
+    if (q < n_sel) {
+      int a = q;
+      for (int steps = 0; a >= 0 && steps <= p.B; ++steps) {  // parents rank earlier
+        if ((a >> 5) == w) bits |= 1u << (a & 31);
+        a = par[a];
+      }
+    }
+    p.mask[mb + e] = bits;
+  }
+  if (threadIdx.x == 0) p.n_out[r] = n_sel;
+}
+
+cudaError_t launch_prune(const PruneParams& p, cudaStream_t st) {
+  int np2 = 1;
+  while (np2 < p.P) np2 <<= 1;
+  const size_t smem = static_cast<size_t>(np2) * 8 + static_cast<size_t>(p.P) * 4 +
+                      static_cast<size_t>(p.B) * 4;
+  k_prune<<<p.R, kPruneThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ root
+
+__global__ void k_root(const RootParams p) {
+  const int m = blockIdx.x;
+  for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
+    const float v = m < p.R ? p.state0[static_cast<size_t>(m) * p.H + h] : 0.f;
+    if (p.bf16)
+      static_cast<uint16_t*>(p.S)[static_cast<size_t>(m) * p.H + h] = float_to_bf16_bits(v);
+    else
+      static_cast<float*>(p.S)[static_cast<size_t>(m) * p.H + h] = v;
+  }
+  if (threadIdx.x == 0) p.score[m] = 0.f;
+}
+
+cudaError_t launch_root(const RootParams& p, cudaStream_t st) {
+  k_root<<<p.n_pad, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t init_select_attrs() {
+  const int smem = 227 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_prune, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace dt

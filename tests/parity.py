@@ -1,0 +1,111 @@
+"""GPU-vs-oracle comparison rules for supertree builds.
+
+Structure (token ids, parents, masks) must match bit for bit, except at
+near-ties: where the oracle's own deciding gap is below NEAR_TIE (1e-4) a
+different GPU choice is counted and reported, and the comparison continues
+from the GPU's choice (teacher forcing), so one flip cannot cascade.
+Scores must agree within the dtype's tolerance: 2e-3 absolute with bf16
+weights, 1e-5 with fp32 weights.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+NEAR_TIE = 1e-4
+TOL = {True: 2e-3, False: 1e-5}
+
+
+def forced_frontier(pool: dict, D: int, W: int, K: int):
+    """GPU pool of one request -> (parent slot, token) per node, pool layout."""
+    sizes, f = [], 1
+    for _ in range(D):
+        f = min(W, K * f)
+        sizes.append(f)
+    slot = np.empty(sum(sizes), np.int32)
+    off_prev, off = 0, 0
+    for d, fd in enumerate(sizes, start=1):
+        par = pool["parent"][off:off + fd]
+        if d == 1:
+            assert np.all(par == -1), "depth-1 parents must be -1"
+            slot[off:off + fd] = 0
+        else:
+            s = par - off_prev
+            prev = sizes[d - 2]
+            assert np.all((s >= 0) & (s < prev)), "parent outside previous depth"
+            slot[off:off + fd] = s
+        assert np.all(pool["depth"][off:off + fd] == d)
+        off_prev, off = off, off + fd
+    return slot, np.ascontiguousarray(pool["token"], np.int32), sizes
+
+
+def compare_request(inp: dict, r: int, D: int, W: int, K: int, B: int, beta: float,
+                    bf16: bool, gpu_pool: dict, gpu_rows: list, gpu_tree: dict) -> dict:
+    """Teacher-forced comparison of one request.  Raises AssertionError on a
+    mismatch that no near-tie explains; returns counters otherwise."""
+    tol = TOL[bf16]
+    slot, tok, sizes = forced_frontier(gpu_pool, D, W, K)
+    o = oracle.build_tree(inp, r, D, W, K, bf16, force_slot=slot, force_tok=tok)
+    rep = {"near_ties": 0, "exact_depths": 0, "max_score_err": 0.0, "max_lse_err": 0.0,
+           "max_logp_err": 0.0, "topk_near_ties": 0}
+    off, F = 0, 1
+    for d in range(1, D + 1):
+        fd = sizes[d - 1]
+        sl = slice(off, off + fd)
+        # --- per-row head results on the (shared) frontier
+        rows = gpu_rows[d - 1]
+        for i in range(F):
+            lse_err = abs(rows["lse"][i] - o["row_lse"][d - 1, i])
+            rep["max_lse_err"] = max(rep["max_lse_err"], lse_err)
+            assert lse_err <= tol, f"depth {d} row {i}: lse {rows['lse'][i]} vs {o['row_lse'][d-1, i]}"
+            gt, ot = rows["tok"][i], o["row_tok"][d - 1, i]
+            olp = {int(t): float(v) for t, v in zip(ot, o["row_logp"][d - 1, i])}
+            if set(gt.tolist()) != set(olp):
+                # only a near-tie at the K-th / (K+1)-th boundary may swap members
+                kg = o["row_kgap"][d - 1, i]
+                assert kg < NEAR_TIE and len(set(gt.tolist()) - set(olp)) == 1, \
+                    f"depth {d} row {i}: top-K {gt} vs {ot} (gap {kg})"
+                rep["topk_near_ties"] += 1
+            common = [(j, int(t)) for j, t in enumerate(gt) if int(t) in olp]
+            vals = [olp[t] for _, t in common]
+            assert np.all(np.diff(vals) <= NEAR_TIE), f"depth {d} row {i}: order {gt} vs {ot}"
+            if not np.array_equal(gt, ot) and set(gt.tolist()) == set(olp):
+                rep["topk_near_ties"] += 1
+            e = max((abs(float(rows["logp"][i][j]) - olp[t]) for j, t in common), default=0.0)
+            rep["max_logp_err"] = max(rep["max_logp_err"], e)
+            assert e <= tol, f"depth {d} row {i}: logp err {e}"
+        # --- kept frontier
+        g_slot, g_tok = slot[sl], tok[sl]
+        c_o = o["pool_score"][sl]               # oracle's score of the GPU's nodes
+        err = float(np.max(np.abs(gpu_pool["score"][sl] - c_o)))
+        rep["max_score_err"] = max(rep["max_score_err"], err)
+        assert err <= tol, f"depth {d}: score err {err}"
+        if np.array_equal(g_slot, o["own_slot"][sl]) and np.array_equal(g_tok, o["own_tok"][sl]):
+            rep["exact_depths"] += 1
+        else:
+            wth = o["w_cut"][d - 1, 0]
+            ok_topk = np.all(o["force_margin"][sl] >= -NEAR_TIE)
+            ok_cut = np.all(c_o >= wth - NEAR_TIE)
+            ok_order = np.all(np.diff(c_o) <= NEAR_TIE)
+            assert ok_topk and ok_cut and ok_order, (
+                f"depth {d}: GPU frontier differs beyond near-ties "
+                f"(topk {ok_topk}, cut {ok_cut}, order {ok_order})")
+            rep["near_ties"] += 1
+        off += fd
+        F = fd
+    # --- deferred Top-B: a pure function of the pool -> bit-exact
+    ref = oracle.topb(gpu_pool["parent"], gpu_pool["token"], gpu_pool["depth"],
+                      gpu_pool["score"], B, beta)
+    assert ref["rc"] == 0
+    n = ref["n_out"]
+    assert int(gpu_tree["n_out"]) == n
+    for k in ("parent", "token", "depth"):
+        assert np.array_equal(gpu_tree[k], ref[k]), k
+    assert np.array_equal(gpu_tree["score"].view(np.uint32), ref["score"].view(np.uint32))
+    assert np.array_equal(gpu_tree["mask"].reshape(ref["mask"].shape).view(np.uint32),
+                          ref["mask"])
+    # Lemma 1 on the GPU's pool
+    heap = oracle.heap_prune(gpu_pool["parent"], gpu_pool["depth"], gpu_pool["score"], B, beta)
+    assert np.array_equal(ref["order"][:n], heap)
+    return rep
