@@ -70,7 +70,7 @@ def build_bytes(w: I.Workload) -> float:
 
 
 def kernels_per_build(w: I.Workload) -> int:
-    return 1 + w.D * 3 + (w.D - 1) + 1      # root, head+merge+select per depth, states, prune
+    return 1 + w.D * 2 + (w.D - 1) + 1      # root, head + merge/select per depth, states, prune
 
 
 def kernel_source_hash() -> str:

@@ -136,7 +136,8 @@ dartree_status dartree_sync_status(dartree_ctx *ctx, void *stream);
 /* Number of batched head calls made by the last build (== its D). */
 int64_t dartree_head_calls(const dartree_ctx *ctx);
 
-/* Text of the last error recorded by this context ("" if none). */
+/* Text of the last error recorded by this context ("" if none); with a NULL
+ * context, why the last dartree_create on this thread failed. */
 const char *dartree_last_error(const dartree_ctx *ctx);
 
 /* Per-kernel timing.  When enabled, every launch of a build is bracketed by

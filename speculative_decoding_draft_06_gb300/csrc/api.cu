@@ -54,10 +54,15 @@ struct dartree_ctx {
   EncodeTiledFn encode = nullptr;
 
   // workspace (device)
-  void* S_cur = nullptr;    // [256][H] states of the current head rows
-  void* S_in = nullptr;     // [256][H] parents' states for the next state step
+  void* S[2] = {nullptr, nullptr};  // [256][H] states of head rows (ping-pong)
   float* score[2] = {nullptr, nullptr};
-  int32_t* tok_next = nullptr;
+  int32_t* tok_next = nullptr;      // [256] token of each next-depth row
+  int32_t* slot_next = nullptr;     // [256] parent row of each next-depth row
+  int32_t* iota = nullptr;          // [256] 0, 1, 2, ...
+  int* counters = nullptr;          // [256] per-request arrival counters (select)
+  float* part = nullptr;            // split-K partial sums of the state step
+  int* tile_cnt = nullptr;          // split-K arrival counters
+  int state_split = 1;
   float* pm = nullptr;
   float* ps = nullptr;
   uint64_t* ptop = nullptr;
@@ -79,8 +84,7 @@ struct dartree_ctx {
   uint32_t* o_mask = nullptr;
   int32_t* o_nout = nullptr;
 
-  CUtensorMap tm_cur[kNumPads];
-  CUtensorMap tm_in[kNumPads];
+  CUtensorMap tm_S[2][kNumPads];
   CUtensorMap tm_A{}, tm_Wout{};
   const void* tm_A_ptr = nullptr;
   const void* tm_Wout_ptr = nullptr;
@@ -113,6 +117,18 @@ struct dartree_ctx {
 };
 
 namespace {
+
+// Why the last dartree_create on this thread failed (no context exists then).
+thread_local std::string g_create_error;
+
+dartree_status create_fail(dartree_status s, const char* what, cudaError_t e = cudaSuccess) {
+  g_create_error = what;
+  if (e != cudaSuccess) {
+    g_create_error += ": ";
+    g_create_error += cudaGetErrorString(e);
+  }
+  return s;
+}
 
 dartree_status encode_2d(dartree_ctx* c, CUtensorMap* m, const void* ptr, uint64_t rows,
                          uint64_t cols, uint32_t box_rows) {
@@ -167,10 +183,12 @@ cudaError_t alloc(T** p, size_t count) {
   return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T) + 16);
 }
 
-// Head call for M rows whose states are in c->S_cur (rows >= M are zero or
-// finite): fused logits + partials, then the per-row merge into rows_*.
-dartree_status run_head(dartree_ctx* c, const float* z, long long z_req_stride, int rows_per_req,
-                        int M, int K, double* lse, int32_t* tok, float* logp, cudaStream_t st) {
+// Head call for M rows whose states are in c->S[sbuf] (rows >= M up to the
+// padded count are zero or finite): fused logits + partials, then the row
+// merge (+ the request's top-W selection when sel != nullptr).
+dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_req_stride,
+                        int rows_per_req, int M, int K, double* lse, int32_t* tok, float* logp,
+                        const dt::MergeParams* sel, cudaStream_t st) {
   const int V = c->cfg.V, H = c->cfg.H;
   const int N = pad_rows(M);
   dt::TcParams p{};
@@ -187,35 +205,37 @@ dartree_status run_head(dartree_ctx* c, const float* z, long long z_req_stride, 
   p.ps = c->ps;
   p.ptop = c->ptop;
   p.cta_stride = c->max_cta;
-  p.list_stride = c->max_cta * dt::kEpiWarps;
+  p.list_stride = c->max_cta;
   int grid;
   cudaError_t e;
   {
     KernelTimer tk(c, st, 0);
     if (c->bf16) {
       grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
-      e = dt::launch_head_tc(N, true, c->tm_Wout, c->tm_cur[pad_index(N)], p, grid, st);
+      e = dt::launch_head_tc(N, true, c->tm_Wout, c->tm_S[sbuf][pad_index(N)], p, grid, st);
     } else {
       grid = p.n_tiles < c->max_cta ? p.n_tiles : c->max_cta;
       p.W_f32 = static_cast<const float*>(c->tm_Wout_ptr);
-      p.S_f32 = static_cast<const float*>(c->S_cur);
+      p.S_f32 = static_cast<const float*>(c->S[sbuf]);
       e = dt::launch_head_simt(N, true, p, grid, st);
     }
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "head logits launch");
   dt::MergeParams mp{};
+  if (sel) mp = *sel;
   mp.pm = c->pm;
   mp.ps = c->ps;
   mp.ptop = c->ptop;
   mp.n_cta = grid;
   mp.cta_stride = c->max_cta;
-  mp.list_stride = c->max_cta * dt::kEpiWarps;
+  mp.list_stride = c->max_cta;
   mp.K = K;
   mp.M = M;
   mp.row_lse = lse;
   mp.row_tok = tok;
   mp.row_logp = logp;
   mp.err = c->d_err;
+  mp.select = sel != nullptr;
   {
     KernelTimer tk(c, st, 2);
     e = dt::launch_merge_rows(mp, st);
@@ -224,29 +244,37 @@ dartree_status run_head(dartree_ctx* c, const float* z, long long z_req_stride, 
   return DARTREE_OK;
 }
 
-// State step for M rows: c->S_cur = q(tanh(A c->S_in + E[tok])).
-dartree_status run_state(dartree_ctx* c, const void* A, const void* E, const int32_t* tok, int M,
-                         cudaStream_t st) {
+// State step: S[src^1][q] = q(tanh(A S[src][slot[q]] + E[tok[q]])) for
+// q < M_out (zeros up to the padded count); S[src] holds M_in rows.
+dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, int M_in,
+                         const int32_t* slot, const int32_t* tok, int M_out, cudaStream_t st) {
   const int H = c->cfg.H;
-  const int N = pad_rows(M);
+  const int N = pad_rows(M_in);
   dt::TcParams p{};
   p.rows = H;
   p.H = H;
-  p.M = M;
+  p.M = M_in;
+  p.M_out = M_out;
+  p.slot = slot;
+  p.tok = tok;
   p.n_tiles = (H + dt::kTileV - 1) / dt::kTileV;
   p.err = c->d_err;
-  p.tok = tok;
   cudaError_t e;
   KernelTimer tk(c, st, 1);
   if (c->bf16) {
     p.E_bf16 = static_cast<const uint16_t*>(E);
-    p.S_out_bf16 = static_cast<uint16_t*>(c->S_cur);
-    e = dt::launch_head_tc(N, false, c->tm_A, c->tm_in[pad_index(N)], p, p.n_tiles, st);
+    p.S_out_bf16 = static_cast<uint16_t*>(c->S[src ^ 1]);
+    p.n_split = c->state_split;
+    p.part = c->part;
+    p.tile_cnt = c->tile_cnt;
+    e = dt::launch_head_tc(N, false, c->tm_A, c->tm_S[src][pad_index(N)], p,
+                           p.n_tiles * p.n_split, st);
   } else {
     p.E_f32 = static_cast<const float*>(E);
-    p.S_out_f32 = static_cast<float*>(c->S_cur);
+    p.S_out_f32 = static_cast<float*>(c->S[src ^ 1]);
     p.W_f32 = static_cast<const float*>(A);
-    p.S_f32 = static_cast<const float*>(c->S_in);
+    p.S_f32 = static_cast<const float*>(c->S[src]);
+    p.n_split = 1;
     e = dt::launch_head_simt(N, false, p, p.n_tiles, st);
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "state step launch");
@@ -307,7 +335,7 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   rp.H = H;
   rp.bf16 = c->bf16;
   rp.state0 = s0;
-  rp.S = c->S_cur;
+  rp.S = c->S[0];
   rp.score = c->score[0];
   cudaError_t e;
   {
@@ -315,49 +343,43 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
     e = dt::launch_root(rp, st);
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "root launch");
-  int F = 1, off_prev = 0, off = 0, cur = 0;
+  int F = 1, F_prev = 1, off_prev = 0, off = 0, cur = 0, sbuf = 0;
   int64_t calls = 0;
   for (int d = 1; d <= D; ++d) {
     const int M = R * F;
     if (d >= 2) {
-      if ((s = run_state(c, head->A, head->E, c->tok_next, M, st)) != DARTREE_OK) return s;
+      // states of this depth's rows from their parents (the rows of call d-1)
+      s = run_state(c, head->A, head->E, sbuf, R * F_prev, c->slot_next, c->tok_next, M, st);
+      if (s != DARTREE_OK) return s;
+      sbuf ^= 1;
     }
+    const int Fd = frontier_after(F, W, K);
+    dt::MergeParams sel{};
+    sel.R = R;
+    sel.F = F;
+    sel.Fd = Fd;
+    sel.depth = d;
+    sel.off_prev = off_prev;
+    sel.off = off;
+    sel.pool_stride = P;
+    sel.score_in = c->score[cur];
+    sel.score_out = c->score[cur ^ 1];
+    sel.slot_next = c->slot_next;
+    sel.tok_next = c->tok_next;
+    sel.pool_parent = c->pool_parent;
+    sel.pool_token = c->pool_token;
+    sel.pool_depth = c->pool_depth;
+    sel.pool_score = c->pool_score;
+    sel.counters = c->counters;
     const size_t ro = static_cast<size_t>(d - 1) * dt::kMaxRows;
-    s = run_head(c, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V, F, M, K,
-                 c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, st);
+    s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V, F,
+                 M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel, st);
     if (s != DARTREE_OK) return s;
     ++calls;
-    const int Fd = frontier_after(F, W, K);
-    dt::SelectParams sp{};
-    sp.R = R;
-    sp.F = F;
-    sp.Fd = Fd;
-    sp.K = K;
-    sp.depth = d;
-    sp.off_prev = off_prev;
-    sp.off = off;
-    sp.pool_stride = P;
-    sp.row_tok = c->rows_tok + ro * K;
-    sp.row_logp = c->rows_logp + ro * K;
-    sp.score_in = c->score[cur];
-    sp.score_out = c->score[cur ^ 1];
-    sp.tok_next = c->tok_next;
-    sp.pool_parent = c->pool_parent;
-    sp.pool_token = c->pool_token;
-    sp.pool_depth = c->pool_depth;
-    sp.pool_score = c->pool_score;
-    sp.S_cur = c->S_cur;
-    sp.S_next_in = d < D ? c->S_in : nullptr;
-    sp.H = H;
-    sp.elem_bytes = static_cast<int>(c->elem);
-    {
-      KernelTimer tk(c, st, 3);
-      e = dt::launch_select(sp, st);
-    }
-    if (e != cudaSuccess) return c->cuda_fail(e, "select launch");
     cur ^= 1;
     off_prev = off;
     off += Fd;
+    F_prev = F;
     F = Fd;
   }
   dt::PruneParams pp{};
@@ -401,7 +423,8 @@ void free_events(dartree_ctx* c) {
 
 void free_all(dartree_ctx* c) {
   free_events(c);
-  void* ptrs[] = {c->S_cur,     c->S_in,       c->score[0],    c->score[1],   c->tok_next,
+  void* ptrs[] = {c->S[0],      c->S[1],       c->score[0],    c->score[1],   c->tok_next,
+                  c->slot_next, c->iota,       c->counters,    c->part,       c->tile_cnt,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
                   c->d_err,     c->z_stage,    c->s0_stage,    c->o_parent,   c->o_token,
@@ -425,17 +448,20 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K) {
 }
 
 dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
-  if (!cfg || !out) return DARTREE_ERR_INVALID_ARG;
+  if (!cfg || !out) return create_fail(DARTREE_ERR_INVALID_ARG, "null argument");
   *out = nullptr;
+  g_create_error.clear();
   const dartree_config g = *cfg;
-  if (g.wdtype != DARTREE_W_F32 && g.wdtype != DARTREE_W_BF16) return DARTREE_ERR_INVALID_ARG;
+  if (g.wdtype != DARTREE_W_F32 && g.wdtype != DARTREE_W_BF16)
+    return create_fail(DARTREE_ERR_INVALID_ARG, "unknown weight dtype");
   if (g.V < 1 || g.H < 1 || g.max_D < 1 || g.max_W < 1 || g.max_K < 1 || g.max_B < 1 ||
       g.max_requests < 1)
-    return DARTREE_ERR_INVALID_ARG;
+    return create_fail(DARTREE_ERR_INVALID_ARG, "sizes must be >= 1");
   if (g.max_K > DARTREE_MAX_K || g.max_D > DARTREE_MAX_D || g.max_B > DARTREE_MAX_B ||
       g.max_W > DARTREE_MAX_ROWS || static_cast<long long>(g.max_requests) * g.max_W > DARTREE_MAX_ROWS)
-    return DARTREE_ERR_UNSUPPORTED;
-  if (g.wdtype == DARTREE_W_BF16 ? (g.H % 64 != 0) : (g.H % 8 != 0)) return DARTREE_ERR_UNSUPPORTED;
+    return create_fail(DARTREE_ERR_UNSUPPORTED, "capacity beyond the build limits");
+  if (g.wdtype == DARTREE_W_BF16 ? (g.H % 64 != 0) : (g.H % 8 != 0))
+    return create_fail(DARTREE_ERR_UNSUPPORTED, "H must be a multiple of 64 (bf16) or 8 (fp32)");
 
   dartree_ctx* c = new (std::nothrow) dartree_ctx();
   if (!c) return DARTREE_ERR_OOM;
@@ -447,11 +473,11 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (e == cudaSuccess) e = cudaGetDeviceProperties(&prop, c->device);
   if (e != cudaSuccess) {
     delete c;
-    return DARTREE_ERR_CUDA;
+    return create_fail(DARTREE_ERR_CUDA, "device query", e);
   }
   if (prop.major != 10 || prop.minor != 3) {
     delete c;
-    return DARTREE_ERR_UNSUPPORTED;
+    return create_fail(DARTREE_ERR_UNSUPPORTED, "needs a compute capability 10.3 device");
   }
   c->num_sms = prop.multiProcessorCount;
   c->max_cta = 2 * c->num_sms;
@@ -462,17 +488,26 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
   if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
     delete c;
-    return DARTREE_ERR_CUDA;
+    return create_fail(DARTREE_ERR_CUDA, "cuTensorMapEncodeTiled entry point", e);
   }
   c->encode = reinterpret_cast<EncodeTiledFn>(fn);
 
   const size_t rows = dt::kMaxRows;
   const size_t Rc = static_cast<size_t>(g.max_requests);
   const size_t B = static_cast<size_t>(g.max_B), words = (B + 31) / 32;
-  bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S_cur), rows * g.H * c->elem) == cudaSuccess &&
-            alloc(reinterpret_cast<uint8_t**>(&c->S_in), rows * g.H * c->elem) == cudaSuccess &&
+  const int h_tiles = (g.H + dt::kTileV - 1) / dt::kTileV;
+  const int nk = g.H / dt::kTileH;
+  c->state_split = c->num_sms / h_tiles;
+  if (c->state_split > nk) c->state_split = nk;
+  if (c->state_split < 1) c->state_split = 1;
+  bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S[0]), rows * g.H * c->elem) == cudaSuccess &&
+            alloc(reinterpret_cast<uint8_t**>(&c->S[1]), rows * g.H * c->elem) == cudaSuccess &&
             alloc(&c->score[0], rows) == cudaSuccess && alloc(&c->score[1], rows) == cudaSuccess &&
-            alloc(&c->tok_next, rows) == cudaSuccess &&
+            alloc(&c->tok_next, rows) == cudaSuccess && alloc(&c->slot_next, rows) == cudaSuccess &&
+            alloc(&c->iota, rows) == cudaSuccess && alloc(&c->counters, rows) == cudaSuccess &&
+            alloc(&c->part, static_cast<size_t>(h_tiles) * c->state_split * rows * dt::kTileV) ==
+                cudaSuccess &&
+            alloc(&c->tile_cnt, static_cast<size_t>(h_tiles)) == cudaSuccess &&
             alloc(&c->pm, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ps, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ptop, rows * c->max_cta * dt::kEpiWarps * g.max_K) == cudaSuccess &&
@@ -494,27 +529,34 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
     cudaGetLastError();
     free_all(c);
     delete c;
-    return DARTREE_ERR_OOM;
+    return create_fail(DARTREE_ERR_OOM, "workspace allocation");
   }
-  e = cudaMemset(c->S_cur, 0, rows * g.H * c->elem);
-  if (e == cudaSuccess) e = cudaMemset(c->S_in, 0, rows * g.H * c->elem);
+  e = cudaMemset(c->S[0], 0, rows * g.H * c->elem);
+  if (e == cudaSuccess) e = cudaMemset(c->S[1], 0, rows * g.H * c->elem);
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, rows * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
+  if (e == cudaSuccess) {
+    int32_t h_iota[dt::kMaxRows];
+    for (int i = 0; i < dt::kMaxRows; ++i) h_iota[i] = i;
+    e = cudaMemcpy(c->iota, h_iota, sizeof h_iota, cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = dt::init_head_attrs();
   if (e == cudaSuccess) e = dt::init_select_attrs();
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(c);
     delete c;
-    return DARTREE_ERR_CUDA;
+    return create_fail(DARTREE_ERR_CUDA, "workspace initialisation", e);
   }
   if (c->bf16) {
     for (int i = 0; i < kNumPads; ++i) {
       const uint32_t n = 16u << i;
-      if (encode_2d(c, &c->tm_cur[i], c->S_cur, rows, g.H, n) != DARTREE_OK ||
-          encode_2d(c, &c->tm_in[i], c->S_in, rows, g.H, n) != DARTREE_OK) {
+      if (encode_2d(c, &c->tm_S[0][i], c->S[0], rows, g.H, n) != DARTREE_OK ||
+          encode_2d(c, &c->tm_S[1][i], c->S[1], rows, g.H, n) != DARTREE_OK) {
         free_all(c);
         delete c;
-        return DARTREE_ERR_CUDA;
+        return create_fail(DARTREE_ERR_CUDA, "state tensor map");
       }
     }
   }
@@ -630,7 +672,7 @@ dartree_status dartree_reset_timing(dartree_ctx* ctx) {
 int64_t dartree_head_calls(const dartree_ctx* ctx) { return ctx ? ctx->head_calls : -1; }
 
 const char* dartree_last_error(const dartree_ctx* ctx) {
-  return ctx ? ctx->last_error.c_str() : "null context";
+  return ctx ? ctx->last_error.c_str() : g_create_error.c_str();
 }
 
 dartree_status dartree_get_pool(dartree_ctx* ctx, int32_t* parent, int32_t* token, int32_t* depth,
@@ -683,11 +725,11 @@ dartree_status dartree_head_topk(dartree_ctx* ctx, const void* S, const float* z
   if (s != DARTREE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
-  cudaError_t e = cudaMemcpyAsync(ctx->S_cur, S, M * rb, cudaMemcpyDeviceToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(ctx->S[0], S, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && pad_rows(M) > M)
-    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S_cur) + M * rb, 0, (pad_rows(M) - M) * rb, st);
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S[0]) + M * rb, 0, (pad_rows(M) - M) * rb, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy");
-  return run_head(ctx, z, z_req_stride, rows_per_req, M, K, lse, tok, logp, st);
+  return run_head(ctx, 0, z, z_req_stride, rows_per_req, M, K, lse, tok, logp, nullptr, st);
 }
 
 dartree_status dartree_state_step(dartree_ctx* ctx, const void* S_par, const int32_t* tok,
@@ -702,12 +744,12 @@ dartree_status dartree_state_step(dartree_ctx* ctx, const void* S_par, const int
   if (!ctx->bf16) ctx->tm_A_ptr = A;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
-  cudaError_t e = cudaMemcpyAsync(ctx->S_in, S_par, M * rb, cudaMemcpyDeviceToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(ctx->S[0], S_par, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && pad_rows(M) > M)
-    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S_in) + M * rb, 0, (pad_rows(M) - M) * rb, st);
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S[0]) + M * rb, 0, (pad_rows(M) - M) * rb, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy");
-  if ((s = run_state(ctx, A, E, tok, M, st)) != DARTREE_OK) return s;
-  e = cudaMemcpyAsync(S_out, ctx->S_cur, M * rb, cudaMemcpyDeviceToDevice, st);
+  if ((s = run_state(ctx, A, E, 0, M, ctx->iota, tok, M, st)) != DARTREE_OK) return s;
+  e = cudaMemcpyAsync(S_out, ctx->S[1], M * rb, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy back");
   return DARTREE_OK;
 }

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
 namespace dt {
 
@@ -58,6 +59,78 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
 
 __device__ __forceinline__ float fast_exp(float x) {  // e^x, x <= 0 in practice
   return exp2f(x * 1.4426950408889634f);
+}
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(kFullMask, static_cast<uint32_t>(v), src);
+  const uint32_t hi = __shfl_sync(kFullMask, static_cast<uint32_t>(v >> 32), src);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int mask) {
+  const uint32_t lo = __shfl_xor_sync(kFullMask, static_cast<uint32_t>(v), mask);
+  const uint32_t hi = __shfl_xor_sync(kFullMask, static_cast<uint32_t>(v >> 32), mask);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Smallest power of two >= k (k <= 32).
+__host__ __device__ __forceinline__ int pow2_ceil32(int k) {
+  return k <= 1 ? 1 : k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32;
+}
+
+// Warp-wide merge of two descending key lists of length p2 (a power of two
+// <= 32); the result is the best p2 keys, descending, in lanes 0..p2-1.
+//   p2 == 32: v = a[lane], y = b[31 - lane].
+//   p2 <= 16: v = a[lane] in lanes < p2 and b[2*p2 - 1 - lane] in lanes
+//             p2 .. 2*p2-1 (a bitonic sequence); y is unused.
+// One half-cleaner keeps the larger of each mirrored pair, then a bitonic
+// merge sorts the surviving half.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t v, uint64_t y, int p2) {
+  const int lane = threadIdx.x & 31;
+  int s;
+  if (p2 == 32) {
+    v = v > y ? v : y;
+    s = 16;
+  } else {
+    const uint64_t o = shfl_xor_u64(v, p2);
+    v = (lane & p2) ? (v < o ? v : o) : (v > o ? v : o);
+    s = p2 >> 1;
+  }
+  for (; s > 0; s >>= 1) {
+    const uint64_t o = shfl_xor_u64(v, s);
+    v = (lane & s) ? (v < o ? v : o) : (v > o ? v : o);
+  }
+  return v;
+}
+
+// Operands for folding the descending list L (K valid keys, zero-padded to
+// p2) into a running list held in lanes 0..p2-1 (v): on return (v, y) are
+// the arguments of warp_merge_desc.
+__device__ __forceinline__ void merge_operands(const uint64_t* L, int K, int p2, uint64_t& v,
+                                               uint64_t& y) {
+  const int lane = threadIdx.x & 31;
+  if (p2 == 32) {
+    const int j = 31 - lane;
+    y = j < K ? L[j] : 0ull;
+  } else {
+    const int j = 2 * p2 - 1 - lane;
+    const uint64_t b = (lane >= p2 && lane < 2 * p2 && j < K) ? L[j] : 0ull;
+    v = lane < p2 ? v : b;
+    y = 0ull;
+  }
+}
+
+// Opt a kernel into the largest dynamic shared memory it can use: the
+// per-block limit minus its static shared memory.
+template <typename Kern>
+inline cudaError_t set_max_dynamic_smem(Kern* k) {
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, k);
+  if (e != cudaSuccess) return e;
+  const int limit = 227 * 1024 - static_cast<int>(a.sharedSizeBytes);
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
 }
 
 // Padded column count for r valid head rows (an MMA N: 16, 32, 64, 128, 256).

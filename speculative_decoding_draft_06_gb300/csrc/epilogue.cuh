@@ -20,19 +20,7 @@
 
 namespace dt {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
-
-__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
-  const uint32_t lo = __shfl_sync(kFull, static_cast<uint32_t>(v), src);
-  const uint32_t hi = __shfl_sync(kFull, static_cast<uint32_t>(v >> 32), src);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int mask) {
-  const uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), mask);
-  const uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), mask);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
+constexpr unsigned kFull = kFullMask;
 
 // Bitonic sort of one key per lane; afterwards lane 0 holds the largest.
 static __device__ __noinline__ uint64_t warp_sort_desc(uint64_t k) {
@@ -213,10 +201,20 @@ struct LogitsEpilogue {
       pm[(size_t)c * cta_stride + cta] = m;
       ps[(size_t)c * cta_stride + cta] = s;
     }
-    for (int c = 0; c < M; ++c) {
-      if (lane < K)
-        ptop[((size_t)c * list_stride + (size_t)cta * kEpiWarps + warp) * K + lane] =
-            lists[c * K + lane];
+    // one list per CTA and row: warp (c % 4) folds the four warps' lists
+    // (this warp's lists start at `lists`; the CTA's are [warp][N][K])
+    uint64_t* all = lists - static_cast<size_t>(warp) * N * K;
+    const int p2 = pow2_ceil32(K);
+    for (int c = warp; c < M; c += kEpiWarps) {
+      const uint64_t* L0 = all + static_cast<size_t>(c) * K;
+      uint64_t v = lane < K ? L0[lane] : 0ull;
+#pragma unroll
+      for (int w = 1; w < kEpiWarps; ++w) {
+        uint64_t y;
+        merge_operands(all + (static_cast<size_t>(w) * N + c) * K, K, p2, v, y);
+        v = warp_merge_desc(v, y, p2);
+      }
+      if (lane < K) ptop[((size_t)c * list_stride + cta) * K + lane] = v;
     }
     if (bad) atomicOr(err, DT_ERR_NONFINITE);
   }

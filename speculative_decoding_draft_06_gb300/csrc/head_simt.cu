@@ -110,25 +110,25 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
         }
       }
     } else {
-      for (int c0 = 0; c0 < N; c0 += 16) {
+      // U = A S_in for the M input rows (kept per thread in shared memory),
+      // then output row q takes U[:, slot[q]]
+      float* Us = reinterpret_cast<float*>(red + kEpiWarps * N) + tid * (N + 1);
+      for (int c0 = 0; c0 < mcols; c0 += 16) {
         float acc[16];
-        if (c0 < mcols) {
-          dot16(acc, c0);
-        } else {
+        dot16(acc, c0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        }
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = c0 + j;
-            float out = 0.f;
-            if (m < p.M) {
-              const int tok = __ldg(p.tok + m);
-              out = tanhf(acc[j] + __ldg(p.E_f32 + static_cast<size_t>(tok) * p.H + row));
-            }
-            p.S_out_f32[static_cast<size_t>(m) * p.H + row] = out;
+        for (int j = 0; j < 16; ++j) Us[c0 + j] = acc[j];
+      }
+      if (valid) {
+        const int n_out = pad_rows(p.M_out);
+        for (int q = 0; q < n_out; ++q) {
+          float out = 0.f;
+          if (q < p.M_out) {
+            const int tok = __ldg(p.tok + q);
+            out = tanhf(Us[__ldg(p.slot + q)] +
+                        __ldg(p.E_f32 + static_cast<size_t>(tok) * p.H + row));
           }
+          p.S_out_f32[static_cast<size_t>(q) * p.H + row] = out;
         }
       }
     }
@@ -143,7 +143,8 @@ template <int N, bool kLogits>
 static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(kTileV) * (kSimtH + 1) * 4 + 16 * kSimtH * 4 +
                       static_cast<size_t>(kLogits ? kEpiWarps * N * p.K : 0) * 8 +
-                      static_cast<size_t>(kEpiWarps) * N * sizeof(float2);
+                      static_cast<size_t>(kEpiWarps) * N * sizeof(float2) +
+                      (kLogits ? 0 : static_cast<size_t>(kTileV) * (N + 1) * 4);
   k_head_simt<N, kLogits><<<grid, 128, smem, st>>>(p);
   return cudaGetLastError();
 }
@@ -156,12 +157,9 @@ static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
 #define DT_CAT(a, b) DT_CAT2(a, b)
 
 cudaError_t DT_CAT(init_head_simt_attrs_, DT_N)() {
-  const int smem = 227 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_head_simt<DT_N, true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_max_dynamic_smem(k_head_simt<DT_N, true>);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_head_simt<DT_N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem);
+  return set_max_dynamic_smem(k_head_simt<DT_N, false>);
 }
 
 cudaError_t DT_CAT(launch_head_simt_, DT_N)(bool logits, const TcParams& p, int grid,

@@ -39,6 +39,74 @@ struct TcLayout {
   static constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
 };
 
+__device__ __forceinline__ void state_store(const TcParams& p, int q, int row, float u) {
+  float out = 0.f;
+  if (q < p.M_out) {
+    const int tok = __ldg(p.tok + q);
+    out = tanhf(u + bf16_bits_to_float(__ldg(p.E_bf16 + static_cast<size_t>(tok) * p.H + row)));
+  }
+  p.S_out_bf16[static_cast<size_t>(q) * p.H + row] = float_to_bf16_bits(out);
+}
+
+// State step epilogue (all 128 epilogue threads; thread = hidden unit `row`).
+// Output row q takes column slot[q] of U = A S_in (its parent's row).
+template <int N>
+__device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase, int tile,
+                                               int split, int warp, int lane, int row,
+                                               bool valid) {
+  const int n_out = pad_rows(p.M_out);
+  if (p.n_split == 1) {
+    for (int q0 = 0; q0 < n_out; q0 += 8) {
+      float u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int q = q0 + j;
+        const int col = q < p.M_out ? __ldg(p.slot + q) : 0;   // same for the whole warp
+        uint32_t r;
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                     : "=r"(r)
+                     : "r"(tbase + static_cast<uint32_t>(col)));
+        u[j] = __uint_as_float(r);
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) state_store(p, q0 + j, row, u[j]);
+      }
+    }
+    return;
+  }
+  // split-K: publish this CTA's partial tile; the last CTA of the tile sums
+  // the partials in split order (deterministic) and finishes the rows
+  const int lr = warp * 32 + lane;
+  float* mine = p.part + (static_cast<size_t>(tile) * p.n_split + split) * kMaxRows * kTileV;
+  for (int c0 = 0; c0 < p.M; c0 += 16) {
+    float x[16];
+    tmem_ld16(tbase + c0, x);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < p.M) mine[static_cast<size_t>(c0 + j) * kTileV + lr] = x[j];
+  }
+  __threadfence();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  __shared__ int last;
+  if (lr == 0) last = (atomicAdd(p.tile_cnt + tile, 1) == p.n_split - 1);
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (!last) return;
+  __threadfence();
+  const float* all = p.part + static_cast<size_t>(tile) * p.n_split * kMaxRows * kTileV;
+  for (int q = 0; q < n_out; ++q) {
+    float u = 0.f;
+    if (q < p.M_out) {
+      const int col = __ldg(p.slot + q);
+      for (int sp = 0; sp < p.n_split; ++sp)
+        u += __ldcg(all + (static_cast<size_t>(sp) * kMaxRows + col) * kTileV + lr);
+    }
+    if (valid) state_store(p, q, row, u);
+  }
+  if (lr == 0) p.tile_cnt[tile] = 0;
+}
+
 template <int N, bool kLogits>
 __global__ void __launch_bounds__(192, 1)
     k_head_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
@@ -65,11 +133,21 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // contiguous, balanced tile range of this CTA
-  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
-  const int t_end =
-      static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
-  const int nk = p.H / kTileH;
+  // work of this CTA: logits -- a contiguous, balanced range of tiles over
+  // the whole contraction; state -- one tile and one slice of the
+  // contraction (split-K, reduced through global scratch)
+  const int nk_all = p.H / kTileH;
+  int t_begin, t_end, kb_begin = 0, kb_end = nk_all, split = 0;
+  if constexpr (kLogits) {
+    t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
+    t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
+  } else {
+    t_begin = blockIdx.x / p.n_split;
+    t_end = t_begin + 1;
+    split = blockIdx.x % p.n_split;
+    kb_begin = split * nk_all / p.n_split;
+    kb_end = (split + 1) * nk_all / p.n_split;
+  }
 
   if (warp == 5) tmem_alloc<L::kTmemCols>(tmem_slot);
   if (threadIdx.x == 0) {
@@ -105,7 +183,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       long long issued = 0;
       for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err)) {
             *abort_flag = 1;
             break;
@@ -146,7 +224,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * N);
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.err)) {
             *abort_flag = 1;
             ok = false;
@@ -159,7 +237,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < kTileH / 16; ++k) {
             tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
-                        idesc, (kb | k) != 0);
+                        idesc, (kb != kb_begin || k != 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == S) {
@@ -224,24 +302,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         epi.tile_done();
       } else {
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          float x[16];
-          tmem_ld16(tbase + c0, x);
-          if (valid) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int m = c0 + j;
-              float out = 0.f;
-              if (m < p.M) {
-                const int tok = __ldg(p.tok + m);
-                const float e = bf16_bits_to_float(
-                    __ldg(p.E_bf16 + static_cast<size_t>(tok) * p.H + row));
-                out = tanhf(x[j] + e);
-              }
-              p.S_out_bf16[static_cast<size_t>(m) * p.H + row] = float_to_bf16_bits(out);
-            }
-          }
-        }
+        state_epilogue<N>(p, tbase, t, split, warp, lane, row, valid);
       }
       tc_fence_before();
       __syncwarp();
@@ -285,12 +346,9 @@ static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, con
 #define DT_CAT(a, b) DT_CAT2(a, b)
 
 cudaError_t DT_CAT(init_head_tc_attrs_, DT_N)() {
-  const int smem = 227 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_head_tc<DT_N, true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_max_dynamic_smem(k_head_tc<DT_N, true>);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_head_tc<DT_N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem);
+  return set_max_dynamic_smem(k_head_tc<DT_N, false>);
 }
 
 cudaError_t DT_CAT(launch_head_tc_, DT_N)(bool logits, const CUtensorMap& tw, const CUtensorMap& ts,

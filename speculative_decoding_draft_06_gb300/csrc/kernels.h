@@ -24,12 +24,19 @@ struct TcParams {
   uint64_t* ptop;      // [rows_max][list_stride][K] per-warp top-K keys
   int cta_stride;
   int list_stride;
-  // state epilogue
-  const int32_t* tok;        // [M] committed token of each head row
+  // state epilogue: U = A S_in for the M input rows, then output row q
+  // (q < M_out) is q(tanh(U[:, slot[q]] + E[tok[q]])); rows M_out .. pad
+  // are written as zeros.
+  int M_out;
+  const int32_t* slot;       // [M_out] input row (parent) of each output row
+  const int32_t* tok;        // [M_out] committed token of each output row
   const uint16_t* E_bf16;    // [V][H]
   uint16_t* S_out_bf16;      // [rows_max][H]
   const float* E_f32;
   float* S_out_f32;
+  int n_split;               // contraction split across CTAs (tensor-core path)
+  float* part;               // [tiles * n_split][256][128] fp32 partial sums
+  int* tile_cnt;             // [tiles] arrival counters, zero between launches
   // SIMT operands (fp32 path)
   const float* W_f32;        // [rows][H]
   const float* S_f32;        // [rows_max][H]
@@ -74,7 +81,8 @@ inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, i
   }
 }
 
-// Merge of per-CTA partials into per-row lse and top-K (log-probs).
+// Merge of per-CTA partials into per-row lse and top-K (log-probs), and
+// (select != 0) the global top-W of each request with pool append.
 struct MergeParams {
   const float* pm;
   const float* ps;
@@ -88,29 +96,22 @@ struct MergeParams {
   int32_t* row_tok;    // [M][K]
   float* row_logp;     // [M][K]
   int* err;
-};
-cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
-
-// Global top-W of the candidates of each request + pool append + state gather.
-struct SelectParams {
-  int R, F, Fd, K, depth;    // depth is 1-based
+  // fused selection
+  int select;
+  int R, F, Fd, depth;       // depth is 1-based; F = rows per request
   int off_prev, off;         // pool offsets of depth-1 and depth
   int pool_stride;           // pool entries per request
-  const int32_t* row_tok;    // [R*F][K]
-  const float* row_logp;     // [R*F][K]
   const float* score_in;     // [R*F]
   float* score_out;          // [R*Fd]
+  int32_t* slot_next;        // [R*Fd] parent row (in this call) of each kept node
   int32_t* tok_next;         // [R*Fd]
   int32_t* pool_parent;
   int32_t* pool_token;
   int32_t* pool_depth;
   float* pool_score;
-  const void* S_cur;         // [R*F][H] states of this depth's head rows
-  void* S_next_in;           // [R*Fd][H] parent states gathered for the next state step
-  int H;
-  int elem_bytes;
+  int* counters;             // [R] zero between launches
 };
-cudaError_t launch_select(const SelectParams& p, cudaStream_t st);
+cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
 
 // Deferred Top-B, compaction and the ancestor mask.
 struct PruneParams {

@@ -56,24 +56,70 @@ __device__ T block_reduce(T v, Op op, T* scratch) {
   return r;
 }
 
-// ---------------------------------------------------------- merge of rows
+// ------------------------------------------------ merge of rows + top-W
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeCap = 4096;  // keys sorted at once
+constexpr int kMergeWarps = kMergeThreads / 32;
 
-// One block per head row.  lse = max + log(sum_cta s_cta exp(m_cta - max)) in
-// fp64; top-K = best K of all per-warp lists, after discarding every list
-// entry below the largest K-th entry of any list (that bound is <= the
-// row's true K-th key, because that list alone holds K keys at or above it).
+// Global top-W of one request's candidates (run by the last merge block of
+// the request).  Candidate (i, j) = child j of frontier slot i, score
+// c = score_i + logp_ij (one fp32 add), index i*K + j; the best |F_d| by
+// (c desc, index asc) become the new frontier in rank order ("DARTree:
+// Teaching a Chain-Trained Corrector to Think in Trees", Core Mechanism:
+// score by accumulated path probability, keep the top W; "Accelerating
+// Language Models with Diffusion Draft Trees", Summary: global top-W child
+// prefixes, states carried forward).
+__device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys) {
+  const int n = p.F * p.K;
+  const int np2 = pow2_at_least(n);
+  for (int e = threadIdx.x; e < np2; e += blockDim.x) {
+    uint64_t k = 0ull;
+    if (e < n) {
+      const int row = r * p.F + e / p.K;
+      const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + (e % p.K));
+      const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
+      k = make_key(c, static_cast<uint32_t>(e));
+    }
+    keys[e] = k;
+  }
+  __syncthreads();
+  block_sort_desc(keys, np2);
+  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) {
+    const uint64_t k = keys[q];
+    const int idx = static_cast<int>(key_index(k));
+    const int i = idx / p.K, j = idx % p.K;
+    const int row = r * p.F + i;
+    const float c = key_value(k);
+    const int32_t tok = __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + j);
+    const size_t pi = static_cast<size_t>(r) * p.pool_stride + p.off + q;
+    p.pool_parent[pi] = (p.depth == 1) ? -1 : p.off_prev + i;
+    p.pool_token[pi] = tok;
+    p.pool_depth[pi] = p.depth;
+    p.pool_score[pi] = c;
+    const int m = r * p.Fd + q;
+    p.score_out[m] = c;
+    p.tok_next[m] = tok;
+    p.slot_next[m] = row;
+  }
+}
+
+// One block per head row.
+//   lse = max + log(sum_cta s_cta exp(m_cta - max)), the merge in fp64;
+//   top-K = best K keys over the per-CTA sorted lists, by warp-wide bitonic
+//   merges (each warp folds every 8th list into a running list held in
+//   registers, then warp 0 folds the 8 warp results);
+//   logp = fp32(logit - lse).
+// With p.select set, the last block of each request (counted with an
+// atomic, reset afterwards) runs the request's top-W selection.
 __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams p) {
-  __shared__ uint64_t buf[kMergeCap];
+  extern __shared__ uint64_t dyn[];
+  __shared__ uint64_t wl[kMergeWarps][32];
   __shared__ double dscr[32];
   __shared__ float fscr[32];
-  __shared__ unsigned long long uscr[32];
-  __shared__ int iscr[32];
-  __shared__ int n_buf;
+  __shared__ int last_flag;
   const int row = blockIdx.x;
   const int K = p.K;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- log-sum-exp
   float mloc = -INFINITY;
@@ -92,126 +138,68 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   const double lse = (mx == -INFINITY) ? -INFINITY : static_cast<double>(mx) + log(ssum);
   if (threadIdx.x == 0 && mx == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
 
-  // ---- top-K
-  const int n_lists = p.n_cta * kEpiWarps;
+  // ---- top-K over the per-CTA lists
+  const int p2 = pow2_ceil32(K);
   const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;
-  unsigned long long th = 0;
-  for (int l = threadIdx.x; l < n_lists; l += blockDim.x) {
-    const unsigned long long k = base[static_cast<size_t>(l) * K + K - 1];
-    th = k > th ? k : th;
-  }
-  th = block_reduce(th,
-                    [](unsigned long long a, unsigned long long b) { return a > b ? a : b; },
-                    uscr);
-
-  // lists per chunk so that one chunk's survivors plus the best K fit
-  const int lists_per_chunk = (kMergeCap - kMaxK) / K;
-  for (int i = threadIdx.x; i < kMergeCap; i += blockDim.x) buf[i] = 0ull;
-  if (threadIdx.x == 0) n_buf = 0;
-  __syncthreads();
-  bool have_best = false;
-  for (int l0 = 0; l0 < n_lists; l0 += lists_per_chunk) {
-    const int l1 = min(n_lists, l0 + lists_per_chunk);
-    if (threadIdx.x == 0) n_buf = have_best ? K : 0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < (l1 - l0) * K; e += blockDim.x) {
-      const uint64_t k = base[static_cast<size_t>(l0) * K + e];
-      if (k >= th && k != 0ull) {
-        const int pos = atomicAdd(&n_buf, 1);
-        buf[pos] = k;
-      }
+  uint64_t v = 0ull;
+  int l = warp;
+  for (; l + 3 * kMergeWarps < p.n_cta; l += 4 * kMergeWarps) {  // 4 loads in flight
+    uint64_t y[4], vv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      vv[u] = v;
+      merge_operands(base + static_cast<size_t>(l + u * kMergeWarps) * K, K, p2, vv[u], y[u]);
     }
-    __syncthreads();
-    const int n = n_buf;
-    const int np2 = pow2_at_least(n < K ? K : n);
-    for (int i = n + threadIdx.x; i < np2; i += blockDim.x) buf[i] = 0ull;
-    __syncthreads();
-    block_sort_desc(buf, np2);
-    for (int i = K + threadIdx.x; i < np2; i += blockDim.x) buf[i] = 0ull;
-    __syncthreads();
-    have_best = true;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t a = (p2 < 32 && lane >= p2) ? vv[u] : v;
+      v = warp_merge_desc(a, y[u], p2);
+    }
   }
-  if (threadIdx.x < K) {
-    const uint64_t k = buf[threadIdx.x];
-    const float val = key_value(k);
-    p.row_tok[static_cast<size_t>(row) * K + threadIdx.x] = static_cast<int32_t>(key_index(k));
-    p.row_logp[static_cast<size_t>(row) * K + threadIdx.x] =
-        static_cast<float>(static_cast<double>(val) - lse);
+  for (; l < p.n_cta; l += kMergeWarps) {
+    uint64_t y;
+    merge_operands(base + static_cast<size_t>(l) * K, K, p2, v, y);
+    v = warp_merge_desc(v, y, p2);
   }
-  if (threadIdx.x == 0) p.row_lse[row] = lse;
-  (void)iscr;
+  wl[warp][lane] = lane < p2 ? v : 0ull;
+  __syncthreads();
+  if (warp == 0) {
+    v = wl[0][lane];
+    for (int w = 1; w < kMergeWarps; ++w) {
+      uint64_t y;
+      merge_operands(wl[w], p2, p2, v, y);
+      v = warp_merge_desc(v, y, p2);
+    }
+    if (lane < K) {
+      const float val = key_value(v);
+      p.row_tok[static_cast<size_t>(row) * K + lane] = static_cast<int32_t>(key_index(v));
+      p.row_logp[static_cast<size_t>(row) * K + lane] =
+          static_cast<float>(static_cast<double>(val) - lse);
+    }
+    if (lane == 0) p.row_lse[row] = lse;
+  }
+  if (!p.select) return;
+
+  // ---- the last block of request r runs its top-W selection
+  const int r = row / p.F;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_flag = (atomicAdd(p.counters + r, 1) == p.F - 1);
+  __syncthreads();
+  if (!last_flag) return;
+  __threadfence();
+  select_frontier(p, r, dyn);
+  if (threadIdx.x == 0) p.counters[r] = 0;
 }
 
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st) {
-  k_merge_rows<<<p.M, kMergeThreads, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
-// -------------------------------------------------------- top-W per request
-
-constexpr int kSelectThreads = 1024;
-
-// One block per request.  Candidate (i, j) = child j of frontier slot i,
-// score c = score_i + logp_ij (one fp32 add), index i*K + j.  The best
-// |F_d| by (c desc, index asc) become the new frontier in rank order
-// ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
-// Mechanism: score by accumulated path probability, keep the top W;
-// "Accelerating Language Models with Diffusion Draft Trees", Summary: global
-// top-W child prefixes, states carried forward).
-__global__ void __launch_bounds__(kSelectThreads) k_select(const SelectParams p) {
-  extern __shared__ uint64_t keys[];
-  const int r = blockIdx.x;
-  const int n = p.F * p.K;
-  const int np2 = pow2_at_least(n);
-  for (int e = threadIdx.x; e < np2; e += blockDim.x) {
-    uint64_t k = 0ull;
-    if (e < n) {
-      const int i = e / p.K;
-      const int row = r * p.F + i;
-      const float c = __fadd_rn(p.score_in[row], p.row_logp[static_cast<size_t>(row) * p.K + (e % p.K)]);
-      k = make_key(c, static_cast<uint32_t>(e));
-    }
-    keys[e] = k;
+  size_t smem = 0;
+  if (p.select) {
+    int np2 = 1;
+    while (np2 < p.F * p.K) np2 <<= 1;
+    smem = static_cast<size_t>(np2) * 8;
   }
-  __syncthreads();
-  block_sort_desc(keys, np2);
-  int32_t* slot_of = reinterpret_cast<int32_t*>(keys + np2);  // [Fd] parent slot
-  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) {
-    const uint64_t k = keys[q];
-    const int idx = static_cast<int>(key_index(k));
-    const int i = idx / p.K, j = idx % p.K;
-    const int row = r * p.F + i;
-    const float c = key_value(k);
-    const int32_t tok = p.row_tok[static_cast<size_t>(row) * p.K + j];
-    const size_t pi = static_cast<size_t>(r) * p.pool_stride + p.off + q;
-    p.pool_parent[pi] = (p.depth == 1) ? -1 : p.off_prev + i;
-    p.pool_token[pi] = tok;
-    p.pool_depth[pi] = p.depth;
-    p.pool_score[pi] = c;
-    const int m = r * p.Fd + q;
-    p.score_out[m] = c;
-    p.tok_next[m] = tok;
-    slot_of[q] = row;
-  }
-  __syncthreads();
-  if (p.S_next_in != nullptr) {
-    // gather the parents' states for the next state step (16-byte words)
-    const int words = p.H * p.elem_bytes / 16;
-    const uint4* src = reinterpret_cast<const uint4*>(p.S_cur);
-    uint4* dst = reinterpret_cast<uint4*>(p.S_next_in);
-    for (int e = threadIdx.x; e < p.Fd * words; e += blockDim.x) {
-      const int q = e / words, w = e % words;
-      dst[static_cast<size_t>(r * p.Fd + q) * words + w] =
-          src[static_cast<size_t>(slot_of[q]) * words + w];
-    }
-  }
-}
-
-cudaError_t launch_select(const SelectParams& p, cudaStream_t st) {
-  int np2 = 1;
-  while (np2 < p.F * p.K) np2 <<= 1;
-  const size_t smem = static_cast<size_t>(np2) * 8 + static_cast<size_t>(p.Fd) * 4;
-  k_select<<<p.R, kSelectThreads, smem, st>>>(p);
+  k_merge_rows<<<p.M, kMergeThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -320,10 +308,9 @@ cudaError_t launch_root(const RootParams& p, cudaStream_t st) {
 }
 
 cudaError_t init_select_attrs() {
-  const int smem = 227 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_max_dynamic_smem(k_merge_rows);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_prune, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return set_max_dynamic_smem(k_prune);
 }
 
 }  // namespace dt

@@ -150,7 +150,7 @@ class DARTree:
         h = ctypes.c_void_p()
         s = lib.dartree_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if s != 0:
-            raise DartreeError(s, "dartree_create failed")
+            raise DartreeError(s, "dartree_create: " + lib.dartree_last_error(None).decode())
         self._h = h
         self._lib = lib
 
