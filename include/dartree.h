@@ -137,7 +137,8 @@ dartree_status dartree_sync_status(dartree_ctx *ctx, void *stream);
 int64_t dartree_head_calls(const dartree_ctx *ctx);
 
 /* Text of the last error recorded by this context ("" if none); with a NULL
- * context, why the last dartree_create on this thread failed. */
+ * context, why the last failed context-free call on this thread
+ * (dartree_create or dartree_state_step_noalloc) failed. */
 const char *dartree_last_error(const dartree_ctx *ctx);
 
 /* Per-kernel timing.  When enabled, every launch of a build is bracketed by
@@ -189,6 +190,30 @@ dartree_status dartree_prune(dartree_ctx *ctx, const int32_t *pool_parent,
                              const int32_t *pool_token, const int32_t *pool_depth,
                              const float *pool_score, int32_t R, int32_t P, int32_t B, float beta,
                              const dartree_tree *out, void *stream);
+
+/* Head state step that allocates no device memory, for callers that cannot
+ * create a context: code whose device heap belongs to someone else (an
+ * inference server or framework whose caching allocator has reserved the
+ * GPU's memory, a plugin that may only use the buffers it is handed) and
+ * latency-critical paths that cannot pay for cudaMalloc/cudaFree, which
+ * synchronise the device.  The paper has no counterpart; this is a library
+ * convenience.
+ *   Computes S_out[m] = bf16(tanh(A S_par[m] + E[tok[m]])) for m < M, like
+ *   dartree_state_step, with bf16 weights: S_par, S_out [M, H] bf16 bits,
+ *   tok [M] int32 in [0, V), A [H, H], E [V, H] bf16 bits (A 16-byte
+ *   aligned).  Device pointers; asynchronous on `stream`.
+ *   Limits: M <= 256, H <= 4096 and H % 64 == 0; larger sizes return
+ *   DARTREE_ERR_UNSUPPORTED (reason in dartree_last_error(NULL)) and launch
+ *   nothing.
+ *   Scratch: about 12 MiB of statically allocated device memory, held by
+ *   every GPU that loads the library until the process exits.  The first
+ *   call on a device sets that device up (symbol lookup, a small synchronous
+ *   copy): make it before any stream capture.  All calls share the scratch,
+ *   so calls that overlap on the GPU race; order them on one stream.  Each
+ *   call clears the scratch it needs zeroed. */
+dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok, const void *A,
+                                          const void *E, int32_t H, int32_t M, void *S_out,
+                                          void *stream);
 
 #ifdef __cplusplus
 }

@@ -435,6 +435,8 @@ void free_all(dartree_ctx* c) {
 
 }  // namespace
 
+void dt::set_context_free_error(const std::string& why) { g_create_error = why; }
+
 extern "C" {
 
 int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K) {

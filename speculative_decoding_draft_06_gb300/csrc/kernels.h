@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <string>
+
 namespace dt {
 
 // Batched head contraction (tensor-core bf16 path and SIMT fp32 path).
@@ -139,6 +141,10 @@ struct RootParams {
   float* score;
 };
 cudaError_t launch_root(const RootParams& p, cudaStream_t st);
+
+// Records why the last context-free call on this thread failed; read back
+// through dartree_last_error(NULL).
+void set_context_free_error(const std::string& why);
 
 // One-time kernel attribute setup (dynamic shared memory opt-in).
 cudaError_t init_select_attrs();

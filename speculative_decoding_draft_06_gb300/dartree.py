@@ -90,6 +90,7 @@ def load():
         "dartree_get_timing": (st, [_vp, _i32, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_int64)]),
         "dartree_reset_timing": (st, [_vp]),
+        "dartree_state_step_noalloc": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -313,6 +314,24 @@ class DARTree:
                                             _ptr(score), R, P, B, ctypes.c_float(beta),
                                             ctypes.byref(t), _stream(stream)))
         return out
+
+
+def state_step_noalloc(S_par, tok, A, E, stream=None):
+    """Context-free bf16 state step (dartree_state_step_noalloc): for callers
+    that cannot allocate device memory.  The output tensor is allocated here
+    by PyTorch only because this is the Python convenience wrapper; the C
+    entry point itself allocates nothing.  Raises DartreeError on failure."""
+    lib = load()
+    for n, t in (("S_par", S_par), ("A", A), ("E", E)):
+        _dev(t, n, _W16)
+    _dev(tok, "tok", (torch.int32,))
+    M, H = S_par.shape
+    out = torch.empty_like(S_par)
+    s = lib.dartree_state_step_noalloc(_ptr(S_par), _ptr(tok), _ptr(A), _ptr(E), H, M, _ptr(out),
+                                       _stream(stream))
+    if s != 0:
+        raise DartreeError(s, lib.dartree_last_error(None).decode())
+    return out
 
 
 def weights_to_device(inp: dict, bf16: bool, device="cuda") -> dict:
