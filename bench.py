@@ -45,6 +45,11 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-head", type=int, default=0, metavar="N",
+                    help="profiling aid: run N head calls (fused logits + log-softmax + "
+                         "top-K) of the workload's widest depth and exit")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="override V (profiling aid for small ncu captures)")
     return ap.parse_args(argv)
 
 
@@ -366,8 +371,40 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
+def run_profile_head(args) -> None:
+    """N head calls on one stream, for ncu captures of k_head_tc on a case
+    that still streams its weights from HBM but holds only a few GB."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_draft_06_gb300 import dartree as dtl
+    torch.cuda.set_device(0)
+    w = I.CONFIGS[args.config]
+    if args.vocab:
+        w = w.replace(V=args.vocab)
+    M = max(w.head_rows())
+    inp = I.make_inputs(w.replace(D=1))
+    dev = dtl.weights_to_device(inp, w.bf16)
+    g = np.random.default_rng(1)
+    S = np.tanh(g.standard_normal((M, w.H))).astype(np.float32)
+    S = torch.from_numpy(I.to_bf16_bits(S)).view(torch.int16).cuda() if w.bf16 else \
+        torch.from_numpy(S).cuda()
+    ctx = dtl.DARTree(w.V, w.H, max_D=1, max_W=w.W, max_K=w.K, max_B=w.B, max_requests=w.R,
+                      bf16=w.bf16)
+    z = dev["z"][:, 0].contiguous()
+    for _ in range(args.profile_head):
+        ctx.head_topk(S, z, dev["Wout"], K=w.K, rows_per_req=M // w.R, z_req_stride=w.V)
+    ctx.sync()
+    print(json.dumps({"profile_head": args.profile_head, "V": w.V, "H": w.H, "M": M,
+                      "K": w.K}), flush=True)
+    ctx.close()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.profile_head:
+        run_profile_head(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

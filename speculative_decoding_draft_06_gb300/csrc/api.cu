@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -63,6 +64,8 @@ struct dartree_ctx {
   float* part = nullptr;            // split-K partial sums of the state step
   int* tile_cnt = nullptr;          // split-K arrival counters
   int state_split = 1;
+  int tc_max_stages = 0;   // tuning: pipeline depth cap of the head call (0: default)
+  int tc_ctas_per_sm = 1;  // tuning: head-call CTAs per SM
   float* pm = nullptr;
   float* ps = nullptr;
   uint64_t* ptop = nullptr;
@@ -211,7 +214,10 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   {
     KernelTimer tk(c, st, 0);
     if (c->bf16) {
-      grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
+      const int slots = c->num_sms * c->tc_ctas_per_sm;
+      grid = p.n_tiles < slots ? p.n_tiles : slots;
+      p.max_stages = c->tc_max_stages;
+      p.ctas_per_sm = c->tc_ctas_per_sm;
       e = dt::launch_head_tc(N, true, c->tm_Wout, c->tm_S[sbuf][pad_index(N)], p, grid, st);
     } else {
       grid = p.n_tiles < c->max_cta ? p.n_tiles : c->max_cta;
@@ -483,6 +489,12 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   }
   c->num_sms = prop.multiProcessorCount;
   c->max_cta = 2 * c->num_sms;
+  // tuning knobs of the head-call pipeline (defaults when unset)
+  if (const char* v = getenv("DARTREE_TC_MAX_STAGES")) c->tc_max_stages = atoi(v);
+  if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
+    const int n = atoi(v);
+    c->tc_ctas_per_sm = n == 2 ? 2 : 1;
+  }
   c->pool_cap = dartree_pool_size(g.max_D, g.max_W, g.max_K);
 
   cudaDriverEntryPointQueryResult q;

@@ -31,6 +31,8 @@
 
 namespace dt {
 
+constexpr int kDefaultMaxStages = 8;
+
 template <int N>
 struct TcLayout {
   static constexpr int kABytes = kTileV * kTileH * 2;  // 16 KB
@@ -148,6 +150,18 @@ __global__ void __launch_bounds__(192, 1)
     kb_begin = split * nk_all / p.n_split;
     kb_end = (split + 1) * nk_all / p.n_split;
   }
+  // The contraction of each tile starts at a tile-dependent k-block and
+  // wraps around.  Tiles are 128 consecutive weight rows, so at a common
+  // k-block every CTA would read 128-byte pieces at the same offset of
+  // power-of-two-strided rows -- the same low address bits everywhere, which
+  // concentrates the stream on a few DRAM channels.  Rotating the start
+  // spreads concurrent CTAs over different offsets.
+  const int kb_span = kb_end - kb_begin;
+  auto kb_at = [&](int t, int i) {
+    int j = i + (t * 5) % kb_span;
+    if (j >= kb_span) j -= kb_span;
+    return kb_begin + j;
+  };
 
   if (warp == 5) tmem_alloc<L::kTmemCols>(tmem_slot);
   if (threadIdx.x == 0) {
@@ -183,7 +197,8 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       long long issued = 0;
       for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
+        for (int i = 0; i < kb_span; ++i) {
+          const int kb = kb_at(t, i);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err)) {
             *abort_flag = 1;
             break;
@@ -224,7 +239,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * N);
         bool ok = true;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
+        for (int i = 0; i < kb_span; ++i) {
           if (!mbar_wait(&full[stage], phase, p.err)) {
             *abort_flag = 1;
             ok = false;
@@ -237,7 +252,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < kTileH / 16; ++k) {
             tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
-                        idesc, (kb != kb_begin || k != 0) ? 1u : 0u);
+                        idesc, (i != 0 || k != 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == S) {
@@ -327,9 +342,13 @@ static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, con
   using L = TcLayout<N>;
   size_t fixed = 1024 + static_cast<size_t>(kLogits ? kEpiWarps * N * p.K : 0) * 8 +
                  static_cast<size_t>(kEpiWarps) * N * sizeof(float2) + 64 * 8 + 64;
-  const size_t budget = 227 * 1024;
+  // per-SM shared memory is 228 KB, 1 KB of it reserved per resident CTA
+  const int cps = p.ctas_per_sm > 1 ? p.ctas_per_sm : 1;
+  const size_t budget = cps == 1 ? 227 * 1024 : 228 * 1024 / cps - 1024;
+  if (budget <= fixed) return cudaErrorInvalidConfiguration;
   int stages = static_cast<int>((budget - fixed) / L::kStageBytes);
-  if (stages > 8) stages = 8;
+  const int cap = p.max_stages > 0 ? p.max_stages : kDefaultMaxStages;
+  if (stages > cap) stages = cap;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   TcParams q = p;
   q.stages = stages;

@@ -15,6 +15,8 @@ struct TcParams {
   int M;               // valid head rows (GEMM columns)
   int n_tiles;         // ceil(rows / 128)
   int stages;          // pipeline depth (set by the launcher)
+  int max_stages;      // launcher cap on the pipeline depth (0: default)
+  int ctas_per_sm;     // CTAs sharing one SM's shared memory (0: 1)
   int* err;            // device error word
   // logits epilogue
   const float* z;      // base logits of this depth, request 0
