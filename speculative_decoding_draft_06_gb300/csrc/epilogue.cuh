@@ -2,17 +2,22 @@
 // column) an online log-sum-exp over the vocabulary and a running top-K by
 // (logit desc, token asc).  The [rows, V] logit matrix never leaves the SM.
 //
-// Layout: each of the 4 epilogue warps sees 32 vocabulary entries of every
-// 128-entry tile (one per lane) for all head rows.  A warp keeps, per head
-// row, a private sorted list of its K best 64-bit keys in shared memory;
-// the CTA writes those lists and one (max, sum-exp) pair per row as
+// Each tile holds 128 vocabulary entries x N head rows.  The producer side
+// hands over 16 rows at a time, one vocabulary entry per thread (the
+// tensor-memory lane layout).  The chunk is transposed through shared memory
+// so that a warp owns whole head rows: row j of a chunk belongs to warp j % 4,
+// which reads its 128 values, 4 per lane.  Because one warp owns a row for
+// the whole kernel, the row has a single top-K list per CTA (shared memory,
+// sorted, best first) and needs no cross-warp synchronisation:
+//   * a value enters only if its key beats the list's K-th key; one or two
+//     entrants are inserted one at a time, more are warp-sorted and merged
+//     with the list by a bitonic merge;
+//   * softmax state: for <= 64 rows each lane keeps a running (max, sum) per
+//     owned row in registers and lanes are combined once at the end; for more
+//     rows each chunk is reduced across the warp and folded into a per-row
+//     running pair in shared memory.
+// The CTA then writes one (max, sum-exp) pair and one sorted list per row as
 // partials, which a second kernel merges across CTAs.
-//
-// Softmax state: for <= 32 head rows every lane keeps a running (max, sum)
-// per row in registers (columns unrolled at compile time) and lanes are
-// combined once at the end; for more rows each 16-column chunk is reduced
-// across the warp and the row's owner lane folds it into a per-warp running
-// pair kept in shared memory.
 #pragma once
 #include <cstdint>
 
@@ -82,139 +87,196 @@ static __device__ __noinline__ void list_insert_lanes(uint64_t* L, int K, uint64
   }
 }
 
-// First tile: the list of each row is the sorted best K of the 32 lanes.
-static __device__ __noinline__ void list_fill(uint64_t* L, int K, uint64_t key) {
-  const uint64_t s = warp_sort_desc(key);
-  if ((threadIdx.x & 31) < K) L[threadIdx.x & 31] = s;
+// Fold the candidate keys of the lanes (0 = no candidate) into the sorted
+// list L: warp-sort the candidates, keep their best p2, and bitonic-merge
+// with the list.  Warp-collective.
+static __device__ __noinline__ void list_merge_batch(uint64_t* L, int K, uint64_t key) {
+  const int lane = threadIdx.x & 31;
+  const int p2 = pow2_ceil32(K);
+  const uint64_t srt = warp_sort_desc(key);
+  uint64_t v = lane < K ? L[lane] : 0ull;
+  uint64_t y = 0ull;
+  if (p2 == 32) {
+    y = shfl_u64(srt, 31 - lane);
+  } else {
+    const int src = 2 * p2 - 1 - lane;
+    const uint64_t b = shfl_u64(srt, src < 0 ? 0 : src);
+    v = lane < p2 ? v : (lane < 2 * p2 ? b : 0ull);
+  }
+  v = warp_merge_desc(v, y, p2);
   __syncwarp();
+  if (lane < K) L[lane] = v;
+  __syncwarp();
+}
+
+// Shared-memory footprint of the epilogue (bytes) for N rows and top-K.
+__host__ __device__ constexpr size_t epi_smem_bytes(int N, int K) {
+  return static_cast<size_t>(N) * K * 8            // lists
+         + 2 * 16 * 132 * 4                         // transposed chunk, 2 buffers
+         + static_cast<size_t>(N) * 8;              // running (max, sum) per row
 }
 
 template <int N>
 struct LogitsEpilogue {
-  static constexpr bool kLaneLocal = N <= 32;
-  float lm[kLaneLocal ? N : 1], ls[kLaneLocal ? N : 1];
-  uint64_t* lists;  // this warp's lists, [N][K]
-  float2* run;      // this warp's running (max, sum) per row (shared, N > 32)
-  int K, M, lane;
-  bool first;
+  static constexpr bool kLaneLocal = N <= 64;
+  static constexpr int kSlots = kLaneLocal ? N / 4 : 1;  // rows owned per warp
+  static constexpr int kTPitch = 132;                    // floats per transposed row
+  float lm[kSlots], ls[kSlots];
+  uint64_t* lists;  // [N][K], one sorted list per row
+  float* T;         // [2][16][kTPitch]
+  float2* run;      // [N] (N > 64)
+  int K, M, lane, warp, t;
+  int nchunk;       // chunks handed over so far (selects the T buffer)
   bool bad;
 
-  __device__ __forceinline__ void init(uint64_t* warp_lists, float2* warp_run, int K_, int M_) {
-    lists = warp_lists;
-    run = warp_run;
+  __device__ __forceinline__ void init(uint8_t* smem, int K_, int M_) {
+    lists = reinterpret_cast<uint64_t*>(smem);
+    T = reinterpret_cast<float*>(lists + static_cast<size_t>(N) * K_);
+    run = reinterpret_cast<float2*>(T + 2 * 16 * kTPitch);
     K = K_;
     M = M_;
+    t = threadIdx.x & 127;
     lane = threadIdx.x & 31;
-    first = true;
+    warp = t >> 5;
+    nchunk = 0;
     bad = false;
 #pragma unroll
-    for (int c = 0; c < (kLaneLocal ? N : 1); ++c) {
-      lm[c] = -INFINITY;
-      ls[c] = 0.f;
+    for (int i = 0; i < kSlots; ++i) {
+      lm[i] = -INFINITY;
+      ls[i] = 0.f;
     }
-    for (int i = lane; i < N * K_; i += 32) lists[i] = 0ull;
-    for (int c = lane; c < N; c += 32) run[c] = make_float2(-INFINITY, 0.f);
-    __syncwarp();
+    for (int i = t; i < N * K_; i += 128) lists[i] = 0ull;
+    for (int c = t; c < N; c += 128) run[c] = make_float2(-INFINITY, 0.f);
+    asm volatile("bar.sync 1, 128;" ::: "memory");
   }
 
-  __device__ __forceinline__ void topk(int c, float xv, bool valid_v, uint32_t v) {
-    const uint64_t key = (valid_v && xv == xv) ? make_key(xv, v) : 0ull;
-    uint64_t* L = lists + c * K;
-    if (first) {
-      list_fill(L, K, key);
-    } else {
-      const unsigned bal = __ballot_sync(kFull, key > L[K - 1]);
-      if (bal) list_insert_lanes(L, K, key, bal);
-    }
-  }
-
-  // <= 32 rows: columns C0..C0+15 with compile-time indices.
-  template <int C0>
-  __device__ __forceinline__ void consume_static(const float (&x)[16], bool valid_v, uint32_t v) {
+  // Stage x (rows c0..c0+15 of this thread's vocabulary entry) transposed.
+  __device__ __forceinline__ float* stage(const float (&x)[16]) {
+    float* Tb = T + (nchunk & 1) * 16 * kTPitch;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (C0 + j >= M) break;  // uniform across the warp
-      const float xv = x[j];
-      if (valid_v && (xv != xv || xv == INFINITY)) bad = true;
-      if (valid_v && xv > -INFINITY && xv < INFINITY) {
-        const float d = xv - lm[C0 + j];
+    for (int j = 0; j < 16; ++j) Tb[j * kTPitch + t] = x[j];
+    ++nchunk;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    return Tb;
+  }
+
+  // Top-K update of row c with this lane's 4 values (vocabulary v0 + lane + 32 i).
+  __device__ __forceinline__ void topk4(int c, const float (&xv)[4], uint32_t v0, int V) {
+    uint64_t* L = lists + static_cast<size_t>(c) * K;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t v = v0 + lane + 32 * i;
+      const bool valid = static_cast<int>(v) < V;
+      const uint64_t key = (valid && xv[i] == xv[i]) ? make_key(xv[i], v) : 0ull;
+      const uint64_t th = L[K - 1];
+      const unsigned bal = __ballot_sync(kFull, key > th);
+      if (bal == 0u) continue;
+      if (__popc(bal) <= 2)
+        list_insert_lanes(L, K, key, bal);
+      else
+        list_merge_batch(L, K, key > th ? key : 0ull);
+    }
+  }
+
+  __device__ __forceinline__ void load4(const float* Tb, int j, uint32_t v0, int V, float (&xv)[4],
+                                        bool (&fin)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xv[i] = Tb[j * kTPitch + lane + 32 * i];
+      const bool valid = static_cast<int>(v0 + lane + 32 * i) < V;
+      if (valid && (xv[i] != xv[i] || xv[i] == INFINITY)) bad = true;
+      fin[i] = valid && xv[i] > -INFINITY && xv[i] < INFINITY;
+    }
+  }
+
+  // <= 64 rows: chunk CH (rows 16 CH .. 16 CH + 15) with compile-time slots.
+  template <int CH>
+  __device__ __forceinline__ void chunk_static(const float (&x)[16], uint32_t v0, int V) {
+    const float* Tb = stage(x);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = warp + 4 * jj;
+      const int c = CH * 16 + j;
+      if (c >= M) continue;  // uniform across the warp
+      float xv[4];
+      bool fin[4];
+      load4(Tb, j, v0, V, xv, fin);
+      constexpr int kBase = CH * 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (!fin[i]) continue;
+        const float d = xv[i] - lm[kBase + jj];
         const float e = fast_exp(-fabsf(d));
         const bool up = d > 0.f;
-        ls[C0 + j] = up ? fmaf(ls[C0 + j], e, 1.f) : ls[C0 + j] + e;
-        lm[C0 + j] = up ? xv : lm[C0 + j];
+        ls[kBase + jj] = up ? fmaf(ls[kBase + jj], e, 1.f) : ls[kBase + jj] + e;
+        lm[kBase + jj] = up ? xv[i] : lm[kBase + jj];
       }
-      topk(C0 + j, xv, valid_v, v);
+      topk4(c, xv, v0, V);
     }
   }
 
-  // > 32 rows: columns c0..c0+15 (c0 a runtime multiple of 16).
-  __device__ __forceinline__ void consume_dyn(const float (&x)[16], int c0, bool valid_v,
-                                              uint32_t v) {
+  // > 64 rows: chunk starting at row c0 (runtime).
+  __device__ __forceinline__ void chunk_dyn(const float (&x)[16], int c0, uint32_t v0, int V) {
+    const float* Tb = stage(x);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = warp + 4 * jj;
       const int c = c0 + j;
-      if (c >= M) break;
-      const float xv = x[j];
-      if (valid_v && (xv != xv || xv == INFINITY)) bad = true;
-      const bool fin = valid_v && xv > -INFINITY && xv < INFINITY;
-      const float xm = fin ? xv : -INFINITY;
-      const float mx = warp_max_f(xm);
+      if (c >= M) continue;
+      float xv[4];
+      bool fin[4];
+      load4(Tb, j, v0, V, xv, fin);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx = fin[i] ? fmaxf(mx, xv[i]) : mx;
+      mx = warp_max_f(mx);
       if (mx != -INFINITY) {
-        const float se = warp_sum_f(fin ? fast_exp(xm - mx) : 0.f);
-        if (lane == (c & 31)) {
+        float se = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) se += fin[i] ? fast_exp(xv[i] - mx) : 0.f;
+        se = warp_sum_f(se);
+        if (lane == 0) {
           float2 r = run[c];
           lse_merge(r.x, r.y, mx, se);
           run[c] = r;
         }
       }
-      topk(c, xv, valid_v, v);
+      topk4(c, xv, v0, V);
     }
   }
 
-  __device__ __forceinline__ void tile_done() { first = false; }
-
-  // Write this CTA's partials.  red = [4][N] float2 (all warps' running
-  // pairs); all 128 epilogue threads must call it.
-  __device__ __forceinline__ void finish(float2* red, int warp, int cta, float* pm, float* ps,
-                                         int cta_stride, uint64_t* ptop, int list_stride,
-                                         int* err) {
+  // Write this CTA's partials: one (max, sum-exp) pair and one list per row,
+  // each by the row's owner warp.
+  __device__ __forceinline__ void finish(int cta, float* pm, float* ps, int cta_stride,
+                                         uint64_t* ptop, int list_stride, int* err) {
+    __syncwarp();
     if constexpr (kLaneLocal) {
 #pragma unroll
-      for (int c = 0; c < N; ++c) {
-        if (c >= M) break;
-        float m = lm[c], s = ls[c];
+      for (int s = 0; s < kSlots; ++s) {
+        const int c = (s / 4) * 16 + warp + 4 * (s % 4);
+        float m = lm[s], sm = ls[s];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           const float m2 = __shfl_xor_sync(kFull, m, o);
-          const float s2 = __shfl_xor_sync(kFull, s, o);
-          lse_merge(m, s, m2, s2);
+          const float s2 = __shfl_xor_sync(kFull, sm, o);
+          lse_merge(m, sm, m2, s2);
         }
-        if (lane == 0) red[warp * N + c] = make_float2(m, s);
+        if (lane == 0 && c < M) {
+          pm[(size_t)c * cta_stride + cta] = m;
+          ps[(size_t)c * cta_stride + cta] = sm;
+        }
+      }
+    } else {
+      for (int c = warp; c < M; c += kEpiWarps) {
+        // rows owned by this warp: c % 16 in {warp, warp + 4, ...} -> c % 4 == warp
+        if (lane == 0) {
+          pm[(size_t)c * cta_stride + cta] = run[c].x;
+          ps[(size_t)c * cta_stride + cta] = run[c].y;
+        }
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const int t = warp * 32 + lane;
-    for (int c = t; c < M; c += 128) {
-      float m = red[c].x, s = red[c].y;
-#pragma unroll
-      for (int w = 1; w < kEpiWarps; ++w) lse_merge(m, s, red[w * N + c].x, red[w * N + c].y);
-      pm[(size_t)c * cta_stride + cta] = m;
-      ps[(size_t)c * cta_stride + cta] = s;
-    }
-    // one list per CTA and row: warp (c % 4) folds the four warps' lists
-    // (this warp's lists start at `lists`; the CTA's are [warp][N][K])
-    uint64_t* all = lists - static_cast<size_t>(warp) * N * K;
-    const int p2 = pow2_ceil32(K);
     for (int c = warp; c < M; c += kEpiWarps) {
-      const uint64_t* L0 = all + static_cast<size_t>(c) * K;
-      uint64_t v = lane < K ? L0[lane] : 0ull;
-#pragma unroll
-      for (int w = 1; w < kEpiWarps; ++w) {
-        uint64_t y;
-        merge_operands(all + (static_cast<size_t>(w) * N + c) * K, K, p2, v, y);
-        v = warp_merge_desc(v, y, p2);
-      }
-      if (lane < K) ptop[((size_t)c * list_stride + cta) * K + lane] = v;
+      if (lane < K) ptop[((size_t)c * list_stride + cta) * K + lane] = lists[(size_t)c * K + lane];
     }
     if (bad) atomicOr(err, DT_ERR_NONFINITE);
   }

@@ -26,19 +26,15 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   float* sW = reinterpret_cast<float*>(smem_raw);            // [128][33]
   float* sS = sW + kTileV * (kSimtH + 1);                    // [16][32]
-  uint64_t* lists = reinterpret_cast<uint64_t*>(sS + 16 * kSimtH);
-  const int list_words = kLogits ? kEpiWarps * N * p.K : 0;
-  float2* red = reinterpret_cast<float2*>(lists + list_words);
+  uint8_t* tail = reinterpret_cast<uint8_t*>(sS + 16 * kSimtH);  // epilogue or U rows
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
   const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
   const int t_end =
       static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
 
   LogitsEpilogue<N> epi;
-  if (kLogits) epi.init(lists + warp * N * p.K, red + warp * N, p.K, p.M);
+  if (kLogits) epi.init(tail, p.K, p.M);
   const int mcols = p.M < N ? p.M : N;  // columns that carry data
 
   for (int t = t_begin; t < t_end; ++t) {
@@ -91,14 +87,15 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
       }
     };
     if constexpr (kLogits) {
-      if constexpr (N <= 32) {
+      const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
+      if constexpr (N <= 64) {
         static_for<0, N / 16>([&](auto i) {
-          constexpr int C0 = decltype(i)::value * 16;
-          if (C0 < mcols) {
+          constexpr int CH = decltype(i)::value;
+          if (CH * 16 < mcols) {
             float acc[16];
-            dot16(acc, C0);
-            add_z(acc, C0);
-            epi.template consume_static<C0>(acc, valid, static_cast<uint32_t>(row));
+            dot16(acc, CH * 16);
+            add_z(acc, CH * 16);
+            epi.template chunk_static<CH>(acc, v0, p.rows);
           }
         });
       } else {
@@ -106,13 +103,13 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
           float acc[16];
           dot16(acc, c0);
           add_z(acc, c0);
-          epi.consume_dyn(acc, c0, valid, static_cast<uint32_t>(row));
+          epi.chunk_dyn(acc, c0, v0, p.rows);
         }
       }
     } else {
       // U = A S_in for the M input rows (kept per thread in shared memory),
       // then output row q takes U[:, slot[q]]
-      float* Us = reinterpret_cast<float*>(red + kEpiWarps * N) + tid * (N + 1);
+      float* Us = reinterpret_cast<float*>(tail) + tid * (N + 1);
       for (int c0 = 0; c0 < mcols; c0 += 16) {
         float acc[16];
         dot16(acc, c0);
@@ -132,19 +129,17 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
         }
       }
     }
-    if constexpr (kLogits) epi.tile_done();
   }
   if constexpr (kLogits) {
-    epi.finish(red, warp, blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
+    epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
   }
 }
 
 template <int N, bool kLogits>
 static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(kTileV) * (kSimtH + 1) * 4 + 16 * kSimtH * 4 +
-                      static_cast<size_t>(kLogits ? kEpiWarps * N * p.K : 0) * 8 +
-                      static_cast<size_t>(kEpiWarps) * N * sizeof(float2) +
-                      (kLogits ? 0 : static_cast<size_t>(kTileV) * (N + 1) * 4);
+                      (kLogits ? epi_smem_bytes(N, p.K)
+                               : static_cast<size_t>(kTileV) * (N + 1) * 4);
   k_head_simt<N, kLogits><<<grid, 128, smem, st>>>(p);
   return cudaGetLastError();
 }

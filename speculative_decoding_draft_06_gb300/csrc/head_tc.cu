@@ -120,10 +120,9 @@ __global__ void __launch_bounds__(192, 1)
   const int S = p.stages;
   uint8_t* stage_base = smem;
   uint8_t* after = smem + static_cast<size_t>(S) * L::kStageBytes;
-  uint64_t* lists = reinterpret_cast<uint64_t*>(after);
-  const int list_words = kLogits ? kEpiWarps * N * p.K : 0;
-  float2* red = reinterpret_cast<float2*>(lists + list_words);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + kEpiWarps * N);
+  uint8_t* epi_smem = after;  // logits epilogue: lists, transposed chunks, row state
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(after + (kLogits ? epi_smem_bytes(N, p.K) : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -182,7 +181,8 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tmap_s);
   }
   LogitsEpilogue<N> epi;
-  if (kLogits && warp < kEpiWarps) epi.init(lists + warp * N * p.K, red + warp * N, p.K, p.M);
+  if (kLogits && warp < kEpiWarps) epi.init(epi_smem, p.K, p.M);
+  __shared__ int epi_go;  // per-tile decision shared by the 4 epilogue warps
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -269,15 +269,21 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue
+    // The four warps synchronise with named barriers, so they must take every
+    // decision together: one thread waits for the accumulator and broadcasts
+    // whether to go on (a timed-out wait ends all four warps' loops at once).
     int it = 0;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = it & 1;
-      if (*abort_flag) break;
-      if (!mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err)) {
-        *abort_flag = 1;
-        break;
+      if (threadIdx.x == 0) {
+        const bool ok = !*abort_flag &&
+                        mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err);
+        if (!ok) *abort_flag = 1;
+        epi_go = ok;
       }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!epi_go) break;
       tc_fence_after();
       const int row = t * kTileV + warp * 32 + lane;  // vocabulary (or hidden) index
       const bool valid = row < p.rows;
@@ -298,13 +304,16 @@ __global__ void __launch_bounds__(192, 1)
             x[j] += zv;
           }
         };
-        if constexpr (N <= 32) {
+        const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
+        if constexpr (N <= 64) {
           static_for<0, N / 16>([&](auto i) {
-            constexpr int C0 = decltype(i)::value * 16;
-            float x[16];
-            tmem_ld16(tbase + C0, x);
-            add_z(x, C0);
-            epi.template consume_static<C0>(x, valid, static_cast<uint32_t>(row));
+            constexpr int CH = decltype(i)::value;
+            if (CH * 16 < p.M) {  // same for all four warps
+              float x[16];
+              tmem_ld16(tbase + CH * 16, x);
+              add_z(x, CH * 16);
+              epi.template chunk_static<CH>(x, v0, p.rows);
+            }
           });
         } else {
           const int c_end = (p.M + 15) & ~15;
@@ -312,10 +321,9 @@ __global__ void __launch_bounds__(192, 1)
             float x[16];
             tmem_ld16(tbase + c0, x);
             add_z(x, c0);
-            epi.consume_dyn(x, c0, valid, static_cast<uint32_t>(row));
+            epi.chunk_dyn(x, c0, v0, p.rows);
           }
         }
-        epi.tile_done();
       } else {
         state_epilogue<N>(p, tbase, t, split, warp, lane, row, valid);
       }
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(&tempty[a]);
     }
     if constexpr (kLogits) {
-      epi.finish(red, warp, blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
+      epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
     }
   }
 
@@ -340,13 +348,17 @@ template <int N, bool kLogits>
 static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p,
                                int grid, cudaStream_t st) {
   using L = TcLayout<N>;
-  size_t fixed = 1024 + static_cast<size_t>(kLogits ? kEpiWarps * N * p.K : 0) * 8 +
-                 static_cast<size_t>(kEpiWarps) * N * sizeof(float2) + 64 * 8 + 64;
-  // per-SM shared memory is 228 KB, 1 KB of it reserved per resident CTA
-  const int cps = p.ctas_per_sm > 1 ? p.ctas_per_sm : 1;
-  const size_t budget = cps == 1 ? 227 * 1024 : 228 * 1024 / cps - 1024;
-  if (budget <= fixed) return cudaErrorInvalidConfiguration;
-  int stages = static_cast<int>((budget - fixed) / L::kStageBytes);
+  size_t fixed = 1024 + (kLogits ? epi_smem_bytes(N, p.K) : 0) + 64 * 8 + 64;
+  // per-SM shared memory is 228 KB, 1 KB of it reserved per resident CTA,
+  // less the kernel's own static shared memory (at most 2 KB)
+  auto stages_for = [&](int cps) -> int {
+    const size_t budget = (cps == 1 ? 227 * 1024 : 228 * 1024 / cps - 1024) - 2048;
+    return budget > fixed ? static_cast<int>((budget - fixed) / L::kStageBytes) : 0;
+  };
+  // two CTAs per SM only where both fit with a real pipeline, else one
+  int cps = p.ctas_per_sm > 1 ? p.ctas_per_sm : 1;
+  if (cps > 1 && stages_for(cps) < 3) cps = 1;
+  int stages = stages_for(cps);
   const int cap = p.max_stages > 0 ? p.max_stages : kDefaultMaxStages;
   if (stages > cap) stages = cap;
   if (stages < 2) return cudaErrorInvalidConfiguration;
