@@ -115,7 +115,13 @@ void dartree_destroy(dartree_ctx *ctx);
  *   Requires 1 <= D, W, K, B, R within the context's limits, K <= V,
  *   beta <= 0 (Lemma 1 needs a non-positive depth bonus).
  * Runs D batched head calls (dartree_head_calls() reports them), then the
- * deferred Top-B and the mask; writes `out`.  Asynchronous; never allocates. */
+ * deferred Top-B and the mask; writes `out`.  Asynchronous; never allocates
+ * device memory.  On a created stream (not the legacy NULL stream, not one
+ * being captured by the caller) the launches of a build are captured once
+ * into a CUDA graph; a later call with the same arguments (sizes, pointers,
+ * stream) replays it, reading the buffers' current contents.  Set
+ * DARTREE_GRAPH=0 to launch eagerly, DARTREE_PDL=0 to turn off programmatic
+ * dependent launch between the kernels. */
 dartree_status dartree_build(dartree_ctx *ctx, const float *base_logits, const float *state0,
                              const dartree_head *head, int32_t R, int32_t D, int32_t W, int32_t K,
                              int32_t B, float beta, const dartree_tree *out, void *stream);

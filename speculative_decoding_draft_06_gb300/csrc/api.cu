@@ -65,6 +65,21 @@ struct dartree_ctx {
   int* tile_cnt = nullptr;          // split-K arrival counters
   int state_split = 1;
   int tc_max_stages = 0;   // tuning: pipeline depth cap of the head call (0: default)
+  bool pdl = true;         // programmatic dependent launch between the kernels of a build
+  bool use_graph = true;   // capture each build shape once into a CUDA graph
+
+  // the captured build and the arguments it was captured with
+  struct GraphKey {
+    const float *z, *s0;
+    const void *A, *E, *Wout;
+    int R, D, W, K, B;
+    float beta;
+    dartree_tree out;
+    cudaStream_t st;
+    bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof o) == 0; }
+  };
+  cudaGraphExec_t gexec = nullptr;
+  GraphKey gkey{};
   int tc_ctas_per_sm = 1;  // tuning: head-call CTAs per SM
   float* pm = nullptr;
   float* ps = nullptr;
@@ -209,6 +224,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.ptop = c->ptop;
   p.cta_stride = c->max_cta;
   p.list_stride = c->max_cta;
+  p.pdl = c->pdl;
   int grid;
   cudaError_t e;
   {
@@ -242,6 +258,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   mp.row_logp = logp;
   mp.err = c->d_err;
   mp.select = sel != nullptr;
+  mp.pdl = c->pdl;
   {
     KernelTimer tk(c, st, 2);
     e = dt::launch_merge_rows(mp, st);
@@ -265,6 +282,7 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
   p.tok = tok;
   p.n_tiles = (H + dt::kTileV - 1) / dt::kTileV;
   p.err = c->d_err;
+  p.pdl = c->pdl;
   cudaError_t e;
   KernelTimer tk(c, st, 1);
   if (c->bf16) {
@@ -343,6 +361,7 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   rp.state0 = s0;
   rp.S = c->S[0];
   rp.score = c->score[0];
+  rp.pdl = c->pdl;
   cudaError_t e;
   {
     KernelTimer tk(c, st, 5);
@@ -406,6 +425,7 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   pp.mask = out->mask;
   pp.n_out = out->n_out;
   pp.err = c->d_err;
+  pp.pdl = c->pdl;
   {
     KernelTimer tk(c, st, 4);
     e = dt::launch_prune(pp, st);
@@ -420,6 +440,65 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   return DARTREE_OK;
 }
 
+// One build: replay the captured graph when the arguments match the last
+// capture, else capture the launches of run_build into a new graph (eager
+// launches on the legacy stream and while kernel timing is on).
+dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
+                              const dartree_head* head, int R, int D, int W, int K, int B,
+                              float beta, const dartree_tree* out, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (st != nullptr && cudaStreamIsCapturing(st, &cap) != cudaSuccess) cap = cudaStreamCaptureStatusNone;
+  if (!c->use_graph || c->timing || st == nullptr || cap != cudaStreamCaptureStatusNone)
+    return run_build(c, z, s0, head, R, D, W, K, B, beta, out, st);
+  dartree_ctx::GraphKey key{};
+  key.z = z;
+  key.s0 = s0;
+  key.A = head->A;
+  key.E = head->E;
+  key.Wout = head->Wout;
+  key.R = R;
+  key.D = D;
+  key.W = W;
+  key.K = K;
+  key.B = B;
+  key.beta = beta;
+  key.out = *out;
+  key.st = st;
+  if (c->gexec == nullptr || !(key == c->gkey)) {
+    if (c->gexec) {
+      cudaGraphExecDestroy(c->gexec);
+      c->gexec = nullptr;
+    }
+    cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return c->cuda_fail(e, "begin capture");
+    dartree_status s = run_build(c, z, s0, head, R, D, W, K, B, beta, out, st);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(st, &g);
+    if (s != DARTREE_OK) {
+      if (g) cudaGraphDestroy(g);
+      return s;
+    }
+    if (e != cudaSuccess) return c->cuda_fail(e, "end capture");
+    e = cudaGraphInstantiate(&c->gexec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      c->gexec = nullptr;
+      return c->cuda_fail(e, "graph instantiate");
+    }
+    c->gkey = key;
+  } else {
+    c->last_R = R;
+    c->last_D = D;
+    c->last_W = W;
+    c->last_K = K;
+    c->last_P = dartree_pool_size(D, W, K);
+    c->head_calls = D;
+  }
+  cudaError_t e = cudaGraphLaunch(c->gexec, st);
+  if (e != cudaSuccess) return c->cuda_fail(e, "graph launch");
+  return DARTREE_OK;
+}
+
 void free_events(dartree_ctx* c) {
   for (cudaEvent_t ev : c->ev_pool) cudaEventDestroy(ev);
   c->ev_pool.clear();
@@ -429,6 +508,8 @@ void free_events(dartree_ctx* c) {
 
 void free_all(dartree_ctx* c) {
   free_events(c);
+  if (c->gexec) cudaGraphExecDestroy(c->gexec);
+  c->gexec = nullptr;
   void* ptrs[] = {c->S[0],      c->S[1],       c->score[0],    c->score[1],   c->tok_next,
                   c->slot_next, c->iota,       c->counters,    c->part,       c->tile_cnt,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
@@ -491,6 +572,8 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   c->max_cta = 2 * c->num_sms;
   // tuning knobs of the head-call pipeline (defaults when unset)
   if (const char* v = getenv("DARTREE_TC_MAX_STAGES")) c->tc_max_stages = atoi(v);
+  if (const char* v = getenv("DARTREE_PDL")) c->pdl = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
     const int n = atoi(v);
     c->tc_ctas_per_sm = n == 2 ? 2 : 1;
@@ -591,8 +674,8 @@ dartree_status dartree_build(dartree_ctx* ctx, const float* base_logits, const f
   if (!ctx) return DARTREE_ERR_INVALID_ARG;
   dartree_status s = check_build_args(ctx, base_logits, state0, head, R, D, W, K, B, beta, out);
   if (s != DARTREE_OK) return s;
-  return run_build(ctx, base_logits, state0, head, R, D, W, K, B, beta, out,
-                   static_cast<cudaStream_t>(stream));
+  return build_dispatch(ctx, base_logits, state0, head, R, D, W, K, B, beta, out,
+                        static_cast<cudaStream_t>(stream));
 }
 
 dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
@@ -624,7 +707,7 @@ dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->s0_stage, s0h, sn * 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "input copy");
   dartree_tree dev{ctx->o_parent, ctx->o_token, ctx->o_depth, ctx->o_score, ctx->o_mask, ctx->o_nout};
-  s = run_build(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta, &dev, st);
+  s = build_dispatch(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta, &dev, st);
   if (s != DARTREE_OK) return s;
   const size_t nb = static_cast<size_t>(R) * B, nw = nb * ((B + 31) / 32);
   struct {

@@ -122,6 +122,34 @@ __device__ __forceinline__ void merge_operands(const uint64_t* L, int K, int p2,
   }
 }
 
+// Programmatic dependent launch.  A kernel launched with it may start while
+// the previous kernel on the stream is still running; everything before
+// pdl_wait() must touch no memory that another kernel writes or still reads.
+// pdl_wait() returns once every earlier kernel has completed and its writes
+// are visible; pdl_trigger() lets the next kernel begin its own prologue.
+// Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `k` on `st`, with programmatic dependent launch when `pdl`.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // Opt a kernel into the largest dynamic shared memory it can use: the
 // per-block limit minus its static shared memory.
 template <typename Kern>

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
 
   LogitsEpilogue<N> epi;
   if (kLogits) epi.init(tail, p.K, p.M);
+  pdl_wait();
+  pdl_trigger();
   const int mcols = p.M < N ? p.M : N;  // columns that carry data
 
   for (int t = t_begin; t < t_end; ++t) {
@@ -140,8 +142,7 @@ static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(kTileV) * (kSimtH + 1) * 4 + 16 * kSimtH * 4 +
                       (kLogits ? epi_smem_bytes(N, p.K)
                                : static_cast<size_t>(kTileV) * (N + 1) * 4);
-  k_head_simt<N, kLogits><<<grid, 128, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(k_head_simt<N, kLogits>, dim3(grid), dim3(128), smem, st, p.pdl != 0, p);
 }
 
 #ifndef DT_N

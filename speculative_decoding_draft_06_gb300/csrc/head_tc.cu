@@ -187,6 +187,9 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // prologue done; from here on the kernel reads and writes shared buffers
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer
@@ -365,8 +368,8 @@ static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, con
   TcParams q = p;
   q.stages = stages;
   const size_t smem = fixed + static_cast<size_t>(stages) * L::kStageBytes;
-  k_head_tc<N, kLogits><<<grid, 192, smem, st>>>(tw, ts, q);
-  return cudaGetLastError();
+  return launch_kernel(k_head_tc<N, kLogits>, dim3(grid), dim3(192), smem, st, q.pdl != 0, tw, ts,
+                       q);
 }
 
 #ifndef DT_N

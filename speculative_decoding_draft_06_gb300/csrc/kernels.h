@@ -10,6 +10,7 @@ namespace dt {
 
 // Batched head contraction (tensor-core bf16 path and SIMT fp32 path).
 struct TcParams {
+  int pdl;             // launch with programmatic dependent launch (host only)
   int rows;            // rows of the weight matrix: V (logits) or H (state)
   int H;               // contraction length
   int M;               // valid head rows (GEMM columns)
@@ -88,6 +89,7 @@ inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, i
 // Merge of per-CTA partials into per-row lse and top-K (log-probs), and
 // (select != 0) the global top-W of each request with pool append.
 struct MergeParams {
+  int pdl;             // launch with programmatic dependent launch (host only)
   const float* pm;
   const float* ps;
   const uint64_t* ptop;
@@ -119,6 +121,7 @@ cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
 
 // Deferred Top-B, compaction and the ancestor mask.
 struct PruneParams {
+  int pdl;             // launch with programmatic dependent launch (host only)
   int R, P, pool_stride, B, words;
   float beta;
   const int32_t* pool_parent;
@@ -137,6 +140,7 @@ cudaError_t launch_prune(const PruneParams& p, cudaStream_t st);
 
 // Root rows: S[r] = q(state0[r]), zero padding rows, scores 0.
 struct RootParams {
+  int pdl;             // launch with programmatic dependent launch (host only)
   int R, n_pad, H, bf16;
   const float* state0;
   void* S;

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   const int row = blockIdx.x;
   const int K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
 
   // ---- log-sum-exp
   float mloc = -INFINITY;
@@ -199,8 +201,7 @@ cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st) {
     while (np2 < p.F * p.K) np2 <<= 1;
     smem = static_cast<size_t>(np2) * 8;
   }
-  k_merge_rows<<<p.M, kMergeThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(k_merge_rows, dim3(p.M), dim3(kMergeThreads), smem, st, p.pdl != 0, p);
 }
 
 // ------------------------------------------------- Top-B, compaction, mask
@@ -217,6 +218,8 @@ constexpr int kPruneThreads = 1024;
 // sparse attention mask lets the target check every branch in one forward).
 __global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
   extern __shared__ uint64_t keys[];
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int np2 = pow2_at_least(p.P);
   int32_t* map = reinterpret_cast<int32_t*>(keys + np2);  // [P] pool -> rank
@@ -284,13 +287,14 @@ cudaError_t launch_prune(const PruneParams& p, cudaStream_t st) {
   while (np2 < p.P) np2 <<= 1;
   const size_t smem = static_cast<size_t>(np2) * 8 + static_cast<size_t>(p.P) * 4 +
                       static_cast<size_t>(p.B) * 4;
-  k_prune<<<p.R, kPruneThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(k_prune, dim3(p.R), dim3(kPruneThreads), smem, st, p.pdl != 0, p);
 }
 
 // ------------------------------------------------------------------ root
 
 __global__ void k_root(const RootParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
     const float v = m < p.R ? p.state0[static_cast<size_t>(m) * p.H + h] : 0.f;
@@ -303,8 +307,7 @@ __global__ void k_root(const RootParams p) {
 }
 
 cudaError_t launch_root(const RootParams& p, cudaStream_t st) {
-  k_root<<<p.n_pad, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(k_root, dim3(p.n_pad), dim3(256), 0, st, p.pdl != 0, p);
 }
 
 cudaError_t init_select_attrs() {
