@@ -41,13 +41,23 @@ struct TcLayout {
   static constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
 };
 
-__device__ __forceinline__ void state_store(const TcParams& p, int q, int row, float u) {
-  float out = 0.f;
-  if (q < p.M_out) {
-    const int tok = __ldg(p.tok + q);
-    out = tanhf(u + bf16_bits_to_float(__ldg(p.E_bf16 + static_cast<size_t>(tok) * p.H + row)));
+// Finish 8 output rows q0..q0+7 of hidden unit `row`: u[j] holds U at the
+// row's parent column; adds E[tok], tanh, rounds to bf16 (zeros past M_out).
+// The token and embedding loads of all 8 rows are issued before any use.
+__device__ __forceinline__ void state_store8(const TcParams& p, int q0, int row,
+                                             const float (&u)[8]) {
+  int tok[8];
+  float e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) tok[j] = q0 + j < p.M_out ? __ldg(p.tok + q0 + j) : 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    e[j] = bf16_bits_to_float(__ldg(p.E_bf16 + static_cast<size_t>(tok[j]) * p.H + row));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float out = q0 + j < p.M_out ? tanhf(u[j] + e[j]) : 0.f;
+    p.S_out_bf16[static_cast<size_t>(q0 + j) * p.H + row] = float_to_bf16_bits(out);
   }
-  p.S_out_bf16[static_cast<size_t>(q) * p.H + row] = float_to_bf16_bits(out);
 }
 
 // State step epilogue (all 128 epilogue threads; thread = hidden unit `row`).
@@ -71,10 +81,7 @@ __device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase
         u[j] = __uint_as_float(r);
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      if (valid) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) state_store(p, q0 + j, row, u[j]);
-      }
+      if (valid) state_store8(p, q0, row, u);
     }
     return;
   }
@@ -97,14 +104,23 @@ __device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase
   if (!last) return;
   __threadfence();
   const float* all = p.part + static_cast<size_t>(tile) * p.n_split * kMaxRows * kTileV;
-  for (int q = 0; q < n_out; ++q) {
-    float u = 0.f;
-    if (q < p.M_out) {
-      const int col = __ldg(p.slot + q);
-      for (int sp = 0; sp < p.n_split; ++sp)
-        u += __ldcg(all + (static_cast<size_t>(sp) * kMaxRows + col) * kTileV + lr);
+  for (int q0 = 0; q0 < n_out; q0 += 8) {
+    int col[8];
+    float u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      col[j] = q0 + j < p.M_out ? __ldg(p.slot + q0 + j) : 0;
+      u[j] = 0.f;
     }
-    if (valid) state_store(p, q, row, u);
+    for (int sp = 0; sp < p.n_split; ++sp) {   // fixed order over the splits
+      float part[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        part[j] = __ldcg(all + (static_cast<size_t>(sp) * kMaxRows + col[j]) * kTileV + lr);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u[j] += part[j];
+    }
+    if (valid) state_store8(p, q0, row, u);
   }
   if (lr == 0) p.tile_cnt[tile] = 0;
 }

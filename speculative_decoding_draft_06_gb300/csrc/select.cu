@@ -69,7 +69,59 @@ constexpr int kMergeWarps = kMergeThreads / 32;
 // score by accumulated path probability, keep the top W; "Accelerating
 // Language Models with Diffusion Draft Trees", Summary: global top-W child
 // prefixes, states carried forward).
+__device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k) {
+  const int idx = static_cast<int>(key_index(k));
+  const int i = idx / p.K, j = idx % p.K;
+  const int row = r * p.F + i;
+  const float c = key_value(k);
+  const int32_t tok = __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + j);
+  const size_t pi = static_cast<size_t>(r) * p.pool_stride + p.off + q;
+  p.pool_parent[pi] = (p.depth == 1) ? -1 : p.off_prev + i;
+  p.pool_token[pi] = tok;
+  p.pool_depth[pi] = p.depth;
+  p.pool_score[pi] = c;
+  const int m = r * p.Fd + q;
+  p.score_out[m] = c;
+  p.tok_next[m] = tok;
+  p.slot_next[m] = row;
+}
+
+// Warp 0 only, for |F_d| <= 32: every row's candidates are already sorted
+// (log-probs descending, one fp32 add keeps the order, ties by index), so
+// the top |F_d| is a fold of the F sorted lists with warp bitonic merges.
+__device__ void select_frontier_warp(const MergeParams& p, int r) {
+  const int lane = threadIdx.x & 31;
+  const int p2 = pow2_ceil32(p.Fd > p.K ? p.Fd : p.K);
+  auto row_key = [&](int i) -> uint64_t {
+    const int row = r * p.F + i;
+    if (lane >= p.K) return 0ull;
+    const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + lane);
+    const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
+    return make_key(c, static_cast<uint32_t>(i * p.K + lane));
+  };
+  uint64_t v = lane < p2 ? row_key(0) : 0ull;
+  uint64_t nxt = p.F > 1 ? row_key(1) : 0ull;
+  for (int i = 1; i < p.F; ++i) {
+    const uint64_t cur = nxt;
+    if (i + 1 < p.F) nxt = row_key(i + 1);   // next row's loads in flight
+    uint64_t y = 0ull;
+    if (p2 == 32) {
+      y = shfl_u64(cur, 31 - lane);
+    } else {
+      const int src = 2 * p2 - 1 - lane;
+      const uint64_t b = shfl_u64(cur, src < 0 ? 0 : src);
+      v = lane < p2 ? v : (lane < 2 * p2 ? b : 0ull);
+    }
+    v = warp_merge_desc(v, y, p2);
+  }
+  if (lane < p.Fd) write_frontier(p, r, lane, v);
+}
+
 __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys) {
+  if (p.Fd <= 32) {
+    if (threadIdx.x < 32) select_frontier_warp(p, r);
+    return;
+  }
   const int n = p.F * p.K;
   const int np2 = pow2_at_least(n);
   for (int e = threadIdx.x; e < np2; e += blockDim.x) {
@@ -84,23 +136,7 @@ __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys) {
   }
   __syncthreads();
   block_sort_desc(keys, np2);
-  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) {
-    const uint64_t k = keys[q];
-    const int idx = static_cast<int>(key_index(k));
-    const int i = idx / p.K, j = idx % p.K;
-    const int row = r * p.F + i;
-    const float c = key_value(k);
-    const int32_t tok = __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + j);
-    const size_t pi = static_cast<size_t>(r) * p.pool_stride + p.off + q;
-    p.pool_parent[pi] = (p.depth == 1) ? -1 : p.off_prev + i;
-    p.pool_token[pi] = tok;
-    p.pool_depth[pi] = p.depth;
-    p.pool_score[pi] = c;
-    const int m = r * p.Fd + q;
-    p.score_out[m] = c;
-    p.tok_next[m] = tok;
-    p.slot_next[m] = row;
-  }
+  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, keys[q]);
 }
 
 // One block per head row.
@@ -145,15 +181,15 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;
   uint64_t v = 0ull;
   int l = warp;
-  for (; l + 3 * kMergeWarps < p.n_cta; l += 4 * kMergeWarps) {  // 4 loads in flight
-    uint64_t y[4], vv[4];
+  for (; l + 7 * kMergeWarps < p.n_cta; l += 8 * kMergeWarps) {  // 8 lists' loads in flight
+    uint64_t y[8], vv[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       vv[u] = v;
       merge_operands(base + static_cast<size_t>(l + u * kMergeWarps) * K, K, p2, vv[u], y[u]);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const uint64_t a = (p2 < 32 && lane >= p2) ? vv[u] : v;
       v = warp_merge_desc(a, y[u], p2);
     }
@@ -196,7 +232,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
 
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st) {
   size_t smem = 0;
-  if (p.select) {
+  if (p.select && p.Fd > 32) {
     int np2 = 1;
     while (np2 < p.F * p.K) np2 <<= 1;
     smem = static_cast<size_t>(np2) * 8;
