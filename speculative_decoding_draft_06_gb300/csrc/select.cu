@@ -58,7 +58,7 @@ __device__ T block_reduce(T v, Op op, T* scratch) {
 
 // ------------------------------------------------ merge of rows + top-W
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
 // Global top-W of one request's candidates (run by the last merge block of
@@ -86,24 +86,44 @@ __device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k) {
   p.slot_next[m] = row;
 }
 
-// Warp 0 only, for |F_d| <= 32: every row's candidates are already sorted
-// (log-probs descending, one fp32 add keeps the order, ties by index), so
-// the top |F_d| is a fold of the F sorted lists with warp bitonic merges.
-__device__ void select_frontier_warp(const MergeParams& p, int r) {
-  const int lane = threadIdx.x & 31;
+// Fold the per-warp lists wl[w] (descending, p2 keys) into warp 0's `v` by
+// a pairwise tree: log2(warps) levels of one merge each.  All threads of the
+// block call it; on return warp 0's lanes 0..p2-1 hold the best p2 keys.
+__device__ uint64_t block_tree_merge(uint64_t v, uint64_t (*wl)[32], int p2) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  wl[warp][lane] = lane < p2 ? v : 0ull;
+  __syncthreads();
+  for (int stride = 1; stride < nw; stride <<= 1) {
+    if ((warp & (2 * stride - 1)) == 0 && warp + stride < nw) {
+      uint64_t y;
+      merge_operands(wl[warp + stride], p2, p2, v, y);
+      v = warp_merge_desc(v, y, p2);
+      __syncwarp();
+      wl[warp][lane] = lane < p2 ? v : 0ull;
+    }
+    __syncthreads();
+  }
+  return v;
+}
+
+// For |F_d| <= 32: every row's candidates are already sorted (log-probs
+// descending, one fp32 add keeps the order, ties by index), so the top |F_d|
+// is a fold of the F sorted lists with warp bitonic merges -- rows spread
+// over the warps, then a tree across warps.  All threads of the block call it.
+__device__ void select_frontier_warp(const MergeParams& p, int r, uint64_t (*wl)[32]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
   const int p2 = pow2_ceil32(p.Fd > p.K ? p.Fd : p.K);
-  auto row_key = [&](int i) -> uint64_t {
+  uint64_t v = 0ull;
+  for (int i = warp; i < p.F; i += nw) {
     const int row = r * p.F + i;
-    if (lane >= p.K) return 0ull;
-    const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + lane);
-    const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
-    return make_key(c, static_cast<uint32_t>(i * p.K + lane));
-  };
-  uint64_t v = lane < p2 ? row_key(0) : 0ull;
-  uint64_t nxt = p.F > 1 ? row_key(1) : 0ull;
-  for (int i = 1; i < p.F; ++i) {
-    const uint64_t cur = nxt;
-    if (i + 1 < p.F) nxt = row_key(i + 1);   // next row's loads in flight
+    uint64_t cur = 0ull;
+    if (lane < p.K) {
+      const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + lane);
+      const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
+      cur = make_key(c, static_cast<uint32_t>(i * p.K + lane));
+    }
     uint64_t y = 0ull;
     if (p2 == 32) {
       y = shfl_u64(cur, 31 - lane);
@@ -114,12 +134,14 @@ __device__ void select_frontier_warp(const MergeParams& p, int r) {
     }
     v = warp_merge_desc(v, y, p2);
   }
-  if (lane < p.Fd) write_frontier(p, r, lane, v);
+  v = block_tree_merge(v, wl, p2);
+  if (warp == 0 && lane < p.Fd) write_frontier(p, r, lane, v);
 }
 
-__device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys) {
+__device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
+                                uint64_t (*wl)[32]) {
   if (p.Fd <= 32) {
-    if (threadIdx.x < 32) select_frontier_warp(p, r);
+    select_frontier_warp(p, r, wl);
     return;
   }
   const int n = p.F * p.K;
@@ -142,8 +164,8 @@ __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys) {
 // One block per head row.
 //   lse = max + log(sum_cta s_cta exp(m_cta - max)), the merge in fp64;
 //   top-K = best K keys over the per-CTA sorted lists, by warp-wide bitonic
-//   merges (each warp folds every 8th list into a running list held in
-//   registers, then warp 0 folds the 8 warp results);
+//   merges (each of the 16 warps folds every 16th list into a running list
+//   held in registers, then a pairwise tree across the warps);
 //   logp = fp32(logit - lse).
 // With p.select set, the last block of each request (counted with an
 // atomic, reset afterwards) runs the request's top-W selection.
@@ -169,7 +191,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
     for (int i = threadIdx.x; i < p.n_cta; i += blockDim.x) {
       const float m = p.pm[static_cast<size_t>(row) * p.cta_stride + i];
       const float s = p.ps[static_cast<size_t>(row) * p.cta_stride + i];
-      if (m != -INFINITY) sloc += static_cast<double>(s) * exp(static_cast<double>(m) - mx);
+      if (m != -INFINITY) sloc += static_cast<double>(s * expf(m - mx));  // fp32 term, fp64 sum
     }
   }
   const double ssum = block_reduce(sloc, [](double a, double b) { return a + b; }, dscr);
@@ -199,15 +221,8 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
     merge_operands(base + static_cast<size_t>(l) * K, K, p2, v, y);
     v = warp_merge_desc(v, y, p2);
   }
-  wl[warp][lane] = lane < p2 ? v : 0ull;
-  __syncthreads();
+  v = block_tree_merge(v, wl, p2);
   if (warp == 0) {
-    v = wl[0][lane];
-    for (int w = 1; w < kMergeWarps; ++w) {
-      uint64_t y;
-      merge_operands(wl[w], p2, p2, v, y);
-      v = warp_merge_desc(v, y, p2);
-    }
     if (lane < K) {
       const float val = key_value(v);
       p.row_tok[static_cast<size_t>(row) * K + lane] = static_cast<int32_t>(key_index(v));
@@ -226,7 +241,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   __syncthreads();
   if (!last_flag) return;
   __threadfence();
-  select_frontier(p, r, dyn);
+  select_frontier(p, r, dyn, wl);
   if (threadIdx.x == 0) p.counters[r] = 0;
 }
 
