@@ -136,7 +136,11 @@ dartree_status dartree_build_host(dartree_ctx *ctx, const float *base_logits_hos
                                   const dartree_tree *out_host, void *stream);
 
 /* Synchronises `stream`, reads and clears the device check word and returns
- * OK, DEVICE_CHECK or TIMEOUT (or CUDA if the synchronisation failed). */
+ * OK, DEVICE_CHECK or TIMEOUT (or CUDA if the synchronisation failed).  After
+ * a device error it also resets the context's arrival counters, so the
+ * context can be used again; the failed build's outputs are undefined.
+ * Test knob: DARTREE_WAIT_LIMIT_CYCLES (read at dartree_create) shortens the
+ * kernels' pipeline waits to provoke the TIMEOUT path. */
 dartree_status dartree_sync_status(dartree_ctx *ctx, void *stream);
 
 /* Number of batched head calls made by the last build (== its D). */

@@ -66,6 +66,7 @@ struct dartree_ctx {
   int state_split = 1;
   int tc_max_stages = 0;   // tuning: pipeline depth cap of the head call (0: default)
   bool pdl = true;         // programmatic dependent launch between the kernels of a build
+  long long wait_limit = 0;  // test knob: pipeline wait limit in cycles (0: full)
   bool use_graph = true;   // capture each build shape once into a CUDA graph
 
   // the captured build and the arguments it was captured with
@@ -225,6 +226,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.cta_stride = c->max_cta;
   p.list_stride = c->max_cta;
   p.pdl = c->pdl;
+  p.wait_limit = c->wait_limit;
   int grid;
   cudaError_t e;
   {
@@ -283,6 +285,8 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
   p.n_tiles = (H + dt::kTileV - 1) / dt::kTileV;
   p.err = c->d_err;
   p.pdl = c->pdl;
+  p.wait_limit = c->wait_limit;
+  p.V_tok = c->cfg.V;
   cudaError_t e;
   KernelTimer tk(c, st, 1);
   if (c->bf16) {
@@ -573,6 +577,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   // tuning knobs of the head-call pipeline (defaults when unset)
   if (const char* v = getenv("DARTREE_TC_MAX_STAGES")) c->tc_max_stages = atoi(v);
   if (const char* v = getenv("DARTREE_PDL")) c->pdl = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_WAIT_LIMIT_CYCLES")) c->wait_limit = atoll(v);
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
     const int n = atoi(v);
@@ -686,7 +691,15 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
   flush_timing(ctx);
   int h = 0;
   e = cudaMemcpy(&h, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && h != 0) e = cudaMemset(ctx->d_err, 0, sizeof(int));
+  if (e == cudaSuccess && h != 0) {
+    // a failed launch may have left arrival counters part-way: clear them so
+    // the next build starts from a clean workspace
+    e = cudaMemset(ctx->d_err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(ctx->counters, 0, dt::kMaxRows * sizeof(int));
+    if (e == cudaSuccess)
+      e = cudaMemset(ctx->tile_cnt, 0,
+                     sizeof(int) * ((ctx->cfg.H + dt::kTileV - 1) / dt::kTileV));
+  }
   if (e != cudaSuccess) return ctx->cuda_fail(e, "error word read");
   if (h & dt::DT_ERR_TIMEOUT)
     return ctx->fail(DARTREE_ERR_TIMEOUT, "device wait timed out (flags 0x%x)", h);

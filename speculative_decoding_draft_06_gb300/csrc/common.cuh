@@ -12,9 +12,12 @@ enum : int {
   DT_ERR_TIMEOUT = 2,     // a bounded pipeline wait gave up
   DT_ERR_CLOSURE = 4,     // Top-B selected a node whose parent is unselected
   DT_ERR_EMPTY_ROW = 8,   // a corrected row has no finite logit
+  DT_ERR_BAD_INDEX = 16,  // a token / row index out of range was clamped
 };
 
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at GB300 clocks
+// (pipeline waits may be given a shorter limit to test the timeout path;
+// waits for copies or MMAs already in flight always use the full limit)
 
 constexpr int kMaxK = 32;      // children per node
 constexpr int kMaxRows = 256;  // head rows per call (R * W), one MMA N

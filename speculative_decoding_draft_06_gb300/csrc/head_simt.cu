@@ -123,9 +123,14 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
         for (int q = 0; q < n_out; ++q) {
           float out = 0.f;
           if (q < p.M_out) {
-            const int tok = __ldg(p.tok + q);
-            out = tanhf(Us[__ldg(p.slot + q)] +
-                        __ldg(p.E_f32 + static_cast<size_t>(tok) * p.H + row));
+            int tok = __ldg(p.tok + q);
+            int col = __ldg(p.slot + q);
+            if (tok < 0 || tok >= p.V_tok || col < 0 || col >= p.M) {  // upstream failure only
+              atomicOr(p.err, DT_ERR_BAD_INDEX);
+              tok = 0;
+              col = 0;
+            }
+            out = tanhf(Us[col] + __ldg(p.E_f32 + static_cast<size_t>(tok) * p.H + row));
           }
           p.S_out_f32[static_cast<size_t>(q) * p.H + row] = out;
         }

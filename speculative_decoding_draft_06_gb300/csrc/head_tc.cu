@@ -48,8 +48,16 @@ __device__ __forceinline__ void state_store8(const TcParams& p, int q0, int row,
                                              const float (&u)[8]) {
   int tok[8];
   float e[8];
+  bool bad = false;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) tok[j] = q0 + j < p.M_out ? __ldg(p.tok + q0 + j) : 0;
+  for (int j = 0; j < 8; ++j) {
+    tok[j] = q0 + j < p.M_out ? __ldg(p.tok + q0 + j) : 0;
+    if (tok[j] < 0 || tok[j] >= p.V_tok) {  // only after an upstream failure
+      bad = true;
+      tok[j] = 0;
+    }
+  }
+  if (bad) atomicOr(p.err, DT_ERR_BAD_INDEX);
 #pragma unroll
   for (int j = 0; j < 8; ++j)
     e[j] = bf16_bits_to_float(__ldg(p.E_bf16 + static_cast<size_t>(tok[j]) * p.H + row));
@@ -73,7 +81,8 @@ __device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int q = q0 + j;
-        const int col = q < p.M_out ? __ldg(p.slot + q) : 0;   // same for the whole warp
+        int col = q < p.M_out ? __ldg(p.slot + q) : 0;   // same for the whole warp
+        if (col < 0 || col >= p.M) col = 0;               // (never, unless upstream failed)
         uint32_t r;
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
                      : "=r"(r)
@@ -110,6 +119,7 @@ __device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       col[j] = q0 + j < p.M_out ? __ldg(p.slot + q0 + j) : 0;
+      if (col[j] < 0 || col[j] >= p.M) col[j] = 0;
       u[j] = 0.f;
     }
     for (int sp = 0; sp < p.n_split; ++sp) {   // fixed order over the splits
@@ -218,7 +228,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
         for (int i = 0; i < kb_span; ++i) {
           const int kb = kb_at(t, i);
-          if (!mbar_wait(&empty[stage], phase ^ 1u, p.err)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.wait_limit)) {
             *abort_flag = 1;
             break;
           }
@@ -251,7 +261,8 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;
       for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
         const int a = it & 1;
-        if (!mbar_wait(&tempty[a], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.err)) {
+        if (!mbar_wait(&tempty[a], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.err,
+                       p.wait_limit)) {
           *abort_flag = 1;
           break;
         }
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * N);
         bool ok = true;
         for (int i = 0; i < kb_span; ++i) {
-          if (!mbar_wait(&full[stage], phase, p.err)) {
+          if (!mbar_wait(&full[stage], phase, p.err, p.wait_limit)) {
             *abort_flag = 1;
             ok = false;
             break;
@@ -297,7 +308,8 @@ __global__ void __launch_bounds__(192, 1)
       const int a = it & 1;
       if (threadIdx.x == 0) {
         const bool ok = !*abort_flag &&
-                        mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err);
+                        mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err,
+                                  p.wait_limit);
         if (!ok) *abort_flag = 1;
         epi_go = ok;
       }

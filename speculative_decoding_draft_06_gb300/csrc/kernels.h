@@ -19,6 +19,8 @@ struct TcParams {
   int max_stages;      // launcher cap on the pipeline depth (0: default)
   int ctas_per_sm;     // CTAs sharing one SM's shared memory (0: 1)
   int* err;            // device error word
+  long long wait_limit;  // pipeline wait limit in cycles (0: the full ~2 s)
+  int V_tok;           // vocabulary size (bound of state-step tokens)
   // logits epilogue
   const float* z;      // base logits of this depth, request 0
   long long z_req_stride;

@@ -190,6 +190,7 @@ extern "C" dartree_status dartree_state_step_noalloc(const void* S_par, const in
   p.n_split = n_split;
   p.part = d->part;
   p.tile_cnt = d->cnt;
+  p.V_tok = 0x7FFFFFFF;  // tokens are the caller's to keep in [0, V)
   e = dt::launch_head_tc(N, false, tm_a, tm_s, p, tiles * n_split, st);
   if (e != cudaSuccess) return na_cuda_fail("state step launch", e);
   e = cudaMemcpyAsync(S_out, d->out, M * rb, cudaMemcpyDeviceToDevice, st);

@@ -49,13 +49,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// Bounded wait for the phase with the given parity to complete; gives up
+// after `limit` cycles (<= 0: the full limit).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          long long limit = 0) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
+  const long long lim = limit > 0 ? limit : kWaitLimitCycles;
   const long long t0 = clock64();
   while (!mbar_try_wait(a, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > lim) {
       atomicOr(err, DT_ERR_TIMEOUT);
       return false;
     }

@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   v = block_tree_merge(v, wl, p2);
   if (warp == 0) {
     if (lane < K) {
+      if (v == 0ull) atomicOr(p.err, DT_ERR_BAD_INDEX);  // fewer than K real entries
       const float val = key_value(v);
       p.row_tok[static_cast<size_t>(row) * K + lane] = static_cast<int32_t>(key_index(v));
       p.row_logp[static_cast<size_t>(row) * K + lane] =
@@ -297,8 +298,8 @@ __global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
     if (q < n_sel) {
       const int n = static_cast<int>(key_index(keys[q]));
       const int pp = p.pool_parent[pb + n];
-      int pr = pp < 0 ? -1 : map[pp];
-      if ((pp >= 0 && pr < 0) || pr >= q) {
+      int pr = (pp < 0 || pp >= p.P) ? -1 : map[pp];
+      if ((pp >= 0 && pr < 0) || pr >= q || pp >= p.P) {
         broken = true;
         pr = -1;
       }
