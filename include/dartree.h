@@ -175,6 +175,11 @@ dartree_status dartree_get_pool(dartree_ctx *ctx, int32_t *parent, int32_t *toke
 dartree_status dartree_get_rows(dartree_ctx *ctx, int32_t d, double *lse, int32_t *tok,
                                 float *logp, void *stream);
 
+/* Debug: the head states used by head call d (1-based) of the last build,
+ * [R*|F_{d-1}|, H] in the context's dtype (bf16 bits or fp32), row order as
+ * dartree_get_rows.  Any memory; asynchronous. */
+dartree_status dartree_get_states(dartree_ctx *ctx, int32_t d, void *states, void *stream);
+
 /* One batched head call (corrected logits fused with log-softmax and top-K)
  * for M head rows with states S [M, H] (context dtype: bf16 bits or fp32).
  * Row m belongs to request m / rows_per_req and uses base logits

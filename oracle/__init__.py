@@ -61,7 +61,7 @@ def _load():
         lib.orc_topk_row.restype = None
         lib.orc_pool_size.argtypes = [ctypes.c_int] * 3
         lib.orc_pool_size.restype = ctypes.c_int
-        lib.orc_build.argtypes = [ctypes.c_int] * 6 + [P] * 20
+        lib.orc_build.argtypes = [ctypes.c_int] * 6 + [P] * 21
         lib.orc_build.restype = ctypes.c_int
         lib.orc_topb.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_int, f32] + [P] * 7
         lib.orc_topb.restype = ctypes.c_int
@@ -123,11 +123,12 @@ def topk_row(ell, K: int):
 
 
 def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
-               force_slot=None, force_tok=None) -> dict:
+               force_slot=None, force_tok=None, force_state=None) -> dict:
     """Depth-wise supertree construction for request ``r`` of ``inp``.
 
     ``force_slot`` / ``force_tok`` ([P] each, pool layout) force the kept
-    frontier at every depth (teacher forcing).  Returns the kept pool, the
+    frontier at every depth (teacher forcing); ``force_state`` ([D, W, H]
+    fp32) forces the head states of every depth's rows.  Returns the kept pool, the
     oracle's own per-depth selection, per-row results and diagnostics.
     """
     z = _c(inp["z"][r, :D], np.float32)
@@ -149,9 +150,10 @@ def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
     fs = ft = None
     if force_slot is not None:
         fs, ft = _c(force_slot, np.int32), _c(force_tok, np.int32)
+    fst = None if force_state is None else _c(force_state, np.float32)
     rc = _load().orc_build(
         V, H, D, W, K, int(bf16), _ptr(z), _ptr(s0), _ptr(A), _ptr(E), _ptr(Wo),
-        _ptr(fs), _ptr(ft),
+        _ptr(fs), _ptr(ft), _ptr(fst),
         _ptr(o["pool_parent"]), _ptr(o["pool_token"]), _ptr(o["pool_depth"]),
         _ptr(o["pool_score"]), _ptr(o["own_slot"]), _ptr(o["own_tok"]),
         _ptr(o["own_score"]), _ptr(o["force_margin"]), _ptr(o["row_lse"]),

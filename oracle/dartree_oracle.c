@@ -206,6 +206,10 @@ int orc_pool_size(int D, int W, int K) {
  * like the pool), the frontier kept at each depth is the forced one (parent
  * slot in F_{d-1}, token) instead of the oracle's own top-W; the oracle still
  * records its own choice and scores the forced nodes in its own arithmetic.
+ * When force_state is given ([D][W][H] fp32), the head rows of depth d use
+ * those states instead of the oracle's own (state-level forcing, to compare
+ * each head call on identical inputs: the bf16-rounded tanh recurrence
+ * amplifies accumulation-order differences from depth to depth).
  *
  * Outputs ([P] = pool size, rows = W per depth):
  *   pool_parent/token/depth/score [P]: the pool that was kept, pool index =
@@ -221,6 +225,7 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
               const float *z, const float *state0,
               const void *A, const void *E, const void *Wout,
               const int32_t *force_slot, const int32_t *force_tok,
+              const float *force_state,
               int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
               float *pool_score,
               int32_t *own_slot, int32_t *own_tok, float *own_score,
@@ -254,6 +259,8 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
     for (int d = 1; d <= D; ++d) {
         const float *zd = z + (size_t)(d - 1) * V;
         int fd = (K * fp < W) ? K * fp : W;
+        if (force_state)
+            memcpy(st, force_state + (size_t)(d - 1) * W * H, sizeof(float) * (size_t)fp * H);
         /* one batched head call over every frontier row */
         *calls += 1;
         for (int i = 0; i < fp; ++i) {

@@ -55,7 +55,8 @@ struct dartree_ctx {
   EncodeTiledFn encode = nullptr;
 
   // workspace (device)
-  void* S[2] = {nullptr, nullptr};  // [256][H] states of head rows (ping-pong)
+  void* S_all = nullptr;  // [n_slots][256][H]: slot d-1 = states of head call d
+  int n_slots = 0;
   float* score[2] = {nullptr, nullptr};
   int32_t* tok_next = nullptr;      // [256] token of each next-depth row
   int32_t* slot_next = nullptr;     // [256] parent row of each next-depth row
@@ -103,7 +104,11 @@ struct dartree_ctx {
   uint32_t* o_mask = nullptr;
   int32_t* o_nout = nullptr;
 
-  CUtensorMap tm_S[2][kNumPads];
+  std::vector<CUtensorMap> tm_S;  // [n_slots * kNumPads]
+  void* S(int slot) const {
+    return static_cast<uint8_t*>(S_all) + static_cast<size_t>(slot) * dt::kMaxRows * cfg.H * elem;
+  }
+  const CUtensorMap& tmS(int slot, int n_pad) const { return tm_S[slot * kNumPads + pad_index(n_pad)]; }
   CUtensorMap tm_A{}, tm_Wout{};
   const void* tm_A_ptr = nullptr;
   const void* tm_Wout_ptr = nullptr;
@@ -202,7 +207,7 @@ cudaError_t alloc(T** p, size_t count) {
   return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T) + 16);
 }
 
-// Head call for M rows whose states are in c->S[sbuf] (rows >= M up to the
+// Head call for M rows whose states are in state slot `sbuf` (rows >= M up to the
 // padded count are zero or finite): fused logits + partials, then the row
 // merge (+ the request's top-W selection when sel != nullptr).
 dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_req_stride,
@@ -236,11 +241,11 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
       grid = p.n_tiles < slots ? p.n_tiles : slots;
       p.max_stages = c->tc_max_stages;
       p.ctas_per_sm = c->tc_ctas_per_sm;
-      e = dt::launch_head_tc(N, true, c->tm_Wout, c->tm_S[sbuf][pad_index(N)], p, grid, st);
+      e = dt::launch_head_tc(N, true, c->tm_Wout, c->tmS(sbuf, N), p, grid, st);
     } else {
       grid = p.n_tiles < c->max_cta ? p.n_tiles : c->max_cta;
       p.W_f32 = static_cast<const float*>(c->tm_Wout_ptr);
-      p.S_f32 = static_cast<const float*>(c->S[sbuf]);
+      p.S_f32 = static_cast<const float*>(c->S(sbuf));
       e = dt::launch_head_simt(N, true, p, grid, st);
     }
   }
@@ -269,8 +274,8 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   return DARTREE_OK;
 }
 
-// State step: S[src^1][q] = q(tanh(A S[src][slot[q]] + E[tok[q]])) for
-// q < M_out (zeros up to the padded count); S[src] holds M_in rows.
+// State step: slot src+1 row q = q(tanh(A S[slot[q]] + E[tok[q]])) for
+// q < M_out (zeros up to the padded count); state slot src holds M_in rows.
 dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, int M_in,
                          const int32_t* slot, const int32_t* tok, int M_out, cudaStream_t st) {
   const int H = c->cfg.H;
@@ -291,17 +296,17 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
   KernelTimer tk(c, st, 1);
   if (c->bf16) {
     p.E_bf16 = static_cast<const uint16_t*>(E);
-    p.S_out_bf16 = static_cast<uint16_t*>(c->S[src ^ 1]);
+    p.S_out_bf16 = static_cast<uint16_t*>(c->S(src + 1));
     p.n_split = c->state_split;
     p.part = c->part;
     p.tile_cnt = c->tile_cnt;
-    e = dt::launch_head_tc(N, false, c->tm_A, c->tm_S[src][pad_index(N)], p,
+    e = dt::launch_head_tc(N, false, c->tm_A, c->tmS(src, N), p,
                            p.n_tiles * p.n_split, st);
   } else {
     p.E_f32 = static_cast<const float*>(E);
-    p.S_out_f32 = static_cast<float*>(c->S[src ^ 1]);
+    p.S_out_f32 = static_cast<float*>(c->S(src + 1));
     p.W_f32 = static_cast<const float*>(A);
-    p.S_f32 = static_cast<const float*>(c->S[src]);
+    p.S_f32 = static_cast<const float*>(c->S(src));
     p.n_split = 1;
     e = dt::launch_head_simt(N, false, p, p.n_tiles, st);
   }
@@ -363,7 +368,7 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   rp.H = H;
   rp.bf16 = c->bf16;
   rp.state0 = s0;
-  rp.S = c->S[0];
+  rp.S = c->S(0);
   rp.score = c->score[0];
   rp.pdl = c->pdl;
   cudaError_t e;
@@ -380,7 +385,7 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
       // states of this depth's rows from their parents (the rows of call d-1)
       s = run_state(c, head->A, head->E, sbuf, R * F_prev, c->slot_next, c->tok_next, M, st);
       if (s != DARTREE_OK) return s;
-      sbuf ^= 1;
+      ++sbuf;  // each depth keeps its own state slot
     }
     const int Fd = frontier_after(F, W, K);
     dt::MergeParams sel{};
@@ -514,7 +519,7 @@ void free_all(dartree_ctx* c) {
   free_events(c);
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   c->gexec = nullptr;
-  void* ptrs[] = {c->S[0],      c->S[1],       c->score[0],    c->score[1],   c->tok_next,
+  void* ptrs[] = {c->S_all,     c->score[0],    c->score[1],   c->tok_next,
                   c->slot_next, c->iota,       c->counters,    c->part,       c->tile_cnt,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
@@ -602,8 +607,9 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   c->state_split = c->num_sms / h_tiles;
   if (c->state_split > nk) c->state_split = nk;
   if (c->state_split < 1) c->state_split = 1;
-  bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S[0]), rows * g.H * c->elem) == cudaSuccess &&
-            alloc(reinterpret_cast<uint8_t**>(&c->S[1]), rows * g.H * c->elem) == cudaSuccess &&
+  c->n_slots = g.max_D > 2 ? g.max_D : 2;
+  const size_t slot_bytes = rows * g.H * c->elem;
+  bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S_all), c->n_slots * slot_bytes) == cudaSuccess &&
             alloc(&c->score[0], rows) == cudaSuccess && alloc(&c->score[1], rows) == cudaSuccess &&
             alloc(&c->tok_next, rows) == cudaSuccess && alloc(&c->slot_next, rows) == cudaSuccess &&
             alloc(&c->iota, rows) == cudaSuccess && alloc(&c->counters, rows) == cudaSuccess &&
@@ -633,8 +639,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
     delete c;
     return create_fail(DARTREE_ERR_OOM, "workspace allocation");
   }
-  e = cudaMemset(c->S[0], 0, rows * g.H * c->elem);
-  if (e == cudaSuccess) e = cudaMemset(c->S[1], 0, rows * g.H * c->elem);
+  e = cudaMemset(c->S_all, 0, c->n_slots * slot_bytes);
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
@@ -652,10 +657,11 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
     return create_fail(DARTREE_ERR_CUDA, "workspace initialisation", e);
   }
   if (c->bf16) {
+    c->tm_S.resize(static_cast<size_t>(c->n_slots) * kNumPads);
+    for (int sl = 0; sl < c->n_slots; ++sl)
     for (int i = 0; i < kNumPads; ++i) {
       const uint32_t n = 16u << i;
-      if (encode_2d(c, &c->tm_S[0][i], c->S[0], rows, g.H, n) != DARTREE_OK ||
-          encode_2d(c, &c->tm_S[1][i], c->S[1], rows, g.H, n) != DARTREE_OK) {
+      if (encode_2d(c, &c->tm_S[sl * kNumPads + i], c->S(sl), rows, g.H, n) != DARTREE_OK) {
         free_all(c);
         delete c;
         return create_fail(DARTREE_ERR_CUDA, "state tensor map");
@@ -818,6 +824,19 @@ dartree_status dartree_get_rows(dartree_ctx* ctx, int32_t d, double* lse, int32_
   return DARTREE_OK;
 }
 
+dartree_status dartree_get_states(dartree_ctx* ctx, int32_t d, void* states, void* stream) {
+  if (!ctx || !states) return DARTREE_ERR_INVALID_ARG;
+  if (ctx->last_P == 0 || d < 1 || d > ctx->last_D)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "depth %d not in the last build", d);
+  int F = 1;
+  for (int i = 1; i < d; ++i) F = frontier_after(F, ctx->last_W, ctx->last_K);
+  const size_t bytes = static_cast<size_t>(ctx->last_R) * F * ctx->cfg.H * ctx->elem;
+  cudaError_t e = cudaMemcpyAsync(states, ctx->S(d - 1), bytes, cudaMemcpyDefault,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "states copy");
+  return DARTREE_OK;
+}
+
 dartree_status dartree_head_topk(dartree_ctx* ctx, const void* S, const float* z,
                                  int64_t z_req_stride, int32_t rows_per_req, const void* Wout,
                                  int32_t M, int32_t K, double* lse, int32_t* tok, float* logp,
@@ -835,9 +854,9 @@ dartree_status dartree_head_topk(dartree_ctx* ctx, const void* S, const float* z
   if (s != DARTREE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
-  cudaError_t e = cudaMemcpyAsync(ctx->S[0], S, M * rb, cudaMemcpyDeviceToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(ctx->S(0), S, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && pad_rows(M) > M)
-    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S[0]) + M * rb, 0, (pad_rows(M) - M) * rb, st);
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S(0)) + M * rb, 0, (pad_rows(M) - M) * rb, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy");
   return run_head(ctx, 0, z, z_req_stride, rows_per_req, M, K, lse, tok, logp, nullptr, st);
 }
@@ -854,12 +873,12 @@ dartree_status dartree_state_step(dartree_ctx* ctx, const void* S_par, const int
   if (!ctx->bf16) ctx->tm_A_ptr = A;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
-  cudaError_t e = cudaMemcpyAsync(ctx->S[0], S_par, M * rb, cudaMemcpyDeviceToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(ctx->S(0), S_par, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && pad_rows(M) > M)
-    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S[0]) + M * rb, 0, (pad_rows(M) - M) * rb, st);
+    e = cudaMemsetAsync(static_cast<uint8_t*>(ctx->S(0)) + M * rb, 0, (pad_rows(M) - M) * rb, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy");
   if ((s = run_state(ctx, A, E, 0, M, ctx->iota, tok, M, st)) != DARTREE_OK) return s;
-  e = cudaMemcpyAsync(S_out, ctx->S[1], M * rb, cudaMemcpyDeviceToDevice, st);
+  e = cudaMemcpyAsync(S_out, ctx->S(1), M * rb, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "state copy back");
   return DARTREE_OK;
 }

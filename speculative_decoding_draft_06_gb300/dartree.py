@@ -15,6 +15,7 @@ import os
 import platform
 import re
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -91,6 +92,7 @@ def load():
                                     ctypes.POINTER(ctypes.c_int64)]),
         "dartree_reset_timing": (st, [_vp]),
         "dartree_state_step_noalloc": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
+        "dartree_get_states": (st, [_vp, _i32, _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -274,6 +276,16 @@ class DARTree:
                                                _ptr(o["logp"]), _stream(stream)))
         torch.cuda.synchronize()
         return o
+
+    def get_states(self, d: int, rows: int, stream=None):
+        """Head states of head call d as fp32 [rows, H] (bf16 values widened)."""
+        dt = torch.int16 if self.bf16 else torch.float32
+        o = torch.empty(rows, self.H, dtype=dt)
+        self._check(self._lib.dartree_get_states(self._h, d, _ptr(o), _stream(stream)))
+        torch.cuda.synchronize()
+        if self.bf16:
+            return (o.numpy().view(np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+        return o.numpy()
 
     # ------------------------------------------------ single-step entries
     def head_topk(self, S, z, Wout, *, K: int, rows_per_req: int | None = None,

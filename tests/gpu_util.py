@@ -21,14 +21,15 @@ def run_build(ctx: dtl.DARTree, w: Workload, dev: dict) -> dict:
     ctx.sync()
     P = dtl.pool_size(w.D, w.W, w.K)
     pool = ctx.get_pool(w.R, P)
-    rows = []
+    rows, states = [], []
     F = 1
     for d, fd in enumerate(dtl.frontier_sizes(w.D, w.W, w.K), start=1):
         rows.append({k: v.numpy() for k, v in ctx.get_rows(d, w.R * F, w.K).items()})
+        states.append(ctx.get_states(d, w.R * F))
         F = fd
     tree = {k: v.cpu().numpy() for k, v in out.items()}
     return {"pool": {k: v.numpy() for k, v in pool.items()}, "rows": rows, "tree": tree,
-            "head_calls": ctx.head_calls()}
+            "states": states, "head_calls": ctx.head_calls()}
 
 
 def split_request(res: dict, w: Workload, r: int):
@@ -42,6 +43,15 @@ def split_request(res: dict, w: Workload, r: int):
         F = fd
     tree = {k: v[r] for k, v in res["tree"].items()}
     return pool, rows, tree
+
+
+def request_states(res: dict, w: Workload, r: int) -> list:
+    """Per-depth head states of request r ([F_{d-1}, H] each)."""
+    out, F = [], 1
+    for d, fd in enumerate(dtl.frontier_sizes(w.D, w.W, w.K), start=1):
+        out.append(res["states"][d - 1][r * F:(r + 1) * F])
+        F = fd
+    return out
 
 
 def cuda_ok() -> bool:

@@ -40,13 +40,49 @@ def forced_frontier(pool: dict, D: int, W: int, K: int):
     return slot, np.ascontiguousarray(pool["token"], np.int32), sizes
 
 
+def check_state_steps(inp: dict, bf16: bool, slot, tok, sizes, gpu_states: list,
+                      max_rows: int | None = None) -> int:
+    """Each GPU head state of depth >= 2 against the oracle's state step
+    applied to the GPU's own parent state and token: equal up to one bf16
+    rounding step (+2e-5 absolute near zero) with bf16 weights, 2e-6 with
+    fp32.  Returns the number of differing elements."""
+    flips, off = 0, sizes[0]
+    for d in range(2, len(gpu_states) + 1):
+        fd = sizes[d - 2]                       # rows of call d = nodes of depth d-1
+        base = off - fd
+        n = fd if max_rows is None else min(fd, max_rows)
+        for i in range(n):
+            par = gpu_states[d - 2][slot[base + i]]
+            ref = oracle.state_step(inp["A"], inp["E"], par, int(tok[base + i]), bf16)
+            got = gpu_states[d - 1][i]
+            dif = np.abs(got - ref)
+            if bf16:
+                ulp = np.spacing(np.abs(ref).astype(np.float32)) * 2 ** 16
+                assert np.all(dif <= ulp + 2e-5), (d, i, float(dif.max()))
+            else:
+                assert np.all(dif <= 2e-6), (d, i, float(dif.max()))
+            flips += int(np.count_nonzero(dif))
+        off += sizes[d - 1] if d - 1 < len(sizes) else 0
+    return flips
+
+
 def compare_request(inp: dict, r: int, D: int, W: int, K: int, B: int, beta: float,
-                    bf16: bool, gpu_pool: dict, gpu_rows: list, gpu_tree: dict) -> dict:
+                    bf16: bool, gpu_pool: dict, gpu_rows: list, gpu_tree: dict,
+                    gpu_states: list | None = None) -> dict:
     """Teacher-forced comparison of one request.  Raises AssertionError on a
-    mismatch that no near-tie explains; returns counters otherwise."""
+    mismatch that no near-tie explains; returns counters otherwise.  With
+    gpu_states (per depth [F_{d-1}, H] fp32), every head call is compared on
+    the GPU's own states and every state step is checked separately."""
     tol = TOL[bf16]
     slot, tok, sizes = forced_frontier(gpu_pool, D, W, K)
-    o = oracle.build_tree(inp, r, D, W, K, bf16, force_slot=slot, force_tok=tok)
+    fst = None
+    if gpu_states is not None:
+        H = inp["A"].shape[0]
+        fst = np.zeros((D, W, H), np.float32)
+        for d, s in enumerate(gpu_states):
+            fst[d, :s.shape[0]] = s
+    o = oracle.build_tree(inp, r, D, W, K, bf16, force_slot=slot, force_tok=tok,
+                          force_state=fst)
     rep = {"near_ties": 0, "exact_depths": 0, "max_score_err": 0.0, "max_lse_err": 0.0,
            "max_logp_err": 0.0, "topk_near_ties": 0}
     off, F = 0, 1
@@ -94,6 +130,8 @@ def compare_request(inp: dict, r: int, D: int, W: int, K: int, B: int, beta: flo
             rep["near_ties"] += 1
         off += fd
         F = fd
+    if gpu_states is not None:
+        rep["state_flips"] = check_state_steps(inp, bf16, slot, tok, sizes, gpu_states)
     # --- deferred Top-B: a pure function of the pool -> bit-exact
     ref = oracle.topb(gpu_pool["parent"], gpu_pool["token"], gpu_pool["depth"],
                       gpu_pool["score"], B, beta)

@@ -46,7 +46,8 @@ def test_build_matches_oracle_small(idx):
     tot = {"near_ties": 0, "topk_near_ties": 0}
     for r in range(w.R):
         pool, rows, tree = gu.split_request(res, w, r)
-        rep = parity.compare_request(inp, r, w.D, w.W, w.K, w.B, w.beta, w.bf16, pool, rows, tree)
+        rep = parity.compare_request(inp, r, w.D, w.W, w.K, w.B, w.beta, w.bf16, pool, rows, tree,
+                                     gpu_states=gu.request_states(res, w, r))
         for k in tot:
             tot[k] += rep[k]
     # near-ties must stay rare on random data

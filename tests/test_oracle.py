@@ -396,6 +396,26 @@ def test_teacher_forcing_with_own_choice_is_identity():
     assert np.all(b["force_margin"] >= 0)
 
 
+def test_state_forcing_with_own_states_is_identity():
+    w = I.small_workload(802, V=150, H=16, D=4, W=4, K=3, B=9, bf16=True)
+    inp = I.make_inputs(w)
+    a = oracle.build_tree(inp, 0, w.D, w.W, w.K, True)
+    # the oracle's own head states, depth by depth, from its own frontier
+    st = np.zeros((w.D, w.W, w.H), np.float32)
+    rows = [bf.q(inp["state0"][0], True)]
+    off, sizes = 0, w.frontier_sizes()
+    for d in range(w.D):
+        for i, s in enumerate(rows):
+            st[d, i] = s
+        fd = sizes[d]
+        rows = [oracle.state_step(inp["A"], inp["E"], rows[a["own_slot"][off + q]],
+                                  int(a["own_tok"][off + q]), True) for q in range(fd)]
+        off += fd
+    b = oracle.build_tree(inp, 0, w.D, w.W, w.K, True, force_state=st)
+    for k in ("pool_parent", "pool_token", "pool_score", "row_lse", "row_logp"):
+        assert np.array_equal(a[k], b[k], equal_nan=k.startswith("row")), k
+
+
 def test_teacher_forcing_scores_an_off_beam_choice():
     w = I.small_workload(801, V=120, H=16, D=3, W=2, K=2, B=4, bf16=False)
     inp = I.make_inputs(w)
