@@ -128,6 +128,12 @@ def aggregate(ms_local: float, world: int) -> float:
     return float(t.item())
 
 
+def job_value(ms_max: float, world: int, requests: int) -> float:
+    """Whole-job builds/s: every rank builds `requests` trees per step and the
+    step time is the slowest rank's (weak scaling, no data-path collective)."""
+    return world * requests * 1e3 / ms_max
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -181,28 +187,40 @@ class ClockSampler:
 # -------------------------------------------------------------- CPU oracle
 
 def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0) -> dict:
-    """Time the CPU oracle on the first depths of one request's build, as
-    many as fit in about budget_s, and scale to a full build by head rows
-    (the dominant cost is one V x H fp64 pass per head row)."""
+    """Time the CPU oracle on a bounded sample of one request's build and
+    scale to a full build by head rows (the dominant cost is one V x H fp64
+    pass per head row).  The sample is the first depths of the build when at
+    least one head row fits in budget_s, else one head row restricted to a
+    vocabulary slice, scaled by V / slice."""
+    import numpy as np
+
     import oracle
     rows = [m // w.R for m in w.head_rows()]       # head rows per request per depth
+    total_rows = sum(rows)
+    s0 = inp["state0"][request]
+    vs = min(w.V, 4096)
     t0 = time.perf_counter()
-    oracle.build_tree(inp, request, 1, w.W, w.K, w.bf16)
-    t1 = time.perf_counter() - t0                  # one depth, one row
+    oracle.logits_row(inp["z"][request, 0, :vs], inp["Wout"][:vs], s0, w.bf16)
+    t_row = (time.perf_counter() - t0) * w.V / vs  # estimated cost of one full row
+    if t_row > budget_s:
+        vs = max(256, min(w.V, int(w.V * budget_s / t_row)))
+        t0 = time.perf_counter()
+        oracle.logits_row(inp["z"][request, 0, :vs], inp["Wout"][:vs], s0, w.bf16)
+        t = time.perf_counter() - t0
+        per_build = t * (w.V / vs) * total_rows
+        return {"builds_per_s": 1.0 / per_build, "seconds": t,
+                "sample": (f"oracle (fp64, 1 thread): one head row over {vs} of {w.V} "
+                           f"vocabulary entries ({t:.2f} s), scaled by V/{vs} and "
+                           f"{total_rows} head rows per build")}
     d_s, acc = 1, rows[0]
-    while d_s < w.D and (acc + rows[d_s]) * t1 <= budget_s:
+    while d_s < w.D and (acc + rows[d_s]) * t_row <= budget_s:
         acc += rows[d_s]
         d_s += 1
-    if d_s > 1:
-        t0 = time.perf_counter()
-        oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16)
-        t = time.perf_counter() - t0
-    else:
-        t = t1
-    total_rows = sum(rows)
+    t0 = time.perf_counter()
+    oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16)
+    t = time.perf_counter() - t0
     per_build = t * total_rows / acc
-    return {"builds_per_s": 1.0 / per_build, "seconds": t, "depths": d_s, "rows": acc,
-            "total_rows": total_rows,
+    return {"builds_per_s": 1.0 / per_build, "seconds": t,
             "sample": (f"oracle (fp64, 1 thread) on depths 1..{d_s} of request {request} "
                        f"({acc} of {total_rows} head rows, {t:.1f} s), scaled by head rows")}
 
@@ -299,7 +317,7 @@ def run_gpu(args) -> None:
     barrier()
     ms_local = e0.elapsed_time(e1) / args.steps
     ms = aggregate(ms_local, world)
-    value = world * w.R * 1e3 / ms
+    value = job_value(ms, world, w.R)
 
     # per-kernel durations (events around each launch, same stream)
     ctx.set_timing(True)

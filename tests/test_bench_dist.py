@@ -1,0 +1,47 @@
+"""Host logic of the multi-GPU bench path on CPU: world_size 2 over gloo.
+The build shards by request (replicas, no data-path collective); the only
+exchange is the max of the per-rank step time."""
+from __future__ import annotations
+
+import os
+import socket
+
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, world: int, port: int, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = bench.aggregate(2.0 + rank, world)          # ranks report 2 ms and 3 ms
+    q.put((rank, ms, bench.job_value(ms, world, 32)))
+    dist.destroy_process_group()
+
+
+def test_step_time_is_the_max_over_ranks_and_value_counts_all_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, ms, value in got:
+        assert ms == 3.0
+        assert abs(value - 2 * 32 * 1e3 / 3.0) < 1e-9
+
+
+def test_single_rank_value():
+    assert bench.aggregate(4.0, 1) == 4.0
+    assert bench.job_value(4.0, 1, 1) == 250.0
