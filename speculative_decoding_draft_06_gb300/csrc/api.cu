@@ -62,6 +62,9 @@ struct dartree_ctx {
   int32_t* slot_next = nullptr;     // [256] parent row of each next-depth row
   int32_t* iota = nullptr;          // [256] 0, 1, 2, ...
   int* counters = nullptr;          // [256] per-request arrival counters (select)
+  int* row_cnt = nullptr;           // [256] per-row group arrival counters (merge)
+  uint64_t* gpl = nullptr;          // [256][8][32] per-group top-K lists (merge)
+  float2* gls = nullptr;            // [256][8] per-group (max, sum-exp) (merge)
   float* part = nullptr;            // split-K partial sums of the state step
   int* tile_cnt = nullptr;          // split-K arrival counters
   int state_split = 1;
@@ -266,6 +269,12 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   mp.err = c->d_err;
   mp.select = sel != nullptr;
   mp.pdl = c->pdl;
+  mp.groups = (grid + 19) / 20;  // about 20 CTA partials per merge block, at most 8
+  if (mp.groups > 8) mp.groups = 8;
+  if (mp.groups < 1) mp.groups = 1;
+  mp.gpl = c->gpl;
+  mp.gls = c->gls;
+  mp.row_cnt = c->row_cnt;
   {
     KernelTimer tk(c, st, 2);
     e = dt::launch_merge_rows(mp, st);
@@ -521,6 +530,7 @@ void free_all(dartree_ctx* c) {
   c->gexec = nullptr;
   void* ptrs[] = {c->S_all,     c->score[0],    c->score[1],   c->tok_next,
                   c->slot_next, c->iota,       c->counters,    c->part,       c->tile_cnt,
+                  c->row_cnt,   c->gpl,        c->gls,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
                   c->d_err,     c->z_stage,    c->s0_stage,    c->o_parent,   c->o_token,
@@ -616,6 +626,8 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
             alloc(&c->part, static_cast<size_t>(h_tiles) * c->state_split * rows * dt::kTileV) ==
                 cudaSuccess &&
             alloc(&c->tile_cnt, static_cast<size_t>(h_tiles)) == cudaSuccess &&
+            alloc(&c->row_cnt, rows) == cudaSuccess && alloc(&c->gpl, rows * 8 * 32) == cudaSuccess &&
+            alloc(&c->gls, rows * 8) == cudaSuccess &&
             alloc(&c->pm, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ps, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ptop, rows * c->max_cta * dt::kEpiWarps * g.max_K) == cudaSuccess &&
@@ -642,6 +654,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   e = cudaMemset(c->S_all, 0, c->n_slots * slot_bytes);
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, rows * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->row_cnt, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
   if (e == cudaSuccess) {
     int32_t h_iota[dt::kMaxRows];
@@ -702,6 +715,7 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
     // the next build starts from a clean workspace
     e = cudaMemset(ctx->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->counters, 0, dt::kMaxRows * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(ctx->row_cnt, 0, dt::kMaxRows * sizeof(int));
     if (e == cudaSuccess)
       e = cudaMemset(ctx->tile_cnt, 0,
                      sizeof(int) * ((ctx->cfg.H + dt::kTileV - 1) / dt::kTileV));

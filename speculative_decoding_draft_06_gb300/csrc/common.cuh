@@ -78,6 +78,18 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int mask) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
+// (m, s) <- (m, s) (+) (m2, s2): log-sum-exp pairs, s = sum exp(x - m).
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float mx = fmaxf(m, m2);
+  if (mx == -INFINITY) {
+    m = -INFINITY;
+    s = 0.f;
+    return;
+  }
+  s = s * expf(m - mx) + s2 * expf(m2 - mx);
+  m = mx;
+}
+
 // Smallest power of two >= k (k <= 32).
 __host__ __device__ __forceinline__ int pow2_ceil32(int k) {
   return k <= 1 ? 1 : k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32;

@@ -56,18 +56,6 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
-// (m, s) <- (m, s) (+) (m2, s2): log-sum-exp pairs, s = sum exp(x - m).
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-  const float mx = fmaxf(m, m2);
-  if (mx == -INFINITY) {
-    m = -INFINITY;
-    s = 0.f;
-    return;
-  }
-  s = s * expf(m - mx) + s2 * expf(m2 - mx);
-  m = mx;
-}
-
 // Insert every key of `bal` lanes (keys differ per lane) into the sorted
 // list L of K keys, best first.  Warp-collective.
 static __device__ __noinline__ void list_insert_lanes(uint64_t* L, int K, uint64_t key, unsigned bal) {

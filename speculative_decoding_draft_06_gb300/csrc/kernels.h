@@ -92,6 +92,10 @@ inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, i
 // (select != 0) the global top-W of each request with pool append.
 struct MergeParams {
   int pdl;             // launch with programmatic dependent launch (host only)
+  int groups;          // blocks per row, each merging a contiguous share of the CTAs
+  uint64_t* gpl;       // [256][8][32] per-group top-K lists
+  float2* gls;         // [256][8] per-group (max, sum-exp)
+  int* row_cnt;        // [256] group arrival counters, zero between launches
   const float* pm;
   const float* ps;
   const uint64_t* ptop;

@@ -58,7 +58,7 @@ __device__ T block_reduce(T v, Op op, T* scratch) {
 
 // ------------------------------------------------ merge of rows + top-W
 
-constexpr int kMergeThreads = 512;
+constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
 // Global top-W of one request's candidates (run by the last merge block of
@@ -161,68 +161,79 @@ __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
   for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, keys[q]);
 }
 
-// One block per head row.
-//   lse = max + log(sum_cta s_cta exp(m_cta - max)), the merge in fp64;
-//   top-K = best K keys over the per-CTA sorted lists, by warp-wide bitonic
-//   merges (each of the 16 warps folds every 16th list into a running list
-//   held in registers, then a pairwise tree across the warps);
-//   logp = fp32(logit - lse).
-// With p.select set, the last block of each request (counted with an
-// atomic, reset afterwards) runs the request's top-W selection.
+// Row merge.  Grid = (groups, M): block (g, c) merges a contiguous share of
+// the per-CTA partials of head row c -- the (max, sum-exp) pairs with fp32
+// log-sum-exp merges, and the sorted top-K lists by warp bitonic merges (each
+// warp folds every 8th list, then a tree across the warps) -- and publishes
+// one partial pair and one list.  The last group block of the row (atomic
+// count) combines the group partials (fp64 sum across groups) into
+//   lse = max + log(sum), top-K = best K keys, logp = fp32(logit - lse).
+// With p.select set, the last row of each request then runs the request's
+// top-W selection.  Short dependency chains in many blocks instead of one
+// long chain per row.
 __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams p) {
   extern __shared__ uint64_t dyn[];
   __shared__ uint64_t wl[kMergeWarps][32];
-  __shared__ double dscr[32];
-  __shared__ float fscr[32];
   __shared__ int last_flag;
-  const int row = blockIdx.x;
+  const int g = blockIdx.x, row = blockIdx.y;
   const int K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p2 = pow2_ceil32(K);
   pdl_wait();
   pdl_trigger();
 
-  // ---- log-sum-exp
-  float mloc = -INFINITY;
-  for (int i = threadIdx.x; i < p.n_cta; i += blockDim.x)
-    mloc = fmaxf(mloc, p.pm[static_cast<size_t>(row) * p.cta_stride + i]);
-  const float mx = block_reduce(mloc, [](float a, float b) { return fmaxf(a, b); }, fscr);
-  double sloc = 0.0;
-  if (mx != -INFINITY) {
-    for (int i = threadIdx.x; i < p.n_cta; i += blockDim.x) {
-      const float m = p.pm[static_cast<size_t>(row) * p.cta_stride + i];
-      const float s = p.ps[static_cast<size_t>(row) * p.cta_stride + i];
-      if (m != -INFINITY) sloc += static_cast<double>(s * expf(m - mx));  // fp32 term, fp64 sum
+  const int l0 = static_cast<int>(static_cast<long long>(g) * p.n_cta / p.groups);
+  const int l1 = static_cast<int>(static_cast<long long>(g + 1) * p.n_cta / p.groups);
+  // ---- this group's log-sum-exp pair (warp 0)
+  if (warp == 0) {
+    float m = -INFINITY, s = 0.f;
+    for (int i = l0 + lane; i < l1; i += 32)
+      lse_merge(m, s, p.pm[static_cast<size_t>(row) * p.cta_stride + i],
+                p.ps[static_cast<size_t>(row) * p.cta_stride + i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+      lse_merge(m, s, m2, s2);
     }
+    if (lane == 0) p.gls[row * 8 + g] = make_float2(m, s);
   }
-  const double ssum = block_reduce(sloc, [](double a, double b) { return a + b; }, dscr);
-  const double lse = (mx == -INFINITY) ? -INFINITY : static_cast<double>(mx) + log(ssum);
-  if (threadIdx.x == 0 && mx == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
-
-  // ---- top-K over the per-CTA lists
-  const int p2 = pow2_ceil32(K);
+  // ---- this group's top-K
   const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;
   uint64_t v = 0ull;
-  int l = warp;
-  for (; l + 7 * kMergeWarps < p.n_cta; l += 8 * kMergeWarps) {  // 8 lists' loads in flight
-    uint64_t y[8], vv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      vv[u] = v;
-      merge_operands(base + static_cast<size_t>(l + u * kMergeWarps) * K, K, p2, vv[u], y[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint64_t a = (p2 < 32 && lane >= p2) ? vv[u] : v;
-      v = warp_merge_desc(a, y[u], p2);
-    }
-  }
-  for (; l < p.n_cta; l += kMergeWarps) {
+  for (int l = l0 + warp; l < l1; l += kMergeWarps) {
     uint64_t y;
     merge_operands(base + static_cast<size_t>(l) * K, K, p2, v, y);
     v = warp_merge_desc(v, y, p2);
   }
   v = block_tree_merge(v, wl, p2);
+  if (warp == 0) p.gpl[(static_cast<size_t>(row) * 8 + g) * 32 + lane] = lane < p2 ? v : 0ull;
+
+  // ---- the last group block of the row combines the groups
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_flag = (atomicAdd(p.row_cnt + row, 1) == p.groups - 1);
+  __syncthreads();
+  if (!last_flag) return;
+  __threadfence();
+  if (threadIdx.x == 0) p.row_cnt[row] = 0;
+  v = warp < p.groups ? __ldcg(p.gpl + (static_cast<size_t>(row) * 8 + warp) * 32 + lane) : 0ull;
+  v = block_tree_merge(v, wl, p2);
   if (warp == 0) {
+    float m = -INFINITY, s = 0.f;
+    if (lane < p.groups) {
+      const float2 gp = __ldcg(p.gls + row * 8 + lane);
+      m = gp.x;
+      s = gp.y;
+    }
+    float mx = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    double sd = (m != -INFINITY) ? static_cast<double>(s * expf(m - mx)) : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xFFFFFFFFu, sd, o);
+    const double lse = (mx == -INFINITY) ? -INFINITY : static_cast<double>(mx) + log(sd);
+    if (lane == 0 && mx == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
     if (lane < K) {
       if (v == 0ull) atomicOr(p.err, DT_ERR_BAD_INDEX);  // fewer than K real entries
       const float val = key_value(v);
@@ -234,7 +245,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   }
   if (!p.select) return;
 
-  // ---- the last block of request r runs its top-W selection
+  // ---- the last row of request r runs its top-W selection
   const int r = row / p.F;
   __threadfence();
   __syncthreads();
@@ -253,7 +264,8 @@ cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st) {
     while (np2 < p.F * p.K) np2 <<= 1;
     smem = static_cast<size_t>(np2) * 8;
   }
-  return launch_kernel(k_merge_rows, dim3(p.M), dim3(kMergeThreads), smem, st, p.pdl != 0, p);
+  return launch_kernel(k_merge_rows, dim3(p.groups, p.M), dim3(kMergeThreads), smem, st,
+                       p.pdl != 0, p);
 }
 
 // ------------------------------------------------- Top-B, compaction, mask
