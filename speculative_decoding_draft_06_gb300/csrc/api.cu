@@ -65,6 +65,7 @@ struct dartree_ctx {
   int* row_cnt = nullptr;           // [256] per-row group arrival counters (merge)
   uint64_t* gpl = nullptr;          // [256][8][32] per-group top-K lists (merge)
   float2* gls = nullptr;            // [256][8] per-group (max, sum-exp) (merge)
+  unsigned long long* gth = nullptr;  // [256] per-row top-K bound of a head call
   float* part = nullptr;            // split-K partial sums of the state step
   int* tile_cnt = nullptr;          // split-K arrival counters
   int state_split = 1;
@@ -231,6 +232,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.pm = c->pm;
   p.ps = c->ps;
   p.ptop = c->ptop;
+  p.gth = c->gth;
   p.cta_stride = c->max_cta;
   p.list_stride = c->max_cta;
   p.pdl = c->pdl;
@@ -275,6 +277,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   mp.gpl = c->gpl;
   mp.gls = c->gls;
   mp.row_cnt = c->row_cnt;
+  mp.gth = c->gth;
   {
     KernelTimer tk(c, st, 2);
     e = dt::launch_merge_rows(mp, st);
@@ -530,7 +533,7 @@ void free_all(dartree_ctx* c) {
   c->gexec = nullptr;
   void* ptrs[] = {c->S_all,     c->score[0],    c->score[1],   c->tok_next,
                   c->slot_next, c->iota,       c->counters,    c->part,       c->tile_cnt,
-                  c->row_cnt,   c->gpl,        c->gls,
+                  c->row_cnt,   c->gpl,        c->gls,         c->gth,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
                   c->d_err,     c->z_stage,    c->s0_stage,    c->o_parent,   c->o_token,
@@ -627,7 +630,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
                 cudaSuccess &&
             alloc(&c->tile_cnt, static_cast<size_t>(h_tiles)) == cudaSuccess &&
             alloc(&c->row_cnt, rows) == cudaSuccess && alloc(&c->gpl, rows * 8 * 32) == cudaSuccess &&
-            alloc(&c->gls, rows * 8) == cudaSuccess &&
+            alloc(&c->gls, rows * 8) == cudaSuccess && alloc(&c->gth, rows) == cudaSuccess &&
             alloc(&c->pm, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ps, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ptop, rows * c->max_cta * dt::kEpiWarps * g.max_K) == cudaSuccess &&
@@ -655,6 +658,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->row_cnt, 0, rows * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->gth, 0, rows * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
   if (e == cudaSuccess) {
     int32_t h_iota[dt::kMaxRows];
@@ -716,6 +720,7 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
     e = cudaMemset(ctx->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->counters, 0, dt::kMaxRows * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->row_cnt, 0, dt::kMaxRows * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(ctx->gth, 0, dt::kMaxRows * sizeof(unsigned long long));
     if (e == cudaSuccess)
       e = cudaMemset(ctx->tile_cnt, 0,
                      sizeof(int) * ((ctx->cfg.H + dt::kTileV - 1) / dt::kTileV));

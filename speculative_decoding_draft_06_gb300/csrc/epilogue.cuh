@@ -9,9 +9,14 @@
 // which reads its 128 values, 4 per lane.  Because one warp owns a row for
 // the whole kernel, the row has a single top-K list per CTA (shared memory,
 // sorted, best first) and needs no cross-warp synchronisation:
-//   * a value enters only if its key beats the list's K-th key; one or two
-//     entrants are inserted one at a time, more are warp-sorted and merged
-//     with the list by a bitonic merge;
+//   * a value enters only if its key beats the list's K-th key and the row's
+//     global bound -- the best K-th key any CTA's list has reached so far,
+//     shared through a 64-bit atomicMax.  Any list's K-th key bounds the
+//     row's true K-th key from below (that list alone holds K keys at or
+//     above it), so no key of the final top-K is ever filtered out; the
+//     bound only spares CTAs the insertions of keys that cannot make it;
+//   * one or two entrants are inserted one at a time, more are warp-sorted
+//     and merged with the list by a bitonic merge;
 //   * softmax state: for <= 64 rows each lane keeps a running (max, sum) per
 //     owned row in registers and lanes are combined once at the end; for more
 //     rows each chunk is reduced across the warp and folded into a per-row
@@ -111,13 +116,16 @@ struct LogitsEpilogue {
   static constexpr int kTPitch = 132;                    // floats per transposed row
   float lm[kSlots], ls[kSlots];
   uint64_t* lists;  // [N][K], one sorted list per row
+  unsigned long long* gth;  // [N] global per-row lower bound of the K-th key (or null)
   float* T;         // [2][16][kTPitch]
   float2* run;      // [N] (N > 64)
   int K, M, lane, warp, t;
   int nchunk;       // chunks handed over so far (selects the T buffer)
   bool bad;
 
-  __device__ __forceinline__ void init(uint8_t* smem, int K_, int M_) {
+  __device__ __forceinline__ void init(uint8_t* smem, int K_, int M_,
+                                       unsigned long long* gth_ = nullptr) {
+    gth = gth_;
     lists = reinterpret_cast<uint64_t*>(smem);
     T = reinterpret_cast<float*>(lists + static_cast<size_t>(N) * K_);
     run = reinterpret_cast<float2*>(T + 2 * 16 * kTPitch);
@@ -151,12 +159,15 @@ struct LogitsEpilogue {
   // Top-K update of row c with this lane's 4 values (vocabulary v0 + lane + 32 i).
   __device__ __forceinline__ void topk4(int c, const float (&xv)[4], uint32_t v0, int V) {
     uint64_t* L = lists + static_cast<size_t>(c) * K;
+    const uint64_t g = gth ? *reinterpret_cast<volatile unsigned long long*>(gth + c) : 0ull;
+    const uint64_t k_before = L[K - 1];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t v = v0 + lane + 32 * i;
       const bool valid = static_cast<int>(v) < V;
       const uint64_t key = (valid && xv[i] == xv[i]) ? make_key(xv[i], v) : 0ull;
-      const uint64_t th = L[K - 1];
+      uint64_t th = L[K - 1];
+      th = th > g ? th : g;
       const unsigned bal = __ballot_sync(kFull, key > th);
       if (bal == 0u) continue;
       if (__popc(bal) <= 2)
@@ -164,6 +175,9 @@ struct LogitsEpilogue {
       else
         list_merge_batch(L, K, key > th ? key : 0ull);
     }
+    // publish an improved bound (the list's K-th key, once the list is full)
+    const uint64_t k_after = L[K - 1];
+    if (gth && lane == 0 && k_after > k_before && k_after > g) atomicMax(gth + c, k_after);
   }
 
   __device__ __forceinline__ void load4(const float* Tb, int j, uint32_t v0, int V, float (&xv)[4],

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
       static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
 
   LogitsEpilogue<N> epi;
-  if (kLogits) epi.init(tail, p.K, p.M);
+  if (kLogits) epi.init(tail, p.K, p.M, p.gth);
   pdl_wait();
   pdl_trigger();
   const int mcols = p.M < N ? p.M : N;  // columns that carry data

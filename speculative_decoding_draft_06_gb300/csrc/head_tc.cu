@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tmap_s);
   }
   LogitsEpilogue<N> epi;
-  if (kLogits && warp < kEpiWarps) epi.init(epi_smem, p.K, p.M);
+  if (kLogits && warp < kEpiWarps) epi.init(epi_smem, p.K, p.M, p.gth);
   __shared__ int epi_go;  // per-tile decision shared by the 4 epilogue warps
   tc_fence_before();
   __syncthreads();

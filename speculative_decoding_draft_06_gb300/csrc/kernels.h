@@ -28,7 +28,9 @@ struct TcParams {
   int K;
   float* pm;           // [rows_max][cta_stride] running max per CTA
   float* ps;           // [rows_max][cta_stride] sum exp(x - max) per CTA
-  uint64_t* ptop;      // [rows_max][list_stride][K] per-warp top-K keys
+  uint64_t* ptop;      // [rows_max][list_stride][K] per-CTA top-K keys
+  unsigned long long* gth;  // [rows_max] per-row global bound of the K-th key (zero
+                            // between launches)
   int cta_stride;
   int list_stride;
   // state epilogue: U = A S_in for the M input rows, then output row q
@@ -96,6 +98,7 @@ struct MergeParams {
   uint64_t* gpl;       // [256][8][32] per-group top-K lists
   float2* gls;         // [256][8] per-group (max, sum-exp)
   int* row_cnt;        // [256] group arrival counters, zero between launches
+  unsigned long long* gth;  // [256] per-row top-K bounds of the head call (reset here)
   const float* pm;
   const float* ps;
   const uint64_t* ptop;

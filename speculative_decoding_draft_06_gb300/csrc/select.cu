@@ -216,7 +216,10 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   __syncthreads();
   if (!last_flag) return;
   __threadfence();
-  if (threadIdx.x == 0) p.row_cnt[row] = 0;
+  if (threadIdx.x == 0) {
+    p.row_cnt[row] = 0;
+    if (p.gth) p.gth[row] = 0ull;  // the head call's bound, ready for the next call
+  }
   v = warp < p.groups ? __ldcg(p.gpl + (static_cast<size_t>(row) * 8 + warp) * 32 + lane) : 0ull;
   v = block_tree_merge(v, wl, p2);
   if (warp == 0) {
