@@ -102,38 +102,62 @@ static __device__ __noinline__ void list_merge_batch(uint64_t* L, int K, uint64_
   __syncwarp();
 }
 
-// Shared-memory footprint of the epilogue (bytes) for N rows and top-K.
-__host__ __device__ constexpr size_t epi_smem_bytes(int N, int K) {
-  return static_cast<size_t>(N) * K * 8            // lists
-         + 2 * 16 * 132 * 4                         // transposed chunk, 2 buffers
-         + static_cast<size_t>(N) * 8;              // running (max, sum) per row
+// Shared-memory footprint of the epilogue (bytes) for N rows, top-K and NG
+// warpgroups.
+__host__ __device__ constexpr size_t epi_smem_bytes(int N, int K, int NG = 1) {
+  return static_cast<size_t>(N) * K * 8                    // lists
+         + static_cast<size_t>(NG) * 2 * 16 * 132 * 4       // transposed chunks, 2 per group
+         + static_cast<size_t>(N) * 8                       // running (max, sum) per row
+         + static_cast<size_t>(N) * 8;                      // per-tile copy of the row bounds
 }
 
-template <int N>
+// NG warpgroups (1 or 2) share the epilogue.  The head rows come in chunks of
+// 16 (one 16-column TMEM load); chunk CH belongs to group CH % NG, which hands
+// it over (one vocabulary entry per thread) and processes it alone, each of
+// its four warps owning 4 of the 16 rows (row c to warp c % 4).  The groups
+// synchronise only within themselves (named barrier 1 + group).
+template <int N, int NG = 1>
 struct LogitsEpilogue {
+  static_assert(NG == 1 || NG == 2, "epilogue warpgroups");
   static constexpr bool kLaneLocal = N <= 64;
-  static constexpr int kSlots = kLaneLocal ? N / 4 : 1;  // rows owned per warp
-  static constexpr int kTPitch = 132;                    // floats per transposed row
+  static constexpr int kChunks = N / 16;
+  static constexpr int kSlots = kLaneLocal ? 4 * ((kChunks + NG - 1) / NG) : 1;
+  static constexpr int kTPitch = 132;  // floats per transposed row
+  static constexpr int kThreads = NG * 128;
   float lm[kSlots], ls[kSlots];
-  uint64_t* lists;  // [N][K], one sorted list per row
+  uint64_t* lists;          // [N][K], one sorted list per row
   unsigned long long* gth;  // [N] global per-row lower bound of the K-th key (or null)
-  float* T;         // [2][16][kTPitch]
-  float2* run;      // [N] (N > 64)
-  int K, M, lane, warp, t;
-  int nchunk;       // chunks handed over so far (selects the T buffer)
+  uint64_t* gcache;         // [N] this tile's copy of gth
+  float* T;                 // [2][16][kTPitch] of this group
+  float2* run;              // [N] (N > 64)
+  int K, M, lane, w4, g, t;
+  int nchunk;               // chunks handed over so far (selects the T buffer)
   bool bad;
+
+  __device__ __forceinline__ void bar() {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+  }
+
+  // Row of this warp's slot s (lane-local path): local chunk s / 4, row s % 4.
+  __device__ __forceinline__ int slot_row(int s) const {
+    return ((s >> 2) * NG + g) * 16 + w4 + 4 * (s & 3);
+  }
 
   __device__ __forceinline__ void init(uint8_t* smem, int K_, int M_,
                                        unsigned long long* gth_ = nullptr) {
     gth = gth_;
     lists = reinterpret_cast<uint64_t*>(smem);
-    T = reinterpret_cast<float*>(lists + static_cast<size_t>(N) * K_);
-    run = reinterpret_cast<float2*>(T + 2 * 16 * kTPitch);
+    float* T0 = reinterpret_cast<float*>(lists + static_cast<size_t>(N) * K_);
+    run = reinterpret_cast<float2*>(T0 + NG * 2 * 16 * kTPitch);
+    gcache = reinterpret_cast<uint64_t*>(run + N);
     K = K_;
     M = M_;
-    t = threadIdx.x & 127;
+    const int tt = threadIdx.x % kThreads;
+    g = tt >> 7;
+    t = tt & 127;
     lane = threadIdx.x & 31;
-    warp = t >> 5;
+    w4 = t >> 5;
+    T = T0 + g * 2 * 16 * kTPitch;
     nchunk = 0;
     bad = false;
 #pragma unroll
@@ -141,25 +165,40 @@ struct LogitsEpilogue {
       lm[i] = -INFINITY;
       ls[i] = 0.f;
     }
-    for (int i = t; i < N * K_; i += 128) lists[i] = 0ull;
-    for (int c = t; c < N; c += 128) run[c] = make_float2(-INFINITY, 0.f);
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int i = tt; i < N * K_; i += kThreads) lists[i] = 0ull;
+    for (int c = tt; c < N; c += kThreads) {
+      run[c] = make_float2(-INFINITY, 0.f);
+      gcache[c] = 0ull;
+    }
+    asm volatile("bar.sync 3, %0;" ::"r"(kThreads) : "memory");
   }
 
-  // Stage x (rows c0..c0+15 of this thread's vocabulary entry) transposed.
+  // At the start of a tile: this warp's rows' global bounds, all loads in
+  // flight together (the list update then reads shared memory only).
+  __device__ __forceinline__ void tile_begin() {
+    if (!gth) return;
+    for (int i = lane;; i += 32) {
+      const int c = ((i >> 2) * NG + g) * 16 + w4 + 4 * (i & 3);
+      if (c >= M) break;
+      gcache[c] = *reinterpret_cast<volatile unsigned long long*>(gth + c);
+    }
+    __syncwarp();
+  }
+
+  // Stage x (rows c0..c0+15 of vocabulary entry t of the tile) transposed.
   __device__ __forceinline__ float* stage(const float (&x)[16]) {
     float* Tb = T + (nchunk & 1) * 16 * kTPitch;
 #pragma unroll
     for (int j = 0; j < 16; ++j) Tb[j * kTPitch + t] = x[j];
     ++nchunk;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    bar();
     return Tb;
   }
 
   // Top-K update of row c with this lane's 4 values (vocabulary v0 + lane + 32 i).
   __device__ __forceinline__ void topk4(int c, const float (&xv)[4], uint32_t v0, int V) {
     uint64_t* L = lists + static_cast<size_t>(c) * K;
-    const uint64_t g = gth ? *reinterpret_cast<volatile unsigned long long*>(gth + c) : 0ull;
+    const uint64_t gb = gcache[c];
     const uint64_t k_before = L[K - 1];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -167,7 +206,7 @@ struct LogitsEpilogue {
       const bool valid = static_cast<int>(v) < V;
       const uint64_t key = (valid && xv[i] == xv[i]) ? make_key(xv[i], v) : 0ull;
       uint64_t th = L[K - 1];
-      th = th > g ? th : g;
+      th = th > gb ? th : gb;
       const unsigned bal = __ballot_sync(kFull, key > th);
       if (bal == 0u) continue;
       if (__popc(bal) <= 2)
@@ -177,7 +216,7 @@ struct LogitsEpilogue {
     }
     // publish an improved bound (the list's K-th key, once the list is full)
     const uint64_t k_after = L[K - 1];
-    if (gth && lane == 0 && k_after > k_before && k_after > g) atomicMax(gth + c, k_after);
+    if (gth && lane == 0 && k_after > k_before && k_after > gb) atomicMax(gth + c, k_after);
   }
 
   __device__ __forceinline__ void load4(const float* Tb, int j, uint32_t v0, int V, float (&xv)[4],
@@ -191,19 +230,20 @@ struct LogitsEpilogue {
     }
   }
 
-  // <= 64 rows: chunk CH (rows 16 CH .. 16 CH + 15) with compile-time slots.
+  // <= 64 rows: chunk CH (rows 16 CH .. 16 CH + 15, a chunk of this group)
+  // with compile-time slots.
   template <int CH>
   __device__ __forceinline__ void chunk_static(const float (&x)[16], uint32_t v0, int V) {
     const float* Tb = stage(x);
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      const int j = warp + 4 * jj;
+      const int j = w4 + 4 * jj;
       const int c = CH * 16 + j;
       if (c >= M) continue;  // uniform across the warp
       float xv[4];
       bool fin[4];
       load4(Tb, j, v0, V, xv, fin);
-      constexpr int kBase = CH * 4;
+      constexpr int kBase = (CH / NG) * 4;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (!fin[i]) continue;
@@ -217,12 +257,12 @@ struct LogitsEpilogue {
     }
   }
 
-  // > 64 rows: chunk starting at row c0 (runtime).
+  // > 64 rows: chunk starting at row c0 (a chunk of this group, runtime).
   __device__ __forceinline__ void chunk_dyn(const float (&x)[16], int c0, uint32_t v0, int V) {
     const float* Tb = stage(x);
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      const int j = warp + 4 * jj;
+      const int j = w4 + 4 * jj;
       const int c = c0 + j;
       if (c >= M) continue;
       float xv[4];
@@ -255,7 +295,7 @@ struct LogitsEpilogue {
     if constexpr (kLaneLocal) {
 #pragma unroll
       for (int s = 0; s < kSlots; ++s) {
-        const int c = (s / 4) * 16 + warp + 4 * (s % 4);
+        const int c = slot_row(s);
         float m = lm[s], sm = ls[s];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -268,17 +308,20 @@ struct LogitsEpilogue {
           ps[(size_t)c * cta_stride + cta] = sm;
         }
       }
-    } else {
-      for (int c = warp; c < M; c += kEpiWarps) {
-        // rows owned by this warp: c % 16 in {warp, warp + 4, ...} -> c % 4 == warp
-        if (lane == 0) {
-          pm[(size_t)c * cta_stride + cta] = run[c].x;
-          ps[(size_t)c * cta_stride + cta] = run[c].y;
-        }
-      }
     }
-    for (int c = warp; c < M; c += kEpiWarps) {
-      if (lane < K) ptop[((size_t)c * list_stride + cta) * K + lane] = lists[(size_t)c * K + lane];
+    for (int c0 = g * 16; c0 < M; c0 += 16 * NG) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int c = c0 + w4 + 4 * jj;
+        if (c >= M) break;
+        if constexpr (!kLaneLocal) {
+          if (lane == 0) {
+            pm[(size_t)c * cta_stride + cta] = run[c].x;
+            ps[(size_t)c * cta_stride + cta] = run[c].y;
+          }
+        }
+        if (lane < K) ptop[((size_t)c * list_stride + cta) * K + lane] = lists[(size_t)c * K + lane];
+      }
     }
     if (bad) atomicOr(err, DT_ERR_NONFINITE);
   }

@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
       }
     };
     if constexpr (kLogits) {
+      epi.tile_begin();
       const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
       if constexpr (N <= 64) {
         static_for<0, N / 16>([&](auto i) {

@@ -17,10 +17,13 @@
 // the fp32 accumulator lives in TMEM (two buffers, so the epilogue of tile i
 // overlaps the MMAs of tile i+1).
 //
-// Warp roles (192 threads): warps 0-3 epilogue (TMEM lane quarter = warp),
-// warp 4 TMA producer, warp 5 TMEM allocator + single-thread MMA issuer.
-// Each CTA owns a contiguous range of 128-row weight tiles (persistent, one
-// CTA per SM).
+// Warp roles: warps 0..4G-1 epilogue (G warpgroups; TMEM lane quarter =
+// warp % 4), warp 4G TMA producer, warp 4G+1 TMEM allocator + single-thread
+// MMA issuer.  The logits kernel for more than 16 head rows runs two epilogue
+// warpgroups, which take alternate 16-row chunks of each accumulator tile, so
+// every SM sub-partition has two epilogue warps to overlap the latency of the
+// top-K updates.  Each CTA owns a contiguous range of 128-row weight tiles
+// (persistent, one CTA per SM).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,6 +42,16 @@ struct TcLayout {
   static constexpr int kBBytes = N * kTileH * 2;       // N rows of 128 B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+};
+
+// Epilogue warpgroups of a kernel variant.
+template <int N, bool kLogits>
+struct TcRoles {
+  static constexpr int kGroups = (kLogits && N > 16) ? 2 : 1;
+  static constexpr int kEpiWarps = 4 * kGroups;
+  static constexpr int kProducer = kEpiWarps;
+  static constexpr int kMma = kEpiWarps + 1;
+  static constexpr int kThreads = 32 * (kEpiWarps + 2);
 };
 
 // Finish 8 output rows q0..q0+7 of hidden unit `row`: u[j] holds U at the
@@ -136,10 +149,11 @@ __device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase
 }
 
 template <int N, bool kLogits>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     k_head_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
               const TcParams p) {
   using L = TcLayout<N>;
+  using R = TcRoles<N, kLogits>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* after = smem + static_cast<size_t>(S) * L::kStageBytes;
   uint8_t* epi_smem = after;  // logits epilogue: lists, transposed chunks, row state
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(after + (kLogits ? epi_smem_bytes(N, p.K) : 0));
+      reinterpret_cast<uint64_t*>(after + (kLogits ? epi_smem_bytes(N, p.K, R::kGroups) : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -188,7 +202,7 @@ __global__ void __launch_bounds__(192, 1)
     return kb_begin + j;
   };
 
-  if (warp == 5) tmem_alloc<L::kTmemCols>(tmem_slot);
+  if (warp == R::kMma) tmem_alloc<L::kTmemCols>(tmem_slot);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -196,19 +210,19 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], R::kEpiWarps);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == R::kProducer && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_s);
   }
-  LogitsEpilogue<N> epi;
-  if (kLogits && warp < kEpiWarps) epi.init(epi_smem, p.K, p.M, p.gth);
-  __shared__ int epi_go;  // per-tile decision shared by the 4 epilogue warps
+  LogitsEpilogue<N, R::kGroups> epi;
+  if (kLogits && warp < R::kEpiWarps) epi.init(epi_smem, p.K, p.M, p.gth);
+  __shared__ int epi_go[2];  // per-tile decision of each epilogue warpgroup
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(192, 1)
   pdl_wait();
   pdl_trigger();
 
-  if (warp == 4) {
+  if (warp == R::kProducer) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
@@ -252,7 +266,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&full[s], par, p.err)) break;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == R::kMma) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_m128<N>();
@@ -299,24 +313,28 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue
-    // The four warps synchronise with named barriers, so they must take every
-    // decision together: one thread waits for the accumulator and broadcasts
-    // whether to go on (a timed-out wait ends all four warps' loops at once).
+    // The warps of a group synchronise with a named barrier, so they must
+    // take every decision together: one thread per group waits for the
+    // accumulator and broadcasts whether to go on (a timed-out wait ends all
+    // four warps' loops at once).  Every group waits for every tile, so each
+    // arrival on tempty belongs to the tile it was meant for.
     int it = 0;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int grp = warp >> 2;
+    const int wq = warp & 3;  // TMEM lane quarter
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = it & 1;
-      if (threadIdx.x == 0) {
+      if ((threadIdx.x & 127) == 0) {
         const bool ok = !*abort_flag &&
                         mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err,
                                   p.wait_limit);
         if (!ok) *abort_flag = 1;
-        epi_go = ok;
+        epi_go[grp] = ok;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (!epi_go) break;
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+      if (!epi_go[grp]) break;
       tc_fence_after();
-      const int row = t * kTileV + warp * 32 + lane;  // vocabulary (or hidden) index
+      const int row = t * kTileV + wq * 32 + lane;  // vocabulary (or hidden) index
       const bool valid = row < p.rows;
       const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(a * N);
       if constexpr (kLogits) {
@@ -335,11 +353,12 @@ __global__ void __launch_bounds__(192, 1)
             x[j] += zv;
           }
         };
+        epi.tile_begin();
         const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
         if constexpr (N <= 64) {
           static_for<0, N / 16>([&](auto i) {
             constexpr int CH = decltype(i)::value;
-            if (CH * 16 < p.M) {  // same for all four warps
+            if (CH % R::kGroups == grp && CH * 16 < p.M) {  // same for the group's warps
               float x[16];
               tmem_ld16(tbase + CH * 16, x);
               add_z(x, CH * 16);
@@ -348,7 +367,7 @@ __global__ void __launch_bounds__(192, 1)
           });
         } else {
           const int c_end = (p.M + 15) & ~15;
-          for (int c0 = 0; c0 < c_end; c0 += 16) {
+          for (int c0 = 16 * grp; c0 < c_end; c0 += 16 * R::kGroups) {
             float x[16];
             tmem_ld16(tbase + c0, x);
             add_z(x, c0);
@@ -369,7 +388,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == R::kMma) {
     tc_fence_after();
     tmem_dealloc<L::kTmemCols>(tmem_base);
   }
@@ -379,7 +398,8 @@ template <int N, bool kLogits>
 static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p,
                                int grid, cudaStream_t st) {
   using L = TcLayout<N>;
-  size_t fixed = 1024 + (kLogits ? epi_smem_bytes(N, p.K) : 0) + 64 * 8 + 64;
+  using R = TcRoles<N, kLogits>;
+  size_t fixed = 1024 + (kLogits ? epi_smem_bytes(N, p.K, R::kGroups) : 0) + 64 * 8 + 64;
   // per-SM shared memory is 228 KB, 1 KB of it reserved per resident CTA,
   // less the kernel's own static shared memory (at most 2 KB)
   auto stages_for = [&](int cps) -> int {
@@ -396,7 +416,7 @@ static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, con
   TcParams q = p;
   q.stages = stages;
   const size_t smem = fixed + static_cast<size_t>(stages) * L::kStageBytes;
-  return launch_kernel(k_head_tc<N, kLogits>, dim3(grid), dim3(192), smem, st, q.pdl != 0, tw, ts,
+  return launch_kernel(k_head_tc<N, kLogits>, dim3(grid), dim3(R::kThreads), smem, st, q.pdl != 0, tw, ts,
                        q);
 }
 
