@@ -63,6 +63,12 @@ def _load():
         lib.orc_pool_size.restype = ctypes.c_int
         lib.orc_build.argtypes = [ctypes.c_int] * 6 + [P] * 21
         lib.orc_build.restype = ctypes.c_int
+        lib.orc_build_ex.argtypes = [ctypes.c_int] * 7 + [P] * 21
+        lib.orc_build_ex.restype = ctypes.c_int
+        lib.orc_cand_row.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int] + [P] * 4
+        lib.orc_cand_row.restype = None
+        lib.orc_bestfirst.argtypes = [ctypes.c_int] * 6 + [f32] + [P] * 21
+        lib.orc_bestfirst.restype = ctypes.c_int
         lib.orc_topb.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_int, f32] + [P] * 7
         lib.orc_topb.restype = ctypes.c_int
         lib.orc_heap_prune.argtypes = [ctypes.c_int, P, P, P, ctypes.c_int, f32, P]
@@ -92,9 +98,11 @@ def pool_size(D: int, W: int, K: int) -> int:
 
 
 def state_step(A, E, s_par, tok: int, bf16: bool) -> np.ndarray:
-    """One head state update q(tanh(A s_par + E[tok])) -> fp32 [H]."""
-    H = A.shape[0]
-    A, E = _weights(A, bf16), _weights(E, bf16)
+    """One head state update q(tanh(A s_par + E[tok])) -> fp32 [H];
+    A=None is the Markov head q(tanh(E[tok]))."""
+    H = E.shape[1]
+    A = None if A is None else _weights(A, bf16)
+    E = _weights(E, bf16)
     s = _c(s_par, np.float32)
     out = np.empty(H, np.float32)
     _load().orc_state_step(H, int(bf16), _ptr(A), _ptr(E), _ptr(s), tok, _ptr(out))
@@ -122,20 +130,39 @@ def topk_row(ell, K: int):
     return tok, val, float(gap[0])
 
 
+def cand_row(z_d, Wout, s, cand, bf16: bool):
+    """Base-candidate head row: the candidates ``cand`` ordered by corrected
+    logit (desc, token asc), their fp32 logits and the log-sum-exp over them."""
+    V, H = Wout.shape
+    z_d, Wout, s = _c(z_d, np.float32), _weights(Wout, bf16), _c(s, np.float32)
+    cand = _c(cand, np.int32)
+    K = cand.shape[0]
+    tok = np.empty(K, np.int32)
+    val = np.empty(K, np.float32)
+    lse = np.zeros(1, np.float64)
+    _load().orc_cand_row(H, int(bf16), _ptr(z_d), _ptr(Wout), _ptr(s), K, _ptr(cand),
+                         _ptr(tok), _ptr(val), _ptr(lse))
+    return tok, val, float(lse[0])
+
+
 def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
-               force_slot=None, force_tok=None, force_state=None) -> dict:
+               force_slot=None, force_tok=None, force_state=None,
+               markov: bool = False, cand_base: bool = False) -> dict:
     """Depth-wise supertree construction for request ``r`` of ``inp``.
 
     ``force_slot`` / ``force_tok`` ([P] each, pool layout) force the kept
     frontier at every depth (teacher forcing); ``force_state`` ([D, W, H]
-    fp32) forces the head states of every depth's rows.  Returns the kept pool, the
-    oracle's own per-depth selection, per-row results and diagnostics.
+    fp32) forces the head states of every depth's rows.  ``markov`` uses the
+    Markov head (A ignored); ``cand_base`` takes the candidates from the base
+    logits.  Returns the kept pool, the oracle's own per-depth selection,
+    per-row results and diagnostics.
     """
     z = _c(inp["z"][r, :D], np.float32)
     V = z.shape[1]
-    H = inp["A"].shape[0]
+    H = inp["E"].shape[1]
     s0 = _c(inp["state0"][r], np.float32)
-    A, E, Wo = (_weights(inp[k], bf16) for k in ("A", "E", "Wout"))
+    A = None if markov else _weights(inp["A"], bf16)
+    E, Wo = (_weights(inp[k], bf16) for k in ("E", "Wout"))
     P = pool_size(D, W, K)
     o = {k: np.empty(P, np.int32) for k in
          ("pool_parent", "pool_token", "pool_depth", "own_slot", "own_tok")}
@@ -151,8 +178,8 @@ def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
     if force_slot is not None:
         fs, ft = _c(force_slot, np.int32), _c(force_tok, np.int32)
     fst = None if force_state is None else _c(force_state, np.float32)
-    rc = _load().orc_build(
-        V, H, D, W, K, int(bf16), _ptr(z), _ptr(s0), _ptr(A), _ptr(E), _ptr(Wo),
+    rc = _load().orc_build_ex(
+        V, H, D, W, K, int(bf16), int(cand_base), _ptr(z), _ptr(s0), _ptr(A), _ptr(E), _ptr(Wo),
         _ptr(fs), _ptr(ft), _ptr(fst),
         _ptr(o["pool_parent"]), _ptr(o["pool_token"]), _ptr(o["pool_depth"]),
         _ptr(o["pool_score"]), _ptr(o["own_slot"]), _ptr(o["own_tok"]),
@@ -160,7 +187,7 @@ def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
         _ptr(o["row_tok"]), _ptr(o["row_logp"]), _ptr(o["row_kgap"]),
         _ptr(o["w_cut"]), _ptr(calls))
     if rc != ORC_OK:
-        raise RuntimeError(f"orc_build failed with code {rc}")
+        raise RuntimeError(f"orc_build_ex failed with code {rc}")
     o["row_lse"] = o["row_lse"].reshape(D, W)
     o["row_tok"] = o["row_tok"].reshape(D, W, K)
     o["row_logp"] = o["row_logp"].reshape(D, W, K)
@@ -209,3 +236,43 @@ def build_request(inp: dict, r: int, D: int, W: int, K: int, B: int,
     t["tree"] = topb(t["pool_parent"], t["pool_token"], t["pool_depth"],
                      t["pool_score"], B, beta)
     return t
+
+
+def bestfirst(inp: dict, r: int, D: int, K: int, B: int, beta: float, bf16: bool,
+              markov: bool = False, force_tok=None, force_logp=None,
+              force_state=None) -> dict:
+    """Sequential best-first build (one head call per expanded node) for
+    request ``r``: the tree in pop order plus per-call diagnostics.
+    ``force_tok`` / ``force_logp`` ([B, K]) replace each call's children,
+    ``force_state`` ([B, H]) each call's state (teacher forcing)."""
+    z = _c(inp["z"][r, :D], np.float32)
+    V = z.shape[1]
+    H = inp["E"].shape[1]
+    s0 = _c(inp["state0"][r], np.float32)
+    A = None if markov else _weights(inp["A"], bf16)
+    E, Wo = (_weights(inp[k], bf16) for k in ("E", "Wout"))
+    words = (B + 31) // 32
+    o = {"parent": np.empty(B, np.int32), "token": np.empty(B, np.int32),
+         "depth": np.empty(B, np.int32), "score": np.empty(B, np.float32),
+         "mask": np.empty(B * words, np.uint32), "call_rank": np.empty(B, np.int32),
+         "call_state": np.zeros((B, H), np.float32),
+         "row_lse": np.full(B, np.nan, np.float64), "row_tok": np.full((B, K), -1, np.int32),
+         "row_logp": np.full((B, K), np.nan, np.float32),
+         "row_kgap": np.full(B, np.nan, np.float32)}
+    n = np.zeros(1, np.int32)
+    calls = np.zeros(1, np.int64)
+    ft = None if force_tok is None else _c(force_tok, np.int32)
+    fl = None if force_logp is None else _c(force_logp, np.float32)
+    fs = None if force_state is None else _c(force_state, np.float32)
+    rc = _load().orc_bestfirst(
+        V, H, D, K, B, int(bf16), ctypes.c_float(beta), _ptr(z), _ptr(s0), _ptr(A), _ptr(E),
+        _ptr(Wo), _ptr(ft), _ptr(fl), _ptr(fs), _ptr(o["parent"]), _ptr(o["token"]),
+        _ptr(o["depth"]), _ptr(o["score"]), _ptr(o["mask"]), _ptr(n), _ptr(o["call_rank"]),
+        _ptr(o["call_state"]), _ptr(o["row_lse"]), _ptr(o["row_tok"]), _ptr(o["row_logp"]),
+        _ptr(o["row_kgap"]), _ptr(calls))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_bestfirst failed with code {rc}")
+    o["n_out"] = int(n[0])
+    o["calls"] = int(calls[0])
+    o["mask"] = o["mask"].reshape(B, words)
+    return o

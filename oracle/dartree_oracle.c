@@ -99,13 +99,18 @@ static int better(float va, int64_t ia, float vb, int64_t ib) {
 /* State after committing token tok on top of the parent's state:
  * s_out[h] = q( tanh( sum_j A[h,j] s_par[j] + E[tok,h] ) ).
  * [P2] Methodologie 1 ("carries their correction states forward"),
- * [P3] Summary ("updates their states"). */
+ * [P3] Summary ("updates their states").
+ * A == NULL is the Markov head: the state is a function of the last token
+ * alone, s_out[h] = q(tanh(E[tok,h])) -- the A = 0 case of the same form.
+ * [P2] Experimentele Resultaten, Ablatie (Generaliseerbaarheid: the DSpark
+ * drafter with a Markov correction head). */
 void orc_state_step(int H, int bf16, const void *A, const void *E,
                     const float *s_par, int32_t tok, float *s_out) {
     for (int h = 0; h < H; ++h) {
         double u = 0.0;
-        for (int j = 0; j < H; ++j)
-            u += weight(A, bf16, (size_t)h * H + j) * (double)s_par[j];
+        if (A)
+            for (int j = 0; j < H; ++j)
+                u += weight(A, bf16, (size_t)h * H + j) * (double)s_par[j];
         u += weight(E, bf16, (size_t)tok * H + h);
         s_out[h] = qstate(bf16, (float)tanh(u));
     }
@@ -166,6 +171,40 @@ void orc_topk_row(int V, const float *ell, int K, int32_t *tok, float *val,
     *gap = (next_tok < 0) ? INFINITY : val[K - 1] - next;
 }
 
+/* Base-logit candidate variant of one head row.  The K candidates ctok are
+ * the top-K of the base logits z_d (shared by every branch); the row's
+ * corrected logits are evaluated at those tokens only,
+ *   e_j = fp32( z_d[c_j] + sum_h s[h] Wout[c_j,h] ),
+ * and normalised over the K candidates: lse = m + log sum_j exp(e_j - m).
+ * Output: the K candidates ordered by (e desc, token asc) in tok/val.
+ * [P2] Methodologie 1 (Kandidaat Selectie: top-K candidate tokens from the
+ * base logits at every depth; Gebatchte Correctie: the correction head
+ * evaluates those candidates for all branches in one batch). */
+void orc_cand_row(int H, int bf16, const float *z_d, const void *Wout,
+                  const float *s, int K, const int32_t *ctok, int32_t *tok,
+                  float *val, double *lse) {
+    for (int j = 0; j < K; ++j) {                 /* insertion by (e, token) */
+        int32_t c = ctok[j];
+        double acc = (double)z_d[c];
+        for (int h = 0; h < H; ++h)
+            acc += (double)s[h] * weight(Wout, bf16, (size_t)c * H + h);
+        float e = (float)acc;
+        int p = j;
+        while (p > 0 && better(e, c, val[p - 1], tok[p - 1])) {
+            val[p] = val[p - 1];
+            tok[p] = tok[p - 1];
+            --p;
+        }
+        val[p] = e;
+        tok[p] = c;
+    }
+    double m = (double)val[0];
+    if (m == -INFINITY) { *lse = -INFINITY; return; }
+    double sum = 0.0;
+    for (int j = 0; j < K; ++j) sum += exp((double)val[j] - m);
+    *lse = m + log(sum);
+}
+
 /* --------------------------------------------------------- construction */
 
 typedef struct { float c; int32_t idx; } cand_t;
@@ -201,6 +240,10 @@ int orc_pool_size(int D, int W, int K) {
  *
  * Inputs: z [D,V] fp32, state0 [H] fp32, A [H,H], E [V,H], Wout [V,H]
  * (bf16 bits or fp32).  Depth 1 has |F_1| = min(W, K) nodes.
+ * A == NULL selects the Markov head (see orc_state_step).  cand_base != 0
+ * takes each depth's candidates from the base logits (orc_cand_row); the
+ * row gap reported is then the base logits' K/K+1 gap, which alone decides
+ * the candidate set.
  *
  * Teacher forcing: when force_slot/force_tok are given ([P] each, laid out
  * like the pool), the frontier kept at each depth is the forced one (parent
@@ -221,17 +264,17 @@ int orc_pool_size(int D, int W, int K) {
  *   w_cut [2*D]: own W-th and (W+1)-th candidate score (-inf if none).
  *   calls: number of batched head calls made (== D).
  */
-int orc_build(int V, int H, int D, int W, int K, int bf16,
-              const float *z, const float *state0,
-              const void *A, const void *E, const void *Wout,
-              const int32_t *force_slot, const int32_t *force_tok,
-              const float *force_state,
-              int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
-              float *pool_score,
-              int32_t *own_slot, int32_t *own_tok, float *own_score,
-              float *force_margin,
-              double *row_lse, int32_t *row_tok, float *row_logp,
-              float *row_kgap, float *w_cut, int64_t *calls) {
+int orc_build_ex(int V, int H, int D, int W, int K, int bf16, int cand_base,
+                 const float *z, const float *state0,
+                 const void *A, const void *E, const void *Wout,
+                 const int32_t *force_slot, const int32_t *force_tok,
+                 const float *force_state,
+                 int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
+                 float *pool_score,
+                 int32_t *own_slot, int32_t *own_tok, float *own_score,
+                 float *force_margin,
+                 double *row_lse, int32_t *row_tok, float *row_logp,
+                 float *row_kgap, float *w_cut, int64_t *calls) {
     if (V < 1 || H < 1 || D < 1 || W < 1 || K < 1 || K > V) return ORC_ERR_ARG;
     int rc = ORC_OK;
     float *st = malloc(sizeof(float) * (size_t)W * H);      /* row states */
@@ -245,8 +288,10 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
     float *kth = malloc(sizeof(float) * (size_t)W);          /* K-th logit */
     int32_t *tk = malloc(sizeof(int32_t) * (size_t)K);
     float *tv = malloc(sizeof(float) * (size_t)K);
+    int32_t *ctok = malloc(sizeof(int32_t) * (size_t)K);    /* base candidates */
+    float *cval = malloc(sizeof(float) * (size_t)K);
     if (!st || !st_next || !ell || !score || !sel_slot || !sel_tok ||
-        !sel_score || !cand || !kth || !tk || !tv) {
+        !sel_score || !cand || !kth || !tk || !tv || !ctok || !cval) {
         rc = ORC_ERR_MEM;
         goto done;
     }
@@ -261,14 +306,22 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
         int fd = (K * fp < W) ? K * fp : W;
         if (force_state)
             memcpy(st, force_state + (size_t)(d - 1) * W * H, sizeof(float) * (size_t)fp * H);
+        float zgap = 0.0f;
+        if (cand_base) orc_topk_row(V, zd, K, ctok, cval, &zgap);
         /* one batched head call over every frontier row */
         *calls += 1;
         for (int i = 0; i < fp; ++i) {
             double lse;
             float kgap;
-            orc_logits_row(V, H, bf16, zd, Wout, st + (size_t)i * H,
-                           ell + (size_t)i * V, &lse);
-            orc_topk_row(V, ell + (size_t)i * V, K, tk, tv, &kgap);
+            if (cand_base) {
+                orc_cand_row(H, bf16, zd, Wout, st + (size_t)i * H, K, ctok, tk, tv, &lse);
+                for (int j = 0; j < K; ++j) ell[(size_t)i * V + tk[j]] = tv[j];
+                kgap = zgap;     /* the candidate set is decided by z alone */
+            } else {
+                orc_logits_row(V, H, bf16, zd, Wout, st + (size_t)i * H,
+                               ell + (size_t)i * V, &lse);
+                orc_topk_row(V, ell + (size_t)i * V, K, tk, tv, &kgap);
+            }
             size_t r = (size_t)(d - 1) * W + i;
             row_lse[r] = lse;
             row_kgap[r] = kgap;
@@ -304,10 +357,15 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
                     goto done;
                 }
                 size_t r = (size_t)(d - 1) * W + slot;
+                if (cand_base) {              /* only a candidate can be kept */
+                    int in = 0;
+                    for (int j = 0; j < K; ++j) in |= (ctok[j] == tok);
+                    if (!in) { rc = ORC_ERR_ARG; goto done; }
+                }
                 float e = ell[(size_t)slot * V + tok];
                 float logp = (float)((double)e - row_lse[r]);
                 sel_score[q] = score[slot] + logp;
-                force_margin[off + q] = e - kth[slot];
+                force_margin[off + q] = cand_base ? 0.0f : e - kth[slot];
             } else {
                 slot = own_slot[off + q];
                 tok = own_tok[off + q];
@@ -337,7 +395,28 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
 done:
     free(st); free(st_next); free(ell); free(score); free(sel_slot);
     free(sel_tok); free(sel_score); free(cand); free(kth); free(tk); free(tv);
+    free(ctok); free(cval);
     return rc;
+}
+
+/* The construction with the candidates of [P1] (top-K of each branch's
+ * corrected distribution over the whole vocabulary). */
+int orc_build(int V, int H, int D, int W, int K, int bf16,
+              const float *z, const float *state0,
+              const void *A, const void *E, const void *Wout,
+              const int32_t *force_slot, const int32_t *force_tok,
+              const float *force_state,
+              int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
+              float *pool_score,
+              int32_t *own_slot, int32_t *own_tok, float *own_score,
+              float *force_margin,
+              double *row_lse, int32_t *row_tok, float *row_logp,
+              float *row_kgap, float *w_cut, int64_t *calls) {
+    return orc_build_ex(V, H, D, W, K, bf16, 0, z, state0, A, E, Wout,
+                        force_slot, force_tok, force_state, pool_parent,
+                        pool_token, pool_depth, pool_score, own_slot, own_tok,
+                        own_score, force_margin, row_lse, row_tok, row_logp,
+                        row_kgap, w_cut, calls);
 }
 
 /* ------------------------------------------------------ deferred pruning */
@@ -478,4 +557,157 @@ int orc_heap_prune(int P, const int32_t *pool_parent, const int32_t *pool_depth,
 #undef ORC_PUSH
     free(heap);
     return pops;
+}
+
+/* ------------------------------------------- sequential best-first build */
+
+/*
+ * Node-by-node best-first construction with one head call per expanded
+ * node: the sequential baseline that DARTree's depth-wise batching replaces.
+ * [P2] Probleemstelling (Causale Correctie: a standard best-first build with
+ * a max-heap makes the correction head run node by node -- pop one node,
+ * correct it, push its children, and only then expand the next) and
+ * Experimentele Resultaten, Ablatie (latency of the sequential heap build);
+ * [P1] Core Mechanism (the expansion by top-k children and the scores).
+ *
+ * Nodes get ids in order of creation.  Head call 0 expands the root (state
+ * q(state0), score 0, children at depth 1 from z_1).  Then for rank
+ * q = 0 .. B-1: pop the best node under (key desc, id asc), key = score +
+ * beta*depth (the orc_topb key); it becomes output rank q.  If q + 1 < B and
+ * its depth d < D, head call q + 1 expands it: its state is the state step
+ * of its parent's state (the root's for depth 1) with its token, the call
+ * scores its children at depth d + 1 (z_{d+1}), and its top-K children are
+ * created in rank order with score = node score + logp (one fp32 add);
+ * otherwise call q + 1 is not made.  Stops early when no node is left.
+ *
+ * Children come from the corrected top-K as in orc_build.  Teacher forcing:
+ * force_tok/force_logp ([B][K], by call) replace the children of each call
+ * (the call's own row is still computed and reported); force_state ([B][H],
+ * by call) replaces the state the call is made with.
+ *
+ * Outputs: the tree in pop order (parent rank, -1 at depth 1; token; depth;
+ * score; ancestor mask as in orc_topb), n_out, call_rank[B] (rank expanded
+ * by each call, -1 for the root, -2 if the call was not made), the call
+ * states call_state[B][H], per-call rows (row_lse [B], row_tok/row_logp
+ * [B][K], row_kgap [B]) and calls = head calls made.
+ */
+int orc_bestfirst(int V, int H, int D, int K, int B, int bf16, float beta,
+                  const float *z, const float *state0,
+                  const void *A, const void *E, const void *Wout,
+                  const int32_t *force_tok, const float *force_logp,
+                  const float *force_state,
+                  int32_t *out_parent, int32_t *out_token, int32_t *out_depth,
+                  float *out_score, uint32_t *out_mask, int32_t *n_out,
+                  int32_t *call_rank, float *call_state,
+                  double *row_lse, int32_t *row_tok, float *row_logp,
+                  float *row_kgap, int64_t *calls) {
+    if (V < 1 || H < 1 || D < 1 || K < 1 || K > V || B < 1) return ORC_ERR_ARG;
+    int rc = ORC_OK;
+    const int words = (B + 31) / 32;
+    const int max_nodes = B * K;
+    int32_t *n_par = malloc(sizeof(int32_t) * (size_t)max_nodes);   /* parent id */
+    int32_t *n_tok = malloc(sizeof(int32_t) * (size_t)max_nodes);
+    int32_t *n_dep = malloc(sizeof(int32_t) * (size_t)max_nodes);
+    float *n_score = malloc(sizeof(float) * (size_t)max_nodes);
+    int32_t *n_rank = malloc(sizeof(int32_t) * (size_t)max_nodes);  /* -1: not popped */
+    key_t_ *heap = malloc(sizeof(key_t_) * (size_t)max_nodes);
+    float *s_root = malloc(sizeof(float) * (size_t)H);
+    float *s_rank = malloc(sizeof(float) * (size_t)B * H);           /* state per rank */
+    float *ell = malloc(sizeof(float) * (size_t)V);
+    int32_t *tk = malloc(sizeof(int32_t) * (size_t)K);
+    float *tv = malloc(sizeof(float) * (size_t)K);
+    if (!n_par || !n_tok || !n_dep || !n_score || !n_rank || !heap || !s_root ||
+        !s_rank || !ell || !tk || !tv) {
+        rc = ORC_ERR_MEM;
+        goto done;
+    }
+    for (int h = 0; h < H; ++h) s_root[h] = qstate(bf16, state0[h]);
+    for (int c = 0; c < B; ++c) call_rank[c] = -2;
+    memset(out_mask, 0, sizeof(uint32_t) * (size_t)B * words);
+    for (int q = 0; q < B; ++q) {
+        out_parent[q] = -1; out_token[q] = -1; out_depth[q] = 0; out_score[q] = 0.0f;
+    }
+    *calls = 0;
+    int n_nodes = 0, hn = 0, pops = 0;
+    int expand = -1;                 /* node expanded by the next call: -1 = root */
+    for (int c = 0; c < B; ++c) {
+        if (expand >= -1) {
+            /* ---- head call c expands the root (c = 0) or rank c-1 */
+            int dep = (expand < 0) ? 0 : n_dep[expand];
+            float sc = (expand < 0) ? 0.0f : n_score[expand];
+            float *s = call_state + (size_t)c * H;
+            if (expand < 0) {
+                memcpy(s, s_root, sizeof(float) * (size_t)H);
+            } else {
+                int p = n_par[expand];
+                const float *sp = (p < 0) ? s_root : s_rank + (size_t)n_rank[p] * H;
+                orc_state_step(H, bf16, A, E, sp, n_tok[expand], s);
+            }
+            if (force_state) memcpy(s, force_state + (size_t)c * H, sizeof(float) * (size_t)H);
+            if (expand >= 0) memcpy(s_rank + (size_t)n_rank[expand] * H, s, sizeof(float) * (size_t)H);
+            call_rank[c] = (expand < 0) ? -1 : n_rank[expand];
+            *calls += 1;
+            double lse;
+            float kgap;
+            orc_logits_row(V, H, bf16, z + (size_t)dep * V, Wout, s, ell, &lse);
+            orc_topk_row(V, ell, K, tk, tv, &kgap);
+            row_lse[c] = lse;
+            row_kgap[c] = kgap;
+            for (int j = 0; j < K; ++j) {
+                row_tok[(size_t)c * K + j] = tk[j];
+                row_logp[(size_t)c * K + j] = (float)((double)tv[j] - lse);
+            }
+            /* ---- its children enter the heap, ids in rank order */
+            for (int j = 0; j < K; ++j) {
+                int id = n_nodes++;
+                n_par[id] = expand;
+                n_tok[id] = force_tok ? force_tok[(size_t)c * K + j] : row_tok[(size_t)c * K + j];
+                float lp = force_logp ? force_logp[(size_t)c * K + j] : row_logp[(size_t)c * K + j];
+                n_dep[id] = dep + 1;
+                n_score[id] = sc + lp;                   /* one fp32 add */
+                n_rank[id] = -1;
+                key_t_ e = { prune_key(n_score[id], n_dep[id], beta), id };
+                int i = hn++;                            /* sift up */
+                while (i > 0) {
+                    int pi = (i - 1) / 2;
+                    if (!better(e.key, e.idx, heap[pi].key, heap[pi].idx)) break;
+                    heap[i] = heap[pi];
+                    i = pi;
+                }
+                heap[i] = e;
+            }
+        }
+        /* ---- pop rank c */
+        expand = -2;
+        if (hn == 0) break;
+        key_t_ top = heap[0];
+        key_t_ last = heap[--hn];
+        int i = 0;
+        for (;;) {                                       /* sift down */
+            int l = 2 * i + 1, r = l + 1, b = i;
+            key_t_ bv = last;
+            if (l < hn && better(heap[l].key, heap[l].idx, bv.key, bv.idx)) { b = l; bv = heap[l]; }
+            if (r < hn && better(heap[r].key, heap[r].idx, bv.key, bv.idx)) { b = r; bv = heap[r]; }
+            if (b == i) break;
+            heap[i] = heap[b];
+            i = b;
+        }
+        if (hn > 0) heap[i] = last;
+        int m = top.idx, q = pops++;
+        n_rank[m] = q;
+        int pr = (n_par[m] < 0) ? -1 : n_rank[n_par[m]];
+        out_parent[q] = pr;
+        out_token[q] = n_tok[m];
+        out_depth[q] = n_dep[m];
+        out_score[q] = n_score[m];
+        uint32_t *row = out_mask + (size_t)q * words;
+        if (pr >= 0) memcpy(row, out_mask + (size_t)pr * words, sizeof(uint32_t) * (size_t)words);
+        row[q / 32] |= 1u << (q % 32);
+        if (n_dep[m] < D) expand = m;                    /* call c+1 expands it */
+    }
+    *n_out = pops;
+done:
+    free(n_par); free(n_tok); free(n_dep); free(n_score); free(n_rank);
+    free(heap); free(s_root); free(s_rank); free(ell); free(tk); free(tv);
+    return rc;
 }

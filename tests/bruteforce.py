@@ -30,11 +30,12 @@ def weights_f64(w: np.ndarray, bf16: bool) -> np.ndarray:
 class Head:
     """The synthetic correction head, evaluated one path at a time."""
 
-    def __init__(self, inp: dict, r: int, bf16: bool):
+    def __init__(self, inp: dict, r: int, bf16: bool, markov: bool = False):
         self.bf16 = bf16
         self.z = inp["z"][r].astype(np.float64)
         self.s0 = inp["state0"][r]
-        self.A = weights_f64(inp["A"], bf16)
+        # the Markov head is the A = 0 case of the recurrence
+        self.A = np.zeros(inp["A"].shape) if markov else weights_f64(inp["A"], bf16)
         self.E = weights_f64(inp["E"], bf16)
         self.Wout = weights_f64(inp["Wout"], bf16)
 
@@ -58,15 +59,29 @@ class Head:
         order = np.argsort(-ell.astype(np.float64), kind="stable")[:K]
         return [(int(t), np.float32(np.float64(ell[t]) - lse)) for t in order]
 
+    def children_base(self, s: np.ndarray, d: int, K: int):
+        """Base-logit candidates: the top-K tokens of z_d, scored by the
+        corrected logits at those tokens and normalised over the K; ordered
+        by (corrected logit desc, token asc)."""
+        z = self.z[d - 1]
+        cand = np.argsort(-z, kind="stable")[:K]
+        ell = (z[cand] + self.Wout[cand] @ s.astype(np.float64)).astype(np.float32)
+        e = ell.astype(np.float64)
+        lse = e.max() + np.log(np.exp(e - e.max()).sum())
+        order = sorted(range(K), key=lambda j: (-float(ell[j]), int(cand[j])))
+        return [(int(cand[j]), np.float32(e[j] - lse)) for j in order]
 
-def enumerate_tree(head: Head, D: int, K: int) -> list[dict]:
-    """Every path of length 1..D through top-K children, with its score."""
+
+def enumerate_tree(head: Head, D: int, K: int, base: bool = False) -> list[dict]:
+    """Every path of length 1..D through top-K children, with its score
+    (children from the base-logit candidates when ``base``)."""
     out = []
+    children = head.children_base if base else head.children
 
     def rec(path, state, score, d):
         if d > D:
             return
-        for tok, logp in head.children(state, d, K):
+        for tok, logp in children(state, d, K):
             sc = np.float32(score + logp)
             p = path + (tok,)
             out.append({"path": p, "score": float(sc), "depth": d})
