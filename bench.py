@@ -8,6 +8,11 @@ one JSON line (rank 0).
 
   python bench.py [--config q8b] [--steps K] [--warmup W] [--gpus N]
   python bench.py --impl reference ...    # the CPU oracle, timed as stated
+  python bench.py --variant markov|base|bestfirst ...   # a build variant
+
+The default line is the depth-wise DARTree build; --variant measures one of
+the build variants (Markov correction head, base-logit candidates, the
+sequential best-first baseline) on the same workload.
 """
 from __future__ import annotations
 
@@ -50,32 +55,69 @@ def parse_args(argv=None):
                          "top-K) of the workload's widest depth and exit")
     ap.add_argument("--vocab", type=int, default=0,
                     help="override V (profiling aid for small ncu captures)")
+    ap.add_argument("--variant", choices=sorted(VARIANTS), default="dartree")
     return ap.parse_args(argv)
+
+
+# build variants: options of DARTree.build
+VARIANTS = {
+    "dartree": {},
+    "markov": {"head": "markov"},
+    "base": {"candidates": "base"},
+    "markov-base": {"head": "markov", "candidates": "base"},
+    "bestfirst": {"expansion": "bestfirst"},
+}
 
 
 # ------------------------------------------------------------- bookkeeping
 
-def head_bytes_per_launch(w: I.Workload) -> float:
-    """Algorithmic bytes of one head call, averaged over the D calls:
-    the output projection once, the base logits of every request and the
-    head-row states (weights bf16/fp32, logits fp32)."""
-    wb = 2 if w.bf16 else 4
-    rows = w.head_rows()
-    per = [w.V * w.H * wb + w.R * w.V * 4 + m * w.H * wb for m in rows]
-    return sum(per) / len(per)
-
-
-def build_bytes(w: I.Workload) -> float:
+def build_bytes(w: I.Workload, variant: str = "dartree") -> float:
     """Algorithmic bytes of one build: D output projections, D-1 state
-    matrices, the gathered embedding rows and all base logits."""
+    matrices, the gathered embedding rows and all base logits (per variant:
+    no state matrix for the Markov head; K gathered Wout rows per request
+    instead of the projection for base candidates; B head calls of one row
+    per request for best-first)."""
     wb = 2 if w.bf16 else 4
     rows = w.head_rows()
-    return (w.D * w.V * w.H * wb + (w.D - 1) * w.H * w.H * wb + sum(rows[1:]) * w.H * wb
-            + w.R * w.D * w.V * 4)
+    opt = VARIANTS[variant]
+    if opt.get("expansion") == "bestfirst":
+        return (w.B * (w.V * w.H * wb + w.R * w.V * 4 + w.R * w.H * wb)
+                + (w.B - 1) * (w.H * w.H * wb + 2 * w.R * w.H * wb))
+    state = 0 if opt.get("head") == "markov" else (w.D - 1) * w.H * w.H * wb
+    gathered = sum(rows[1:]) * w.H * wb
+    if opt.get("candidates") == "base":
+        return (w.D * (w.R * w.K * w.H * wb + max(rows) * w.H * wb) + state + gathered
+                + w.R * w.D * w.V * 4)
+    return w.D * w.V * w.H * wb + state + gathered + w.R * w.D * w.V * 4
 
 
-def kernels_per_build(w: I.Workload) -> int:
-    return 1 + w.D * 2 + (w.D - 1) + 1      # root, head + merge/select per depth, states, prune
+def kernel_bytes_per_launch(w: I.Workload, variant: str, kind: str) -> float | None:
+    """Algorithmic bytes of one launch of kernel kind `kind` (averaged over a
+    build's launches of that kind), or None where no byte count bounds it."""
+    wb = 2 if w.bf16 else 4
+    opt = VARIANTS[variant]
+    rows = [w.R] * w.B if opt.get("expansion") == "bestfirst" else w.head_rows()
+    if kind == "head":
+        if opt.get("candidates") == "base":
+            per = [w.R * w.K * w.H * wb + m * w.H * wb + w.R * w.K * 4 for m in rows]
+        else:
+            per = [w.V * w.H * wb + w.R * w.V * 4 + m * w.H * wb for m in rows]
+        return sum(per) / len(per)
+    if kind == "state":
+        per = [2 * m * w.H * wb + (0 if opt.get("head") == "markov" else w.H * w.H * wb)
+               for m in rows[1:]]
+        return sum(per) / len(per) if per else None
+    if kind == "candidates":
+        return w.R * w.D * w.V * 4
+    return None
+
+
+def kernels_per_build(w: I.Workload, variant: str = "dartree") -> int:
+    opt = VARIANTS[variant]
+    if opt.get("expansion") == "bestfirst":      # root, init, B x (head, merge, step), states
+        return 2 + 3 * w.B + (w.B - 1)
+    base = 1 if opt.get("candidates") == "base" else 0
+    return 1 + base + w.D * 2 + (w.D - 1) + 1  # root, head + merge/select, states, prune
 
 
 def kernel_source_hash() -> str:
@@ -186,16 +228,36 @@ class ClockSampler:
 
 # -------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0) -> dict:
+def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0,
+                  variant: str = "dartree") -> dict:
     """Time the CPU oracle on a bounded sample of one request's build and
     scale to a full build by head rows (the dominant cost is one V x H fp64
     pass per head row).  The sample is the first depths of the build when at
     least one head row fits in budget_s, else one head row restricted to a
-    vocabulary slice, scaled by V / slice."""
+    vocabulary slice, scaled by V / slice.  Best-first: one head row per
+    call, B calls.  Base candidates: the first depths of the variant's own
+    oracle build, scaled by depths."""
     import numpy as np
 
     import oracle
-    rows = [m // w.R for m in w.head_rows()]       # head rows per request per depth
+    opt = VARIANTS[variant]
+    markov = opt.get("head") == "markov"
+    if opt.get("candidates") == "base":
+        d_s, t = 0, 0.0
+        while d_s < w.D and t * (d_s + 1) / max(1, d_s) <= budget_s:
+            d_s += 1
+            t0 = time.perf_counter()
+            oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16, markov=markov,
+                              cand_base=True)
+            t = time.perf_counter() - t0
+        per_build = t * w.D / d_s
+        return {"builds_per_s": 1.0 / per_build, "seconds": t,
+                "sample": (f"oracle (fp64, 1 thread), base-candidate build of depths 1..{d_s} "
+                           f"of request {request} ({t:.2f} s), scaled by depths")}
+    if opt.get("expansion") == "bestfirst":
+        rows = [1] * w.B
+    else:
+        rows = [m // w.R for m in w.head_rows()]   # head rows per request per depth
     total_rows = sum(rows)
     s0 = inp["state0"][request]
     vs = min(w.V, 4096)
@@ -212,12 +274,22 @@ def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0) -
                 "sample": (f"oracle (fp64, 1 thread): one head row over {vs} of {w.V} "
                            f"vocabulary entries ({t:.2f} s), scaled by V/{vs} and "
                            f"{total_rows} head rows per build")}
+    if opt.get("expansion") == "bestfirst":
+        n = max(1, min(w.B, int(budget_s / t_row)))
+        t0 = time.perf_counter()
+        o = oracle.bestfirst(inp, request, w.D, w.K, n, w.beta, w.bf16, markov=markov)
+        t = time.perf_counter() - t0
+        per_build = t * w.B / o["calls"]
+        return {"builds_per_s": 1.0 / per_build, "seconds": t,
+                "sample": (f"oracle (fp64, 1 thread): best-first build with budget {n} of "
+                           f"request {request} ({o['calls']} head calls, {t:.1f} s), scaled "
+                           f"to {w.B} calls")}
     d_s, acc = 1, rows[0]
     while d_s < w.D and (acc + rows[d_s]) * t_row <= budget_s:
         acc += rows[d_s]
         d_s += 1
     t0 = time.perf_counter()
-    oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16)
+    oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16, markov=markov)
     t = time.perf_counter() - t0
     per_build = t * total_rows / acc
     return {"builds_per_s": 1.0 / per_build, "seconds": t,
@@ -235,8 +307,8 @@ def run_reference(args) -> None:
     inp = I.make_inputs(w)
     budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(w, inp, budget)
-    vals = [oracle_sample(w, inp, budget) for _ in range(args.steps)]
+        oracle_sample(w, inp, budget, variant=args.variant)
+    vals = [oracle_sample(w, inp, budget, variant=args.variant) for _ in range(args.steps)]
     per_build = statistics.mean(1.0 / v["builds_per_s"] for v in vals)
     value = 1.0 / per_build
     line = {
@@ -244,7 +316,7 @@ def run_reference(args) -> None:
         "unit": "builds/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_build * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w), "variant": args.variant,
         "cpu_baseline": {"value": value, "unit": "builds/s", "cores": 1, "kind": "oracle",
                          "sample": vals[-1]["sample"]},
         "e2e": {"value": value, "unit": "builds/s", "h2d_bytes_per_step": 0,
@@ -288,7 +360,8 @@ def run_gpu(args) -> None:
                       max_requests=w.R, bf16=w.bf16)
     stream = torch.cuda.Stream()
     out = ctx.alloc_tree(w.R, w.B)
-    kw = dict(D=w.D, W=w.W, K=w.K, B=w.B, beta=w.beta, out=out, stream=stream)
+    opt = VARIANTS[args.variant]
+    kw = dict(D=w.D, W=w.W, K=w.K, B=w.B, beta=w.beta, out=out, stream=stream, **opt)
     args_t = (dev["z"], dev["state0"], dev["A"], dev["E"], dev["Wout"])
 
     def barrier():
@@ -327,16 +400,56 @@ def run_gpu(args) -> None:
         ctx.sync(stream)
     kt = ctx.timing()
     ctx.set_timing(False)
-    head_ms, head_n = kt["head"]
-    head_avg_ms = head_ms / max(1, head_n)
+    # the dominant kernel: the head call of the default build; for a variant
+    # the kind with the most device time among those with a byte count
+    kind = "head"
+    if args.variant != "dartree":
+        kind = max((k for k in ("head", "state", "candidates")
+                    if kernel_bytes_per_launch(w, args.variant, k) and kt[k][1]),
+                   key=lambda k: kt[k][0])
+    k_ms, k_n = kt[kind]
+    head_avg_ms = k_ms / max(1, k_n)
     peak, peak_kind = measured_peaks()
-    bytes_launch = head_bytes_per_launch(w)
+    bytes_launch = kernel_bytes_per_launch(w, args.variant, kind)
     achieved = bytes_launch / (head_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.config)
+    traffic = profiled_traffic(args.config) if args.variant == "dartree" else None
+    kernel_name = {
+        "head": ("k_cand_logits (candidate logits)" if opt.get("candidates") == "base" else
+                 "k_head_tc (head call: Wout stream, fused log-softmax + top-K)" if w.bf16
+                 else "k_head_simt"),
+        "state": ("k_state_markov" if opt.get("head") == "markov" else
+                  "k_head_tc (state step: A stream, split-K)"),
+        "candidates": "k_base_topk (top-K of the base logits)"}[kind]
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.variant != "dartree":
+        # host inputs -> device, build, tree -> host, through the public API
+        zh = torch.from_numpy(inp["z"]).pin_memory()
+        sh = torch.from_numpy(inp["state0"]).pin_memory()
+        oh = ctx.alloc_tree(w.R, w.B, device="cpu", pin=True)
+
+        def step_host():
+            with torch.cuda.stream(stream):
+                dev["z"].copy_(zh, non_blocking=True)
+                dev["state0"].copy_(sh, non_blocking=True)
+                ctx.build(*args_t, **kw)
+                for k in oh:
+                    oh[k].copy_(out[k], non_blocking=True)
+            ctx.sync(stream)
+        for _ in range(max(3, args.warmup)):
+            step_host()
+        barrier()
+        n_e2e = max(5, min(args.steps, 100))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            step_host()
+        t_e2e = aggregate((time.perf_counter() - t0) / n_e2e * 1e3, world)
+        e2e = {"value": world * w.R * 1e3 / t_e2e, "unit": "builds/s",
+               "h2d_bytes_per_step": int(zh.numel() * 4 + sh.numel() * 4),
+               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in oh.values())),
+               "ms_per_step": t_e2e}
+    elif not args.no_e2e:
         zh = torch.from_numpy(inp["z"]).pin_memory()
         sh = torch.from_numpy(inp["state0"]).pin_memory()
         oh = ctx.alloc_tree(w.R, w.B, device="cpu", pin=True)
@@ -358,7 +471,7 @@ def run_gpu(args) -> None:
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        s = oracle_sample(w, inp, args.cpu_budget)
+        s = oracle_sample(w, inp, args.cpu_budget, variant=args.variant)
         cpu = {"value": s["builds_per_s"], "unit": "builds/s", "cores": 1, "kind": "oracle",
                "sample": s["sample"]}
 
@@ -369,17 +482,19 @@ def run_gpu(args) -> None:
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.bf16 else "f32", "data": "synthetic",
             "config": workload_config(w),
-            "nodes_scored_per_s": value / w.R * w.candidates_per_build(),
-            "path_GBps_per_gpu": build_bytes(w) * (value / world / w.R) / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "k_head_tc (head call: Wout stream, fused "
-                         "log-softmax + top-K)" if w.bf16 else "k_head_simt",
+            "variant": args.variant,
+            "head_calls_per_build": ctx.head_calls(),
+            "nodes_scored_per_s": (value / w.R * w.candidates_per_build()
+                                   if args.variant != "bestfirst" else None),
+            "path_GBps_per_gpu": build_bytes(w, args.variant) * (value / world / w.R) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic, "bytes_per_launch": bytes_launch,
                          "launch_ms": head_avg_ms},
             "kernel_ms_per_build": {k: v[0] / max(1, min(args.steps, 50)) for k, v in kt.items()},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": kernels_per_build(w) * args.steps,
+            "gpu_launches": kernels_per_build(w, args.variant) * args.steps,
             "clocks": clock_info,
         }
         print(json.dumps(line), flush=True)

@@ -126,6 +126,57 @@ dartree_status dartree_build(dartree_ctx *ctx, const float *base_logits, const f
                              const dartree_head *head, int32_t R, int32_t D, int32_t W, int32_t K,
                              int32_t B, float beta, const dartree_tree *out, void *stream);
 
+/* Build variants (dartree_build_ex).  All zeros = dartree_build.
+ *
+ * head_kind
+ *   DARTREE_HEAD_RECURRENT  s' = q(tanh(A s + E[tok])) (A required).
+ *   DARTREE_HEAD_MARKOV     s' = q(tanh(E[tok])): the state after a token
+ *       depends on that token alone (the A = 0 case; head->A may be NULL and
+ *       is not read).  "Technische Samenvatting: DARTree", Experimentele
+ *       Resultaten, Ablatie: DARTree applied to the DSpark drafter, whose
+ *       correction head is Markov.
+ * candidates
+ *   DARTREE_CAND_CORRECTED  each branch's children are the top-K of its own
+ *       corrected distribution over the whole vocabulary ("DARTree: Teaching
+ *       a Chain-Trained Corrector to Think in Trees", Core Mechanism).
+ *   DARTREE_CAND_BASE       the K candidates of depth d are the top-K of the
+ *       base logits z_d (z desc, token asc), shared by every branch of the
+ *       request; each branch scores them with its corrected logits
+ *       z_d[c] + s . Wout[c], normalised over the K candidates (log-softmax
+ *       restricted to them).  "Technische Samenvatting: DARTree",
+ *       Methodologie 1 (Kandidaat Selectie from the base logits; Gebatchte
+ *       Correctie of the candidates of all branches in one batch).
+ * expansion
+ *   DARTREE_EXPAND_DEPTHWISE   the DARTree build: D batched head calls, then
+ *       the deferred Top-B.
+ *   DARTREE_EXPAND_BESTFIRST   the sequential baseline that DARTree replaces:
+ *       node-by-node best-first growth with one head call per expanded node
+ *       (B calls).  "Technische Samenvatting: DARTree", Probleemstelling
+ *       (Causale Correctie: pop one node, correct it, push its children) and
+ *       Experimentele Resultaten, Ablatie (latency of the sequential
+ *       heap build).  The tree, in pop order, goes to `out` in the same
+ *       layout; W is ignored; candidates must be CORRECTED. */
+typedef enum dartree_head_kind {
+  DARTREE_HEAD_RECURRENT = 0,
+  DARTREE_HEAD_MARKOV = 1
+} dartree_head_kind;
+typedef enum dartree_cand_kind { DARTREE_CAND_CORRECTED = 0, DARTREE_CAND_BASE = 1 } dartree_cand_kind;
+typedef enum dartree_expand_kind {
+  DARTREE_EXPAND_DEPTHWISE = 0,
+  DARTREE_EXPAND_BESTFIRST = 1
+} dartree_expand_kind;
+typedef struct dartree_options {
+  int32_t head_kind, candidates, expansion;
+} dartree_options;
+
+/* dartree_build with options (NULL = all zeros).  Same arguments, errors,
+ * graph capture and output layout as dartree_build.  INVALID_ARG for an
+ * unknown option value; UNSUPPORTED for BESTFIRST with BASE candidates. */
+dartree_status dartree_build_ex(dartree_ctx *ctx, const float *base_logits, const float *state0,
+                                const dartree_head *head, int32_t R, int32_t D, int32_t W,
+                                int32_t K, int32_t B, float beta, const dartree_options *opt,
+                                const dartree_tree *out, void *stream);
+
 /* Same as dartree_build with HOST base_logits, state0 and outputs (weights
  * stay on the device): copies the inputs into the context's staging buffers,
  * builds, copies the tree back and synchronises the stream.  Returns the
@@ -143,7 +194,9 @@ dartree_status dartree_build_host(dartree_ctx *ctx, const float *base_logits_hos
  * kernels' pipeline waits to provoke the TIMEOUT path. */
 dartree_status dartree_sync_status(dartree_ctx *ctx, void *stream);
 
-/* Number of batched head calls made by the last build (== its D). */
+/* Number of head calls made by the last build: D for a depth-wise build,
+ * B for a best-first one (one per step, including steps whose node cannot
+ * be expanded). */
 int64_t dartree_head_calls(const dartree_ctx *ctx);
 
 /* Text of the last error recorded by this context ("" if none); with a NULL
@@ -154,30 +207,36 @@ const char *dartree_last_error(const dartree_ctx *ctx);
 /* Per-kernel timing.  When enabled, every launch of a build is bracketed by
  * CUDA events on the build's stream; dartree_sync_status() adds the elapsed
  * times to per-kind totals.  Kinds: 0 head call (fused logits + log-softmax
- * + top-K partials), 1 state step, 2 row merge, 3 top-W select, 4 Top-B +
- * mask, 5 root rows.  Enabling creates the events (no device memory). */
-#define DARTREE_KERNEL_KINDS 6
+ * + top-K partials; with base candidates the candidate logits), 1 state
+ * step, 2 row merge, 3 top-W select, 4 Top-B + mask, 5 root rows, 6 base
+ * candidates (top-K of the base logits), 7 best-first step (node append +
+ * pop).  Enabling creates the events (no device memory). */
+#define DARTREE_KERNEL_KINDS 8
 dartree_status dartree_set_timing(dartree_ctx *ctx, int32_t enable);
 /* Totals since the last reset: milliseconds and launch count per kind. */
 dartree_status dartree_get_timing(const dartree_ctx *ctx, int32_t kind, double *total_ms,
                                   int64_t *launches);
 dartree_status dartree_reset_timing(dartree_ctx *ctx);
 
-/* Debug: copy the last build's pool ([R, P] each, pool index depth-major,
- * rank order within a depth, parent = pool index or -1) into any memory
- * (host or device).  Asynchronous on `stream`. */
+/* Debug: copy the last depth-wise build's pool ([R, P] each, pool index
+ * depth-major, rank order within a depth, parent = pool index or -1) into
+ * any memory (host or device).  Asynchronous on `stream`. */
 dartree_status dartree_get_pool(dartree_ctx *ctx, int32_t *parent, int32_t *token,
                                 int32_t *depth, float *score, void *stream);
 
 /* Debug: the last build's per-row head results at depth d (1-based) for its
  * R*|F_{d-1}| head rows: lse [rows] fp64, top-K tokens [rows, K] and their
- * log-probs [rows, K].  Any memory; asynchronous. */
+ * log-probs [rows, K].  After a best-first build, d = 1..B selects head call
+ * d-1 and rows = R (one per request; call 0 expands the root, call q+1 the
+ * node popped at rank q when its depth is below D, otherwise its results
+ * are unused).  Any memory; asynchronous. */
 dartree_status dartree_get_rows(dartree_ctx *ctx, int32_t d, double *lse, int32_t *tok,
                                 float *logp, void *stream);
 
 /* Debug: the head states used by head call d (1-based) of the last build,
  * [R*|F_{d-1}|, H] in the context's dtype (bf16 bits or fp32), row order as
- * dartree_get_rows.  Any memory; asynchronous. */
+ * dartree_get_rows (best-first: [R, H], the states of call d-1).  Any
+ * memory; asynchronous. */
 dartree_status dartree_get_states(dartree_ctx *ctx, int32_t d, void *states, void *stream);
 
 /* One batched head call (corrected logits fused with log-softmax and top-K)

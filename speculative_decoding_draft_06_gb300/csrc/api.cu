@@ -16,6 +16,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <string>
@@ -80,6 +81,8 @@ struct dartree_ctx {
     const void *A, *E, *Wout;
     int R, D, W, K, B;
     float beta;
+    dartree_options opt;
+    int32_t unused;  // keeps the layout free of padding (the key is compared bytewise)
     dartree_tree out;
     cudaStream_t st;
     bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof o) == 0; }
@@ -98,6 +101,28 @@ struct dartree_ctx {
   int32_t* pool_depth = nullptr;
   float* pool_score = nullptr;
   int* d_err = nullptr;
+  // base-logit candidates (dartree_build_ex, DARTREE_CAND_BASE)
+  int32_t* cand = nullptr;          // [max_requests * max_D][max_K]
+  uint64_t* base_part = nullptr;    // [max_requests * max_D][base_chunks][max_K]
+  int* base_cnt = nullptr;          // [max_requests * max_D]
+  int base_chunks = 0;
+  // sequential best-first baseline (DARTREE_EXPAND_BESTFIRST)
+  int bf_nodes = 0;                 // node table entries per request (max_B * max_K)
+  int32_t* bf_par = nullptr;        // [max_requests][bf_nodes]
+  int32_t* bf_tok = nullptr;
+  int32_t* bf_dep = nullptr;
+  int32_t* bf_rank = nullptr;
+  float* bf_score = nullptr;
+  int* bf_st = nullptr;             // [max_requests][4]
+  int32_t* bf_tok_next = nullptr;   // [max_requests]
+  int32_t* bf_zrow = nullptr;       // [max_requests]
+  float* bf_z = nullptr;            // [max_requests][V] base logits of the next call
+  void* bf_S = nullptr;             // [max_requests][max_B][H] state per popped rank
+  double* bf_lse = nullptr;         // [max_B][max_requests] rows of each call
+  int32_t* bf_rtok = nullptr;       // [max_B][max_requests][max_K]
+  float* bf_rlogp = nullptr;
+  int last_expansion = DARTREE_EXPAND_DEPTHWISE;
+  int last_B = 0;
   // staging for dartree_build_host
   float* z_stage = nullptr;
   float* s0_stage = nullptr;
@@ -214,6 +239,9 @@ cudaError_t alloc(T** p, size_t count) {
 // Head call for M rows whose states are in state slot `sbuf` (rows >= M up to the
 // padded count are zero or finite): fused logits + partials, then the row
 // merge (+ the request's top-W selection when sel != nullptr).
+dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, int32_t* tok,
+                         float* logp, const dt::MergeParams* sel, cudaStream_t st);
+
 dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_req_stride,
                         int rows_per_req, int M, int K, double* lse, int32_t* tok, float* logp,
                         const dt::MergeParams* sel, cudaStream_t st) {
@@ -255,6 +283,15 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
     }
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "head logits launch");
+  return run_merge(c, grid, M, K, lse, tok, logp, sel, st);
+}
+
+// Row merge of n_cta partials per row (+ the request's top-W selection when
+// sel != nullptr).
+dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, int32_t* tok,
+                         float* logp, const dt::MergeParams* sel, cudaStream_t st) {
+  const int grid = n_cta;
+  cudaError_t e;
   dt::MergeParams mp{};
   if (sel) mp = *sel;
   mp.pm = c->pm;
@@ -289,7 +326,8 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
 // State step: slot src+1 row q = q(tanh(A S[slot[q]] + E[tok[q]])) for
 // q < M_out (zeros up to the padded count); state slot src holds M_in rows.
 dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, int M_in,
-                         const int32_t* slot, const int32_t* tok, int M_out, cudaStream_t st) {
+                         const int32_t* slot, const int32_t* tok, int M_out, cudaStream_t st,
+                         bool early = false) {
   const int H = c->cfg.H;
   const int N = pad_rows(M_in);
   dt::TcParams p{};
@@ -312,6 +350,7 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
     p.n_split = c->state_split;
     p.part = c->part;
     p.tile_cnt = c->tile_cnt;
+    p.early_operands = early && c->pdl;
     e = dt::launch_head_tc(N, false, c->tm_A, c->tmS(src, N), p,
                            p.n_tiles * p.n_split, st);
   } else {
@@ -326,6 +365,65 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
   return DARTREE_OK;
 }
 
+// Markov head state step: slot src+1 row q = q(tanh(E[tok[q]])) for
+// q < M_out, zeros up to the padded count.
+dartree_status run_state_markov(dartree_ctx* c, const void* E, int src, const int32_t* tok,
+                                int M_out, cudaStream_t st) {
+  dt::MarkovParams p{};
+  p.pdl = c->pdl;
+  p.M_out = M_out;
+  p.n_out = pad_rows(M_out);
+  p.H = c->cfg.H;
+  p.V = c->cfg.V;
+  p.bf16 = c->bf16;
+  p.tok = tok;
+  p.E = E;
+  p.S_out = c->S(src + 1);
+  p.err = c->d_err;
+  cudaError_t e;
+  {
+    KernelTimer tk(c, st, 1);
+    e = dt::launch_state_markov(p, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "Markov state launch");
+  return DARTREE_OK;
+}
+
+// Base-candidate head call for M rows in state slot `sbuf`: the corrected
+// logits of each row's K candidates as one partial per row, then the row
+// merge (+ selection).
+dartree_status run_cand(dartree_ctx* c, int sbuf, const float* z, long long z_req_stride,
+                        const int32_t* cand, long long cand_req_stride, int rows_per_req, int M,
+                        int K, const void* Wout, double* lse, int32_t* tok, float* logp,
+                        const dt::MergeParams* sel, cudaStream_t st) {
+  dt::CandParams p{};
+  p.pdl = c->pdl;
+  p.M = M;
+  p.H = c->cfg.H;
+  p.K = K;
+  p.rows_per_req = rows_per_req;
+  p.bf16 = c->bf16;
+  p.z = z;
+  p.z_req_stride = z_req_stride;
+  p.cand = cand;
+  p.cand_req_stride = cand_req_stride;
+  p.S = c->S(sbuf);
+  p.Wout = Wout;
+  p.pm = c->pm;
+  p.ps = c->ps;
+  p.ptop = c->ptop;
+  p.cta_stride = c->max_cta;
+  p.list_stride = c->max_cta;
+  p.err = c->d_err;
+  cudaError_t e;
+  {
+    KernelTimer tk(c, st, 0);
+    e = dt::launch_cand_logits(p, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "candidate logits launch");
+  return run_merge(c, 1, M, K, lse, tok, logp, sel, st);
+}
+
 dartree_status bind_weights(dartree_ctx* c, const void* A, const void* Wout) {
   if (!c->bf16) {
     c->tm_A_ptr = A;
@@ -334,6 +432,7 @@ dartree_status bind_weights(dartree_ctx* c, const void* A, const void* Wout) {
   }
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Wout)) & 15)
     return c->fail(DARTREE_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
+  // (A is null for the Markov head)
   dartree_status s;
   if (A != nullptr && A != c->tm_A_ptr) {
     if ((s = encode_2d(c, &c->tm_A, A, c->cfg.H, c->cfg.H, dt::kTileV)) != DARTREE_OK) return s;
@@ -349,9 +448,19 @@ dartree_status bind_weights(dartree_ctx* c, const void* A, const void* Wout) {
 
 dartree_status check_build_args(dartree_ctx* c, const void* z, const void* s0,
                                 const dartree_head* head, int R, int D, int W, int K, int B,
-                                float beta, const dartree_tree* out) {
-  if (!z || !s0 || !head || !head->A || !head->E || !head->Wout || !out || !out->parent ||
-      !out->token || !out->depth || !out->score || !out->mask || !out->n_out)
+                                float beta, const dartree_tree* out,
+                                const dartree_options& o = dartree_options{}) {
+  if (o.head_kind != DARTREE_HEAD_RECURRENT && o.head_kind != DARTREE_HEAD_MARKOV)
+    return c->fail(DARTREE_ERR_INVALID_ARG, "unknown head kind %d", o.head_kind);
+  if (o.candidates != DARTREE_CAND_CORRECTED && o.candidates != DARTREE_CAND_BASE)
+    return c->fail(DARTREE_ERR_INVALID_ARG, "unknown candidate kind %d", o.candidates);
+  if (o.expansion != DARTREE_EXPAND_DEPTHWISE && o.expansion != DARTREE_EXPAND_BESTFIRST)
+    return c->fail(DARTREE_ERR_INVALID_ARG, "unknown expansion kind %d", o.expansion);
+  if (o.expansion == DARTREE_EXPAND_BESTFIRST && o.candidates != DARTREE_CAND_CORRECTED)
+    return c->fail(DARTREE_ERR_UNSUPPORTED, "best-first growth takes corrected candidates only");
+  const bool need_A = o.head_kind == DARTREE_HEAD_RECURRENT;
+  if (!z || !s0 || !head || (need_A && !head->A) || !head->E || !head->Wout || !out ||
+      !out->parent || !out->token || !out->depth || !out->score || !out->mask || !out->n_out)
     return c->fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
   const dartree_config& g = c->cfg;
   if (R < 1 || R > g.max_requests) return c->fail(DARTREE_ERR_INVALID_ARG, "R=%d out of [1,%d]", R, g.max_requests);
@@ -361,16 +470,25 @@ dartree_status check_build_args(dartree_ctx* c, const void* z, const void* s0,
   if (K > g.V) return c->fail(DARTREE_ERR_INVALID_ARG, "K=%d exceeds V=%d", K, g.V);
   if (B < 1 || B > g.max_B) return c->fail(DARTREE_ERR_INVALID_ARG, "B=%d out of [1,%d]", B, g.max_B);
   if (!(beta <= 0.0f)) return c->fail(DARTREE_ERR_INVALID_ARG, "beta must be <= 0 (Lemma 1)");
-  if (R * W > dt::kMaxRows) return c->fail(DARTREE_ERR_UNSUPPORTED, "R*W=%d > 256", R * W);
-  if (c->bf16 && pad_rows(R * W) * K > 2048)
-    return c->fail(DARTREE_ERR_UNSUPPORTED, "padded rows x K = %d > 2048", pad_rows(R * W) * K);
+  const int rows = o.expansion == DARTREE_EXPAND_BESTFIRST ? R : R * W;  // head rows per call
+  if (rows > dt::kMaxRows) return c->fail(DARTREE_ERR_UNSUPPORTED, "%d head rows > 256", rows);
+  if (c->bf16 && o.candidates == DARTREE_CAND_CORRECTED && pad_rows(rows) * K > 2048)
+    return c->fail(DARTREE_ERR_UNSUPPORTED, "padded rows x K = %d > 2048", pad_rows(rows) * K);
   return DARTREE_OK;
 }
 
+dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
+                             const dartree_head* head, int R, int D, int K, int B, float beta,
+                             const dartree_options& o, const dartree_tree* out, cudaStream_t st);
+
 dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const dartree_head* head,
-                         int R, int D, int W, int K, int B, float beta, const dartree_tree* out,
-                         cudaStream_t st) {
-  dartree_status s = bind_weights(c, head->A, head->Wout);
+                         int R, int D, int W, int K, int B, float beta, const dartree_options& o,
+                         const dartree_tree* out, cudaStream_t st) {
+  if (o.expansion == DARTREE_EXPAND_BESTFIRST)
+    return run_bestfirst(c, z, s0, head, R, D, K, B, beta, o, out, st);
+  const bool markov = o.head_kind == DARTREE_HEAD_MARKOV;
+  const bool base = o.candidates == DARTREE_CAND_BASE;
+  dartree_status s = bind_weights(c, markov ? nullptr : head->A, head->Wout);
   if (s != DARTREE_OK) return s;
   const int V = c->cfg.V, H = c->cfg.H;
   const int P = dartree_pool_size(D, W, K);
@@ -389,13 +507,37 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
     e = dt::launch_root(rp, st);
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "root launch");
+  if (base) {
+    // the candidates of every (request, depth): top-K of the base logits
+    dt::BaseTopkParams bp{};
+    bp.pdl = c->pdl;
+    bp.rows = R * D;
+    bp.V = V;
+    bp.K = K;
+    bp.n_chunks = c->base_chunks;
+    bp.z = z;
+    bp.part = c->base_part;
+    bp.cnt = c->base_cnt;
+    bp.cand = c->cand;
+    bp.err = c->d_err;
+    {
+      KernelTimer tk(c, st, 6);
+      e = dt::launch_base_topk(bp, st);
+    }
+    if (e != cudaSuccess) return c->cuda_fail(e, "base candidates launch");
+  }
   int F = 1, F_prev = 1, off_prev = 0, off = 0, cur = 0, sbuf = 0;
   int64_t calls = 0;
   for (int d = 1; d <= D; ++d) {
     const int M = R * F;
     if (d >= 2) {
       // states of this depth's rows from their parents (the rows of call d-1)
-      s = run_state(c, head->A, head->E, sbuf, R * F_prev, c->slot_next, c->tok_next, M, st);
+      // A and the parent states (written three kernels back) are complete
+      // before the merge that precedes this step starts: the step streams
+      // them while that merge runs
+      s = markov ? run_state_markov(c, head->E, sbuf, c->tok_next, M, st)
+                 : run_state(c, head->A, head->E, sbuf, R * F_prev, c->slot_next, c->tok_next,
+                             M, st, /*early=*/true);
       if (s != DARTREE_OK) return s;
       ++sbuf;  // each depth keeps its own state slot
     }
@@ -418,8 +560,15 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
     sel.pool_score = c->pool_score;
     sel.counters = c->counters;
     const size_t ro = static_cast<size_t>(d - 1) * dt::kMaxRows;
-    s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V, F,
-                 M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel, st);
+    if (base)
+      s = run_cand(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
+                   c->cand + static_cast<size_t>(d - 1) * K, static_cast<long long>(D) * K, F, M,
+                   K, head->Wout, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K,
+                   &sel, st);
+    else
+      s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
+                   F, M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel,
+                   st);
     if (s != DARTREE_OK) return s;
     ++calls;
     cur ^= 1;
@@ -457,7 +606,108 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   c->last_W = W;
   c->last_K = K;
   c->last_P = P;
+  c->last_B = B;
+  c->last_expansion = DARTREE_EXPAND_DEPTHWISE;
   c->head_calls = calls;
+  return DARTREE_OK;
+}
+
+// Sequential best-first growth: B steps, each one head call with one row per
+// request (call 0 on the root states, call q+1 on the node popped at rank q),
+// then the step kernel that appends the children and pops the next node.
+// State slots: 0 root states, 1 staged parent states, 2 the call's states.
+dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
+                             const dartree_head* head, int R, int D, int K, int B, float beta,
+                             const dartree_options& o, const dartree_tree* out, cudaStream_t st) {
+  const bool markov = o.head_kind == DARTREE_HEAD_MARKOV;
+  dartree_status s = bind_weights(c, markov ? nullptr : head->A, head->Wout);
+  if (s != DARTREE_OK) return s;
+  const int V = c->cfg.V, H = c->cfg.H;
+  dt::RootParams rp{};
+  rp.R = R;
+  rp.n_pad = pad_rows(R);
+  rp.H = H;
+  rp.bf16 = c->bf16;
+  rp.state0 = s0;
+  rp.S = c->S(0);
+  rp.score = c->score[0];
+  rp.pdl = c->pdl;
+  cudaError_t e;
+  {
+    KernelTimer tk(c, st, 5);
+    e = dt::launch_root(rp, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "root launch");
+  dt::BestFirstParams bp{};
+  bp.pdl = c->pdl;
+  bp.R = R;
+  bp.B = B;
+  bp.K = K;
+  bp.D = D;
+  bp.H = H;
+  bp.words = (B + 31) / 32;
+  bp.bf16 = c->bf16;
+  bp.beta = beta;
+  bp.max_nodes = c->bf_nodes;
+  bp.node_par = c->bf_par;
+  bp.node_tok = c->bf_tok;
+  bp.node_dep = c->bf_dep;
+  bp.node_rank = c->bf_rank;
+  bp.node_score = c->bf_score;
+  bp.st = c->bf_st;
+  bp.S_pop = c->bf_S;
+  bp.S_stage = c->S(1);
+  bp.S_root = c->S(0);
+  bp.tok_next = c->bf_tok_next;
+  bp.z_row = c->bf_zrow;
+  bp.V = V;
+  bp.z = z;
+  bp.z_stage = c->bf_z;
+  bp.parent = out->parent;
+  bp.token = out->token;
+  bp.depth = out->depth;
+  bp.score = out->score;
+  bp.mask = out->mask;
+  bp.n_out = out->n_out;
+  bp.err = c->d_err;
+  {
+    KernelTimer tk(c, st, 7);
+    e = dt::launch_bestfirst_init(bp, st);
+  }
+  if (e != cudaSuccess) return c->cuda_fail(e, "best-first init launch");
+  for (int call = 0; call < B; ++call) {
+    {
+      KernelTimer tk(c, st, 7);
+      e = dt::launch_bestfirst_z(bp, st);
+    }
+    if (e != cudaSuccess) return c->cuda_fail(e, "best-first base logits launch");
+    if (call >= 1) {
+      s = markov ? run_state_markov(c, head->E, 1, c->bf_tok_next, R, st)
+                 : run_state(c, head->A, head->E, 1, R, c->iota, c->bf_tok_next, R, st);
+      if (s != DARTREE_OK) return s;
+    }
+    const int sbuf = call == 0 ? 0 : 2;
+    const size_t ro = static_cast<size_t>(call) * c->cfg.max_requests;
+    s = run_head(c, sbuf, c->bf_z, V, 1, R, K, c->bf_lse + ro, c->bf_rtok + ro * K,
+                 c->bf_rlogp + ro * K, nullptr, st);
+    if (s != DARTREE_OK) return s;
+    bp.row_tok = c->bf_rtok + ro * K;
+    bp.row_logp = c->bf_rlogp + ro * K;
+    bp.S_call = c->S(sbuf);
+    {
+      KernelTimer tk(c, st, 7);
+      e = dt::launch_bestfirst_step(bp, st);
+    }
+    if (e != cudaSuccess) return c->cuda_fail(e, "best-first step launch");
+  }
+  c->last_R = R;
+  c->last_D = D;
+  c->last_W = 1;
+  c->last_K = K;
+  c->last_P = 0;
+  c->last_B = B;
+  c->last_expansion = DARTREE_EXPAND_BESTFIRST;
+  c->head_calls = B;
   return DARTREE_OK;
 }
 
@@ -466,12 +716,14 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
 // launches on the legacy stream and while kernel timing is on).
 dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
                               const dartree_head* head, int R, int D, int W, int K, int B,
-                              float beta, const dartree_tree* out, cudaStream_t st) {
+                              float beta, const dartree_options& o, const dartree_tree* out,
+                              cudaStream_t st) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (st != nullptr && cudaStreamIsCapturing(st, &cap) != cudaSuccess) cap = cudaStreamCaptureStatusNone;
   if (!c->use_graph || c->timing || st == nullptr || cap != cudaStreamCaptureStatusNone)
-    return run_build(c, z, s0, head, R, D, W, K, B, beta, out, st);
+    return run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st);
   dartree_ctx::GraphKey key{};
+  key.opt = o;
   key.z = z;
   key.s0 = s0;
   key.A = head->A;
@@ -492,7 +744,7 @@ dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
     }
     cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return c->cuda_fail(e, "begin capture");
-    dartree_status s = run_build(c, z, s0, head, R, D, W, K, B, beta, out, st);
+    dartree_status s = run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st);
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(st, &g);
     if (s != DARTREE_OK) {
@@ -508,12 +760,15 @@ dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
     }
     c->gkey = key;
   } else {
+    const bool bf = o.expansion == DARTREE_EXPAND_BESTFIRST;
     c->last_R = R;
     c->last_D = D;
-    c->last_W = W;
+    c->last_W = bf ? 1 : W;
     c->last_K = K;
-    c->last_P = dartree_pool_size(D, W, K);
-    c->head_calls = D;
+    c->last_P = bf ? 0 : dartree_pool_size(D, W, K);
+    c->last_B = B;
+    c->last_expansion = o.expansion;
+    c->head_calls = bf ? B : D;
   }
   cudaError_t e = cudaGraphLaunch(c->gexec, st);
   if (e != cudaSuccess) return c->cuda_fail(e, "graph launch");
@@ -537,7 +792,10 @@ void free_all(dartree_ctx* c) {
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
                   c->d_err,     c->z_stage,    c->s0_stage,    c->o_parent,   c->o_token,
-                  c->o_depth,   c->o_score,    c->o_mask,      c->o_nout};
+                  c->o_depth,   c->o_score,    c->o_mask,      c->o_nout,     c->cand,
+                  c->base_part, c->base_cnt,   c->bf_par,      c->bf_tok,     c->bf_dep,
+                  c->bf_rank,   c->bf_score,   c->bf_st,       c->bf_tok_next, c->bf_zrow,
+                  c->bf_S,      c->bf_lse,     c->bf_rtok,     c->bf_rlogp,   c->bf_z};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -620,7 +878,11 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   c->state_split = c->num_sms / h_tiles;
   if (c->state_split > nk) c->state_split = nk;
   if (c->state_split < 1) c->state_split = 1;
-  c->n_slots = g.max_D > 2 ? g.max_D : 2;
+  c->n_slots = g.max_D > 3 ? g.max_D : 3;
+  c->base_chunks = (g.V + dt::kBaseChunk - 1) / dt::kBaseChunk;
+  c->bf_nodes = g.max_B * g.max_K;
+  const size_t RD = Rc * g.max_D;
+  const size_t bfn = Rc * c->bf_nodes;
   const size_t slot_bytes = rows * g.H * c->elem;
   bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S_all), c->n_slots * slot_bytes) == cudaSuccess &&
             alloc(&c->score[0], rows) == cudaSuccess && alloc(&c->score[1], rows) == cudaSuccess &&
@@ -647,7 +909,19 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
             alloc(&c->o_parent, Rc * B) == cudaSuccess && alloc(&c->o_token, Rc * B) == cudaSuccess &&
             alloc(&c->o_depth, Rc * B) == cudaSuccess && alloc(&c->o_score, Rc * B) == cudaSuccess &&
             alloc(&c->o_mask, Rc * B * words) == cudaSuccess &&
-            alloc(&c->o_nout, Rc) == cudaSuccess;
+            alloc(&c->o_nout, Rc) == cudaSuccess &&
+            alloc(&c->cand, RD * g.max_K) == cudaSuccess &&
+            alloc(&c->base_part, RD * c->base_chunks * g.max_K) == cudaSuccess &&
+            alloc(&c->base_cnt, RD) == cudaSuccess &&
+            alloc(&c->bf_par, bfn) == cudaSuccess && alloc(&c->bf_tok, bfn) == cudaSuccess &&
+            alloc(&c->bf_dep, bfn) == cudaSuccess && alloc(&c->bf_rank, bfn) == cudaSuccess &&
+            alloc(&c->bf_score, bfn) == cudaSuccess && alloc(&c->bf_st, Rc * 4) == cudaSuccess &&
+            alloc(&c->bf_tok_next, Rc) == cudaSuccess && alloc(&c->bf_zrow, Rc) == cudaSuccess &&
+            alloc(&c->bf_z, Rc * g.V) == cudaSuccess &&
+            alloc(reinterpret_cast<uint8_t**>(&c->bf_S), Rc * B * g.H * c->elem) == cudaSuccess &&
+            alloc(&c->bf_lse, B * Rc) == cudaSuccess &&
+            alloc(&c->bf_rtok, B * Rc * g.max_K) == cudaSuccess &&
+            alloc(&c->bf_rlogp, B * Rc * g.max_K) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(c);
@@ -660,6 +934,9 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->row_cnt, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->gth, 0, rows * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->base_cnt, 0, RD * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->bf_tok_next, 0, Rc * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->bf_zrow, 0, Rc * sizeof(int32_t));
   if (e == cudaSuccess) {
     int32_t h_iota[dt::kMaxRows];
     for (int i = 0; i < dt::kMaxRows; ++i) h_iota[i] = i;
@@ -699,10 +976,20 @@ void dartree_destroy(dartree_ctx* ctx) {
 dartree_status dartree_build(dartree_ctx* ctx, const float* base_logits, const float* state0,
                              const dartree_head* head, int32_t R, int32_t D, int32_t W, int32_t K,
                              int32_t B, float beta, const dartree_tree* out, void* stream) {
+  return dartree_build_ex(ctx, base_logits, state0, head, R, D, W, K, B, beta, nullptr, out,
+                          stream);
+}
+
+dartree_status dartree_build_ex(dartree_ctx* ctx, const float* base_logits, const float* state0,
+                                const dartree_head* head, int32_t R, int32_t D, int32_t W,
+                                int32_t K, int32_t B, float beta, const dartree_options* opt,
+                                const dartree_tree* out, void* stream) {
   if (!ctx) return DARTREE_ERR_INVALID_ARG;
-  dartree_status s = check_build_args(ctx, base_logits, state0, head, R, D, W, K, B, beta, out);
+  const dartree_options o = opt ? *opt : dartree_options{};
+  dartree_status s =
+      check_build_args(ctx, base_logits, state0, head, R, D, W, K, B, beta, out, o);
   if (s != DARTREE_OK) return s;
-  return build_dispatch(ctx, base_logits, state0, head, R, D, W, K, B, beta, out,
+  return build_dispatch(ctx, base_logits, state0, head, R, D, W, K, B, beta, o, out,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -724,6 +1011,9 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
     if (e == cudaSuccess)
       e = cudaMemset(ctx->tile_cnt, 0,
                      sizeof(int) * ((ctx->cfg.H + dt::kTileV - 1) / dt::kTileV));
+    if (e == cudaSuccess)
+      e = cudaMemset(ctx->base_cnt, 0,
+                     sizeof(int) * static_cast<size_t>(ctx->cfg.max_requests) * ctx->cfg.max_D);
   }
   if (e != cudaSuccess) return ctx->cuda_fail(e, "error word read");
   if (h & dt::DT_ERR_TIMEOUT)
@@ -745,7 +1035,8 @@ dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->s0_stage, s0h, sn * 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "input copy");
   dartree_tree dev{ctx->o_parent, ctx->o_token, ctx->o_depth, ctx->o_score, ctx->o_mask, ctx->o_nout};
-  s = build_dispatch(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta, &dev, st);
+  s = build_dispatch(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta,
+                     dartree_options{}, &dev, st);
   if (s != DARTREE_OK) return s;
   const size_t nb = static_cast<size_t>(R) * B, nw = nb * ((B + 31) / 32);
   struct {
@@ -771,7 +1062,7 @@ dartree_status dartree_set_timing(dartree_ctx* ctx, int32_t enable) {
     return DARTREE_OK;
   }
   if (ctx->ev_pool.empty()) {
-    const size_t n = 2 * (4 * static_cast<size_t>(ctx->cfg.max_D) + 8);
+    const size_t n = 2 * (4 * static_cast<size_t>(std::max(ctx->cfg.max_D, ctx->cfg.max_B)) + 8);
     for (size_t i = 0; i < n; ++i) {
       cudaEvent_t ev;
       cudaError_t e = cudaEventCreate(&ev);
@@ -813,7 +1104,7 @@ const char* dartree_last_error(const dartree_ctx* ctx) {
 dartree_status dartree_get_pool(dartree_ctx* ctx, int32_t* parent, int32_t* token, int32_t* depth,
                                 float* score, void* stream) {
   if (!ctx || !parent || !token || !depth || !score) return DARTREE_ERR_INVALID_ARG;
-  if (ctx->last_P == 0) return ctx->fail(DARTREE_ERR_INVALID_ARG, "no build yet");
+  if (ctx->last_P == 0) return ctx->fail(DARTREE_ERR_INVALID_ARG, "no depth-wise build yet");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t n = static_cast<size_t>(ctx->last_R) * ctx->last_P * 4;
   cudaError_t e = cudaMemcpyAsync(parent, ctx->pool_parent, n, cudaMemcpyDefault, st);
@@ -827,6 +1118,20 @@ dartree_status dartree_get_pool(dartree_ctx* ctx, int32_t* parent, int32_t* toke
 dartree_status dartree_get_rows(dartree_ctx* ctx, int32_t d, double* lse, int32_t* tok, float* logp,
                                 void* stream) {
   if (!ctx || !lse || !tok || !logp) return DARTREE_ERR_INVALID_ARG;
+  if (ctx->last_expansion == DARTREE_EXPAND_BESTFIRST) {  // rows of call d-1
+    if (d < 1 || d > ctx->last_B)
+      return ctx->fail(DARTREE_ERR_INVALID_ARG, "call %d not in the last build", d - 1);
+    const size_t rows = ctx->last_R, K = ctx->last_K;
+    const size_t ro = static_cast<size_t>(d - 1) * ctx->cfg.max_requests;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(lse, ctx->bf_lse + ro, rows * 8, cudaMemcpyDefault, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(tok, ctx->bf_rtok + ro * K, rows * K * 4, cudaMemcpyDefault, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(logp, ctx->bf_rlogp + ro * K, rows * K * 4, cudaMemcpyDefault, st);
+    if (e != cudaSuccess) return ctx->cuda_fail(e, "rows copy");
+    return DARTREE_OK;
+  }
   if (ctx->last_P == 0 || d < 1 || d > ctx->last_D)
     return ctx->fail(DARTREE_ERR_INVALID_ARG, "depth %d not in the last build", d);
   int F = 1;
@@ -845,6 +1150,22 @@ dartree_status dartree_get_rows(dartree_ctx* ctx, int32_t d, double* lse, int32_
 
 dartree_status dartree_get_states(dartree_ctx* ctx, int32_t d, void* states, void* stream) {
   if (!ctx || !states) return DARTREE_ERR_INVALID_ARG;
+  if (ctx->last_expansion == DARTREE_EXPAND_BESTFIRST) {  // states of call d-1
+    if (d < 1 || d > ctx->last_B)
+      return ctx->fail(DARTREE_ERR_INVALID_ARG, "call %d not in the last build", d - 1);
+    const size_t rowb = static_cast<size_t>(ctx->cfg.H) * ctx->elem;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (d == 1)
+      e = cudaMemcpyAsync(states, ctx->S(0), ctx->last_R * rowb, cudaMemcpyDefault, st);
+    else
+      e = cudaMemcpy2DAsync(states, rowb,
+                            static_cast<const uint8_t*>(ctx->bf_S) + static_cast<size_t>(d - 2) * rowb,
+                            static_cast<size_t>(ctx->last_B) * rowb, rowb, ctx->last_R,
+                            cudaMemcpyDefault, st);
+    if (e != cudaSuccess) return ctx->cuda_fail(e, "states copy");
+    return DARTREE_OK;
+  }
   if (ctx->last_P == 0 || d < 1 || d > ctx->last_D)
     return ctx->fail(DARTREE_ERR_INVALID_ARG, "depth %d not in the last build", d);
   int F = 1;

@@ -227,8 +227,13 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // prologue done; from here on the kernel reads and writes shared buffers
-  pdl_wait();
+  // prologue done; from here on the kernel reads and writes shared buffers.
+  // A state step whose operands were complete before the previous kernel
+  // began streams them at once and waits only before its epilogue, which
+  // reads the previous kernel's selection (slot, tok) -- the contraction then
+  // overlaps the previous kernel.
+  const bool early = !kLogits && p.early_operands;
+  if (!early) pdl_wait();
   pdl_trigger();
 
   if (warp == R::kProducer) {
@@ -318,12 +323,23 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     // accumulator and broadcasts whether to go on (a timed-out wait ends all
     // four warps' loops at once).  Every group waits for every tile, so each
     // arrival on tempty belongs to the tile it was meant for.
+    if (early) pdl_wait();
     int it = 0;
     const int grp = warp >> 2;
     const int wq = warp & 3;  // TMEM lane quarter
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    // all rows of one request (the usual case): one base logit per thread
+    // and tile, loaded before the accumulator wait
+    const bool one_req = kLogits && p.rows_per_req >= p.M;
     for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = it & 1;
+      const int row = t * kTileV + wq * 32 + lane;  // vocabulary (or hidden) index
+      const bool valid = row < p.rows;
+      float z1 = 0.f;
+      if constexpr (kLogits) {
+        if (one_req && valid) z1 = __ldg(p.z + row);
+        epi.tile_begin();  // the rows' global bounds, also ahead of the wait
+      }
       if ((threadIdx.x & 127) == 0) {
         const bool ok = !*abort_flag &&
                         mbar_wait(&tfull[a], static_cast<uint32_t>(it >> 1) & 1u, p.err,
@@ -334,13 +350,16 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
       asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
       if (!epi_go[grp]) break;
       tc_fence_after();
-      const int row = t * kTileV + wq * 32 + lane;  // vocabulary (or hidden) index
-      const bool valid = row < p.rows;
       const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(a * N);
       if constexpr (kLogits) {
         int req_prev = -1;
         float zv = 0.f;
         auto add_z = [&](float (&x)[16], int c0) {
+          if (one_req) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] += z1;
+            return;
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = c0 + j;
@@ -353,7 +372,6 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
             x[j] += zv;
           }
         };
-        epi.tile_begin();
         const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
         if constexpr (N <= 64) {
           static_for<0, N / 16>([&](auto i) {

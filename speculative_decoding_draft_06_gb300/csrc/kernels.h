@@ -44,6 +44,9 @@ struct TcParams {
   const float* E_f32;
   float* S_out_f32;
   int n_split;               // contraction split across CTAs (tensor-core path)
+  int early_operands;        // the weights and S_in were complete before the previous
+                             // kernel started: stream them before waiting for it
+                             // (only slot / tok / scratch come from that kernel)
   float* part;               // [tiles * n_split][256][128] fp32 partial sums
   int* tile_cnt;             // [tiles] arrival counters, zero between launches
   // SIMT operands (fp32 path)
@@ -156,6 +159,91 @@ struct RootParams {
   float* score;
 };
 cudaError_t launch_root(const RootParams& p, cudaStream_t st);
+
+// Markov head state (the state depends on the last token only):
+// S_out[q] = q(tanh(E[tok[q]])) for q < M_out, zero rows up to n_out.
+struct MarkovParams {
+  int pdl;
+  int M_out, n_out, H, V, bf16;
+  const int32_t* tok;  // [M_out]
+  const void* E;       // [V][H] bf16 bits or fp32
+  void* S_out;         // [n_out][H]
+  int* err;
+};
+cudaError_t launch_state_markov(const MarkovParams& p, cudaStream_t st);
+
+// Base-logit candidates: the top-K of every row of z ([rows][V], a row per
+// (request, depth)) by (z desc, token asc).  Grid (chunks, rows); the last
+// chunk block of a row merges the chunk lists.
+struct BaseTopkParams {
+  int pdl;
+  int rows, V, K, n_chunks;
+  const float* z;
+  uint64_t* part;   // [rows][n_chunks][K] chunk lists
+  int* cnt;         // [rows] arrival counters, zero between launches
+  int32_t* cand;    // [rows][K] candidate tokens, best first
+  int* err;
+};
+constexpr int kBaseChunk = 8192;  // vocabulary entries per chunk block
+cudaError_t launch_base_topk(const BaseTopkParams& p, cudaStream_t st);
+
+// Corrected logits of the K base candidates of each head row, written as the
+// row's single partial (n_cta = 1) of the row merge: one (max, sum-exp) pair
+// over the K candidates and the K keys sorted.
+struct CandParams {
+  int pdl;
+  int M, H, K, rows_per_req, bf16;
+  const float* z;           // this depth's base logits, request 0
+  long long z_req_stride;
+  const int32_t* cand;      // this depth's candidates, request 0
+  long long cand_req_stride;
+  const void* S;            // [M][H] head states (bf16 bits or fp32)
+  const void* Wout;         // [V][H]
+  float* pm;
+  float* ps;
+  uint64_t* ptop;
+  int cta_stride, list_stride;
+  int* err;
+};
+cudaError_t launch_cand_logits(const CandParams& p, cudaStream_t st);
+
+// Sequential best-first baseline: requests advance in lockstep, one head
+// call (one row per request) per step.  Per request a node table holds every
+// created node; `st` = {nodes created, nodes popped, node expanded by the
+// current call (-1 root), expand flag}.
+struct BestFirstParams {
+  int pdl;
+  int R, B, K, D, H, words, bf16;
+  float beta;
+  int max_nodes;                 // node table entries per request (B * K)
+  int32_t* node_par;             // [R][max_nodes] parent node (-1: root)
+  int32_t* node_tok;
+  int32_t* node_dep;
+  int32_t* node_rank;            // popped rank, -1 while in the heap
+  float* node_score;
+  int* st;                       // [R][4]
+  const int32_t* row_tok;        // [R][K] this call's children
+  const float* row_logp;         // [R][K]
+  const void* S_call;            // [256][H] this call's head states
+  void* S_pop;                   // [R][B][H] state of each popped rank
+  void* S_stage;                 // [256][H] parent state of the next expansion
+  const void* S_root;            // [256][H] root states
+  int32_t* tok_next;             // [R] token of the next expansion
+  int32_t* z_row;                // [R] depth of the next expanded node (z row of its children)
+  int V;
+  const float* z;                // [R][D][V] base logits
+  float* z_stage;                // [R][V] the base logits of the next call
+  int32_t* parent;               // outputs, as dartree_tree
+  int32_t* token;
+  int32_t* depth;
+  float* score;
+  uint32_t* mask;
+  int32_t* n_out;
+  int* err;
+};
+cudaError_t launch_bestfirst_init(const BestFirstParams& p, cudaStream_t st);
+cudaError_t launch_bestfirst_step(const BestFirstParams& p, cudaStream_t st);
+cudaError_t launch_bestfirst_z(const BestFirstParams& p, cudaStream_t st);
 
 // Records why the last context-free call on this thread failed; read back
 // through dartree_last_error(NULL).

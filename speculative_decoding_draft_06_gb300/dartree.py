@@ -25,6 +25,9 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "dartree.h")
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "DEVICE_CHECK",
           5: "TIMEOUT", 6: "OOM"}
 W_F32, W_BF16 = 0, 1
+HEAD_KINDS = {"recurrent": 0, "markov": 1}
+CAND_KINDS = {"corrected": 0, "base": 1}
+EXPANSIONS = {"depthwise": 0, "bestfirst": 1}
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -37,6 +40,11 @@ class Config(ctypes.Structure):
 
 class HeadWeights(ctypes.Structure):
     _fields_ = [("A", _vp), ("E", _vp), ("Wout", _vp)]
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("head_kind", ctypes.c_int32), ("candidates", ctypes.c_int32),
+                ("expansion", ctypes.c_int32)]
 
 
 class Tree(ctypes.Structure):
@@ -75,6 +83,9 @@ def load():
         "dartree_destroy": (None, [_vp]),
         "dartree_build": (st, [_vp, _vp, _vp, ctypes.POINTER(HeadWeights), _i32, _i32, _i32,
                                _i32, _i32, ctypes.c_float, ctypes.POINTER(Tree), _vp]),
+        "dartree_build_ex": (st, [_vp, _vp, _vp, ctypes.POINTER(HeadWeights), _i32, _i32,
+                                  _i32, _i32, _i32, ctypes.c_float, ctypes.POINTER(Options),
+                                  ctypes.POINTER(Tree), _vp]),
         "dartree_build_host": (st, [_vp, _vp, _vp, ctypes.POINTER(HeadWeights), _i32, _i32,
                                     _i32, _i32, _i32, ctypes.c_float, ctypes.POINTER(Tree), _vp]),
         "dartree_sync_status": (st, [_vp, _vp]),
@@ -177,9 +188,12 @@ class DARTree:
         return _W16 if self.bf16 else (torch.float32,)
 
     def _head(self, A, E, Wout) -> HeadWeights:
+        """A may be None (Markov head)."""
         wt = self._wtypes()
-        _dev(A, "A", wt), _dev(E, "E", wt), _dev(Wout, "Wout", wt)
-        return HeadWeights(A.data_ptr(), E.data_ptr(), Wout.data_ptr())
+        _dev(E, "E", wt), _dev(Wout, "Wout", wt)
+        if A is not None:
+            _dev(A, "A", wt)
+        return HeadWeights(None if A is None else A.data_ptr(), E.data_ptr(), Wout.data_ptr())
 
     def alloc_tree(self, R: int, B: int, *, device="cuda", pin: bool = False) -> dict:
         words = (B + 31) // 32
@@ -198,8 +212,11 @@ class DARTree:
 
     # ------------------------------------------------------------ the path
     def build(self, z, state0, A, E, Wout, *, D: int, W: int, K: int, B: int, beta: float,
-              out: dict | None = None, stream=None) -> dict:
-        """Asynchronous supertree build; z [R,D,V] fp32, state0 [R,H] fp32."""
+              out: dict | None = None, stream=None, head: str = "recurrent",
+              candidates: str = "corrected", expansion: str = "depthwise") -> dict:
+        """Asynchronous supertree build; z [R,D,V] fp32, state0 [R,H] fp32.
+        ``head`` / ``candidates`` / ``expansion`` select the build variant
+        (dartree_build_ex); the defaults are dartree_build."""
         _dev(z, "z", (torch.float32,)), _dev(state0, "state0", (torch.float32,))
         R = state0.shape[0]
         if z.shape != (R, D, self.V) or state0.shape != (R, self.H):
@@ -207,11 +224,18 @@ class DARTree:
                              f"R={R}, D={D}, V={self.V}, H={self.H}")
         if out is None:
             out = self.alloc_tree(R, B, device=z.device)
-        head = self._head(A, E, Wout)
+        hw = self._head(A, E, Wout)
         t = self._tree(out)
-        self._check(self._lib.dartree_build(self._h, _ptr(z), _ptr(state0), ctypes.byref(head),
-                                            R, D, W, K, B, ctypes.c_float(beta),
-                                            ctypes.byref(t), _stream(stream)))
+        opt = (head, candidates, expansion)
+        if opt == ("recurrent", "corrected", "depthwise"):
+            self._check(self._lib.dartree_build(self._h, _ptr(z), _ptr(state0), ctypes.byref(hw),
+                                                R, D, W, K, B, ctypes.c_float(beta),
+                                                ctypes.byref(t), _stream(stream)))
+        else:
+            o = Options(HEAD_KINDS[head], CAND_KINDS[candidates], EXPANSIONS[expansion])
+            self._check(self._lib.dartree_build_ex(
+                self._h, _ptr(z), _ptr(state0), ctypes.byref(hw), R, D, W, K, B,
+                ctypes.c_float(beta), ctypes.byref(o), ctypes.byref(t), _stream(stream)))
         return out
 
     def build_host(self, z_host, state0_host, A, E, Wout, *, D: int, W: int, K: int, B: int,
@@ -235,7 +259,8 @@ class DARTree:
     def sync_status(self, stream=None) -> int:
         return int(self._lib.dartree_sync_status(self._h, _stream(stream)))
 
-    KERNEL_KINDS = ("head", "state", "merge", "select", "prune", "root")
+    KERNEL_KINDS = ("head", "state", "merge", "select", "prune", "root", "candidates",
+                    "bestfirst")
 
     def set_timing(self, on: bool) -> None:
         self._check(self._lib.dartree_set_timing(self._h, 1 if on else 0))

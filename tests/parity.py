@@ -41,7 +41,7 @@ def forced_frontier(pool: dict, D: int, W: int, K: int):
 
 
 def check_state_steps(inp: dict, bf16: bool, slot, tok, sizes, gpu_states: list,
-                      max_rows: int | None = None) -> int:
+                      max_rows: int | None = None, markov: bool = False) -> int:
     """Each GPU head state of depth >= 2 against the oracle's state step
     applied to the GPU's own parent state and token: equal up to one bf16
     rounding step (+2e-5 absolute near zero) with bf16 weights, 2e-6 with
@@ -53,7 +53,8 @@ def check_state_steps(inp: dict, bf16: bool, slot, tok, sizes, gpu_states: list,
         n = fd if max_rows is None else min(fd, max_rows)
         for i in range(n):
             par = gpu_states[d - 2][slot[base + i]]
-            ref = oracle.state_step(inp["A"], inp["E"], par, int(tok[base + i]), bf16)
+            ref = oracle.state_step(None if markov else inp["A"], inp["E"], par,
+                                    int(tok[base + i]), bf16)
             got = gpu_states[d - 1][i]
             dif = np.abs(got - ref)
             if bf16:
@@ -68,21 +69,23 @@ def check_state_steps(inp: dict, bf16: bool, slot, tok, sizes, gpu_states: list,
 
 def compare_request(inp: dict, r: int, D: int, W: int, K: int, B: int, beta: float,
                     bf16: bool, gpu_pool: dict, gpu_rows: list, gpu_tree: dict,
-                    gpu_states: list | None = None) -> dict:
+                    gpu_states: list | None = None, markov: bool = False,
+                    cand_base: bool = False) -> dict:
     """Teacher-forced comparison of one request.  Raises AssertionError on a
     mismatch that no near-tie explains; returns counters otherwise.  With
     gpu_states (per depth [F_{d-1}, H] fp32), every head call is compared on
-    the GPU's own states and every state step is checked separately."""
+    the GPU's own states and every state step is checked separately.
+    ``markov`` / ``cand_base`` select the build variant."""
     tol = TOL[bf16]
     slot, tok, sizes = forced_frontier(gpu_pool, D, W, K)
     fst = None
     if gpu_states is not None:
-        H = inp["A"].shape[0]
+        H = inp["E"].shape[1]
         fst = np.zeros((D, W, H), np.float32)
         for d, s in enumerate(gpu_states):
             fst[d, :s.shape[0]] = s
     o = oracle.build_tree(inp, r, D, W, K, bf16, force_slot=slot, force_tok=tok,
-                          force_state=fst)
+                          force_state=fst, markov=markov, cand_base=cand_base)
     rep = {"near_ties": 0, "exact_depths": 0, "max_score_err": 0.0, "max_lse_err": 0.0,
            "max_logp_err": 0.0, "topk_near_ties": 0}
     off, F = 0, 1
@@ -131,7 +134,8 @@ def compare_request(inp: dict, r: int, D: int, W: int, K: int, B: int, beta: flo
         off += fd
         F = fd
     if gpu_states is not None:
-        rep["state_flips"] = check_state_steps(inp, bf16, slot, tok, sizes, gpu_states)
+        rep["state_flips"] = check_state_steps(inp, bf16, slot, tok, sizes, gpu_states,
+                                               markov=markov)
     # --- deferred Top-B: a pure function of the pool -> bit-exact
     ref = oracle.topb(gpu_pool["parent"], gpu_pool["token"], gpu_pool["depth"],
                       gpu_pool["score"], B, beta)
@@ -146,4 +150,55 @@ def compare_request(inp: dict, r: int, D: int, W: int, K: int, B: int, beta: flo
     # Lemma 1 on the GPU's pool
     heap = oracle.heap_prune(gpu_pool["parent"], gpu_pool["depth"], gpu_pool["score"], B, beta)
     assert np.array_equal(ref["order"][:n], heap)
+    return rep
+
+
+def compare_bestfirst(inp: dict, r: int, D: int, K: int, B: int, beta: float, bf16: bool,
+                      gpu_tree: dict, gpu_rows: list, gpu_states: list,
+                      markov: bool = False) -> dict:
+    """Teacher-forced comparison of a best-first build of request r.
+
+    gpu_rows[c] / gpu_states[c] are head call c's row ({lse, tok, logp}) and
+    state ([H] fp32).  The oracle replays the build with the GPU's children
+    and states, so the tree (pops, parents, scores, mask) must then match
+    bit for bit; each call the oracle makes is compared with the GPU's row
+    (near-ties at the K-th child allowed) and each state with the oracle's
+    state step from the GPU's parent state."""
+    tol = TOL[bf16]
+    ft = np.stack([x["tok"] for x in gpu_rows]).astype(np.int32)
+    fl = np.stack([x["logp"] for x in gpu_rows]).astype(np.float32)
+    fs = np.stack(gpu_states).astype(np.float32)
+    o = oracle.bestfirst(inp, r, D, K, B, beta, bf16, markov=markov, force_tok=ft,
+                         force_logp=fl, force_state=fs)
+    n = int(gpu_tree["n_out"])
+    assert n == o["n_out"], (n, o["n_out"])
+    for k in ("parent", "token", "depth"):
+        assert np.array_equal(gpu_tree[k], o[k]), k
+    assert np.array_equal(gpu_tree["score"].view(np.uint32), o["score"].view(np.uint32))
+    assert np.array_equal(gpu_tree["mask"].reshape(o["mask"].shape).view(np.uint32), o["mask"])
+    rep = {"calls": o["calls"], "topk_near_ties": 0, "max_lse_err": 0.0, "max_logp_err": 0.0}
+    for c in range(B):
+        if o["call_rank"][c] < -1:
+            continue                               # a call whose result is unused
+        g = gpu_rows[c]
+        err = abs(float(g["lse"]) - o["row_lse"][c])
+        rep["max_lse_err"] = max(rep["max_lse_err"], err)
+        assert err <= tol, (c, float(g["lse"]), o["row_lse"][c])
+        olp = {int(t): float(v) for t, v in zip(o["row_tok"][c], o["row_logp"][c])}
+        if set(g["tok"].tolist()) != set(olp):
+            assert o["row_kgap"][c] < NEAR_TIE and len(set(g["tok"].tolist()) - set(olp)) == 1, c
+            rep["topk_near_ties"] += 1
+        e = max((abs(float(lp) - olp[int(t)]) for t, lp in zip(g["tok"], g["logp"])
+                 if int(t) in olp), default=0.0)
+        rep["max_logp_err"] = max(rep["max_logp_err"], e)
+        assert e <= tol, (c, e)
+        if c >= 1:                                 # the state of rank c-1
+            q = c - 1
+            pr = int(o["parent"][q])
+            par = gpu_states[0] if pr < 0 else gpu_states[pr + 1]
+            ref = oracle.state_step(None if markov else inp["A"], inp["E"], par,
+                                    int(o["token"][q]), bf16)
+            dif = np.abs(gpu_states[c] - ref)
+            lim = (np.spacing(np.abs(ref).astype(np.float32)) * 2 ** 16 + 2e-5) if bf16 else 2e-6
+            assert np.all(dif <= lim), (c, float(dif.max()))
     return rep
