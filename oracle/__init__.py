@@ -69,6 +69,10 @@ def _load():
         lib.orc_cand_row.restype = None
         lib.orc_bestfirst.argtypes = [ctypes.c_int] * 6 + [f32] + [P] * 21
         lib.orc_bestfirst.restype = ctypes.c_int
+        lib.orc_tree_attention.argtypes = [ctypes.c_int] * 6 + [f32] + [P] * 7
+        lib.orc_tree_attention.restype = ctypes.c_int
+        lib.orc_accept.argtypes = [ctypes.c_int] * 2 + [P] * 6
+        lib.orc_accept.restype = ctypes.c_int
         lib.orc_topb.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_int, f32] + [P] * 7
         lib.orc_topb.restype = ctypes.c_int
         lib.orc_heap_prune.argtypes = [ctypes.c_int, P, P, P, ctypes.c_int, f32, P]
@@ -276,3 +280,37 @@ def bestfirst(inp: dict, r: int, D: int, K: int, B: int, beta: float, bf16: bool
     o["calls"] = int(calls[0])
     o["mask"] = o["mask"].reshape(B, words)
     return o
+
+
+def tree_attention(Q, Kp, Vp, Kt, Vt, mask, scale: float, bf16: bool) -> np.ndarray:
+    """Tree attention of one request (see orc_tree_attention): Q [B+1, Hq, dh],
+    Kp/Vp [Lp, Hkv, dh], Kt/Vt [B, Hkv, dh] (bf16 bits or fp32), mask
+    [B, words] -> O [B+1, Hq, dh] fp32."""
+    Bp1, Hq, dh = Q.shape
+    B = Bp1 - 1
+    Lp, Hkv = Kp.shape[0], Kp.shape[1]
+    arrs = [_weights(x, bf16) for x in (Q, Kp, Vp, Kt, Vt)]
+    m = _c(mask, np.uint32).reshape(-1)
+    O = np.empty((Bp1, Hq, dh), np.float32)
+    rc = _load().orc_tree_attention(Lp, B, Hq, Hkv, dh, int(bf16), ctypes.c_float(scale),
+                                    *[_ptr(a) for a in arrs], _ptr(m), _ptr(O))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_tree_attention failed with code {rc}")
+    return O
+
+
+def accept(parent, token, n_out: int, pred) -> dict:
+    """Longest accepted prefix of one request's tree under the target's
+    predictions pred [B+1] (root first)."""
+    pp, tt = _c(parent, np.int32), _c(token, np.int32)
+    pr = _c(pred, np.int32)
+    B = pp.shape[0]
+    nodes = np.full(max(B, 1), -1, np.int32)
+    ln = np.zeros(1, np.int32)
+    bonus = np.zeros(1, np.int32)
+    rc = _load().orc_accept(B, n_out, _ptr(pp), _ptr(tt), _ptr(pr), _ptr(ln), _ptr(nodes),
+                            _ptr(bonus))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_accept failed with code {rc}")
+    n = int(ln[0])
+    return {"len": n, "nodes": nodes[:n].copy(), "bonus": int(bonus[0])}

@@ -711,3 +711,107 @@ done:
     free(heap); free(s_root); free(s_rank); free(ell); free(tk); free(tv);
     return rc;
 }
+
+/* ------------------------------------------- verification: tree attention */
+
+/*
+ * One attention layer of the target's verification forward over the prefix
+ * and the draft tree.  [P1] Core Mechanism (the verification tree and a
+ * sparse attention mask let the target check every branch in ONE forward,
+ * then the longest matching prefix is accepted); [P2] Methodologie 2
+ * (Verificatie: one forward pass with tree attention); [P3] Summary.
+ *
+ * Query rows: row 0 is the root (the last verified token, whose key and
+ * value are the last prefix position), rows 1..B are the tree nodes in the
+ * build's canonical order.  Row 0 attends to the Lp prefix positions; row
+ * i >= 1 attends to the prefix and to the tree nodes j with bit j of mask
+ * row i-1 (its ancestors and itself).  Grouped heads: query head h reads
+ * key/value head h / (Hq / Hkv).
+ *   O[i,h] = sum_j softmax_j(scale * q[i,h] . k[j,h']) v[j,h']   (fp64)
+ * Layouts (one request): Q [B+1][Hq][dh], Kp/Vp [Lp][Hkv][dh],
+ * Kt/Vt [B][Hkv][dh] (bf16 bits or fp32 as `bf16` says), mask [B][words],
+ * O [B+1][Hq][dh] fp32.
+ */
+int orc_tree_attention(int Lp, int B, int Hq, int Hkv, int dh, int bf16, float scale,
+                       const void *Q, const void *Kp, const void *Vp,
+                       const void *Kt, const void *Vt, const uint32_t *mask,
+                       float *O) {
+    if (Lp < 0 || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || dh < 1 || Lp + B < 1)
+        return ORC_ERR_ARG;
+    const int words = (B + 31) / 32;
+    const int g = Hq / Hkv;
+    double *s = malloc(sizeof(double) * (size_t)(Lp + B > 0 ? Lp + B : 1));
+    if (!s) return ORC_ERR_MEM;
+    for (int i = 0; i <= B; ++i) {
+        for (int h = 0; h < Hq; ++h) {
+            const int hk = h / g;
+            const size_t qo = ((size_t)i * Hq + h) * dh;
+            double m = -INFINITY;
+            /* scores of every key the row may see; -inf for the others */
+            for (int j = 0; j < Lp + B; ++j) {
+                int visible;
+                const void *K;
+                size_t ko;
+                if (j < Lp) {
+                    visible = 1;
+                    K = Kp;
+                    ko = ((size_t)j * Hkv + hk) * dh;
+                } else {
+                    const int t = j - Lp;
+                    visible = i >= 1 && ((mask[(size_t)(i - 1) * words + t / 32] >> (t % 32)) & 1u);
+                    K = Kt;
+                    ko = ((size_t)t * Hkv + hk) * dh;
+                }
+                if (!visible) { s[j] = -INFINITY; continue; }
+                double acc = 0.0;
+                for (int c = 0; c < dh; ++c)
+                    acc += weight(Q, bf16, qo + c) * weight(K, bf16, ko + c);
+                s[j] = (double)scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < Lp + B; ++j) l += (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m);
+            for (int c = 0; c < dh; ++c) {
+                double acc = 0.0;
+                for (int j = 0; j < Lp + B; ++j) {
+                    if (s[j] == -INFINITY) continue;
+                    const size_t vo = (j < Lp) ? ((size_t)j * Hkv + hk) * dh
+                                               : ((size_t)(j - Lp) * Hkv + hk) * dh;
+                    acc += exp(s[j] - m) * weight(j < Lp ? Vp : Vt, bf16, vo + c);
+                }
+                O[qo + c] = (l > 0.0) ? (float)(acc / l) : 0.0f;
+            }
+        }
+    }
+    free(s);
+    return ORC_OK;
+}
+
+/*
+ * Longest accepted prefix.  pred[0] is the target's token after the root,
+ * pred[i] (i = 1..B) its token after tree node i-1.  Starting at the root,
+ * the child (among the first n_out nodes, parent rank = current node, -1 for
+ * the root) whose token equals the current node's prediction is accepted
+ * and becomes the current node; siblings carry distinct tokens, so at most
+ * one child matches.  [P1] Core Mechanism ("accept longest matching
+ * prefix").  Outputs: accept_len, accept_nodes[0..accept_len) (ranks),
+ * bonus = the prediction at the last accepted node (the root's if none).
+ */
+int orc_accept(int B, int n_out, const int32_t *parent, const int32_t *token,
+               const int32_t *pred, int32_t *accept_len, int32_t *accept_nodes,
+               int32_t *bonus) {
+    if (B < 0 || n_out < 0 || n_out > B) return ORC_ERR_ARG;
+    int cur = -1, len = 0;
+    for (;;) {
+        const int32_t want = pred[cur + 1];
+        int next = -1;
+        for (int n = 0; n < n_out; ++n)
+            if (parent[n] == cur && token[n] == want) { next = n; break; }
+        if (next < 0) break;
+        accept_nodes[len++] = next;
+        cur = next;
+    }
+    *accept_len = len;
+    *bonus = pred[cur + 1];
+    return ORC_OK;
+}
