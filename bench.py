@@ -66,6 +66,7 @@ VARIANTS = {
     "base": {"candidates": "base"},
     "markov-base": {"head": "markov", "candidates": "base"},
     "bestfirst": {"expansion": "bestfirst"},
+    "verify": {},    # the default build followed by the verification consumer
 }
 
 
@@ -504,6 +505,148 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
+def measured_bf16_tflops() -> tuple[float, str]:
+    p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_verify(args) -> None:
+    """A step = one default build, then the verification consumer on its
+    tree: tree attention of a synthetic target layer (Qwen3-8B attention
+    shape, 2048 prefix positions) with the build's mask, the target's greedy
+    token per row through an output projection [V, 4096] (the head-call
+    kernel, K = 1, zero base logits; the stand-in projection is the head's
+    Wout), and the longest accepted prefix.  One GPU (replicas as run_gpu)."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_draft_06_gb300 import dartree as dtl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    w = I.CONFIGS[args.config]
+    if world > 1:
+        w = w.replace(seed=w.seed + 7919 * rank)
+    vs = I.VerifyShape()
+    inp = I.make_inputs(w)
+    dev = dtl.weights_to_device(inp, w.bf16)
+    xv = I.make_verify_inputs(w.R, w.B, vs)
+    xd = {k: torch.from_numpy(v.view(np.int16)).cuda() for k, v in xv.items()}
+    ctx = dtl.DARTree(w.V, w.H, max_D=w.D, max_W=w.W, max_K=w.K, max_B=w.B,
+                      max_requests=w.R, bf16=w.bf16)
+    H2 = vs.Hq * vs.dh
+    rows = w.R * (w.B + 1)
+    tgt = dtl.DARTree(w.V, H2, max_D=1, max_W=rows, max_K=1, max_B=1, bf16=True)
+    U = dev["Wout"] if H2 == w.H else None
+    if U is None:
+        raise SystemExit("verify: the stand-in projection needs H == Hq * dh")
+    zero = torch.zeros(w.V, dtype=torch.float32, device="cuda")
+    work = torch.empty(max(16, dtl.load().dartree_tree_attention_workspace(
+        w.R, vs.Lp, w.B, vs.Hq, vs.Hkv)), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    out = ctx.alloc_tree(w.R, w.B)
+    kw = dict(D=w.D, W=w.W, K=w.K, B=w.B, beta=w.beta, out=out, stream=stream)
+    args_t = (dev["z"], dev["state0"], dev["A"], dev["E"], dev["Wout"])
+    ev = {}
+
+    def step(timed: bool = False):
+        ctx.build(*args_t, **kw)
+        with torch.cuda.stream(stream):
+            if timed:
+                ev["a0"].record(stream)
+            att = dtl.tree_attention(xd["Q"], xd["Kp"], xd["Vp"], xd["Kt"], xd["Vt"],
+                                     out["mask"], work=work, stream=stream)
+            if timed:
+                ev["a1"].record(stream)
+            S = att["O16"].view(rows, H2)
+            r = tgt.head_topk(S, zero, U, K=1, rows_per_req=rows, stream=stream)
+            if timed:
+                ev["p1"].record(stream)
+            pred = r["tok"].view(w.R, w.B + 1)
+            acc = dtl.accept(out["parent"], out["token"], out["n_out"], pred, max_len=w.D,
+                             stream=stream)
+        return acc
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    clock_info = clocks.stop()
+    ctx.sync(stream)
+    ms = aggregate(e0.elapsed_time(e1) / args.steps, world)
+    # the attention and projection launches alone (events on the same stream)
+    ev = {k: torch.cuda.Event(enable_timing=True) for k in ("a0", "a1", "p1")}
+    n_t = min(args.steps, 20)
+    t_att = t_proj = 0.0
+    for _ in range(n_t):
+        acc = step(timed=True)
+        stream.synchronize()
+        t_att += ev["a0"].elapsed_time(ev["a1"])
+        t_proj += ev["a1"].elapsed_time(ev["p1"])
+    t_att /= n_t
+    t_proj /= n_t
+    acc_len = acc["len"].cpu().numpy()
+    depth = out["depth"].cpu().numpy()
+    n_out = out["n_out"].cpu().numpy()
+    # attention flops: QK and PV, 2 * 2 * dh per visible (row, key) pair
+    vis = sum(vs.Hq * ((w.B + 1) * vs.Lp + int(depth[r, :n_out[r]].sum())) for r in range(w.R))
+    att_flops = 4.0 * vs.dh * vis
+    tfl, tfl_kind = measured_bf16_tflops()
+    proj_bytes = w.V * H2 * 2 + w.V * 4 + rows * H2 * 2
+    peak, peak_kind = measured_peaks()
+    if rank == 0:
+        value = world * w.R * 1e3 / ms
+        line = {
+            "metric": "supertree builds + verifications/s", "value": value,
+            "unit": "verified builds/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "variant": "verify",
+            "config": dict(workload_config(w), verify=(
+                f"target layer: prefix {vs.Lp}, {vs.Hq} query heads, {vs.Hkv} kv heads, head "
+                f"dim {vs.dh}; projection [V, {H2}] (the head's Wout as stand-in)")),
+            "roofline": {"bound": "hbm", "kernel": "k_head_tc (target output projection, "
+                         f"{rows} rows, K=1)", "achieved": proj_bytes / (t_proj * 1e-3) / 1e9,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": proj_bytes / (t_proj * 1e-3) / 1e9 / peak,
+                         "peak_source": peak_kind, "traffic": None,
+                         "bytes_per_launch": proj_bytes, "launch_ms": t_proj},
+            "attention": {"kernel": "k_tree_attention (bf16 mma.sync m16n8k16, online softmax, key split)",
+                          "bound": "tensor", "launch_ms": t_att,
+                          "achieved": att_flops / (t_att * 1e-3) / 1e12, "peak": tfl,
+                          "unit": "TFLOP/s", "frac": att_flops / (t_att * 1e-3) / 1e12 / tfl,
+                          "peak_source": tfl_kind, "flops_per_launch": att_flops},
+            "accept_len_mean": float(acc_len.mean()),
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": (kernels_per_build(w) + 4) * args.steps,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    tgt.close()
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_profile_head(args) -> None:
     """N head calls on one stream, for ncu captures of k_head_tc on a case
     that still streams its weights from HBM but holds only a few GB."""
@@ -540,6 +683,8 @@ def main(argv=None):
         return
     if args.impl == "reference":
         run_reference(args)
+    elif args.variant == "verify":
+        run_verify(args)
     else:
         run_gpu(args)
 

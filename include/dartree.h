@@ -289,6 +289,61 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
                                           const void *E, int32_t H, int32_t M, void *S_out,
                                           void *stream);
 
+/* ------------------------------------------------------------------
+ * Verification consumer of a built tree ("DARTree: Teaching a Chain-Trained
+ * Corrector to Think in Trees", Core Mechanism: the verification tree and
+ * its sparse attention mask let the target check every branch in one
+ * forward, then the longest matching prefix is accepted; "Technische
+ * Samenvatting: DARTree", Methodologie 2, Verificatie).  Context-free,
+ * asynchronous on `stream`, no allocation.  Errors are INVALID_ARG /
+ * UNSUPPORTED before any launch; dartree_last_error(NULL) has the text.
+ * ------------------------------------------------------------------ */
+
+/* One attention layer of the target over the prefix and the tree of R
+ * requests (all device memory, bf16 bits unless stated):
+ *   Q    [R][B+1][Hq][dh]  queries; row 0 = the root (the last verified
+ *                          token, already at prefix position Lp-1), rows
+ *                          1..B = the tree nodes in canonical order;
+ *   Kp,Vp [R][Lp][Hkv][dh] prefix keys / values (may be NULL when Lp = 0);
+ *   Kt,Vt [R][B][Hkv][dh]  tree keys / values;
+ *   mask [R][B][ceil(B/32)] the build's ancestor mask (dartree_tree.mask);
+ *   O    [R][B+1][Hq][dh] fp32 out; O_bf16 the same rounded to bf16 (or NULL).
+ * Row 0 attends to the Lp prefix positions; node i attends to the prefix and
+ * to the nodes j of mask row i-1.  Query head h reads key/value head
+ * h / (Hq/Hkv).  O = softmax(scale * q.k) v, fp32 accumulation; the softmax
+ * weights are rounded to bf16 for the P.V product and its normaliser.  A row
+ * with no visible key gives 0.  dh must be 128 (UNSUPPORTED otherwise);
+ * Hq % Hkv == 0, B <= 1024; pointers 16-byte aligned.
+ * work / work_bytes: optional caller-owned device scratch (16-byte aligned)
+ * for splitting the keys over more CTAs when a launch would leave SMs idle;
+ * dartree_tree_attention_workspace() gives the size that allows the largest
+ * split.  NULL or too small: fewer or no splits, same results up to
+ * rounding.  Calls sharing one workspace must not overlap on the GPU. */
+dartree_status dartree_tree_attention(const void *Q, const void *Kp, const void *Vp,
+                                      const void *Kt, const void *Vt, const uint32_t *mask,
+                                      int32_t R, int32_t Lp, int32_t B, int32_t Hq, int32_t Hkv,
+                                      int32_t dh, float scale, float *O, void *O_bf16,
+                                      void *work, size_t work_bytes, void *stream);
+
+/* Workspace bytes for the largest key split of dartree_tree_attention (0 on
+ * bad sizes). */
+size_t dartree_tree_attention_workspace(int32_t R, int32_t Lp, int32_t B, int32_t Hq,
+                                        int32_t Hkv);
+
+/* Longest accepted prefix of each request's tree (device memory):
+ *   parent, token [R][B], n_out [R]  the build's output;
+ *   pred [R][B+1]  the target's token after the root (0) and after node i (i+1).
+ * From the root, the child whose token equals the current node's prediction
+ * is accepted and becomes the current node (siblings carry distinct tokens).
+ * Out: accept_len [R] (number of accepted draft tokens), accept_nodes
+ * [R][max_len] (their ranks in order, -1 after the end; a longer path keeps
+ * only its first max_len ranks), bonus [R] (the prediction at the last
+ * accepted node, the root's when none). */
+dartree_status dartree_accept(const int32_t *parent, const int32_t *token, const int32_t *n_out,
+                              const int32_t *pred, int32_t R, int32_t B, int32_t max_len,
+                              int32_t *accept_len, int32_t *accept_nodes, int32_t *bonus,
+                              void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -104,6 +104,11 @@ def load():
         "dartree_reset_timing": (st, [_vp]),
         "dartree_state_step_noalloc": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
         "dartree_get_states": (st, [_vp, _i32, _vp, _vp]),
+        "dartree_tree_attention": (st, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                        _i32, _i32, ctypes.c_float, _vp, _vp, _vp,
+                                        ctypes.c_size_t, _vp]),
+        "dartree_tree_attention_workspace": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
+        "dartree_accept": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -381,3 +386,50 @@ def weights_to_device(inp: dict, bf16: bool, device="cuda") -> dict:
     return {"A": w(inp["A"]), "E": w(inp["E"]), "Wout": w(inp["Wout"]),
             "z": torch.from_numpy(inp["z"]).to(device),
             "state0": torch.from_numpy(inp["state0"]).to(device)}
+
+
+def _check_free(s: int) -> None:
+    if s != 0:
+        raise DartreeError(s, load().dartree_last_error(None).decode())
+
+
+def tree_attention(Q, Kp, Vp, Kt, Vt, mask, *, scale: float | None = None, want_bf16: bool = True,
+                   work=None, split: bool = True, stream=None) -> dict:
+    """Tree attention of the verification forward (dartree_tree_attention):
+    Q [R,B+1,Hq,dh], Kp/Vp [R,Lp,Hkv,dh], Kt/Vt [R,B,Hkv,dh] (bf16 CUDA
+    tensors), mask [R,B,words] int32 -> {"O": fp32, "O16": bf16 bits}.
+    ``work`` is the key-split scratch (allocated here when None and
+    ``split``; ``split=False`` runs unsplit)."""
+    for n, t in (("Q", Q), ("Kt", Kt), ("Vt", Vt), ("Kp", Kp), ("Vp", Vp)):
+        _dev(t, n, _W16)
+    _dev(mask, "mask", (torch.int32,))
+    R, Bp1, Hq, dh = Q.shape
+    Lp, Hkv = Kp.shape[1], Kp.shape[2]
+    O = torch.empty(R, Bp1, Hq, dh, dtype=torch.float32, device=Q.device)
+    O16 = torch.empty(R, Bp1, Hq, dh, dtype=torch.int16, device=Q.device) if want_bf16 else None
+    sc = float(scale) if scale is not None else dh ** -0.5
+    if work is None and split:
+        n = int(load().dartree_tree_attention_workspace(R, Lp, Bp1 - 1, Hq, Hkv))
+        work = torch.empty(max(n, 16), dtype=torch.uint8, device=Q.device)
+    wb = 0 if work is None else work.numel() * work.element_size()
+    _check_free(load().dartree_tree_attention(
+        _ptr(Q), _ptr(Kp) if Lp else None, _ptr(Vp) if Lp else None, _ptr(Kt), _ptr(Vt),
+        _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh, ctypes.c_float(sc), _ptr(O), _ptr(O16),
+        _ptr(work), wb, _stream(stream)))
+    return {"O": O, "O16": O16}
+
+
+def accept(parent, token, n_out, pred, *, max_len: int, stream=None) -> dict:
+    """Longest accepted prefix per request (dartree_accept); CUDA int32
+    tensors parent/token [R,B], n_out [R], pred [R,B+1]."""
+    for n, t in (("parent", parent), ("token", token), ("n_out", n_out), ("pred", pred)):
+        _dev(t, n, (torch.int32,))
+    R, B = parent.shape
+    dev = parent.device
+    o = {"len": torch.empty(R, dtype=torch.int32, device=dev),
+         "nodes": torch.empty(R, max(max_len, 1), dtype=torch.int32, device=dev),
+         "bonus": torch.empty(R, dtype=torch.int32, device=dev)}
+    _check_free(load().dartree_accept(_ptr(parent), _ptr(token), _ptr(n_out), _ptr(pred), R, B,
+                                      max_len, _ptr(o["len"]), _ptr(o["nodes"]), _ptr(o["bonus"]),
+                                      _stream(stream)))
+    return o

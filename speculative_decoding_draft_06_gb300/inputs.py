@@ -201,3 +201,48 @@ def small_workload(seed: int, *, V: int, H: int, D: int, W: int, K: int,
     return Workload(f"small-{seed}", V=V, H=H, D=D, W=W, K=K, B=B, beta=beta,
                     bf16=bf16, R=R, zipf_s=zipf_s, sigma=sigma,
                     seed=90000 + seed)
+
+
+# ------------------------------------------------ verification consumer
+
+@dataclasses.dataclass(frozen=True)
+class VerifyShape:
+    """One attention layer of a synthetic target over prefix + draft tree.
+    Qwen3-8B attention shape: 32 query heads, 8 key/value heads, head dim 128
+    (Hq * dh = 4096 = the hidden size, so the layer's output feeds an output
+    projection of the head's shape)."""
+    Lp: int = 2048
+    Hq: int = 32
+    Hkv: int = 8
+    dh: int = 128
+    seed: int = 20261202 + 7000
+
+
+def make_verify_inputs(R: int, B: int, s: VerifyShape) -> dict:
+    """Seeded synthetic Q [R,B+1,Hq,dh], prefix Kp/Vp [R,Lp,Hkv,dh] and tree
+    Kt/Vt [R,B,Hkv,dh], all N(0,1) rounded to bf16 bits."""
+    root = np.random.SeedSequence(s.seed + 31 * R + B)
+    kids = root.spawn(5)
+    shapes = [(R, B + 1, s.Hq, s.dh), (R, s.Lp, s.Hkv, s.dh), (R, s.Lp, s.Hkv, s.dh),
+              (R, B, s.Hkv, s.dh), (R, B, s.Hkv, s.dh)]
+    out = {}
+    for name, ss, shp in zip(("Q", "Kp", "Vp", "Kt", "Vt"), kids, shapes):
+        rows = int(np.prod(shp[:-1]))
+        out[name] = _normal_matrix(ss, max(rows, 1), shp[-1], 1.0, True)[:rows].reshape(shp)
+    return out
+
+
+def random_tree(g: np.random.Generator, B: int, n_out: int | None = None) -> dict:
+    """A random rooted tree in canonical form: parent ranks before their
+    children (parent -1 = the root), distinct tokens among siblings; rows
+    at or beyond n_out are empty (parent/token -1, depth 0)."""
+    n_out = B if n_out is None else n_out
+    parent = np.full(B, -1, np.int32)
+    token = np.full(B, -1, np.int32)
+    depth = np.zeros(B, np.int32)
+    for n in range(n_out):
+        parent[n] = -1 if n == 0 or g.random() < 0.2 else int(g.integers(0, n))
+        sib = int(np.count_nonzero(parent[:n] == parent[n]))
+        token[n] = 1000 * (parent[n] + 1) + sib
+        depth[n] = 1 if parent[n] < 0 else depth[parent[n]] + 1
+    return {"parent": parent, "token": token, "depth": depth, "n_out": n_out}
