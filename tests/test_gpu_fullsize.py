@@ -134,3 +134,111 @@ def test_full_size_properties_and_sampled_rows(name):
     if w.R > 1:
         samples += [(w.R - 1, 1, 0), (w.R // 2, w.D // 2, 1)]
     _check_sampled_rows(inp, w, res, samples)
+
+
+# ------------------------------------------------ build variants at full size
+
+def _run_variant(w, **variant):
+    inp = I.make_inputs(w)
+    dev = dtl.weights_to_device(inp, w.bf16)
+    ctx = gu.make_ctx(w)
+    s = torch.cuda.Stream()
+    out = ctx.alloc_tree(w.R, w.B)
+    kw = dict(D=w.D, W=w.W, K=w.K, B=w.B, beta=w.beta, out=out, stream=s, **variant)
+    for _ in range(2):
+        ctx.build(dev["z"], dev["state0"], dev["A"], dev["E"], dev["Wout"], **kw)
+    ctx.sync(s)
+    return inp, ctx, out
+
+
+@pytest.mark.parametrize("variant", [dict(head="markov"), dict(candidates="base")])
+def test_q8b_depthwise_variants_properties_and_sampled_rows(variant):
+    w = I.CONFIGS["q8b"]
+    inp, ctx, out = _run_variant(w, **variant)
+    res = {"pool": {k: v.numpy() for k, v in ctx.get_pool(w.R, w.pool_size()).items()},
+           "tree": {k: v.cpu().numpy() for k, v in out.items()}, "rows": [], "states": []}
+    F = 1
+    for d, fd in enumerate(w.frontier_sizes(), 1):
+        res["rows"].append({k: v.numpy() for k, v in ctx.get_rows(d, w.R * F, w.K).items()})
+        res["states"].append(ctx.get_states(d, w.R * F))
+        F = fd
+    res["head_calls"] = ctx.head_calls()
+    ctx.close()
+    _check_properties(w, res)
+    markov = variant.get("head") == "markov"
+    base = variant.get("candidates") == "base"
+    pool, rows, _ = gu.split_request(res, w, 0)
+    states = gu.request_states(res, w, 0)
+    offs = np.concatenate([[0], np.cumsum(w.frontier_sizes())])
+    tol = parity.TOL[True]
+    for (d, i) in [(1, 0), (2, 3), (w.D, 15)]:
+        s = states[d - 1][i]
+        if d >= 2:                         # the state step that produced this row
+            node = int(offs[d - 2]) + i
+            par = int(pool["parent"][node])
+            ps = states[d - 2][0] if par < 0 else states[d - 2][par - int(offs[d - 3])]
+            ref = oracle.state_step(None if markov else inp["A"], inp["E"], ps,
+                                    int(pool["token"][node]), True)
+            ulp = np.spacing(np.abs(ref)) * 2 ** 16
+            assert np.all(np.abs(s - ref) <= ulp + 2e-5), (d, i)
+        g_lse, g_tok, g_lp = rows[d - 1]["lse"][i], rows[d - 1]["tok"][i], rows[d - 1]["logp"][i]
+        if base:
+            z = torch.from_numpy(inp["z"][0, d - 1].astype(np.float64))
+            cand = torch.sort(z, descending=True, stable=True).indices[:w.K].numpy()
+            assert set(g_tok.tolist()) == set(cand.tolist()), (d, i)
+            tk, val, lse = oracle.cand_row(inp["z"][0, d - 1], inp["Wout"], s, cand, True)
+            ref_lp = {int(t): float(np.float64(v) - lse) for t, v in zip(tk, val)}
+        else:
+            ell, lse = oracle.logits_row(inp["z"][0, d - 1], inp["Wout"], s, True)
+            tk, _, gap = oracle.topk_row(ell, w.K)
+            if gap >= parity.NEAR_TIE:
+                assert set(g_tok.tolist()) == set(tk.tolist()), (d, i)
+            ref_lp = {int(t): float(np.float64(ell[t]) - lse) for t in g_tok}
+        assert abs(g_lse - lse) <= 1e-4, (d, i, g_lse, lse)
+        assert max(abs(float(lp) - ref_lp[int(t)]) for t, lp in zip(g_tok, g_lp)) <= min(tol, 1e-4)
+
+
+def test_q8b_bestfirst_properties_and_sampled_calls():
+    w = I.CONFIGS["q8b"]
+    inp, ctx, out = _run_variant(w, expansion="bestfirst")
+    assert ctx.head_calls() == w.B
+    t = {k: v.cpu().numpy()[0] for k, v in out.items()}
+    n = int(t["n_out"])
+    assert n == w.B
+    calls = {}
+    for c in sorted({0, 1, 2, n // 2, n - 1}):
+        calls[c] = ({k: v.numpy()[0] for k, v in ctx.get_rows(c + 1, 1, w.K).items()},
+                    ctx.get_states(c + 1, 1)[0])
+    all_rows = [{k: v.numpy()[0] for k, v in ctx.get_rows(c + 1, 1, w.K).items()}
+                for c in range(n)]
+    ctx.close()
+    beta = np.float32(w.beta)
+    key = (t["score"][:n] + beta * t["depth"][:n].astype(np.float32)).astype(np.float32)
+    assert np.all(np.diff(key) <= 0)                    # pops in best-first order
+    for q in range(n):
+        pr = int(t["parent"][q])
+        assert pr < q
+        assert t["depth"][q] == (1 if pr < 0 else t["depth"][pr] + 1)
+        # its score is its parent's plus the log-prob its parent's call gave it
+        row = all_rows[pr + 1]
+        j = int(np.flatnonzero(row["tok"] == t["token"][q])[0])
+        base = np.float32(0.0) if pr < 0 else t["score"][pr]
+        assert np.float32(base + row["logp"][j]) == t["score"][q]
+    words = (w.B + 31) // 32
+    mask = t["mask"].reshape(w.B, words).view(np.uint32)
+    for q in range(n):
+        anc, u = set(), q
+        while u >= 0:
+            anc.add(u)
+            u = int(t["parent"][u])
+        bits = {j for j in range(w.B) if mask[q, j // 32] >> (j % 32) & 1}
+        assert bits == anc
+    for c, (row, s) in calls.items():          # sampled calls from the GPU's own states
+        if c >= 1 and t["depth"][c - 1] >= w.D:
+            continue
+        d_child = 1 if c == 0 else int(t["depth"][c - 1]) + 1
+        ell, lse = oracle.logits_row(inp["z"][0, d_child - 1], inp["Wout"], s, True)
+        tk, _, gap = oracle.topk_row(ell, w.K)
+        assert abs(row["lse"] - lse) <= 1e-4, (c, row["lse"], lse)
+        if gap >= parity.NEAR_TIE:
+            assert set(row["tok"].tolist()) == set(tk.tolist()), c
