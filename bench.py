@@ -542,6 +542,7 @@ def run_verify(args) -> None:
     dev = dtl.weights_to_device(inp, w.bf16)
     xv = I.make_verify_inputs(w.R, w.B, vs)
     xd = {k: torch.from_numpy(v.view(np.int16)).cuda() for k, v in xv.items()}
+    Kc, VTc = dtl.kv_cache(xd["Kp"], xd["Vp"], xd["Kt"], xd["Vt"])
     ctx = dtl.DARTree(w.V, w.H, max_D=w.D, max_W=w.W, max_K=w.K, max_B=w.B,
                       max_requests=w.R, bf16=w.bf16)
     H2 = vs.Hq * vs.dh
@@ -564,8 +565,8 @@ def run_verify(args) -> None:
         with torch.cuda.stream(stream):
             if timed:
                 ev["a0"].record(stream)
-            att = dtl.tree_attention(xd["Q"], xd["Kp"], xd["Vp"], xd["Kt"], xd["Vt"],
-                                     out["mask"], work=work, stream=stream)
+            att = dtl.tree_attention(xd["Q"], Kc, VTc, out["mask"], Lp=vs.Lp, work=work,
+                                     stream=stream)
             if timed:
                 ev["a1"].record(stream)
             S = att["O16"].view(rows, H2)
@@ -629,7 +630,7 @@ def run_verify(args) -> None:
                          "frac": proj_bytes / (t_proj * 1e-3) / 1e9 / peak,
                          "peak_source": peak_kind, "traffic": None,
                          "bytes_per_launch": proj_bytes, "launch_ms": t_proj},
-            "attention": {"kernel": "k_tree_attention (bf16 mma.sync m16n8k16, online softmax, key split)",
+            "attention": {"kernel": "k_tree_attention (tcgen05, S and O in TMEM, two-pass softmax, key split)",
                           "bound": "tensor", "launch_ms": t_att,
                           "achieved": att_flops / (t_att * 1e-3) / 1e12, "peak": tfl,
                           "unit": "TFLOP/s", "frac": att_flops / (t_att * 1e-3) / 1e12 / tfl,

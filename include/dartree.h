@@ -304,26 +304,31 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
  *   Q    [R][B+1][Hq][dh]  queries; row 0 = the root (the last verified
  *                          token, already at prefix position Lp-1), rows
  *                          1..B = the tree nodes in canonical order;
- *   Kp,Vp [R][Lp][Hkv][dh] prefix keys / values (may be NULL when Lp = 0);
- *   Kt,Vt [R][B][Hkv][dh]  tree keys / values;
+ *   K    [R][L][Hkv][dh]   the key cache, L = Lp + B: the Lp prefix keys,
+ *                          then the B tree nodes' keys in canonical order;
+ *   Vt   [R][Hkv][dh][ldv] the value cache, transposed (keys innermost,
+ *                          same key order; ldv >= L, a multiple of 8);
  *   mask [R][B][ceil(B/32)] the build's ancestor mask (dartree_tree.mask);
  *   O    [R][B+1][Hq][dh] fp32 out; O_bf16 the same rounded to bf16 (or NULL).
- * Row 0 attends to the Lp prefix positions; node i attends to the prefix and
- * to the nodes j of mask row i-1.  Query head h reads key/value head
- * h / (Hq/Hkv).  O = softmax(scale * q.k) v, fp32 accumulation; the softmax
- * weights are rounded to bf16 for the P.V product and its normaliser.  A row
- * with no visible key gives 0.  dh must be 128 (UNSUPPORTED otherwise);
- * Hq % Hkv == 0, B <= 1024; pointers 16-byte aligned.
+ * Row 0 attends to the Lp prefix keys; node i attends to the prefix and to
+ * the nodes j of mask row i-1.  Query head h reads key/value head
+ * h / (Hq/Hkv).  O = softmax(scale * q.k) v with fp32 accumulation on the
+ * tensor cores; the softmax weights are rounded to bf16 for the P.V
+ * product and its normaliser.  A row with no visible key gives 0.  dh must
+ * be 128 (UNSUPPORTED otherwise); Hq % Hkv == 0, B <= 1024; Q, K, Vt, O
+ * 16-byte aligned.
  * work / work_bytes: optional caller-owned device scratch (16-byte aligned)
  * for splitting the keys over more CTAs when a launch would leave SMs idle;
  * dartree_tree_attention_workspace() gives the size that allows the largest
  * split.  NULL or too small: fewer or no splits, same results up to
- * rounding.  Calls sharing one workspace must not overlap on the GPU. */
-dartree_status dartree_tree_attention(const void *Q, const void *Kp, const void *Vp,
-                                      const void *Kt, const void *Vt, const uint32_t *mask,
-                                      int32_t R, int32_t Lp, int32_t B, int32_t Hq, int32_t Hkv,
-                                      int32_t dh, float scale, float *O, void *O_bf16,
-                                      void *work, size_t work_bytes, void *stream);
+ * rounding.  Calls sharing one workspace must not overlap on the GPU.
+ * err: optional device word; a bounded pipeline wait that runs out ORs
+ * 2 (timeout) into it (NULL: a library-internal word). */
+dartree_status dartree_tree_attention(const void *Q, const void *K, const void *Vt, int64_t ldv,
+                                      const uint32_t *mask, int32_t R, int32_t Lp, int32_t B,
+                                      int32_t Hq, int32_t Hkv, int32_t dh, float scale, float *O,
+                                      void *O_bf16, void *work, size_t work_bytes, int32_t *err,
+                                      void *stream);
 
 /* Workspace bytes for the largest key split of dartree_tree_attention (0 on
  * bad sizes). */

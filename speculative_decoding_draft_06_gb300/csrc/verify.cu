@@ -6,15 +6,27 @@
 // check every branch in ONE forward, then the longest matching prefix is
 // accepted; "Technische Samenvatting: DARTree", Methodologie 2, Verificatie).
 //
-// Tree attention, flash-style, one pass with an online softmax: a CTA owns
-// 64 query rows (4 warps x 16) of one request and one key/value head; key
-// and value tiles of 64 positions stream through double-buffered shared
-// memory (16-byte async copies, XOR-swizzled rows); scores and P.V run on
-// bf16 warp-level MMAs (m16n8k16, fp32 accumulation), P staying in
-// registers between the two products.  Query row q of a key/value head is
-// (node q / g, query head hk * g + q % g), g = Hq / Hkv.  Row 0 (the root)
-// sees the prefix; node i >= 1 sees the prefix and the tree nodes of mask
-// row i - 1.
+// Tree attention on the 5th-generation tensor cores.  A CTA owns 128 query
+// rows (one TMEM lane each) of one request and one key/value head, and a
+// share of the key range (the keys are split over CTAs until one wave fills
+// the GPU; the last split to finish a query tile combines the partials).
+// Query row q of a key/value head is (node q / g, query head hk * g + q % g),
+// g = Hq / Hkv.  Row 0 (the root) sees the prefix; node i >= 1 sees the
+// prefix and the tree nodes of mask row i - 1.
+//
+// Warp roles (192 threads): warps 0-3 softmax (thread = query row = TMEM
+// lane), warp 4 TMA producer (64-key tiles of K and of the transposed value
+// cache, 128-byte swizzle), warp 5 TMEM allocator + single-thread MMA issuer.
+// Two passes over the CTA's keys: the first finds each row's maximum scaled
+// score (S = Q K^T, M = 128 rows, N = 64 keys, K = 128 head dims); the
+// second recomputes S, forms P = 2^(s - max) rounded to bf16 in shared
+// memory (the 128-byte swizzled K-major layout the MMA reads) and
+// accumulates O += P V (M = 128, N = 128 head dims, K = 64 keys) in TMEM.
+// The rounded weights also form the normaliser, so O is an exact convex
+// combination of the visible values with weights within 2^-8 of the exact
+// softmax.  S is double-buffered in TMEM so the softmax of one tile overlaps
+// the products of the next.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -27,68 +39,34 @@
 namespace dt {
 namespace {
 
-constexpr int kDh = 128;          // head dimension (fixed)
-constexpr int kQRows = 64;        // query rows per CTA
-constexpr int kKeys = 64;         // keys per tile
-constexpr int kAttnThreads = 128;
-constexpr int kRowBytes = kDh * 2;  // 256 B per bf16 row
-constexpr int kTileBytes = kKeys * kRowBytes;
+constexpr int kDh = 128;           // head dimension (fixed)
+constexpr int kQRows = 128;        // query rows per CTA (TMEM lanes)
+constexpr int kKeys = 64;          // keys per tile
+constexpr int kAttnThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kStages = 4;
+constexpr int kQBytes = kQRows * kDh * 2;        // 32 KB: 2 swizzle atoms of 64 head dims
+constexpr int kPBytes = kQRows * kKeys * 2;      // 16 KB per buffer: one atom of 64 keys
+constexpr int kKBytes = kKeys * kDh * 2;         // 16 KB: 2 atoms of 64 head dims
+constexpr int kVBytes = kDh * kKeys * 2;         // 16 KB: 128 head-dim rows x 64 keys
+constexpr int kStageBytes = kKBytes + kVBytes;
+constexpr uint32_t kTmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
+constexpr uint32_t kColO = 128;
 
 struct AttnParams {
-  int Lp, B, Hq, Hkv, g, words, rows;  // rows = (B + 1) * g query rows per key/value head
-  float scale_log2;                     // scale * log2(e)
-  const uint16_t* Q;                    // [R][B+1][Hq][dh]
-  const uint16_t* Kp;                   // [R][Lp][Hkv][dh]
-  const uint16_t* Vp;
-  const uint16_t* Kt;                   // [R][B][Hkv][dh]
-  const uint16_t* Vt;
-  const uint32_t* mask;                 // [R][B][words]
-  float* O;                             // [R][B+1][Hq][dh]
-  uint16_t* O16;                        // same, bf16 bits, or null
-  // key split (flash-decoding): CTA (tile, split) covers a share of the key
-  // tiles; the last split to finish a query tile combines the partials
+  int Lp, B, L, Hq, Hkv, g, words, rows;  // L = Lp + B keys; rows = (B + 1) * g
+  float scale_log2;                       // scale * log2(e)
+  const uint16_t* Q;                      // [R][B+1][Hq][dh]
+  const uint32_t* mask;                   // [R][B][words]
+  float* O;                               // [R][B+1][Hq][dh]
+  uint16_t* O16;                          // same, bf16 bits, or null
+  int* err;
+  long long wait_limit;
   int n_split, q_tiles;
-  float* part_O;                        // [tiles][n_split][64][dh] unnormalised
-  float2* part_ml;                      // [tiles][n_split][64] (max, sum) in base 2
-  int* cnt;                             // [tiles] arrivals, zero before the launch
+  float* part_O;                          // [tiles][n_split][128][dh] unnormalised
+  float2* part_ml;                        // [tiles][n_split][128] (max, sum) in base 2
+  int* cnt;                               // [tiles] arrivals, zero before the launch
 };
-
-// Byte offset of 16-byte chunk c of row r in a swizzled [rows][256 B] tile.
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0: fill with zeros, read nothing
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// d += a (16x16, row) * b (16x8, col), bf16 in, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 // 2^x (approximate hardware exp2; -inf -> +0).
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -104,280 +82,385 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   return d;
 }
 
-// Two fp32 -> packed bf16 pair (round to nearest even), lower column first.
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return static_cast<uint32_t>(float_to_bf16_bits(lo)) |
-         (static_cast<uint32_t>(float_to_bf16_bits(hi)) << 16);
+// 4-D tiled load (x, y, z, w) into shared memory, bytes completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
 }
 
-// Stage key/value tile `t` (keys t*64 .. t*64+63 of prefix + tree) of head hk.
-__device__ __forceinline__ void load_kv(const AttnParams& p, int r, int hk, int t, uint32_t sK,
-                                        uint32_t sV) {
-  for (int e = threadIdx.x; e < kKeys * 16; e += kAttnThreads) {
-    const int row = e >> 4, c = e & 15;
-    const int j = t * kKeys + row;
-    const uint16_t *k, *v;
-    bool valid = true;
-    if (j < p.Lp) {
-      const size_t o = ((static_cast<size_t>(r) * p.Lp + j) * p.Hkv + hk) * kDh + c * 8;
-      k = p.Kp + o;
-      v = p.Vp + o;
-    } else if (j < p.Lp + p.B) {
-      const size_t o = ((static_cast<size_t>(r) * p.B + (j - p.Lp)) * p.Hkv + hk) * kDh + c * 8;
-      k = p.Kt + o;
-      v = p.Vt + o;
-    } else {
-      k = p.Kp;  // any mapped address; nothing is read
-      v = p.Kp;
-      valid = false;
-    }
-    cp_async16(sK + swz(row, c), k, valid);
-    cp_async16(sV + swz(row, c), v, valid);
-  }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Publish this CTA's partial (unnormalised O, row max and sum in base 2);
+// Byte offset of 16-byte granule gr (of 8 in a 128-byte row) of row r in a
+// 128-byte swizzled atom.
+__device__ __forceinline__ uint32_t sw128(int r, int gr) {
+  return static_cast<uint32_t>(r * 128 + ((gr ^ (r & 7)) << 4));
+}
+
+// Publish this CTA's partial row (unnormalised O, max and sum in base 2);
 // the last split of the query tile to arrive combines all of them:
 //   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
-__device__ __forceinline__ void combine_splits(const AttnParams& p, int r, int hk, int qt, int split,
-                                            const float (&o)[16][4], float m_a, float m_b,
-                                            float l_a, float l_b) {
+// All 128 softmax threads call it (thread = row of the tile).
+__device__ __forceinline__ void combine_splits(const AttnParams& p, int r, int hk, int qt,
+                                               int split, const float (&o)[kDh], float m,
+                                               float l) {
   __shared__ int last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = threadIdx.x;
   const size_t tile = (static_cast<size_t>(r) * p.Hkv + hk) * p.q_tiles + qt;
-  float* po = p.part_O + (tile * p.n_split + split) * kQRows * kDh;
-  float2* pml = p.part_ml + (tile * p.n_split + split) * kQRows;
-  const int ra = warp * 16 + (lane >> 2), rb = ra + 8;  // rows within the tile
+  float* po = p.part_O + ((tile * p.n_split + split) * kQRows + row) * kDh;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int col = i * 8 + (lane & 3) * 2;
-    *reinterpret_cast<float2*>(po + ra * kDh + col) = make_float2(o[i][0], o[i][1]);
-    *reinterpret_cast<float2*>(po + rb * kDh + col) = make_float2(o[i][2], o[i][3]);
-  }
-  if ((lane & 3) == 0) {
-    pml[ra] = make_float2(m_a, l_a);
-    pml[rb] = make_float2(m_b, l_b);
-  }
+  for (int i = 0; i < kDh; i += 4)
+    *reinterpret_cast<float4*>(po + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+  p.part_ml[(tile * p.n_split + split) * kQRows + row] = make_float2(m, l);
   __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(p.cnt + tile, 1) == p.n_split - 1);
-  __syncthreads();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (row == 0) last = (atomicAdd(p.cnt + tile, 1) == p.n_split - 1);
+  asm volatile("bar.sync 1, 128;" ::: "memory");
   if (!last) return;
   __threadfence();
   const float* all_o = p.part_O + tile * p.n_split * kQRows * kDh;
   const float2* all_ml = p.part_ml + tile * p.n_split * kQRows;
-  for (int e = threadIdx.x; e < kQRows * (kDh / 4); e += kAttnThreads) {
-    const int row = e / (kDh / 4), c4 = (e % (kDh / 4)) * 4;
-    const int q = qt * kQRows + row;
-    if (q >= p.rows) continue;
+  const int q = qt * kQRows + row;
+  if (q < p.rows) {  // this thread combines its own row over the splits
     float M = -INFINITY;
     for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, __ldcg(&all_ml[s * kQRows + row]).x);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Lsum = 0.f;
+    float acc[kDh];
+#pragma unroll
+    for (int c = 0; c < kDh; ++c) acc[c] = 0.f;
     for (int s = 0; s < p.n_split; ++s) {  // fixed order: deterministic
       const float2 ml = __ldcg(&all_ml[s * kQRows + row]);
-      if (ml.x == -INFINITY) continue;
-      const float f = exp2f(ml.x - M);
-      L += ml.y * f;
-      const float4 v =
-          __ldcg(reinterpret_cast<const float4*>(all_o + (s * kQRows + row) * kDh + c4));
-      acc.x += v.x * f;
-      acc.y += v.y * f;
-      acc.z += v.z * f;
-      acc.w += v.w * f;
+      const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
+      Lsum += ml.y * f;
+      const float4* src = reinterpret_cast<const float4*>(all_o + (s * kQRows + row) * kDh);
+#pragma unroll
+      for (int c = 0; c < kDh / 4; ++c) {
+        const float4 v = __ldcg(src + c);
+        acc[4 * c] += v.x * f;
+        acc[4 * c + 1] += v.y * f;
+        acc[4 * c + 2] += v.z * f;
+        acc[4 * c + 3] += v.w * f;
+      }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const float4 out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     const int node = q / p.g, h = hk * p.g + q % p.g;
-    const size_t base = ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh + c4;
-    *reinterpret_cast<float4*>(p.O + base) = out;
-    if (p.O16)
-      *reinterpret_cast<uint2*>(p.O16 + base) =
-          make_uint2(pack_bf16(out.x, out.y), pack_bf16(out.z, out.w));
+    const size_t base = ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
+#pragma unroll
+    for (int c = 0; c < kDh; c += 4) {
+      const float4 out = make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv,
+                                     acc[c + 3] * inv);
+      *reinterpret_cast<float4*>(p.O + base + c) = out;
+      if (p.O16)
+        *reinterpret_cast<uint2*>(p.O16 + base + c) =
+            make_uint2(cvt_bf16x2(out.x, out.y), cvt_bf16x2(out.z, out.w));
+    }
   }
   if (threadIdx.x == 0) p.cnt[tile] = 0;
 }
 
-__global__ void __launch_bounds__(kAttnThreads) k_tree_attention(const AttnParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sKV = sQ + kQRows * kRowBytes;  // [2 stages][K tile, V tile]
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    k_tree_attention(const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sP = sQ + kQBytes;
+  uint8_t* sStage = sP + 2 * kPBytes;  // P is double-buffered
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + kStages * kStageBytes);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + kStages;
+  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;   // [2]
+  uint64_t* p_empty = p_full + 2;   // [2]
+  uint64_t* o_done = p_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.z, hk = blockIdx.y;
   const int qt = blockIdx.x / p.n_split, split = blockIdx.x % p.n_split;
   const int q0 = qt * kQRows;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- query tile: 64 rows of (node, head) gathered into shared memory
-  for (int e = threadIdx.x; e < kQRows * 16; e += kAttnThreads) {
-    const int row = e >> 4, c = e & 15;
-    const int q = q0 + row;
-    const bool valid = q < p.rows;
-    const int node = q / p.g, h = hk * p.g + q % p.g;
-    const uint16_t* src =
-        valid ? p.Q + ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh + c * 8 : p.Q;
-    cp_async16(sQ + swz(row, c), src, valid);
-  }
-  const int n_keys = p.Lp + p.B;
-  const int n_tiles = (n_keys + kKeys - 1) / kKeys;
-  // the largest node of this tile bounds the tree keys any row can see
+  // key tiles of this CTA: the query tile's largest node bounds the tree
+  // keys any of its rows can see
   const int last_node = min(p.B, (q0 + kQRows - 1) / p.g);
-  const int t_all = min(n_tiles, (p.Lp + last_node + kKeys - 1) / kKeys);
+  const int t_all = (p.Lp + last_node + kKeys - 1) / kKeys;
   const int t_beg = split * t_all / p.n_split, t_end = (split + 1) * t_all / p.n_split;
-  if (t_beg < t_end) load_kv(p, r, hk, t_beg, sKV, sKV + kTileBytes);
-  cp_async_commit();
+  const int nt = t_end - t_beg;
 
-  // this thread's two query rows (within the warp's 16) and their nodes
-  const int qa = q0 + warp * 16 + (lane >> 2), qb = qa + 8;
-  const int node_a = qa / p.g, node_b = qb / p.g;
-  const uint32_t* mrow_a =
-      (node_a >= 1 && qa < p.rows) ? p.mask + (static_cast<size_t>(r) * p.B + node_a - 1) * p.words
-                                   : nullptr;
-  const uint32_t* mrow_b =
-      (node_b >= 1 && qb < p.rows) ? p.mask + (static_cast<size_t>(r) * p.B + node_b - 1) * p.words
-                                   : nullptr;
-
-  float o[16][4];  // 16 x 128 output of the warp: 16 column tiles of 8
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-  uint32_t qf[8][4];  // A fragments of the warp's 16 query rows, 8 k-steps
-
-  for (int t = t_beg; t < t_end; ++t) {
-    const int st = t - t_beg;
-    const uint32_t sK = sKV + (st & 1) * 2 * kTileBytes, sV = sK + kTileBytes;
-    if (t + 1 < t_end) {
-      const uint32_t nK = sKV + ((st + 1) & 1) * 2 * kTileBytes;
-      load_kv(p, r, hk, t + 1, nK, nK + kTileBytes);
+  if (warp == 5) tmem_alloc<kTmemCols>(tmem_slot);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (t == t_beg) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 4);  // one arrival per softmax warp
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&p_full[b], 4);
+      mbar_init(&p_empty[b], 1);
+    }
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_vt);
+  }
+  // the query tile, written by the softmax threads in the swizzled layout
+  if (threadIdx.x < kSoftmaxThreads) {
+    const int row = threadIdx.x, q = q0 + row;
+    const bool valid = q < p.rows;
+    const uint4* src = nullptr;
+    if (valid) {
+      const int node = q / p.g, h = hk * p.g + q % p.g;
+      src = reinterpret_cast<const uint4*>(
+          p.Q + ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh);
+    }
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        ldsm_x4(sQ + swz(row, ks * 2 + (lane >> 4)), qf[ks]);
+    for (int gi = 0; gi < 16; ++gi) {
+      const uint4 v = valid ? __ldg(src + gi) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sQ + (gi >> 3) * (kQRows * 128) + sw128(row, gi & 7)) = v;
+    }
+    fence_proxy_async_smem();  // visible to the tensor cores
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      long long issued = 0;
+      for (int f = 0; f < 2 * nt && !*abort_flag; ++f) {
+        const bool pass2 = f >= nt;
+        const int t = t_beg + (pass2 ? f - nt : f);
+        const int stage = f % kStages;
+        const uint32_t ph = static_cast<uint32_t>((f / kStages) & 1);
+        if (!mbar_wait(&kv_empty[stage], ph ^ 1u, p.err, p.wait_limit)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* k_dst = sStage + stage * kStageBytes;
+        mbar_arrive_expect_tx(&kv_full[stage], pass2 ? kStageBytes : kKBytes);
+        tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, hk, t * kKeys, r);
+        tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, hk, t * kKeys, r);
+        if (pass2) tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], t * kKeys, 0, hk, r);
+        ++issued;
+      }
+      // drain: every issued copy must have landed before the CTA may exit
+      const long long first = issued > kStages ? issued - kStages : 0;
+      for (long long n = first; n < issued; ++n) {
+        const int s = static_cast<int>(n % kStages);
+        if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((n / kStages) & 1), p.err)) break;
       }
     }
-    // ---- S = Q K^T for 64 keys: 8 column tiles of 8 keys
-    float s[8][4];
+  } else if (warp == 5) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_m128<kKeys>();
+      constexpr uint32_t idesc_o = idesc_bf16_m128<kDh>();
+      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (ok && !*abort_flag && mbar_wait(bar, par, p.err, p.wait_limit)) return true;
+        ok = false;
+        *abort_flag = 1;
+        return false;
+      };
+      // S[b] = Q K^T for the tile in stage `stage`
+      auto issue_s = [&](int u, int stage) {
+        const int b = u & 1;
+        if (!wait(&s_empty[b], (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u)) return false;
+        if (!wait(&kv_full[stage], static_cast<uint32_t>((u / kStages) & 1))) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sStage + stage * kStageBytes);
 #pragma unroll
-    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        for (int kk = 0; kk < kDh / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32u;  // 16 head dims within the 128-byte row
+          tc_mma_bf16(tmem_base + static_cast<uint32_t>(b * kKeys),
+                      smem_desc_sw128(q_addr + (kk >> 2) * (kQRows * 128) + off),
+                      smem_desc_sw128(k_addr + (kk >> 2) * (kKeys * 128) + off), idesc_s,
+                      kk != 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[b]);
+        return true;
+      };
+      // O += P V for pass-2 tile j (its stage), then release P and the stage
+      auto issue_o = [&](int j) {
+        const int f = nt + j, stage = f % kStages, pb = j & 1;
+        if (!wait(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sStage + stage * kStageBytes + kKBytes);
+        const uint32_t pa = p_addr + pb * kPBytes;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-      for (int n2 = 0; n2 < 4; ++n2) {  // two key tiles per ldmatrix
-        uint32_t b[4];
-        const int krow = n2 * 16 + (lane & 7) + (lane >> 4) * 8;
-        ldsm_x4(sK + swz(krow, ks * 2 + ((lane >> 3) & 1)), b);
-        mma_bf16(s[2 * n2], qf[ks], b[0], b[1]);
-        mma_bf16(s[2 * n2 + 1], qf[ks], b[2], b[3]);
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc_mma_bf16(tmem_base + kColO, smem_desc_sw128(pa + kk * 32),
+                      smem_desc_sw128(v_addr + kk * 32), idesc_o, (j != 0 || kk != 0) ? 1u : 0u);
+        tc_commit(&p_empty[pb]);
+        tc_commit(&kv_empty[stage]);
+        return true;
+      };
+      // pass 1: scores only
+      for (int j = 0; j < nt && ok; ++j) {
+        if (!issue_s(j, j % kStages)) break;
+        tc_commit(&kv_empty[j % kStages]);
       }
+      // pass 2: scores of tile j, then the product of tile j - 1
+      for (int j = 0; j < nt && ok; ++j) {
+        if (!issue_s(nt + j, (nt + j) % kStages)) break;
+        if (j > 0 && !issue_o(j - 1)) break;
+      }
+      if (ok && nt > 0) issue_o(nt - 1);
+      tc_commit(o_done);
+      mbar_wait(o_done, 0, p.err);
     }
-    // ---- visibility, online softmax (base 2), P in registers
-    const int j0 = t * kKeys;
-    float mx_a = m_a, mx_b = m_b;
-    if (j0 + kKeys <= p.Lp) {  // prefix keys only: every row sees all of them
+  } else {
+    // -------------------------------------------------------- softmax
+    const int row = threadIdx.x, q = q0 + row;
+    const int node = q < p.rows ? q / p.g : 0;
+    const uint32_t* mrow =
+        (q < p.rows && node >= 1) ? p.mask + (static_cast<size_t>(r) * p.B + node - 1) * p.words
+                                  : nullptr;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // scaled scores of tile t for this row, -inf where not visible
+    auto load_s = [&](int u, int t, float (&s)[kKeys]) {
+      const int b = u & 1;
+      const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * kKeys);
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int c = 0; c < kKeys; c += 16) {
+        float x[16];
+        tmem_ld16(taddr + c, x);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[n][e] *= p.scale_log2;
-        mx_a = fmaxf(mx_a, fmaxf(s[n][0], s[n][1]));
-        mx_b = fmaxf(mx_b, fmaxf(s[n][2], s[n][3]));
+        for (int i = 0; i < 16; ++i) s[c + i] = x[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[b]);  // S[b] may be overwritten
+      const int j0 = t * kKeys;
+      if (j0 + kKeys <= p.Lp) {
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) s[c] *= p.scale_log2;
+      } else {
+        uint32_t w[3] = {0u, 0u, 0u};  // mask words covering the tile's tree keys
+        const int tt0 = j0 - p.Lp;     // tree index of the tile's first key
+        const int wb = tt0 >= 0 ? tt0 >> 5 : 0;
+        if (mrow) {
+#pragma unroll
+          for (int k = 0; k < 3; ++k)
+            if (wb + k < p.words) w[k] = __ldg(mrow + wb + k);
+        }
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) {
+          const int j = j0 + c;
+          bool vis = j < p.Lp;
+          if (!vis && j < p.L) {
+            const int tt = j - p.Lp - wb * 32;  // within the loaded words
+            vis = (w[tt >> 5] >> (tt & 31)) & 1u;
+          }
+          s[c] = vis ? s[c] * p.scale_log2 : -INFINITY;
+        }
+      }
+    };
+    bool go = true;
+    float m = -INFINITY;
+    for (int j = 0; j < nt; ++j) {  // pass 1: the row maximum
+      if (*abort_flag || !mbar_wait(&s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, p.err,
+                                    p.wait_limit)) {
+        go = false;
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      float s[kKeys];
+      load_s(j, t_beg + j, s);
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) m = fmaxf(m, s[c]);
+    }
+    const float sub = m == -INFINITY ? 0.f : m;
+    float l = 0.f;
+    for (int j = 0; j < nt && go; ++j) {  // pass 2: P and the normaliser
+      const int u = nt + j;
+      if (*abort_flag || !mbar_wait(&s_full[u & 1], static_cast<uint32_t>(u >> 1) & 1u, p.err,
+                                    p.wait_limit)) {
+        go = false;
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      float s[kKeys];
+      load_s(u, t_beg + j, s);
+      uint32_t pk[kKeys / 2];
+#pragma unroll
+      for (int c = 0; c < kKeys; c += 2) {
+        const uint32_t v = cvt_bf16x2(fast_ex2(s[c] - sub), fast_ex2(s[c + 1] - sub));
+        l += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+        pk[c / 2] = v;
+      }
+      // the product two tiles back has released this P buffer
+      const int pb = j & 1;
+      if (!mbar_wait(&p_empty[pb], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.err,
+                     p.wait_limit)) {
+        go = false;
+        *abort_flag = 1;
+        break;
+      }
+      uint8_t* dst = sP + pb * kPBytes;
+#pragma unroll
+      for (int gi = 0; gi < 8; ++gi)
+        *reinterpret_cast<uint4*>(dst + sw128(row, gi)) =
+            make_uint4(pk[gi * 4], pk[gi * 4 + 1], pk[gi * 4 + 2], pk[gi * 4 + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[pb]);
+    }
+    float o[kDh];
+    if (go && nt > 0 && mbar_wait(o_done, 0, p.err)) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kDh; c += 16) {
+        float x[16];
+        tmem_ld16(tmem_base + lane_base + kColO + c, x);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[c + i] = x[i];
       }
     } else {
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int c = 0; c < kDh; ++c) o[c] = 0.f;
+      if (nt > 0) l = 0.f;
+    }
+    if (p.n_split > 1) {
+      combine_splits(p, r, hk, qt, split, o, m, l);
+    } else if (q < p.rows) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int h = hk * p.g + q % p.g;
+      const size_t base = ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = j0 + n * 8 + (lane & 3) * 2 + (e & 1);
-          const bool row_b = e >= 2;
-          const uint32_t* mr = row_b ? mrow_b : mrow_a;
-          bool vis = j < p.Lp;
-          if (!vis && j < n_keys && mr != nullptr) {
-            const int tt = j - p.Lp;
-            vis = (__ldg(mr + (tt >> 5)) >> (tt & 31)) & 1u;
-          }
-          const float v = vis ? s[n][e] * p.scale_log2 : -INFINITY;
-          s[n][e] = v;
-          if (row_b) mx_b = fmaxf(mx_b, v); else mx_a = fmaxf(mx_a, v);
-        }
+      for (int c = 0; c < kDh; c += 4) {
+        const float4 v = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+        *reinterpret_cast<float4*>(p.O + base + c) = v;
+        if (p.O16)
+          *reinterpret_cast<uint2*>(p.O16 + base + c) =
+              make_uint2(cvt_bf16x2(v.x, v.y), cvt_bf16x2(v.z, v.w));
       }
     }
-#pragma unroll
-    for (int o2 = 1; o2 <= 2; o2 <<= 1) {
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFullMask, mx_a, o2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFullMask, mx_b, o2));
-    }
-    // (ex2 of -inf is +0: invisible keys get weight 0 without a test)
-    const float al_a = (mx_a == -INFINITY) ? 1.f : fast_ex2(m_a - mx_a);
-    const float al_b = (mx_b == -INFINITY) ? 1.f : fast_ex2(m_b - mx_b);
-    m_a = mx_a;
-    m_b = mx_b;
-    const float sub_a = (m_a == -INFINITY) ? 0.f : m_a, sub_b = (m_b == -INFINITY) ? 0.f : m_b;
-    uint32_t pf[4][4];  // A fragments of P: 4 k-steps of 16 keys
-    float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      // the bf16-rounded weights are used for both P.V and the normaliser
-      const uint32_t pa = cvt_bf16x2(fast_ex2(s[n][0] - sub_a), fast_ex2(s[n][1] - sub_a));
-      const uint32_t pb = cvt_bf16x2(fast_ex2(s[n][2] - sub_b), fast_ex2(s[n][3] - sub_b));
-      ps_a += __uint_as_float(pa << 16) + __uint_as_float(pa & 0xFFFF0000u);
-      ps_b += __uint_as_float(pb << 16) + __uint_as_float(pb & 0xFFFF0000u);
-      const int ks = n >> 1, hi = n & 1;
-      pf[ks][hi * 2 + 0] = pa;
-      pf[ks][hi * 2 + 1] = pb;
-    }
-    l_a = l_a * al_a + ps_a;
-    l_b = l_b * al_b + ps_b;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= al_a;
-      o[i][1] *= al_a;
-      o[i][2] *= al_b;
-      o[i][3] *= al_b;
-    }
-    // ---- O += P V: 16 column tiles of 8 (head dim), 4 k-steps of 16 keys
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-      for (int d2 = 0; d2 < 8; ++d2) {  // two head-dim tiles per ldmatrix
-        uint32_t b[4];
-        const int vrow = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        ldsm_x4_t(sV + swz(vrow, d2 * 2 + (lane >> 4)), b);
-        mma_bf16(o[2 * d2], pf[ks], b[0], b[1]);
-        mma_bf16(o[2 * d2 + 1], pf[ks], b[2], b[3]);
-      }
-    }
-    __syncthreads();  // the stage is refilled by the next iteration
   }
-  cp_async_wait<0>();
 
-  // ---- normalise and write the two rows of this thread
-#pragma unroll
-  for (int o2 = 1; o2 <= 2; o2 <<= 1) {
-    l_a += __shfl_xor_sync(kFullMask, l_a, o2);
-    l_b += __shfl_xor_sync(kFullMask, l_b, o2);
-  }
-  if (p.n_split > 1) {
-    combine_splits(p, r, hk, qt, split, o, m_a, m_b, l_a, l_b);
-    return;
-  }
-  const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f, inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int q = half ? qb : qa;
-    if (q >= p.rows) continue;
-    const int node = q / p.g, h = hk * p.g + q % p.g;
-    const size_t base = ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
-    const float inv = half ? inv_b : inv_a;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int col = i * 8 + (lane & 3) * 2;
-      const float x0 = o[i][half * 2] * inv, x1 = o[i][half * 2 + 1] * inv;
-      *reinterpret_cast<float2*>(p.O + base + col) = make_float2(x0, x1);
-      if (p.O16) *reinterpret_cast<uint32_t*>(p.O16 + base + col) = pack_bf16(x0, x1);
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem_base);
   }
 }
 
@@ -430,11 +513,35 @@ dartree_status fail(dartree_status s, const char* why) {
   return s;
 }
 
-}  // namespace
-}  // namespace dt
 
-namespace dt {
-namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+bool encode_4d(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4],
+               const cuuint64_t (&strides)[3], const cuuint32_t (&box)[4]) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kMaxSplit = 16;
 
 size_t split_bytes(int R, int B, int Hq, int Hkv, int n_split) {
@@ -443,6 +550,9 @@ size_t split_bytes(int R, int B, int Hq, int Hkv, int n_split) {
   const size_t o = tiles * n_split * kQRows * kDh * 4, ml = tiles * n_split * kQRows * 8;
   return o + ml + tiles * 4 + 64;
 }
+
+__device__ int g_attn_err;  // error word when the caller passes none
+
 }  // namespace
 }  // namespace dt
 
@@ -453,27 +563,50 @@ extern "C" size_t dartree_tree_attention_workspace(int32_t R, int32_t Lp, int32_
   return dt::split_bytes(R, B, Hq, Hkv, dt::kMaxSplit);
 }
 
-extern "C" dartree_status dartree_tree_attention(const void* Q, const void* Kp, const void* Vp,
-                                                 const void* Kt, const void* Vt,
-                                                 const uint32_t* mask, int32_t R, int32_t Lp,
-                                                 int32_t B, int32_t Hq, int32_t Hkv, int32_t dh,
-                                                 float scale, float* O, void* O_bf16, void* work,
-                                                 size_t work_bytes, void* stream) {
+extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, const void* Vt,
+                                                 int64_t ldv, const uint32_t* mask, int32_t R,
+                                                 int32_t Lp, int32_t B, int32_t Hq, int32_t Hkv,
+                                                 int32_t dh, float scale, float* O, void* O_bf16,
+                                                 void* work, size_t work_bytes, int32_t* err,
+                                                 void* stream) {
   using namespace dt;
-  if (!Q || !Kt || !Vt || !O || (Lp > 0 && (!Kp || !Vp)) || (B > 0 && !mask))
+  if (!Q || !K || !Vt || !O || (B > 0 && !mask))
     return fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
   if (R < 1 || Lp < 0 || B < 0 || B > DARTREE_MAX_B || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
       Lp + B < 1 || !(scale > 0.f))
     return fail(DARTREE_ERR_INVALID_ARG, "bad R, Lp, B, Hq, Hkv or scale");
   if (dh != kDh) return fail(DARTREE_ERR_UNSUPPORTED, "head dimension must be 128");
-  const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(Kt) |
-                       reinterpret_cast<uintptr_t>(Vt) | reinterpret_cast<uintptr_t>(Kp) |
-                       reinterpret_cast<uintptr_t>(Vp) | reinterpret_cast<uintptr_t>(O) |
+  if (ldv < Lp + B || ldv % 8 != 0)
+    return fail(DARTREE_ERR_INVALID_ARG, "ldv must be >= Lp + B and a multiple of 8");
+  const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                       reinterpret_cast<uintptr_t>(Vt) | reinterpret_cast<uintptr_t>(O) |
                        reinterpret_cast<uintptr_t>(O_bf16);
-  if (al & 15) return fail(DARTREE_ERR_INVALID_ARG, "Q, K, V and O must be 16-byte aligned");
+  if (al & 15) return fail(DARTREE_ERR_INVALID_ARG, "Q, K, Vt and O must be 16-byte aligned");
+  const int L = Lp + B;
+  CUtensorMap tm_k, tm_vt;
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDh), static_cast<cuuint64_t>(Hkv),
+                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(R)};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(kDh) * 2,
+                               static_cast<cuuint64_t>(Hkv) * kDh * 2,
+                               static_cast<cuuint64_t>(L) * Hkv * kDh * 2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kKeys), 1};
+    if (!encode_4d(&tm_k, K, dims, str, box)) return fail(DARTREE_ERR_CUDA, "key tensor map");
+  }
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(kDh),
+                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(R)};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(ldv) * 2,
+                               static_cast<cuuint64_t>(ldv) * kDh * 2,
+                               static_cast<cuuint64_t>(ldv) * kDh * Hkv * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kKeys), static_cast<cuuint32_t>(kDh), 1,
+                               1};
+    if (!encode_4d(&tm_vt, Vt, dims, str, box)) return fail(DARTREE_ERR_CUDA, "value tensor map");
+  }
   AttnParams p{};
   p.Lp = Lp;
   p.B = B;
+  p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
@@ -481,28 +614,28 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* Kp, 
   p.rows = (B + 1) * p.g;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.Q = static_cast<const uint16_t*>(Q);
-  p.Kp = static_cast<const uint16_t*>(Lp > 0 ? Kp : Kt);
-  p.Vp = static_cast<const uint16_t*>(Lp > 0 ? Vp : Vt);
-  p.Kt = static_cast<const uint16_t*>(Kt);
-  p.Vt = static_cast<const uint16_t*>(Vt);
   p.mask = mask;
   p.O = O;
   p.O16 = static_cast<uint16_t*>(O_bf16);
-  const size_t smem = static_cast<size_t>(kQRows) * kRowBytes + 4 * static_cast<size_t>(kTileBytes);
-  cudaError_t e = cudaFuncSetAttribute(k_tree_attention,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  p.err = err;
+  cudaError_t e;
+  if (!p.err) {
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p.err), g_attn_err);
+    if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
+  }
+  const size_t smem =
+      1024 + kQBytes + 2 * kPBytes + static_cast<size_t>(kStages) * kStageBytes + 256;
+  e = cudaFuncSetAttribute(k_tree_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   // split the keys so that one wave of CTAs fills the GPU, as the workspace allows
   p.q_tiles = (p.rows + kQRows - 1) / kQRows;
   const int tiles = R * Hkv * p.q_tiles;
-  const int key_tiles = (Lp + B + kKeys - 1) / kKeys;
-  int dev = 0, sms = 148, per_sm = 1;
+  const int key_tiles = (L + kKeys - 1) / kKeys;
+  int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_tree_attention, kAttnThreads, smem);
-  if (per_sm < 1) per_sm = 1;
-  int n_split = (per_sm * sms) / tiles;  // one full wave of CTAs
+  int n_split = sms / tiles;  // one CTA per SM
   n_split = n_split < kMaxSplit ? n_split : kMaxSplit;
   n_split = n_split < key_tiles ? n_split : key_tiles;
   if (n_split < 1) n_split = 1;
@@ -510,6 +643,7 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* Kp, 
   while (n_split > 1 && (work == nullptr || split_bytes(R, B, Hq, Hkv, n_split) > work_bytes))
     --n_split;
   p.n_split = n_split;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (n_split > 1) {
     const size_t ot = static_cast<size_t>(tiles) * n_split * kQRows * kDh * 4;
     const size_t mt = static_cast<size_t>(tiles) * n_split * kQRows * 8;
@@ -517,12 +651,11 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* Kp, 
     p.part_O = reinterpret_cast<float*>(wb);
     p.part_ml = reinterpret_cast<float2*>(wb + ot);
     p.cnt = reinterpret_cast<int*>(wb + ot + mt);
-    e = cudaMemsetAsync(p.cnt, 0, sizeof(int) * tiles, static_cast<cudaStream_t>(stream));
+    e = cudaMemsetAsync(p.cnt, 0, sizeof(int) * tiles, st);
     if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   }
   const dim3 grid(p.q_tiles * n_split, Hkv, R);
-  e = launch_kernel(k_tree_attention, grid, dim3(kAttnThreads), smem,
-                                static_cast<cudaStream_t>(stream), false, p);
+  e = launch_kernel(k_tree_attention, grid, dim3(kAttnThreads), smem, st, false, tm_k, tm_vt, p);
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   return DARTREE_OK;
 }

@@ -104,9 +104,9 @@ def load():
         "dartree_reset_timing": (st, [_vp]),
         "dartree_state_step_noalloc": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
         "dartree_get_states": (st, [_vp, _i32, _vp, _vp]),
-        "dartree_tree_attention": (st, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
-                                        _i32, _i32, ctypes.c_float, _vp, _vp, _vp,
-                                        ctypes.c_size_t, _vp]),
+        "dartree_tree_attention": (st, [_vp, _vp, _vp, ctypes.c_int64, _vp, _i32, _i32, _i32,
+                                        _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp,
+                                        ctypes.c_size_t, _vp, _vp]),
         "dartree_tree_attention_workspace": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
         "dartree_accept": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     }
@@ -393,18 +393,20 @@ def _check_free(s: int) -> None:
         raise DartreeError(s, load().dartree_last_error(None).decode())
 
 
-def tree_attention(Q, Kp, Vp, Kt, Vt, mask, *, scale: float | None = None, want_bf16: bool = True,
-                   work=None, split: bool = True, stream=None) -> dict:
+def tree_attention(Q, K, Vt, mask, *, Lp: int, scale: float | None = None,
+                   want_bf16: bool = True, work=None, split: bool = True, err=None,
+                   stream=None) -> dict:
     """Tree attention of the verification forward (dartree_tree_attention):
-    Q [R,B+1,Hq,dh], Kp/Vp [R,Lp,Hkv,dh], Kt/Vt [R,B,Hkv,dh] (bf16 CUDA
-    tensors), mask [R,B,words] int32 -> {"O": fp32, "O16": bf16 bits}.
-    ``work`` is the key-split scratch (allocated here when None and
-    ``split``; ``split=False`` runs unsplit)."""
-    for n, t in (("Q", Q), ("Kt", Kt), ("Vt", Vt), ("Kp", Kp), ("Vp", Vp)):
+    Q [R,B+1,Hq,dh], key cache K [R,Lp+B,Hkv,dh] (prefix keys, then the tree
+    nodes'), transposed value cache Vt [R,Hkv,dh,ldv] (bf16 CUDA tensors),
+    mask [R,B,words] int32 -> {"O": fp32, "O16": bf16 bits}.  ``work`` is
+    the key-split scratch (allocated here when None and ``split``)."""
+    for n, t in (("Q", Q), ("K", K), ("Vt", Vt)):
         _dev(t, n, _W16)
     _dev(mask, "mask", (torch.int32,))
     R, Bp1, Hq, dh = Q.shape
-    Lp, Hkv = Kp.shape[1], Kp.shape[2]
+    Hkv = K.shape[2]
+    ldv = Vt.shape[3]
     O = torch.empty(R, Bp1, Hq, dh, dtype=torch.float32, device=Q.device)
     O16 = torch.empty(R, Bp1, Hq, dh, dtype=torch.int16, device=Q.device) if want_bf16 else None
     sc = float(scale) if scale is not None else dh ** -0.5
@@ -413,10 +415,22 @@ def tree_attention(Q, Kp, Vp, Kt, Vt, mask, *, scale: float | None = None, want_
         work = torch.empty(max(n, 16), dtype=torch.uint8, device=Q.device)
     wb = 0 if work is None else work.numel() * work.element_size()
     _check_free(load().dartree_tree_attention(
-        _ptr(Q), _ptr(Kp) if Lp else None, _ptr(Vp) if Lp else None, _ptr(Kt), _ptr(Vt),
-        _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh, ctypes.c_float(sc), _ptr(O), _ptr(O16),
-        _ptr(work), wb, _stream(stream)))
+        _ptr(Q), _ptr(K), _ptr(Vt), ldv, _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh,
+        ctypes.c_float(sc), _ptr(O), _ptr(O16), _ptr(work), wb, _ptr(err), _stream(stream)))
     return {"O": O, "O16": O16}
+
+
+def kv_cache(Kp, Vp, Kt, Vt) -> tuple[torch.Tensor, torch.Tensor]:
+    """Key cache [R, Lp+B, Hkv, dh] and transposed value cache [R, Hkv, dh,
+    ldv] (ldv = Lp+B rounded up to 8) from prefix and tree keys / values
+    (CUDA tensors; data movement only)."""
+    K = torch.cat([Kp, Kt], dim=1).contiguous()
+    V = torch.cat([Vp, Vt], dim=1)                       # [R, L, Hkv, dh]
+    R, L, Hkv, dh = V.shape
+    ldv = (L + 7) // 8 * 8
+    VT = torch.zeros(R, Hkv, dh, ldv, dtype=V.dtype, device=V.device)
+    VT[..., :L] = V.permute(0, 2, 3, 1)
+    return K, VT
 
 
 def accept(parent, token, n_out, pred, *, max_len: int, stream=None) -> dict:

@@ -62,9 +62,12 @@ def test_tree_attention_parity(case, split):
     trees = [I.random_tree(g, B, int(g.integers(max(1, B // 2), B + 1))) for _ in range(R)]
     masks = np.stack([ancestor_mask(t["parent"], t["n_out"], B) for t in trees])
     scale = 128 ** -0.5
-    out = dtl.tree_attention(*(_cuda16(x[k]) for k in ("Q", "Kp", "Vp", "Kt", "Vt")),
-                             torch.from_numpy(masks.view(np.int32)).cuda(), scale=scale,
-                             split=split)
+    K, VT = dtl.kv_cache(*(_cuda16(x[k]) for k in ("Kp", "Vp", "Kt", "Vt")))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = dtl.tree_attention(_cuda16(x["Q"]), K, VT,
+                             torch.from_numpy(masks.view(np.int32)).cuda(), Lp=Lp, scale=scale,
+                             split=split, err=err)
+    assert int(err.item()) == 0                       # no pipeline wait ran out
     O = out["O"].cpu().numpy()
     O16 = out["O16"].cpu().numpy().view(np.uint16)
     assert np.array_equal(O16, I.to_bf16_bits(O))     # the bf16 copy is O rounded
@@ -115,8 +118,9 @@ def test_verify_step_on_a_built_tree():
     t = {k: v.cpu().numpy() for k, v in tree.items()}
     shape = I.VerifyShape(Lp=77, Hq=8, Hkv=2, dh=128, seed=4100)
     x = I.make_verify_inputs(1, w.B, shape)
-    out = dtl.tree_attention(*(_cuda16(x[k]) for k in ("Q", "Kp", "Vp", "Kt", "Vt")),
-                             tree["mask"], scale=128 ** -0.5)
+    K, VT = dtl.kv_cache(*(_cuda16(x[k]) for k in ("Kp", "Vp", "Kt", "Vt")))
+    out = dtl.tree_attention(_cuda16(x["Q"]), K, VT, tree["mask"], Lp=shape.Lp,
+                             scale=128 ** -0.5)
     mask = t["mask"][0].view(np.uint32)
     ref = oracle.tree_attention(x["Q"][0], x["Kp"][0], x["Vp"][0], x["Kt"][0], x["Vt"][0], mask,
                                 128 ** -0.5, True)
