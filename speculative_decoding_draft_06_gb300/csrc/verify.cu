@@ -14,9 +14,10 @@
 // g = Hq / Hkv.  Row 0 (the root) sees the prefix; node i >= 1 sees the
 // prefix and the tree nodes of mask row i - 1.
 //
-// Warp roles (192 threads): warps 0-3 softmax (thread = query row = TMEM
-// lane), warp 4 TMA producer (64-key tiles of K and of the transposed value
-// cache, 128-byte swizzle), warp 5 TMEM allocator + single-thread MMA issuer.
+// Warp roles (320 threads): warps 0-7 softmax (two warpgroups; a thread
+// owns a query row = TMEM lane, its group half of each key tile and half of
+// the head dimensions of O), warp 8 TMA producer (64-key tiles of K and of the transposed value
+// cache, 128-byte swizzle), warp 9 TMEM allocator + single-thread MMA issuer.
 // Two passes over the CTA's keys: the first finds each row's maximum scaled
 // score (S = Q K^T, M = 128 rows, N = 64 keys, K = 128 head dims); the
 // second recomputes S, forms P = 2^(s - max) rounded to bf16 in shared
@@ -42,8 +43,10 @@ namespace {
 constexpr int kDh = 128;           // head dimension (fixed)
 constexpr int kQRows = 128;        // query rows per CTA (TMEM lanes)
 constexpr int kKeys = 64;          // keys per tile
-constexpr int kAttnThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kAttnThreads = 320;
+constexpr int kSoftmaxThreads = 256;   // two warpgroups, one per half of each key tile
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kHalf = kKeys / 2;       // keys of a tile per warpgroup
 constexpr int kStages = 4;
 constexpr int kQBytes = kQRows * kDh * 2;        // 32 KB: 2 swizzle atoms of 64 head dims
 constexpr int kPBytes = kQRows * kKeys * 2;      // 16 KB per buffer: one atom of 64 keys
@@ -102,44 +105,46 @@ __device__ __forceinline__ uint32_t sw128(int r, int gr) {
   return static_cast<uint32_t>(r * 128 + ((gr ^ (r & 7)) << 4));
 }
 
-// Publish this CTA's partial row (unnormalised O, max and sum in base 2);
-// the last split of the query tile to arrive combines all of them:
+// Publish this CTA's partial row half (unnormalised O, and the row's max
+// and sum in base 2); the last split of the query tile to arrive combines
+// all of them:
 //   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
-// All 128 softmax threads call it (thread = row of the tile).
+// All 256 softmax threads call it (thread = (row, half of the head dims)).
 __device__ __forceinline__ void combine_splits(const AttnParams& p, int r, int hk, int qt,
-                                               int split, const float (&o)[kDh], float m,
-                                               float l) {
+                                               int split, int row, int half,
+                                               const float (&o)[kDh / 2], float m, float l) {
+  constexpr int kOH = kDh / 2;
   __shared__ int last;
-  const int row = threadIdx.x;
   const size_t tile = (static_cast<size_t>(r) * p.Hkv + hk) * p.q_tiles + qt;
-  float* po = p.part_O + ((tile * p.n_split + split) * kQRows + row) * kDh;
+  float* po = p.part_O + ((tile * p.n_split + split) * kQRows + row) * kDh + half * kOH;
 #pragma unroll
-  for (int i = 0; i < kDh; i += 4)
+  for (int i = 0; i < kOH; i += 4)
     *reinterpret_cast<float4*>(po + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
-  p.part_ml[(tile * p.n_split + split) * kQRows + row] = make_float2(m, l);
+  if (half == 0) p.part_ml[(tile * p.n_split + split) * kQRows + row] = make_float2(m, l);
   __threadfence();
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-  if (row == 0) last = (atomicAdd(p.cnt + tile, 1) == p.n_split - 1);
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (threadIdx.x == 0) last = (atomicAdd(p.cnt + tile, 1) == p.n_split - 1);
+  asm volatile("bar.sync 1, 256;" ::: "memory");
   if (!last) return;
   __threadfence();
   const float* all_o = p.part_O + tile * p.n_split * kQRows * kDh;
   const float2* all_ml = p.part_ml + tile * p.n_split * kQRows;
   const int q = qt * kQRows + row;
-  if (q < p.rows) {  // this thread combines its own row over the splits
+  if (q < p.rows) {  // this thread combines its own row half over the splits
     float M = -INFINITY;
     for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, __ldcg(&all_ml[s * kQRows + row]).x);
     float Lsum = 0.f;
-    float acc[kDh];
+    float acc[kOH];
 #pragma unroll
-    for (int c = 0; c < kDh; ++c) acc[c] = 0.f;
+    for (int c = 0; c < kOH; ++c) acc[c] = 0.f;
     for (int s = 0; s < p.n_split; ++s) {  // fixed order: deterministic
       const float2 ml = __ldcg(&all_ml[s * kQRows + row]);
       const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
       Lsum += ml.y * f;
-      const float4* src = reinterpret_cast<const float4*>(all_o + (s * kQRows + row) * kDh);
+      const float4* src =
+          reinterpret_cast<const float4*>(all_o + (s * kQRows + row) * kDh + half * kOH);
 #pragma unroll
-      for (int c = 0; c < kDh / 4; ++c) {
+      for (int c = 0; c < kOH / 4; ++c) {
         const float4 v = __ldcg(src + c);
         acc[4 * c] += v.x * f;
         acc[4 * c + 1] += v.y * f;
@@ -149,9 +154,10 @@ __device__ __forceinline__ void combine_splits(const AttnParams& p, int r, int h
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     const int node = q / p.g, h = hk * p.g + q % p.g;
-    const size_t base = ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
+    const size_t base =
+        ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh + half * kOH;
 #pragma unroll
-    for (int c = 0; c < kDh; c += 4) {
+    for (int c = 0; c < kOH; c += 4) {
       const float4 out = make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv,
                                      acc[c + 3] * inv);
       *reinterpret_cast<float4*>(p.O + base + c) = out;
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int t_beg = split * t_all / p.n_split, t_end = (split + 1) * t_all / p.n_split;
   const int nt = t_end - t_beg;
 
-  if (warp == 5) tmem_alloc<kTmemCols>(tmem_slot);
+  if (warp == kMmaWarp) tmem_alloc<kTmemCols>(tmem_slot);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -202,22 +208,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 4);  // one arrival per softmax warp
+      mbar_init(&s_empty[b], 8);  // one arrival per softmax warp
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&p_full[b], 4);
+      mbar_init(&p_full[b], 8);
       mbar_init(&p_empty[b], 1);
     }
     mbar_init(o_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_vt);
   }
   // the query tile, written by the softmax threads in the swizzled layout
-  if (threadIdx.x < kSoftmaxThreads) {
+  if (threadIdx.x < kQRows) {
     const int row = threadIdx.x, q = q0 + row;
     const bool valid = q < p.rows;
     const uint4* src = nullptr;
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       long long issued = 0;
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((n / kStages) & 1), p.err)) break;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_m128<kKeys>();
@@ -327,18 +333,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // -------------------------------------------------------- softmax
-    const int row = threadIdx.x, q = q0 + row;
+    __shared__ float red[2][kQRows];   // per-row exchange between the two groups
+    const int wg = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane, q = q0 + row;
     const int node = q < p.rows ? q / p.g : 0;
     const uint32_t* mrow =
         (q < p.rows && node >= 1) ? p.mask + (static_cast<size_t>(r) * p.B + node - 1) * p.words
                                   : nullptr;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    // scaled scores of tile t for this row, -inf where not visible
-    auto load_s = [&](int u, int t, float (&s)[kKeys]) {
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int col0 = wg * kHalf;  // this group's keys within a tile
+    // scaled scores of this group's half of tile t, -inf where not visible
+    auto load_s = [&](int u, int t, float (&s)[kHalf]) {
       const int b = u & 1;
-      const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * kKeys);
+      const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * kKeys + col0);
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 16) {
+      for (int c = 0; c < kHalf; c += 16) {
         float x[16];
         tmem_ld16(taddr + c, x);
 #pragma unroll
@@ -347,21 +356,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);  // S[b] may be overwritten
-      const int j0 = t * kKeys;
-      if (j0 + kKeys <= p.Lp) {
+      const int j0 = t * kKeys + col0;
+      if (j0 + kHalf <= p.Lp) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) s[c] *= p.scale_log2;
+        for (int c = 0; c < kHalf; ++c) s[c] *= p.scale_log2;
       } else {
-        uint32_t w[3] = {0u, 0u, 0u};  // mask words covering the tile's tree keys
-        const int tt0 = j0 - p.Lp;     // tree index of the tile's first key
+        uint32_t w[2] = {0u, 0u};   // mask words covering the half tile's tree keys
+        const int tt0 = j0 - p.Lp;  // tree index of the first key
         const int wb = tt0 >= 0 ? tt0 >> 5 : 0;
         if (mrow) {
 #pragma unroll
-          for (int k = 0; k < 3; ++k)
+          for (int k = 0; k < 2; ++k)
             if (wb + k < p.words) w[k] = __ldg(mrow + wb + k);
         }
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
+        for (int c = 0; c < kHalf; ++c) {
           const int j = j0 + c;
           bool vis = j < p.Lp;
           if (!vis && j < p.L) {
@@ -382,11 +391,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       tc_fence_after();
-      float s[kKeys];
+      float s[kHalf];
       load_s(j, t_beg + j, s);
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) m = fmaxf(m, s[c]);
+      for (int c = 0; c < kHalf; ++c) m = fmaxf(m, s[c]);
     }
+    red[wg][row] = m;  // the two halves' maxima -> the row's
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    m = fmaxf(red[0][row], red[1][row]);
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     const float sub = m == -INFINITY ? 0.f : m;
     float l = 0.f;
     for (int j = 0; j < nt && go; ++j) {  // pass 2: P and the normaliser
@@ -398,11 +411,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       tc_fence_after();
-      float s[kKeys];
+      float s[kHalf];
       load_s(u, t_beg + j, s);
-      uint32_t pk[kKeys / 2];
+      uint32_t pk[kHalf / 2];
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 2) {
+      for (int c = 0; c < kHalf; c += 2) {
         const uint32_t v = cvt_bf16x2(fast_ex2(s[c] - sub), fast_ex2(s[c + 1] - sub));
         l += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
         pk[c / 2] = v;
@@ -417,36 +430,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       uint8_t* dst = sP + pb * kPBytes;
 #pragma unroll
-      for (int gi = 0; gi < 8; ++gi)
-        *reinterpret_cast<uint4*>(dst + sw128(row, gi)) =
+      for (int gi = 0; gi < 4; ++gi)
+        *reinterpret_cast<uint4*>(dst + sw128(row, wg * 4 + gi)) =
             make_uint4(pk[gi * 4], pk[gi * 4 + 1], pk[gi * 4 + 2], pk[gi * 4 + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
     }
-    float o[kDh];
+    red[wg][row] = l;  // the two halves' sums -> the row's
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    l = red[0][row] + red[1][row];
+    // this group's half of the head dimensions of O
+    constexpr int kOH = kDh / 2;
+    float o[kOH];
     if (go && nt > 0 && mbar_wait(o_done, 0, p.err)) {
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kDh; c += 16) {
+      for (int c = 0; c < kOH; c += 16) {
         float x[16];
-        tmem_ld16(tmem_base + lane_base + kColO + c, x);
+        tmem_ld16(tmem_base + lane_base + kColO + wg * kOH + c, x);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[c + i] = x[i];
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < kDh; ++c) o[c] = 0.f;
+      for (int c = 0; c < kOH; ++c) o[c] = 0.f;
       if (nt > 0) l = 0.f;
     }
     if (p.n_split > 1) {
-      combine_splits(p, r, hk, qt, split, o, m, l);
+      combine_splits(p, r, hk, qt, split, row, wg, o, m, l);
     } else if (q < p.rows) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int h = hk * p.g + q % p.g;
-      const size_t base = ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
+      const size_t base =
+          ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh + wg * kOH;
 #pragma unroll
-      for (int c = 0; c < kDh; c += 4) {
+      for (int c = 0; c < kOH; c += 4) {
         const float4 v = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
         *reinterpret_cast<float4*>(p.O + base + c) = v;
         if (p.O16)
@@ -458,7 +477,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc<kTmemCols>(tmem_base);
   }
