@@ -304,10 +304,12 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
  *   Q    [R][B+1][Hq][dh]  queries; row 0 = the root (the last verified
  *                          token, already at prefix position Lp-1), rows
  *                          1..B = the tree nodes in canonical order;
- *   K    [R][L][Hkv][dh]   the key cache, L = Lp + B: the Lp prefix keys,
- *                          then the B tree nodes' keys in canonical order;
- *   Vt   [R][Hkv][dh][ldv] the value cache, transposed (keys innermost,
- *                          same key order; ldv >= L, a multiple of 8);
+ *   K    [R][Hkv][L][dh]  the key cache, L = Lp + B: per key/value head the
+ *                          Lp prefix keys, then the B tree nodes' keys in
+ *                          canonical order;
+ *   Vt   [R][Hkv][ceil(L/64)][dh][64]  the value cache in blocks of 64 keys,
+ *                          each block transposed (keys innermost; same key
+ *                          order; entries past L are ignored);
  *   mask [R][B][ceil(B/32)] the build's ancestor mask (dartree_tree.mask);
  *   O    [R][B+1][Hq][dh] fp32 out; O_bf16 the same rounded to bf16 (or NULL).
  * Row 0 attends to the Lp prefix keys; node i attends to the prefix and to
@@ -324,7 +326,7 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
  * rounding.  Calls sharing one workspace must not overlap on the GPU.
  * err: optional device word; a bounded pipeline wait that runs out ORs
  * 2 (timeout) into it (NULL: a library-internal word). */
-dartree_status dartree_tree_attention(const void *Q, const void *K, const void *Vt, int64_t ldv,
+dartree_status dartree_tree_attention(const void *Q, const void *K, const void *Vt,
                                       const uint32_t *mask, int32_t R, int32_t Lp, int32_t B,
                                       int32_t Hq, int32_t Hkv, int32_t dh, float scale, float *O,
                                       void *O_bf16, void *work, size_t work_bytes, int32_t *err,

@@ -16,17 +16,18 @@
 //
 // Warp roles (320 threads): warps 0-7 softmax (two warpgroups; a thread
 // owns a query row = TMEM lane, its group half of each key tile and half of
-// the head dimensions of O), warp 8 TMA producer (64-key tiles of K and of the transposed value
-// cache, 128-byte swizzle), warp 9 TMEM allocator + single-thread MMA issuer.
-// Two passes over the CTA's keys: the first finds each row's maximum scaled
-// score (S = Q K^T, M = 128 rows, N = 64 keys, K = 128 head dims); the
-// second recomputes S, forms P = 2^(s - max) rounded to bf16 in shared
-// memory (the 128-byte swizzled K-major layout the MMA reads) and
-// accumulates O += P V (M = 128, N = 128 head dims, K = 64 keys) in TMEM.
+// the head dimensions of O), warp 8 TMA producer (64-key tiles of K and of
+// the blocked, transposed value cache, 128-byte swizzle), warp 9 TMEM
+// allocator + single-thread MMA issuer.
+// One pass over the CTA's keys with an online softmax: S = Q K^T (M = 128
+// rows, N = 64 keys, K = 128 head dims) into double-buffered TMEM, P =
+// 2^(s - m) rounded to bf16 into shared memory (the 128-byte swizzled
+// K-major layout the MMA reads; double-buffered), O += P V (M = 128, N = 128
+// head dims, K = 64 keys) in TMEM.  The reference maximum m is raised only
+// when a tile beats it by more than 8 (base 2), which rescales O in TMEM.
 // The rounded weights also form the normaliser, so O is an exact convex
 // combination of the visible values with weights within 2^-8 of the exact
-// softmax.  S is double-buffered in TMEM so the softmax of one tile overlaps
-// the products of the next.
+// softmax.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -248,9 +249,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       long long issued = 0;
-      for (int f = 0; f < 2 * nt && !*abort_flag; ++f) {
-        const bool pass2 = f >= nt;
-        const int t = t_beg + (pass2 ? f - nt : f);
+      for (int f = 0; f < nt && !*abort_flag; ++f) {
+        const int t = t_beg + f;
         const int stage = f % kStages;
         const uint32_t ph = static_cast<uint32_t>((f / kStages) & 1);
         if (!mbar_wait(&kv_empty[stage], ph ^ 1u, p.err, p.wait_limit)) {
@@ -258,10 +258,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         uint8_t* k_dst = sStage + stage * kStageBytes;
-        mbar_arrive_expect_tx(&kv_full[stage], pass2 ? kStageBytes : kKBytes);
-        tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, hk, t * kKeys, r);
-        tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, hk, t * kKeys, r);
-        if (pass2) tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], t * kKeys, 0, hk, r);
+        mbar_arrive_expect_tx(&kv_full[stage], kStageBytes);
+        tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, t * kKeys, hk, r);
+        tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, t * kKeys, hk, r);
+        tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], 0, 0, t, hk + p.Hkv * r);
         ++issued;
       }
       // drain: every issued copy must have landed before the CTA may exit
@@ -302,9 +302,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_commit(&s_full[b]);
         return true;
       };
-      // O += P V for pass-2 tile j (its stage), then release P and the stage
+      // O += P V for tile j (its stage), then release P and the stage
       auto issue_o = [&](int j) {
-        const int f = nt + j, stage = f % kStages, pb = j & 1;
+        const int stage = j % kStages, pb = j & 1;
         if (!wait(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sStage + stage * kStageBytes + kKBytes);
@@ -317,14 +317,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_commit(&kv_empty[stage]);
         return true;
       };
-      // pass 1: scores only
+      // scores of tile j, then the product of tile j - 1
       for (int j = 0; j < nt && ok; ++j) {
         if (!issue_s(j, j % kStages)) break;
-        tc_commit(&kv_empty[j % kStages]);
-      }
-      // pass 2: scores of tile j, then the product of tile j - 1
-      for (int j = 0; j < nt && ok; ++j) {
-        if (!issue_s(nt + j, (nt + j) % kStages)) break;
         if (j > 0 && !issue_o(j - 1)) break;
       }
       if (ok && nt > 0) issue_o(nt - 1);
@@ -333,7 +328,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // -------------------------------------------------------- softmax
-    __shared__ float red[2][kQRows];   // per-row exchange between the two groups
+    __shared__ float red[2][kQRows];      // per-row exchange between the two groups
+    __shared__ float red2[2][2][kQRows];  // per-tile row maxima (double-buffered)
+    __shared__ int stop_slot[2][8];       // per-tile stop marks of the 8 warps
     const int wg = warp >> 2, wq = warp & 3;
     const int row = wq * 32 + lane, q = q0 + row;
     const int node = q < p.rows ? q / p.g : 0;
@@ -381,38 +378,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     };
+    // One pass with an online maximum.  P uses a reference maximum m that
+    // is raised only when a tile's row maximum exceeds it by more than 8
+    // (base 2), so weights stay <= 2^8; raising it rescales l and the O
+    // accumulated so far (after the products issued so far have landed).
+    // The two groups meet at a named barrier every tile, so every decision
+    // to stop is taken by all 256 threads together at that barrier: a warp
+    // whose wait ran out marks its stop slot and goes on to the barrier.
     bool go = true;
-    float m = -INFINITY;
-    for (int j = 0; j < nt; ++j) {  // pass 1: the row maximum
-      if (*abort_flag || !mbar_wait(&s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, p.err,
-                                    p.wait_limit)) {
-        go = false;
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
+    float m = -INFINITY, l = 0.f;
+    constexpr int kOH = kDh / 2;
+    // a warp-uniform bounded wait (lane 0 polls, the warp takes its answer)
+    auto wait_w = [&](uint64_t* bar, uint32_t par) {
+      int okl = 0;
+      if (lane == 0) okl = mbar_wait(bar, par, p.err, p.wait_limit) ? 1 : 0;
+      return __shfl_sync(kFullMask, okl, 0) != 0;
+    };
+    for (int j = 0; j < nt; ++j) {
+      const bool okw = go && !*abort_flag && wait_w(&s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u);
       float s[kHalf];
-      load_s(j, t_beg + j, s);
+      float mh = -INFINITY;
+      if (okw) {
+        tc_fence_after();
+        load_s(j, t_beg + j, s);
 #pragma unroll
-      for (int c = 0; c < kHalf; ++c) m = fmaxf(m, s[c]);
-    }
-    red[wg][row] = m;  // the two halves' maxima -> the row's
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    m = fmaxf(red[0][row], red[1][row]);
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    const float sub = m == -INFINITY ? 0.f : m;
-    float l = 0.f;
-    for (int j = 0; j < nt && go; ++j) {  // pass 2: P and the normaliser
-      const int u = nt + j;
-      if (*abort_flag || !mbar_wait(&s_full[u & 1], static_cast<uint32_t>(u >> 1) & 1u, p.err,
-                                    p.wait_limit)) {
+        for (int c = 0; c < kHalf; ++c) mh = fmaxf(mh, s[c]);
+      }
+      red2[j & 1][wg][row] = mh;  // the row maximum of the tile, both halves
+      if (lane == 0) stop_slot[j & 1][warp] = okw ? 0 : 1;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      int stop = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) stop |= stop_slot[j & 1][w];
+      if (stop) {  // the same for all 256 threads
         go = false;
         *abort_flag = 1;
         break;
       }
-      tc_fence_after();
-      float s[kHalf];
-      load_s(u, t_beg + j, s);
+      const float mx = fmaxf(red2[j & 1][0][row], red2[j & 1][1][row]);
+      const bool raise = mx > m + 8.f;  // the same in both groups
+      bool failed = false;
+      if (__any_sync(kFullMask, raise)) {
+        const float m_new = raise ? mx : m;
+        const float alpha = raise ? fast_ex2(m - m_new) : 1.f;  // 0 when m was -inf
+        l *= alpha;
+        m = m_new;
+        if (j > 0) {  // O holds the products of tiles 0..j-1: wait for the last
+          failed = !wait_w(&p_empty[(j - 1) & 1], static_cast<uint32_t>((j - 1) >> 1) & 1u);
+          if (!failed) {
+            tc_fence_after();
+            const uint32_t oaddr = tmem_base + lane_base + kColO + wg * kOH;
+#pragma unroll
+            for (int c = 0; c < kOH; c += 16) {
+              float x[16];
+              tmem_ld16(oaddr + c, x);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) x[i] *= alpha;
+              tmem_st16(oaddr + c, x);
+            }
+            tmem_wait_st();
+          }
+        }
+      }
+      const float sub = m == -INFINITY ? 0.f : m;
       uint32_t pk[kHalf / 2];
 #pragma unroll
       for (int c = 0; c < kHalf; c += 2) {
@@ -422,11 +450,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       // the product two tiles back has released this P buffer
       const int pb = j & 1;
-      if (!mbar_wait(&p_empty[pb], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.err,
-                     p.wait_limit)) {
+      if (!failed) failed = !wait_w(&p_empty[pb], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u);
+      if (failed) {  // stop at the next tile's barrier, with the other group
         go = false;
         *abort_flag = 1;
-        break;
+        continue;
       }
       uint8_t* dst = sP + pb * kPBytes;
 #pragma unroll
@@ -434,16 +462,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         *reinterpret_cast<uint4*>(dst + sw128(row, wg * 4 + gi)) =
             make_uint4(pk[gi * 4], pk[gi * 4 + 1], pk[gi * 4 + 2], pk[gi * 4 + 3]);
       fence_proxy_async_smem();
+      tc_fence_before();  // the rescaled O is ordered before the next product
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
     }
+    // (a group that stopped early still meets the other at every barrier
+    // below; the barriers inside the loop are met by both while neither
+    // has stopped, and a stop sets the abort flag both then see)
     red[wg][row] = l;  // the two halves' sums -> the row's
     asm volatile("bar.sync 1, 256;" ::: "memory");
     l = red[0][row] + red[1][row];
     // this group's half of the head dimensions of O
-    constexpr int kOH = kDh / 2;
     float o[kOH];
-    if (go && nt > 0 && mbar_wait(o_done, 0, p.err)) {
+    if (go && nt > 0 && wait_w(o_done, 0)) {
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < kOH; c += 16) {
@@ -583,7 +614,7 @@ extern "C" size_t dartree_tree_attention_workspace(int32_t R, int32_t Lp, int32_
 }
 
 extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, const void* Vt,
-                                                 int64_t ldv, const uint32_t* mask, int32_t R,
+                                                 const uint32_t* mask, int32_t R,
                                                  int32_t Lp, int32_t B, int32_t Hq, int32_t Hkv,
                                                  int32_t dh, float scale, float* O, void* O_bf16,
                                                  void* work, size_t work_bytes, int32_t* err,
@@ -595,29 +626,29 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
       Lp + B < 1 || !(scale > 0.f))
     return fail(DARTREE_ERR_INVALID_ARG, "bad R, Lp, B, Hq, Hkv or scale");
   if (dh != kDh) return fail(DARTREE_ERR_UNSUPPORTED, "head dimension must be 128");
-  if (ldv < Lp + B || ldv % 8 != 0)
-    return fail(DARTREE_ERR_INVALID_ARG, "ldv must be >= Lp + B and a multiple of 8");
   const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                        reinterpret_cast<uintptr_t>(Vt) | reinterpret_cast<uintptr_t>(O) |
                        reinterpret_cast<uintptr_t>(O_bf16);
   if (al & 15) return fail(DARTREE_ERR_INVALID_ARG, "Q, K, Vt and O must be 16-byte aligned");
   const int L = Lp + B;
   CUtensorMap tm_k, tm_vt;
-  {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDh), static_cast<cuuint64_t>(Hkv),
-                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(R)};
+  const int nblk = (L + kKeys - 1) / kKeys;
+  {  // keys [R][Hkv][L][dh]: a tile is 64 consecutive rows of one head
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDh), static_cast<cuuint64_t>(L),
+                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(R)};
     const cuuint64_t str[3] = {static_cast<cuuint64_t>(kDh) * 2,
-                               static_cast<cuuint64_t>(Hkv) * kDh * 2,
-                               static_cast<cuuint64_t>(L) * Hkv * kDh * 2};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kKeys), 1};
+                               static_cast<cuuint64_t>(L) * kDh * 2,
+                               static_cast<cuuint64_t>(Hkv) * L * kDh * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kKeys), 1, 1};
     if (!encode_4d(&tm_k, K, dims, str, box)) return fail(DARTREE_ERR_CUDA, "key tensor map");
   }
-  {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(kDh),
-                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(R)};
-    const cuuint64_t str[3] = {static_cast<cuuint64_t>(ldv) * 2,
-                               static_cast<cuuint64_t>(ldv) * kDh * 2,
-                               static_cast<cuuint64_t>(ldv) * kDh * Hkv * 2};
+  {  // values [R][Hkv][nblk][dh][64]: a tile is one contiguous transposed block
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kKeys), static_cast<cuuint64_t>(kDh),
+                                static_cast<cuuint64_t>(nblk),
+                                static_cast<cuuint64_t>(Hkv) * R};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(kKeys) * 2,
+                               static_cast<cuuint64_t>(kKeys) * kDh * 2,
+                               static_cast<cuuint64_t>(nblk) * kKeys * kDh * 2};
     const cuuint32_t box[4] = {static_cast<cuuint32_t>(kKeys), static_cast<cuuint32_t>(kDh), 1,
                                1};
     if (!encode_4d(&tm_vt, Vt, dims, str, box)) return fail(DARTREE_ERR_CUDA, "value tensor map");

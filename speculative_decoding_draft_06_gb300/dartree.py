@@ -104,9 +104,9 @@ def load():
         "dartree_reset_timing": (st, [_vp]),
         "dartree_state_step_noalloc": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
         "dartree_get_states": (st, [_vp, _i32, _vp, _vp]),
-        "dartree_tree_attention": (st, [_vp, _vp, _vp, ctypes.c_int64, _vp, _i32, _i32, _i32,
-                                        _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp,
-                                        ctypes.c_size_t, _vp, _vp]),
+        "dartree_tree_attention": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                        ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _vp,
+                                        _vp]),
         "dartree_tree_attention_workspace": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
         "dartree_accept": (st, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     }
@@ -397,16 +397,16 @@ def tree_attention(Q, K, Vt, mask, *, Lp: int, scale: float | None = None,
                    want_bf16: bool = True, work=None, split: bool = True, err=None,
                    stream=None) -> dict:
     """Tree attention of the verification forward (dartree_tree_attention):
-    Q [R,B+1,Hq,dh], key cache K [R,Lp+B,Hkv,dh] (prefix keys, then the tree
-    nodes'), transposed value cache Vt [R,Hkv,dh,ldv] (bf16 CUDA tensors),
+    Q [R,B+1,Hq,dh], key cache K [R,Hkv,Lp+B,dh] (prefix keys, then the tree
+    nodes'), blocked transposed value cache Vt [R,Hkv,ceil(L/64),dh,64] (bf16
+    CUDA tensors; see kv_cache),
     mask [R,B,words] int32 -> {"O": fp32, "O16": bf16 bits}.  ``work`` is
     the key-split scratch (allocated here when None and ``split``)."""
     for n, t in (("Q", Q), ("K", K), ("Vt", Vt)):
         _dev(t, n, _W16)
     _dev(mask, "mask", (torch.int32,))
     R, Bp1, Hq, dh = Q.shape
-    Hkv = K.shape[2]
-    ldv = Vt.shape[3]
+    Hkv = K.shape[1]
     O = torch.empty(R, Bp1, Hq, dh, dtype=torch.float32, device=Q.device)
     O16 = torch.empty(R, Bp1, Hq, dh, dtype=torch.int16, device=Q.device) if want_bf16 else None
     sc = float(scale) if scale is not None else dh ** -0.5
@@ -415,21 +415,22 @@ def tree_attention(Q, K, Vt, mask, *, Lp: int, scale: float | None = None,
         work = torch.empty(max(n, 16), dtype=torch.uint8, device=Q.device)
     wb = 0 if work is None else work.numel() * work.element_size()
     _check_free(load().dartree_tree_attention(
-        _ptr(Q), _ptr(K), _ptr(Vt), ldv, _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh,
+        _ptr(Q), _ptr(K), _ptr(Vt), _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh,
         ctypes.c_float(sc), _ptr(O), _ptr(O16), _ptr(work), wb, _ptr(err), _stream(stream)))
     return {"O": O, "O16": O16}
 
 
 def kv_cache(Kp, Vp, Kt, Vt) -> tuple[torch.Tensor, torch.Tensor]:
-    """Key cache [R, Lp+B, Hkv, dh] and transposed value cache [R, Hkv, dh,
-    ldv] (ldv = Lp+B rounded up to 8) from prefix and tree keys / values
-    (CUDA tensors; data movement only)."""
-    K = torch.cat([Kp, Kt], dim=1).contiguous()
-    V = torch.cat([Vp, Vt], dim=1)                       # [R, L, Hkv, dh]
-    R, L, Hkv, dh = V.shape
-    ldv = (L + 7) // 8 * 8
-    VT = torch.zeros(R, Hkv, dh, ldv, dtype=V.dtype, device=V.device)
-    VT[..., :L] = V.permute(0, 2, 3, 1)
+    """Key cache [R, Hkv, Lp+B, dh] and blocked transposed value cache
+    [R, Hkv, ceil(L/64), dh, 64] from prefix [R, Lp, Hkv, dh] and tree
+    [R, B, Hkv, dh] keys / values (CUDA tensors; data movement only)."""
+    K = torch.cat([Kp, Kt], dim=1).permute(0, 2, 1, 3).contiguous()   # [R, Hkv, L, dh]
+    V = torch.cat([Vp, Vt], dim=1).permute(0, 2, 1, 3)                 # [R, Hkv, L, dh]
+    R, Hkv, L, dh = V.shape
+    nb = (L + 63) // 64
+    Vb = torch.zeros(R, Hkv, nb * 64, dh, dtype=V.dtype, device=V.device)
+    Vb[:, :, :L] = V
+    VT = Vb.view(R, Hkv, nb, 64, dh).transpose(3, 4).contiguous()      # [R, Hkv, nb, dh, 64]
     return K, VT
 
 
