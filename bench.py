@@ -630,7 +630,7 @@ def run_verify(args) -> None:
                          "frac": proj_bytes / (t_proj * 1e-3) / 1e9 / peak,
                          "peak_source": peak_kind, "traffic": None,
                          "bytes_per_launch": proj_bytes, "launch_ms": t_proj},
-            "attention": {"kernel": "k_tree_attention (tcgen05, S and O in TMEM, two-pass softmax, key split)",
+            "attention": {"kernel": "k_tree_attention (tcgen05, S and O in TMEM, online softmax, key split)",
                           "bound": "tensor", "launch_ms": t_att,
                           "achieved": att_flops / (t_att * 1e-3) / 1e12, "peak": tfl,
                           "unit": "TFLOP/s", "frac": att_flops / (t_att * 1e-3) / 1e12 / tfl,

@@ -16,14 +16,14 @@
 //
 // Warp roles (320 threads): warps 0-7 softmax (two warpgroups; a thread
 // owns a query row = TMEM lane, its group half of each key tile and half of
-// the head dimensions of O), warp 8 TMA producer (64-key tiles of K and of
+// the head dimensions of O), warp 8 TMA producer (128-key tiles of K and of
 // the blocked, transposed value cache, 128-byte swizzle), warp 9 TMEM
 // allocator + single-thread MMA issuer.
 // One pass over the CTA's keys with an online softmax: S = Q K^T (M = 128
-// rows, N = 64 keys, K = 128 head dims) into double-buffered TMEM, P =
+// rows, N = 128 keys, K = 128 head dims) into double-buffered TMEM, P =
 // 2^(s - m) rounded to bf16 into shared memory (the 128-byte swizzled
-// K-major layout the MMA reads; double-buffered), O += P V (M = 128, N = 128
-// head dims, K = 64 keys) in TMEM.  The reference maximum m is raised only
+// K-major layout the MMA reads), O += P V (M = 128, N = 128 head dims,
+// K = 128 keys) in TMEM.  The reference maximum m is raised only
 // when a tile beats it by more than 8 (base 2), which rescales O in TMEM.
 // The rounded weights also form the normaliser, so O is an exact convex
 // combination of the visible values with weights within 2^-8 of the exact
@@ -43,19 +43,21 @@ namespace {
 
 constexpr int kDh = 128;           // head dimension (fixed)
 constexpr int kQRows = 128;        // query rows per CTA (TMEM lanes)
-constexpr int kKeys = 64;          // keys per tile
+constexpr int kKeys = 128;         // keys per tile
+constexpr int kVBlock = 64;        // keys per value-cache block (one swizzle atom)
+constexpr int kPBufs = 1;          // P buffers in shared memory
 constexpr int kAttnThreads = 320;
 constexpr int kSoftmaxThreads = 256;   // two warpgroups, one per half of each key tile
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kHalf = kKeys / 2;       // keys of a tile per warpgroup
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr int kQBytes = kQRows * kDh * 2;        // 32 KB: 2 swizzle atoms of 64 head dims
-constexpr int kPBytes = kQRows * kKeys * 2;      // 16 KB per buffer: one atom of 64 keys
-constexpr int kKBytes = kKeys * kDh * 2;         // 16 KB: 2 atoms of 64 head dims
-constexpr int kVBytes = kDh * kKeys * 2;         // 16 KB: 128 head-dim rows x 64 keys
+constexpr int kPBytes = kQRows * kKeys * 2;      // 32 KB: 2 atoms of 64 keys
+constexpr int kKBytes = kKeys * kDh * 2;         // 32 KB: 2 atoms of 64 head dims
+constexpr int kVBytes = kDh * kKeys * 2;         // 32 KB: 2 blocks of 128 head dims x 64 keys
 constexpr int kStageBytes = kKBytes + kVBytes;
-constexpr uint32_t kTmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kTmemCols = 512;              // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint32_t kColO = 256;
 
 struct AttnParams {
   int Lp, B, L, Hq, Hkv, g, words, rows;  // L = Lp + B keys; rows = (B + 1) * g
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sP = sQ + kQBytes;
-  uint8_t* sStage = sP + 2 * kPBytes;  // P is double-buffered
+  uint8_t* sStage = sP + kPBufs * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + kStages * kStageBytes);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + kStages;
@@ -261,7 +263,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive_expect_tx(&kv_full[stage], kStageBytes);
         tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, t * kKeys, hk, r);
         tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, t * kKeys, hk, r);
-        tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], 0, 0, t, hk + p.Hkv * r);
+        tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], 0, 0, 2 * t, hk + p.Hkv * r);
+        tma_load_4d(k_dst + kKBytes + kVBytes / 2, &tm_vt, &kv_full[stage], 0, 0, 2 * t + 1,
+                    hk + p.Hkv * r);
         ++issued;
       }
       // drain: every issued copy must have landed before the CTA may exit
@@ -304,15 +308,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       // O += P V for tile j (its stage), then release P and the stage
       auto issue_o = [&](int j) {
-        const int stage = j % kStages, pb = j & 1;
-        if (!wait(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u)) return false;
+        const int stage = j % kStages, pb = j % kPBufs;
+        if (!wait(&p_full[pb], static_cast<uint32_t>(j / kPBufs) & 1u)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sStage + stage * kStageBytes + kKBytes);
         const uint32_t pa = p_addr + pb * kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          tc_mma_bf16(tmem_base + kColO, smem_desc_sw128(pa + kk * 32),
-                      smem_desc_sw128(v_addr + kk * 32), idesc_o, (j != 0 || kk != 0) ? 1u : 0u);
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32u;  // 16 keys within the 128-byte row
+          tc_mma_bf16(tmem_base + kColO, smem_desc_sw128(pa + (kk >> 2) * (kQRows * 128) + off),
+                      smem_desc_sw128(v_addr + (kk >> 2) * (kDh * 128) + off), idesc_o,
+                      (j != 0 || kk != 0) ? 1u : 0u);
+        }
         tc_commit(&p_empty[pb]);
         tc_commit(&kv_empty[stage]);
         return true;
@@ -358,12 +365,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) s[c] *= p.scale_log2;
       } else {
-        uint32_t w[2] = {0u, 0u};   // mask words covering the half tile's tree keys
+        uint32_t w[3] = {0u, 0u, 0u};  // mask words covering the half tile's tree keys
         const int tt0 = j0 - p.Lp;  // tree index of the first key
         const int wb = tt0 >= 0 ? tt0 >> 5 : 0;
         if (mrow) {
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
+          for (int k = 0; k < 3; ++k)
             if (wb + k < p.words) w[k] = __ldg(mrow + wb + k);
         }
 #pragma unroll
@@ -424,7 +431,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l *= alpha;
         m = m_new;
         if (j > 0) {  // O holds the products of tiles 0..j-1: wait for the last
-          failed = !wait_w(&p_empty[(j - 1) & 1], static_cast<uint32_t>((j - 1) >> 1) & 1u);
+          failed = !wait_w(&p_empty[(j - 1) % kPBufs],
+                           static_cast<uint32_t>((j - 1) / kPBufs) & 1u);
           if (!failed) {
             tc_fence_after();
             const uint32_t oaddr = tmem_base + lane_base + kColO + wg * kOH;
@@ -448,18 +456,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
         pk[c / 2] = v;
       }
-      // the product two tiles back has released this P buffer
-      const int pb = j & 1;
-      if (!failed) failed = !wait_w(&p_empty[pb], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u);
+      // the product that last read this P buffer has finished
+      const int pb = j % kPBufs;
+      if (!failed)
+        failed = !wait_w(&p_empty[pb], (static_cast<uint32_t>(j / kPBufs) & 1u) ^ 1u);
       if (failed) {  // stop at the next tile's barrier, with the other group
         go = false;
         *abort_flag = 1;
         continue;
       }
-      uint8_t* dst = sP + pb * kPBytes;
+      uint8_t* dst = sP + pb * kPBytes + wg * (kQRows * 128);  // this group's atom
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi)
-        *reinterpret_cast<uint4*>(dst + sw128(row, wg * 4 + gi)) =
+      for (int gi = 0; gi < 8; ++gi)
+        *reinterpret_cast<uint4*>(dst + sw128(row, gi)) =
             make_uint4(pk[gi * 4], pk[gi * 4 + 1], pk[gi * 4 + 2], pk[gi * 4 + 3]);
       fence_proxy_async_smem();
       tc_fence_before();  // the rescaled O is ordered before the next product
@@ -632,7 +641,7 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
   if (al & 15) return fail(DARTREE_ERR_INVALID_ARG, "Q, K, Vt and O must be 16-byte aligned");
   const int L = Lp + B;
   CUtensorMap tm_k, tm_vt;
-  const int nblk = (L + kKeys - 1) / kKeys;
+  const int nblk = (L + kVBlock - 1) / kVBlock;
   {  // keys [R][Hkv][L][dh]: a tile is 64 consecutive rows of one head
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDh), static_cast<cuuint64_t>(L),
                                 static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(R)};
@@ -643,13 +652,13 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     if (!encode_4d(&tm_k, K, dims, str, box)) return fail(DARTREE_ERR_CUDA, "key tensor map");
   }
   {  // values [R][Hkv][nblk][dh][64]: a tile is one contiguous transposed block
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kKeys), static_cast<cuuint64_t>(kDh),
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kVBlock), static_cast<cuuint64_t>(kDh),
                                 static_cast<cuuint64_t>(nblk),
                                 static_cast<cuuint64_t>(Hkv) * R};
-    const cuuint64_t str[3] = {static_cast<cuuint64_t>(kKeys) * 2,
-                               static_cast<cuuint64_t>(kKeys) * kDh * 2,
-                               static_cast<cuuint64_t>(nblk) * kKeys * kDh * 2};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kKeys), static_cast<cuuint32_t>(kDh), 1,
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(kVBlock) * 2,
+                               static_cast<cuuint64_t>(kVBlock) * kDh * 2,
+                               static_cast<cuuint64_t>(nblk) * kVBlock * kDh * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kVBlock), static_cast<cuuint32_t>(kDh), 1,
                                1};
     if (!encode_4d(&tm_vt, Vt, dims, str, box)) return fail(DARTREE_ERR_CUDA, "value tensor map");
   }
@@ -674,7 +683,7 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   }
   const size_t smem =
-      1024 + kQBytes + 2 * kPBytes + static_cast<size_t>(kStages) * kStageBytes + 256;
+      1024 + kQBytes + kPBufs * kPBytes + static_cast<size_t>(kStages) * kStageBytes + 256;
   e = cudaFuncSetAttribute(k_tree_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
@@ -687,7 +696,10 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int n_split = sms / tiles;  // one CTA per SM
   n_split = n_split < kMaxSplit ? n_split : kMaxSplit;
-  n_split = n_split < key_tiles ? n_split : key_tiles;
+  // a split must keep at least 12 key tiles: the partials' round trip and
+  // the combine cost about as much as a dozen tiles
+  const int by_keys = key_tiles / 12;
+  n_split = n_split < by_keys ? n_split : by_keys;
   if (n_split < 1) n_split = 1;
   if ((reinterpret_cast<uintptr_t>(work) & 15) != 0) work = nullptr;
   while (n_split > 1 && (work == nullptr || split_bytes(R, B, Hq, Hkv, n_split) > work_bytes))

@@ -49,6 +49,9 @@ ATTN_CASES = [  # R, B, Lp, Hq, Hkv
     (2, 130, 300, 8, 2),
     (1, 256, 64, 16, 4),
     (1, 40, 1000, 2, 1),
+    (1, 40, 3000, 2, 1),      # long key ranges: the keys are split over CTAs
+    (1, 130, 4000, 8, 2),
+    (2, 16, 8000, 4, 2),
 ]
 
 
