@@ -15,8 +15,10 @@
 //     row's true K-th key from below (that list alone holds K keys at or
 //     above it), so no key of the final top-K is ever filtered out; the
 //     bound only spares CTAs the insertions of keys that cannot make it;
-//   * one or two entrants are inserted one at a time, more are warp-sorted
-//     and merged with the list by a bitonic merge;
+//   * the common case -- no key of the row's 128 beats the threshold -- is
+//     one 64-bit compare per value and one vote; rows with entrants go
+//     through list_update (a tighter bound from the tile itself, then one
+//     compacted batch);
 //   * softmax state: for <= 64 rows each lane keeps a running (max, sum) per
 //     owned row in registers and lanes are combined once at the end; for more
 //     rows each chunk is reduced across the warp and folded into a per-row
@@ -102,13 +104,81 @@ static __device__ __noinline__ void list_merge_batch(uint64_t* L, int K, uint64_
   __syncwarp();
 }
 
+// The entrants of one row (keys above th; cnt of this lane, total of the
+// warp) into the sorted list L.  With many entrants the threshold is first
+// raised to a bound from the keys themselves: split the lanes into K
+// disjoint groups; the K group maxima are K distinct keys at or above their
+// minimum, so no key below it is in the row's top-K.  The entrants are then
+// compacted to one per lane (staging stg) and go in by single inserts or
+// one batch merge.  Warp-collective.
+static __device__ __forceinline__ void list_update(uint64_t* L, int K, uint64_t* stg, uint64_t th,
+                                                uint64_t k0, uint64_t k1, uint64_t k2, uint64_t k3,
+                                                int cnt, int total) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t key[4] = {k0, k1, k2, k3};
+  if (total > 4) {
+    // K disjoint groups of gs lanes: the minimum of the group maxima
+    const int gs = 1 << (31 - __clz(32 / K));
+    uint64_t m = key[0] > key[1] ? key[0] : key[1];
+    const uint64_t m23 = key[2] > key[3] ? key[2] : key[3];
+    m = m > m23 ? m : m23;
+    for (int s = 1; s < gs; s <<= 1) {
+      const uint64_t o = shfl_xor_u64(m, s);
+      m = m > o ? m : o;
+    }
+    if (lane >= K * gs) m = ~0ull;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const uint64_t o = shfl_xor_u64(m, s);
+      m = m < o ? m : o;
+    }
+    if (m > 0ull && m - 1ull > th) {  // keys >= m may enter
+      th = m - 1ull;
+      cnt = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cnt += key[i] > th ? 1 : 0;
+      total = __reduce_add_sync(kFull, static_cast<unsigned>(cnt));
+    }
+  }
+  if (total <= 32) {
+    // compact: this lane's entrants go after those of the lanes below it
+    const unsigned below = (1u << lane) - 1u;
+    int pos = __popc(__ballot_sync(kFull, cnt & 1) & below) +
+              2 * __popc(__ballot_sync(kFull, cnt & 2) & below) +
+              4 * __popc(__ballot_sync(kFull, cnt & 4) & below);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (key[i] > th) stg[pos++] = key[i];
+    __syncwarp();
+    const uint64_t kk = lane < total ? stg[lane] : 0ull;
+    __syncwarp();
+    if (total <= 2)
+      list_insert_lanes(L, K, kk, __ballot_sync(kFull, lane < total));
+    else
+      list_merge_batch(L, K, kk);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint64_t t = L[K - 1];
+      t = t > th ? t : th;
+      const unsigned bal = __ballot_sync(kFull, key[i] > t);
+      if (bal == 0u) continue;
+      if (__popc(bal) <= 2)
+        list_insert_lanes(L, K, key[i], bal);
+      else
+        list_merge_batch(L, K, key[i] > t ? key[i] : 0ull);
+    }
+  }
+}
+
 // Shared-memory footprint of the epilogue (bytes) for N rows, top-K and NG
 // warpgroups.
 __host__ __device__ constexpr size_t epi_smem_bytes(int N, int K, int NG = 1) {
   return static_cast<size_t>(N) * K * 8                    // lists
          + static_cast<size_t>(NG) * 2 * 16 * 132 * 4       // transposed chunks, 2 per group
          + static_cast<size_t>(N) * 8                       // running (max, sum) per row
-         + static_cast<size_t>(N) * 8;                      // per-tile copy of the row bounds
+         + static_cast<size_t>(N) * 8                       // per-tile copy of the row bounds
+         + static_cast<size_t>(NG) * 4 * 32 * 8;            // entrant staging, 32 keys per warp
 }
 
 // NG warpgroups (1 or 2) share the epilogue.  The head rows come in chunks of
@@ -128,6 +198,7 @@ struct LogitsEpilogue {
   uint64_t* lists;          // [N][K], one sorted list per row
   unsigned long long* gth;  // [N] global per-row lower bound of the K-th key (or null)
   uint64_t* gcache;         // [N] this tile's copy of gth
+  uint64_t* stg;            // [32] entrant staging of this warp
   float* T;                 // [2][16][kTPitch] of this group
   float2* run;              // [N] (N > 64)
   int K, M, lane, w4, g, t;
@@ -158,6 +229,7 @@ struct LogitsEpilogue {
     lane = threadIdx.x & 31;
     w4 = t >> 5;
     T = T0 + g * 2 * 16 * kTPitch;
+    stg = gcache + N + (tt >> 5) * 32;
     nchunk = 0;
     bad = false;
 #pragma unroll
@@ -200,23 +272,21 @@ struct LogitsEpilogue {
     uint64_t* L = lists + static_cast<size_t>(c) * K;
     const uint64_t gb = gcache[c];
     const uint64_t k_before = L[K - 1];
+    const uint64_t th = k_before > gb ? k_before : gb;
+    uint64_t key[4];
+    int cnt = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t v = v0 + lane + 32 * i;
-      const bool valid = static_cast<int>(v) < V;
-      const uint64_t key = (valid && xv[i] == xv[i]) ? make_key(xv[i], v) : 0ull;
-      uint64_t th = L[K - 1];
-      th = th > gb ? th : gb;
-      const unsigned bal = __ballot_sync(kFull, key > th);
-      if (bal == 0u) continue;
-      if (__popc(bal) <= 2)
-        list_insert_lanes(L, K, key, bal);
-      else
-        list_merge_batch(L, K, key > th ? key : 0ull);
+      key[i] = (static_cast<int>(v) < V && xv[i] == xv[i]) ? make_key(xv[i], v) : 0ull;
+      cnt += key[i] > th ? 1 : 0;
     }
+    const int total = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(cnt)));
+    if (total == 0) return;  // the common case once the bounds have filled
+    list_update(L, K, stg, th, key[0], key[1], key[2], key[3], cnt, total);
     // publish an improved bound (the list's K-th key, once the list is full)
     const uint64_t k_after = L[K - 1];
-    if (gth && lane == 0 && k_after > k_before && k_after > gb) atomicMax(gth + c, k_after);
+    if (gth && lane == 0 && k_after > th) atomicMax(gth + c, k_after);
   }
 
   __device__ __forceinline__ void load4(const float* Tb, int j, uint32_t v0, int V, float (&xv)[4],
