@@ -33,10 +33,12 @@ from speculative_decoding_draft_06_gb300 import inputs as I  # noqa: E402
 
 DEFAULT_CONFIG = "q8b"
 FALLBACK_HBM_GBS = 6800.0
+ROWS_MIN = 65  # head calls with this many rows run k_head_rows (the library's default)
 KERNEL_SOURCES = ("speculative_decoding_draft_06_gb300/csrc/head_tc.cu",
                   "speculative_decoding_draft_06_gb300/csrc/epilogue.cuh",
                   "speculative_decoding_draft_06_gb300/csrc/ptx.cuh",
-                  "speculative_decoding_draft_06_gb300/csrc/common.cuh")
+                  "speculative_decoding_draft_06_gb300/csrc/common.cuh",
+                  "speculative_decoding_draft_06_gb300/csrc/head_rows.cu")
 
 
 def parse_args(argv=None):
@@ -414,10 +416,13 @@ def run_gpu(args) -> None:
     bytes_launch = kernel_bytes_per_launch(w, args.variant, kind)
     achieved = bytes_launch / (head_avg_ms * 1e-3) / 1e9
     traffic = profiled_traffic(args.config) if args.variant == "dartree" else None
+    big = [m for m in w.head_rows() if m >= ROWS_MIN]
     kernel_name = {
         "head": ("k_cand_logits (candidate logits)" if opt.get("candidates") == "base" else
-                 "k_head_tc (head call: Wout stream, fused log-softmax + top-K)" if w.bf16
-                 else "k_head_simt"),
+                 "k_head_simt" if not w.bf16 else
+                 "k_head_tc (head call: Wout stream, fused log-softmax + top-K)" if not big else
+                 f"k_head_rows (head call, {max(big)} head rows on the MMA M side: Wout stream, "
+                 f"fused log-softmax + top-K; calls with fewer than {ROWS_MIN} rows: k_head_tc)"),
         "state": ("k_state_markov" if opt.get("head") == "markov" else
                   "k_head_tc (state step: A stream, split-K)"),
         "candidates": "k_base_topk (top-K of the base logits)"}[kind]
@@ -624,8 +629,9 @@ def run_verify(args) -> None:
             "config": dict(workload_config(w), verify=(
                 f"target layer: prefix {vs.Lp}, {vs.Hq} query heads, {vs.Hkv} kv heads, head "
                 f"dim {vs.dh}; projection [V, {H2}] (the head's Wout as stand-in)")),
-            "roofline": {"bound": "hbm", "kernel": "k_head_tc (target output projection, "
-                         f"{rows} rows, K=1)", "achieved": proj_bytes / (t_proj * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": (
+                             "k_head_rows" if rows >= ROWS_MIN else "k_head_tc") +
+                         f" (target output projection, {rows} rows, K=1)", "achieved": proj_bytes / (t_proj * 1e-3) / 1e9,
                          "peak": peak, "unit": "GB/s",
                          "frac": proj_bytes / (t_proj * 1e-3) / 1e9 / peak,
                          "peak_source": peak_kind, "traffic": None,

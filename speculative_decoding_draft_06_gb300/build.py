@@ -15,7 +15,8 @@ LIB = os.path.join(OUT_DIR, "libdartree.so")
 # (source, extra flags, object name): the head kernels are built once per MMA N
 _NS = (16, 32, 64, 128, 256)
 SOURCES = ([("api.cu", [], "api.o"), ("select.cu", [], "select.o"),
-            ("noalloc.cu", [], "noalloc.o"), ("variants.cu", [], "variants.o"), ("verify.cu", [], "verify.o")]
+            ("noalloc.cu", [], "noalloc.o"), ("variants.cu", [], "variants.o"), ("verify.cu", [], "verify.o"),
+            ("head_rows.cu", [], "head_rows.o")]
            + [("head_tc.cu", [f"-DDT_N={n}"], f"head_tc_{n}.o") for n in _NS]
            + [("head_simt.cu", [f"-DDT_N={n}"], f"head_simt_{n}.o") for n in _NS])
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -66,7 +66,8 @@ struct dartree_ctx {
   int* row_cnt = nullptr;           // [256] per-row group arrival counters (merge)
   uint64_t* gpl = nullptr;          // [256][8][32] per-group top-K lists (merge)
   float2* gls = nullptr;            // [256][8] per-group (max, sum-exp) (merge)
-  unsigned long long* gth = nullptr;  // [256] per-row top-K bound of a head call
+  unsigned long long* gth = nullptr;  // [256] per-row top-K bound of a head call, then
+                                      // [256][32] per-row CTA-group best keys
   float* part = nullptr;            // split-K partial sums of the state step
   int* tile_cnt = nullptr;          // split-K arrival counters
   int state_split = 1;
@@ -90,6 +91,8 @@ struct dartree_ctx {
   cudaGraphExec_t gexec = nullptr;
   GraphKey gkey{};
   int tc_ctas_per_sm = 1;  // tuning: head-call CTAs per SM
+  int rows_min = 65;       // head calls with at least this many rows put the rows on the MMA M side
+  int rows_nv = 128;       // ... in vocabulary tiles of this many entries (128 or 256)
   float* pm = nullptr;
   float* ps = nullptr;
   uint64_t* ptop = nullptr;
@@ -261,6 +264,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.ps = c->ps;
   p.ptop = c->ptop;
   p.gth = c->gth;
+  p.gmx = c->gth + dt::kMaxRows;
   p.cta_stride = c->max_cta;
   p.list_stride = c->max_cta;
   p.pdl = c->pdl;
@@ -269,7 +273,12 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   cudaError_t e;
   {
     KernelTimer tk(c, st, 0);
-    if (c->bf16) {
+    if (c->bf16 && M >= c->rows_min) {  // head rows on the MMA M side
+      const int tiles = (V + c->rows_nv - 1) / c->rows_nv;
+      grid = tiles < c->num_sms ? tiles : c->num_sms;
+      p.max_stages = c->tc_max_stages;
+      e = dt::launch_head_rows(M, c->rows_nv, c->tm_Wout, c->tmS(sbuf, 128), p, grid, st);
+    } else if (c->bf16) {
       const int slots = c->num_sms * c->tc_ctas_per_sm;
       grid = p.n_tiles < slots ? p.n_tiles : slots;
       p.max_stages = c->tc_max_stages;
@@ -315,6 +324,7 @@ dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, i
   mp.gls = c->gls;
   mp.row_cnt = c->row_cnt;
   mp.gth = c->gth;
+  mp.gmx = c->gth + dt::kMaxRows;
   {
     KernelTimer tk(c, st, 2);
     e = dt::launch_merge_rows(mp, st);
@@ -472,7 +482,10 @@ dartree_status check_build_args(dartree_ctx* c, const void* z, const void* s0,
   if (!(beta <= 0.0f)) return c->fail(DARTREE_ERR_INVALID_ARG, "beta must be <= 0 (Lemma 1)");
   const int rows = o.expansion == DARTREE_EXPAND_BESTFIRST ? R : R * W;  // head rows per call
   if (rows > dt::kMaxRows) return c->fail(DARTREE_ERR_UNSUPPORTED, "%d head rows > 256", rows);
-  if (c->bf16 && o.candidates == DARTREE_CAND_CORRECTED && pad_rows(rows) * K > 2048)
+  // the vocabulary-on-M head kernel (fewer than rows_min rows) keeps its
+  // rows' lists in shared memory next to a deep pipeline
+  if (c->bf16 && o.candidates == DARTREE_CAND_CORRECTED && rows < c->rows_min &&
+      pad_rows(rows) * K > 2048)
     return c->fail(DARTREE_ERR_UNSUPPORTED, "padded rows x K = %d > 2048", pad_rows(rows) * K);
   return DARTREE_OK;
 }
@@ -855,6 +868,8 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_PDL")) c->pdl = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_WAIT_LIMIT_CYCLES")) c->wait_limit = atoll(v);
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
+  if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
     const int n = atoi(v);
     c->tc_ctas_per_sm = n == 2 ? 2 : 1;
@@ -892,7 +907,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
                 cudaSuccess &&
             alloc(&c->tile_cnt, static_cast<size_t>(h_tiles)) == cudaSuccess &&
             alloc(&c->row_cnt, rows) == cudaSuccess && alloc(&c->gpl, rows * 8 * 32) == cudaSuccess &&
-            alloc(&c->gls, rows * 8) == cudaSuccess && alloc(&c->gth, rows) == cudaSuccess &&
+            alloc(&c->gls, rows * 8) == cudaSuccess && alloc(&c->gth, rows * 33) == cudaSuccess &&
             alloc(&c->pm, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ps, rows * c->max_cta) == cudaSuccess &&
             alloc(&c->ptop, rows * c->max_cta * dt::kEpiWarps * g.max_K) == cudaSuccess &&
@@ -932,7 +947,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->row_cnt, 0, rows * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(c->gth, 0, rows * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(c->gth, 0, rows * 33 * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->base_cnt, 0, RD * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->bf_tok_next, 0, Rc * sizeof(int32_t));
@@ -1007,7 +1022,8 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
     e = cudaMemset(ctx->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->counters, 0, dt::kMaxRows * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->row_cnt, 0, dt::kMaxRows * sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(ctx->gth, 0, dt::kMaxRows * sizeof(unsigned long long));
+    if (e == cudaSuccess)
+      e = cudaMemset(ctx->gth, 0, dt::kMaxRows * 33 * sizeof(unsigned long long));
     if (e == cudaSuccess)
       e = cudaMemset(ctx->tile_cnt, 0,
                      sizeof(int) * ((ctx->cfg.H + dt::kTileV - 1) / dt::kTileV));
@@ -1188,7 +1204,7 @@ dartree_status dartree_head_topk(dartree_ctx* ctx, const void* S, const float* z
       K > ctx->cfg.V)
     return ctx->fail(DARTREE_ERR_INVALID_ARG, "bad M=%d, rows_per_req=%d or K=%d", M,
                      rows_per_req, K);
-  if (ctx->bf16 && pad_rows(M) * K > 2048)
+  if (ctx->bf16 && M < ctx->rows_min && pad_rows(M) * K > 2048)
     return ctx->fail(DARTREE_ERR_UNSUPPORTED, "padded rows x K > 2048");
   dartree_status s = bind_weights(ctx, ctx->tm_A_ptr, Wout);
   if (s != DARTREE_OK) return s;

@@ -171,6 +171,26 @@ static __device__ __forceinline__ void list_update(uint64_t* L, int K, uint64_t*
   }
 }
 
+// This CTA's best key of a row improved: raise its group's maximum (group =
+// CTA % K), then the row's bound gth to the least of the K group maxima (K
+// distinct keys at or above it; the new value stands in for this CTA's
+// group).  Warp-collective.
+static __device__ __noinline__ void publish_group_best(unsigned long long* gth,
+                                                       unsigned long long* gm, int K,
+                                                       uint64_t best) {
+  const int lane = threadIdx.x & 31;
+  const int mine = blockIdx.x % K;
+  if (lane == 0) atomicMax(gm + mine, best);
+  uint64_t v = lane < K ? __ldcg(gm + lane) : ~0ull;
+  if (lane == mine) v = v > best ? v : best;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = shfl_xor_u64(v, o);
+    v = w < v ? w : v;
+  }
+  if (lane == 0 && v != ~0ull && v > 0ull) atomicMax(gth, v);
+}
+
 // Shared-memory footprint of the epilogue (bytes) for N rows, top-K and NG
 // warpgroups.
 __host__ __device__ constexpr size_t epi_smem_bytes(int N, int K, int NG = 1) {
@@ -178,6 +198,7 @@ __host__ __device__ constexpr size_t epi_smem_bytes(int N, int K, int NG = 1) {
          + static_cast<size_t>(NG) * 2 * 16 * 132 * 4       // transposed chunks, 2 per group
          + static_cast<size_t>(N) * 8                       // running (max, sum) per row
          + static_cast<size_t>(N) * 8                       // per-tile copy of the row bounds
+         + static_cast<size_t>(N) * 8                       // best keys as last published
          + static_cast<size_t>(NG) * 4 * 32 * 8;            // entrant staging, 32 keys per warp
 }
 
@@ -197,7 +218,9 @@ struct LogitsEpilogue {
   float lm[kSlots], ls[kSlots];
   uint64_t* lists;          // [N][K], one sorted list per row
   unsigned long long* gth;  // [N] global per-row lower bound of the K-th key (or null)
+  unsigned long long* gmx;  // [N][32] per-row best key of each CTA group (or null)
   uint64_t* gcache;         // [N] this tile's copy of gth
+  uint64_t* gpub;           // [N] this CTA's best key per row as last published
   uint64_t* stg;            // [32] entrant staging of this warp
   float* T;                 // [2][16][kTPitch] of this group
   float2* run;              // [N] (N > 64)
@@ -215,8 +238,10 @@ struct LogitsEpilogue {
   }
 
   __device__ __forceinline__ void init(uint8_t* smem, int K_, int M_,
-                                       unsigned long long* gth_ = nullptr) {
+                                       unsigned long long* gth_ = nullptr,
+                                       unsigned long long* gmx_ = nullptr) {
     gth = gth_;
+    gmx = gth_ ? gmx_ : nullptr;
     lists = reinterpret_cast<uint64_t*>(smem);
     float* T0 = reinterpret_cast<float*>(lists + static_cast<size_t>(N) * K_);
     run = reinterpret_cast<float2*>(T0 + NG * 2 * 16 * kTPitch);
@@ -229,7 +254,8 @@ struct LogitsEpilogue {
     lane = threadIdx.x & 31;
     w4 = t >> 5;
     T = T0 + g * 2 * 16 * kTPitch;
-    stg = gcache + N + (tt >> 5) * 32;
+    gpub = gcache + N;
+    stg = gpub + N + (tt >> 5) * 32;
     nchunk = 0;
     bad = false;
 #pragma unroll
@@ -241,6 +267,7 @@ struct LogitsEpilogue {
     for (int c = tt; c < N; c += kThreads) {
       run[c] = make_float2(-INFINITY, 0.f);
       gcache[c] = 0ull;
+      gpub[c] = 0ull;
     }
     asm volatile("bar.sync 3, %0;" ::"r"(kThreads) : "memory");
   }
@@ -252,7 +279,7 @@ struct LogitsEpilogue {
     for (int i = lane;; i += 32) {
       const int c = ((i >> 2) * NG + g) * 16 + w4 + 4 * (i & 3);
       if (c >= M) break;
-      gcache[c] = *reinterpret_cast<volatile unsigned long long*>(gth + c);
+      gcache[c] = __ldcg(gth + c);
     }
     __syncwarp();
   }
@@ -284,9 +311,16 @@ struct LogitsEpilogue {
     const int total = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(cnt)));
     if (total == 0) return;  // the common case once the bounds have filled
     list_update(L, K, stg, th, key[0], key[1], key[2], key[3], cnt, total);
-    // publish an improved bound (the list's K-th key, once the list is full)
-    const uint64_t k_after = L[K - 1];
+    // publish improved bounds: the list's K-th key (once the list is full)
+    // and this CTA's best key for its group (gpub: as last published)
+    const uint64_t k_after = L[K - 1], best = L[0];
     if (gth && lane == 0 && k_after > th) atomicMax(gth + c, k_after);
+    if (gmx && best > gpub[c]) {
+      publish_group_best(gth + c, gmx + static_cast<size_t>(c) * 32, K, best);
+      __syncwarp();
+      if (lane == 0) gpub[c] = best;
+      __syncwarp();
+    }
   }
 
   __device__ __forceinline__ void load4(const float* Tb, int j, uint32_t v0, int V, float (&xv)[4],

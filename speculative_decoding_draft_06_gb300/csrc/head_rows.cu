@@ -1,0 +1,456 @@
+// Head call for many head rows (more than 64): the corrected logits
+//   ell[m, v] = z_d[v] + sum_h S[m, h] Wout[v, h]
+// with the online log-sum-exp and the per-row top-K fused into the epilogue
+// ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
+// Mechanism: ONE batched head call on all W paths; "Technische Samenvatting:
+// DARTree", Methodologie 1: the top-k children of every branch, scored from
+// the normalised corrected distribution).
+//
+// Orientation.  With 128 or more head rows the rows fill the tensor core's
+// M side by themselves, so here the head rows are the MMA M (one or two
+// M = 128 halves) and a vocabulary tile of NV = 128 or 256 entries is the
+// MMA N.  The accumulator then holds one head row per TMEM lane: an
+// epilogue thread reads its own row's NV logits of the tile with
+// tcgen05.ld and keeps the row's running (max, sum-exp) and its top-K
+// threshold in registers -- no transposition, no cross-lane reduction, a
+// compare per value.  (The kernel for up to 64 rows, k_head_tc, puts the
+// vocabulary on M instead.)  The states are re-read from L2 for every
+// tile; the wider tile halves that stream per weight byte, at the price of
+// a single accumulator for two halves (the MMAs of a tile wait for the
+// previous tile's epilogue, which is short).
+//
+// Warp roles: warps 0..4MH-1 epilogue (warp w reads TMEM lane quarter w % 4
+// of half w / 4), warp 4MH TMA producer (per 64-wide K step: MH boxes of
+// 128 state rows and NV / 128 boxes of 128 Wout rows, 128-byte swizzle),
+// warp 4MH+1 TMEM allocator + single-thread MMA issuer.  Two accumulators
+// where 2 x MH x NV columns fit in TMEM, else one.  Persistent: each CTA
+// owns a contiguous range of vocabulary tiles.
+//
+// Per CTA and row the result is one (max, sum-exp) pair and one sorted list
+// of K keys, the same partials as k_head_tc, merged across CTAs by the row
+// merge kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dt {
+namespace {
+
+// MH halves of 128 head rows (MMA M) x NV vocabulary entries (MMA N) per tile.
+template <int MH, int NV>
+struct RowsCfg {
+  static constexpr int kRows = 128 * MH;             // head rows of the tile (padded)
+  static constexpr int kABytes = kRows * kTileH * 2; // states: MH boxes of 128 rows x 128 B
+  static constexpr int kBBytes = NV * kTileH * 2;    // Wout: NV / 128 boxes of 128 rows x 128 B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kAccCols = MH * NV;           // TMEM columns of one accumulator
+  static constexpr int kBufs = 2 * kAccCols <= 512 ? 2 : 1;
+  static constexpr uint32_t kTmemCols = kBufs * kAccCols < 32 ? 32 : kBufs * kAccCols;
+  static constexpr int kEpiWarps = 4 * MH;
+  static constexpr int kProducer = kEpiWarps;
+  static constexpr int kMma = kEpiWarps + 1;
+  static constexpr int kThreads = 32 * (kEpiWarps + 2);
+  static_assert(NV == 128 || NV == 256, "vocabulary tile");
+  static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
+};
+
+constexpr int kRowsMaxStages = 8;
+
+// Each thread of the warp reads 32 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Threshold value of a key bound: values below it cannot beat the key (0,
+// the empty bound, lets every value through).
+__device__ __forceinline__ float bound_value(uint64_t th) {
+  return th == 0ull ? -INFINITY : key_value(th);
+}
+
+// Sorted insert (best first) of `key`, which beats the K-th key, into the
+// list whose slot i is Lr[i * stride]; returns the new K-th key.
+__device__ __noinline__ uint64_t list_insert_row(uint64_t* Lr, int stride, int K, uint64_t key) {
+  int pos = K - 1;
+  while (pos > 0) {
+    const uint64_t prev = Lr[(pos - 1) * stride];
+    if (prev >= key) break;
+    Lr[pos * stride] = prev;
+    --pos;
+  }
+  Lr[pos * stride] = key;
+  return Lr[(K - 1) * stride];
+}
+
+// This CTA's best key of a row improved: raise its group's maximum (group =
+// CTA % K), then the row's bound gth to the least of the K group maxima (K
+// distinct keys at or above it; the new value stands in for this CTA's
+// group).  One thread.
+__device__ __noinline__ void publish_group_best(unsigned long long* gth, unsigned long long* gm,
+                                                int K, uint64_t best) {
+  const int mine = blockIdx.x % K;
+  atomicMax(gm + mine, best);
+  uint64_t mn = ~0ull;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (i < K) {
+      uint64_t v = __ldcg(gm + i);
+      if (i == mine) v = v > best ? v : best;
+      mn = v < mn ? v : mn;
+    }
+  }
+  if (mn != ~0ull && mn > 0ull) atomicMax(gth, mn);
+}
+
+template <int MH, int NV>
+__global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
+    k_head_rows(const __grid_constant__ CUtensorMap tmap_w,
+                const __grid_constant__ CUtensorMap tmap_s, const TcParams p) {
+  using C = RowsCfg<MH, NV>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  uint8_t* stage_base = smem;  // stage: [states kABytes][Wout kBBytes]
+  // top-K lists, slot-major: slot i of row r at lists[i * kRows + r]
+  uint64_t* lists = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * C::kStageBytes);
+  uint64_t* bars = lists + static_cast<size_t>(p.K) * C::kRows;
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles = (p.rows + NV - 1) / NV;
+  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * n_tiles) / gridDim.x);
+  const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * n_tiles) / gridDim.x);
+  const int nk = p.H / kTileH;
+  // each tile starts its contraction at a tile-dependent K step (spreads the
+  // concurrent CTAs' reads over DRAM channels)
+  auto kb_at = [&](int t, int i) {
+    int j = i + (t * 5) % nk;
+    if (j >= nk) j -= nk;
+    return j;
+  };
+
+  if (warp == C::kMma) tmem_alloc<C::kTmemCols>(tmem_slot);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], C::kEpiWarps);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kProducer && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_s);
+  }
+  if (warp < C::kEpiWarps)
+    for (int i = threadIdx.x; i < p.K * C::kRows; i += 32 * C::kEpiWarps) lists[i] = 0ull;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the states, z and the bounds come from earlier kernels
+  pdl_trigger();
+
+  if (warp == C::kProducer) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_s = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
+        for (int i = 0; i < nk; ++i) {
+          const int kb = kb_at(t, i);
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.wait_limit)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* dst = stage_base + static_cast<size_t>(stage) * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+#pragma unroll
+          for (int h = 0; h < MH; ++h)
+            tma_load_2d(dst + h * (128 * 128), &tmap_s, &full[stage], kb * kTileH, h * 128, pol_s);
+#pragma unroll
+          for (int j = 0; j < NV / 128; ++j)
+            tma_load_2d(dst + C::kABytes + j * (128 * 128), &tmap_w, &full[stage], kb * kTileH,
+                        t * NV + j * 128, pol_w);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: every issued copy must have landed before the CTA may exit
+      const long long first = issued > S ? issued - S : 0;
+      for (long long n = first; n < issued; ++n) {
+        const int s = static_cast<int>(n % S);
+        if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), p.err)) break;
+      }
+    }
+  } else if (warp == C::kMma) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_m128<NV>();  // M 128 rows, N NV entries
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
+        const int a = C::kBufs == 2 ? (it & 1) : 0;
+        const uint32_t par = static_cast<uint32_t>(C::kBufs == 2 ? (it >> 1) : it) & 1u;
+        if (!mbar_wait(&tempty[a], par ^ 1u, p.err, p.wait_limit)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(a * C::kAccCols);
+        bool ok = true;
+        for (int i = 0; i < nk; ++i) {
+          if (!mbar_wait(&full[stage], phase, p.err, p.wait_limit)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_base + static_cast<size_t>(stage) * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+          for (int h = 0; h < MH; ++h) {
+#pragma unroll
+            for (int k = 0; k < kTileH / 16; ++k)
+              tc_mma_bf16(d0 + static_cast<uint32_t>(h * NV),
+                          smem_desc_sw128(a_addr + h * (128 * 128) + k * 32),
+                          smem_desc_sw128(b_addr + k * 32), idesc, (i != 0 || k != 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[a]);
+      }
+      // all issued MMAs complete before TMEM is released
+      tc_commit(done);
+      mbar_wait(done, 0, p.err);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    // thread = head row; its running (max, sum-exp) and K-th key in registers
+    const int h = warp >> 2, wq = warp & 3;
+    const int row = h * 128 + wq * 32 + lane;
+    const bool live = row < p.M;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int req = live ? row / p.rows_per_req : 0;
+    const float* zrow = p.z + static_cast<long long>(req) * p.z_req_stride;
+    const bool z_vec = (p.z_req_stride & 3) == 0 && (reinterpret_cast<uintptr_t>(p.z) & 15) == 0;
+    uint64_t* Lr = lists + row;  // slot i at Lr[i * kRows]
+    const int K = p.K, V = p.rows;
+    float m = -INFINITY, s = 0.f;
+    uint64_t kth = 0ull;  // the list's K-th key (0 until it holds K keys)
+    uint64_t best_pub = 0ull;  // this row's best key as last published
+    bool bad = false;
+    int it = 0;
+    for (int t = t_begin; t < t_end; ++t, ++it) {
+      const int a = C::kBufs == 2 ? (it & 1) : 0;
+      const uint32_t par = static_cast<uint32_t>(C::kBufs == 2 ? (it >> 1) : it) & 1u;
+      // the row's global bound, read before the wait
+      uint64_t gb = 0ull;
+      if (p.gth && live) gb = __ldcg(p.gth + row);
+      int okl = 0;
+      if (lane == 0)
+        okl = (!*abort_flag &&
+               mbar_wait(&tfull[a], par, p.err, p.wait_limit))
+                  ? 1
+                  : 0;
+      if (__shfl_sync(kFullMask, okl, 0) == 0) {  // the warp leaves together
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + lane_base + static_cast<uint32_t>(a * C::kAccCols + h * NV);
+      const uint64_t th0 = kth > gb ? kth : gb;
+      uint64_t th = th0;
+      float thv = bound_value(th);
+#pragma unroll 1
+      for (int q = 0; q < NV / 32; ++q) {
+        const int vb = t * NV + q * 32;
+        int nv = V - vb < 32 ? V - vb : 32;  // valid entries of this chunk
+        nv = nv < 0 ? 0 : nv;
+        float zv[32];
+        if (live && z_vec && nv == 32) {
+          const float4* z4 = reinterpret_cast<const float4*>(zrow + vb);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 u = __ldg(z4 + j);
+            zv[4 * j] = u.x;
+            zv[4 * j + 1] = u.y;
+            zv[4 * j + 2] = u.z;
+            zv[4 * j + 3] = u.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) zv[j] = (live && j < nv) ? __ldg(zrow + vb + j) : 0.f;
+        }
+        float x[32];
+        __syncwarp();
+        tmem_ld32(tb + static_cast<uint32_t>(q * 32), x);  // the whole warp, live or not
+        if (!live) continue;
+        // log-sum-exp: the chunk's maximum, then exp(x - m) sums
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[j] += zv[j];
+          if (j < nv) {
+            if (x[j] != x[j] || x[j] == INFINITY) bad = true;
+            if (x[j] > -INFINITY && x[j] < INFINITY) cm = fmaxf(cm, x[j]);
+          }
+        }
+        if (cm > m) {
+          s *= fast_exp(m - cm);  // 0 while m is -inf (s is 0 then too)
+          m = cm;
+        }
+        if (m != -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv && x[j] > -INFINITY && x[j] < INFINITY) s += fast_exp(x[j] - m);
+        }
+        // top-K: a value below the bound's value cannot enter.  While the
+        // list is short the chunk bounds itself: the least of G >= K group
+        // maxima (groups of 32 / G values) has G values at or above it.
+        float cb = -INFINITY;
+        if (kth == 0ull && K <= 16) {
+          float pm[16];  // maxima of the pairs of valid, non-NaN values
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pm[i] = -INFINITY;
+            if (2 * i < nv && x[2 * i] == x[2 * i]) pm[i] = x[2 * i];
+            if (2 * i + 1 < nv && x[2 * i + 1] == x[2 * i + 1]) pm[i] = fmaxf(pm[i], x[2 * i + 1]);
+          }
+          cb = INFINITY;
+          if (K <= 8) {  // 8 groups of 4
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cb = fminf(cb, fmaxf(pm[2 * i], pm[2 * i + 1]));
+          } else {  // 16 groups of 2
+#pragma unroll
+            for (int i = 0; i < 16; ++i) cb = fminf(cb, pm[i]);
+          }
+        }
+        float thv_e = fmaxf(thv, cb);
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) any |= j < nv && x[j] >= thv_e;
+        if (any) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nv && x[j] >= thv_e) {
+              const uint64_t key = make_key(x[j], static_cast<uint32_t>(vb + j));
+              if (key > th) {
+                kth = list_insert_row(Lr, C::kRows, K, key);
+                th = kth > gb ? kth : gb;
+                thv = bound_value(th);
+                thv_e = fmaxf(thv, cb);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      // publish improved bounds: the list's K-th key (once the list is
+      // full) and this CTA's best key for its group
+      if (p.gth && live && kth > th0) atomicMax(p.gth + row, kth);
+      if (p.gth && p.gmx && live) {
+        const uint64_t best = Lr[0];
+        if (best > best_pub) {
+          publish_group_best(p.gth + row, p.gmx + static_cast<size_t>(row) * 32, K, best);
+          best_pub = best;
+        }
+      }
+    }
+    if (live) {
+      const int cta = blockIdx.x;
+      p.pm[static_cast<size_t>(row) * p.cta_stride + cta] = m;
+      p.ps[static_cast<size_t>(row) * p.cta_stride + cta] = s;
+      uint64_t* dst = p.ptop + (static_cast<size_t>(row) * p.list_stride + cta) * K;
+      for (int i = 0; i < K; ++i) dst[i] = Lr[i * C::kRows];
+    }
+    if (bad) atomicOr(p.err, DT_ERR_NONFINITE);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMma) {
+    tc_fence_after();
+    tmem_dealloc<C::kTmemCols>(tmem_base);
+  }
+}
+
+template <int MH, int NV>
+cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int grid,
+                        cudaStream_t st) {
+  using C = RowsCfg<MH, NV>;
+  const size_t fixed = 1024 + static_cast<size_t>(p.K) * C::kRows * 8 + 64 * 8 + 64;
+  const size_t budget = 227 * 1024 - 2048;
+  int stages = budget > fixed ? static_cast<int>((budget - fixed) / C::kStageBytes) : 0;
+  const int cap = p.max_stages > 0 ? p.max_stages : kRowsMaxStages;
+  if (stages > cap) stages = cap;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  TcParams q = p;
+  q.stages = stages;
+  const size_t smem = fixed + static_cast<size_t>(stages) * C::kStageBytes;
+  return launch_kernel(k_head_rows<MH, NV>, dim3(grid), dim3(C::kThreads), smem, st, q.pdl != 0,
+                       tw, ts, q);
+}
+
+}  // namespace
+
+cudaError_t init_head_rows_attrs() {
+  cudaError_t e;
+  if ((e = set_max_dynamic_smem(k_head_rows<1, 128>)) != cudaSuccess) return e;
+  if ((e = set_max_dynamic_smem(k_head_rows<2, 128>)) != cudaSuccess) return e;
+  if ((e = set_max_dynamic_smem(k_head_rows<1, 256>)) != cudaSuccess) return e;
+  return set_max_dynamic_smem(k_head_rows<2, 256>);
+}
+
+cudaError_t launch_head_rows(int M, int nv, const CUtensorMap& tw, const CUtensorMap& ts,
+                             const TcParams& p, int grid, cudaStream_t st) {
+  if (M < 1 || M > kMaxRows || (nv != 128 && nv != 256)) return cudaErrorInvalidValue;
+  if (M <= 128)
+    return nv == 128 ? launch_rows<1, 128>(tw, ts, p, grid, st) : launch_rows<1, 256>(tw, ts, p, grid, st);
+  return nv == 128 ? launch_rows<2, 128>(tw, ts, p, grid, st) : launch_rows<2, 256>(tw, ts, p, grid, st);
+}
+
+}  // namespace dt

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     tma_prefetch_desc(&tmap_s);
   }
   LogitsEpilogue<N, R::kGroups> epi;
-  if (kLogits && warp < R::kEpiWarps) epi.init(epi_smem, p.K, p.M, p.gth);
+  if (kLogits && warp < R::kEpiWarps) epi.init(epi_smem, p.K, p.M, p.gth, p.gmx);
   __shared__ int epi_go[2];  // per-tile decision of each epilogue warpgroup
   tc_fence_before();
   __syncthreads();

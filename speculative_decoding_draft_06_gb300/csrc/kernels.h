@@ -31,6 +31,8 @@ struct TcParams {
   uint64_t* ptop;      // [rows_max][list_stride][K] per-CTA top-K keys
   unsigned long long* gth;  // [rows_max] per-row global bound of the K-th key (zero
                             // between launches)
+  unsigned long long* gmx;  // [rows_max][32] per row, the best key of each CTA group
+                            // (CTA % K); zero between launches
   int cta_stride;
   int list_stride;
   // state epilogue: U = A S_in for the M input rows, then output row q
@@ -81,6 +83,13 @@ inline cudaError_t launch_head_tc(int n_pad, bool logits, const CUtensorMap& tw,
   }
 }
 
+// Logits head call with the head rows on the MMA M side (head_rows.cu):
+// M in [1, 256] rows (one or two 128-row halves), vocabulary tiles of nv
+// (128 or 256) entries; ts is the state map with 128-row boxes.
+cudaError_t init_head_rows_attrs();
+cudaError_t launch_head_rows(int M, int nv, const CUtensorMap& tw, const CUtensorMap& ts,
+                             const TcParams& p, int grid, cudaStream_t st);
+
 inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, int grid,
                                     cudaStream_t st) {
   switch (n_pad) {
@@ -102,6 +111,7 @@ struct MergeParams {
   float2* gls;         // [256][8] per-group (max, sum-exp)
   int* row_cnt;        // [256] group arrival counters, zero between launches
   unsigned long long* gth;  // [256] per-row top-K bounds of the head call (reset here)
+  unsigned long long* gmx;  // [256][32] per-row CTA-group best keys (reset here)
   const float* pm;
   const float* ps;
   const uint64_t* ptop;
@@ -258,6 +268,7 @@ inline cudaError_t init_head_attrs() {
   if ((e = init_head_tc_attrs_64()) != cudaSuccess) return e;
   if ((e = init_head_tc_attrs_128()) != cudaSuccess) return e;
   if ((e = init_head_tc_attrs_256()) != cudaSuccess) return e;
+  if ((e = init_head_rows_attrs()) != cudaSuccess) return e;
   if ((e = init_head_simt_attrs_16()) != cudaSuccess) return e;
   if ((e = init_head_simt_attrs_32()) != cudaSuccess) return e;
   if ((e = init_head_simt_attrs_64()) != cudaSuccess) return e;

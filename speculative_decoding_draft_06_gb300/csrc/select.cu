@@ -155,8 +155,9 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   __threadfence();
   if (threadIdx.x == 0) {
     p.row_cnt[row] = 0;
-    if (p.gth) p.gth[row] = 0ull;  // the head call's bound, ready for the next call
+    if (p.gth) p.gth[row] = 0ull;  // the head call's bounds, ready for the next call
   }
+  if (p.gmx && threadIdx.x < 32) p.gmx[static_cast<size_t>(row) * 32 + threadIdx.x] = 0ull;
   v = warp < p.groups ? __ldcg(p.gpl + (static_cast<size_t>(row) * 8 + warp) * 32 + lane) : 0ull;
   v = block_tree_merge(v, wl, p2);
   if (warp == 0) {

@@ -29,6 +29,8 @@ SMALL = [
     ("bf16-n64", dict(V=1500, H=64, D=3, W=64, K=32, B=100, beta=-0.5, bf16=True)),
     ("bf16-n128", dict(V=1300, H=128, D=3, W=100, K=5, B=128, beta=-0.05, bf16=True)),
     ("bf16-batch", dict(V=1100, H=64, D=4, W=8, K=8, B=40, beta=0.0, bf16=True, R=32)),
+    # z rows of the requests at an odd stride (3 * 1101 floats): unaligned loads
+    ("bf16-batch-odd", dict(V=1101, H=128, D=3, W=8, K=4, B=30, beta=-0.2, bf16=True, R=20)),
     ("bf16-k1w1", dict(V=500, H=64, D=6, W=1, K=1, B=6, beta=0.0, bf16=True)),
     ("bf16-bigB", dict(V=700, H=64, D=3, W=6, K=3, B=200, beta=-1.0, bf16=True, R=2)),
 ]
@@ -69,7 +71,8 @@ def test_two_runs_are_bit_identical():
 
 
 @pytest.mark.parametrize("bf16,M,K", [(True, 5, 8), (True, 16, 16), (True, 40, 4),
-                                      (True, 200, 8), (False, 3, 4), (False, 70, 9)])
+                                      (True, 65, 32), (True, 129, 1), (True, 200, 8),
+                                      (True, 256, 32), (False, 3, 4), (False, 70, 9)])
 def test_head_topk_matches_oracle_rows(bf16, M, K):
     w = I.small_workload(11 + M, V=2600, H=128 if bf16 else 96, D=1, W=1, K=K, B=1, bf16=bf16)
     inp = I.make_inputs(w)
@@ -95,6 +98,33 @@ def test_head_topk_matches_oracle_rows(bf16, M, K):
         lp = out["logp"][m].cpu().numpy()
         ref = (ell[gt].astype(np.float64) - lse).astype(np.float32)
         assert np.max(np.abs(lp - ref)) <= tol
+        assert np.all(np.diff(ell[gt]) <= parity.NEAR_TIE)
+    ctx.close()
+
+
+@pytest.mark.parametrize("nv", [128, 256])
+@pytest.mark.parametrize("M,K", [(130, 8), (256, 3)])
+def test_head_rows_tile_widths_match_oracle(monkeypatch, nv, M, K):
+    """The row-major head kernel with 128- and 256-entry vocabulary tiles
+    (the latter has one accumulator) against the oracle rows."""
+    monkeypatch.setenv("DARTREE_ROWS_NV", str(nv))
+    w = I.small_workload(60 + M + K, V=1900, H=192, D=1, W=1, K=K, B=1, bf16=True)
+    inp = I.make_inputs(w)
+    g = np.random.default_rng(M + nv)
+    S = I.bf16_bits_to_f32(I.to_bf16_bits(np.tanh(g.standard_normal((M, w.H))).astype(np.float32)))
+    z = inp["z"][0, 0]
+    ctx = gu.make_ctx(w, max_K=K)
+    Wd = dtl.weights_to_device(inp, True)["Wout"]
+    Sd = torch.from_numpy(I.to_bf16_bits(S)).view(torch.int16).cuda()
+    out = ctx.head_topk(Sd, torch.from_numpy(z).cuda(), Wd, K=K)
+    ctx.sync()
+    for m in range(M):
+        ell, lse = oracle.logits_row(z, inp["Wout"], S[m], True)
+        tok, _, gap = oracle.topk_row(ell, K)
+        assert abs(out["lse"][m].item() - lse) <= parity.TOL[True]
+        gt = out["tok"][m].cpu().numpy()
+        if gap >= parity.NEAR_TIE:
+            assert set(gt.tolist()) == set(tok.tolist())
         assert np.all(np.diff(ell[gt]) <= parity.NEAR_TIE)
     ctx.close()
 
