@@ -117,19 +117,77 @@ __device__ __noinline__ void publish_group_best(unsigned long long* gth, unsigne
   if (mn != ~0ull && mn > 0ull) atomicMax(gth, mn);
 }
 
-template <int MH, int NV>
+constexpr float kLog2e = 1.4426950408889634f;
+
+// A thread's top-K list of its head row, best first.  KR > 0: in KR
+// registers (K <= KR), the list in the last K slots and slots before it
+// holding ~0 (above every key, so never displaced) -- the K-th key is then
+// always the last slot; KR == 0: K keys in shared memory, slot i at
+// L[i * stride].  Empty slots hold key 0.
+template <int KR>
+struct RowList {
+  uint64_t L[KR];
+  int K;
+  __device__ __forceinline__ void init(uint64_t*, int, int K_) {
+    K = K_;
+#pragma unroll
+    for (int i = 0; i < KR; ++i) L[i] = i < KR - K ? ~0ull : 0ull;
+  }
+  __device__ __forceinline__ uint64_t best() const {
+    uint64_t b = 0ull;
+#pragma unroll
+    for (int i = 0; i < KR; ++i) b = (L[i] != ~0ull && L[i] > b) ? L[i] : b;
+    return b;
+  }
+  // insert a key that beats the K-th; returns the new K-th key
+  __device__ __forceinline__ uint64_t insert(uint64_t key) {
+#pragma unroll
+    for (int i = KR - 1; i > 0; --i) {
+      const uint64_t up = L[i - 1];
+      L[i] = key > up ? up : (key > L[i] ? key : L[i]);
+    }
+    L[0] = key > L[0] ? key : L[0];
+    return L[KR - 1];
+  }
+  __device__ __forceinline__ void store(uint64_t* dst) const {
+#pragma unroll
+    for (int i = 0; i < KR; ++i)
+      if (i >= KR - K) dst[i - (KR - K)] = L[i];
+  }
+};
+
+template <>
+struct RowList<0> {
+  uint64_t* L;
+  int stride, K;
+  __device__ __forceinline__ void init(uint64_t* l, int st, int K_) {
+    L = l;
+    stride = st;
+    K = K_;
+  }
+  __device__ __forceinline__ uint64_t best() const { return L[0]; }
+  __device__ __forceinline__ uint64_t insert(uint64_t key) {
+    return list_insert_row(L, stride, K, key);
+  }
+  __device__ __forceinline__ void store(uint64_t* dst) const {
+    for (int i = 0; i < K; ++i) dst[i] = L[i * stride];
+  }
+};
+
+template <int MH, int NV, int KR>
 __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     k_head_rows(const __grid_constant__ CUtensorMap tmap_w,
                 const __grid_constant__ CUtensorMap tmap_s, const TcParams p) {
   using C = RowsCfg<MH, NV>;
+  static_assert(KR == 0 || KR == 8, "register list capacity");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
   uint8_t* stage_base = smem;  // stage: [states kABytes][Wout kBBytes]
-  // top-K lists, slot-major: slot i of row r at lists[i * kRows + r]
+  // top-K lists (K > 8 only), slot-major: slot i of row r at lists[i * kRows + r]
   uint64_t* lists = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * C::kStageBytes);
-  uint64_t* bars = lists + static_cast<size_t>(p.K) * C::kRows;
+  uint64_t* bars = lists + (KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -170,7 +228,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_s);
   }
-  if (warp < C::kEpiWarps)
+  if (KR == 0 && warp < C::kEpiWarps)
     for (int i = threadIdx.x; i < p.K * C::kRows; i += 32 * C::kEpiWarps) lists[i] = 0ull;
   tc_fence_before();
   __syncthreads();
@@ -266,7 +324,8 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue
-    // thread = head row; its running (max, sum-exp) and K-th key in registers
+    // thread = head row; its running (max, sum-exp), its top-K list (in
+    // registers for K <= KR, else in shared memory) and K-th key
     const int h = warp >> 2, wq = warp & 3;
     const int row = h * 128 + wq * 32 + lane;
     const bool live = row < p.M;
@@ -274,12 +333,33 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     const int req = live ? row / p.rows_per_req : 0;
     const float* zrow = p.z + static_cast<long long>(req) * p.z_req_stride;
     const bool z_vec = (p.z_req_stride & 3) == 0 && (reinterpret_cast<uintptr_t>(p.z) & 15) == 0;
-    uint64_t* Lr = lists + row;  // slot i at Lr[i * kRows]
     const int K = p.K, V = p.rows;
+    RowList<KR> list;
+    list.init(lists + row, C::kRows, K);
     float m = -INFINITY, s = 0.f;
-    uint64_t kth = 0ull;  // the list's K-th key (0 until it holds K keys)
+    uint64_t kth = 0ull;       // the list's K-th key (0 until it holds K keys)
     uint64_t best_pub = 0ull;  // this row's best key as last published
     bool bad = false;
+    // the base logits of one 32-entry chunk (loaded one chunk ahead)
+    auto load_z = [&](int vb, float (&zv)[32]) {
+      const int nv = V - vb < 32 ? V - vb : 32;
+      if (live && z_vec && nv == 32) {
+        const float4* z4 = reinterpret_cast<const float4*>(zrow + vb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 u = __ldg(z4 + j);
+          zv[4 * j] = u.x;
+          zv[4 * j + 1] = u.y;
+          zv[4 * j + 2] = u.z;
+          zv[4 * j + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) zv[j] = (live && j < nv) ? __ldg(zrow + vb + j) : 0.f;
+      }
+    };
+    float zn[32];
+    if (t_begin < t_end) load_z(t_begin * NV, zn);
     int it = 0;
     for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = C::kBufs == 2 ? (it & 1) : 0;
@@ -289,17 +369,13 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
       if (p.gth && live) gb = __ldcg(p.gth + row);
       int okl = 0;
       if (lane == 0)
-        okl = (!*abort_flag &&
-               mbar_wait(&tfull[a], par, p.err, p.wait_limit))
-                  ? 1
-                  : 0;
+        okl = (!*abort_flag && mbar_wait(&tfull[a], par, p.err, p.wait_limit)) ? 1 : 0;
       if (__shfl_sync(kFullMask, okl, 0) == 0) {  // the warp leaves together
         if (lane == 0) *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t tb =
-          tmem_base + lane_base + static_cast<uint32_t>(a * C::kAccCols + h * NV);
+      const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(a * C::kAccCols + h * NV);
       const uint64_t th0 = kth > gb ? kth : gb;
       uint64_t th = th0;
       float thv = bound_value(th);
@@ -308,43 +384,54 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
         const int vb = t * NV + q * 32;
         int nv = V - vb < 32 ? V - vb : 32;  // valid entries of this chunk
         nv = nv < 0 ? 0 : nv;
-        float zv[32];
-        if (live && z_vec && nv == 32) {
-          const float4* z4 = reinterpret_cast<const float4*>(zrow + vb);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 u = __ldg(z4 + j);
-            zv[4 * j] = u.x;
-            zv[4 * j + 1] = u.y;
-            zv[4 * j + 2] = u.z;
-            zv[4 * j + 3] = u.w;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) zv[j] = (live && j < nv) ? __ldg(zrow + vb + j) : 0.f;
-        }
         float x[32];
         __syncwarp();
         tmem_ld32(tb + static_cast<uint32_t>(q * 32), x);  // the whole warp, live or not
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] += zn[j];
+        {  // next chunk's base logits, in flight while this one is processed
+          const int vn = q + 1 < NV / 32 ? vb + 32 : (t + 1) * NV;
+          if (q + 1 < NV / 32 || t + 1 < t_end) load_z(vn, zn);
+        }
         if (!live) continue;
-        // log-sum-exp: the chunk's maximum, then exp(x - m) sums
-        float cm = -INFINITY;
+        // x * 0 is NaN exactly for NaN and +-inf: one probe per value
+        float pr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] += zv[j];
-          if (j < nv) {
-            if (x[j] != x[j] || x[j] == INFINITY) bad = true;
-            if (x[j] > -INFINITY && x[j] < INFINITY) cm = fmaxf(cm, x[j]);
+        for (int j = 0; j < 32; ++j) pr[j & 3] = fmaf(x[j], 0.f, pr[j & 3]);
+        if (nv == 32 && (pr[0] + pr[1]) + (pr[2] + pr[3]) == 0.f) {
+          // all 32 finite: four independent chains for the maximum and sum
+          float c4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+          for (int j = 4; j < 32; ++j) c4[j & 3] = fmaxf(c4[j & 3], x[j]);
+          const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+          if (cm > m) {
+            s *= fast_exp(m - cm);  // 0 while m is -inf (s is 0 then too)
+            m = cm;
           }
-        }
-        if (cm > m) {
-          s *= fast_exp(m - cm);  // 0 while m is -inf (s is 0 then too)
-          m = cm;
-        }
-        if (m != -INFINITY) {
+          const float ml = m * kLog2e;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nv && x[j] > -INFINITY && x[j] < INFINITY) s += fast_exp(x[j] - m);
+          for (int j = 0; j < 32; ++j) s4[j & 3] += exp2f(fmaf(x[j], kLog2e, -ml));
+          s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        } else {
+          // a tail chunk or a non-finite value: per-value checks
+          float cm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nv) {
+              if (x[j] != x[j] || x[j] == INFINITY) bad = true;
+              if (x[j] > -INFINITY && x[j] < INFINITY) cm = fmaxf(cm, x[j]);
+            }
+          }
+          if (cm > m) {
+            s *= fast_exp(m - cm);
+            m = cm;
+          }
+          if (m != -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nv && x[j] > -INFINITY && x[j] < INFINITY) s += fast_exp(x[j] - m);
+          }
         }
         // top-K: a value below the bound's value cannot enter.  While the
         // list is short the chunk bounds itself: the least of G >= K group
@@ -367,24 +454,23 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
             for (int i = 0; i < 16; ++i) cb = fminf(cb, pm[i]);
           }
         }
-        float thv_e = fmaxf(thv, cb);
-        bool any = false;
+        const float thv_e = fmaxf(thv, cb);
+        uint32_t cand = 0u;  // the chunk's candidates, one bit per entry
 #pragma unroll
-        for (int j = 0; j < 32; ++j) any |= j < nv && x[j] >= thv_e;
-        if (any) {
+        for (int j = 0; j < 32; ++j) cand |= (j < nv && x[j] >= thv_e) ? 1u << j : 0u;
+        while (cand) {  // rare: one insertion site, the value picked by index
+          const int j = __ffs(cand) - 1;
+          cand &= cand - 1u;
+          float xj = x[0];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j < nv && x[j] >= thv_e) {
-              const uint64_t key = make_key(x[j], static_cast<uint32_t>(vb + j));
-              if (key > th) {
-                kth = list_insert_row(Lr, C::kRows, K, key);
-                th = kth > gb ? kth : gb;
-                thv = bound_value(th);
-                thv_e = fmaxf(thv, cb);
-              }
-            }
+          for (int i = 1; i < 32; ++i) xj = j == i ? x[i] : xj;
+          const uint64_t key = make_key(xj, static_cast<uint32_t>(vb + j));
+          if (key > th) {  // exact test against the bound as it stands now
+            kth = list.insert(key);
+            th = kth > gb ? kth : gb;
           }
         }
+        thv = bound_value(th);
       }
       tc_fence_before();
       __syncwarp();
@@ -393,7 +479,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
       // full) and this CTA's best key for its group
       if (p.gth && live && kth > th0) atomicMax(p.gth + row, kth);
       if (p.gth && p.gmx && live) {
-        const uint64_t best = Lr[0];
+        const uint64_t best = list.best();
         if (best > best_pub) {
           publish_group_best(p.gth + row, p.gmx + static_cast<size_t>(row) * 32, K, best);
           best_pub = best;
@@ -404,8 +490,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
       const int cta = blockIdx.x;
       p.pm[static_cast<size_t>(row) * p.cta_stride + cta] = m;
       p.ps[static_cast<size_t>(row) * p.cta_stride + cta] = s;
-      uint64_t* dst = p.ptop + (static_cast<size_t>(row) * p.list_stride + cta) * K;
-      for (int i = 0; i < K; ++i) dst[i] = Lr[i * C::kRows];
+      list.store(p.ptop + (static_cast<size_t>(row) * p.list_stride + cta) * K);
     }
     if (bad) atomicOr(p.err, DT_ERR_NONFINITE);
   }
@@ -418,11 +503,12 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
   }
 }
 
-template <int MH, int NV>
+template <int MH, int NV, int KR>
 cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int grid,
                         cudaStream_t st) {
   using C = RowsCfg<MH, NV>;
-  const size_t fixed = 1024 + static_cast<size_t>(p.K) * C::kRows * 8 + 64 * 8 + 64;
+  const size_t lists = KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows * 8;
+  const size_t fixed = 1024 + lists + 64 * 8 + 64;
   const size_t budget = 227 * 1024 - 2048;
   int stages = budget > fixed ? static_cast<int>((budget - fixed) / C::kStageBytes) : 0;
   const int cap = p.max_stages > 0 ? p.max_stages : kRowsMaxStages;
@@ -431,26 +517,41 @@ cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcPa
   TcParams q = p;
   q.stages = stages;
   const size_t smem = fixed + static_cast<size_t>(stages) * C::kStageBytes;
-  return launch_kernel(k_head_rows<MH, NV>, dim3(grid), dim3(C::kThreads), smem, st, q.pdl != 0,
-                       tw, ts, q);
+  return launch_kernel(k_head_rows<MH, NV, KR>, dim3(grid), dim3(C::kThreads), smem, st,
+                       q.pdl != 0, tw, ts, q);
+}
+
+template <int MH, int NV>
+cudaError_t launch_rows_k(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int grid,
+                          cudaStream_t st) {
+  return p.K <= 8 ? launch_rows<MH, NV, 8>(tw, ts, p, grid, st)
+                  : launch_rows<MH, NV, 0>(tw, ts, p, grid, st);
+}
+
+template <int MH, int NV>
+cudaError_t set_rows_attrs() {
+  cudaError_t e = set_max_dynamic_smem(k_head_rows<MH, NV, 8>);
+  return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_rows<MH, NV, 0>);
 }
 
 }  // namespace
 
 cudaError_t init_head_rows_attrs() {
   cudaError_t e;
-  if ((e = set_max_dynamic_smem(k_head_rows<1, 128>)) != cudaSuccess) return e;
-  if ((e = set_max_dynamic_smem(k_head_rows<2, 128>)) != cudaSuccess) return e;
-  if ((e = set_max_dynamic_smem(k_head_rows<1, 256>)) != cudaSuccess) return e;
-  return set_max_dynamic_smem(k_head_rows<2, 256>);
+  if ((e = set_rows_attrs<1, 128>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<2, 128>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<1, 256>()) != cudaSuccess) return e;
+  return set_rows_attrs<2, 256>();
 }
 
 cudaError_t launch_head_rows(int M, int nv, const CUtensorMap& tw, const CUtensorMap& ts,
                              const TcParams& p, int grid, cudaStream_t st) {
   if (M < 1 || M > kMaxRows || (nv != 128 && nv != 256)) return cudaErrorInvalidValue;
   if (M <= 128)
-    return nv == 128 ? launch_rows<1, 128>(tw, ts, p, grid, st) : launch_rows<1, 256>(tw, ts, p, grid, st);
-  return nv == 128 ? launch_rows<2, 128>(tw, ts, p, grid, st) : launch_rows<2, 256>(tw, ts, p, grid, st);
+    return nv == 128 ? launch_rows_k<1, 128>(tw, ts, p, grid, st)
+                     : launch_rows_k<1, 256>(tw, ts, p, grid, st);
+  return nv == 128 ? launch_rows_k<2, 128>(tw, ts, p, grid, st)
+                   : launch_rows_k<2, 256>(tw, ts, p, grid, st);
 }
 
 }  // namespace dt
