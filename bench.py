@@ -115,12 +115,16 @@ def kernel_bytes_per_launch(w: I.Workload, variant: str, kind: str) -> float | N
     return None
 
 
-def kernels_per_build(w: I.Workload, variant: str = "dartree") -> int:
+def kernels_per_build(w: I.Workload, variant: str = "dartree", sms: int = 152) -> int:
     opt = VARIANTS[variant]
+    # a bf16 state step splits its contraction over the SMs and then runs a
+    # finish kernel; the Markov head's step is one kernel
+    tiles = -(-w.H // 128)
+    state = 2 if (w.bf16 and opt.get("head") != "markov" and sms // tiles > 1) else 1
     if opt.get("expansion") == "bestfirst":      # root, init, B x (head, merge, step), states
-        return 2 + 3 * w.B + (w.B - 1)
+        return 2 + 3 * w.B + (w.B - 1) * state
     base = 1 if opt.get("candidates") == "base" else 0
-    return 1 + base + w.D * 2 + (w.D - 1) + 1  # root, head + merge/select, states, prune
+    return 1 + base + w.D * 2 + (w.D - 1) * state + 1  # root, head + merge/select, states, prune
 
 
 def kernel_source_hash() -> str:

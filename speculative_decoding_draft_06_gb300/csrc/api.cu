@@ -69,7 +69,6 @@ struct dartree_ctx {
   unsigned long long* gth = nullptr;  // [256] per-row top-K bound of a head call, then
                                       // [256][32] per-row CTA-group best keys
   float* part = nullptr;            // split-K partial sums of the state step
-  int* tile_cnt = nullptr;          // split-K arrival counters
   int state_split = 1;
   int tc_max_stages = 0;   // tuning: pipeline depth cap of the head call (0: default)
   bool pdl = true;         // programmatic dependent launch between the kernels of a build
@@ -359,10 +358,26 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
     p.S_out_bf16 = static_cast<uint16_t*>(c->S(src + 1));
     p.n_split = c->state_split;
     p.part = c->part;
-    p.tile_cnt = c->tile_cnt;
     p.early_operands = early && c->pdl;
     e = dt::launch_head_tc(N, false, c->tm_A, c->tmS(src, N), p,
                            p.n_tiles * p.n_split, st);
+    if (e == cudaSuccess && p.n_split > 1) {
+      dt::StateFinishParams f{};
+      f.pdl = c->pdl;
+      f.H = H;
+      f.M_in = M_in;
+      f.M_out = M_out;
+      f.n_out = pad_rows(M_out);
+      f.n_split = p.n_split;
+      f.V_tok = c->cfg.V;
+      f.part = c->part;
+      f.slot = slot;
+      f.tok = tok;
+      f.E = p.E_bf16;
+      f.S_out = p.S_out_bf16;
+      f.err = c->d_err;
+      e = dt::launch_state_finish(f, st);
+    }
   } else {
     p.E_f32 = static_cast<const float*>(E);
     p.S_out_f32 = static_cast<float*>(c->S(src + 1));
@@ -800,7 +815,7 @@ void free_all(dartree_ctx* c) {
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   c->gexec = nullptr;
   void* ptrs[] = {c->S_all,     c->score[0],    c->score[1],   c->tok_next,
-                  c->slot_next, c->iota,       c->counters,    c->part,       c->tile_cnt,
+                  c->slot_next, c->iota,       c->counters,    c->part,
                   c->row_cnt,   c->gpl,        c->gls,         c->gth,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
@@ -905,7 +920,6 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
             alloc(&c->iota, rows) == cudaSuccess && alloc(&c->counters, rows) == cudaSuccess &&
             alloc(&c->part, static_cast<size_t>(h_tiles) * c->state_split * rows * dt::kTileV) ==
                 cudaSuccess &&
-            alloc(&c->tile_cnt, static_cast<size_t>(h_tiles)) == cudaSuccess &&
             alloc(&c->row_cnt, rows) == cudaSuccess && alloc(&c->gpl, rows * 8 * 32) == cudaSuccess &&
             alloc(&c->gls, rows * 8) == cudaSuccess && alloc(&c->gth, rows * 33) == cudaSuccess &&
             alloc(&c->pm, rows * c->max_cta) == cudaSuccess &&
@@ -948,7 +962,6 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->row_cnt, 0, rows * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->gth, 0, rows * 33 * sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaMemset(c->tile_cnt, 0, h_tiles * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->base_cnt, 0, RD * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->bf_tok_next, 0, Rc * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->bf_zrow, 0, Rc * sizeof(int32_t));
@@ -1024,9 +1037,6 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
     if (e == cudaSuccess) e = cudaMemset(ctx->row_cnt, 0, dt::kMaxRows * sizeof(int));
     if (e == cudaSuccess)
       e = cudaMemset(ctx->gth, 0, dt::kMaxRows * 33 * sizeof(unsigned long long));
-    if (e == cudaSuccess)
-      e = cudaMemset(ctx->tile_cnt, 0,
-                     sizeof(int) * ((ctx->cfg.H + dt::kTileV - 1) / dt::kTileV));
     if (e == cudaSuccess)
       e = cudaMemset(ctx->base_cnt, 0,
                      sizeof(int) * static_cast<size_t>(ctx->cfg.max_requests) * ctx->cfg.max_D);

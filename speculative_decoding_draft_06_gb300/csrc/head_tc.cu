@@ -54,98 +54,78 @@ struct TcRoles {
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
 };
 
-// Finish 8 output rows q0..q0+7 of hidden unit `row`: u[j] holds U at the
-// row's parent column; adds E[tok], tanh, rounds to bf16 (zeros past M_out).
-// The token and embedding loads of all 8 rows are issued before any use.
-__device__ __forceinline__ void state_store8(const TcParams& p, int q0, int row,
-                                             const float (&u)[8]) {
-  int tok[8];
-  float e[8];
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    tok[j] = q0 + j < p.M_out ? __ldg(p.tok + q0 + j) : 0;
-    if (tok[j] < 0 || tok[j] >= p.V_tok) {  // only after an upstream failure
-      bad = true;
-      tok[j] = 0;
-    }
-  }
-  if (bad) atomicOr(p.err, DT_ERR_BAD_INDEX);
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    e[j] = bf16_bits_to_float(__ldg(p.E_bf16 + static_cast<size_t>(tok[j]) * p.H + row));
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float out = q0 + j < p.M_out ? tanhf(u[j] + e[j]) : 0.f;
-    p.S_out_bf16[static_cast<size_t>(q0 + j) * p.H + row] = float_to_bf16_bits(out);
-  }
-}
-
 // State step epilogue (all 128 epilogue threads; thread = hidden unit `row`).
-// Output row q takes column slot[q] of U = A S_in (its parent's row).
+// Unsplit: output row q takes column slot[q] of U = A S_in (its parent's
+// row), adds E[tok[q]], tanh, rounds to bf16 (zeros past M_out); the rows'
+// slots and tokens are staged in shared memory, and each batch of 16 rows
+// issues its embedding loads together.  Split-K: this CTA's partial U for
+// every input row goes to part[split][c][hidden]; k_state_finish sums the
+// splits and finishes the rows.
 template <int N>
 __device__ __forceinline__ void state_epilogue(const TcParams& p, uint32_t tbase, int tile,
                                                int split, int warp, int lane, int row,
                                                bool valid) {
-  const int n_out = pad_rows(p.M_out);
-  if (p.n_split == 1) {
-    for (int q0 = 0; q0 < n_out; q0 += 8) {
-      float u[8];
+  const int lr = warp * 32 + lane;
+  if (p.n_split > 1) {
+    float* mine = p.part + static_cast<size_t>(split) * kMaxRows * p.H + row;
+    for (int c0 = 0; c0 < p.M; c0 += 16) {
+      float x[16];
+      tmem_ld16(tbase + c0, x);
+      if (valid) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int q = q0 + j;
-        int col = q < p.M_out ? __ldg(p.slot + q) : 0;   // same for the whole warp
-        if (col < 0 || col >= p.M) col = 0;               // (never, unless upstream failed)
-        uint32_t r;
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                     : "=r"(r)
-                     : "r"(tbase + static_cast<uint32_t>(col)));
-        u[j] = __uint_as_float(r);
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < p.M) mine[static_cast<size_t>(c0 + j) * p.H] = x[j];
       }
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      if (valid) state_store8(p, q0, row, u);
     }
     return;
   }
-  // split-K: publish this CTA's partial tile; the last CTA of the tile sums
-  // the partials in split order (deterministic) and finishes the rows
-  const int lr = warp * 32 + lane;
-  float* mine = p.part + (static_cast<size_t>(tile) * p.n_split + split) * kMaxRows * kTileV;
-  for (int c0 = 0; c0 < p.M; c0 += 16) {
-    float x[16];
-    tmem_ld16(tbase + c0, x);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (c0 + j < p.M) mine[static_cast<size_t>(c0 + j) * kTileV + lr] = x[j];
-  }
-  __threadfence();
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-  __shared__ int last;
-  if (lr == 0) last = (atomicAdd(p.tile_cnt + tile, 1) == p.n_split - 1);
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-  if (!last) return;
-  __threadfence();
-  const float* all = p.part + static_cast<size_t>(tile) * p.n_split * kMaxRows * kTileV;
-  for (int q0 = 0; q0 < n_out; q0 += 8) {
-    int col[8];
-    float u[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      col[j] = q0 + j < p.M_out ? __ldg(p.slot + q0 + j) : 0;
-      if (col[j] < 0 || col[j] >= p.M) col[j] = 0;
-      u[j] = 0.f;
+  constexpr int kB = 16;  // output rows per batch
+  __shared__ int s_col[kMaxRows], s_tok[kMaxRows];
+  const int n_out = pad_rows(p.M_out);
+  bool bad = false;
+  for (int q = lr; q < n_out; q += 128) {
+    int col = q < p.M_out ? __ldg(p.slot + q) : 0;
+    int tok = q < p.M_out ? __ldg(p.tok + q) : 0;
+    if (col < 0 || col >= p.M) col = 0;  // (never, unless upstream failed)
+    if (tok < 0 || tok >= p.V_tok) {     // only after an upstream failure
+      bad = true;
+      tok = 0;
     }
-    for (int sp = 0; sp < p.n_split; ++sp) {   // fixed order over the splits
-      float part[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        part[j] = __ldcg(all + (static_cast<size_t>(sp) * kMaxRows + col[j]) * kTileV + lr);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) u[j] += part[j];
-    }
-    if (valid) state_store8(p, q0, row, u);
+    s_col[q] = col;
+    s_tok[q] = tok;
   }
-  if (lr == 0) p.tile_cnt[tile] = 0;
+  if (bad) atomicOr(p.err, DT_ERR_BAD_INDEX);
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  for (int q0 = 0; q0 < n_out; q0 += kB) {
+    float u[kB], e[kB];
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int q = q0 + j < n_out ? q0 + j : 0;
+        e[j] = bf16_bits_to_float(__ldg(p.E_bf16 + static_cast<size_t>(s_tok[q]) * p.H + row));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int q = q0 + j < n_out ? q0 + j : 0;
+      uint32_t r;
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                   : "=r"(r)
+                   : "r"(tbase + static_cast<uint32_t>(s_col[q])));
+      u[j] = __uint_as_float(r);
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int q = q0 + j;
+        if (q < n_out) {
+          const float out = q < p.M_out ? tanhf(u[j] + e[j]) : 0.f;
+          p.S_out_bf16[static_cast<size_t>(q) * p.H + row] = float_to_bf16_bits(out);
+        }
+      }
+    }
+  }
 }
 
 template <int N, bool kLogits>
@@ -419,9 +399,9 @@ static cudaError_t launch_tc_n(const CUtensorMap& tw, const CUtensorMap& ts, con
   using R = TcRoles<N, kLogits>;
   size_t fixed = 1024 + (kLogits ? epi_smem_bytes(N, p.K, R::kGroups) : 0) + 64 * 8 + 64;
   // per-SM shared memory is 228 KB, 1 KB of it reserved per resident CTA,
-  // less the kernel's own static shared memory (at most 2 KB)
+  // less the kernel's own static shared memory (at most 4 KB)
   auto stages_for = [&](int cps) -> int {
-    const size_t budget = (cps == 1 ? 227 * 1024 : 228 * 1024 / cps - 1024) - 2048;
+    const size_t budget = (cps == 1 ? 227 * 1024 : 228 * 1024 / cps - 1024) - 4096;
     return budget > fixed ? static_cast<int>((budget - fixed) / L::kStageBytes) : 0;
   };
   // two CTAs per SM only where both fit with a real pipeline, else one

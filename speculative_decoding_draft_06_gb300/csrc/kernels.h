@@ -49,8 +49,8 @@ struct TcParams {
   int early_operands;        // the weights and S_in were complete before the previous
                              // kernel started: stream them before waiting for it
                              // (only slot / tok / scratch come from that kernel)
-  float* part;               // [tiles * n_split][256][128] fp32 partial sums
-  int* tile_cnt;             // [tiles] arrival counters, zero between launches
+  float* part;               // [n_split][256][H] fp32 partial sums of U = A S_in
+                             // (split-K; finished by k_state_finish)
   // SIMT operands (fp32 path)
   const float* W_f32;        // [rows][H]
   const float* S_f32;        // [rows_max][H]
@@ -101,6 +101,20 @@ inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, i
     default: return cudaErrorInvalidValue;
   }
 }
+
+// Finish of a split-K state step: output row q (q < n_out, zeros from
+// M_out on) is q(tanh(sum_s part[s][slot[q]][:] + E[tok[q]][:])).
+struct StateFinishParams {
+  int pdl;             // launch with programmatic dependent launch (host only)
+  int H, M_in, M_out, n_out, n_split, V_tok;
+  const float* part;   // [n_split][256][H]
+  const int32_t* slot; // [M_out] input row (parent) of each output row
+  const int32_t* tok;  // [M_out]
+  const uint16_t* E;   // [V][H] bf16
+  uint16_t* S_out;     // [256][H] bf16
+  int* err;
+};
+cudaError_t launch_state_finish(const StateFinishParams& p, cudaStream_t st);
 
 // Merge of per-CTA partials into per-row lse and top-K (log-probs), and
 // (select != 0) the global top-W of each request with pool append.

@@ -40,15 +40,14 @@ namespace {
 
 constexpr int kNaMaxH = 4096;                  // largest head width
 constexpr int kNaSlots = 64;                   // partial tiles (tile x split) held
-constexpr int kNaTilesMax = kNaMaxH / dt::kTileV;
 
 // Scratch of the context-free state step.  The host-side names below are
 // stand-ins, not device addresses: host code must use the addresses that
 // cudaGetSymbolAddress returns.
+// split-K partials [n_split][256][H]: n_split * H <= kNaSlots * 128
 static __device__ __align__(256) float g_na_part[kNaSlots * dt::kMaxRows * dt::kTileV];  // 8 MiB
 static __device__ __align__(256) uint16_t g_na_in[dt::kMaxRows * kNaMaxH];               // 2 MiB
 static __device__ __align__(256) uint16_t g_na_out[dt::kMaxRows * kNaMaxH];              // 2 MiB
-static __device__ __align__(256) int g_na_cnt[kNaTilesMax];
 static __device__ __align__(256) int32_t g_na_iota[dt::kMaxRows];
 static __device__ __align__(256) int g_na_err;
 
@@ -63,7 +62,6 @@ struct DeviceScratch {
   float* part = nullptr;
   uint16_t* in = nullptr;
   uint16_t* out = nullptr;
-  int* cnt = nullptr;
   int32_t* iota = nullptr;
   int* err = nullptr;
 };
@@ -119,7 +117,6 @@ dartree_status setup(int dev, DeviceScratch** out) {
   if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.part), g_na_part)) != cudaSuccess ||
       (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.in), g_na_in)) != cudaSuccess ||
       (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.out), g_na_out)) != cudaSuccess ||
-      (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.cnt), g_na_cnt)) != cudaSuccess ||
       (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.iota), g_na_iota)) != cudaSuccess ||
       (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_na_err)) != cudaSuccess)
     return na_cuda_fail("cudaGetSymbolAddress", e);
@@ -173,7 +170,6 @@ extern "C" dartree_status dartree_state_step_noalloc(const void* S_par, const in
   const size_t rb = static_cast<size_t>(H) * 2;
   e = cudaMemcpyAsync(d->in, S_par, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && N > M) e = cudaMemsetAsync(d->in + static_cast<size_t>(M) * H, 0, (N - M) * rb, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(d->cnt, 0, sizeof(int) * kNaTilesMax, st);
   if (e != cudaSuccess) return na_cuda_fail("staging", e);
 
   dt::TcParams p{};
@@ -189,9 +185,24 @@ extern "C" dartree_status dartree_state_step_noalloc(const void* S_par, const in
   p.S_out_bf16 = d->out;
   p.n_split = n_split;
   p.part = d->part;
-  p.tile_cnt = d->cnt;
   p.V_tok = 0x7FFFFFFF;  // tokens are the caller's to keep in [0, V)
   e = dt::launch_head_tc(N, false, tm_a, tm_s, p, tiles * n_split, st);
+  if (e == cudaSuccess && n_split > 1) {
+    dt::StateFinishParams f{};
+    f.H = H;
+    f.M_in = M;
+    f.M_out = M;
+    f.n_out = N;
+    f.n_split = n_split;
+    f.V_tok = p.V_tok;
+    f.part = d->part;
+    f.slot = d->iota;
+    f.tok = tok;
+    f.E = p.E_bf16;
+    f.S_out = d->out;
+    f.err = d->err;
+    e = dt::launch_state_finish(f, st);
+  }
   if (e != cudaSuccess) return na_cuda_fail("state step launch", e);
   e = cudaMemcpyAsync(S_out, d->out, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return na_cuda_fail("output copy", e);

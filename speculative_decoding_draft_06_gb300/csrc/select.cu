@@ -315,6 +315,57 @@ cudaError_t launch_root(const RootParams& p, cudaStream_t st) {
   return launch_kernel(k_root, dim3(p.n_pad), dim3(256), 0, st, p.pdl != 0, p);
 }
 
+// ------------------------------------------------------- state finish
+
+// Finish of a split-K state step ("Technische Samenvatting: DARTree",
+// Methodologie 1: the kept branches carry their correction states): block
+// (q, hb) = output row q, hidden units [1024 hb, 1024 hb + 1024), four per
+// thread.  The splits are summed in split order, so the result does not
+// depend on timing.
+__global__ void __launch_bounds__(256) k_state_finish(const StateFinishParams p) {
+  pdl_wait();  // the partials and the selection (slot, tok) come from earlier kernels
+  pdl_trigger();
+  const int q = blockIdx.x;
+  const int h = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (h >= p.H) return;
+  uint16_t* out = p.S_out + static_cast<size_t>(q) * p.H + h;
+  if (q >= p.M_out) {  // padding rows of the next head call
+    *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
+    return;
+  }
+  int col = __ldg(p.slot + q), tok = __ldg(p.tok + q);
+  if (col < 0 || col >= p.M_in) col = 0;  // (never, unless upstream failed)
+  if (tok < 0 || tok >= p.V_tok) {        // only after an upstream failure
+    if (h == 0) atomicOr(p.err, DT_ERR_BAD_INDEX);
+    tok = 0;
+  }
+  const uint2 eb = __ldg(reinterpret_cast<const uint2*>(p.E + static_cast<size_t>(tok) * p.H + h));
+  float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < p.n_split; ++s) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+        p.part + (static_cast<size_t>(s) * kMaxRows + col) * p.H + h));
+    u.x += v.x;
+    u.y += v.y;
+    u.z += v.z;
+    u.w += v.w;
+  }
+  const float o0 = tanhf(u.x + bf16_bits_to_float(static_cast<uint16_t>(eb.x & 0xFFFFu)));
+  const float o1 = tanhf(u.y + bf16_bits_to_float(static_cast<uint16_t>(eb.x >> 16)));
+  const float o2 = tanhf(u.z + bf16_bits_to_float(static_cast<uint16_t>(eb.y & 0xFFFFu)));
+  const float o3 = tanhf(u.w + bf16_bits_to_float(static_cast<uint16_t>(eb.y >> 16)));
+  *reinterpret_cast<uint2*>(out) =
+      make_uint2(static_cast<uint32_t>(float_to_bf16_bits(o0)) |
+                     (static_cast<uint32_t>(float_to_bf16_bits(o1)) << 16),
+                 static_cast<uint32_t>(float_to_bf16_bits(o2)) |
+                     (static_cast<uint32_t>(float_to_bf16_bits(o3)) << 16));
+}
+
+cudaError_t launch_state_finish(const StateFinishParams& p, cudaStream_t st) {
+  if (p.H % 4 != 0) return cudaErrorInvalidValue;
+  const dim3 grid(p.n_out, (p.H + 1023) / 1024);
+  return launch_kernel(k_state_finish, grid, dim3(256), 0, st, p.pdl != 0, p);
+}
+
 cudaError_t init_select_attrs() {
   cudaError_t e = set_max_dynamic_smem(k_merge_rows);
   if (e != cudaSuccess) return e;
