@@ -75,10 +75,75 @@ __device__ void select_frontier_warp(const MergeParams& p, int r, uint64_t (*wl)
   if (warp == 0 && lane < p.Fd) write_frontier(p, r, lane, v);
 }
 
+// Best 64 of two descending 64-key lists, each held by a warp as (element
+// lane, element lane + 32): the larger of A[e] and B[63 - e] for every e
+// (a bitonic sequence holding the best 64), then a bitonic merge -- stride
+// 32 inside the lane, strides 16 .. 1 across lanes.  Result in (a0, a1).
+__device__ __forceinline__ void warp_merge64(uint64_t& a0, uint64_t& a1, uint64_t b0,
+                                             uint64_t b1) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t r0 = shfl_u64(b1, 31 - lane);  // B[63 - lane]
+  const uint64_t r1 = shfl_u64(b0, 31 - lane);  // B[31 - lane]
+  uint64_t c0 = a0 > r0 ? a0 : r0, c1 = a1 > r1 ? a1 : r1;
+  a0 = c0 > c1 ? c0 : c1;
+  a1 = c0 > c1 ? c1 : c0;
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) {
+    const uint64_t o0 = shfl_xor_u64(a0, s), o1 = shfl_xor_u64(a1, s);
+    const bool lo = (lane & s) != 0;
+    a0 = lo ? (a0 < o0 ? a0 : o0) : (a0 > o0 ? a0 : o0);
+    a1 = lo ? (a1 < o1 ? a1 : o1) : (a1 > o1 ? a1 : o1);
+  }
+}
+
+// For 32 < |F_d| <= 64: as select_frontier_warp with 64-key lists (two per
+// lane).  A warp's rows (at most 8: |F_{d-1}| <= 64 over 8 warps) have their
+// loads issued together; the warps' lists then fold by a pairwise tree
+// through shared memory.  All threads of the block call it.
+__device__ void select_frontier_warp64(const MergeParams& p, int r, uint64_t* sl) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kRowsPerWarp = 64 / kMergeWarps;
+  uint64_t cur[kRowsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) {
+    const int i = warp + k * kMergeWarps;
+    cur[k] = 0ull;
+    if (i < p.F && lane < p.K) {
+      const int row = r * p.F + i;
+      const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + lane);
+      const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
+      cur[k] = make_key(c, static_cast<uint32_t>(i * p.K + lane));
+    }
+  }
+  uint64_t v0 = 0ull, v1 = 0ull;
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) warp_merge64(v0, v1, cur[k], 0ull);
+  // pairwise tree over the warps: sl[w][64]
+  sl[warp * 64 + lane] = v0;
+  sl[warp * 64 + 32 + lane] = v1;
+  __syncthreads();
+  for (int stride = 1; stride < kMergeWarps; stride <<= 1) {
+    if ((warp & (2 * stride - 1)) == 0) {
+      warp_merge64(v0, v1, sl[(warp + stride) * 64 + lane], sl[(warp + stride) * 64 + 32 + lane]);
+      sl[warp * 64 + lane] = v0;
+      sl[warp * 64 + 32 + lane] = v1;
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    if (lane < p.Fd) write_frontier(p, r, lane, v0);
+    if (lane + 32 < p.Fd) write_frontier(p, r, lane + 32, v1);
+  }
+}
+
 __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
                                 uint64_t (*wl)[32]) {
   if (p.Fd <= 32) {
     select_frontier_warp(p, r, wl);
+    return;
+  }
+  if (p.Fd <= 64 && p.F <= 64) {
+    select_frontier_warp64(p, r, keys);
     return;
   }
   const int n = p.F * p.K;
@@ -200,10 +265,12 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
 
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st) {
   size_t smem = 0;
-  if (p.select && p.Fd > 32) {
+  if (p.select && (p.Fd > 64 || p.F > 64)) {
     int np2 = 1;
     while (np2 < p.F * p.K) np2 <<= 1;
     smem = static_cast<size_t>(np2) * 8;
+  } else if (p.select && p.Fd > 32) {
+    smem = static_cast<size_t>(kMergeWarps) * 64 * 8;  // the warps' 64-key lists
   }
   return launch_kernel(k_merge_rows, dim3(p.groups, p.M), dim3(kMergeThreads), smem, st,
                        p.pdl != 0, p);

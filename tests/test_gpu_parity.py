@@ -28,6 +28,8 @@ SMALL = [
     ("bf16-n32", dict(V=2049, H=192, D=4, W=32, K=6, B=64, beta=-0.1, bf16=True)),
     ("bf16-n64", dict(V=1500, H=64, D=3, W=64, K=32, B=100, beta=-0.5, bf16=True)),
     ("bf16-n128", dict(V=1300, H=128, D=3, W=100, K=5, B=128, beta=-0.05, bf16=True)),
+    # frontiers of 33..64 (the 64-key warp fold of the top-W), two requests
+    ("bf16-w48", dict(V=900, H=64, D=5, W=48, K=3, B=60, beta=-0.2, bf16=True, R=2)),
     ("bf16-batch", dict(V=1100, H=64, D=4, W=8, K=8, B=40, beta=0.0, bf16=True, R=32)),
     # z rows of the requests at an odd stride (3 * 1101 floats): unaligned loads
     ("bf16-batch-odd", dict(V=1101, H=128, D=3, W=8, K=4, B=30, beta=-0.2, bf16=True, R=20)),
