@@ -316,9 +316,15 @@ dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, i
   mp.err = c->d_err;
   mp.select = sel != nullptr;
   mp.pdl = c->pdl;
-  mp.groups = (grid + 19) / 20;  // about 20 CTA partials per merge block, at most 8
-  if (mp.groups > 8) mp.groups = 8;
-  if (mp.groups < 1) mp.groups = 1;
+  // split each row's CTA partials over group blocks (at most 8, at most 160
+  // partials each: 20 per warp, loaded before any is merged) until about 256
+  // blocks run; the last group block of a row combines the groups
+  int groups = (256 + M - 1) / M;
+  const int min_groups = (grid + 159) / 160;
+  const int max_groups = (grid + 19) / 20;
+  if (groups > max_groups) groups = max_groups;
+  if (groups < min_groups) groups = min_groups;
+  mp.groups = groups < 1 ? 1 : groups > 8 ? 8 : groups;
   mp.gpl = c->gpl;
   mp.gls = c->gls;
   mp.row_cnt = c->row_cnt;

@@ -166,13 +166,13 @@ __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
 // Row merge.  Grid = (groups, M): block (g, c) merges a contiguous share of
 // the per-CTA partials of head row c -- the (max, sum-exp) pairs with fp32
 // log-sum-exp merges, and the sorted top-K lists by warp bitonic merges (each
-// warp folds every 8th list, then a tree across the warps) -- and publishes
-// one partial pair and one list.  The last group block of the row (atomic
-// count) combines the group partials (fp64 sum across groups) into
-//   lse = max + log(sum), top-K = best K keys, logp = fp32(logit - lse).
+// warp folds every 8th list, all of its lists' keys loaded up front, then a
+// tree across the warps).  One group (up to 160 partials) finishes the row
+// itself; with several, each publishes one pair and one list and the last
+// group block of the row (atomic count) combines them.  The row's
+//   lse = max + log(sum) (fp64 sum), top-K = best K keys, logp = fp32(logit - lse).
 // With p.select set, the last row of each request then runs the request's
-// top-W selection.  Short dependency chains in many blocks instead of one
-// long chain per row.
+// top-W selection.
 __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams p) {
   extern __shared__ uint64_t dyn[];
   __shared__ uint64_t wl[kMergeWarps][32];
@@ -186,51 +186,76 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
 
   const int l0 = static_cast<int>(static_cast<long long>(g) * p.n_cta / p.groups);
   const int l1 = static_cast<int>(static_cast<long long>(g + 1) * p.n_cta / p.groups);
-  // ---- this group's log-sum-exp pair (warp 0)
+  // ---- this group's log-sum-exp pair (warp 0; every lane ends with it)
+  float gm = -INFINITY, gs = 0.f;
   if (warp == 0) {
-    float m = -INFINITY, s = 0.f;
     for (int i = l0 + lane; i < l1; i += 32)
-      lse_merge(m, s, p.pm[static_cast<size_t>(row) * p.cta_stride + i],
+      lse_merge(gm, gs, p.pm[static_cast<size_t>(row) * p.cta_stride + i],
                 p.ps[static_cast<size_t>(row) * p.cta_stride + i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-      lse_merge(m, s, m2, s2);
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, gm, o);
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, gs, o);
+      lse_merge(gm, gs, m2, s2);
     }
-    if (lane == 0) p.gls[row * 8 + g] = make_float2(m, s);
   }
-  // ---- this group's top-K
+  // ---- this group's top-K: warp w folds lists l0 + w, l0 + w + 8, ...;
+  // the keys of up to kPre lists are loaded before any of them is merged
+  constexpr int kPre = 20;
   const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;
+  // the list element this lane contributes to a merge (warp_merge_desc layout)
+  const int jl = p2 == 32 ? 31 - lane : 2 * p2 - 1 - lane;
+  const bool takes = p2 == 32 ? jl < K : (lane >= p2 && lane < 2 * p2 && jl < K);
   uint64_t v = 0ull;
-  for (int l = l0 + warp; l < l1; l += kMergeWarps) {
-    uint64_t y;
-    merge_operands(base + static_cast<size_t>(l) * K, K, p2, v, y);
-    v = warp_merge_desc(v, y, p2);
+  for (int lb = l0 + warp; lb < l1; lb += kMergeWarps * kPre) {
+    uint64_t pre[kPre];
+#pragma unroll
+    for (int q = 0; q < kPre; ++q) {
+      const int l = lb + q * kMergeWarps;
+      pre[q] = (l < l1 && takes) ? __ldcg(base + static_cast<size_t>(l) * K + jl) : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < kPre; ++q) {
+      if (lb + q * kMergeWarps >= l1) break;  // the same for the whole warp
+      if (p2 == 32) {
+        v = warp_merge_desc(v, pre[q], 32);
+      } else {
+        v = lane < p2 ? v : pre[q];
+        v = warp_merge_desc(v, 0ull, p2);
+      }
+    }
   }
   v = block_tree_merge(v, wl, p2);
-  if (warp == 0) p.gpl[(static_cast<size_t>(row) * 8 + g) * 32 + lane] = lane < p2 ? v : 0ull;
 
-  // ---- the last group block of the row combines the groups
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last_flag = (atomicAdd(p.row_cnt + row, 1) == p.groups - 1);
-  __syncthreads();
-  if (!last_flag) return;
-  __threadfence();
-  if (threadIdx.x == 0) {
-    p.row_cnt[row] = 0;
-    if (p.gth) p.gth[row] = 0ull;  // the head call's bounds, ready for the next call
+  // ---- several groups: the last group block of the row combines them
+  if (p.groups > 1) {
+    if (warp == 0) {
+      if (lane == 0) p.gls[row * 8 + g] = make_float2(gm, gs);
+      p.gpl[(static_cast<size_t>(row) * 8 + g) * 32 + lane] = lane < p2 ? v : 0ull;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_flag = (atomicAdd(p.row_cnt + row, 1) == p.groups - 1);
+    __syncthreads();
+    if (!last_flag) return;
+    __threadfence();
+    if (threadIdx.x == 0) p.row_cnt[row] = 0;
+    v = warp < p.groups ? __ldcg(p.gpl + (static_cast<size_t>(row) * 8 + warp) * 32 + lane) : 0ull;
+    v = block_tree_merge(v, wl, p2);
   }
+  if (threadIdx.x == 0 && p.gth) p.gth[row] = 0ull;  // the head call's bounds, ready for the next call
   if (p.gmx && threadIdx.x < 32) p.gmx[static_cast<size_t>(row) * 32 + threadIdx.x] = 0ull;
-  v = warp < p.groups ? __ldcg(p.gpl + (static_cast<size_t>(row) * 8 + warp) * 32 + lane) : 0ull;
-  v = block_tree_merge(v, wl, p2);
   if (warp == 0) {
     float m = -INFINITY, s = 0.f;
-    if (lane < p.groups) {
-      const float2 gp = __ldcg(p.gls + row * 8 + lane);
-      m = gp.x;
-      s = gp.y;
+    if (p.groups > 1) {
+      if (lane < p.groups) {
+        const float2 gp = __ldcg(p.gls + row * 8 + lane);
+        m = gp.x;
+        s = gp.y;
+      }
+    } else if (lane == 0) {
+      m = gm;
+      s = gs;
     }
     float mx = m;
 #pragma unroll

@@ -59,6 +59,22 @@ def test_build_matches_oracle_small(idx):
     ctx.close()
 
 
+def test_build_with_two_ctas_per_sm_merges_row_groups(monkeypatch):
+    """Two head-call CTAs per SM: more than 160 CTA partials per row, so the
+    row merge runs in several group blocks and combines them."""
+    monkeypatch.setenv("DARTREE_TC_CTAS_PER_SM", "2")
+    w = I.small_workload(590, V=30000, H=64, D=3, W=6, K=5, B=20, beta=-0.1, bf16=True)
+    inp = I.make_inputs(w)
+    dev = dtl.weights_to_device(inp, w.bf16)
+    ctx = gu.make_ctx(w)
+    res = gu.run_build(ctx, w, dev)
+    pool, rows, tree = gu.split_request(res, w, 0)
+    rep = parity.compare_request(inp, 0, w.D, w.W, w.K, w.B, w.beta, w.bf16, pool, rows, tree,
+                                 gpu_states=gu.request_states(res, w, 0))
+    assert rep["near_ties"] <= 2
+    ctx.close()
+
+
 def test_two_runs_are_bit_identical():
     w = I.small_workload(7, V=2500, H=128, D=4, W=16, K=8, B=40, beta=-0.1, bf16=True, R=2)
     dev = dtl.weights_to_device(I.make_inputs(w), True)
