@@ -92,6 +92,7 @@ struct dartree_ctx {
   int tc_ctas_per_sm = 1;  // tuning: head-call CTAs per SM
   int rows_min = 65;       // head calls with at least this many rows put the rows on the MMA M side
   int rows_nv = 128;       // ... in vocabulary tiles of this many entries (128 or 256)
+  bool rows_pair = true;   // ... and with more than 128 rows on CTA pairs (two-CTA MMA)
   float* pm = nullptr;
   float* ps = nullptr;
   uint64_t* ptop = nullptr;
@@ -273,10 +274,14 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   {
     KernelTimer tk(c, st, 0);
     if (c->bf16 && M >= c->rows_min) {  // head rows on the MMA M side
-      const int tiles = (V + c->rows_nv - 1) / c->rows_nv;
-      grid = tiles < c->num_sms ? tiles : c->num_sms;
+      // more than 128 rows: CTA pairs with the two-CTA MMA (256-entry tiles)
+      const bool pair = M > 128 && c->rows_pair;
+      const int nv = pair ? 256 : c->rows_nv;
+      const int tiles = (V + nv - 1) / nv;
+      int units = pair ? c->num_sms / 2 : c->num_sms;
+      if (units > tiles) units = tiles;
       p.max_stages = c->tc_max_stages;
-      e = dt::launch_head_rows(M, c->rows_nv, c->tm_Wout, c->tmS(sbuf, 128), p, grid, st);
+      e = dt::launch_head_rows(M, nv, pair, c->tm_Wout, c->tmS(sbuf, 128), p, units, st, &grid);
     } else if (c->bf16) {
       const int slots = c->num_sms * c->tc_ctas_per_sm;
       grid = p.n_tiles < slots ? p.n_tiles : slots;
@@ -891,6 +896,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
+  if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
     const int n = atoi(v);
     c->tc_ctas_per_sm = n == 2 ? 2 : 1;

@@ -165,6 +165,28 @@ inline cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
 }
 
+// Launch `k` as clusters of `cl` CTAs along x (grid.x a multiple of cl),
+// with programmatic dependent launch when `pdl`.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel_cluster(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                         cudaStream_t st, bool pdl, int cl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // Opt a kernel into the largest dynamic shared memory it can use: the
 // per-block limit minus its static shared memory.
 template <typename Kern>

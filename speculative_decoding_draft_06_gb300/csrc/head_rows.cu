@@ -39,12 +39,16 @@
 namespace dt {
 namespace {
 
-// MH halves of 128 head rows (MMA M) x NV vocabulary entries (MMA N) per tile.
-template <int MH, int NV>
+// MH halves of 128 head rows (MMA M) x NV vocabulary entries (MMA N) per
+// tile.  kPair: a CTA pair computes one M = 256 x N = NV tile with the
+// two-CTA MMA; each CTA holds 128 of the rows (MH = 1) and NV / 2 of the
+// tile's Wout rows, and its TMEM holds its 128 rows x NV columns.
+template <int MH, int NV, bool kPair = false>
 struct RowsCfg {
-  static constexpr int kRows = 128 * MH;             // head rows of the tile (padded)
+  static constexpr int kRows = 128 * MH;             // head rows of this CTA (padded)
   static constexpr int kABytes = kRows * kTileH * 2; // states: MH boxes of 128 rows x 128 B
-  static constexpr int kBBytes = NV * kTileH * 2;    // Wout: NV / 128 boxes of 128 rows x 128 B
+  static constexpr int kBRows = kPair ? NV / 2 : NV; // Wout rows of the tile in this CTA
+  static constexpr int kBBytes = kBRows * kTileH * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kAccCols = MH * NV;           // TMEM columns of one accumulator
   static constexpr int kBufs = 2 * kAccCols <= 512 ? 2 : 1;
@@ -54,8 +58,103 @@ struct RowsCfg {
   static constexpr int kMma = kEpiWarps + 1;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
   static_assert(NV == 128 || NV == 256, "vocabulary tile");
+  static_assert(!kPair || (MH == 1 && NV == 256), "pair tile");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
+  // instruction descriptor: bf16 x bf16 -> fp32, K-major A and B, N = NV,
+  // M = 128 (one CTA) or 256 (the pair)
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     (static_cast<uint32_t>(NV >> 3) << 17) |
+                                     (static_cast<uint32_t>((kPair ? 256 : 128) >> 4) << 24);
 };
+
+// ----------------------------------------------------- two-CTA (pair) PTX
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Cluster address of the variable at `p` in the CTA of the given rank.
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2-D tiled load into this CTA's shared memory whose bytes complete on an
+// mbarrier of either CTA of the pair (bar: cluster address).  x a multiple
+// of 64 bf16 elements.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+// Arrive on an mbarrier of either CTA of the cluster (cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Once the pair's MMAs issued so far complete, arrive on the mbarrier at
+// `bar`'s offset in the CTAs of `mask` (bit = rank in the pair).
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+template <uint32_t NCOLS>
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)), "r"(NCOLS)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <uint32_t NCOLS>
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(NCOLS)
+               : "memory");
+}
+// Bounded wait with cluster-scope acquire (the barrier receives arrivals
+// from the other CTA of the pair); gives up like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err,
+                                                  long long limit) {
+  const uint32_t a = smem_u32(bar);
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const long long lim = limit > 0 ? limit : kWaitLimitCycles;
+  const long long t0 = clock64();
+  while (!try_wait()) {
+    if (clock64() - t0 > lim) {
+      atomicOr(err, DT_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
 
 constexpr int kRowsMaxStages = 8;
 
@@ -98,12 +197,12 @@ __device__ __noinline__ uint64_t list_insert_row(uint64_t* Lr, int stride, int K
 }
 
 // This CTA's best key of a row improved: raise its group's maximum (group =
-// CTA % K), then the row's bound gth to the least of the K group maxima (K
+// unit % K, unit = the CTA or CTA pair owning a vocabulary range), then the row's bound gth to the least of the K group maxima (K
 // distinct keys at or above it; the new value stands in for this CTA's
 // group).  One thread.
 __device__ __noinline__ void publish_group_best(unsigned long long* gth, unsigned long long* gm,
-                                                int K, uint64_t best) {
-  const int mine = blockIdx.x % K;
+                                                int K, int unit, uint64_t best) {
+  const int mine = unit % K;
   atomicMax(gm + mine, best);
   uint64_t mn = ~0ull;
 #pragma unroll
@@ -174,11 +273,11 @@ struct RowList<0> {
   }
 };
 
-template <int MH, int NV, int KR>
-__global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
+template <int MH, int NV, int KR, bool kPair>
+__global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
     k_head_rows(const __grid_constant__ CUtensorMap tmap_w,
                 const __grid_constant__ CUtensorMap tmap_s, const TcParams p) {
-  using C = RowsCfg<MH, NV>;
+  using C = RowsCfg<MH, NV, kPair>;
   static_assert(KR == 0 || KR == 8, "register list capacity");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -198,9 +297,13 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // unit = the CTA, or the CTA pair (cluster ranks 0 = leader, 1 = peer)
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const int unit = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int n_units = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   const int n_tiles = (p.rows + NV - 1) / NV;
-  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * n_tiles) / gridDim.x);
-  const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * n_tiles) / gridDim.x);
+  const int t_begin = static_cast<int>((static_cast<long long>(unit) * n_tiles) / n_units);
+  const int t_end = static_cast<int>((static_cast<long long>(unit + 1) * n_tiles) / n_units);
   const int nk = p.H / kTileH;
   // each tile starts its contraction at a tile-dependent K step (spreads the
   // concurrent CTAs' reads over DRAM channels)
@@ -210,7 +313,12 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     return j;
   };
 
-  if (warp == C::kMma) tmem_alloc<C::kTmemCols>(tmem_slot);
+  if (warp == C::kMma) {
+    if constexpr (kPair)
+      tmem_alloc_pair<C::kTmemCols>(tmem_slot);  // the same columns in both CTAs
+    else
+      tmem_alloc<C::kTmemCols>(tmem_slot);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -218,7 +326,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], C::kEpiWarps);
+      mbar_init(&tempty[a], kPair ? 2 * C::kEpiWarps : C::kEpiWarps);  // pair: both CTAs' warps
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -232,6 +340,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     for (int i = threadIdx.x; i < p.K * C::kRows; i += 32 * C::kEpiWarps) lists[i] = 0ull;
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers exist before either signals
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the states, z and the bounds come from earlier kernels
@@ -253,14 +362,25 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
             break;
           }
           uint8_t* dst = stage_base + static_cast<size_t>(stage) * C::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          if constexpr (kPair) {
+            // this CTA's 128 state rows and 128 Wout rows; both CTAs' bytes
+            // complete on the leader's barrier, which the leader arms
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+            const uint32_t fb = map_to_rank(&full[stage], 0);
+            tma_load_2d_pair(dst, &tmap_s, fb, kb * kTileH, static_cast<int>(rank) * 128, pol_s);
+            tma_load_2d_pair(dst + C::kABytes, &tmap_w, fb, kb * kTileH,
+                             t * NV + static_cast<int>(rank) * 128, pol_w);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
 #pragma unroll
-          for (int h = 0; h < MH; ++h)
-            tma_load_2d(dst + h * (128 * 128), &tmap_s, &full[stage], kb * kTileH, h * 128, pol_s);
+            for (int h = 0; h < MH; ++h)
+              tma_load_2d(dst + h * (128 * 128), &tmap_s, &full[stage], kb * kTileH, h * 128,
+                          pol_s);
 #pragma unroll
-          for (int j = 0; j < NV / 128; ++j)
-            tma_load_2d(dst + C::kABytes + j * (128 * 128), &tmap_w, &full[stage], kb * kTileH,
-                        t * NV + j * 128, pol_w);
+            for (int j = 0; j < NV / 128; ++j)
+              tma_load_2d(dst + C::kABytes + j * (128 * 128), &tmap_w, &full[stage], kb * kTileH,
+                          t * NV + j * 128, pol_w);
+          }
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -269,23 +389,27 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
         }
       }
       // drain: every issued copy must have landed before the CTA may exit
+      // (pair: the peer's copies complete on the leader's barriers, so the
+      // leader drains both, and the final cluster barrier holds the peer)
       const long long first = issued > S ? issued - S : 0;
-      for (long long n = first; n < issued; ++n) {
+      for (long long n = first; n < issued && rank == 0; ++n) {
         const int s = static_cast<int>(n % S);
         if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), p.err)) break;
       }
     }
   } else if (warp == C::kMma) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_m128<NV>();  // M 128 rows, N NV entries
+    if (lane == 0 && rank == 0) {  // pair: the leader issues for both CTAs
+      constexpr uint32_t idesc = C::kIdesc;
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
         const int a = C::kBufs == 2 ? (it & 1) : 0;
         const uint32_t par = static_cast<uint32_t>(C::kBufs == 2 ? (it >> 1) : it) & 1u;
-        if (!mbar_wait(&tempty[a], par ^ 1u, p.err, p.wait_limit)) {
+        const bool free_acc = kPair ? mbar_wait_cluster(&tempty[a], par ^ 1u, p.err, p.wait_limit)
+                                    : mbar_wait(&tempty[a], par ^ 1u, p.err, p.wait_limit);
+        if (!free_acc) {
           *abort_flag = 1;
           break;
         }
@@ -301,25 +425,39 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_base + static_cast<size_t>(stage) * C::kStageBytes);
           const uint32_t b_addr = a_addr + C::kABytes;
-#pragma unroll
-          for (int h = 0; h < MH; ++h) {
+          if constexpr (kPair) {
 #pragma unroll
             for (int k = 0; k < kTileH / 16; ++k)
-              tc_mma_bf16(d0 + static_cast<uint32_t>(h * NV),
-                          smem_desc_sw128(a_addr + h * (128 * 128) + k * 32),
-                          smem_desc_sw128(b_addr + k * 32), idesc, (i != 0 || k != 0) ? 1u : 0u);
+              tc_mma_bf16_pair(d0, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
+                               idesc, (i != 0 || k != 0) ? 1u : 0u);
+            tc_commit_pair(&empty[stage], 3);  // the stage is free in both CTAs
+          } else {
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {
+#pragma unroll
+              for (int k = 0; k < kTileH / 16; ++k)
+                tc_mma_bf16(d0 + static_cast<uint32_t>(h * NV),
+                            smem_desc_sw128(a_addr + h * (128 * 128) + k * 32),
+                            smem_desc_sw128(b_addr + k * 32), idesc, (i != 0 || k != 0) ? 1u : 0u);
+            }
+            tc_commit(&empty[stage]);
           }
-          tc_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&tfull[a]);
+        if constexpr (kPair)
+          tc_commit_pair(&tfull[a], 3);
+        else
+          tc_commit(&tfull[a]);
       }
       // all issued MMAs complete before TMEM is released
-      tc_commit(done);
+      if constexpr (kPair)
+        tc_commit_pair(done, 1);
+      else
+        tc_commit(done);
       mbar_wait(done, 0, p.err);
     }
   } else {
@@ -327,7 +465,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
     // thread = head row; its running (max, sum-exp), its top-K list (in
     // registers for K <= KR, else in shared memory) and K-th key
     const int h = warp >> 2, wq = warp & 3;
-    const int row = h * 128 + wq * 32 + lane;
+    const int row = static_cast<int>(rank) * 128 + h * 128 + wq * 32 + lane;
     const bool live = row < p.M;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int req = live ? row / p.rows_per_req : 0;
@@ -369,7 +507,10 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
       if (p.gth && live) gb = __ldcg(p.gth + row);
       int okl = 0;
       if (lane == 0)
-        okl = (!*abort_flag && mbar_wait(&tfull[a], par, p.err, p.wait_limit)) ? 1 : 0;
+        okl = (!*abort_flag && (kPair ? mbar_wait_cluster(&tfull[a], par, p.err, p.wait_limit)
+                                      : mbar_wait(&tfull[a], par, p.err, p.wait_limit)))
+                  ? 1
+                  : 0;
       if (__shfl_sync(kFullMask, okl, 0) == 0) {  // the warp leaves together
         if (lane == 0) *abort_flag = 1;
         break;
@@ -474,20 +615,25 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (lane == 0) {
+        if (kPair && rank != 0)
+          mbar_arrive_cluster(map_to_rank(&tempty[a], 0));  // the leader's accumulator barrier
+        else
+          mbar_arrive(&tempty[a]);
+      }
       // publish improved bounds: the list's K-th key (once the list is
       // full) and this CTA's best key for its group
       if (p.gth && live && kth > th0) atomicMax(p.gth + row, kth);
       if (p.gth && p.gmx && live) {
         const uint64_t best = list.best();
         if (best > best_pub) {
-          publish_group_best(p.gth + row, p.gmx + static_cast<size_t>(row) * 32, K, best);
+          publish_group_best(p.gth + row, p.gmx + static_cast<size_t>(row) * 32, K, unit, best);
           best_pub = best;
         }
       }
     }
     if (live) {
-      const int cta = blockIdx.x;
+      const int cta = unit;  // the partial slot of this vocabulary range
       p.pm[static_cast<size_t>(row) * p.cta_stride + cta] = m;
       p.ps[static_cast<size_t>(row) * p.cta_stride + cta] = s;
       list.store(p.ptop + (static_cast<size_t>(row) * p.list_stride + cta) * K);
@@ -497,16 +643,22 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // pair: neither CTA leaves (or frees its TMEM) while the other may still
+  // signal it or the leader's MMAs may still use its memory
+  if constexpr (kPair) cluster_sync_all();
   if (warp == C::kMma) {
     tc_fence_after();
-    tmem_dealloc<C::kTmemCols>(tmem_base);
+    if constexpr (kPair)
+      tmem_dealloc_pair<C::kTmemCols>(tmem_base);
+    else
+      tmem_dealloc<C::kTmemCols>(tmem_base);
   }
 }
 
-template <int MH, int NV, int KR>
-cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int grid,
+template <int MH, int NV, int KR, bool kPair>
+cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int units,
                         cudaStream_t st) {
-  using C = RowsCfg<MH, NV>;
+  using C = RowsCfg<MH, NV, kPair>;
   const size_t lists = KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows * 8;
   const size_t fixed = 1024 + lists + 64 * 8 + 64;
   const size_t budget = 227 * 1024 - 2048;
@@ -517,41 +669,73 @@ cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcPa
   TcParams q = p;
   q.stages = stages;
   const size_t smem = fixed + static_cast<size_t>(stages) * C::kStageBytes;
-  return launch_kernel(k_head_rows<MH, NV, KR>, dim3(grid), dim3(C::kThreads), smem, st,
-                       q.pdl != 0, tw, ts, q);
+  if constexpr (kPair)
+    return launch_kernel_cluster(k_head_rows<MH, NV, KR, kPair>, dim3(2 * units),
+                                 dim3(C::kThreads), smem, st, q.pdl != 0, 2, tw, ts, q);
+  else
+    return launch_kernel(k_head_rows<MH, NV, KR, kPair>, dim3(units), dim3(C::kThreads), smem, st,
+                         q.pdl != 0, tw, ts, q);
 }
 
-template <int MH, int NV>
-cudaError_t launch_rows_k(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int grid,
-                          cudaStream_t st) {
-  return p.K <= 8 ? launch_rows<MH, NV, 8>(tw, ts, p, grid, st)
-                  : launch_rows<MH, NV, 0>(tw, ts, p, grid, st);
+template <int MH, int NV, bool kPair>
+cudaError_t launch_rows_k(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p,
+                          int units, cudaStream_t st) {
+  return p.K <= 8 ? launch_rows<MH, NV, 8, kPair>(tw, ts, p, units, st)
+                  : launch_rows<MH, NV, 0, kPair>(tw, ts, p, units, st);
 }
 
-template <int MH, int NV>
+template <int MH, int NV, bool kPair>
 cudaError_t set_rows_attrs() {
-  cudaError_t e = set_max_dynamic_smem(k_head_rows<MH, NV, 8>);
-  return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_rows<MH, NV, 0>);
+  cudaError_t e = set_max_dynamic_smem(k_head_rows<MH, NV, 8, kPair>);
+  return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_rows<MH, NV, 0, kPair>);
 }
+
+int g_max_pairs = 0;  // CTA pairs of the pair kernel that can be resident together
 
 }  // namespace
 
 cudaError_t init_head_rows_attrs() {
   cudaError_t e;
-  if ((e = set_rows_attrs<1, 128>()) != cudaSuccess) return e;
-  if ((e = set_rows_attrs<2, 128>()) != cudaSuccess) return e;
-  if ((e = set_rows_attrs<1, 256>()) != cudaSuccess) return e;
-  return set_rows_attrs<2, 256>();
+  if ((e = set_rows_attrs<1, 128, false>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<2, 128, false>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<1, 256, false>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<2, 256, false>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<1, 256, true>()) != cudaSuccess) return e;
+  // resident clusters of two at the largest shared-memory footprint
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(RowsCfg<1, 256, true>::kThreads);
+  cfg.dynamicSmemBytes = 227 * 1024 - 2048;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, k_head_rows<1, 256, 0, true>, &cfg);
+  if (e != cudaSuccess) return e;
+  g_max_pairs = n;
+  return cudaSuccess;
 }
 
-cudaError_t launch_head_rows(int M, int nv, const CUtensorMap& tw, const CUtensorMap& ts,
-                             const TcParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_head_rows(int M, int nv, bool pair, const CUtensorMap& tw, const CUtensorMap& ts,
+                             const TcParams& p, int units, cudaStream_t st, int* units_used) {
   if (M < 1 || M > kMaxRows || (nv != 128 && nv != 256)) return cudaErrorInvalidValue;
+  if (pair) {  // 129..256 rows over a CTA pair, 256-entry vocabulary tiles
+    if (M <= 128 || nv != 256) return cudaErrorInvalidValue;
+    if (units > g_max_pairs) units = g_max_pairs;
+    if (units < 1) return cudaErrorInvalidConfiguration;
+    *units_used = units;
+    return launch_rows_k<1, 256, true>(tw, ts, p, units, st);
+  }
+  *units_used = units;
   if (M <= 128)
-    return nv == 128 ? launch_rows_k<1, 128>(tw, ts, p, grid, st)
-                     : launch_rows_k<1, 256>(tw, ts, p, grid, st);
-  return nv == 128 ? launch_rows_k<2, 128>(tw, ts, p, grid, st)
-                   : launch_rows_k<2, 256>(tw, ts, p, grid, st);
+    return nv == 128 ? launch_rows_k<1, 128, false>(tw, ts, p, units, st)
+                     : launch_rows_k<1, 256, false>(tw, ts, p, units, st);
+  return nv == 128 ? launch_rows_k<2, 128, false>(tw, ts, p, units, st)
+                   : launch_rows_k<2, 256, false>(tw, ts, p, units, st);
 }
 
 }  // namespace dt

@@ -85,10 +85,13 @@ inline cudaError_t launch_head_tc(int n_pad, bool logits, const CUtensorMap& tw,
 
 // Logits head call with the head rows on the MMA M side (head_rows.cu):
 // M in [1, 256] rows (one or two 128-row halves), vocabulary tiles of nv
-// (128 or 256) entries; ts is the state map with 128-row boxes.
+// (128 or 256) entries; ts is the state map with 128-row boxes.  pair: M in
+// [129, 256] with the two-CTA MMA over CTA pairs (nv = 256).  `units` CTAs
+// (pairs) requested; units_used receives the count launched (= the number
+// of partial slots per row).
 cudaError_t init_head_rows_attrs();
-cudaError_t launch_head_rows(int M, int nv, const CUtensorMap& tw, const CUtensorMap& ts,
-                             const TcParams& p, int grid, cudaStream_t st);
+cudaError_t launch_head_rows(int M, int nv, bool pair, const CUtensorMap& tw, const CUtensorMap& ts,
+                             const TcParams& p, int units, cudaStream_t st, int* units_used);
 
 inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, int grid,
                                     cudaStream_t st) {

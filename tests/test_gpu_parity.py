@@ -120,15 +120,17 @@ def test_head_topk_matches_oracle_rows(bf16, M, K):
     ctx.close()
 
 
-@pytest.mark.parametrize("nv", [128, 256])
-@pytest.mark.parametrize("M,K", [(130, 8), (256, 3)])
-def test_head_rows_tile_widths_match_oracle(monkeypatch, nv, M, K):
-    """The row-major head kernel with 128- and 256-entry vocabulary tiles
-    (the latter has one accumulator) against the oracle rows."""
-    monkeypatch.setenv("DARTREE_ROWS_NV", str(nv))
+@pytest.mark.parametrize("mode", ["nv128", "nv256", "pair"])
+@pytest.mark.parametrize("M,K", [(130, 8), (256, 3), (200, 16)])
+def test_head_rows_tile_widths_match_oracle(monkeypatch, mode, M, K):
+    """The row-major head kernel -- one CTA with 128- or 256-entry vocabulary
+    tiles (the latter with one accumulator), or CTA pairs with the two-CTA
+    MMA -- against the oracle rows."""
+    monkeypatch.setenv("DARTREE_ROWS_PAIR", "1" if mode == "pair" else "0")
+    monkeypatch.setenv("DARTREE_ROWS_NV", "256" if mode == "nv256" else "128")
     w = I.small_workload(60 + M + K, V=1900, H=192, D=1, W=1, K=K, B=1, bf16=True)
     inp = I.make_inputs(w)
-    g = np.random.default_rng(M + nv)
+    g = np.random.default_rng(M + len(mode))
     S = I.bf16_bits_to_f32(I.to_bf16_bits(np.tanh(g.standard_normal((M, w.H))).astype(np.float32)))
     z = inp["z"][0, 0]
     ctx = gu.make_ctx(w, max_K=K)
