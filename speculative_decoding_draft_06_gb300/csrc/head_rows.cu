@@ -53,7 +53,10 @@ struct RowsCfg {
   static constexpr int kAccCols = MH * NV;           // TMEM columns of one accumulator
   static constexpr int kBufs = 2 * kAccCols <= 512 ? 2 : 1;
   static constexpr uint32_t kTmemCols = kBufs * kAccCols < 32 ? 32 : kBufs * kAccCols;
-  static constexpr int kEpiWarps = 4 * MH;
+  // epilogue warpgroups: one per 128-row half (one CTA), or two per CTA of
+  // a pair, each taking half of every tile's columns
+  static constexpr int kColGroups = kPair ? 2 : 1;
+  static constexpr int kEpiWarps = 4 * MH * kColGroups;
   static constexpr int kProducer = kEpiWarps;
   static constexpr int kMma = kEpiWarps + 1;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
@@ -284,9 +287,10 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
   uint8_t* stage_base = smem;  // stage: [states kABytes][Wout kBBytes]
-  // top-K lists (K > 8 only), slot-major: slot i of row r at lists[i * kRows + r]
+  // top-K lists (K > 8 only), slot-major: slot i of list r at lists[i * kListRows + r]
   uint64_t* lists = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * C::kStageBytes);
-  uint64_t* bars = lists + (KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows);
+  constexpr int kListRows = C::kRows * C::kColGroups;  // lists per CTA: (column group, row)
+  uint64_t* bars = lists + (KR > 0 ? 0 : static_cast<size_t>(p.K) * kListRows);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
     tma_prefetch_desc(&tmap_s);
   }
   if (KR == 0 && warp < C::kEpiWarps)
-    for (int i = threadIdx.x; i < p.K * C::kRows; i += 32 * C::kEpiWarps) lists[i] = 0ull;
+    for (int i = threadIdx.x; i < p.K * kListRows; i += 32 * C::kEpiWarps) lists[i] = 0ull;
   tc_fence_before();
   __syncthreads();
   if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers exist before either signals
@@ -464,7 +468,11 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
     // --------------------------------------------------------- epilogue
     // thread = head row; its running (max, sum-exp), its top-K list (in
     // registers for K <= KR, else in shared memory) and K-th key
-    const int h = warp >> 2, wq = warp & 3;
+    const int gi = warp >> 2, wq = warp & 3;
+    const int h = kPair ? 0 : gi;   // this thread's 128-row half (one CTA)
+    const int cg = kPair ? gi : 0;  // this thread's half of the tile's columns (pair)
+    constexpr int kChunks = NV / 32 / C::kColGroups;  // 32-column chunks per tile and thread
+    const int slot = unit * C::kColGroups + cg;       // the partial slot of this (row, columns)
     const int row = static_cast<int>(rank) * 128 + h * 128 + wq * 32 + lane;
     const bool live = row < p.M;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
     const bool z_vec = (p.z_req_stride & 3) == 0 && (reinterpret_cast<uintptr_t>(p.z) & 15) == 0;
     const int K = p.K, V = p.rows;
     RowList<KR> list;
-    list.init(lists + row, C::kRows, K);
+    list.init(lists + cg * C::kRows + h * 128 + wq * 32 + lane, kListRows, K);
     float m = -INFINITY, s = 0.f;
     uint64_t kth = 0ull;       // the list's K-th key (0 until it holds K keys)
     uint64_t best_pub = 0ull;  // this row's best key as last published
@@ -497,7 +505,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
       }
     };
     float zn[32];
-    if (t_begin < t_end) load_z(t_begin * NV, zn);
+    if (t_begin < t_end) load_z(t_begin * NV + cg * kChunks * 32, zn);
     int it = 0;
     for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = C::kBufs == 2 ? (it & 1) : 0;
@@ -521,18 +529,19 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
       uint64_t th = th0;
       float thv = bound_value(th);
 #pragma unroll 1
-      for (int q = 0; q < NV / 32; ++q) {
-        const int vb = t * NV + q * 32;
+      for (int q = 0; q < kChunks; ++q) {
+        const int qq = cg * kChunks + q;  // chunk within the tile
+        const int vb = t * NV + qq * 32;
         int nv = V - vb < 32 ? V - vb : 32;  // valid entries of this chunk
         nv = nv < 0 ? 0 : nv;
         float x[32];
         __syncwarp();
-        tmem_ld32(tb + static_cast<uint32_t>(q * 32), x);  // the whole warp, live or not
+        tmem_ld32(tb + static_cast<uint32_t>(qq * 32), x);  // the whole warp, live or not
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] += zn[j];
         {  // next chunk's base logits, in flight while this one is processed
-          const int vn = q + 1 < NV / 32 ? vb + 32 : (t + 1) * NV;
-          if (q + 1 < NV / 32 || t + 1 < t_end) load_z(vn, zn);
+          const int vn = q + 1 < kChunks ? vb + 32 : (t + 1) * NV + cg * kChunks * 32;
+          if (q + 1 < kChunks || t + 1 < t_end) load_z(vn, zn);
         }
         if (!live) continue;
         // x * 0 is NaN exactly for NaN and +-inf: one probe per value
@@ -627,13 +636,13 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
       if (p.gth && p.gmx && live) {
         const uint64_t best = list.best();
         if (best > best_pub) {
-          publish_group_best(p.gth + row, p.gmx + static_cast<size_t>(row) * 32, K, unit, best);
+          publish_group_best(p.gth + row, p.gmx + static_cast<size_t>(row) * 32, K, slot, best);
           best_pub = best;
         }
       }
     }
     if (live) {
-      const int cta = unit;  // the partial slot of this vocabulary range
+      const int cta = slot;
       p.pm[static_cast<size_t>(row) * p.cta_stride + cta] = m;
       p.ps[static_cast<size_t>(row) * p.cta_stride + cta] = s;
       list.store(p.ptop + (static_cast<size_t>(row) * p.list_stride + cta) * K);
@@ -659,7 +668,7 @@ template <int MH, int NV, int KR, bool kPair>
 cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int units,
                         cudaStream_t st) {
   using C = RowsCfg<MH, NV, kPair>;
-  const size_t lists = KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows * 8;
+  const size_t lists = KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows * C::kColGroups * 8;
   const size_t fixed = 1024 + lists + 64 * 8 + 64;
   const size_t budget = 227 * 1024 - 2048;
   int stages = budget > fixed ? static_cast<int>((budget - fixed) / C::kStageBytes) : 0;
@@ -727,7 +736,7 @@ cudaError_t launch_head_rows(int M, int nv, bool pair, const CUtensorMap& tw, co
     if (M <= 128 || nv != 256) return cudaErrorInvalidValue;
     if (units > g_max_pairs) units = g_max_pairs;
     if (units < 1) return cudaErrorInvalidConfiguration;
-    *units_used = units;
+    *units_used = 2 * units;  // partial slots: two column halves per pair
     return launch_rows_k<1, 256, true>(tw, ts, p, units, st);
   }
   *units_used = units;
