@@ -26,6 +26,16 @@
 // where 2 x MH x NV columns fit in TMEM, else one.  Persistent: each CTA
 // owns a contiguous range of vocabulary tiles.
 //
+// Pair mode (129..256 rows).  With 256 rows one CTA's shared memory is the
+// bottleneck: per K step its MMAs read both row halves' states and the Wout
+// tile twice.  A cluster of two CTAs instead computes M = 256 x N = 256
+// with the two-CTA MMA: each CTA holds 128 state rows and 128 of the tile's
+// Wout rows, the leader issues the MMAs for both, both CTAs' copies complete
+// on the leader's stage barrier, the MMA commits arrive in both CTAs, and
+// each CTA's TMEM receives its 128 rows x 256 columns.  Each CTA runs two
+// epilogue warpgroups, one per half of the tile's columns (warps 0-3 and
+// 4-7), each a separate partial slot for the row merge.
+//
 // Per CTA and row the result is one (max, sum-exp) pair and one sorted list
 // of K keys, the same partials as k_head_tc, merged across CTAs by the row
 // merge kernel.
