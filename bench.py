@@ -33,7 +33,7 @@ from speculative_decoding_draft_06_gb300 import inputs as I  # noqa: E402
 
 DEFAULT_CONFIG = "q8b"
 FALLBACK_HBM_GBS = 6800.0
-ROWS_MIN = 65  # head calls with this many rows run k_head_rows (the library's default)
+ROWS_MIN = 64  # head calls with this many rows run k_head_rows (the library's default)
 KERNEL_SOURCES = ("speculative_decoding_draft_06_gb300/csrc/head_tc.cu",
                   "speculative_decoding_draft_06_gb300/csrc/epilogue.cuh",
                   "speculative_decoding_draft_06_gb300/csrc/ptx.cuh",

@@ -90,8 +90,8 @@ struct dartree_ctx {
   cudaGraphExec_t gexec = nullptr;
   GraphKey gkey{};
   int tc_ctas_per_sm = 1;  // tuning: head-call CTAs per SM
-  int rows_min = 65;       // head calls with at least this many rows put the rows on the MMA M side
-  int rows_nv = 128;       // ... in vocabulary tiles of this many entries (128 or 256)
+  int rows_min = 64;       // head calls with at least this many rows put the rows on the MMA M side
+  int rows_nv = 256;       // ... in vocabulary tiles of this many entries (128 or 256)
   bool rows_pair = true;   // ... and with more than 128 rows on CTA pairs (two-CTA MMA)
   float* pm = nullptr;
   float* ps = nullptr;

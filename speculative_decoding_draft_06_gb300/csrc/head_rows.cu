@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
     k_head_rows(const __grid_constant__ CUtensorMap tmap_w,
                 const __grid_constant__ CUtensorMap tmap_s, const TcParams p) {
   using C = RowsCfg<MH, NV, kPair>;
-  static_assert(KR == 0 || KR == 8, "register list capacity");
+  static_assert(KR == 0 || KR == 8 || KR == 32, "register list capacity");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -696,16 +696,23 @@ cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcPa
                          q.pdl != 0, tw, ts, q);
 }
 
+// The top-K lists: in registers for K <= 8; for K <= 32 as well where one
+// warpgroup of epilogue threads leaves the registers (one 128-row CTA);
+// else in shared memory.
 template <int MH, int NV, bool kPair>
 cudaError_t launch_rows_k(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p,
                           int units, cudaStream_t st) {
-  return p.K <= 8 ? launch_rows<MH, NV, 8, kPair>(tw, ts, p, units, st)
-                  : launch_rows<MH, NV, 0, kPair>(tw, ts, p, units, st);
+  if (p.K <= 8) return launch_rows<MH, NV, 8, kPair>(tw, ts, p, units, st);
+  if constexpr (MH == 1 && !kPair)
+    if (p.K <= 32) return launch_rows<MH, NV, 32, kPair>(tw, ts, p, units, st);
+  return launch_rows<MH, NV, 0, kPair>(tw, ts, p, units, st);
 }
 
 template <int MH, int NV, bool kPair>
 cudaError_t set_rows_attrs() {
   cudaError_t e = set_max_dynamic_smem(k_head_rows<MH, NV, 8, kPair>);
+  if constexpr (MH == 1 && !kPair)
+    if (e == cudaSuccess) e = set_max_dynamic_smem(k_head_rows<MH, NV, 32, kPair>);
   return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_rows<MH, NV, 0, kPair>);
 }
 
