@@ -107,7 +107,8 @@ def kernel_bytes_per_launch(w: I.Workload, variant: str, kind: str) -> float | N
             per = [w.V * w.H * wb + w.R * w.V * 4 + m * w.H * wb for m in rows]
         return sum(per) / len(per)
     if kind == "state":
-        per = [2 * m * w.H * wb + (0 if opt.get("head") == "markov" else w.H * w.H * wb)
+        # parent states in, the tokens' embedding rows, new states out (+ A)
+        per = [3 * m * w.H * wb + (0 if opt.get("head") == "markov" else w.H * w.H * wb)
                for m in rows[1:]]
         return sum(per) / len(per) if per else None
     if kind == "candidates":
@@ -428,7 +429,7 @@ def run_gpu(args) -> None:
                  f"k_head_rows (head call, {max(big)} head rows on the MMA M side: Wout stream, "
                  f"fused log-softmax + top-K; calls with fewer than {ROWS_MIN} rows: k_head_tc)"),
         "state": ("k_state_markov" if opt.get("head") == "markov" else
-                  "k_head_tc (state step: A stream, split-K)"),
+                  "k_head_tc + k_state_finish (state step: A stream, split-K, finish)"),
         "candidates": "k_base_topk (top-K of the base logits)"}[kind]
 
     # end to end through the public API with host buffers
