@@ -410,6 +410,14 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
         const int s = static_cast<int>(n % S);
         if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), p.err)) break;
       }
+      if (kPair && rank != 0 && *abort_flag) {
+        // after a timeout the peer may have issued a stage the leader never
+        // consumed (whose completion it cannot observe): hold the CTA for
+        // ~50 us, far longer than a copy takes to land
+        const long long t0 = clock64();
+        while (clock64() - t0 < 100000) {
+        }
+      }
     }
   } else if (warp == C::kMma) {
     // ------------------------------------------------------- MMA issuer

@@ -31,8 +31,15 @@ def _small():
     return w, I.make_inputs(w)
 
 
-def test_wait_timeout_is_reported_and_context_stays_usable(monkeypatch):
-    w, inp = _small()
+@pytest.mark.parametrize("shape", ["tc", "rows", "pair"])
+def test_wait_timeout_is_reported_and_context_stays_usable(monkeypatch, shape):
+    """Every head kernel: the vocabulary-on-M kernel (8 rows), the row-major
+    kernel (64 rows) and the CTA-pair kernel (160 rows)."""
+    w = {"tc": I.small_workload(91, V=3000, H=128, D=3, W=8, K=8, B=16, beta=-0.1, bf16=True),
+         "rows": I.small_workload(92, V=3000, H=128, D=3, W=64, K=8, B=40, beta=-0.1, bf16=True),
+         "pair": I.small_workload(93, V=3000, H=128, D=3, W=8, K=8, B=16, beta=-0.1, bf16=True,
+                                  R=20)}[shape]
+    inp = I.make_inputs(w)
     dev = dtl.weights_to_device(inp, True)
     monkeypatch.setenv("DARTREE_WAIT_LIMIT_CYCLES", "1")
     ctx = gu.make_ctx(w)
@@ -44,8 +51,9 @@ def test_wait_timeout_is_reported_and_context_stays_usable(monkeypatch):
     # same process, same device: a normal context builds correctly
     ctx = gu.make_ctx(w)
     res = gu.run_build(ctx, w, dev)
-    pool, rows, tree = gu.split_request(res, w, 0)
-    parity.compare_request(inp, 0, w.D, w.W, w.K, w.B, w.beta, True, pool, rows, tree)
+    for r in range(w.R):
+        pool, rows, tree = gu.split_request(res, w, r)
+        parity.compare_request(inp, r, w.D, w.W, w.K, w.B, w.beta, True, pool, rows, tree)
     ctx.close()
 
 
