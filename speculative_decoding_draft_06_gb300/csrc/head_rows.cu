@@ -1,4 +1,4 @@
-// Head call for many head rows (more than 64): the corrected logits
+// Head call for many head rows (64 and more): the corrected logits
 //   ell[m, v] = z_d[v] + sum_h S[m, h] Wout[v, h]
 // with the online log-sum-exp and the per-row top-K fused into the epilogue
 // ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
@@ -6,18 +6,17 @@
 // DARTree", Methodologie 1: the top-k children of every branch, scored from
 // the normalised corrected distribution).
 //
-// Orientation.  With 128 or more head rows the rows fill the tensor core's
-// M side by themselves, so here the head rows are the MMA M (one or two
-// M = 128 halves) and a vocabulary tile of NV = 128 or 256 entries is the
+// Orientation.  Here the head rows are the MMA M (one or two M = 128
+// halves, padded) and a vocabulary tile of NV = 128 or 256 entries is the
 // MMA N.  The accumulator then holds one head row per TMEM lane: an
-// epilogue thread reads its own row's NV logits of the tile with
-// tcgen05.ld and keeps the row's running (max, sum-exp) and its top-K
-// threshold in registers -- no transposition, no cross-lane reduction, a
-// compare per value.  (The kernel for up to 64 rows, k_head_tc, puts the
-// vocabulary on M instead.)  The states are re-read from L2 for every
-// tile; the wider tile halves that stream per weight byte, at the price of
-// a single accumulator for two halves (the MMAs of a tile wait for the
-// previous tile's epilogue, which is short).
+// epilogue thread reads its own row's logits of the tile with tcgen05.ld
+// and keeps the row's running (max, sum-exp), its top-K list and threshold
+// -- no transposition, no cross-lane reduction, a compare per value.  (The
+// kernel for fewer than 64 rows, k_head_tc, puts the vocabulary on M
+// instead.)  The states are re-read from L2 for every tile; the wider tile
+// halves that stream per weight byte (one CTA with MH = 2 and NV = 256 has a
+// single accumulator: the MMAs of a tile wait for the previous tile's
+// epilogue).
 //
 // Warp roles: warps 0..4MH-1 epilogue (warp w reads TMEM lane quarter w % 4
 // of half w / 4), warp 4MH TMA producer (per 64-wide K step: MH boxes of
