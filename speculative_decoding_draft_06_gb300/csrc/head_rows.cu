@@ -687,7 +687,7 @@ cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcPa
   using C = RowsCfg<MH, NV, kPair>;
   const size_t lists = KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows * C::kColGroups * 8;
   const size_t fixed = 1024 + lists + 64 * 8 + 64;
-  const size_t budget = 227 * 1024 - 2048;
+  const size_t budget = 227 * 1024 - 512;  // no static shared memory in this kernel
   int stages = budget > fixed ? static_cast<int>((budget - fixed) / C::kStageBytes) : 0;
   const int cap = p.max_stages > 0 ? p.max_stages : kRowsMaxStages;
   if (stages > cap) stages = cap;
