@@ -8,9 +8,11 @@
 // Mechanism, and "Technische Samenvatting: DARTree", Methodologie 1).
 //
 // A CTA of 128 threads owns contiguous 128-row weight tiles; thread t owns
-// weight row tile*128 + t.  Weight and state slices of 32 columns are staged
-// through shared memory (coalesced loads, padded rows); each thread keeps 16
-// head-row accumulators in registers and runs over the columns in chunks.
+// weight row tile*128 + t and reads it straight from global memory with
+// 16-byte loads, eight in flight (the row's cache lines stay in L1 between
+// its loads).  The 16 head rows of a chunk are staged in shared memory in
+// slices of 256 columns and read as broadcasts; each thread keeps 16
+// head-row accumulators in registers.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -19,13 +21,12 @@
 
 namespace dt {
 
-constexpr int kSimtH = 32;  // contraction slice staged per step
+constexpr int kSimtH = 256;  // state columns staged per slice
 
 template <int N, bool kLogits>
 __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  float* sW = reinterpret_cast<float*>(smem_raw);            // [128][33]
-  float* sS = sW + kTileV * (kSimtH + 1);                    // [16][32]
+  float* sS = reinterpret_cast<float*>(smem_raw);                // [16][256] state slice
   uint8_t* tail = reinterpret_cast<uint8_t*>(sS + 16 * kSimtH);  // epilogue or U rows
 
   const int tid = threadIdx.x;
@@ -43,33 +44,47 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
     const int row = t * kTileV + tid;
     const bool valid = row < p.rows;
     // contraction of 16 head rows c0..c0+15 against this thread's weight row
+    const float* wrow = p.W_f32 + static_cast<size_t>(valid ? row : 0) * p.H;
+    const bool w_vec = (p.H & 3) == 0 && (reinterpret_cast<uintptr_t>(p.W_f32) & 15) == 0;
     auto dot16 = [&](float (&acc)[16], int c0) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0.f;
       for (int h0 = 0; h0 < p.H; h0 += kSimtH) {
+        const int hn = p.H - h0 < kSimtH ? p.H - h0 : kSimtH;  // columns of this slice
         __syncthreads();
-#pragma unroll 4
-        for (int i = 0; i < kSimtH; ++i) {
-          const int e = i * kTileV + tid;
-          const int r = e >> 5, c = e & 31;
-          const int gr = t * kTileV + r, gc = h0 + c;
-          sW[r * (kSimtH + 1) + c] =
-              (gr < p.rows && gc < p.H) ? __ldg(p.W_f32 + static_cast<size_t>(gr) * p.H + gc) : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int e = i * kTileV + tid;
-          const int r = e >> 5, c = e & 31;
-          const int m = c0 + r, gc = h0 + c;
-          sS[r * kSimtH + c] =
-              (m < p.M && gc < p.H) ? __ldg(p.S_f32 + static_cast<size_t>(m) * p.H + gc) : 0.f;
+        for (int e = tid; e < 16 * kSimtH; e += kTileV) {
+          const int r = e / kSimtH, c = e % kSimtH;
+          const int m = c0 + r;
+          sS[e] = (m < p.M && c < hn) ? __ldg(p.S_f32 + static_cast<size_t>(m) * p.H + h0 + c)
+                                      : 0.f;
         }
         __syncthreads();
-#pragma unroll 8
-        for (int hh = 0; hh < kSimtH; ++hh) {
-          const float w = sW[tid * (kSimtH + 1) + hh];
+        if (w_vec && (hn & 31) == 0) {
+          for (int hb = 0; hb < hn; hb += 32) {  // 32 columns: eight 16-byte loads
+            float4 w[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = fmaf(w, sS[j * kSimtH + hh], acc[j]);
+            for (int q = 0; q < 8; ++q)
+              w[q] = valid ? __ldg(reinterpret_cast<const float4*>(wrow + h0 + hb) + q)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float* sc = sS + hb + 4 * q;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float4 sv = *reinterpret_cast<const float4*>(sc + j * kSimtH);
+                acc[j] = fmaf(w[q].x, sv.x, acc[j]);
+                acc[j] = fmaf(w[q].y, sv.y, acc[j]);
+                acc[j] = fmaf(w[q].z, sv.z, acc[j]);
+                acc[j] = fmaf(w[q].w, sv.w, acc[j]);
+              }
+            }
+          }
+        } else {
+          for (int hh = 0; hh < hn; ++hh) {
+            const float w = valid ? __ldg(wrow + h0 + hh) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = fmaf(w, sS[j * kSimtH + hh], acc[j]);
+          }
         }
       }
     };
@@ -145,9 +160,8 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
 
 template <int N, bool kLogits>
 static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(kTileV) * (kSimtH + 1) * 4 + 16 * kSimtH * 4 +
-                      (kLogits ? epi_smem_bytes(N, p.K)
-                               : static_cast<size_t>(kTileV) * (N + 1) * 4);
+  const size_t smem = 16 * kSimtH * 4 + (kLogits ? epi_smem_bytes(N, p.K)
+                                                 : static_cast<size_t>(kTileV) * (N + 1) * 4);
   return launch_kernel(k_head_simt<N, kLogits>, dim3(grid), dim3(128), smem, st, p.pdl != 0, p);
 }
 
