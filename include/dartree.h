@@ -103,7 +103,14 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
 
 /* Creates a context on the current CUDA device and allocates all workspace
  * (the only allocating call).  Fails with UNSUPPORTED on a device other than
- * compute capability 10.3. */
+ * compute capability 10.3.
+ * Tuning (environment, read here; defaults in brackets): the head call runs
+ * the vocabulary-on-M kernel below DARTREE_ROWS_MIN head rows [64] and the
+ * row-major kernel from there, in vocabulary tiles of DARTREE_ROWS_NV
+ * entries [256; or 128], with more than 128 rows on CTA pairs unless
+ * DARTREE_ROWS_PAIR=0; DARTREE_TC_MAX_STAGES caps the pipeline depth and
+ * DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs on an SM.  Results
+ * are the same under every setting (up to the order of fp32 additions). */
 dartree_status dartree_create(const dartree_config *cfg, dartree_ctx **out);
 
 /* Releases the context and its workspace (synchronises the device). */
