@@ -108,8 +108,10 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
  * the vocabulary-on-M kernel below DARTREE_ROWS_MIN head rows [64] and the
  * row-major kernel from there, in vocabulary tiles of DARTREE_ROWS_NV
  * entries [256; or 128], with more than 128 rows on CTA pairs unless
- * DARTREE_ROWS_PAIR=0; DARTREE_TC_MAX_STAGES caps the pipeline depth and
- * DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs on an SM.  Results
+ * DARTREE_ROWS_PAIR=0, and with at most 64 rows on one CTA streaming 64-row
+ * state boxes unless DARTREE_ROWS_HALF_S=0; DARTREE_TC_MAX_STAGES caps the
+ * pipeline depth and DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs
+ * on an SM.  Results
  * are the same under every setting (up to the order of fp32 additions). */
 dartree_status dartree_create(const dartree_config *cfg, dartree_ctx **out);
 

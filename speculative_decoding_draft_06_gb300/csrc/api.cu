@@ -93,6 +93,7 @@ struct dartree_ctx {
   int rows_min = 64;       // head calls with at least this many rows put the rows on the MMA M side
   int rows_nv = 256;       // ... in vocabulary tiles of this many entries (128 or 256)
   bool rows_pair = true;   // ... and with more than 128 rows on CTA pairs (two-CTA MMA)
+  bool rows_half_s = true;  // ... and with at most 64 rows on one CTA, 64-row state boxes
   float* pm = nullptr;
   float* ps = nullptr;
   uint64_t* ptop = nullptr;
@@ -281,7 +282,9 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
       int units = pair ? c->num_sms / 2 : c->num_sms;
       if (units > tiles) units = tiles;
       p.max_stages = c->tc_max_stages;
-      e = dt::launch_head_rows(M, nv, pair, c->tm_Wout, c->tmS(sbuf, 128), p, units, st, &grid);
+      p.s_rows = !pair && M <= 64 && nv == 256 && c->rows_half_s ? 64 : 128;
+      e = dt::launch_head_rows(M, nv, pair, c->tm_Wout, c->tmS(sbuf, p.s_rows), p, units, st,
+                               &grid);
     } else if (c->bf16) {
       const int slots = c->num_sms * c->tc_ctas_per_sm;
       grid = p.n_tiles < slots ? p.n_tiles : slots;
@@ -897,6 +900,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_ROWS_HALF_S")) c->rows_half_s = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
     const int n = atoi(v);
     c->tc_ctas_per_sm = n == 2 ? 2 : 1;

@@ -52,10 +52,15 @@ namespace {
 // tile.  kPair: a CTA pair computes one M = 256 x N = NV tile with the
 // two-CTA MMA; each CTA holds 128 of the rows (MH = 1) and NV / 2 of the
 // tile's Wout rows, and its TMEM holds its 128 rows x NV columns.
-template <int MH, int NV, bool kPair = false>
+//
+// kHalfS (one CTA, at most 64 live rows): the stage holds a 64-row state box
+// ([states 8 KB][Wout]); the MMA's A rows 64..127 then read the first Wout
+// rows of the same stage, which only the never-read TMEM lanes 64..127 see.
+// The smaller stage leaves room for one more in flight.
+template <int MH, int NV, bool kPair = false, bool kHalfS = false>
 struct RowsCfg {
   static constexpr int kRows = 128 * MH;             // head rows of this CTA (padded)
-  static constexpr int kABytes = kRows * kTileH * 2; // states: MH boxes of 128 rows x 128 B
+  static constexpr int kABytes = (kHalfS ? 64 : kRows) * kTileH * 2;  // states, 128 B rows
   static constexpr int kBRows = kPair ? NV / 2 : NV; // Wout rows of the tile in this CTA
   static constexpr int kBBytes = kBRows * kTileH * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -71,6 +76,7 @@ struct RowsCfg {
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
   static_assert(NV == 128 || NV == 256, "vocabulary tile");
   static_assert(!kPair || (MH == 1 && NV == 256), "pair tile");
+  static_assert(!kHalfS || (MH == 1 && !kPair), "64-row state box");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
   // instruction descriptor: bf16 x bf16 -> fp32, K-major A and B, N = NV,
   // M = 128 (one CTA) or 256 (the pair)
@@ -285,11 +291,11 @@ struct RowList<0> {
   }
 };
 
-template <int MH, int NV, int KR, bool kPair>
-__global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
+template <int MH, int NV, int KR, bool kPair, bool kHalfS>
+__global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
     k_head_rows(const __grid_constant__ CUtensorMap tmap_w,
                 const __grid_constant__ CUtensorMap tmap_s, const TcParams p) {
-  using C = RowsCfg<MH, NV, kPair>;
+  using C = RowsCfg<MH, NV, kPair, kHalfS>;
   static_assert(KR == 0 || KR == 8 || KR == 32, "register list capacity");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -681,10 +687,10 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair>::kThreads, 1)
   }
 }
 
-template <int MH, int NV, int KR, bool kPair>
+template <int MH, int NV, int KR, bool kPair, bool kHalfS>
 cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p, int units,
                         cudaStream_t st) {
-  using C = RowsCfg<MH, NV, kPair>;
+  using C = RowsCfg<MH, NV, kPair, kHalfS>;
   const size_t lists = KR > 0 ? 0 : static_cast<size_t>(p.K) * C::kRows * C::kColGroups * 8;
   const size_t fixed = 1024 + lists + 64 * 8 + 64;
   const size_t budget = 227 * 1024 - 512;  // no static shared memory in this kernel
@@ -696,31 +702,31 @@ cudaError_t launch_rows(const CUtensorMap& tw, const CUtensorMap& ts, const TcPa
   q.stages = stages;
   const size_t smem = fixed + static_cast<size_t>(stages) * C::kStageBytes;
   if constexpr (kPair)
-    return launch_kernel_cluster(k_head_rows<MH, NV, KR, kPair>, dim3(2 * units),
+    return launch_kernel_cluster(k_head_rows<MH, NV, KR, kPair, kHalfS>, dim3(2 * units),
                                  dim3(C::kThreads), smem, st, q.pdl != 0, 2, tw, ts, q);
   else
-    return launch_kernel(k_head_rows<MH, NV, KR, kPair>, dim3(units), dim3(C::kThreads), smem, st,
-                         q.pdl != 0, tw, ts, q);
+    return launch_kernel(k_head_rows<MH, NV, KR, kPair, kHalfS>, dim3(units), dim3(C::kThreads),
+                         smem, st, q.pdl != 0, tw, ts, q);
 }
 
 // The top-K lists: in registers for K <= 8; for K <= 32 as well where one
 // warpgroup of epilogue threads leaves the registers (one 128-row CTA);
 // else in shared memory.
-template <int MH, int NV, bool kPair>
+template <int MH, int NV, bool kPair, bool kHalfS = false>
 cudaError_t launch_rows_k(const CUtensorMap& tw, const CUtensorMap& ts, const TcParams& p,
                           int units, cudaStream_t st) {
-  if (p.K <= 8) return launch_rows<MH, NV, 8, kPair>(tw, ts, p, units, st);
+  if (p.K <= 8) return launch_rows<MH, NV, 8, kPair, kHalfS>(tw, ts, p, units, st);
   if constexpr (MH == 1 && !kPair)
-    if (p.K <= 32) return launch_rows<MH, NV, 32, kPair>(tw, ts, p, units, st);
-  return launch_rows<MH, NV, 0, kPair>(tw, ts, p, units, st);
+    if (p.K <= 32) return launch_rows<MH, NV, 32, kPair, kHalfS>(tw, ts, p, units, st);
+  return launch_rows<MH, NV, 0, kPair, kHalfS>(tw, ts, p, units, st);
 }
 
-template <int MH, int NV, bool kPair>
+template <int MH, int NV, bool kPair, bool kHalfS = false>
 cudaError_t set_rows_attrs() {
-  cudaError_t e = set_max_dynamic_smem(k_head_rows<MH, NV, 8, kPair>);
+  cudaError_t e = set_max_dynamic_smem(k_head_rows<MH, NV, 8, kPair, kHalfS>);
   if constexpr (MH == 1 && !kPair)
-    if (e == cudaSuccess) e = set_max_dynamic_smem(k_head_rows<MH, NV, 32, kPair>);
-  return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_rows<MH, NV, 0, kPair>);
+    if (e == cudaSuccess) e = set_max_dynamic_smem(k_head_rows<MH, NV, 32, kPair, kHalfS>);
+  return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_rows<MH, NV, 0, kPair, kHalfS>);
 }
 
 int g_max_pairs = 0;  // CTA pairs of the pair kernel that can be resident together
@@ -734,6 +740,7 @@ cudaError_t init_head_rows_attrs() {
   if ((e = set_rows_attrs<1, 256, false>()) != cudaSuccess) return e;
   if ((e = set_rows_attrs<2, 256, false>()) != cudaSuccess) return e;
   if ((e = set_rows_attrs<1, 256, true>()) != cudaSuccess) return e;
+  if ((e = set_rows_attrs<1, 256, false, true>()) != cudaSuccess) return e;
   // resident clusters of two at the largest shared-memory footprint
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2);
@@ -747,7 +754,7 @@ cudaError_t init_head_rows_attrs() {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, k_head_rows<1, 256, 0, true>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, k_head_rows<1, 256, 0, true, false>, &cfg);
   if (e != cudaSuccess) return e;
   g_max_pairs = n;
   return cudaSuccess;
@@ -764,6 +771,10 @@ cudaError_t launch_head_rows(int M, int nv, bool pair, const CUtensorMap& tw, co
     return launch_rows_k<1, 256, true>(tw, ts, p, units, st);
   }
   *units_used = units;
+  if (p.s_rows == 64) {  // 64-row state boxes (the map's box), 256-entry tiles
+    if (M > 64 || nv != 256) return cudaErrorInvalidValue;
+    return launch_rows_k<1, 256, false, true>(tw, ts, p, units, st);
+  }
   if (M <= 128)
     return nv == 128 ? launch_rows_k<1, 128, false>(tw, ts, p, units, st)
                      : launch_rows_k<1, 256, false>(tw, ts, p, units, st);

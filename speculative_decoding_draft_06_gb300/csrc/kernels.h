@@ -21,6 +21,8 @@ struct TcParams {
   int* err;            // device error word
   long long wait_limit;  // pipeline wait limit in cycles (0: the full ~2 s)
   int V_tok;           // vocabulary size (bound of state-step tokens)
+  int s_rows;          // row-major head kernel: state rows per TMA box of tmap_s (64: one
+                       // CTA with at most 64 live rows and 256-entry tiles; else 128)
   // logits epilogue
   const float* z;      // base logits of this depth, request 0
   long long z_req_stride;

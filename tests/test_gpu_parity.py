@@ -128,9 +128,24 @@ def test_head_rows_tile_widths_match_oracle(monkeypatch, mode, M, K):
     MMA -- against the oracle rows."""
     monkeypatch.setenv("DARTREE_ROWS_PAIR", "1" if mode == "pair" else "0")
     monkeypatch.setenv("DARTREE_ROWS_NV", "256" if mode == "nv256" else "128")
+    _check_head_rows(M, K, seed=M + len(mode))
+
+
+@pytest.mark.parametrize("half", ["0", "1"])
+@pytest.mark.parametrize("M,K", [(1, 4), (40, 32), (64, 8), (64, 17)])
+def test_head_rows_with_at_most_64_rows_match_oracle(monkeypatch, half, M, K):
+    """The one-CTA row-major kernel with 64-row state boxes (the other 64
+    TMEM lanes hold whatever the stage held and are never read) or full
+    128-row boxes."""
+    monkeypatch.setenv("DARTREE_ROWS_MIN", "1")
+    monkeypatch.setenv("DARTREE_ROWS_HALF_S", half)
+    _check_head_rows(M, K, seed=1000 + M + int(half))
+
+
+def _check_head_rows(M, K, seed):
     w = I.small_workload(60 + M + K, V=1900, H=192, D=1, W=1, K=K, B=1, bf16=True)
     inp = I.make_inputs(w)
-    g = np.random.default_rng(M + len(mode))
+    g = np.random.default_rng(seed)
     S = I.bf16_bits_to_f32(I.to_bf16_bits(np.tanh(g.standard_normal((M, w.H))).astype(np.float32)))
     z = inp["z"][0, 0]
     ctx = gu.make_ctx(w, max_K=K)
