@@ -209,9 +209,10 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   // prologue done; from here on the kernel reads and writes shared buffers.
   // A state step whose operands were complete before the previous kernel
-  // began streams them at once and waits only before its epilogue, which
-  // reads the previous kernel's selection (slot, tok) -- the contraction then
-  // overlaps the previous kernel.
+  // began streams them at once and waits only in its epilogue (the unsplit
+  // epilogue reads the previous kernel's selection (slot, tok); the split
+  // one waits after storing its partials) -- the contraction then overlaps
+  // the previous kernel.
   const bool early = !kLogits && p.early_operands;
   if (!early) pdl_wait();
   pdl_trigger();
@@ -303,7 +304,12 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     // accumulator and broadcasts whether to go on (a timed-out wait ends all
     // four warps' loops at once).  Every group waits for every tile, so each
     // arrival on tempty belongs to the tile it was meant for.
-    if (early) pdl_wait();
+    // Split-K partials need nothing from the previous kernel and go to a
+    // scratch that only the finish kernel after this one reads: they are
+    // stored first, and the wait (which keeps the kernels' completion order)
+    // comes after them.
+    const bool wait_last = early && p.n_split > 1;
+    if (early && !wait_last) pdl_wait();
     int it = 0;
     const int grp = warp >> 2;
     const int wq = warp & 3;  // TMEM lane quarter
@@ -382,6 +388,7 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     if constexpr (kLogits) {
       epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
     }
+    if (wait_last) pdl_wait();
   }
 
   tc_fence_before();

@@ -54,6 +54,9 @@ def test_create_rejects_bad_configs_before_touching_the_device(lib):
     bad = [dtl.Config(1000, 60, 4, 4, 4, 8, 1, dtl.W_BF16),     # H % 64 != 0
            dtl.Config(1000, 64, 4, 4, 33, 8, 1, dtl.W_BF16),    # K > 32
            dtl.Config(1000, 64, 4, 64, 4, 8, 8, dtl.W_BF16),    # R * W > 256
+           dtl.Config(1000, 64, 4, 257, 4, 8, 1, dtl.W_BF16),   # W > 256
+           dtl.Config(1000, 64, 33, 4, 4, 8, 1, dtl.W_BF16),    # D > 32
+           dtl.Config(1000, 64, 4, 4, 4, 1025, 1, dtl.W_BF16),  # B > 1024
            dtl.Config(0, 64, 4, 4, 4, 8, 1, dtl.W_F32),
            dtl.Config(1000, 64, 4, 4, 4, 8, 1, 7)]
     for cfg in bad:

@@ -35,6 +35,11 @@ SMALL = [
     ("bf16-batch-odd", dict(V=1101, H=128, D=3, W=8, K=4, B=30, beta=-0.2, bf16=True, R=20)),
     ("bf16-k1w1", dict(V=500, H=64, D=6, W=1, K=1, B=6, beta=0.0, bf16=True)),
     ("bf16-bigB", dict(V=700, H=64, D=3, W=6, K=3, B=200, beta=-1.0, bf16=True, R=2)),
+    # the build limits: W = 256 (256-row head calls on CTA pairs, a top-W over
+    # 8192 candidates), K = 32, B = 1024 <= P = 1056
+    ("bf16-max", dict(V=1500, H=64, D=5, W=256, K=32, B=1024, beta=-0.05, bf16=True)),
+    # fp32 at the limits, B above the pool (P = 800)
+    ("f32-max", dict(V=700, H=32, D=4, W=256, K=32, B=1024, beta=0.0, bf16=False)),
 ]
 
 
