@@ -94,6 +94,8 @@ struct dartree_ctx {
   int rows_nv = 256;       // ... in vocabulary tiles of this many entries (128 or 256)
   bool rows_pair = true;   // ... and with more than 128 rows on CTA pairs (two-CTA MMA)
   bool rows_half_s = true;  // ... and with at most 64 rows on one CTA, 64-row state boxes
+  bool merge_bound = true;  // row merge through the head call's row bound (k_merge_bound)
+  int merge_surv_cap = 512;  // ... staging at most this many keys (test knob)
   float* pm = nullptr;
   float* ps = nullptr;
   uint64_t* ptop = nullptr;
@@ -338,9 +340,11 @@ dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, i
   mp.row_cnt = c->row_cnt;
   mp.gth = c->gth;
   mp.gmx = c->gth + dt::kMaxRows;
+  mp.surv_cap = c->merge_surv_cap;
   {
     KernelTimer tk(c, st, 2);
-    e = dt::launch_merge_rows(mp, st);
+    e = c->merge_bound && dt::merge_bound_fits(mp) ? dt::launch_merge_bound(mp, st)
+                                                   : dt::launch_merge_rows(mp, st);
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "merge launch");
   return DARTREE_OK;
@@ -901,6 +905,8 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_ROWS_HALF_S")) c->rows_half_s = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_MERGE_BOUND")) c->merge_bound = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_MERGE_SURV_CAP")) c->merge_surv_cap = atoi(v);
   if (const char* v = getenv("DARTREE_TC_CTAS_PER_SM")) {
     const int n = atoi(v);
     c->tc_ctas_per_sm = n == 2 ? 2 : 1;

@@ -157,8 +157,15 @@ struct MergeParams {
   int32_t* pool_depth;
   float* pool_score;
   int* counters;             // [R] zero between launches
+  int surv_cap;              // k_merge_bound: keys at or above the bound staged in shared
+                             // memory (at most 512; more go the slow way)
 };
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
+// The same merge (and selection) with one block per row that reads only the
+// CTA lists reaching the head call's row bound (K <= 16, at most 320
+// partials per row; merge_bound_fits says which).
+bool merge_bound_fits(const MergeParams& p);
+cudaError_t launch_merge_bound(const MergeParams& p, cudaStream_t st);
 
 // Deferred Top-B, compaction and the ancestor mask.
 struct PruneParams {

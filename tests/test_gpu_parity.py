@@ -64,10 +64,33 @@ def test_build_matches_oracle_small(idx):
     ctx.close()
 
 
-def test_build_with_two_ctas_per_sm_merges_row_groups(monkeypatch):
+@pytest.mark.parametrize("name", ["bf16-n16", "bf16-batch", "f32-ragged"])
+def test_build_with_the_row_group_merge_matches_oracle(monkeypatch, name):
+    """The per-row group merge (every CTA list folded), forced here instead
+    of the merge through the row bound, gives the same trees."""
+    monkeypatch.setenv("DARTREE_MERGE_BOUND", "0")
+    test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
+
+
+@pytest.mark.parametrize("cap", ["0", "40"])
+@pytest.mark.parametrize("name", ["bf16-n32", "bf16-batch", "f32-wide"])
+def test_build_with_small_bound_key_buffers_matches_oracle(monkeypatch, name, cap):
+    """The merge through the row bound with a small staging buffer: with none,
+    every key of the lists that reach the bound is folded straight from
+    memory (the path taken when more keys reach it than the buffer holds);
+    with 40, rows with 6..40 keys at or above the bound are folded by all
+    warps and a tree, rows with more straight from memory."""
+    monkeypatch.setenv("DARTREE_MERGE_SURV_CAP", cap)
+    test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
+
+
+@pytest.mark.parametrize("merge_bound", ["0", "1"])
+def test_build_with_two_ctas_per_sm_merges_row_groups(monkeypatch, merge_bound):
     """Two head-call CTAs per SM: more than 160 CTA partials per row, so the
-    row merge runs in several group blocks and combines them."""
+    per-row group merge runs in several group blocks and combines them; the
+    merge through the row bound reads all pairs in one block per row."""
     monkeypatch.setenv("DARTREE_TC_CTAS_PER_SM", "2")
+    monkeypatch.setenv("DARTREE_MERGE_BOUND", merge_bound)
     w = I.small_workload(590, V=30000, H=64, D=3, W=6, K=5, B=20, beta=-0.1, bf16=True)
     inp = I.make_inputs(w)
     dev = dtl.weights_to_device(inp, w.bf16)
