@@ -111,7 +111,8 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
  * DARTREE_ROWS_PAIR=0, and with at most 64 rows on one CTA streaming 64-row
  * state boxes unless DARTREE_ROWS_HALF_S=0; DARTREE_TC_MAX_STAGES caps the
  * pipeline depth and DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs
- * on an SM.  Results
+ * on an SM; the row merge reads only the CTA lists that reach the head call's
+ * row bound (K <= 16) unless DARTREE_MERGE_BOUND=0.  Results
  * are the same under every setting (up to the order of fp32 additions). */
 dartree_status dartree_create(const dartree_config *cfg, dartree_ctx **out);
 
