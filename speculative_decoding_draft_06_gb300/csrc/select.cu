@@ -1,11 +1,14 @@
 // Selection kernels of a DARTree build: merge of the head-call partials into
-// per-row log-probabilities and top-K, the per-depth global top-W with pool
-// append and state carry, the deferred global Top-B with compaction and the
-// ancestor (tree-attention) mask, and the root rows.
+// per-row log-probabilities and top-K (k_merge_rows folds every CTA list;
+// k_merge_bound reads only the lists that reach the head call's row bound),
+// the per-depth global top-W with pool append and state carry, the deferred
+// global Top-B with compaction and the ancestor (tree-attention) mask, and
+// the root rows.
 //
-// Every selection sorts 64-bit keys (value desc, index asc; see common.cuh)
-// with a block-wide bitonic sort in shared memory, so results are a
-// deterministic total order and independent of thread timing.
+// Every selection orders 64-bit keys (value desc, index asc; see common.cuh)
+// with bitonic sorts and merges, in warps or in shared memory, and the keys
+// are distinct, so results are a deterministic total order and independent
+// of thread timing (including the order in which k_merge_bound stages keys).
 #include <cuda_runtime.h>
 
 #include "block.cuh"
