@@ -12,7 +12,8 @@
 // 16-byte loads, eight in flight (the row's cache lines stay in L1 between
 // its loads).  The 16 head rows of a chunk are staged in shared memory in
 // slices of 256 columns and read as broadcasts; each thread keeps 16
-// head-row accumulators in registers.
+// head-row accumulators in registers, of which only the first 4 or 8 are
+// computed when no more rows of the chunk carry data.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -46,13 +47,16 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
     // contraction of 16 head rows c0..c0+15 against this thread's weight row
     const float* wrow = p.W_f32 + static_cast<size_t>(valid ? row : 0) * p.H;
     const bool w_vec = (p.H & 3) == 0 && (reinterpret_cast<uintptr_t>(p.W_f32) & 15) == 0;
-    auto dot16 = [&](float (&acc)[16], int c0) {
+    // the first J of the chunk's 16 head rows (the others are zero): J = 4 or
+    // 8 when only that many rows of the chunk carry data
+    auto dot_j = [&](auto jc, float (&acc)[16], int c0) {
+      constexpr int J = decltype(jc)::value;
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0.f;
       for (int h0 = 0; h0 < p.H; h0 += kSimtH) {
         const int hn = p.H - h0 < kSimtH ? p.H - h0 : kSimtH;  // columns of this slice
         __syncthreads();
-        for (int e = tid; e < 16 * kSimtH; e += kTileV) {
+        for (int e = tid; e < J * kSimtH; e += kTileV) {
           const int r = e / kSimtH, c = e % kSimtH;
           const int m = c0 + r;
           sS[e] = (m < p.M && c < hn) ? __ldg(p.S_f32 + static_cast<size_t>(m) * p.H + h0 + c)
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
             for (int q = 0; q < 8; ++q) {
               const float* sc = sS + hb + 4 * q;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+              for (int j = 0; j < J; ++j) {
                 const float4 sv = *reinterpret_cast<const float4*>(sc + j * kSimtH);
                 acc[j] = fmaf(w[q].x, sv.x, acc[j]);
                 acc[j] = fmaf(w[q].y, sv.y, acc[j]);
@@ -83,10 +87,19 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
           for (int hh = 0; hh < hn; ++hh) {
             const float w = valid ? __ldg(wrow + h0 + hh) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = fmaf(w, sS[j * kSimtH + hh], acc[j]);
+            for (int j = 0; j < J; ++j) acc[j] = fmaf(w, sS[j * kSimtH + hh], acc[j]);
           }
         }
       }
+    };
+    auto dot16 = [&](float (&acc)[16], int c0) {
+      const int live = mcols - c0;  // the same for the whole block
+      if (live <= 4)
+        dot_j(IntC<4>{}, acc, c0);
+      else if (live <= 8)
+        dot_j(IntC<8>{}, acc, c0);
+      else
+        dot_j(IntC<16>{}, acc, c0);
     };
     auto add_z = [&](float (&acc)[16], int c0) {
       int req_prev = -1;
