@@ -301,9 +301,9 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
 
 /* ------------------------------------------------------------------
  * Verification consumer of a built tree ("DARTree: Teaching a Chain-Trained
- * Corrector to Think in Trees", Core Mechanism: the verification tree and
- * its sparse attention mask let the target check every branch in one
- * forward, then the longest matching prefix is accepted; "Technische
+ * Corrector to Think in Trees", Core Mechanism: with the tree and its mask a
+ * single target forward verifies all branches, and the longest prefix the
+ * target agrees with is kept; "Technische
  * Samenvatting: DARTree", Methodologie 2, Verificatie).  Context-free,
  * asynchronous on `stream`, no allocation.  Errors are INVALID_ARG /
  * UNSUPPORTED before any launch; dartree_last_error(NULL) has the text.

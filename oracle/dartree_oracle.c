@@ -11,7 +11,7 @@
  *   [P1] "DARTree: Teaching a Chain-Trained Corrector to Think in Trees"
  *        -- Core Mechanism (level-by-level construction; best-first pruning
  *        over cached scores), Key Concepts (marginal vs conditional),
- *        Framework Shift (head calls = O(depth)).
+ *        Framework Shift (one head call per depth, not per node).
  *   [P2] "Technische Samenvatting: DARTree" -- Methodologie, 1. Depth-Wise
  *        Parallel AR Expansie (batched correction, cumulative corrected
  *        score, keep top-W and carry correction states) and 2. Deferred
@@ -19,8 +19,8 @@
  *        Lemma 1: with a non-positive depth bonus it equals a sequential
  *        best-first max-heap).
  *   [P3] "Accelerating Language Models with Diffusion Draft Trees" -- Summary
- *        & Methodology Analysis (global top-W child prefixes per depth, state
- *        update, global top-B, prefix tree verified with a tree-attention
+ *        & Methodology Analysis (a global top-W over each depth's children,
+ *        state update, global top-B, prefix tree verified with a tree-attention
  *        mask).
  *
  * The correction head's architecture is not given by the pages.  The fixed
@@ -119,8 +119,8 @@ void orc_state_step(int H, int bf16, const void *A, const void *E,
 /* Corrected logits of one path and their log-sum-exp over the vocabulary.
  * ell[v] = fp32( z_d[v] + sum_h s[h] Wout[v,h] );
  * lse    = m + log sum_v exp(ell[v] - m), m = max ell, in double.
- * [P1] Core Mechanism ("W corrected conditional distributions, each properly
- * conditioned on the tokens along its own branch"). */
+ * [P1] Core Mechanism (one corrected distribution per branch, conditioned
+ * on that branch's own tokens). */
 void orc_logits_row(int V, int H, int bf16, const float *z_d, const void *Wout,
                     const float *s, float *ell, double *lse) {
     double m = -INFINITY;
@@ -139,7 +139,8 @@ void orc_logits_row(int V, int H, int bf16, const float *z_d, const void *Wout,
 
 /* Top-K of one row by (logit desc, token asc), by insertion into a sorted
  * list.  gap = ell_(K) - ell_(K+1) (+inf when V == K).
- * [P1] Core Mechanism ("Expand each node by its top-k children"). */
+ * [P1] Core Mechanism (every frontier node is expanded by its K best
+ * children). */
 void orc_topk_row(int V, const float *ell, int K, int32_t *tok, float *val,
                   float *gap) {
     int n = 0;
@@ -233,10 +234,10 @@ int orc_pool_size(int D, int W, int K) {
  * Depth-wise batched construction of the supertree for one request.
  * [P1] Core Mechanism: at depth d the W surviving paths go through the head
  * in ONE call; each is expanded by its top-k children (W*k candidates),
- * scored by accumulated path probability; the top W are kept; after D levels
+ * ranked by cumulative path log-probability; the W best survive; after D levels
  * exactly D head calls have been made and a pool of scored nodes is held.
- * [P2] Methodologie 1 and [P3] Summary: global top-W child prefixes per
- * depth, correction states carried forward.
+ * [P2] Methodologie 1 and [P3] Summary: one global top-W over each depth's
+ * children, whose correction states go on to the next depth.
  *
  * Inputs: z [D,V] fp32, state0 [H] fp32, A [H,H], E [V,H], Wout [V,H]
  * (bf16 bits or fp32).  Depth 1 has |F_1| = min(W, K) nodes.
@@ -440,8 +441,8 @@ static float prune_key(float score, int32_t depth, float beta) {
  * Deferred global Top-B, compaction and the tree-attention mask.
  * [P2] Methodologie 2: one global Top-B over every materialised prefix of
  * the supertree, with a non-positive depth bonus; [P1] Core Mechanism: the
- * selected nodes form the verification tree plus the sparse attention mask
- * that lets the target check every branch in one forward; [P3] Summary.
+ * selected nodes form the verification tree, and its ancestor mask lets a
+ * single target forward verify all branches at once; [P3] Summary.
  *
  * Canonical output order = the selection order (key desc, pool index asc).
  * out_parent = rank of the parent in that order (-1 at depth 1).
@@ -504,9 +505,9 @@ done:
 /*
  * Sequential best-first pruning over the cached scores with a max-heap:
  * seed with the depth-1 nodes, then B times pop the best node and push its
- * children from the pool.  [P1] Core Mechanism ("Best-first pruning runs
- * over the cached scores ... The heap operations are still sequential, but
- * they touch no neural network"); Expert Assessment (EAGLE-2's heap moved
+ * children from the pool.  [P1] Core Mechanism (the best-first pruning works
+ * on scores already computed, so its sequential heap steps run no model);
+ * Expert Assessment (EAGLE-2's heap moved
  * after the forwards).  Used to check Lemma 1 against orc_topb.
  * pop_order[r] = pool index popped at step r; returns the number of pops.
  */
@@ -716,9 +717,9 @@ done:
 
 /*
  * One attention layer of the target's verification forward over the prefix
- * and the draft tree.  [P1] Core Mechanism (the verification tree and a
- * sparse attention mask let the target check every branch in ONE forward,
- * then the longest matching prefix is accepted); [P2] Methodologie 2
+ * and the draft tree.  [P1] Core Mechanism (with the tree and its mask a
+ * single target forward verifies all branches, and the longest prefix the
+ * target agrees with is kept); [P2] Methodologie 2
  * (Verificatie: one forward pass with tree attention); [P3] Summary.
  *
  * Query rows: row 0 is the root (the last verified token, whose key and
@@ -793,8 +794,8 @@ int orc_tree_attention(int Lp, int B, int Hq, int Hkv, int dh, int bf16, float s
  * the child (among the first n_out nodes, parent rank = current node, -1 for
  * the root) whose token equals the current node's prediction is accepted
  * and becomes the current node; siblings carry distinct tokens, so at most
- * one child matches.  [P1] Core Mechanism ("accept longest matching
- * prefix").  Outputs: accept_len, accept_nodes[0..accept_len) (ranks),
+ * one child matches.  [P1] Core Mechanism (the longest prefix the target
+ * agrees with is accepted).  Outputs: accept_len, accept_nodes[0..accept_len) (ranks),
  * bonus = the prediction at the last accepted node (the root's if none).
  */
 int orc_accept(int B, int n_out, const int32_t *parent, const int32_t *token,

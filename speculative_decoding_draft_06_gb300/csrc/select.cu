@@ -27,9 +27,9 @@ constexpr int kMergeWarps = kMergeThreads / 32;
 // c = score_i + logp_ij (one fp32 add), index i*K + j; the best |F_d| by
 // (c desc, index asc) become the new frontier in rank order ("DARTree:
 // Teaching a Chain-Trained Corrector to Think in Trees", Core Mechanism:
-// score by accumulated path probability, keep the top W; "Accelerating
-// Language Models with Diffusion Draft Trees", Summary: global top-W child
-// prefixes, states carried forward).
+// children ranked by cumulative path log-probability, the W best survive;
+// "Accelerating Language Models with Diffusion Draft Trees", Summary: one
+// global top-W per depth, whose states go on to the next depth).
 __device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k) {
   const int idx = static_cast<int>(key_index(k));
   const int i = idx / p.K, j = idx % p.K;
@@ -483,8 +483,8 @@ constexpr int kPruneThreads = 1024;
 // Methodologie 2: one global Top-B over all materialised prefixes with a
 // non-positive depth bonus).  parent_out = rank of the pool parent; the mask
 // row of node i has bit j set iff j is i or an ancestor of i ("DARTree:
-// Teaching a Chain-Trained Corrector to Think in Trees", Core Mechanism: the
-// sparse attention mask lets the target check every branch in one forward).
+// Teaching a Chain-Trained Corrector to Think in Trees", Core Mechanism:
+// with this mask a single target forward verifies all branches at once).
 __global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
   extern __shared__ uint64_t keys[];
   pdl_wait();

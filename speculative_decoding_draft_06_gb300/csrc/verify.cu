@@ -2,9 +2,8 @@
 // target over the prefix and the draft tree with the emitted ancestor mask,
 // and the longest accepted prefix under the target's predictions
 // ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
-// Mechanism: the verification tree and sparse attention mask let the target
-// check every branch in ONE forward, then the longest matching prefix is
-// accepted; "Technische Samenvatting: DARTree", Methodologie 2, Verificatie).
+// Mechanism: with the tree and its mask a single target forward verifies
+// all branches, and the longest prefix the target agrees with is kept; "Technische Samenvatting: DARTree", Methodologie 2, Verificatie).
 //
 // Tree attention on the 5th-generation tensor cores.  A CTA owns 128 query
 // rows (one TMEM lane each) of one request and one key/value head, and a
