@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -128,11 +129,18 @@ def kernels_per_build(w: I.Workload, variant: str = "dartree", sms: int = 152) -
     return 1 + base + w.D * 2 + (w.D - 1) * state + 1  # root, head + merge/select, states, prune
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and layout: the hash follows code only."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(_ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(_ROOT, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

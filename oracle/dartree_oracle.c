@@ -10,7 +10,7 @@
  * Sources (page title -- section):
  *   [P1] "DARTree: Teaching a Chain-Trained Corrector to Think in Trees"
  *        -- Core Mechanism (level-by-level construction; best-first pruning
- *        over cached scores), Key Concepts (marginal vs conditional),
+ *        on scores already computed), Key Concepts (marginal vs conditional),
  *        Framework Shift (one head call per depth, not per node).
  *   [P2] "Technische Samenvatting: DARTree" -- Methodologie, 1. Depth-Wise
  *        Parallel AR Expansie (batched correction, cumulative corrected
@@ -503,7 +503,7 @@ done:
 }
 
 /*
- * Sequential best-first pruning over the cached scores with a max-heap:
+ * Sequential best-first pruning on the pool's stored scores with a max-heap:
  * seed with the depth-1 nodes, then B times pop the best node and push its
  * children from the pool.  [P1] Core Mechanism (the best-first pruning works
  * on scores already computed, so its sequential heap steps run no model);

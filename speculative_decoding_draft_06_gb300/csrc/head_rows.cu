@@ -2,7 +2,8 @@
 //   ell[m, v] = z_d[v] + sum_h S[m, h] Wout[v, h]
 // with the online log-sum-exp and the per-row top-K fused into the epilogue
 // ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
-// Mechanism: ONE batched head call on all W paths; "Technische Samenvatting:
+// Mechanism: a single batched head call per depth for every branch;
+// "Technische Samenvatting:
 // DARTree", Methodologie 1: the top-k children of every branch, scored from
 // the normalised corrected distribution).
 //

@@ -3,8 +3,8 @@
 // One kernel shape serves both dense steps of a DARTree head call:
 //   * corrected logits  ell[m, v] = z_d[v] + sum_h S[m, h] Wout[v, h]
 //     ("DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
-//     Mechanism: ONE batched head call on all W paths gives W corrected
-//     conditional distributions), fused with the online log-sum-exp and the
+//     Mechanism: a single batched head call per depth yields a corrected
+//     distribution for every branch), fused with the online log-sum-exp and the
 //     per-row top-K (LogitsEpilogue) -- the logits never reach HBM;
 //   * state step        S'[m, h] = bf16(tanh(sum_j A[h, j] S[m, j] + E[tok_m, h]))
 //     ("Technische Samenvatting: DARTree", Methodologie 1: the kept branches
