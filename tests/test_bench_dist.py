@@ -45,3 +45,14 @@ def test_step_time_is_the_max_over_ranks_and_value_counts_all_ranks():
 def test_single_rank_value():
     assert bench.aggregate(4.0, 1) == 4.0
     assert bench.job_value(4.0, 1, 1) == 250.0
+
+
+def test_kernel_source_hash_follows_code_not_comments():
+    """The profile captures stay valid across comment edits of the head
+    kernels and are voided by any code edit."""
+    a = "int f(int x) {  // one\n  /* two\n three */ return x + 1;\n}\n"
+    b = "int f(int x) {\n  // a different comment\n  return x + 1;   /* more */\n}\n"
+    c = "int f(int x) {  // one\n  return x + 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert len(bench.kernel_source_hash()) == 16
