@@ -339,9 +339,7 @@ constexpr int kSurvCap = 512;     // keys at or above the bound staged in shared
 // (typically a few K of the n_cta K), and sorts them.  The log-sum-exp pairs
 // merge in fp32 in a fixed order (thread, lanes, warps).  With p.select set,
 // the last row of each request then runs the request's top-W selection.
-// Shared memory stays small (about 8 KB + the selection's), so the blocks
-// fit beside the state step's contraction, which streams its operands
-// while this kernel runs.
+// Shared memory stays small (7.5 KB + the selection's).
 __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams p) {
   extern __shared__ uint64_t dyn[];  // the selection's keys
   __shared__ uint64_t wl[kMergeWarps][32];
