@@ -56,3 +56,21 @@ def test_kernel_source_hash_follows_code_not_comments():
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_build_bytes_match_the_closed_forms():
+    """Per-build algorithmic bytes D*V*H*wb + (D-1)*H*H*wb + gathered
+    embedding rows + base logits, at the five workloads (GB)."""
+    from speculative_decoding_draft_06_gb300 import inputs as I
+    want = {"tiny": 0.2650, "q4b": 12.6535, "q8b": 20.4296, "batch": 20.7605, "wide": 20.4352}
+    for name, gb in want.items():
+        w = I.CONFIGS[name]
+        wb = 2 if w.bf16 else 4
+        closed = (w.D * w.V * w.H * wb + (w.D - 1) * w.H * w.H * wb
+                  + sum(w.head_rows()[1:]) * w.H * wb + w.R * w.D * w.V * 4)
+        assert bench.build_bytes(w) == closed, name
+        assert abs(closed / 1e9 - gb) < 1e-3, name
+    # launches per build: root, D head calls, D merges, D-1 two-kernel state
+    # steps (one kernel in fp32), prune
+    assert bench.kernels_per_build(I.CONFIGS["q8b"]) == 1 + 16 + 16 + 2 * 15 + 1
+    assert bench.kernels_per_build(I.CONFIGS["tiny"]) == 1 + 8 + 8 + 7 + 1
