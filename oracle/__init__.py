@@ -63,8 +63,12 @@ def _load():
         lib.orc_pool_size.restype = ctypes.c_int
         lib.orc_build.argtypes = [ctypes.c_int] * 6 + [P] * 21
         lib.orc_build.restype = ctypes.c_int
-        lib.orc_build_ex.argtypes = [ctypes.c_int] * 7 + [P] * 21
+        lib.orc_build_ex.argtypes = [ctypes.c_int] * 7 + [P] * 22
         lib.orc_build_ex.restype = ctypes.c_int
+        lib.orc_depth.argtypes = [ctypes.c_int] * 7 + [P] * 19
+        lib.orc_depth.restype = ctypes.c_int
+        lib.orc_path_scores.argtypes = [ctypes.c_int, P, P, P]
+        lib.orc_path_scores.restype = ctypes.c_int
         lib.orc_cand_row.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int] + [P] * 4
         lib.orc_cand_row.restype = None
         lib.orc_bestfirst.argtypes = [ctypes.c_int] * 6 + [f32] + [P] * 21
@@ -171,7 +175,7 @@ def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
     o = {k: np.empty(P, np.int32) for k in
          ("pool_parent", "pool_token", "pool_depth", "own_slot", "own_tok")}
     o.update({k: np.empty(P, np.float32) for k in
-              ("pool_score", "own_score", "force_margin")})
+              ("pool_score", "pool_logp", "own_score", "force_margin")})
     o["row_lse"] = np.full(D * W, np.nan, np.float64)
     o["row_tok"] = np.full(D * W * K, -1, np.int32)
     o["row_logp"] = np.full(D * W * K, np.nan, np.float32)
@@ -186,7 +190,7 @@ def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
         V, H, D, W, K, int(bf16), int(cand_base), _ptr(z), _ptr(s0), _ptr(A), _ptr(E), _ptr(Wo),
         _ptr(fs), _ptr(ft), _ptr(fst),
         _ptr(o["pool_parent"]), _ptr(o["pool_token"]), _ptr(o["pool_depth"]),
-        _ptr(o["pool_score"]), _ptr(o["own_slot"]), _ptr(o["own_tok"]),
+        _ptr(o["pool_score"]), _ptr(o["pool_logp"]), _ptr(o["own_slot"]), _ptr(o["own_tok"]),
         _ptr(o["own_score"]), _ptr(o["force_margin"]), _ptr(o["row_lse"]),
         _ptr(o["row_tok"]), _ptr(o["row_logp"]), _ptr(o["row_kgap"]),
         _ptr(o["w_cut"]), _ptr(calls))
@@ -199,6 +203,53 @@ def build_tree(inp: dict, r: int, D: int, W: int, K: int, bf16: bool,
     o["w_cut"] = o["w_cut"].reshape(D, 2)
     o["calls"] = int(calls[0])
     return o
+
+
+def depth(z_d, Wout, states, score, W: int, K: int, bf16: bool, force_slot=None,
+          force_tok=None, cand_base: bool = False) -> dict:
+    """One depth of the construction from given frontier rows (see orc_depth):
+    ``states`` [fp, H] fp32 and cumulative ``score`` [fp]; optional forced
+    kept frontier ``force_slot`` / ``force_tok`` [fd].  Returns the per-row
+    head results, the own top-W, the kept frontier's scores and log-probs,
+    the forcing margins and the W-th / (W+1)-th candidate scores."""
+    Wo = _weights(Wout, bf16)
+    V, H = Wo.shape
+    z_d = _c(z_d, np.float32)
+    st = _c(states, np.float32)
+    sc = _c(score, np.float32)
+    fp = st.shape[0]
+    fd = min(W, K * fp)
+    o = {k: np.empty(fd, np.int32) for k in ("own_slot", "own_tok", "sel_slot", "sel_tok")}
+    o.update({k: np.empty(fd, np.float32) for k in
+              ("own_score", "sel_score", "sel_logp", "force_margin")})
+    o["row_lse"] = np.empty(fp, np.float64)
+    o["row_tok"] = np.empty((fp, K), np.int32)
+    o["row_logp"] = np.empty((fp, K), np.float32)
+    o["row_kgap"] = np.empty(fp, np.float32)
+    o["w_cut"] = np.empty(2, np.float32)
+    fs = ft = None
+    if force_slot is not None:
+        fs, ft = _c(force_slot, np.int32), _c(force_tok, np.int32)
+        assert fs.shape == (fd,) and ft.shape == (fd,)
+    rc = _load().orc_depth(
+        V, H, fp, W, K, int(bf16), int(cand_base), _ptr(z_d), _ptr(Wo), _ptr(st), _ptr(sc),
+        _ptr(fs), _ptr(ft), _ptr(o["own_slot"]), _ptr(o["own_tok"]), _ptr(o["own_score"]),
+        _ptr(o["sel_slot"]), _ptr(o["sel_tok"]), _ptr(o["sel_score"]), _ptr(o["sel_logp"]),
+        _ptr(o["force_margin"]), _ptr(o["row_lse"]), _ptr(o["row_tok"]), _ptr(o["row_logp"]),
+        _ptr(o["row_kgap"]), _ptr(o["w_cut"]))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_depth failed with code {rc}")
+    return o
+
+
+def path_scores(pool_parent, pool_logp) -> np.ndarray:
+    """Cumulative scores of a pool from each node's log-prob given its parent."""
+    pp, lp = _c(pool_parent, np.int32), _c(pool_logp, np.float32)
+    out = np.empty(pp.shape[0], np.float32)
+    rc = _load().orc_path_scores(pp.shape[0], _ptr(pp), _ptr(lp), _ptr(out))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_path_scores failed with code {rc}")
+    return out
 
 
 def topb(pool_parent, pool_token, pool_depth, pool_score, B: int, beta: float) -> dict:

@@ -231,6 +231,125 @@ int orc_pool_size(int D, int W, int K) {
 }
 
 /*
+ * One depth of the construction, callable on its own so that any depth of a
+ * build can be replayed from given frontier states and scores.
+ * [P1] Core Mechanism: the frontier's paths go through the head in ONE call;
+ * each is expanded by its top-k children, ranked by cumulative path
+ * log-probability; the W best survive.  [P2] Methodologie 1 and [P3] Summary:
+ * one global top-W over the depth's children.
+ *
+ * Inputs: fp frontier rows with head states st [fp][H] and cumulative scores
+ * score [fp]; the depth's base logits zd [V]; Wout [V,H] (bf16 bits or fp32).
+ * cand_base != 0 takes the candidates from the base logits (orc_cand_row);
+ * the row gap reported is then the base logits' K/K+1 gap, which alone
+ * decides the candidate set.
+ *   head call (one per depth): ell_i = corrected logits, lse_i, top-K of ell_i;
+ *   candidates: c_ij = score[i] + logp_ij (one fp32 add), index i*K + j;
+ *   own top-W : the first fd = min(W, fp*K) candidates by (c desc, index asc).
+ * The kept frontier is force_slot/force_tok [fd] when given (teacher
+ * forcing: slot in [0, fp), token in [0, V)), else the own top-W; the oracle
+ * scores forced nodes in its own arithmetic.
+ *
+ * Outputs: own_slot/own_tok/own_score [fd]; kept frontier sel_slot/sel_tok,
+ * sel_score (cumulative) and sel_logp (its log-prob given its parent) [fd];
+ * force_margin [fd] = ell(slot, tok) - ell_(K)(slot) for forced nodes, else 0;
+ * per row row_lse [fp], row_tok/row_logp [fp*K], row_kgap [fp]; w_cut [2] =
+ * own W-th and (W+1)-th candidate score (-inf if none).
+ */
+int orc_depth(int V, int H, int fp, int W, int K, int bf16, int cand_base,
+              const float *zd, const void *Wout, const float *st, const float *score,
+              const int32_t *force_slot, const int32_t *force_tok,
+              int32_t *own_slot, int32_t *own_tok, float *own_score,
+              int32_t *sel_slot, int32_t *sel_tok, float *sel_score, float *sel_logp,
+              float *force_margin, double *row_lse, int32_t *row_tok, float *row_logp,
+              float *row_kgap, float *w_cut) {
+    if (V < 1 || H < 1 || fp < 1 || W < 1 || K < 1 || K > V) return ORC_ERR_ARG;
+    int rc = ORC_OK;
+    const int fd = (K * fp < W) ? K * fp : W;
+    float *ell = malloc(sizeof(float) * (size_t)fp * V);     /* full rows */
+    cand_t *cand = malloc(sizeof(cand_t) * (size_t)fp * K);
+    float *kth = malloc(sizeof(float) * (size_t)fp);         /* K-th logit */
+    int32_t *tk = malloc(sizeof(int32_t) * (size_t)K);
+    float *tv = malloc(sizeof(float) * (size_t)K);
+    int32_t *ctok = malloc(sizeof(int32_t) * (size_t)K);    /* base candidates */
+    float *cval = malloc(sizeof(float) * (size_t)K);
+    if (!ell || !cand || !kth || !tk || !tv || !ctok || !cval) {
+        rc = ORC_ERR_MEM;
+        goto done;
+    }
+
+    float zgap = 0.0f;
+    if (cand_base) orc_topk_row(V, zd, K, ctok, cval, &zgap);
+    /* the batched head call over every frontier row */
+    for (int i = 0; i < fp; ++i) {
+        double lse;
+        float kgap;
+        if (cand_base) {
+            orc_cand_row(H, bf16, zd, Wout, st + (size_t)i * H, K, ctok, tk, tv, &lse);
+            for (int j = 0; j < K; ++j) ell[(size_t)i * V + tk[j]] = tv[j];
+            kgap = zgap;     /* the candidate set is decided by z alone */
+        } else {
+            orc_logits_row(V, H, bf16, zd, Wout, st + (size_t)i * H,
+                           ell + (size_t)i * V, &lse);
+            orc_topk_row(V, ell + (size_t)i * V, K, tk, tv, &kgap);
+        }
+        row_lse[i] = lse;
+        row_kgap[i] = kgap;
+        kth[i] = tv[K - 1];
+        for (int j = 0; j < K; ++j) {
+            float logp = (float)((double)tv[j] - lse);
+            row_tok[(size_t)i * K + j] = tk[j];
+            row_logp[(size_t)i * K + j] = logp;
+            cand[i * K + j].c = score[i] + logp;       /* one fp32 add */
+            cand[i * K + j].idx = i * K + j;
+        }
+    }
+    /* own global top-W over the fp*K candidates */
+    qsort(cand, (size_t)fp * K, sizeof(cand_t), cand_cmp);
+    for (int q = 0; q < fd; ++q) {
+        own_slot[q] = cand[q].idx / K;
+        own_tok[q] = row_tok[(size_t)own_slot[q] * K + cand[q].idx % K];
+        own_score[q] = cand[q].c;
+    }
+    w_cut[0] = cand[fd - 1].c;
+    w_cut[1] = (fp * K > fd) ? cand[fd].c : -INFINITY;
+
+    /* the frontier that is kept: forced or own */
+    for (int q = 0; q < fd; ++q) {
+        int32_t slot, tok;
+        if (force_slot) {
+            slot = force_slot[q];
+            tok = force_tok[q];
+            if (slot < 0 || slot >= fp || tok < 0 || tok >= V) {
+                rc = ORC_ERR_ARG;
+                goto done;
+            }
+            if (cand_base) {              /* only a candidate can be kept */
+                int in = 0;
+                for (int j = 0; j < K; ++j) in |= (ctok[j] == tok);
+                if (!in) { rc = ORC_ERR_ARG; goto done; }
+            }
+            float e = ell[(size_t)slot * V + tok];
+            sel_logp[q] = (float)((double)e - row_lse[slot]);
+            sel_score[q] = score[slot] + sel_logp[q];
+            force_margin[q] = cand_base ? 0.0f : e - kth[slot];
+        } else {
+            slot = own_slot[q];
+            tok = own_tok[q];
+            sel_score[q] = own_score[q];
+            sel_logp[q] = row_logp[(size_t)slot * K + cand[q].idx % K];
+            force_margin[q] = 0.0f;
+        }
+        sel_slot[q] = slot;
+        sel_tok[q] = tok;
+    }
+
+done:
+    free(ell); free(cand); free(kth); free(tk); free(tv); free(ctok); free(cval);
+    return rc;
+}
+
+/*
  * Depth-wise batched construction of the supertree for one request.
  * [P1] Core Mechanism: at depth d the W surviving paths go through the head
  * in ONE call; each is expanded by its top-k children (W*k candidates),
@@ -242,9 +361,7 @@ int orc_pool_size(int D, int W, int K) {
  * Inputs: z [D,V] fp32, state0 [H] fp32, A [H,H], E [V,H], Wout [V,H]
  * (bf16 bits or fp32).  Depth 1 has |F_1| = min(W, K) nodes.
  * A == NULL selects the Markov head (see orc_state_step).  cand_base != 0
- * takes each depth's candidates from the base logits (orc_cand_row); the
- * row gap reported is then the base logits' K/K+1 gap, which alone decides
- * the candidate set.
+ * takes each depth's candidates from the base logits (see orc_depth).
  *
  * Teacher forcing: when force_slot/force_tok are given ([P] each, laid out
  * like the pool), the frontier kept at each depth is the forced one (parent
@@ -257,7 +374,8 @@ int orc_pool_size(int D, int W, int K) {
  *
  * Outputs ([P] = pool size, rows = W per depth):
  *   pool_parent/token/depth/score [P]: the pool that was kept, pool index =
- *       depth-major, rank order within a depth; parent -1 at depth 1.
+ *       depth-major, rank order within a depth; parent -1 at depth 1;
+ *       pool_logp [P] (may be NULL): each kept node's log-prob given its parent.
  *   own_slot/own_tok/own_score [P]: the oracle's own top-W at each depth
  *       given the kept previous frontier.
  *   force_margin [P]: for kept nodes, ell(parent,tok) - ell_(K)(parent).
@@ -271,7 +389,7 @@ int orc_build_ex(int V, int H, int D, int W, int K, int bf16, int cand_base,
                  const int32_t *force_slot, const int32_t *force_tok,
                  const float *force_state,
                  int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
-                 float *pool_score,
+                 float *pool_score, float *pool_logp,
                  int32_t *own_slot, int32_t *own_tok, float *own_score,
                  float *force_margin,
                  double *row_lse, int32_t *row_tok, float *row_logp,
@@ -280,19 +398,12 @@ int orc_build_ex(int V, int H, int D, int W, int K, int bf16, int cand_base,
     int rc = ORC_OK;
     float *st = malloc(sizeof(float) * (size_t)W * H);      /* row states */
     float *st_next = malloc(sizeof(float) * (size_t)W * H);
-    float *ell = malloc(sizeof(float) * (size_t)W * V);      /* full rows */
     float *score = malloc(sizeof(float) * (size_t)W);        /* row scores */
     int32_t *sel_slot = malloc(sizeof(int32_t) * (size_t)W);
     int32_t *sel_tok = malloc(sizeof(int32_t) * (size_t)W);
     float *sel_score = malloc(sizeof(float) * (size_t)W);
-    cand_t *cand = malloc(sizeof(cand_t) * (size_t)W * K);
-    float *kth = malloc(sizeof(float) * (size_t)W);          /* K-th logit */
-    int32_t *tk = malloc(sizeof(int32_t) * (size_t)K);
-    float *tv = malloc(sizeof(float) * (size_t)K);
-    int32_t *ctok = malloc(sizeof(int32_t) * (size_t)K);    /* base candidates */
-    float *cval = malloc(sizeof(float) * (size_t)K);
-    if (!st || !st_next || !ell || !score || !sel_slot || !sel_tok ||
-        !sel_score || !cand || !kth || !tk || !tv || !ctok || !cval) {
+    float *sel_logp = malloc(sizeof(float) * (size_t)W);
+    if (!st || !st_next || !score || !sel_slot || !sel_tok || !sel_score || !sel_logp) {
         rc = ORC_ERR_MEM;
         goto done;
     }
@@ -303,82 +414,24 @@ int orc_build_ex(int V, int H, int D, int W, int K, int bf16, int cand_base,
     score[0] = 0.0f;
 
     for (int d = 1; d <= D; ++d) {
-        const float *zd = z + (size_t)(d - 1) * V;
         int fd = (K * fp < W) ? K * fp : W;
         if (force_state)
             memcpy(st, force_state + (size_t)(d - 1) * W * H, sizeof(float) * (size_t)fp * H);
-        float zgap = 0.0f;
-        if (cand_base) orc_topk_row(V, zd, K, ctok, cval, &zgap);
-        /* one batched head call over every frontier row */
-        *calls += 1;
-        for (int i = 0; i < fp; ++i) {
-            double lse;
-            float kgap;
-            if (cand_base) {
-                orc_cand_row(H, bf16, zd, Wout, st + (size_t)i * H, K, ctok, tk, tv, &lse);
-                for (int j = 0; j < K; ++j) ell[(size_t)i * V + tk[j]] = tv[j];
-                kgap = zgap;     /* the candidate set is decided by z alone */
-            } else {
-                orc_logits_row(V, H, bf16, zd, Wout, st + (size_t)i * H,
-                               ell + (size_t)i * V, &lse);
-                orc_topk_row(V, ell + (size_t)i * V, K, tk, tv, &kgap);
-            }
-            size_t r = (size_t)(d - 1) * W + i;
-            row_lse[r] = lse;
-            row_kgap[r] = kgap;
-            kth[i] = tv[K - 1];
-            for (int j = 0; j < K; ++j) {
-                float logp = (float)((double)tv[j] - lse);
-                row_tok[r * K + j] = tk[j];
-                row_logp[r * K + j] = logp;
-                cand[i * K + j].c = score[i] + logp;       /* one fp32 add */
-                cand[i * K + j].idx = i * K + j;
-            }
-        }
-        /* own global top-W over the fp*K candidates */
-        qsort(cand, (size_t)fp * K, sizeof(cand_t), cand_cmp);
+        *calls += 1;                   /* one batched head call per depth */
+        size_t r0 = (size_t)(d - 1) * W;
+        rc = orc_depth(V, H, fp, W, K, bf16, cand_base, z + (size_t)(d - 1) * V, Wout, st,
+                       score, force_slot ? force_slot + off : NULL,
+                       force_tok ? force_tok + off : NULL, own_slot + off, own_tok + off,
+                       own_score + off, sel_slot, sel_tok, sel_score, sel_logp,
+                       force_margin + off, row_lse + r0, row_tok + r0 * K, row_logp + r0 * K,
+                       row_kgap + r0, w_cut + 2 * (d - 1));
+        if (rc != ORC_OK) goto done;
         for (int q = 0; q < fd; ++q) {
-            own_slot[off + q] = cand[q].idx / K;
-            int j = cand[q].idx % K;
-            size_t r = (size_t)(d - 1) * W + own_slot[off + q];
-            own_tok[off + q] = row_tok[r * K + j];
-            own_score[off + q] = cand[q].c;
-        }
-        w_cut[2 * (d - 1)] = cand[fd - 1].c;
-        w_cut[2 * (d - 1) + 1] = (fp * K > fd) ? cand[fd].c : -INFINITY;
-
-        /* the frontier that is kept: forced or own */
-        for (int q = 0; q < fd; ++q) {
-            int32_t slot, tok;
-            if (force_slot) {
-                slot = force_slot[off + q];
-                tok = force_tok[off + q];
-                if (slot < 0 || slot >= fp || tok < 0 || tok >= V) {
-                    rc = ORC_ERR_ARG;
-                    goto done;
-                }
-                size_t r = (size_t)(d - 1) * W + slot;
-                if (cand_base) {              /* only a candidate can be kept */
-                    int in = 0;
-                    for (int j = 0; j < K; ++j) in |= (ctok[j] == tok);
-                    if (!in) { rc = ORC_ERR_ARG; goto done; }
-                }
-                float e = ell[(size_t)slot * V + tok];
-                float logp = (float)((double)e - row_lse[r]);
-                sel_score[q] = score[slot] + logp;
-                force_margin[off + q] = cand_base ? 0.0f : e - kth[slot];
-            } else {
-                slot = own_slot[off + q];
-                tok = own_tok[off + q];
-                sel_score[q] = own_score[off + q];
-                force_margin[off + q] = 0.0f;
-            }
-            sel_slot[q] = slot;
-            sel_tok[q] = tok;
-            pool_parent[off + q] = (d == 1) ? -1 : off_prev + slot;
-            pool_token[off + q] = tok;
+            pool_parent[off + q] = (d == 1) ? -1 : off_prev + sel_slot[q];
+            pool_token[off + q] = sel_tok[q];
             pool_depth[off + q] = d;
             pool_score[off + q] = sel_score[q];
+            if (pool_logp) pool_logp[off + q] = sel_logp[q];
         }
         /* carry the correction states forward to the kept nodes */
         if (d < D) {
@@ -394,10 +447,23 @@ int orc_build_ex(int V, int H, int D, int W, int K, int bf16, int cand_base,
     }
 
 done:
-    free(st); free(st_next); free(ell); free(score); free(sel_slot);
-    free(sel_tok); free(sel_score); free(cand); free(kth); free(tk); free(tv);
-    free(ctok); free(cval);
+    free(st); free(st_next); free(score); free(sel_slot); free(sel_tok);
+    free(sel_score); free(sel_logp);
     return rc;
+}
+
+/* Cumulative path scores of a pool from each node's log-prob given its parent:
+ * score[n] = score[parent[n]] + logp[n] (one fp32 add), 0 + logp[n] at depth 1
+ * (parent -1).  Parents precede their children in pool order.  Returns
+ * ORC_ERR_ORDER if a parent index is not below its child's.
+ * [P1] Core Mechanism (children ranked by accumulated path log-probability). */
+int orc_path_scores(int P, const int32_t *parent, const float *logp, float *score) {
+    for (int n = 0; n < P; ++n) {
+        int32_t p = parent[n];
+        if (p >= n) return ORC_ERR_ORDER;
+        score[n] = (p < 0 ? 0.0f : score[p]) + logp[n];
+    }
+    return ORC_OK;
 }
 
 /* The construction with the candidates of [P1] (top-K of each branch's
@@ -415,7 +481,7 @@ int orc_build(int V, int H, int D, int W, int K, int bf16,
               float *row_kgap, float *w_cut, int64_t *calls) {
     return orc_build_ex(V, H, D, W, K, bf16, 0, z, state0, A, E, Wout,
                         force_slot, force_tok, force_state, pool_parent,
-                        pool_token, pool_depth, pool_score, own_slot, own_tok,
+                        pool_token, pool_depth, pool_score, NULL, own_slot, own_tok,
                         own_score, force_margin, row_lse, row_tok, row_logp,
                         row_kgap, w_cut, calls);
 }

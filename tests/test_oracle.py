@@ -430,6 +430,98 @@ def test_teacher_forcing_scores_an_off_beam_choice():
     assert b["force_margin"][1] < 0
 
 
+# ------------------------------------------------ one depth on its own
+
+@pytest.mark.parametrize("bf16,cand_base", [(False, False), (True, False), (True, True)])
+def test_depth_replays_every_depth_of_a_build(bf16, cand_base):
+    """orc_depth called alone, with a depth's input states and the previous
+    frontier's scores, gives bit for bit what that depth gave inside the
+    build (the build is pinned by brute force above)."""
+    w = I.small_workload(810 + 2 * bf16 + cand_base, V=150, H=16, D=4, W=5, K=3, B=9,
+                         bf16=bf16)
+    inp = I.make_inputs(w)
+    g = np.random.default_rng(3)
+    st = np.tanh(g.standard_normal((w.D, w.W, w.H))).astype(np.float32)
+    st = bf.q(st, bf16)
+    a = oracle.build_tree(inp, 0, w.D, w.W, w.K, bf16, force_state=st, cand_base=cand_base)
+    sizes, off, F, prev = w.frontier_sizes(), 0, 1, np.zeros(1, np.float32)
+    for d in range(1, w.D + 1):
+        fd = sizes[d - 1]
+        o = oracle.depth(inp["z"][0, d - 1], inp["Wout"], st[d - 1, :F], prev, w.W, w.K, bf16,
+                         cand_base=cand_base)
+        sl = slice(off, off + fd)
+        for k in ("own_slot", "own_tok", "own_score"):
+            assert np.array_equal(o[k], a[k][sl]), (d, k)
+        assert np.array_equal(o["sel_score"], a["pool_score"][sl])
+        assert np.array_equal(o["sel_logp"], a["pool_logp"][sl])
+        assert np.array_equal(o["row_lse"], a["row_lse"][d - 1, :F])
+        assert np.array_equal(o["row_tok"], a["row_tok"][d - 1, :F])
+        assert np.array_equal(o["row_logp"], a["row_logp"][d - 1, :F])
+        assert np.array_equal(o["w_cut"], a["w_cut"][d - 1])
+        prev, off, F = o["sel_score"], off + fd, fd
+
+
+def test_depth_from_given_rows_equals_bruteforce():
+    """Arbitrary frontier states and scores: the rows are the brute-force
+    head's top-K children, the own top-W is the best fd of all F*K
+    candidates score_i + logp_ij (fp32), ties on the lower index."""
+    V, H, K, W, F = 70, 8, 4, 6, 3
+    w = I.small_workload(820, V=V, H=H, D=2, W=W, K=K, B=4, bf16=False)
+    inp = I.make_inputs(w)
+    head = bf.Head(inp, 0, False)
+    g = np.random.default_rng(9)
+    st = np.tanh(g.standard_normal((F, H))).astype(np.float32)
+    score = (-np.abs(g.standard_normal(F)) * 3).astype(np.float32)
+    o = oracle.depth(inp["z"][0, 1], inp["Wout"], st, score, W, K, False)
+    cands = []
+    for i in range(F):
+        ch = head.children(st[i], 2, K)
+        assert [t for t, _ in ch] == o["row_tok"][i].tolist()
+        assert np.allclose([lp for _, lp in ch], o["row_logp"][i], atol=1e-6, rtol=0)
+        cands += [(np.float32(score[i] + lp), i * K + j, t) for j, (t, lp) in enumerate(ch)]
+    best = sorted(cands, key=lambda c: (-float(c[0]), c[1]))
+    fd = min(W, F * K)
+    assert o["own_slot"].tolist() == [c[1] // K for c in best[:fd]]
+    assert o["own_tok"].tolist() == [c[2] for c in best[:fd]]
+    assert np.allclose(o["own_score"], [c[0] for c in best[:fd]], atol=2e-6, rtol=0)
+    assert abs(o["w_cut"][1] - best[fd][0]) <= 2e-6
+    # no forcing: the kept frontier is the own one, log-probs as in the rows
+    assert np.array_equal(o["sel_slot"], o["own_slot"])
+    for q in range(fd):
+        j = o["row_tok"][o["sel_slot"][q]].tolist().index(o["sel_tok"][q])
+        assert o["sel_logp"][q] == o["row_logp"][o["sel_slot"][q], j]
+    # a forced frontier is scored from the given scores
+    fs = np.array([2, 0, 1, 2, 0, 1], np.int32)
+    ft = np.array([int(o["row_tok"][s_, 1]) for s_ in fs], np.int32)
+    f = oracle.depth(inp["z"][0, 1], inp["Wout"], st, score, W, K, False, force_slot=fs,
+                     force_tok=ft)
+    for q in range(fd):
+        assert f["sel_score"][q] == np.float32(score[fs[q]] + o["row_logp"][fs[q], 1])
+        assert f["force_margin"][q] >= 0
+
+
+def test_path_scores_are_per_path_fp32_sums():
+    g = np.random.default_rng(4)
+    P = 60
+    parent = np.array([-1 if n < 3 or g.random() < 0.1 else int(g.integers(0, n))
+                       for n in range(P)], np.int32)
+    logp = (-np.abs(g.standard_normal(P)) * 2).astype(np.float32)
+    got = oracle.path_scores(parent, logp)
+    for n in range(P):
+        path, u = [], n
+        while u >= 0:
+            path.append(u)
+            u = int(parent[u])
+        s_ = np.float32(0.0)
+        for u in reversed(path):                 # root side first
+            s_ = np.float32(s_ + logp[u])
+        assert got[n] == s_, n
+    bad = parent.copy()
+    bad[5] = 7
+    with pytest.raises(RuntimeError):
+        oracle.path_scores(bad, logp)
+
+
 # ------------------------------------------- the weather / storm example
 
 def _weather_inputs(zero_wout=False):
