@@ -244,17 +244,65 @@ class ClockSampler:
 
 # -------------------------------------------------------------- CPU oracle
 
+def host_info() -> dict:
+    """Host cores and CPU model of the machine the oracle is timed on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model}
+
+
+class PinnedCore:
+    """Runs the enclosed oracle work on one core (the calling thread's
+    affinity), restoring the previous affinity afterwards."""
+
+    def __init__(self):
+        self.core = None
+        self.prev = None
+
+    def __enter__(self):
+        try:
+            self.prev = os.sched_getaffinity(0)
+            self.core = max(self.prev)           # the last allowed core
+            os.sched_setaffinity(0, {self.core})
+        except (AttributeError, OSError):
+            self.core = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            try:
+                os.sched_setaffinity(0, self.prev)
+            except OSError:
+                pass
+        return False
+
+
 def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0,
                   variant: str = "dartree") -> dict:
-    """Time the CPU oracle on a bounded sample of one request's build and
-    scale to a full build by head rows (the dominant cost is one V x H fp64
-    pass per head row).  The sample is the first depths of the build when at
-    least one head row fits in budget_s, else one head row restricted to a
-    vocabulary slice, scaled by V / slice.  Best-first: one head row per
-    call, B calls.  Base candidates: the first depths of the variant's own
-    oracle build, scaled by depths."""
-    import numpy as np
+    """Time the CPU oracle on a bounded sample of one request's build.
 
+    Returns the measured seconds, the fraction of one build the sample
+    covers and builds/s = fraction / seconds.  The sample is the whole build
+    when it fits in budget_s (then nothing is extrapolated), else the first
+    depths of the build (fraction = their head rows over the build's: the
+    dominant cost is one V x H fp64 pass per head row), else one head row
+    restricted to a vocabulary slice.  Best-first: a build with fewer calls.
+    Base candidates: the first depths of the variant's own oracle build."""
     import oracle
     opt = VARIANTS[variant]
     markov = opt.get("head") == "markov"
@@ -266,10 +314,11 @@ def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0,
             oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16, markov=markov,
                               cand_base=True)
             t = time.perf_counter() - t0
-        per_build = t * w.D / d_s
-        return {"builds_per_s": 1.0 / per_build, "seconds": t,
+        frac = d_s / w.D
+        return {"seconds": t, "fraction": frac, "builds_per_s": frac / t,
+                "extrapolated": d_s < w.D,
                 "sample": (f"oracle (fp64, 1 thread), base-candidate build of depths 1..{d_s} "
-                           f"of request {request} ({t:.2f} s), scaled by depths")}
+                           f"of {w.D} of request {request} ({t:.2f} s)")}
     if opt.get("expansion") == "bestfirst":
         rows = [1] * w.B
     else:
@@ -285,32 +334,59 @@ def oracle_sample(w: I.Workload, inp: dict, budget_s: float, request: int = 0,
         t0 = time.perf_counter()
         oracle.logits_row(inp["z"][request, 0, :vs], inp["Wout"][:vs], s0, w.bf16)
         t = time.perf_counter() - t0
-        per_build = t * (w.V / vs) * total_rows
-        return {"builds_per_s": 1.0 / per_build, "seconds": t,
+        frac = vs / w.V / total_rows
+        return {"seconds": t, "fraction": frac, "builds_per_s": frac / t, "extrapolated": True,
                 "sample": (f"oracle (fp64, 1 thread): one head row over {vs} of {w.V} "
-                           f"vocabulary entries ({t:.2f} s), scaled by V/{vs} and "
-                           f"{total_rows} head rows per build")}
+                           f"vocabulary entries ({t:.2f} s) = {frac:.2e} of a build of "
+                           f"{total_rows} head rows")}
     if opt.get("expansion") == "bestfirst":
         n = max(1, min(w.B, int(budget_s / t_row)))
         t0 = time.perf_counter()
         o = oracle.bestfirst(inp, request, w.D, w.K, n, w.beta, w.bf16, markov=markov)
         t = time.perf_counter() - t0
-        per_build = t * w.B / o["calls"]
-        return {"builds_per_s": 1.0 / per_build, "seconds": t,
+        frac = o["calls"] / w.B
+        return {"seconds": t, "fraction": frac, "builds_per_s": frac / t,
+                "extrapolated": n < w.B,
                 "sample": (f"oracle (fp64, 1 thread): best-first build with budget {n} of "
-                           f"request {request} ({o['calls']} head calls, {t:.1f} s), scaled "
-                           f"to {w.B} calls")}
+                           f"{w.B}, request {request} ({o['calls']} head calls, {t:.1f} s)")}
     d_s, acc = 1, rows[0]
     while d_s < w.D and (acc + rows[d_s]) * t_row <= budget_s:
         acc += rows[d_s]
         d_s += 1
     t0 = time.perf_counter()
-    oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16, markov=markov)
+    if d_s == w.D:
+        oracle.build_request(inp, request, w.D, w.W, w.K, w.B, w.beta, w.bf16)
+    else:
+        oracle.build_tree(inp, request, d_s, w.W, w.K, w.bf16, markov=markov)
     t = time.perf_counter() - t0
-    per_build = t * total_rows / acc
-    return {"builds_per_s": 1.0 / per_build, "seconds": t,
-            "sample": (f"oracle (fp64, 1 thread) on depths 1..{d_s} of request {request} "
-                       f"({acc} of {total_rows} head rows, {t:.1f} s), scaled by head rows")}
+    frac = acc / total_rows
+    whole = d_s == w.D
+    return {"seconds": t, "fraction": frac, "builds_per_s": frac / t, "extrapolated": not whole,
+            "sample": (f"oracle (fp64, 1 thread): the whole build of request {request} incl. "
+                       f"Top-B and mask ({t:.2f} s)" if whole else
+                       f"oracle (fp64, 1 thread) on depths 1..{d_s} of {w.D} of request "
+                       f"{request} ({acc} of {total_rows} head rows, {t:.1f} s)")}
+
+
+def cpu_baseline(w: I.Workload, inp: dict, budget_s: float, variant: str) -> dict:
+    """The oracle on one pinned host core: a bounded sample of this workload,
+    plus (for other workloads) one whole tiny build timed directly."""
+    info = host_info()
+    with PinnedCore() as pc:
+        s = oracle_sample(w, inp, budget_s, variant=variant)
+        direct = None
+        if w.name != "tiny" or s["extrapolated"]:
+            import oracle
+            t = I.CONFIGS["tiny"]
+            ti = I.make_inputs(t)
+            t0 = time.perf_counter()
+            oracle.build_request(ti, 0, t.D, t.W, t.K, t.B, t.beta, t.bf16)
+            sec = time.perf_counter() - t0
+            direct = {"workload": "tiny", "seconds": sec, "builds_per_s": 1.0 / sec}
+    return {"value": s["builds_per_s"], "unit": "builds/s", "cores": 1, "kind": "oracle",
+            "sample": s["sample"], "extrapolated": s["extrapolated"],
+            "sample_seconds": s["seconds"], "sample_build_fraction": s["fraction"],
+            "pinned_core": pc.core, **info, "direct_full_build": direct}
 
 
 # -------------------------------------------------------------- reference arm
@@ -322,19 +398,26 @@ def run_reference(args) -> None:
     w = I.CONFIGS[args.config]
     inp = I.make_inputs(w)
     budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        oracle_sample(w, inp, budget, variant=args.variant)
-    vals = [oracle_sample(w, inp, budget, variant=args.variant) for _ in range(args.steps)]
-    per_build = statistics.mean(1.0 / v["builds_per_s"] for v in vals)
-    value = 1.0 / per_build
+    info = host_info()
+    with PinnedCore() as pc:
+        for _ in range(args.warmup):
+            oracle_sample(w, inp, budget, variant=args.variant)
+        vals = [oracle_sample(w, inp, budget, variant=args.variant) for _ in range(args.steps)]
+    sec = sum(v["seconds"] for v in vals)
+    frac = sum(v["fraction"] for v in vals)
+    value = frac / sec                   # builds of work done per second of oracle time
     line = {
         "impl": "reference", "metric": "supertree builds/s", "value": value,
         "unit": "builds/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_build * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": sec / len(vals) * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w), "variant": args.variant,
+        "step": (f"a bounded sample of the workload: {frac / len(vals):.3g} of one build per "
+                 f"step (measured seconds; value = build fraction / seconds)"),
         "cpu_baseline": {"value": value, "unit": "builds/s", "cores": 1, "kind": "oracle",
-                         "sample": vals[-1]["sample"]},
+                         "sample": vals[-1]["sample"],
+                         "extrapolated": any(v["extrapolated"] for v in vals),
+                         "pinned_core": pc.core, **info},
         "e2e": {"value": value, "unit": "builds/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -429,6 +512,10 @@ def run_gpu(args) -> None:
     bytes_launch = kernel_bytes_per_launch(w, args.variant, kind)
     achieved = bytes_launch / (head_avg_ms * 1e-3) / 1e9
     traffic = profiled_traffic(args.config) if args.variant == "dartree" else None
+    traffic_source = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum per head launch, "
+                      f"profiles/head_logits_{args.config}.md @ kernel_source_hash "
+                      f"{kernel_source_hash()}" if traffic is not None else
+                      "none: no ncu capture on the current kernel sources for this workload")
     big = [m for m in w.head_rows() if m >= ROWS_MIN]
     kernel_name = {
         "head": ("k_cand_logits (candidate logits)" if opt.get("candidates") == "base" else
@@ -490,9 +577,7 @@ def run_gpu(args) -> None:
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        s = oracle_sample(w, inp, args.cpu_budget, variant=args.variant)
-        cpu = {"value": s["builds_per_s"], "unit": "builds/s", "cores": 1, "kind": "oracle",
-               "sample": s["sample"]}
+        cpu = cpu_baseline(w, inp, args.cpu_budget, args.variant)
 
     if rank == 0:
         line = {
@@ -509,8 +594,8 @@ def run_gpu(args) -> None:
             "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": traffic, "bytes_per_launch": bytes_launch,
-                         "launch_ms": head_avg_ms},
+                         "traffic": traffic, "traffic_source": traffic_source,
+                         "bytes_per_launch": bytes_launch, "launch_ms": head_avg_ms},
             "kernel_ms_per_build": {k: v[0] / max(1, min(args.steps, 50)) for k, v in kt.items()},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": kernels_per_build(w, args.variant) * args.steps,

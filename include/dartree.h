@@ -123,7 +123,8 @@ void dartree_destroy(dartree_ctx *ctx);
  *   base_logits [R, D, V] fp32 : drafter logits z_d per request and depth.
  *   state0      [R, H]    fp32 : head state at each request's prefix.
  *   Requires 1 <= D, W, K, B, R within the context's limits, K <= V,
- *   beta <= 0 (Lemma 1 needs a non-positive depth bonus).
+ *   beta <= 0 (Lemma 1 needs a non-positive depth bonus), and with bf16
+ *   weights A, E and Wout 16-byte aligned (INVALID_ARG otherwise).
  * Runs D batched head calls (dartree_head_calls() reports them), then the
  * deferred Top-B and the mask; writes `out`.  Asynchronous; never allocates
  * device memory.  On a created stream (not the legacy NULL stream, not one
@@ -200,8 +201,13 @@ dartree_status dartree_build_host(dartree_ctx *ctx, const float *base_logits_hos
  * OK, DEVICE_CHECK or TIMEOUT (or CUDA if the synchronisation failed).  After
  * a device error it also resets the context's arrival counters, so the
  * context can be used again; the failed build's outputs are undefined.
- * Test knob: DARTREE_WAIT_LIMIT_CYCLES (read at dartree_create) shortens the
- * kernels' pipeline waits to provoke the TIMEOUT path. */
+ * With ctx == NULL it reports the context-free state step instead
+ * (dartree_state_step_noalloc on the current device): the flags its calls
+ * gathered since the last such report, cleared on read; OK when no call has
+ * run on the device (reason text in dartree_last_error(NULL)).
+ * Test knob: DARTREE_WAIT_LIMIT_CYCLES (read at dartree_create, and at every
+ * dartree_state_step_noalloc call) shortens the kernels' pipeline waits to
+ * provoke the TIMEOUT path. */
 dartree_status dartree_sync_status(dartree_ctx *ctx, void *stream);
 
 /* Number of head calls made by the last build: D for a depth-wise build,
@@ -262,7 +268,8 @@ dartree_status dartree_head_topk(dartree_ctx *ctx, const void *S, const float *z
 
 /* Head state step for M rows: S_out[m] = q(tanh(A S_par[m] + E[tok[m]])).
  * S_par, S_out [M, H] in the context dtype; tok [M] int32 in [0, V).
- * M <= 256.  Asynchronous. */
+ * M <= 256; bf16 A and E 16-byte aligned (INVALID_ARG otherwise).
+ * Asynchronous. */
 dartree_status dartree_state_step(dartree_ctx *ctx, const void *S_par, const int32_t *tok,
                                   const void *A, const void *E, int32_t M, void *S_out,
                                   void *stream);
@@ -284,8 +291,8 @@ dartree_status dartree_prune(dartree_ctx *ctx, const int32_t *pool_parent,
  * convenience.
  *   Computes S_out[m] = bf16(tanh(A S_par[m] + E[tok[m]])) for m < M, like
  *   dartree_state_step, with bf16 weights: S_par, S_out [M, H] bf16 bits,
- *   tok [M] int32 in [0, V), A [H, H], E [V, H] bf16 bits (A 16-byte
- *   aligned).  Device pointers; asynchronous on `stream`.
+ *   tok [M] int32 in [0, V), A [H, H], E [V, H] bf16 bits (A and E 16-byte
+ *   aligned, else INVALID_ARG).  Device pointers; asynchronous on `stream`.
  *   Limits: M <= 256, H <= 4096 and H % 64 == 0; larger sizes return
  *   DARTREE_ERR_UNSUPPORTED (reason in dartree_last_error(NULL)) and launch
  *   nothing.
@@ -294,7 +301,13 @@ dartree_status dartree_prune(dartree_ctx *ctx, const int32_t *pool_parent,
  *   call on a device sets that device up (symbol lookup, a small synchronous
  *   copy): make it before any stream capture.  All calls share the scratch,
  *   so calls that overlap on the GPU race; order them on one stream.  Each
- *   call clears the scratch it needs zeroed. */
+ *   call zeroes only the padding rows of its staging array (rows M up to
+ *   the MMA's padded row count); every other scratch byte it reads was
+ *   written earlier in the same call.
+ *   Device checks (a pipeline wait that ran out, a bad index) gather in a
+ *   per-device word until dartree_sync_status(NULL, stream) synchronises,
+ *   reports them as TIMEOUT / DEVICE_CHECK and clears the word; S_out of a
+ *   call that failed is undefined. */
 dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok, const void *A,
                                           const void *E, int32_t H, int32_t M, void *S_out,
                                           void *stream);

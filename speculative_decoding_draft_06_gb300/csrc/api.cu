@@ -74,6 +74,9 @@ struct dartree_ctx {
   bool pdl = true;         // programmatic dependent launch between the kernels of a build
   long long wait_limit = 0;  // test knob: pipeline wait limit in cycles (0: full)
   bool use_graph = true;   // capture each build shape once into a CUDA graph
+  bool head_alternate = false;  // consecutive head calls walk Wout in opposite directions
+  bool keep_A = false;     // the state step's A stays in L2 between depths (evict last)
+  int head_dir = 0;        // direction of the next head call (set per call of a build)
 
   // the captured build and the arguments it was captured with
   struct GraphKey {
@@ -272,6 +275,7 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.list_stride = c->max_cta;
   p.pdl = c->pdl;
   p.wait_limit = c->wait_limit;
+  p.reverse = c->head_dir;
   int grid;
   cudaError_t e;
   {
@@ -377,6 +381,7 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
     p.n_split = c->state_split;
     p.part = c->part;
     p.early_operands = early && c->pdl;
+    p.keep_w = c->keep_A;
     e = dt::launch_head_tc(N, false, c->tm_A, c->tmS(src, N), p,
                            p.n_tiles * p.n_split, st);
     if (e == cudaSuccess && p.n_split > 1) {
@@ -513,6 +518,9 @@ dartree_status check_build_args(dartree_ctx* c, const void* z, const void* s0,
   if (K > g.V) return c->fail(DARTREE_ERR_INVALID_ARG, "K=%d exceeds V=%d", K, g.V);
   if (B < 1 || B > g.max_B) return c->fail(DARTREE_ERR_INVALID_ARG, "B=%d out of [1,%d]", B, g.max_B);
   if (!(beta <= 0.0f)) return c->fail(DARTREE_ERR_INVALID_ARG, "beta must be <= 0 (Lemma 1)");
+  // the state finish reads bf16 embedding rows with 8-byte loads
+  if (c->bf16 && (reinterpret_cast<uintptr_t>(head->E) & 15))
+    return c->fail(DARTREE_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
   const int rows = o.expansion == DARTREE_EXPAND_BESTFIRST ? R : R * W;  // head rows per call
   if (rows > dt::kMaxRows) return c->fail(DARTREE_ERR_UNSUPPORTED, "%d head rows > 256", rows);
   // the vocabulary-on-M head kernel (fewer than rows_min rows) keeps its
@@ -611,10 +619,13 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
                    c->cand + static_cast<size_t>(d - 1) * K, static_cast<long long>(D) * K, F, M,
                    K, head->Wout, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K,
                    &sel, st);
-    else
+    else {
+      c->head_dir = c->head_alternate ? (d - 1) & 1 : 0;
       s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
                    F, M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel,
                    st);
+      c->head_dir = 0;
+    }
     if (s != DARTREE_OK) return s;
     ++calls;
     cur ^= 1;
@@ -734,8 +745,10 @@ dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
     }
     const int sbuf = call == 0 ? 0 : 2;
     const size_t ro = static_cast<size_t>(call) * c->cfg.max_requests;
+    c->head_dir = c->head_alternate ? call & 1 : 0;
     s = run_head(c, sbuf, c->bf_z, V, 1, R, K, c->bf_lse + ro, c->bf_rtok + ro * K,
                  c->bf_rlogp + ro * K, nullptr, st);
+    c->head_dir = 0;
     if (s != DARTREE_OK) return s;
     bp.row_tok = c->bf_rtok + ro * K;
     bp.row_logp = c->bf_rlogp + ro * K;
@@ -901,6 +914,8 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_PDL")) c->pdl = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_WAIT_LIMIT_CYCLES")) c->wait_limit = atoll(v);
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_HEAD_ALTERNATE")) c->head_alternate = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_KEEP_A")) c->keep_A = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;
@@ -1044,8 +1059,27 @@ dartree_status dartree_build_ex(dartree_ctx* ctx, const float* base_logits, cons
 }
 
 dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
-  if (!ctx) return DARTREE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!ctx) {  // the context-free state step's check word on this device
+    cudaError_t e = cudaSuccess;
+    const int h = dt::noalloc_take_status(st, &e);
+    if (e != cudaSuccess) {
+      dt::set_context_free_error(std::string("status read: ") + cudaGetErrorString(e));
+      return DARTREE_ERR_CUDA;
+    }
+    char msg[96];
+    if (h > 0 && (h & dt::DT_ERR_TIMEOUT)) {
+      snprintf(msg, sizeof msg, "device wait timed out (flags 0x%x)", h);
+      dt::set_context_free_error(msg);
+      return DARTREE_ERR_TIMEOUT;
+    }
+    if (h > 0) {
+      snprintf(msg, sizeof msg, "device check failed (flags 0x%x)", h);
+      dt::set_context_free_error(msg);
+      return DARTREE_ERR_DEVICE_CHECK;
+    }
+    return DARTREE_OK;
+  }
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return ctx->cuda_fail(e, "stream synchronize");
   flush_timing(ctx);
@@ -1256,6 +1290,8 @@ dartree_status dartree_state_step(dartree_ctx* ctx, const void* S_par, const int
   if (!S_par || !tok || !A || !E || !S_out)
     return ctx->fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
   if (M < 1 || M > dt::kMaxRows) return ctx->fail(DARTREE_ERR_INVALID_ARG, "bad M=%d", M);
+  if (ctx->bf16 && (reinterpret_cast<uintptr_t>(E) & 15))
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
   dartree_status s = bind_weights(ctx, A, ctx->tm_Wout_ptr);
   if (s != DARTREE_OK) return s;
   if (!ctx->bf16) ctx->tm_A_ptr = A;

@@ -24,6 +24,8 @@ struct TcParams {
   int s_rows;          // row-major head kernel: state rows per TMA box of tmap_s (64: one
                        // CTA with at most 64 live rows and 256-entry tiles; else 128)
   // logits epilogue
+  int reverse;         // logits: walk this CTA's tiles and k-blocks last to first
+  int keep_w;          // state step: load the weight matrix with the L2 evict-last policy
   const float* z;      // base logits of this depth, request 0
   long long z_req_stride;
   int rows_per_req;    // head rows per request (|F_{d-1}|)
@@ -284,6 +286,9 @@ cudaError_t launch_bestfirst_z(const BestFirstParams& p, cudaStream_t st);
 // Records why the last context-free call on this thread failed; read back
 // through dartree_last_error(NULL).
 void set_context_free_error(const std::string& why);
+// Flags gathered by dartree_state_step_noalloc on the current device (read
+// and cleared after synchronising `st`); -1 if no call set the device up.
+int noalloc_take_status(cudaStream_t st, cudaError_t* err);
 
 // One-time kernel attribute setup (dynamic shared memory opt-in).
 cudaError_t init_select_attrs();

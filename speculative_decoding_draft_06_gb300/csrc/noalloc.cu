@@ -16,18 +16,28 @@
 //
 // Set-up: the first call on each device (that device current) looks up the
 // arrays' device addresses with cudaGetSymbolAddress, fills the identity
-// row map, encodes the staging tensor map and sets the kernels' shared-memory
-// attributes.  That first call synchronises with the device, so make it
-// before any stream capture.  Later calls on the device only enqueue work.
+// row map and sets the kernels' shared-memory attributes.  That first call
+// synchronises with the device, so make it before any stream capture.  Later
+// calls on the device only enqueue work.
 //
 // All calls share the arrays and the arrays keep the previous call's
-// contents: each call clears the split-K arrival counters before its kernel
-// runs, and everything else is fully overwritten before it is read.  Calls
-// whose work overlaps on the GPU (different streams, or different host
-// threads without ordering) race on the arrays and give wrong results.
+// contents.  Each call copies its parent states into the staging array and
+// zeroes the staging rows between M and the MMA's padded row count; the
+// split-K partials and the output rows are fully written before they are
+// read, so nothing else needs clearing.  Calls whose work overlaps on the GPU
+// (different streams, or different host threads without ordering) race on
+// the arrays and give wrong results.
+//
+// Device checks: the kernels OR a timeout (a bounded pipeline wait ran out)
+// or a bad index into a per-device check word that also lives here.  The word
+// gathers the flags of every call until dartree_sync_status(NULL, stream)
+// reads it: that call synchronises the stream, returns TIMEOUT or
+// DEVICE_CHECK when a flag is set (so a failed step is never reported as OK)
+// and clears the word for the calls that follow.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -144,8 +154,9 @@ extern "C" dartree_status dartree_state_step_noalloc(const void* S_par, const in
     return na_fail(DARTREE_ERR_UNSUPPORTED,
                    "dartree_state_step_noalloc handles M <= 256 rows and H <= 4096 (got M=" +
                        std::to_string(M) + ", H=" + std::to_string(H) + ")");
-  if (reinterpret_cast<uintptr_t>(A) & 15)
-    return na_fail(DARTREE_ERR_INVALID_ARG, "A must be 16-byte aligned");
+  // A is read by TMA (16-byte aligned base); E by 8-byte loads of four bf16
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(E)) & 15)
+    return na_fail(DARTREE_ERR_INVALID_ARG, "A and E must be 16-byte aligned");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return na_cuda_fail("cudaGetDevice", e);
@@ -186,6 +197,8 @@ extern "C" dartree_status dartree_state_step_noalloc(const void* S_par, const in
   p.n_split = n_split;
   p.part = d->part;
   p.V_tok = 0x7FFFFFFF;  // tokens are the caller's to keep in [0, V)
+  // test knob (as for contexts): shorten the pipeline waits to provoke TIMEOUT
+  if (const char* v = getenv("DARTREE_WAIT_LIMIT_CYCLES")) p.wait_limit = atoll(v);
   e = dt::launch_head_tc(N, false, tm_a, tm_s, p, tiles * n_split, st);
   if (e == cudaSuccess && n_split > 1) {
     dt::StateFinishParams f{};
@@ -207,4 +220,25 @@ extern "C" dartree_status dartree_state_step_noalloc(const void* S_par, const in
   e = cudaMemcpyAsync(S_out, d->out, M * rb, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return na_cuda_fail("output copy", e);
   return DARTREE_OK;
+}
+
+// The device checks of the calls above on the current device: synchronise
+// `st`, read the check word, clear it.  Returns the flags (0: none), or -1
+// when the device was never set up by a call (nothing to report).
+int dt::noalloc_take_status(cudaStream_t st, cudaError_t* err) {
+  *err = cudaSuccess;
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= kMaxDevices) return -1;
+  int* word = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_dev[dev].ready) return -1;
+    word = g_dev[dev].err;
+  }
+  if ((*err = cudaStreamSynchronize(st)) != cudaSuccess) return 0;
+  int h = 0;
+  if ((*err = cudaMemcpy(&h, word, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return 0;
+  if (h != 0 && (*err = cudaMemset(word, 0, sizeof(int))) != cudaSuccess) return 0;
+  return h;
 }

@@ -1,17 +1,21 @@
 """Parity at the five full workload sizes, in the launch configuration the
 bench times (dartree_build on a created stream, so the captured graph).
 
-The oracle cannot build the large trees in test time, so these tests check
-(a) properties that hold at any size -- exactly D head calls, pool layout,
-every score = parent score + that row's log-prob (one fp32 add), every
-kept frontier = the top-W of the GPU's own candidates under the total
-order, Top-B / compaction / mask bit-exact against the oracle on the GPU's
-pool and equal to the best-first heap (Lemma 1) -- and (b) sampled head rows
-recomputed by the oracle along the GPU's own paths (states from scratch,
-full-vocabulary logits, log-sum-exp and top-K).  The tiny workload (fp32) is
-compared in full with the teacher-forced oracle.
+Every head row of every build is compared with the oracle.  The oracle
+replays each (request, depth) slice of a build on its own from the GPU's
+head states and kept frontier (teacher and state forcing), and a process
+pool spreads the slices over the host's cores (tests/oracle_pool.py); the
+comparison rules are those of tests/parity.py: top-K sets, log-sum-exp and
+log-probs of every row, every kept frontier (exact, or a valid choice among
+near-ties), every state step, the oracle's accumulated scores along the
+GPU's paths, and Top-B / compaction / mask bit-exact with Lemma 1.  Besides,
+properties that hold at any size are checked on the GPU's own numbers.  The
+tiny workload (fp32) is also compared free-running: the oracle runs its own
+states along the GPU's frontier, at the 1e-5 tolerance.
 """
 from __future__ import annotations
+
+import warnings
 
 import numpy as np
 import pytest
@@ -20,8 +24,10 @@ import torch
 import oracle
 from speculative_decoding_draft_06_gb300 import dartree as dtl
 from speculative_decoding_draft_06_gb300 import inputs as I
+from tests import bruteforce as bf
 from tests import gpu_util as gu
 from tests import parity
+from tests.oracle_pool import OraclePool
 
 pytestmark = pytest.mark.gpu
 
@@ -81,36 +87,35 @@ def _check_properties(w, res):
         assert np.array_equal(ref["order"][:ref["n_out"]], heap)
 
 
-def _check_sampled_rows(inp, w, res, samples):
-    """Head rows recomputed by the oracle from the GPU's own states (the
-    input of that head call), and the state steps that produced them."""
-    tol = parity.TOL[w.bf16]
-    offs = np.concatenate([[0], np.cumsum(w.frontier_sizes())])
-    for (r, d, i) in samples:
-        pool, rows, _ = gu.split_request(res, w, r)
-        states = gu.request_states(res, w, r)
-        s = states[d - 1][i]
-        if d == 1:
-            want = inp["state0"][r].astype(np.float32)
-            if w.bf16:
-                want = np.array([oracle.round_bf16(float(x)) for x in want], np.float32)
-            assert np.array_equal(s, want)
-        else:
-            node = int(offs[d - 2]) + i                 # frontier slot i of depth d-1
-            par = int(pool["parent"][node])
-            ps = states[d - 2][0] if par < 0 else states[d - 2][par - int(offs[d - 3])]
-            ref = oracle.state_step(inp["A"], inp["E"], ps, int(pool["token"][node]), w.bf16)
-            ulp = np.spacing(np.abs(ref)) * (2 ** 16 if w.bf16 else 1)
-            assert np.all(np.abs(s - ref) <= ulp + (2e-5 if w.bf16 else 2e-6)), (r, d, i)
-        ell, lse = oracle.logits_row(inp["z"][r, d - 1], inp["Wout"], s, w.bf16)
-        tk, val, gap = oracle.topk_row(ell, w.K)
-        g_lse, g_tok, g_lp = rows[d - 1]["lse"][i], rows[d - 1]["tok"][i], rows[d - 1]["logp"][i]
-        assert abs(g_lse - lse) <= 1e-4, (r, d, i, g_lse, lse)
-        if gap >= parity.NEAR_TIE:
-            assert set(g_tok.tolist()) == set(tk.tolist()), (r, d, i)
-        ref_lp = (ell[g_tok].astype(np.float64) - lse).astype(np.float32)
-        assert np.max(np.abs(g_lp - ref_lp)) <= min(tol, 1e-4), (r, d, i)
-        assert np.all(np.diff(ell[g_tok]) <= parity.NEAR_TIE)
+def _report(msg: str) -> None:
+    """Parity figures, shown in the test run's warnings summary."""
+    warnings.warn(msg, UserWarning, stacklevel=2)
+
+
+def _sliced_parity(w, inp, res, markov=False, cand_base=False):
+    """Every head row of every request against the oracle (sliced, in
+    parallel); returns the summed counters."""
+    tasks = []
+    for r in range(w.R):
+        pool, _, _ = gu.split_request(res, w, r)
+        tasks += parity.slice_tasks(r, w.D, w.W, w.K, w.bf16, pool, gu.request_states(res, w, r),
+                                    cand_base=cand_base, markov=markov)
+    with OraclePool(inp) as p:
+        flat = p.run(tasks)
+    tot = {"near_ties": 0, "topk_near_ties": 0, "state_flips": 0, "state_elems": 0,
+           "max_lse_err": 0.0, "max_logp_err": 0.0, "max_score_err": 0.0,
+           "max_acc_score_err": 0.0, "rows": sum(w.head_rows())}
+    for r in range(w.R):
+        pool, rows, tree = gu.split_request(res, w, r)
+        rep = parity.compare_request_sliced(flat[r * w.D:(r + 1) * w.D], w.D, w.W, w.K, w.B,
+                                            w.beta, w.bf16, pool, rows, tree,
+                                            gu.request_states(res, w, r))
+        for k in tot:
+            if k.startswith("max_"):
+                tot[k] = max(tot[k], rep[k])
+            elif k != "rows":
+                tot[k] += rep[k]
+    return tot
 
 
 def test_tiny_full_oracle_parity():
@@ -118,22 +123,95 @@ def test_tiny_full_oracle_parity():
     inp, res = _run(w)
     _check_properties(w, res)
     pool, rows, tree = gu.split_request(res, w, 0)
+    # state-forced: every head call on the GPU's states, every state step checked
     rep = parity.compare_request(inp, 0, w.D, w.W, w.K, w.B, w.beta, w.bf16, pool, rows, tree,
                                  gpu_states=gu.request_states(res, w, 0))
     assert rep["near_ties"] <= 1
+    # free-running: the oracle's own fp32 states along the GPU's frontier
+    free = parity.compare_request(inp, 0, w.D, w.W, w.K, w.B, w.beta, w.bf16, pool, rows, tree)
+    assert free["near_ties"] <= 1
+    _report(f"tiny parity: {sum(w.head_rows())} head rows, free-running max score err "
+            f"{free['max_acc_score_err']:.2e} (tolerance 1e-5), max lse err "
+            f"{free['max_lse_err']:.2e}, near-ties {free['near_ties']}/{free['topk_near_ties']}")
 
 
 @pytest.mark.parametrize("name", ["q4b", "q8b", "wide", "batch"])
-def test_full_size_properties_and_sampled_rows(name):
+def test_full_size_oracle_parity_every_row(name):
     w = I.CONFIGS[name]
     inp, res = _run(w)
     _check_properties(w, res)
-    last = w.frontier_sizes()[-2]
-    samples = [(0, 1, 0), (0, 2, 0), (0, 2, min(3, w.frontier_sizes()[0] - 1)),
-               (0, w.D, last - 1)]
-    if w.R > 1:
-        samples += [(w.R - 1, 1, 0), (w.R // 2, w.D // 2, 1)]
-    _check_sampled_rows(inp, w, res, samples)
+    tot = _sliced_parity(w, inp, res)
+    # near-ties stay rare on these inputs (about one per build is expected)
+    assert tot["near_ties"] <= max(2, w.R // 4), tot
+    _report(f"{name} parity: {tot['rows']} head rows of {w.R} request(s) against the oracle; "
+            f"near-ties top-W {tot['near_ties']}, top-K {tot['topk_near_ties']}; max errors: "
+            f"lse {tot['max_lse_err']:.2e}, logp {tot['max_logp_err']:.2e}, score per depth "
+            f"{tot['max_score_err']:.2e}, accumulated score {tot['max_acc_score_err']:.2e} "
+            f"(tolerance {parity.TOL[w.bf16]:g}); state elements off by one bf16 step "
+            f"{tot['state_flips']}/{tot['state_elems']}")
+
+
+def _fp32_state_chain(inp, slot, tok, sizes, s_root):
+    """The stand-in head's state recurrence with fp32 accumulation (numpy),
+    along a given frontier: a second implementation of the same precision
+    class as the GPU's, to measure how far the bf16-rounded recurrence alone
+    carries accumulation-order differences."""
+    A32 = bf.weights_f64(inp["A"], True).astype(np.float32)
+    E32 = bf.weights_f64(inp["E"], True).astype(np.float32)
+    st, off = [s_root], 0
+    for fd in sizes[:-1]:
+        u = st[-1][slot[off:off + fd]] @ A32.T + E32[tok[off:off + fd]]
+        st.append(bf.q(np.tanh(u).astype(np.float32), True))
+        off += fd
+    return st
+
+
+def test_q8b_free_running_score_drift():
+    """Nothing forced but the frontier: the oracle runs its own head states
+    (fp64 recurrence, bf16-rounded) along the GPU's q8b frontier and
+    recomputes every head row from them.  Rounding the state to bf16 at every
+    depth turns accumulation-order differences into rounding flips that the
+    next depth's contraction spreads, so the drift grows with depth for any
+    fp32-accumulating implementation; an fp32 numpy recurrence along the same
+    frontier measures that.  The GPU's drift is reported beside it and must
+    be of the same size; the first depths, before the flips spread, must stay
+    within the score tolerance."""
+    w = I.CONFIGS["q8b"]
+    inp, res = _run(w)
+    pool, rows, tree = gu.split_request(res, w, 0)
+    slot, tok, sizes = parity.forced_frontier(pool, w.D, w.W, w.K)
+    gst = gu.request_states(res, w, 0)
+    want = np.array([oracle.round_bf16(float(x)) for x in inp["state0"][0]], np.float32)
+    assert np.array_equal(gst[0][0], want)             # depth 1: q(state0), exactly
+    chains = {"oracle": [gst[0]]}
+    off = 0
+    for d in range(1, w.D):
+        fd = sizes[d - 1]
+        chains["oracle"].append(np.stack([
+            oracle.state_step(inp["A"], inp["E"], chains["oracle"][-1][slot[off + q]],
+                              int(tok[off + q]), True) for q in range(fd)]))
+        off += fd
+    chains["fp32"] = _fp32_state_chain(inp, slot, tok, sizes, gst[0])
+    acc = {}
+    with OraclePool(inp) as p:
+        for k, st in chains.items():
+            tasks = parity.slice_tasks(0, w.D, w.W, w.K, True, pool, None, states=st)
+            o = parity.assemble(p.run(tasks), w.D, w.W, w.K)
+            acc[k] = oracle.path_scores(pool["parent"], o["pool_logp"])
+    dep = pool["depth"]
+    by_depth = lambda x: np.array([x[dep == d].max() for d in range(1, w.D + 1)])  # noqa: E731
+    d_gpu = by_depth(np.abs(pool["score"] - acc["oracle"]))
+    d_f32 = by_depth(np.abs(acc["fp32"] - acc["oracle"]))
+    flips = lambda st: sum(int(np.count_nonzero(a != b))                       # noqa: E731
+                           for a, b in zip(st, chains["oracle"]))
+    n_el = sum(a.size for a in chains["oracle"])
+    _report(f"q8b free-running score drift against the fp64 oracle: GPU max {d_gpu.max():.2e}, "
+            f"fp32 numpy recurrence max {d_f32.max():.2e} (score tolerance 2e-3); by depth GPU "
+            + " ".join(f"{x:.1e}" for x in d_gpu) + "; fp32 " + " ".join(f"{x:.1e}" for x in d_f32)
+            + f"; state elements differing from the oracle's: GPU {flips(gst)}, fp32 "
+              f"{flips(chains['fp32'])} of {n_el}")
+    assert np.all(d_gpu[:3] <= parity.TOL[True])
+    assert d_gpu.max() <= 4 * d_f32.max() + parity.TOL[True]
 
 
 # ------------------------------------------------ build variants at full size
@@ -152,7 +230,7 @@ def _run_variant(w, **variant):
 
 
 @pytest.mark.parametrize("variant", [dict(head="markov"), dict(candidates="base")])
-def test_q8b_depthwise_variants_properties_and_sampled_rows(variant):
+def test_q8b_depthwise_variants_oracle_parity_every_row(variant):
     w = I.CONFIGS["q8b"]
     inp, ctx, out = _run_variant(w, **variant)
     res = {"pool": {k: v.numpy() for k, v in ctx.get_pool(w.R, w.pool_size()).items()},
@@ -167,35 +245,19 @@ def test_q8b_depthwise_variants_properties_and_sampled_rows(variant):
     _check_properties(w, res)
     markov = variant.get("head") == "markov"
     base = variant.get("candidates") == "base"
-    pool, rows, _ = gu.split_request(res, w, 0)
-    states = gu.request_states(res, w, 0)
-    offs = np.concatenate([[0], np.cumsum(w.frontier_sizes())])
-    tol = parity.TOL[True]
-    for (d, i) in [(1, 0), (2, 3), (w.D, 15)]:
-        s = states[d - 1][i]
-        if d >= 2:                         # the state step that produced this row
-            node = int(offs[d - 2]) + i
-            par = int(pool["parent"][node])
-            ps = states[d - 2][0] if par < 0 else states[d - 2][par - int(offs[d - 3])]
-            ref = oracle.state_step(None if markov else inp["A"], inp["E"], ps,
-                                    int(pool["token"][node]), True)
-            ulp = np.spacing(np.abs(ref)) * 2 ** 16
-            assert np.all(np.abs(s - ref) <= ulp + 2e-5), (d, i)
-        g_lse, g_tok, g_lp = rows[d - 1]["lse"][i], rows[d - 1]["tok"][i], rows[d - 1]["logp"][i]
-        if base:
+    if base:                              # every row's candidates: top-K of z_d
+        _, rows, _ = gu.split_request(res, w, 0)
+        for d in range(1, w.D + 1):
             z = torch.from_numpy(inp["z"][0, d - 1].astype(np.float64))
-            cand = torch.sort(z, descending=True, stable=True).indices[:w.K].numpy()
-            assert set(g_tok.tolist()) == set(cand.tolist()), (d, i)
-            tk, val, lse = oracle.cand_row(inp["z"][0, d - 1], inp["Wout"], s, cand, True)
-            ref_lp = {int(t): float(np.float64(v) - lse) for t, v in zip(tk, val)}
-        else:
-            ell, lse = oracle.logits_row(inp["z"][0, d - 1], inp["Wout"], s, True)
-            tk, _, gap = oracle.topk_row(ell, w.K)
-            if gap >= parity.NEAR_TIE:
-                assert set(g_tok.tolist()) == set(tk.tolist()), (d, i)
-            ref_lp = {int(t): float(np.float64(ell[t]) - lse) for t in g_tok}
-        assert abs(g_lse - lse) <= 1e-4, (d, i, g_lse, lse)
-        assert max(abs(float(lp) - ref_lp[int(t)]) for t, lp in zip(g_tok, g_lp)) <= min(tol, 1e-4)
+            cand = set(torch.sort(z, descending=True, stable=True).indices[:w.K].tolist())
+            for i in range(rows[d - 1]["tok"].shape[0]):
+                assert set(rows[d - 1]["tok"][i].tolist()) == cand, (d, i)
+    tot = _sliced_parity(w, inp, res, markov=markov, cand_base=base)
+    assert tot["near_ties"] <= 2, tot
+    _report(f"q8b {'Markov head' if markov else 'base-logit candidates'} parity: {tot['rows']} "
+            f"head rows; near-ties {tot['near_ties']}/{tot['topk_near_ties']}; max errors lse "
+            f"{tot['max_lse_err']:.2e}, accumulated score {tot['max_acc_score_err']:.2e}; "
+            f"state elements off by one bf16 step {tot['state_flips']}/{tot['state_elems']}")
 
 
 def test_q8b_bestfirst_properties_and_sampled_calls():
