@@ -112,7 +112,9 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
  * state boxes unless DARTREE_ROWS_HALF_S=0; DARTREE_TC_MAX_STAGES caps the
  * pipeline depth and DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs
  * on an SM; the row merge reads only the CTA lists that reach the head call's
- * row bound (K <= 16) unless DARTREE_MERGE_BOUND=0.  Results
+ * row bound (K <= 16) unless DARTREE_MERGE_BOUND=0; the Top-B of pools of
+ * 512 or more nodes is a block radix select (DARTREE_RADIX=0: never, =1: the
+ * top-W and every Top-B as well).  Results
  * are the same under every setting (up to the order of fp32 additions). */
 dartree_status dartree_create(const dartree_config *cfg, dartree_ctx **out);
 

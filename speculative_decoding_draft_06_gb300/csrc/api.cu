@@ -74,9 +74,11 @@ struct dartree_ctx {
   bool pdl = true;         // programmatic dependent launch between the kernels of a build
   long long wait_limit = 0;  // test knob: pipeline wait limit in cycles (0: full)
   bool use_graph = true;   // capture each build shape once into a CUDA graph
-  bool head_alternate = false;  // consecutive head calls walk Wout in opposite directions
-  bool keep_A = false;     // the state step's A stays in L2 between depths (evict last)
-  int head_dir = 0;        // direction of the next head call (set per call of a build)
+  // selection by block radix select: -1 (default) for the Top-B of pools of at
+  // least 512 nodes only (where it beats the bitonic sort of the pool; the
+  // top-W stays a merge of the already sorted child lists, which is faster),
+  // 1 for the top-W and the Top-B, 0 never
+  int radix = -1;
 
   // the captured build and the arguments it was captured with
   struct GraphKey {
@@ -275,7 +277,6 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.list_stride = c->max_cta;
   p.pdl = c->pdl;
   p.wait_limit = c->wait_limit;
-  p.reverse = c->head_dir;
   int grid;
   cudaError_t e;
   {
@@ -345,6 +346,7 @@ dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, i
   mp.gth = c->gth;
   mp.gmx = c->gth + dt::kMaxRows;
   mp.surv_cap = c->merge_surv_cap;
+  mp.radix = c->radix == 1;
   {
     KernelTimer tk(c, st, 2);
     e = c->merge_bound && dt::merge_bound_fits(mp) ? dt::launch_merge_bound(mp, st)
@@ -381,7 +383,6 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
     p.n_split = c->state_split;
     p.part = c->part;
     p.early_operands = early && c->pdl;
-    p.keep_w = c->keep_A;
     e = dt::launch_head_tc(N, false, c->tm_A, c->tmS(src, N), p,
                            p.n_tiles * p.n_split, st);
     if (e == cudaSuccess && p.n_split > 1) {
@@ -619,13 +620,10 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
                    c->cand + static_cast<size_t>(d - 1) * K, static_cast<long long>(D) * K, F, M,
                    K, head->Wout, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K,
                    &sel, st);
-    else {
-      c->head_dir = c->head_alternate ? (d - 1) & 1 : 0;
+    else
       s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
                    F, M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel,
                    st);
-      c->head_dir = 0;
-    }
     if (s != DARTREE_OK) return s;
     ++calls;
     cur ^= 1;
@@ -652,6 +650,7 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   pp.mask = out->mask;
   pp.n_out = out->n_out;
   pp.err = c->d_err;
+  pp.radix = c->radix == 1 || (c->radix < 0 && P >= 512);
   pp.pdl = c->pdl;
   {
     KernelTimer tk(c, st, 4);
@@ -745,10 +744,8 @@ dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
     }
     const int sbuf = call == 0 ? 0 : 2;
     const size_t ro = static_cast<size_t>(call) * c->cfg.max_requests;
-    c->head_dir = c->head_alternate ? call & 1 : 0;
     s = run_head(c, sbuf, c->bf_z, V, 1, R, K, c->bf_lse + ro, c->bf_rtok + ro * K,
                  c->bf_rlogp + ro * K, nullptr, st);
-    c->head_dir = 0;
     if (s != DARTREE_OK) return s;
     bp.row_tok = c->bf_rtok + ro * K;
     bp.row_logp = c->bf_rlogp + ro * K;
@@ -914,8 +911,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_PDL")) c->pdl = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_WAIT_LIMIT_CYCLES")) c->wait_limit = atoll(v);
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
-  if (const char* v = getenv("DARTREE_HEAD_ALTERNATE")) c->head_alternate = atoi(v) != 0;
-  if (const char* v = getenv("DARTREE_KEEP_A")) c->keep_A = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_RADIX")) c->radix = atoi(v) != 0 ? 1 : 0;
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;
@@ -1336,6 +1332,7 @@ dartree_status dartree_prune(dartree_ctx* ctx, const int32_t* pool_parent, const
   pp.mask = out->mask;
   pp.n_out = out->n_out;
   pp.err = ctx->d_err;
+  pp.radix = ctx->radix == 1 || (ctx->radix < 0 && P >= 512);
   cudaError_t e = dt::launch_prune(pp, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ctx->cuda_fail(e, "prune launch");
   return DARTREE_OK;

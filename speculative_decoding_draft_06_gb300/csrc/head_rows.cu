@@ -332,13 +332,6 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
     if (j >= nk) j -= nk;
     return j;
   };
-  // Alternate calls walk the weight stream in opposite directions (tiles and
-  // the K steps within a tile), so a call begins with the lines the previous
-  // call read last, which are still in L2.
-  const bool rev = p.reverse != 0;
-  const int n_mine = t_end - t_begin;
-  auto tile_at = [&](int j) { return rev ? t_end - 1 - j : t_begin + j; };
-  auto kstep_at = [&](int t, int i) { return kb_at(t, rev ? nk - 1 - i : i); };
 
   if (warp == C::kMma) {
     if constexpr (kPair)
@@ -381,10 +374,9 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (int jt = 0; jt < n_mine && !*abort_flag; ++jt) {
-        const int t = tile_at(jt);
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
         for (int i = 0; i < nk; ++i) {
-          const int kb = kstep_at(t, i);
+          const int kb = kb_at(t, i);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.wait_limit)) {
             *abort_flag = 1;
             break;
@@ -440,7 +432,7 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int jt = 0; jt < n_mine && !*abort_flag; ++jt, ++it) {
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
         const int a = C::kBufs == 2 ? (it & 1) : 0;
         const uint32_t par = static_cast<uint32_t>(C::kBufs == 2 ? (it >> 1) : it) & 1u;
         const bool free_acc = kPair ? mbar_wait_cluster(&tempty[a], par ^ 1u, p.err, p.wait_limit)
@@ -537,10 +529,9 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
       }
     };
     float zn[32];
-    if (n_mine > 0) load_z(tile_at(0) * NV + cg * kChunks * 32, zn);
+    if (t_begin < t_end) load_z(t_begin * NV + cg * kChunks * 32, zn);
     int it = 0;
-    for (int jt = 0; jt < n_mine; ++jt, ++it) {
-      const int t = tile_at(jt);
+    for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = C::kBufs == 2 ? (it & 1) : 0;
       const uint32_t par = static_cast<uint32_t>(C::kBufs == 2 ? (it >> 1) : it) & 1u;
       // the row's global bound, read before the wait
@@ -573,9 +564,8 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] += zn[j];
         {  // next chunk's base logits, in flight while this one is processed
-          const int vn =
-              q + 1 < kChunks ? vb + 32 : (jt + 1 < n_mine ? tile_at(jt + 1) : 0) * NV + cg * kChunks * 32;
-          if (q + 1 < kChunks || jt + 1 < n_mine) load_z(vn, zn);
+          const int vn = q + 1 < kChunks ? vb + 32 : (t + 1) * NV + cg * kChunks * 32;
+          if (q + 1 < kChunks || t + 1 < t_end) load_z(vn, zn);
         }
         if (!live) continue;
         // x * 0 is NaN exactly for NaN and +-inf: one probe per value

@@ -181,13 +181,6 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     if (j >= kb_span) j -= kb_span;
     return kb_begin + j;
   };
-  // Alternate calls walk the weight stream in opposite directions (tiles and
-  // the k-blocks within a tile), so a call begins with the lines the previous
-  // call read last, which are still in L2.
-  const bool rev = kLogits && p.reverse;
-  const int n_mine = t_end - t_begin;
-  auto tile_at = [&](int j) { return rev ? t_end - 1 - j : t_begin + j; };
-  auto kstep_at = [&](int t, int i) { return kb_at(t, rev ? kb_span - 1 - i : i); };
 
   if (warp == R::kMma) tmem_alloc<L::kTmemCols>(tmem_slot);
   if (threadIdx.x == 0) {
@@ -227,19 +220,14 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
   if (warp == R::kProducer) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      // the vocabulary stream goes through L2 once per call (evict first); the
-      // state matrix A of the state step is read again at every depth and
-      // may stay (evict last)
-      const uint64_t pol_w = (!kLogits && p.keep_w) ? l2_policy_evict_last()
-                                                    : l2_policy_evict_first();
+      const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_s = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (int j = 0; j < n_mine && !*abort_flag; ++j) {
-        const int t = tile_at(j);
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
         for (int i = 0; i < kb_span; ++i) {
-          const int kb = kstep_at(t, i);
+          const int kb = kb_at(t, i);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.wait_limit)) {
             *abort_flag = 1;
             break;
@@ -271,7 +259,7 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int j = 0; j < n_mine && !*abort_flag; ++j, ++it) {
+      for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
         const int a = it & 1;
         if (!mbar_wait(&tempty[a], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.err,
                        p.wait_limit)) {
@@ -329,8 +317,7 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     // all rows of one request (the usual case): one base logit per thread
     // and tile, loaded before the accumulator wait
     const bool one_req = kLogits && p.rows_per_req >= p.M;
-    for (int j = 0; j < n_mine; ++j, ++it) {
-      const int t = tile_at(j);
+    for (int t = t_begin; t < t_end; ++t, ++it) {
       const int a = it & 1;
       const int row = t * kTileV + wq * 32 + lane;  // vocabulary (or hidden) index
       const bool valid = row < p.rows;

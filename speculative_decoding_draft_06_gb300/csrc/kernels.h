@@ -24,8 +24,6 @@ struct TcParams {
   int s_rows;          // row-major head kernel: state rows per TMA box of tmap_s (64: one
                        // CTA with at most 64 live rows and 256-entry tiles; else 128)
   // logits epilogue
-  int reverse;         // logits: walk this CTA's tiles and k-blocks last to first
-  int keep_w;          // state step: load the weight matrix with the L2 evict-last policy
   const float* z;      // base logits of this depth, request 0
   long long z_req_stride;
   int rows_per_req;    // head rows per request (|F_{d-1}|)
@@ -161,6 +159,7 @@ struct MergeParams {
   int* counters;             // [R] zero between launches
   int surv_cap;              // k_merge_bound: keys at or above the bound staged in shared
                              // memory (at most 512; more go the slow way)
+  int radix;                 // top-W by block radix select (else merge folds / bitonic sort)
 };
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
 // The same merge (and selection) with one block per row that reads only the
@@ -185,6 +184,7 @@ struct PruneParams {
   uint32_t* mask;
   int32_t* n_out;
   int* err;
+  int radix;           // Top-B by block radix select (else a bitonic sort of the pool)
 };
 cudaError_t launch_prune(const PruneParams& p, cudaStream_t st);
 

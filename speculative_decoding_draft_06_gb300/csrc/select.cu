@@ -6,9 +6,11 @@
 // the root rows.
 //
 // Every selection orders 64-bit keys (value desc, index asc; see common.cuh)
-// with bitonic sorts and merges, in warps or in shared memory, and the keys
-// are distinct, so results are a deterministic total order and independent
-// of thread timing (including the order in which k_merge_bound stages keys).
+// with bitonic sorts and merges, in warps or in shared memory, or with a
+// block radix select of the best keys followed by a sort of those (the Top-B
+// of large pools; block.cuh), and the keys are distinct, so results are a
+// deterministic total order and independent of thread timing (including the
+// order in which k_merge_bound stages keys).
 #include <cuda_runtime.h>
 
 #include "block.cuh"
@@ -139,8 +141,34 @@ __device__ void select_frontier_warp64(const MergeParams& p, int r, uint64_t* sl
   }
 }
 
+// Radix form of the same selection: the request's F*K candidate keys in
+// shared memory, a block radix select of the best |F_d| (block.cuh), then a
+// bitonic sort of those |F_d| into rank order.
+__device__ void select_frontier_radix(const MergeParams& p, int r, uint64_t* keys) {
+  __shared__ unsigned hist[256];
+  __shared__ int sh[4];
+  const int n = p.F * p.K;
+  const int kp2 = pow2_at_least(p.Fd);
+  uint64_t* sel = keys + ((n + 1) & ~1);
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int row = r * p.F + e / p.K;
+    const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + (e % p.K));
+    const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
+    keys[e] = make_key(c, static_cast<uint32_t>(e));
+  }
+  for (int q = p.Fd + threadIdx.x; q < kp2; q += blockDim.x) sel[q] = 0ull;
+  __syncthreads();
+  block_radix_select(keys, n, p.Fd, sel, hist, sh);
+  block_sort_desc(sel, kp2);
+  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, sel[q]);
+}
+
 __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
                                 uint64_t (*wl)[32]) {
+  if (p.radix) {
+    select_frontier_radix(p, r, keys);
+    return;
+  }
   if (p.Fd <= 32) {
     select_frontier_warp(p, r, wl);
     return;
@@ -450,6 +478,11 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
 }
 
 static size_t select_smem(const MergeParams& p) {
+  if (p.select && p.radix) {
+    int kp2 = 1;
+    while (kp2 < p.Fd) kp2 <<= 1;
+    return (static_cast<size_t>((p.F * p.K + 1) & ~1) + kp2) * 8;
+  }
   if (p.select && (p.Fd > 64 || p.F > 64)) {
     int np2 = 1;
     while (np2 < p.F * p.K) np2 <<= 1;
@@ -489,10 +522,15 @@ __global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
   pdl_trigger();
   const int r = blockIdx.x;
   const int np2 = pow2_at_least(p.P);
-  int32_t* map = reinterpret_cast<int32_t*>(keys + np2);  // [P] pool -> rank
+  const int n_sel = p.P < p.B ? p.P : p.B;
+  const int sp2 = pow2_at_least(n_sel);
+  // radix: keys [P] then the selection [pow2(n_sel)]; else keys [pow2(P)] sorted in place
+  uint64_t* sel = p.radix ? keys + ((p.P + 1) & ~1) : keys;
+  int32_t* map = reinterpret_cast<int32_t*>(p.radix ? sel + sp2 : keys + np2);  // [P] pool -> rank
   int32_t* par = map + p.P;                               // [B] parent rank
   const size_t pb = static_cast<size_t>(r) * p.pool_stride;
-  for (int e = threadIdx.x; e < np2; e += blockDim.x) {
+  const int n_keys = p.radix ? p.P : np2;
+  for (int e = threadIdx.x; e < n_keys; e += blockDim.x) {
     uint64_t k = 0ull;
     if (e < p.P) {
       const float key = __fadd_rn(p.pool_score[pb + e],
@@ -502,16 +540,24 @@ __global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
     keys[e] = k;
   }
   for (int e = threadIdx.x; e < p.P; e += blockDim.x) map[e] = -1;
+  if (p.radix)
+    for (int q = n_sel + threadIdx.x; q < sp2; q += blockDim.x) sel[q] = 0ull;
   __syncthreads();
-  block_sort_desc(keys, np2);
-  const int n_sel = p.P < p.B ? p.P : p.B;
-  for (int q = threadIdx.x; q < n_sel; q += blockDim.x) map[key_index(keys[q])] = q;
+  if (p.radix) {
+    __shared__ unsigned hist[256];
+    __shared__ int sh[4];
+    block_radix_select(keys, p.P, n_sel, sel, hist, sh);
+    block_sort_desc(sel, sp2);
+  } else {
+    block_sort_desc(keys, np2);
+  }
+  for (int q = threadIdx.x; q < n_sel; q += blockDim.x) map[key_index(sel[q])] = q;
   __syncthreads();
   const size_t ob = static_cast<size_t>(r) * p.B;
   bool broken = false;
   for (int q = threadIdx.x; q < p.B; q += blockDim.x) {
     if (q < n_sel) {
-      const int n = static_cast<int>(key_index(keys[q]));
+      const int n = static_cast<int>(key_index(sel[q]));
       const int pp = p.pool_parent[pb + n];
       int pr = (pp < 0 || pp >= p.P) ? -1 : map[pp];
       if ((pp >= 0 && pr < 0) || pr >= q || pp >= p.P) {
@@ -552,8 +598,11 @@ __global__ void __launch_bounds__(kPruneThreads) k_prune(const PruneParams p) {
 cudaError_t launch_prune(const PruneParams& p, cudaStream_t st) {
   int np2 = 1;
   while (np2 < p.P) np2 <<= 1;
-  const size_t smem = static_cast<size_t>(np2) * 8 + static_cast<size_t>(p.P) * 4 +
-                      static_cast<size_t>(p.B) * 4;
+  int sp2 = 1;
+  while (sp2 < (p.P < p.B ? p.P : p.B)) sp2 <<= 1;
+  const size_t key_bytes = p.radix ? (static_cast<size_t>((p.P + 1) & ~1) + sp2) * 8
+                                   : static_cast<size_t>(np2) * 8;
+  const size_t smem = key_bytes + static_cast<size_t>(p.P) * 4 + static_cast<size_t>(p.B) * 4;
   return launch_kernel(k_prune, dim3(p.R), dim3(kPruneThreads), smem, st, p.pdl != 0, p);
 }
 

@@ -72,6 +72,15 @@ def test_build_with_the_row_group_merge_matches_oracle(monkeypatch, name):
     test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
 
 
+@pytest.mark.parametrize("name", ["bf16-n16", "bf16-w48", "bf16-batch", "bf16-max", "f32-max",
+                                  "bf16-bigB"])
+def test_build_with_radix_select_matches_oracle(monkeypatch, name):
+    """Top-W and Top-B by block radix select (instead of merge folds and
+    bitonic sorts) give the same trees."""
+    monkeypatch.setenv("DARTREE_RADIX", "1")
+    test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
+
+
 @pytest.mark.parametrize("cap", ["0", "40"])
 @pytest.mark.parametrize("name", ["bf16-n32", "bf16-batch", "f32-wide"])
 def test_build_with_small_bound_key_buffers_matches_oracle(monkeypatch, name, cap):
@@ -229,7 +238,9 @@ def test_state_step_matches_oracle(bf16, M):
     ctx.close()
 
 
-def test_prune_matches_oracle_bit_exact():
+@pytest.mark.parametrize("radix", ["0", "1"])
+def test_prune_matches_oracle_bit_exact(monkeypatch, radix):
+    monkeypatch.setenv("DARTREE_RADIX", radix)
     g = np.random.default_rng(3)
     R, D, W, K = 3, 6, 12, 4
     w = I.small_workload(31, V=200, H=64, D=D, W=W, K=K, B=64, bf16=True, R=R)
