@@ -527,6 +527,43 @@ def run_gpu(args) -> None:
                   "k_head_tc + k_state_finish (state step: A stream, split-K, finish)"),
         "candidates": "k_base_topk (top-K of the base logits)"}[kind]
 
+    # the same head launches against the tensor roofline (their flops are
+    # fixed by the head rows: a few at 16 rows, at the ridge at 256)
+    tensor_line = None
+    fl = head_flops_per_launch(w, args.variant) if kind == "head" else None
+    if fl:
+        tpk, tpk_kind = measured_bf16_tflops(sustained=True)
+        ach = fl / (head_avg_ms * 1e-3) / 1e12
+        tensor_line = {"achieved": ach, "peak": tpk, "unit": "TFLOP/s", "frac": ach / tpk,
+                       "peak_source": f"{tpk_kind} (sustained dense bf16)",
+                       "flops_per_launch": fl}
+
+    # a projection that fits in L2 is re-read from L2 by every head call: its
+    # HBM fraction bounds nothing, so the line also gives the fraction of an
+    # L2-resident copy measured here (two 24 MB buffers, events)
+    l2_line = None
+    w_bytes = w.V * w.H * (2 if w.bf16 else 4)
+    if kind == "head" and w_bytes <= 64e6:
+        a = torch.empty(6 << 20, dtype=torch.float32, device="cuda")
+        b = torch.empty_like(a)
+        for _ in range(20):
+            b.copy_(a)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(200):
+            b.copy_(a)
+        c1.record()
+        c1.synchronize()
+        l2_gbs = 2 * a.numel() * 4 * 200 / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        l2_line = {"achieved": achieved, "peak": l2_gbs, "unit": "GB/s", "frac": achieved / l2_gbs,
+                   "peak_source": "measured in this run: copy of a 24 MB fp32 buffer (L2-resident), "
+                                  "read + write bytes",
+                   "note": (f"the {w_bytes / 1e6:.1f} MB projection stays in L2 between head "
+                            "calls; the call is latency-bound (a short chain of load rounds "
+                            "and the fused epilogue), not bound by a pipe")}
+        del a, b
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and args.variant != "dartree":
@@ -596,6 +633,8 @@ def run_gpu(args) -> None:
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic, "traffic_source": traffic_source,
                          "bytes_per_launch": bytes_launch, "launch_ms": head_avg_ms},
+            "tensor": tensor_line,
+            "l2": l2_line,
             "kernel_ms_per_build": {k: v[0] / max(1, min(args.steps, 50)) for k, v in kt.items()},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": kernels_per_build(w, args.variant) * args.steps,
@@ -608,13 +647,26 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
-def measured_bf16_tflops() -> tuple[float, str]:
+def measured_bf16_tflops(sustained: bool = False) -> tuple[float, str]:
+    """Measured dense bf16 peak: the burst figure for a kernel timed alone,
+    the sustained one for a kernel timed inside a long step."""
     p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     try:
         with open(p) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured"
+            return float(json.load(f)[key]), "measured"
     except (OSError, KeyError, ValueError):
-        return 1900.0, "fallback"
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def head_flops_per_launch(w: I.Workload, variant: str) -> float | None:
+    """Tensor flops of one head call (2 M V H), averaged over a build's calls;
+    None where the head call is not a dense contraction over the vocabulary."""
+    opt = VARIANTS[variant]
+    if opt.get("candidates") == "base" or not w.bf16:
+        return None
+    rows = [w.R] * w.B if opt.get("expansion") == "bestfirst" else w.head_rows()
+    return sum(2.0 * m * w.V * w.H for m in rows) / len(rows)
 
 
 def run_verify(args) -> None:

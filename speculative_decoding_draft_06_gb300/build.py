@@ -16,7 +16,7 @@ LIB = os.path.join(OUT_DIR, "libdartree.so")
 _NS = (16, 32, 64, 128, 256)
 SOURCES = ([("api.cu", [], "api.o"), ("select.cu", [], "select.o"),
             ("noalloc.cu", [], "noalloc.o"), ("variants.cu", [], "variants.o"), ("verify.cu", [], "verify.o"),
-            ("head_rows.cu", [], "head_rows.o")]
+            ("head_rows.cu", [], "head_rows.o"), ("head_f32.cu", [], "head_f32.o")]
            + [("head_tc.cu", [f"-DDT_N={n}"], f"head_tc_{n}.o") for n in _NS]
            + [("head_simt.cu", [f"-DDT_N={n}"], f"head_simt_{n}.o") for n in _NS])
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -79,6 +79,7 @@ struct dartree_ctx {
   // top-W stays a merge of the already sorted child lists, which is faster),
   // 1 for the top-W and the Top-B, 0 never
   int radix = -1;
+  bool f32_split = true;   // fp32 head calls of <= 16 rows: four threads per weight row
 
   // the captured build and the arguments it was captured with
   struct GraphKey {
@@ -298,11 +299,17 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
       p.max_stages = c->tc_max_stages;
       p.ctas_per_sm = c->tc_ctas_per_sm;
       e = dt::launch_head_tc(N, true, c->tm_Wout, c->tmS(sbuf, N), p, grid, st);
+    } else if (c->f32_split && dt::head_f32_fits(M, H, K) &&
+               (reinterpret_cast<uintptr_t>(c->tm_Wout_ptr) & 15) == 0) {
+      grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
+      p.W_f32 = static_cast<const float*>(c->tm_Wout_ptr);
+      p.S_f32 = static_cast<const float*>(c->S(sbuf));
+      e = dt::launch_head_f32(p, grid, st);
     } else {
       grid = p.n_tiles < c->max_cta ? p.n_tiles : c->max_cta;
       p.W_f32 = static_cast<const float*>(c->tm_Wout_ptr);
       p.S_f32 = static_cast<const float*>(c->S(sbuf));
-      e = dt::launch_head_simt(N, true, p, grid, st);
+      e = dt::launch_head_simt(N, p, grid, st);
     }
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "head logits launch");
@@ -403,12 +410,21 @@ dartree_status run_state(dartree_ctx* c, const void* A, const void* E, int src, 
       e = dt::launch_state_finish(f, st);
     }
   } else {
-    p.E_f32 = static_cast<const float*>(E);
-    p.S_out_f32 = static_cast<float*>(c->S(src + 1));
-    p.W_f32 = static_cast<const float*>(A);
-    p.S_f32 = static_cast<const float*>(c->S(src));
-    p.n_split = 1;
-    e = dt::launch_head_simt(N, false, p, p.n_tiles, st);
+    dt::StateF32Params f{};
+    f.pdl = c->pdl;
+    f.H = H;
+    f.M_in = M_in;
+    f.M_out = M_out;
+    f.n_out = pad_rows(M_out);
+    f.V_tok = c->cfg.V;
+    f.A = static_cast<const float*>(A);
+    f.S_in = static_cast<const float*>(c->S(src));
+    f.slot = slot;
+    f.tok = tok;
+    f.E = static_cast<const float*>(E);
+    f.S_out = static_cast<float*>(c->S(src + 1));
+    f.err = c->d_err;
+    e = dt::launch_state_f32(f, st);
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "state step launch");
   return DARTREE_OK;
@@ -912,6 +928,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_WAIT_LIMIT_CYCLES")) c->wait_limit = atoll(v);
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_RADIX")) c->radix = atoi(v) != 0 ? 1 : 0;
+  if (const char* v = getenv("DARTREE_F32_SPLIT")) c->f32_split = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;

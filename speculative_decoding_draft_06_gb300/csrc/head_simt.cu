@@ -1,11 +1,13 @@
-// Batched head contraction for fp32 weights on the CUDA cores.
+// Head call (fused corrected logits + log-sum-exp + top-K) for fp32 weights
+// on the CUDA cores, for calls that the TMA-fed fp32 kernel (head_f32.cu)
+// does not take: more than 16 head rows, or weight rows that are not
+// 16-byte multiples.
 //
 // fp32 weights keep fp32 products: TF32 tensor cores round the operands to
 // 10 mantissa bits, which is far outside a 1e-5 score tolerance, so this
-// path uses FFMA.  Same two epilogues as the tensor-core kernel (fused
-// log-sum-exp + top-K of the corrected logits, or the tanh state step; see
-// "DARTree: Teaching a Chain-Trained Corrector to Think in Trees", Core
-// Mechanism, and "Technische Samenvatting: DARTree", Methodologie 1).
+// path uses FFMA.  Same epilogue as the tensor-core kernel ("DARTree:
+// Teaching a Chain-Trained Corrector to Think in Trees", Core Mechanism: one
+// batched head call per depth yields every branch's corrected distribution).
 //
 // A CTA of 128 threads owns contiguous 128-row weight tiles; thread t owns
 // weight row tile*128 + t and reads it straight from global memory with
@@ -24,11 +26,11 @@ namespace dt {
 
 constexpr int kSimtH = 256;  // state columns staged per slice
 
-template <int N, bool kLogits>
+template <int N>
 __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   float* sS = reinterpret_cast<float*>(smem_raw);                // [16][256] state slice
-  uint8_t* tail = reinterpret_cast<uint8_t*>(sS + 16 * kSimtH);  // epilogue or U rows
+  uint8_t* tail = reinterpret_cast<uint8_t*>(sS + 16 * kSimtH);  // epilogue
 
   const int tid = threadIdx.x;
   const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
@@ -36,7 +38,7 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
       static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
 
   LogitsEpilogue<N> epi;
-  if (kLogits) epi.init(tail, p.K, p.M, p.gth);
+  epi.init(tail, p.K, p.M, p.gth);
   pdl_wait();
   pdl_trigger();
   const int mcols = p.M < N ? p.M : N;  // columns that carry data
@@ -116,66 +118,34 @@ __global__ void __launch_bounds__(128) k_head_simt(const TcParams p) {
         acc[j] += zv;
       }
     };
-    if constexpr (kLogits) {
-      epi.tile_begin();
-      const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
-      if constexpr (N <= 64) {
-        static_for<0, N / 16>([&](auto i) {
-          constexpr int CH = decltype(i)::value;
-          if (CH * 16 < mcols) {
-            float acc[16];
-            dot16(acc, CH * 16);
-            add_z(acc, CH * 16);
-            epi.template chunk_static<CH>(acc, v0, p.rows);
-          }
-        });
-      } else {
-        for (int c0 = 0; c0 < mcols; c0 += 16) {
+    epi.tile_begin();
+    const uint32_t v0 = static_cast<uint32_t>(t * kTileV);
+    if constexpr (N <= 64) {
+      static_for<0, N / 16>([&](auto i) {
+        constexpr int CH = decltype(i)::value;
+        if (CH * 16 < mcols) {
           float acc[16];
-          dot16(acc, c0);
-          add_z(acc, c0);
-          epi.chunk_dyn(acc, c0, v0, p.rows);
+          dot16(acc, CH * 16);
+          add_z(acc, CH * 16);
+          epi.template chunk_static<CH>(acc, v0, p.rows);
         }
-      }
+      });
     } else {
-      // U = A S_in for the M input rows (kept per thread in shared memory),
-      // then output row q takes U[:, slot[q]]
-      float* Us = reinterpret_cast<float*>(tail) + tid * (N + 1);
       for (int c0 = 0; c0 < mcols; c0 += 16) {
         float acc[16];
         dot16(acc, c0);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) Us[c0 + j] = acc[j];
-      }
-      if (valid) {
-        const int n_out = pad_rows(p.M_out);
-        for (int q = 0; q < n_out; ++q) {
-          float out = 0.f;
-          if (q < p.M_out) {
-            int tok = __ldg(p.tok + q);
-            int col = __ldg(p.slot + q);
-            if (tok < 0 || tok >= p.V_tok || col < 0 || col >= p.M) {  // upstream failure only
-              atomicOr(p.err, DT_ERR_BAD_INDEX);
-              tok = 0;
-              col = 0;
-            }
-            out = tanhf(Us[col] + __ldg(p.E_f32 + static_cast<size_t>(tok) * p.H + row));
-          }
-          p.S_out_f32[static_cast<size_t>(q) * p.H + row] = out;
-        }
+        add_z(acc, c0);
+        epi.chunk_dyn(acc, c0, v0, p.rows);
       }
     }
   }
-  if constexpr (kLogits) {
-    epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
-  }
+  epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
 }
 
-template <int N, bool kLogits>
+template <int N>
 static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
-  const size_t smem = 16 * kSimtH * 4 + (kLogits ? epi_smem_bytes(N, p.K)
-                                                 : static_cast<size_t>(kTileV) * (N + 1) * 4);
-  return launch_kernel(k_head_simt<N, kLogits>, dim3(grid), dim3(128), smem, st, p.pdl != 0, p);
+  const size_t smem = 16 * kSimtH * 4 + epi_smem_bytes(N, p.K);
+  return launch_kernel(k_head_simt<N>, dim3(grid), dim3(128), smem, st, p.pdl != 0, p);
 }
 
 #ifndef DT_N
@@ -185,15 +155,10 @@ static cudaError_t launch_simt_n(const TcParams& p, int grid, cudaStream_t st) {
 #define DT_CAT2(a, b) a##b
 #define DT_CAT(a, b) DT_CAT2(a, b)
 
-cudaError_t DT_CAT(init_head_simt_attrs_, DT_N)() {
-  cudaError_t e = set_max_dynamic_smem(k_head_simt<DT_N, true>);
-  if (e != cudaSuccess) return e;
-  return set_max_dynamic_smem(k_head_simt<DT_N, false>);
-}
+cudaError_t DT_CAT(init_head_simt_attrs_, DT_N)() { return set_max_dynamic_smem(k_head_simt<DT_N>); }
 
-cudaError_t DT_CAT(launch_head_simt_, DT_N)(bool logits, const TcParams& p, int grid,
-                                             cudaStream_t st) {
-  return logits ? launch_simt_n<DT_N, true>(p, grid, st) : launch_simt_n<DT_N, false>(p, grid, st);
+cudaError_t DT_CAT(launch_head_simt_, DT_N)(const TcParams& p, int grid, cudaStream_t st) {
+  return launch_simt_n<DT_N>(p, grid, st);
 }
 
 }  // namespace dt

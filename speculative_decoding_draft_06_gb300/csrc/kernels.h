@@ -45,8 +45,6 @@ struct TcParams {
   const int32_t* tok;        // [M_out] committed token of each output row
   const uint16_t* E_bf16;    // [V][H]
   uint16_t* S_out_bf16;      // [rows_max][H]
-  const float* E_f32;
-  float* S_out_f32;
   int n_split;               // contraction split across CTAs (tensor-core path)
   int early_operands;        // the weights and S_in were complete before the previous
                              // kernel started: stream them before waiting for it
@@ -64,7 +62,7 @@ struct TcParams {
   cudaError_t launch_head_tc_##NN(bool logits, const CUtensorMap& tw, const CUtensorMap& ts, \
                                   const TcParams& p, int grid, cudaStream_t st);            \
   cudaError_t init_head_simt_attrs_##NN();                                                  \
-  cudaError_t launch_head_simt_##NN(bool logits, const TcParams& p, int grid, cudaStream_t st);
+  cudaError_t launch_head_simt_##NN(const TcParams& p, int grid, cudaStream_t st);
 DT_DECLARE_N(16)
 DT_DECLARE_N(32)
 DT_DECLARE_N(64)
@@ -95,14 +93,20 @@ cudaError_t init_head_rows_attrs();
 cudaError_t launch_head_rows(int M, int nv, bool pair, const CUtensorMap& tw, const CUtensorMap& ts,
                              const TcParams& p, int units, cudaStream_t st, int* units_used);
 
-inline cudaError_t launch_head_simt(int n_pad, bool logits, const TcParams& p, int grid,
-                                    cudaStream_t st) {
+// Logits head call with fp32 weights and at most 16 head rows, four threads
+// per weight row (head_f32.cu; W_f32 16-byte aligned).  head_f32_fits says
+// which calls it takes.
+bool head_f32_fits(int M, int H, int K);
+cudaError_t init_head_f32_attrs();
+cudaError_t launch_head_f32(const TcParams& p, int grid, cudaStream_t st);
+
+inline cudaError_t launch_head_simt(int n_pad, const TcParams& p, int grid, cudaStream_t st) {
   switch (n_pad) {
-    case 16: return launch_head_simt_16(logits, p, grid, st);
-    case 32: return launch_head_simt_32(logits, p, grid, st);
-    case 64: return launch_head_simt_64(logits, p, grid, st);
-    case 128: return launch_head_simt_128(logits, p, grid, st);
-    case 256: return launch_head_simt_256(logits, p, grid, st);
+    case 16: return launch_head_simt_16(p, grid, st);
+    case 32: return launch_head_simt_32(p, grid, st);
+    case 64: return launch_head_simt_64(p, grid, st);
+    case 128: return launch_head_simt_128(p, grid, st);
+    case 256: return launch_head_simt_256(p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -120,6 +124,21 @@ struct StateFinishParams {
   int* err;
 };
 cudaError_t launch_state_finish(const StateFinishParams& p, cudaStream_t st);
+
+// State step with fp32 weights: S_out[q] = tanh(A S_in[slot[q]] + E[tok[q]])
+// for q < M_out, zeros up to n_out.
+struct StateF32Params {
+  int pdl;             // launch with programmatic dependent launch (host only)
+  int H, M_in, M_out, n_out, V_tok;
+  const float* A;      // [H][H]
+  const float* S_in;   // [M_in][H]
+  const int32_t* slot; // [M_out] input row (parent) of each output row
+  const int32_t* tok;  // [M_out]
+  const float* E;      // [V][H]
+  float* S_out;        // [n_out][H]
+  int* err;
+};
+cudaError_t launch_state_f32(const StateF32Params& p, cudaStream_t st);
 
 // Merge of per-CTA partials into per-row lse and top-K (log-probs), and
 // (select != 0) the global top-W of each request with pool append.
@@ -300,6 +319,7 @@ inline cudaError_t init_head_attrs() {
   if ((e = init_head_tc_attrs_128()) != cudaSuccess) return e;
   if ((e = init_head_tc_attrs_256()) != cudaSuccess) return e;
   if ((e = init_head_rows_attrs()) != cudaSuccess) return e;
+  if ((e = init_head_f32_attrs()) != cudaSuccess) return e;
   if ((e = init_head_simt_attrs_16()) != cudaSuccess) return e;
   if ((e = init_head_simt_attrs_32()) != cudaSuccess) return e;
   if ((e = init_head_simt_attrs_64()) != cudaSuccess) return e;

@@ -671,6 +671,81 @@ __global__ void __launch_bounds__(256) k_state_finish(const StateFinishParams p)
                      (static_cast<uint32_t>(float_to_bf16_bits(o3)) << 16));
 }
 
+// State step with fp32 weights ("Technische Samenvatting: DARTree",
+// Methodologie 1: the kept branches carry their correction states): block b
+// owns hidden units [8 b, 8 b + 8), one per warp.  The warp loads its row of
+// A once (lanes over j, a chunk of 256 columns at a time) and computes
+// U[h][c] = sum_j A[h][j] S_in[c][j] for every input row c, four rows' loads
+// in flight together, each sum finished by a butterfly; U goes to shared
+// memory.  Then output row q, hidden unit 8 b + i is
+// tanh(U[h][slot[q]] + E[tok[q]][h]) (zeros for the padding rows).  The step
+// is a short latency chain, not a stream: few dependent load rounds per warp.
+__global__ void __launch_bounds__(256) k_state_f32(const StateF32Params p) {
+  extern __shared__ float sU[];  // [8][M_in]
+  pdl_wait();  // the input rows and the selection (slot, tok) come from earlier kernels
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 8 + warp;
+  if (h < p.H) {
+    const float* a = p.A + static_cast<size_t>(h) * p.H;
+    for (int j0 = 0; j0 < p.H; j0 += 256) {
+      float av[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int j = j0 + lane + 32 * k;
+        av[k] = j < p.H ? __ldg(a + j) : 0.f;
+      }
+      for (int c0 = 0; c0 < p.M_in; c0 += 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + u < p.M_in ? c0 + u : p.M_in - 1;
+          const float* x = p.S_in + static_cast<size_t>(c) * p.H;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int j = j0 + lane + 32 * k;
+            acc[u] = fmaf(av[k], j < p.H ? __ldcg(x + j) : 0.f, acc[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(kFullMask, acc[u], o);
+          if (lane == 0 && c0 + u < p.M_in) {
+            float* dst = sU + warp * p.M_in + c0 + u;
+            *dst = (j0 == 0 ? 0.f : *dst) + acc[u];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // outputs: thread (q, i) -> hidden unit 8 b + i of output row q
+  const int i = threadIdx.x & 7;
+  const int hh = blockIdx.x * 8 + i;
+  if (hh >= p.H) return;
+  bool bad = false;
+  for (int q = threadIdx.x >> 3; q < p.n_out; q += 32) {
+    float out = 0.f;
+    if (q < p.M_out) {
+      int col = __ldg(p.slot + q), tok = __ldg(p.tok + q);
+      if (col < 0 || col >= p.M_in) col = 0;  // (never, unless upstream failed)
+      if (tok < 0 || tok >= p.V_tok) {        // only after an upstream failure
+        bad = true;
+        tok = 0;
+      }
+      out = tanhf(sU[i * p.M_in + col] + __ldg(p.E + static_cast<size_t>(tok) * p.H + hh));
+    }
+    p.S_out[static_cast<size_t>(q) * p.H + hh] = out;
+  }
+  if (bad) atomicOr(p.err, DT_ERR_BAD_INDEX);
+}
+
+cudaError_t launch_state_f32(const StateF32Params& p, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(8) * p.M_in * 4;
+  return launch_kernel(k_state_f32, dim3((p.H + 7) / 8), dim3(256), smem, st, p.pdl != 0, p);
+}
+
 cudaError_t launch_state_finish(const StateFinishParams& p, cudaStream_t st) {
   if (p.H % 4 != 0) return cudaErrorInvalidValue;
   const dim3 grid(p.n_out, (p.H + 1023) / 1024);
