@@ -8,7 +8,8 @@
 // Tree attention on the 5th-generation tensor cores.  A CTA owns 128 query
 // rows (one TMEM lane each) of one request and one key/value head, and a
 // share of the key range (the keys are split over CTAs until one wave fills
-// the GPU; the last split to finish a query tile combines the partials).
+// the GPU; the last split to finish a query tile combines the partials,
+// whole rows per warp with coalesced 512-byte accesses).
 // Query row q of a key/value head is (node q / g, query head hk * g + q % g),
 // g = Hq / Hkv.  Row 0 (the root) sees the prefix; node i >= 1 sees the
 // prefix and the tree nodes of mask row i - 1.
@@ -31,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "../../include/dartree.h"
 #include "common.cuh"
@@ -107,22 +109,70 @@ __device__ __forceinline__ uint32_t sw128(int r, int gr) {
   return static_cast<uint32_t>(r * 128 + ((gr ^ (r & 7)) << 4));
 }
 
-// Publish this CTA's partial row half (unnormalised O, and the row's max
-// and sum in base 2); the last split of the query tile to arrive combines
-// all of them:
-//   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
-// All 256 softmax threads call it (thread = (row, half of the head dims)).
-__device__ __forceinline__ void combine_splits(const AttnParams& p, int r, int hk, int qt,
-                                               int split, int row, int half,
-                                               const float (&o)[kDh / 2], float m, float l) {
+constexpr int kOPitch = kDh + 4;  // floats per staged O row (16-byte rows spread over the banks)
+
+// Output row q of a query tile (node q / g, query head hk g + q % g).
+__device__ __forceinline__ size_t out_row(const AttnParams& p, int r, int hk, int q) {
+  const int node = q / p.g, h = hk * p.g + q % p.g;
+  return ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
+}
+
+// One row of 128 head dims by one warp: lane i writes dims 4i .. 4i + 3
+// (512 contiguous bytes of fp32, 256 of bf16).
+__device__ __forceinline__ void store_row(const AttnParams& p, size_t base, float4 v) {
+  const int lane = threadIdx.x & 31;
+  *reinterpret_cast<float4*>(p.O + base + 4 * lane) = v;
+  if (p.O16)
+    *reinterpret_cast<uint2*>(p.O16 + base + 4 * lane) =
+        make_uint2(cvt_bf16x2(v.x, v.y), cvt_bf16x2(v.z, v.w));
+}
+
+// The end of a query tile (the 256 softmax threads; thread = (row, half of
+// the head dims), holding its unnormalised O half, the row's max m and sum l
+// in base 2).  The rows are staged in shared memory (sO, the pipeline's
+// stage buffers, free once the last product has landed) so that each warp
+// then moves whole rows with 512-byte accesses.  One split: O = O_row / l.
+// Several: each split publishes its rows and (m, l); the last split of the
+// query tile to arrive combines them,
+//   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L,
+// in split order (deterministic).
+__device__ __forceinline__ void finish_tile(const AttnParams& p, int r, int hk, int qt, int split,
+                                            int row, int half, const float (&o)[kDh / 2],
+                                            float m, float l, float* sO) {
   constexpr int kOH = kDh / 2;
+  __shared__ float2 s_ml[kQRows];
   __shared__ int last;
-  const size_t tile = (static_cast<size_t>(r) * p.Hkv + hk) * p.q_tiles + qt;
-  float* po = p.part_O + ((tile * p.n_split + split) * kQRows + row) * kDh + half * kOH;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* dst = sO + row * kOPitch + half * kOH;
 #pragma unroll
   for (int i = 0; i < kOH; i += 4)
-    *reinterpret_cast<float4*>(po + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
-  if (half == 0) p.part_ml[(tile * p.n_split + split) * kQRows + row] = make_float2(m, l);
+    *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+  if (half == 0) s_ml[row] = make_float2(m, l);
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  const int q0 = qt * kQRows;
+  if (p.n_split == 1) {
+    for (int rr = warp; rr < kQRows; rr += 8) {
+      if (q0 + rr >= p.rows) break;
+      const float lr = s_ml[rr].y;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      float4 v = *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
+      v.x *= inv;
+      v.y *= inv;
+      v.z *= inv;
+      v.w *= inv;
+      store_row(p, out_row(p, r, hk, q0 + rr), v);
+    }
+    return;
+  }
+  const size_t tile = (static_cast<size_t>(r) * p.Hkv + hk) * p.q_tiles + qt;
+  float* po = p.part_O + (tile * p.n_split + split) * kQRows * kDh;
+  float2* pml = p.part_ml + (tile * p.n_split + split) * kQRows;
+  for (int rr = warp; rr < kQRows; rr += 8) {
+    if (q0 + rr >= p.rows) break;
+    *reinterpret_cast<float4*>(po + rr * kDh + 4 * lane) =
+        *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
+    if (lane == 0) pml[rr] = s_ml[rr];
+  }
   __threadfence();
   asm volatile("bar.sync 1, 256;" ::: "memory");
   if (threadIdx.x == 0) last = (atomicAdd(p.cnt + tile, 1) == p.n_split - 1);
@@ -131,41 +181,59 @@ __device__ __forceinline__ void combine_splits(const AttnParams& p, int r, int h
   __threadfence();
   const float* all_o = p.part_O + tile * p.n_split * kQRows * kDh;
   const float2* all_ml = p.part_ml + tile * p.n_split * kQRows;
-  const int q = qt * kQRows + row;
-  if (q < p.rows) {  // this thread combines its own row half over the splits
-    float M = -INFINITY;
-    for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, __ldcg(&all_ml[s * kQRows + row]).x);
-    float Lsum = 0.f;
-    float acc[kOH];
+  const int ns = p.n_split;  // <= 32: lane s holds split s's (m, l)
+  // the (m, l) of this warp's 16 rows, all loads in flight together
+  constexpr int kRows = kQRows / 8;
+  float2 ml[kRows];
 #pragma unroll
-    for (int c = 0; c < kOH; ++c) acc[c] = 0.f;
-    for (int s = 0; s < p.n_split; ++s) {  // fixed order: deterministic
-      const float2 ml = __ldcg(&all_ml[s * kQRows + row]);
-      const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
-      Lsum += ml.y * f;
-      const float4* src =
-          reinterpret_cast<const float4*>(all_o + (s * kQRows + row) * kDh + half * kOH);
+  for (int i = 0; i < kRows; ++i) {
+    const int rr = warp + 8 * i;
+    ml[i] = (lane < ns && q0 + rr < p.rows) ? __ldcg(&all_ml[lane * kQRows + rr])
+                                            : make_float2(-INFINITY, 0.f);
+  }
+  // four rows at a time: every split's partial row loaded before any is summed
 #pragma unroll
-      for (int c = 0; c < kOH / 4; ++c) {
-        const float4 v = __ldcg(src + c);
-        acc[4 * c] += v.x * f;
-        acc[4 * c + 1] += v.y * f;
-        acc[4 * c + 2] += v.z * f;
-        acc[4 * c + 3] += v.w * f;
+  for (int i0 = 0; i0 < kRows; i0 += 4) {
+    float f[4], L[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float M = ml[i0 + i].x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+      f[i] = ml[i0 + i].x == -INFINITY ? 0.f : fast_ex2(ml[i0 + i].x - M);
+      float ls = ml[i0 + i].y * f[i];
+      // the sum over the splits in split order (lane order), deterministic
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(kFullMask, ls, o);
+        if (lane >= o) ls += y;
+      }
+      L[i] = __shfl_sync(kFullMask, ls, 31);
+    }
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = 0; sp < ns; ++sp) {  // fixed order: deterministic
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = warp + 8 * (i0 + i);
+        const float fs = __shfl_sync(kFullMask, f[i], sp);
+        const float4 v =
+            __ldcg(reinterpret_cast<const float4*>(all_o + (sp * kQRows + rr) * kDh) + lane);
+        acc[i].x += v.x * fs;
+        acc[i].y += v.y * fs;
+        acc[i].z += v.z * fs;
+        acc[i].w += v.w * fs;
       }
     }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    const int node = q / p.g, h = hk * p.g + q % p.g;
-    const size_t base =
-        ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh + half * kOH;
 #pragma unroll
-    for (int c = 0; c < kOH; c += 4) {
-      const float4 out = make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv,
-                                     acc[c + 3] * inv);
-      *reinterpret_cast<float4*>(p.O + base + c) = out;
-      if (p.O16)
-        *reinterpret_cast<uint2*>(p.O16 + base + c) =
-            make_uint2(cvt_bf16x2(out.x, out.y), cvt_bf16x2(out.z, out.w));
+    for (int i = 0; i < 4; ++i) {
+      const int rr = warp + 8 * (i0 + i);
+      if (q0 + rr >= p.rows) continue;
+      const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
+      store_row(p, out_row(p, r, hk, q0 + rr),
+                make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv));
     }
   }
   if (threadIdx.x == 0) p.cnt[tile] = 0;
@@ -496,22 +564,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int c = 0; c < kOH; ++c) o[c] = 0.f;
       if (nt > 0) l = 0.f;
     }
-    if (p.n_split > 1) {
-      combine_splits(p, r, hk, qt, split, row, wg, o, m, l);
-    } else if (q < p.rows) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int h = hk * p.g + q % p.g;
-      const size_t base =
-          ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh + wg * kOH;
-#pragma unroll
-      for (int c = 0; c < kOH; c += 4) {
-        const float4 v = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
-        *reinterpret_cast<float4*>(p.O + base + c) = v;
-        if (p.O16)
-          *reinterpret_cast<uint2*>(p.O16 + base + c) =
-              make_uint2(cvt_bf16x2(v.x, v.y), cvt_bf16x2(v.z, v.w));
-      }
-    }
+    // the stage buffers are free: every product (the last reader) has landed
+    finish_tile(p, r, hk, qt, split, row, wg, o, m, l, reinterpret_cast<float*>(sStage));
   }
 
   tc_fence_before();
@@ -695,9 +749,12 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int n_split = sms / tiles;  // one CTA per SM
   n_split = n_split < kMaxSplit ? n_split : kMaxSplit;
-  // a split must keep at least 12 key tiles: the partials' round trip and
-  // the combine cost about as much as a dozen tiles
-  const int by_keys = key_tiles / 12;
+  // a split keeps at least 5 key tiles (tuning: DARTREE_ATTN_SPLIT_MIN): with
+  // fewer, the partials' round trip and the combine cost more than the tiles
+  // they save
+  int min_tiles = 5;
+  if (const char* v = getenv("DARTREE_ATTN_SPLIT_MIN")) min_tiles = atoi(v) > 0 ? atoi(v) : 1;
+  const int by_keys = key_tiles / min_tiles;
   n_split = n_split < by_keys ? n_split : by_keys;
   if (n_split < 1) n_split = 1;
   if ((reinterpret_cast<uintptr_t>(work) & 15) != 0) work = nullptr;
