@@ -21,9 +21,10 @@
 // allocator + single-thread MMA issuer.
 // One pass over the CTA's keys with an online softmax: S = Q K^T (M = 128
 // rows, N = 128 keys, K = 128 head dims) into double-buffered TMEM, P =
-// 2^(s - m) rounded to bf16 into shared memory (the 128-byte swizzled
-// K-major layout the MMA reads), O += P V (M = 128, N = 128 head dims,
-// K = 128 keys) in TMEM.  The reference maximum m is raised only
+// 2^(s - m) rounded to bf16 and stored to tensor memory (double-buffered;
+// each lane holds its row's weights, two keys per 32-bit column), O += P V
+// (M = 128, N = 128 head dims, K = 128 keys; A = P read from tensor memory,
+// B = the value tile in shared memory) in TMEM.  The reference maximum m is raised only
 // when a tile beats it by more than 8 (base 2), which rescales O in TMEM.
 // The rounded weights also form the normaliser, so O is an exact convex
 // combination of the visible values with weights within 2^-8 of the exact
@@ -46,19 +47,19 @@ constexpr int kDh = 128;           // head dimension (fixed)
 constexpr int kQRows = 128;        // query rows per CTA (TMEM lanes)
 constexpr int kKeys = 128;         // keys per tile
 constexpr int kVBlock = 64;        // keys per value-cache block (one swizzle atom)
-constexpr int kPBufs = 1;          // P buffers in shared memory
+constexpr int kPBufs = 2;          // P buffers in tensor memory
 constexpr int kAttnThreads = 320;
 constexpr int kSoftmaxThreads = 256;   // two warpgroups, one per half of each key tile
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kHalf = kKeys / 2;       // keys of a tile per warpgroup
 constexpr int kStages = 2;
 constexpr int kQBytes = kQRows * kDh * 2;        // 32 KB: 2 swizzle atoms of 64 head dims
-constexpr int kPBytes = kQRows * kKeys * 2;      // 32 KB: 2 atoms of 64 keys
 constexpr int kKBytes = kKeys * kDh * 2;         // 32 KB: 2 atoms of 64 head dims
 constexpr int kVBytes = kDh * kKeys * 2;         // 32 KB: 2 blocks of 128 head dims x 64 keys
 constexpr int kStageBytes = kKBytes + kVBytes;
-constexpr uint32_t kTmemCols = 512;              // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;      // P buffer b: 64 columns of bf16 pairs (128 keys) per lane
 
 struct AttnParams {
   int Lp, B, L, Hq, Hkv, g, words, rows;  // L = Lp + B keys; rows = (B + 1) * g
@@ -246,8 +247,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sP = sQ + kQBytes;
-  uint8_t* sStage = sP + kPBufs * kPBytes;
+  uint8_t* sStage = sQ + kQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + kStages * kStageBytes);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + kStages;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_m128<kKeys>();
       constexpr uint32_t idesc_o = idesc_bf16_m128<kDh>();
-      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      const uint32_t q_addr = smem_u32(sQ);
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
         if (ok && !*abort_flag && mbar_wait(bar, par, p.err, p.wait_limit)) return true;
@@ -379,13 +379,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!wait(&p_full[pb], static_cast<uint32_t>(j / kPBufs) & 1u)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sStage + stage * kStageBytes + kKBytes);
-        const uint32_t pa = p_addr + pb * kPBytes;
+        const uint32_t pa = tmem_base + kColP + static_cast<uint32_t>(pb * (kKeys / 2));
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32u;  // 16 keys within the 128-byte row
-          tc_mma_bf16(tmem_base + kColO, smem_desc_sw128(pa + (kk >> 2) * (kQRows * 128) + off),
-                      smem_desc_sw128(v_addr + (kk >> 2) * (kDh * 128) + off), idesc_o,
-                      (j != 0 || kk != 0) ? 1u : 0u);
+          // A = P from tensor memory: keys 16 kk .. 16 kk + 15 are 8 columns
+          tc_mma_bf16_ta(tmem_base + kColO, pa + static_cast<uint32_t>(kk * 8),
+                         smem_desc_sw128(v_addr + (kk >> 2) * (kDh * 128) + off), idesc_o,
+                         (j != 0 || kk != 0) ? 1u : 0u);
         }
         tc_commit(&p_empty[pb]);
         tc_commit(&kv_empty[stage]);
@@ -532,13 +533,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         *abort_flag = 1;
         continue;
       }
-      uint8_t* dst = sP + pb * kPBytes + wg * (kQRows * 128);  // this group's atom
-#pragma unroll
-      for (int gi = 0; gi < 8; ++gi)
-        *reinterpret_cast<uint4*>(dst + sw128(row, gi)) =
-            make_uint4(pk[gi * 4], pk[gi * 4 + 1], pk[gi * 4 + 2], pk[gi * 4 + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();  // the rescaled O is ordered before the next product
+      // this group's 64 keys of the tile: 32 columns of its lane's P row
+      tmem_st32(tmem_base + lane_base + kColP + static_cast<uint32_t>(pb * (kKeys / 2) + wg * 32),
+                pk);
+      tmem_wait_st();
+      tc_fence_before();  // P and the rescaled O are ordered before the next product
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
     }
@@ -736,7 +735,7 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   }
   const size_t smem =
-      1024 + kQBytes + kPBufs * kPBytes + static_cast<size_t>(kStages) * kStageBytes + 256;
+      1024 + kQBytes + static_cast<size_t>(kStages) * kStageBytes + 256;
   e = cudaFuncSetAttribute(k_tree_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
