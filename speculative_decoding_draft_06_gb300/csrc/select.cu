@@ -19,6 +19,16 @@
 
 namespace dt {
 
+// log(x) of a positive fp32 sum: the exponent's share e ln 2 in double, the
+// mantissa's log(f), f in [0.5, 1), in fp32 (absolute error ~1e-7: the
+// fp32 sum it is taken of carries more).  The double-precision log it
+// replaces ran on the GPU's few fp64 units in the merge's critical path.
+__device__ __forceinline__ double log_f32_exp(float x) {
+  int e;
+  const float f = frexpf(x, &e);
+  return static_cast<double>(e) * 0.69314718055994530942 + static_cast<double>(logf(f));
+}
+
 // ------------------------------------------------ merge of rows + top-W
 
 constexpr int kMergeThreads = 256;
@@ -390,11 +400,19 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
   __syncthreads();
   // ---- the (max, sum-exp) pairs, and the lists that reach the bound
   float m = -INFINITY, s = 0.f;
-  for (int i = threadIdx.x; i < n; i += kMergeThreads) {
-    const float mi = __ldcg(pmr + i), si = __ldcg(psr + i);
-    const uint64_t h = __ldcg(base + static_cast<size_t>(i) * K);
+  for (int i0 = 0; i0 < n; i0 += kMergeThreads) {  // the same trip count for every thread
+    const int i = i0 + threadIdx.x;
+    const bool ok = i < n;
+    const float mi = ok ? __ldcg(pmr + i) : -INFINITY, si = ok ? __ldcg(psr + i) : 0.f;
+    const uint64_t h = ok ? __ldcg(base + static_cast<size_t>(i) * K) : 0ull;
     lse_merge(m, s, mi, si);
-    if (h != 0ull && h >= th) rel[atomicAdd(&n_rel, 1)] = i;
+    // one shared atomic per warp for the lists that reach the bound
+    const bool in = h != 0ull && h >= th;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+    int at = 0;
+    if (lane == 0 && bal) at = atomicAdd(&n_rel, __popc(bal));
+    at = __shfl_sync(0xFFFFFFFFu, at, 0);
+    if (in) rel[at + __popc(bal & ((1u << lane) - 1u))] = i;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -416,11 +434,14 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
 #pragma unroll
     for (int q = 0; q < kPre; ++q) kk[q] = rel_key(f0 + q * kMergeThreads + threadIdx.x);
 #pragma unroll
-    for (int q = 0; q < kPre; ++q) {
-      if (kk[q] != 0ull && kk[q] >= th) {
-        const int pos = atomicAdd(&n_sv, 1);
-        if (pos < cap) sv[pos] = kk[q];
-      }
+    for (int q = 0; q < kPre; ++q) {  // one shared atomic per warp and round
+      const bool in = kk[q] != 0ull && kk[q] >= th;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+      int at = 0;
+      if (lane == 0 && bal) at = atomicAdd(&n_sv, __popc(bal));
+      at = __shfl_sync(0xFFFFFFFFu, at, 0);
+      const int pos = at + __popc(bal & ((1u << lane) - 1u));
+      if (in && pos < cap) sv[pos] = kk[q];
     }
   }
   __syncthreads();
@@ -451,7 +472,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
     float mm = -INFINITY, ss = 0.f;
     for (int w = 0; w < kMergeWarps; ++w) lse_merge(mm, ss, wls[w].x, wls[w].y);
     const double lse =
-        (mm == -INFINITY) ? -INFINITY : static_cast<double>(mm) + log(static_cast<double>(ss));
+        (mm == -INFINITY) ? -INFINITY : static_cast<double>(mm) + log_f32_exp(ss);
     if (lane == 0 && mm == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
     if (lane < K) {
       if (v == 0ull) atomicOr(p.err, DT_ERR_BAD_INDEX);  // fewer than K real entries
