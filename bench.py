@@ -126,7 +126,21 @@ def kernels_per_build(w: I.Workload, variant: str = "dartree", sms: int = 152) -
     if opt.get("expansion") == "bestfirst":      # root, init, B x (head, merge, step), states
         return 2 + 3 * w.B + (w.B - 1) * state
     base = 1 if opt.get("candidates") == "base" else 0
-    return 1 + base + w.D * 2 + (w.D - 1) * state + 1  # root, head + merge/select, states, prune
+    # fp32 head calls of at most 16 rows (k_head_f32) also compute the next
+    # state contraction, and their selection finishes the step: no launch
+    folded = 0
+    if not w.bf16 and not opt and w.H % 4 == 0 and f32_head_fits(w.H, w.K):
+        folded = sum(1 for m in w.head_rows()[:-1] if m <= 16)
+    # root, head + merge/select, states, prune
+    return 1 + base + w.D * 2 + (w.D - 1 - folded) * state + 1
+
+
+def f32_head_fits(H: int, K: int) -> bool:
+    """Shared memory of k_head_f32 (head rows, two tile-sum buffers, the
+    16-row epilogue) within its 200 KB."""
+    ld = -(-H // 256) * 256
+    epi = 16 * K * 8 + 2 * 16 * 132 * 4 + 4 * 16 * 8 + 4 * 32 * 8
+    return 16 * ld * 4 + 2 * 128 * 17 * 4 + epi <= 200 * 1024
 
 
 def _code_only(text: str) -> str:

@@ -80,6 +80,7 @@ struct dartree_ctx {
   // 1 for the top-W and the Top-B, 0 never
   int radix = -1;
   bool f32_split = true;   // fp32 head calls of <= 16 rows: four threads per weight row
+  bool f32_fold = true;    // ... which also compute the next state contraction
 
   // the captured build and the arguments it was captured with
   struct GraphKey {
@@ -254,9 +255,18 @@ cudaError_t alloc(T** p, size_t count) {
 dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, int32_t* tok,
                          float* logp, const dt::MergeParams* sel, cudaStream_t st);
 
+// fp32 head call by k_head_f32 (at most 16 rows, 16-byte rows)
+bool head_f32_path(const dartree_ctx* c, int M, int K) {
+  return !c->bf16 && c->f32_split && dt::head_f32_fits(M, c->cfg.H, K) &&
+         (reinterpret_cast<uintptr_t>(c->tm_Wout_ptr) & 15) == 0;
+}
+
+// A_fold (fp32 k_head_f32 calls only): the call also writes U = A S for its
+// rows to c->part, which the selection (sel->U_f32) turns into the next states.
 dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_req_stride,
                         int rows_per_req, int M, int K, double* lse, int32_t* tok, float* logp,
-                        const dt::MergeParams* sel, cudaStream_t st) {
+                        const dt::MergeParams* sel, cudaStream_t st,
+                        const float* A_fold = nullptr) {
   const int V = c->cfg.V, H = c->cfg.H;
   const int N = pad_rows(M);
   dt::TcParams p{};
@@ -299,9 +309,14 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
       p.max_stages = c->tc_max_stages;
       p.ctas_per_sm = c->tc_ctas_per_sm;
       e = dt::launch_head_tc(N, true, c->tm_Wout, c->tmS(sbuf, N), p, grid, st);
-    } else if (c->f32_split && dt::head_f32_fits(M, H, K) &&
-               (reinterpret_cast<uintptr_t>(c->tm_Wout_ptr) & 15) == 0) {
-      grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
+    } else if (head_f32_path(c, M, K)) {
+      int tiles = p.n_tiles;
+      if (A_fold) {  // the state tiles after the vocabulary's
+        p.A_f32 = A_fold;
+        p.U_f32 = c->part;
+        tiles += (H + dt::kTileV - 1) / dt::kTileV;
+      }
+      grid = tiles < c->num_sms ? tiles : c->num_sms;
       p.W_f32 = static_cast<const float*>(c->tm_Wout_ptr);
       p.S_f32 = static_cast<const float*>(c->S(sbuf));
       e = dt::launch_head_f32(p, grid, st);
@@ -599,9 +614,12 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
   }
   int F = 1, F_prev = 1, off_prev = 0, off = 0, cur = 0, sbuf = 0;
   int64_t calls = 0;
+  bool folded = false;  // this depth's states came with the previous selection
   for (int d = 1; d <= D; ++d) {
     const int M = R * F;
-    if (d >= 2) {
+    if (d >= 2 && folded) {
+      ++sbuf;
+    } else if (d >= 2) {
       // states of this depth's rows from their parents (the rows of call d-1)
       // A and the parent states (written three kernels back) are complete
       // before the merge that precedes this step starts: the step streams
@@ -630,6 +648,18 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
     sel.pool_depth = c->pool_depth;
     sel.pool_score = c->pool_score;
     sel.counters = c->counters;
+    // fp32 k_head_f32 call with a next depth: it computes U = A S for its
+    // rows, and the selection finishes the next depth's states (c->part is
+    // the bf16 state step's scratch, unused on this path)
+    const bool fold = !markov && !base && d < D && c->f32_fold && head_f32_path(c, M, K) &&
+                      (reinterpret_cast<uintptr_t>(head->A) & 15) == 0;
+    if (fold) {
+      sel.U_f32 = c->part;
+      sel.E_f32 = static_cast<const float*>(head->E);
+      sel.S_next_f32 = static_cast<float*>(c->S(sbuf + 1));
+      sel.H = H;
+      sel.V_tok = V;
+    }
     const size_t ro = static_cast<size_t>(d - 1) * dt::kMaxRows;
     if (base)
       s = run_cand(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
@@ -639,8 +669,9 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
     else
       s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
                    F, M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel,
-                   st);
+                   st, fold ? static_cast<const float*>(head->A) : nullptr);
     if (s != DARTREE_OK) return s;
+    folded = fold;
     ++calls;
     cur ^= 1;
     off_prev = off;
@@ -929,6 +960,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_GRAPH")) c->use_graph = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_RADIX")) c->radix = atoi(v) != 0 ? 1 : 0;
   if (const char* v = getenv("DARTREE_F32_SPLIT")) c->f32_split = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_F32_FOLD")) c->f32_fold = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;

@@ -8,18 +8,26 @@
 // operands far outside a 1e-5 score tolerance), so the products are FFMA.
 //
 // With fp32 weights the output projection is small (33 MB at V = 32000,
-// H = 256) and the call is bound by latency, not by a pipe: with one thread
-// per weight row and four warps per SM, each thread waited through rounds of
-// dependent loads.  Here a CTA of 512 threads owns 128-row tiles and four
-// threads share a weight row: thread (row, part) reads the row's float4
+// H = 256) and the call is bound by latency, not by a pipe.  A CTA of 640
+// threads owns 128-row tiles.  Warps 4-19 compute the dot products: four
+// threads share a weight row, thread (row, part) reading the row's float4
 // granules part, part + 4, part + 8, ... of each 256-column chunk -- its 16
-// loads issued before any is used, and the four threads of a row together
-// read 64 contiguous bytes per load -- multiplies them with the head rows
-// (staged in shared memory), and the four partial sums meet by two shuffles.
-// Sixteen warps per SM keep enough loads in flight.  The sums of a tile then
-// go through shared memory to warps 0-3 (thread t = vocabulary entry t, the
-// epilogue's layout), which run the epilogue while the other warps start the
-// next tile's loads.
+// loads issued before any is used, the four threads of a row together
+// reading 64 contiguous bytes per load -- and multiplying them with the head
+// rows (staged in shared memory); the four partial sums meet by two
+// shuffles.  Warps 0-3 run the epilogue only (thread t = vocabulary entry t
+// of the tile): the tile sums pass through a double buffer in shared memory
+// with named barriers (full: the dot warps arrive, the epilogue warps wait;
+// empty: the reverse), so the epilogue of tile i, which is longest on a
+// CTA's first tile while its lists fill, runs under the loads of tile i + 1
+// instead of delaying a quarter of them.  The epilogue warps load a tile's
+// base logits and row bounds before they wait for its sums.
+//
+// With A given, the next depth's state contraction U = A S_in rides along:
+// A's H rows are ceil(H / 128) more tiles after the vocabulary's, whose sums
+// the epilogue warps store as U[m][h] (the selection then finishes the step
+// as tanh(U[parent] + E[token])).  The call is latency-bound, so the extra
+// tiles cost little, and the state step needs no launch of its own.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -29,12 +37,23 @@
 namespace dt {
 namespace {
 
-constexpr int kF32Threads = 512;
-constexpr int kF32Chunk = 256;  // columns per load round (16 float4 per thread)
+constexpr int kF32Threads = 640;  // 4 epilogue warps + 16 dot-product warps
+constexpr int kF32Epi = 128;      // epilogue threads (warps 0-3)
+constexpr int kF32Chunk = 256;    // columns per load round (16 float4 per thread)
+
+// named barriers (0 is __syncthreads; the epilogue uses 1 and 3)
+__device__ __forceinline__ void nb_sync(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kF32Threads) : "memory");
+}
+__device__ __forceinline__ void nb_arrive(int id) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(kF32Threads) : "memory");
+}
+constexpr int kBarFull = 4;   // + buffer: the tile sums are written
+constexpr int kBarEmpty = 6;  // + buffer: the epilogue has read them
 
 // granules g = part + 4 k of a 256-column chunk (columns c0 + 4 g .. + 3),
 // in batches of NB loads issued together (16 for up to 8 head rows; two
-// batches of 8 for 16 rows, to stay within the registers of 512 threads)
+// batches of 8 for 16 rows, to stay within the registers of 640 threads)
 template <int J, int NB>
 __device__ __forceinline__ void chunk_dot(const float* wrow, bool valid, int part, int hn,
                                           const float* sS, int ldS, int c0, float (&acc)[16]) {
@@ -70,10 +89,11 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
   uint8_t* epi_smem = reinterpret_cast<uint8_t*>(sX + 2 * kTileV * 17);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int r_in = tid >> 2, part = tid & 3;  // weight row of the tile, its quarter
-  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
-  const int t_end =
-      static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
+  // vocabulary tiles, then (with A) the state tiles
+  const int n_all = p.n_tiles + (p.A_f32 ? (p.H + kTileV - 1) / kTileV : 0);
+  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * n_all) / gridDim.x);
+  const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * n_all) / gridDim.x);
+  const int n_t = t_end - t_begin;  // this CTA's tiles
 
   LogitsEpilogue<16> epi;
   if (warp < 4) epi.init(epi_smem, p.K, p.M, p.gth, p.gmx);
@@ -84,50 +104,73 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
     sS[e] = (j < p.M && c < p.H) ? __ldcg(p.S_f32 + static_cast<size_t>(j) * p.H + c) : 0.f;
   }
   __syncthreads();
-  const int J = p.M;  // live head rows (1..16)
+
+  if (warp >= 4) {
+    // ---- dot-product warps: 128 weight rows x 4 quarters
+    const int dt = tid - kF32Epi;
+    const int r_in = dt >> 2, part = dt & 3;
+    const int J = p.M;  // live head rows (1..16)
+    for (int i = 0; i < n_t; ++i) {
+      const int b = i & 1, t = t_begin + i;
+      const bool st_tile = t >= p.n_tiles;  // a tile of A's rows
+      const int row = (st_tile ? t - p.n_tiles : t) * kTileV + r_in;
+      const bool valid = row < (st_tile ? p.H : p.rows);
+      const float* wrow =
+          (st_tile ? p.A_f32 : p.W_f32) + static_cast<size_t>(valid ? row : 0) * p.H;
+      float acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+      for (int c0 = 0; c0 < p.H; c0 += kF32Chunk) {
+        const int hn = p.H - c0 < kF32Chunk ? p.H - c0 : kF32Chunk;
+        if (J <= 4)
+          chunk_dot<4, 16>(wrow, valid, part, hn, sS, ldS, c0, acc);
+        else if (J <= 8)
+          chunk_dot<8, 16>(wrow, valid, part, hn, sS, ldS, c0, acc);
+        else
+          chunk_dot<16, 8>(wrow, valid, part, hn, sS, ldS, c0, acc);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        acc[j] += __shfl_xor_sync(kFullMask, acc[j], 1);
+        acc[j] += __shfl_xor_sync(kFullMask, acc[j], 2);
+      }
+      if (i >= 2) nb_sync(kBarEmpty + b);  // the epilogue has read tile i - 2
+      if (part == 0) {
+        float* X = sX + b * kTileV * 17;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) X[r_in * 17 + j] = acc[j];
+      }
+      nb_arrive(kBarFull + b);
+    }
+    return;
+  }
+
+  // ---- epilogue warps: thread tid = vocabulary entry tid of the tile
   const bool one_req = p.rows_per_req >= p.M;
-  int buf = 0;
-  for (int t = t_begin; t < t_end; ++t, buf ^= 1) {
-    // the epilogue warps' row bounds, read while the tile's loads are in flight
-    if (warp < 4) epi.tile_begin();
-    // ---- all 512 threads: the tile's dot products
-    const int row = t * kTileV + r_in;
-    const bool valid = row < p.rows;
-    const float* wrow = p.W_f32 + static_cast<size_t>(valid ? row : 0) * p.H;
-    float acc[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    for (int c0 = 0; c0 < p.H; c0 += kF32Chunk) {
-      const int hn = p.H - c0 < kF32Chunk ? p.H - c0 : kF32Chunk;
-      if (J <= 4)
-        chunk_dot<4, 16>(wrow, valid, part, hn, sS, ldS, c0, acc);
-      else if (J <= 8)
-        chunk_dot<8, 16>(wrow, valid, part, hn, sS, ldS, c0, acc);
-      else
-        chunk_dot<16, 8>(wrow, valid, part, hn, sS, ldS, c0, acc);
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      acc[j] += __shfl_xor_sync(kFullMask, acc[j], 1);
-      acc[j] += __shfl_xor_sync(kFullMask, acc[j], 2);
-    }
-    float* X = sX + buf * kTileV * 17;
-    if (part == 0) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) X[r_in * 17 + j] = acc[j];
-    }
-    // the tile's sums are complete, and (double buffer) the epilogue of the
-    // tile before last has read its buffer
-    __syncthreads();
-    if (warp >= 4) continue;
-    // ---- warps 0-3: thread tid = vocabulary entry tid of the tile
+  for (int i = 0; i < n_t; ++i) {
+    const int b = i & 1, t = t_begin + i;
+    const bool st_tile = t >= p.n_tiles;
+    // the row bounds and the base logits, loaded before the sums are ready
+    if (!st_tile) epi.tile_begin();
     const int v = t * kTileV + tid;
-    const bool vv = v < p.rows;
+    const bool vv = !st_tile && v < p.rows;
+    const float z1 = (one_req && vv) ? __ldg(p.z + v) : 0.f;
+    nb_sync(kBarFull + b);
+    const float* X = sX + b * kTileV * 17;
     float x[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) x[j] = X[tid * 17 + j];
+    if (i + 2 < n_t) nb_arrive(kBarEmpty + b);  // the dot warps may refill buffer b
+    if (st_tile) {  // U[m][h] = (A S_in)[h, m], coalesced over h
+      const int hh = (t - p.n_tiles) * kTileV + tid;
+      if (hh < p.H) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < p.M) p.U_f32[static_cast<size_t>(j) * p.H + hh] = x[j];
+      }
+      continue;
+    }
     if (one_req) {
-      const float z1 = vv ? __ldg(p.z + v) : 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) x[j] += z1;
     } else {
@@ -145,7 +188,7 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
     }
     epi.template chunk_static<0>(x, static_cast<uint32_t>(t * kTileV), p.rows);
   }
-  if (warp < 4) epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
+  epi.finish(blockIdx.x, p.pm, p.ps, p.cta_stride, p.ptop, p.list_stride, p.err);
 }
 
 size_t f32_smem(int H, int K) {
@@ -163,7 +206,8 @@ bool head_f32_fits(int M, int H, int K) {
 cudaError_t init_head_f32_attrs() { return set_max_dynamic_smem(k_head_f32); }
 
 cudaError_t launch_head_f32(const TcParams& p, int grid, cudaStream_t st) {
-  if (!head_f32_fits(p.M, p.H, p.K) || (reinterpret_cast<uintptr_t>(p.W_f32) & 15))
+  if (!head_f32_fits(p.M, p.H, p.K) || (reinterpret_cast<uintptr_t>(p.W_f32) & 15) ||
+      (p.A_f32 && ((reinterpret_cast<uintptr_t>(p.A_f32) & 15) || !p.U_f32)))
     return cudaErrorInvalidValue;
   return launch_kernel(k_head_f32, dim3(grid), dim3(kF32Threads), f32_smem(p.H, p.K), st,
                        p.pdl != 0, p);

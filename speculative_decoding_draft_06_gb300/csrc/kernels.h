@@ -54,6 +54,11 @@ struct TcParams {
   // SIMT operands (fp32 path)
   const float* W_f32;        // [rows][H]
   const float* S_f32;        // [rows_max][H]
+  // k_head_f32 with the next depth's state contraction folded in: tiles
+  // n_tiles .. n_tiles + ceil(H / 128) - 1 take A's rows and write
+  // U = A S_in (row-major [M][H]) instead of logits
+  const float* A_f32;        // [H][H], 16-byte aligned, or null
+  float* U_f32;              // [M][H]
 };
 
 // One object file per MMA N (16, 32, 64, 128, 256) defines these.
@@ -179,6 +184,13 @@ struct MergeParams {
   int surv_cap;              // k_merge_bound: keys at or above the bound staged in shared
                              // memory (at most 512; more go the slow way)
   int radix;                 // top-W by block radix select (else merge folds / bitonic sort)
+  // fp32 state step folded into the selection (the head call wrote U = A S
+  // for its rows): the request's next rows S_next[m] = tanh(U[slot_next[m]]
+  // + E[tok_next[m]])
+  const float* U_f32;        // [R*F][H], or null: no state step here
+  const float* E_f32;        // [V_tok][H]
+  float* S_next_f32;         // [R*Fd][H]
+  int H, V_tok;
 };
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
 // The same merge (and selection) with one block per row that reads only the

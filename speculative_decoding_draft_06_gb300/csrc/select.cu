@@ -42,6 +42,10 @@ constexpr int kMergeWarps = kMergeThreads / 32;
 // children ranked by cumulative path log-probability, the W best survive;
 // "Accelerating Language Models with Diffusion Draft Trees", Summary: one
 // global top-W per depth, whose states go on to the next depth).
+// (parent row, token) of each next-depth row of the request, kept for the
+// folded fp32 state step (written by write_frontier, read by state_from_u)
+__shared__ int2 sh_next[kMaxRows];
+
 __device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k) {
   const int idx = static_cast<int>(key_index(k));
   const int i = idx / p.K, j = idx % p.K;
@@ -57,6 +61,46 @@ __device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k) {
   p.score_out[m] = c;
   p.tok_next[m] = tok;
   p.slot_next[m] = row;
+  if (p.U_f32) sh_next[q] = make_int2(row, tok);
+}
+
+// The fp32 state step after request r's selection, when the head call
+// computed U = A S for its rows: next row q of the request (parent row slot,
+// token tok, as write_frontier kept them in shared memory) is
+// tanh(U[slot] + E[tok]) ("DARTree: Teaching a Chain-Trained Corrector to
+// Think in Trees", Core Mechanism: the synthetic correction head's
+// recurrence).  The __syncthreads before the call makes the selection's
+// entries visible.  All threads of the block call it.
+__device__ void state_from_u(const MergeParams& p, int r) {
+  constexpr int kB = 4;  // elements per thread whose loads go out together
+  const int n = p.Fd * p.H;
+  bool bad = false;
+  for (int e0 = 0; e0 < n; e0 += kB * blockDim.x) {
+    float u[kB], ev[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const int e = e0 + k * blockDim.x + threadIdx.x;
+      u[k] = 0.f;
+      ev[k] = 0.f;
+      if (e < n) {
+        const int q = e / p.H, h = e - q * p.H;
+        int2 pt = sh_next[q];
+        if (pt.x < 0 || pt.x >= p.R * p.F) pt.x = 0;  // (never, unless upstream failed)
+        if (pt.y < 0 || pt.y >= p.V_tok) {            // only after an upstream failure
+          bad = true;
+          pt.y = 0;
+        }
+        u[k] = __ldcg(p.U_f32 + static_cast<size_t>(pt.x) * p.H + h);
+        ev[k] = __ldg(p.E_f32 + static_cast<size_t>(pt.y) * p.H + h);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const int e = e0 + k * blockDim.x + threadIdx.x;
+      if (e < n) p.S_next_f32[static_cast<size_t>(r) * p.Fd * p.H + e] = tanhf(u[k] + ev[k]);
+    }
+  }
+  if (bad) atomicOr(p.err, DT_ERR_BAD_INDEX);
 }
 
 // For |F_d| <= 32: every row's candidates are already sorted (log-probs
@@ -327,6 +371,10 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_rows(const MergeParams 
   __threadfence();
   select_frontier(p, r, dyn, wl);
   if (threadIdx.x == 0) p.counters[r] = 0;
+  if (p.U_f32) {
+    __syncthreads();
+    state_from_u(p, r);
+  }
 }
 
 static size_t select_smem(const MergeParams& p);
@@ -496,6 +544,10 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
   __threadfence();
   select_frontier(p, r, dyn, wl);
   if (threadIdx.x == 0) p.counters[r] = 0;
+  if (p.U_f32) {
+    __syncthreads();
+    state_from_u(p, r);
+  }
 }
 
 static size_t select_smem(const MergeParams& p) {

@@ -71,6 +71,9 @@ def test_build_bytes_match_the_closed_forms():
         assert bench.build_bytes(w) == closed, name
         assert abs(closed / 1e9 - gb) < 1e-3, name
     # launches per build: root, D head calls, D merges, D-1 two-kernel state
-    # steps (one kernel in fp32), prune
+    # steps, prune; fp32 head calls of at most 16 rows carry the state step
+    # (no launch), wider fp32 calls leave it to one kernel
     assert bench.kernels_per_build(I.CONFIGS["q8b"]) == 1 + 16 + 16 + 2 * 15 + 1
-    assert bench.kernels_per_build(I.CONFIGS["tiny"]) == 1 + 8 + 8 + 7 + 1
+    assert bench.kernels_per_build(I.CONFIGS["tiny"]) == 1 + 8 + 8 + 0 + 1
+    wide32 = I.CONFIGS["tiny"].replace(W=20)  # rows 1, 4, 16, 20, ...: depths 1-3 fold
+    assert bench.kernels_per_build(wide32) == 1 + 8 + 8 + 4 + 1

@@ -40,6 +40,10 @@ SMALL = [
     ("bf16-max", dict(V=1500, H=64, D=5, W=256, K=32, B=1024, beta=-0.05, bf16=True)),
     # fp32 at the limits, B above the pool (P = 800)
     ("f32-max", dict(V=700, H=32, D=4, W=256, K=32, B=1024, beta=0.0, bf16=False)),
+    # fp32, three requests of 4 rows: the state contraction rides on the head
+    # call (two state tiles, the second ragged) and each request's selection
+    # finishes its own rows
+    ("f32-multi", dict(V=1000, H=200, D=4, W=4, K=3, B=10, beta=-0.1, bf16=False, R=3)),
 ]
 
 
@@ -69,6 +73,15 @@ def test_build_with_the_row_group_merge_matches_oracle(monkeypatch, name):
     """The per-row group merge (every CTA list folded), forced here instead
     of the merge through the row bound, gives the same trees."""
     monkeypatch.setenv("DARTREE_MERGE_BOUND", "0")
+    test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
+
+
+@pytest.mark.parametrize("name", ["f32-ragged", "f32-multi"])
+def test_build_with_a_separate_state_step_matches_oracle(monkeypatch, name):
+    """fp32 builds of at most 16 rows with the state step as its own kernel
+    (instead of folded into the head call and the selection) give the same
+    trees."""
+    monkeypatch.setenv("DARTREE_F32_FOLD", "0")
     test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
 
 
