@@ -45,13 +45,21 @@ constexpr int kMergeWarps = kMergeThreads / 32;
 // (parent row, token) of each next-depth row of the request, kept for the
 // folded fp32 state step (written by write_frontier, read by state_from_u)
 __shared__ int2 sh_next[kMaxRows];
+// the request's candidate tokens [F][K], staged by the warp selection while
+// it loads their log-probs (F K <= kTokStage)
+constexpr int kTokStage = 1024;
+__shared__ int32_t sh_tok[kTokStage];
 
-__device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k) {
+// tok_sh: the request's candidate tokens in shared memory, or null (read
+// them from the merged rows)
+__device__ void write_frontier(const MergeParams& p, int r, int q, uint64_t k,
+                               const int32_t* tok_sh = nullptr) {
   const int idx = static_cast<int>(key_index(k));
   const int i = idx / p.K, j = idx % p.K;
   const int row = r * p.F + i;
   const float c = key_value(k);
-  const int32_t tok = __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + j);
+  const int32_t tok =
+      tok_sh ? tok_sh[idx] : __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + j);
   const size_t pi = static_cast<size_t>(r) * p.pool_stride + p.off + q;
   p.pool_parent[pi] = (p.depth == 1) ? -1 : p.off_prev + i;
   p.pool_token[pi] = tok;
@@ -106,32 +114,51 @@ __device__ void state_from_u(const MergeParams& p, int r) {
 // For |F_d| <= 32: every row's candidates are already sorted (log-probs
 // descending, one fp32 add keeps the order, ties by index), so the top |F_d|
 // is a fold of the F sorted lists with warp bitonic merges -- rows spread
-// over the warps, then a tree across warps.  All threads of the block call it.
+// over the warps, then a tree across warps.  The rows' log-probs, scores and
+// tokens (staged in shared memory for write_frontier) are loaded together
+// before the merges.  All threads of the block call it.
 __device__ void select_frontier_warp(const MergeParams& p, int r, uint64_t (*wl)[32]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int p2 = pow2_ceil32(p.Fd > p.K ? p.Fd : p.K);
+  const bool stage = p.F * p.K <= kTokStage;
+  constexpr int kRowsPre = 4;  // rows of this warp loaded up front (F <= 32: all of them)
   uint64_t v = 0ull;
-  for (int i = warp; i < p.F; i += nw) {
-    const int row = r * p.F + i;
-    uint64_t cur = 0ull;
-    if (lane < p.K) {
-      const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + lane);
-      const float c = __fadd_rn(__ldcg(p.score_in + row), lp);
-      cur = make_key(c, static_cast<uint32_t>(i * p.K + lane));
+  for (int i0 = warp; i0 < p.F; i0 += nw * kRowsPre) {
+    float lp[kRowsPre], sc[kRowsPre];
+#pragma unroll
+    for (int u = 0; u < kRowsPre; ++u) {
+      const int i = i0 + u * nw;
+      const int row = r * p.F + i;
+      lp[u] = 0.f;
+      sc[u] = 0.f;
+      if (i < p.F && lane < p.K) {
+        lp[u] = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + lane);
+        sc[u] = __ldcg(p.score_in + row);
+        if (stage)
+          sh_tok[i * p.K + lane] = __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + lane);
+      }
     }
-    uint64_t y = 0ull;
-    if (p2 == 32) {
-      y = shfl_u64(cur, 31 - lane);
-    } else {
-      const int src = 2 * p2 - 1 - lane;
-      const uint64_t b = shfl_u64(cur, src < 0 ? 0 : src);
-      v = lane < p2 ? v : (lane < 2 * p2 ? b : 0ull);
+#pragma unroll
+    for (int u = 0; u < kRowsPre; ++u) {
+      const int i = i0 + u * nw;
+      if (i >= p.F) break;  // the same for the whole warp
+      uint64_t cur = 0ull;
+      if (lane < p.K)
+        cur = make_key(__fadd_rn(sc[u], lp[u]), static_cast<uint32_t>(i * p.K + lane));
+      uint64_t y = 0ull;
+      if (p2 == 32) {
+        y = shfl_u64(cur, 31 - lane);
+      } else {
+        const int src = 2 * p2 - 1 - lane;
+        const uint64_t b = shfl_u64(cur, src < 0 ? 0 : src);
+        v = lane < p2 ? v : (lane < 2 * p2 ? b : 0ull);
+      }
+      v = warp_merge_desc(v, y, p2);
     }
-    v = warp_merge_desc(v, y, p2);
   }
-  v = block_tree_merge(v, wl, p2);
-  if (warp == 0 && lane < p.Fd) write_frontier(p, r, lane, v);
+  v = block_tree_merge(v, wl, p2);  // (its barriers also publish sh_tok)
+  if (warp == 0 && lane < p.Fd) write_frontier(p, r, lane, v, stage ? sh_tok : nullptr);
 }
 
 // Best 64 of two descending 64-key lists, each held by a warp as (element
@@ -419,68 +446,44 @@ constexpr int kSurvCap = 512;     // keys at or above the bound staged in shared
 // Row merge through the head call's row bound.  Block = one head row.  The
 // bound gth[row] never exceeds the row's K-th key (K keys of one CTA, or the
 // best keys of K CTA groups, reach it), so the row's top-K are among the
-// keys at or above it, and those sit at the front of the CTA lists whose
-// first key reaches it: the block reads every CTA's (max, sum-exp) pair and
-// first key, then only those lists, keeps their keys at or above the bound
-// (typically a few K of the n_cta K), and sorts them.  The log-sum-exp pairs
-// merge in fp32 in a fixed order (thread, lanes, warps).  With p.select set,
-// the last row of each request then runs the request's top-W selection.
-// Shared memory stays small (7.5 KB + the selection's).
+// keys at or above it: in one pass over memory (every load of a round in
+// flight together) the block reads every CTA's (max, sum-exp) pair and every
+// list key, keeps the keys at or above the bound (typically a few K of the
+// n_cta K), and sorts them.  The log-sum-exp pairs merge in fp32 in a fixed
+// order (thread, lanes, warps).  With p.select set, the last row of each
+// request then runs the request's top-W selection.  Shared memory stays
+// small (the selection's, the survivors' 4 KB and a few more).
 __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams p) {
   extern __shared__ uint64_t dyn[];  // the selection's keys
   __shared__ uint64_t wl[kMergeWarps][32];
   __shared__ float2 wls[kMergeWarps];
-  __shared__ int rel[kBoundParts];
   __shared__ uint64_t sv[kSurvCap];
-  __shared__ int n_rel, n_sv, last_flag;
+  __shared__ int n_sv, last_flag;
   const int row = blockIdx.x, K = p.K, p2 = pow2_ceil32(K), n = p.n_cta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    n_rel = 0;
-    n_sv = 0;
-  }
+  if (threadIdx.x == 0) n_sv = 0;
   pdl_wait();
   pdl_trigger();
   const uint64_t th = p.gth ? __ldcg(p.gth + row) : 0ull;
   const float* pmr = p.pm + static_cast<size_t>(row) * p.cta_stride;
   const float* psr = p.ps + static_cast<size_t>(row) * p.cta_stride;
-  const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;
-  __syncthreads();
-  // ---- the (max, sum-exp) pairs, and the lists that reach the bound
-  float m = -INFINITY, s = 0.f;
-  for (int i0 = 0; i0 < n; i0 += kMergeThreads) {  // the same trip count for every thread
-    const int i = i0 + threadIdx.x;
-    const bool ok = i < n;
-    const float mi = ok ? __ldcg(pmr + i) : -INFINITY, si = ok ? __ldcg(psr + i) : 0.f;
-    const uint64_t h = ok ? __ldcg(base + static_cast<size_t>(i) * K) : 0ull;
-    lse_merge(m, s, mi, si);
-    // one shared atomic per warp for the lists that reach the bound
-    const bool in = h != 0ull && h >= th;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
-    int at = 0;
-    if (lane == 0 && bal) at = atomicAdd(&n_rel, __popc(bal));
-    at = __shfl_sync(0xFFFFFFFFu, at, 0);
-    if (in) rel[at + __popc(bal & ((1u << lane) - 1u))] = i;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    lse_merge(m, s, m2, s2);
-  }
-  if (lane == 0) wls[warp] = make_float2(m, s);
-  __syncthreads();
-  // ---- their keys at or above the bound (in any order; the sort decides)
-  const int T = n_rel * K;
+  const uint64_t* base = p.ptop + static_cast<size_t>(row) * p.list_stride * K;  // [n][K]
+  // ---- the (max, sum-exp) pairs (n <= 2 x threads) and every list key at
+  // or above the bound (in any order; the sort decides), loaded together
+  const int i0 = threadIdx.x, i1 = threadIdx.x + kMergeThreads;
+  const float m0 = i0 < n ? __ldcg(pmr + i0) : -INFINITY, s0 = i0 < n ? __ldcg(psr + i0) : 0.f;
+  const float m1 = i1 < n ? __ldcg(pmr + i1) : -INFINITY, s1 = i1 < n ? __ldcg(psr + i1) : 0.f;
+  const int T = n * K;
   const int cap = p.surv_cap < kSurvCap ? (p.surv_cap > 0 ? p.surv_cap : 0) : kSurvCap;
   constexpr int kPre = 8;  // keys per thread loaded before any is staged
-  auto rel_key = [&](int f) {
-    return f < T ? __ldcg(base + static_cast<size_t>(rel[f / K]) * K + f % K) : 0ull;
-  };
+  __syncthreads();         // n_sv
   for (int f0 = 0; f0 < T; f0 += kMergeThreads * kPre) {
     uint64_t kk[kPre];
 #pragma unroll
-    for (int q = 0; q < kPre; ++q) kk[q] = rel_key(f0 + q * kMergeThreads + threadIdx.x);
+    for (int q = 0; q < kPre; ++q) {
+      const int f = f0 + q * kMergeThreads + threadIdx.x;
+      kk[q] = f < T ? __ldcg(base + f) : 0ull;
+    }
 #pragma unroll
     for (int q = 0; q < kPre; ++q) {  // one shared atomic per warp and round
       const bool in = kk[q] != 0ull && kk[q] >= th;
@@ -492,6 +495,16 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
       if (in && pos < cap) sv[pos] = kk[q];
     }
   }
+  float m = -INFINITY, s = 0.f;
+  lse_merge(m, s, m0, s0);
+  lse_merge(m, s, m1, s1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  if (lane == 0) wls[warp] = make_float2(m, s);
   __syncthreads();
   const int ns = n_sv;
   // ---- top-K of the survivors: warp 0 alone for a few, else every warp
@@ -510,15 +523,27 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
     for (int c0 = warp * 32; c0 < T; c0 += kMergeThreads * kPre) {
       uint64_t kk[kPre];
 #pragma unroll
-      for (int q = 0; q < kPre; ++q) kk[q] = rel_key(c0 + q * kMergeThreads + lane);
+      for (int q = 0; q < kPre; ++q) {
+        const int f = c0 + q * kMergeThreads + lane;
+        kk[q] = f < T ? __ldcg(base + f) : 0ull;
+      }
 #pragma unroll
       for (int q = 0; q < kPre; ++q) v = fold_chunk(v, kk[q] >= th ? kk[q] : 0ull, p2);
     }
     v = block_tree_merge(v, wl, p2);
   }
   if (warp == 0) {
-    float mm = -INFINITY, ss = 0.f;
-    for (int w = 0; w < kMergeWarps; ++w) lse_merge(mm, ss, wls[w].x, wls[w].y);
+    // the warps' pairs: lanes 0..7, a fixed shuffle tree, lane 0's result to all
+    float mm = lane < kMergeWarps ? wls[lane].x : -INFINITY;
+    float ss = lane < kMergeWarps ? wls[lane].y : 0.f;
+#pragma unroll
+    for (int o = kMergeWarps / 2; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mm, o);
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      lse_merge(mm, ss, m2, s2);
+    }
+    mm = __shfl_sync(0xFFFFFFFFu, mm, 0);
+    ss = __shfl_sync(0xFFFFFFFFu, ss, 0);
     const double lse =
         (mm == -INFINITY) ? -INFINITY : static_cast<double>(mm) + log_f32_exp(ss);
     if (lane == 0 && mm == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
