@@ -114,8 +114,12 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
  * on an SM; the row merge reads only the CTA lists that reach the head call's
  * row bound (K <= 16) unless DARTREE_MERGE_BOUND=0; the Top-B of pools of
  * 512 or more nodes is a block radix select (DARTREE_RADIX=0: never, =1: the
- * top-W and every Top-B as well).  Results
- * are the same under every setting (up to the order of fp32 additions). */
+ * top-W and every Top-B as well); the top-W of at most DARTREE_RANK_MAX
+ * candidates [512, at most 1024] is picked by rank counting; fp32 head calls
+ * of at most 16 rows use four threads per weight row unless
+ * DARTREE_F32_SPLIT=0, and also compute the next state contraction unless
+ * DARTREE_F32_FOLD=0.  Results are the same under every setting (up to the
+ * order of fp32 additions). */
 dartree_status dartree_create(const dartree_config *cfg, dartree_ctx **out);
 
 /* Releases the context and its workspace (synchronises the device). */

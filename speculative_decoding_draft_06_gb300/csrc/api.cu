@@ -81,6 +81,7 @@ struct dartree_ctx {
   int radix = -1;
   bool f32_split = true;   // fp32 head calls of <= 16 rows: four threads per weight row
   bool f32_fold = true;    // ... which also compute the next state contraction
+  int rank_max = 512;      // top-W by rank counting for at most this many candidates
 
   // the captured build and the arguments it was captured with
   struct GraphKey {
@@ -369,6 +370,7 @@ dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, i
   mp.gmx = c->gth + dt::kMaxRows;
   mp.surv_cap = c->merge_surv_cap;
   mp.radix = c->radix == 1;
+  mp.rank_max = c->rank_max;
   {
     KernelTimer tk(c, st, 2);
     e = c->merge_bound && dt::merge_bound_fits(mp) ? dt::launch_merge_bound(mp, st)
@@ -961,6 +963,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_RADIX")) c->radix = atoi(v) != 0 ? 1 : 0;
   if (const char* v = getenv("DARTREE_F32_SPLIT")) c->f32_split = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_F32_FOLD")) c->f32_fold = atoi(v) != 0;
+  if (const char* v = getenv("DARTREE_RANK_MAX")) c->rank_max = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;

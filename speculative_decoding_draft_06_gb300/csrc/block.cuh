@@ -55,6 +55,25 @@ inline __device__ uint64_t block_tree_merge(uint64_t v, uint64_t (*wl)[32], int 
   return v;
 }
 
+// The k largest of n distinct keys keys[0..n) (shared memory) into
+// out[0..k) in descending order: key i belongs at out[r], r = the number of
+// keys above it, whenever r < k (each count stops once it reaches k, so
+// most keys are dropped after a short scan).  Slots of out beyond n keep
+// their contents.  All threads of the block call it; the caller
+// synchronises before reading out.
+inline __device__ void block_rank_select(const uint64_t* keys, int n, int k, uint64_t* out) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint64_t x = keys[i];
+    int above = 0, j = 0;
+    for (; j + 8 <= n && above < k; j += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) above += keys[j + u] > x ? 1 : 0;
+    }
+    for (; j < n && above < k; ++j) above += keys[j] > x ? 1 : 0;
+    if (above < k) out[above] = x;
+  }
+}
+
 // Radix select of the k largest of n distinct 64-bit keys (k <= n).
 // Most significant digit first, 8 bits per pass: each pass histograms the
 // digit of the keys that share the prefix found so far, and one warp picks

@@ -183,7 +183,9 @@ struct MergeParams {
   int* counters;             // [R] zero between launches
   int surv_cap;              // k_merge_bound: keys at or above the bound staged in shared
                              // memory (at most 512; more go the slow way)
-  int radix;                 // top-W by block radix select (else merge folds / bitonic sort)
+  int radix;                 // top-W by block radix select (else as below)
+  int rank_max;              // top-W by rank counting when F K <= rank_max (else merge
+                             // folds / bitonic sort)
   // fp32 state step folded into the selection (the head call wrote U = A S
   // for its rows): the request's next rows S_next[m] = tanh(U[slot_next[m]]
   // + E[tok_next[m]])

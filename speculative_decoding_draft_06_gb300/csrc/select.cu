@@ -244,10 +244,36 @@ __device__ void select_frontier_radix(const MergeParams& p, int r, uint64_t* key
   for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, sel[q]);
 }
 
+// Top-|F_d| of the request's F K candidates by rank counting (F K at most
+// rank_max and kTokStage): each candidate's key (score + log-prob,
+// candidate index) is staged in shared memory with its token, and goes to
+// slot q = the number of keys above it when q < |F_d|.  keys: F K + |F_d|
+// slots.  All threads of the block call it.
+__device__ void select_frontier_rank(const MergeParams& p, int r, uint64_t* keys) {
+  const int n = p.F * p.K;
+  uint64_t* out = keys + n;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int i = e / p.K, j = e - i * p.K;
+    const int row = r * p.F + i;
+    const float lp = __ldcg(p.row_logp + static_cast<size_t>(row) * p.K + j);
+    const float sc = __ldcg(p.score_in + row);
+    sh_tok[e] = __ldcg(p.row_tok + static_cast<size_t>(row) * p.K + j);
+    keys[e] = make_key(__fadd_rn(sc, lp), static_cast<uint32_t>(e));
+  }
+  __syncthreads();
+  block_rank_select(keys, n, p.Fd, out);
+  __syncthreads();
+  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, out[q], sh_tok);
+}
+
 __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
                                 uint64_t (*wl)[32]) {
   if (p.radix) {
     select_frontier_radix(p, r, keys);
+    return;
+  }
+  if (p.F * p.K <= p.rank_max && p.F * p.K <= kTokStage) {
+    select_frontier_rank(p, r, keys);
     return;
   }
   if (p.Fd <= 32) {
@@ -505,20 +531,17 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
     lse_merge(m, s, m2, s2);
   }
   if (lane == 0) wls[warp] = make_float2(m, s);
+  if (threadIdx.x < 32) wl[0][threadIdx.x] = 0ull;  // the top-K slots (fewer survivors: empty)
   __syncthreads();
   const int ns = n_sv;
-  // ---- top-K of the survivors: warp 0 alone for a few, else every warp
-  // folds every 8th chunk of 32 and a tree merges the warps' lists; more
-  // than the buffer holds: every key of those lists, straight from memory
-  // (the ones below the bound as empty)
+  // ---- top-K of the survivors: by rank counting in shared memory; more
+  // than the buffer holds: every list key, straight from memory (the ones
+  // below the bound as empty), folded by every warp and a tree
   uint64_t v = 0ull;
-  if (ns <= cap / 8) {  // up to 64 with the full buffer
-    if (warp == 0)
-      for (int c0 = 0; c0 < ns; c0 += 32) v = fold_chunk(v, c0 + lane < ns ? sv[c0 + lane] : 0ull, p2);
-  } else if (ns <= cap) {
-    for (int c0 = warp * 32; c0 < ns; c0 += kMergeThreads)
-      v = fold_chunk(v, c0 + lane < ns ? sv[c0 + lane] : 0ull, p2);
-    v = block_tree_merge(v, wl, p2);
+  if (ns <= cap) {
+    block_rank_select(sv, ns, K, wl[0]);
+    __syncthreads();
+    v = wl[0][lane];  // (warp 0 uses it: lane = rank)
   } else {
     for (int c0 = warp * 32; c0 < T; c0 += kMergeThreads * kPre) {
       uint64_t kk[kPre];
@@ -581,6 +604,8 @@ static size_t select_smem(const MergeParams& p) {
     while (kp2 < p.Fd) kp2 <<= 1;
     return (static_cast<size_t>((p.F * p.K + 1) & ~1) + kp2) * 8;
   }
+  if (p.select && p.F * p.K <= p.rank_max && p.F * p.K <= kTokStage)
+    return static_cast<size_t>(p.F * p.K + p.Fd) * 8;
   if (p.select && (p.Fd > 64 || p.F > 64)) {
     int np2 = 1;
     while (np2 < p.F * p.K) np2 <<= 1;

@@ -76,6 +76,15 @@ def test_build_with_the_row_group_merge_matches_oracle(monkeypatch, name):
     test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
 
 
+@pytest.mark.parametrize("name", ["bf16-n16", "bf16-n32", "bf16-batch", "f32-ragged",
+                                  "f32-multi"])
+def test_build_with_the_merge_fold_top_w_matches_oracle(monkeypatch, name):
+    """The top-W by warp merge folds (instead of rank counting) gives the
+    same trees."""
+    monkeypatch.setenv("DARTREE_RANK_MAX", "0")
+    test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
+
+
 @pytest.mark.parametrize("name", ["f32-ragged", "f32-multi"])
 def test_build_with_a_separate_state_step_matches_oracle(monkeypatch, name):
     """fp32 builds of at most 16 rows with the state step as its own kernel
