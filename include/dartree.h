@@ -111,8 +111,8 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
  * DARTREE_ROWS_PAIR=0, and with at most 64 rows on one CTA streaming 64-row
  * state boxes unless DARTREE_ROWS_HALF_S=0; DARTREE_TC_MAX_STAGES caps the
  * pipeline depth and DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs
- * on an SM; the row merge reads only the CTA lists that reach the head call's
- * row bound (K <= 16) unless DARTREE_MERGE_BOUND=0; the Top-B of pools of
+ * on an SM; the row merge keeps only the list keys that reach the head
+ * call's row bound unless DARTREE_MERGE_BOUND=0; the Top-B of pools of
  * 512 or more nodes is a block radix select (DARTREE_RADIX=0: never, =1: the
  * top-W and every Top-B as well); the top-W of at most DARTREE_RANK_MAX
  * candidates [512, at most 1024] is picked by rank counting; fp32 head calls

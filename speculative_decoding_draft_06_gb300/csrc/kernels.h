@@ -195,8 +195,8 @@ struct MergeParams {
   int H, V_tok;
 };
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
-// The same merge (and selection) with one block per row that reads only the
-// CTA lists reaching the head call's row bound (K <= 16, at most 320
+// The same merge (and selection) with one block per row that keeps only the
+// list keys reaching the head call's row bound (K <= 32, at most 320
 // partials per row; merge_bound_fits says which).
 bool merge_bound_fits(const MergeParams& p);
 cudaError_t launch_merge_bound(const MergeParams& p, cudaStream_t st);

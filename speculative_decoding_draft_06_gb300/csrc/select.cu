@@ -615,10 +615,8 @@ static size_t select_smem(const MergeParams& p) {
   return 0;
 }
 
-// K <= 16: with K = 32 (wide trees, 64 rows) the build ran 0.8 % slower with
-// this merge than with the group merge, although the merge alone was faster.
 bool merge_bound_fits(const MergeParams& p) {
-  return p.n_cta >= 1 && p.n_cta <= kBoundParts && p.K >= 1 && p.K <= 16;
+  return p.n_cta >= 1 && p.n_cta <= kBoundParts && p.K >= 1 && p.K <= 32;
 }
 
 cudaError_t launch_merge_bound(const MergeParams& p, cudaStream_t st) {

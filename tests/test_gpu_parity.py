@@ -104,7 +104,7 @@ def test_build_with_radix_select_matches_oracle(monkeypatch, name):
 
 
 @pytest.mark.parametrize("cap", ["0", "40"])
-@pytest.mark.parametrize("name", ["bf16-n32", "bf16-batch", "f32-wide"])
+@pytest.mark.parametrize("name", ["bf16-n32", "bf16-n64", "bf16-batch", "f32-wide"])
 def test_build_with_small_bound_key_buffers_matches_oracle(monkeypatch, name, cap):
     """The merge through the row bound with a small staging buffer: with none,
     every key of the lists that reach the bound is folded straight from
