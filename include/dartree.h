@@ -112,9 +112,12 @@ int32_t dartree_pool_size(int32_t D, int32_t W, int32_t K);
  * state boxes unless DARTREE_ROWS_HALF_S=0; DARTREE_TC_MAX_STAGES caps the
  * pipeline depth and DARTREE_TC_CTAS_PER_SM=2 puts two vocabulary-on-M CTAs
  * on an SM; the row merge keeps only the list keys that reach the head
- * call's row bound unless DARTREE_MERGE_BOUND=0; the Top-B of pools of
- * 512 or more nodes is a block radix select (DARTREE_RADIX=0: never, =1: the
- * top-W and every Top-B as well); the top-W of at most DARTREE_RANK_MAX
+ * call's row bound unless DARTREE_MERGE_BOUND=0, with the row blocks of a
+ * request (at most 16) as one thread-block cluster that hands the rows to
+ * the selection in shared memory unless DARTREE_MERGE_CLUSTER=0; the Top-B
+ * of pools of 512 or more nodes is a block radix select (DARTREE_RADIX=0:
+ * never, =1: the top-W and every Top-B as well); the top-W of at most
+ * DARTREE_RANK_MAX
  * candidates [512, at most 1024] is picked by rank counting; fp32 head calls
  * of at most 16 rows use four threads per weight row unless
  * DARTREE_F32_SPLIT=0, and also compute the next state contraction unless

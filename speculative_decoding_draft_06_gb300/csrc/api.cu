@@ -82,6 +82,8 @@ struct dartree_ctx {
   bool f32_split = true;   // fp32 head calls of <= 16 rows: four threads per weight row
   bool f32_fold = true;    // ... which also compute the next state contraction
   int rank_max = 512;      // top-W by rank counting for at most this many candidates
+  bool merge_cluster = true;  // the row blocks of a request as one cluster (k_merge_bound)
+  int cluster_limit = 0;   // the largest such cluster the device schedules
 
   // the captured build and the arguments it was captured with
   struct GraphKey {
@@ -371,10 +373,12 @@ dartree_status run_merge(dartree_ctx* c, int n_cta, int M, int K, double* lse, i
   mp.surv_cap = c->merge_surv_cap;
   mp.radix = c->radix == 1;
   mp.rank_max = c->rank_max;
+  const bool bound = c->merge_bound && dt::merge_bound_fits(mp);
+  mp.cluster = bound && sel && c->merge_cluster && !mp.radix && sel->F <= c->cluster_limit &&
+               K <= 32;
   {
     KernelTimer tk(c, st, 2);
-    e = c->merge_bound && dt::merge_bound_fits(mp) ? dt::launch_merge_bound(mp, st)
-                                                   : dt::launch_merge_rows(mp, st);
+    e = bound ? dt::launch_merge_bound(mp, st) : dt::launch_merge_rows(mp, st);
   }
   if (e != cudaSuccess) return c->cuda_fail(e, "merge launch");
   return DARTREE_OK;
@@ -964,6 +968,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   if (const char* v = getenv("DARTREE_F32_SPLIT")) c->f32_split = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_F32_FOLD")) c->f32_fold = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_RANK_MAX")) c->rank_max = atoi(v);
+  if (const char* v = getenv("DARTREE_MERGE_CLUSTER")) c->merge_cluster = atoi(v) != 0;
   if (const char* v = getenv("DARTREE_ROWS_MIN")) c->rows_min = atoi(v);
   if (const char* v = getenv("DARTREE_ROWS_NV")) c->rows_nv = atoi(v) == 128 ? 128 : 256;
   if (const char* v = getenv("DARTREE_ROWS_PAIR")) c->rows_pair = atoi(v) != 0;
@@ -1057,6 +1062,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   }
   if (e == cudaSuccess) e = dt::init_head_attrs();
   if (e == cudaSuccess) e = dt::init_select_attrs();
+  if (e == cudaSuccess) c->cluster_limit = dt::merge_cluster_limit();
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(c);

@@ -186,6 +186,9 @@ struct MergeParams {
   int radix;                 // top-W by block radix select (else as below)
   int rank_max;              // top-W by rank counting when F K <= rank_max (else merge
                              // folds / bitonic sort)
+  int cluster;               // k_merge_bound with select: the F row blocks of a request
+                             // are one thread-block cluster (F <= kClusterRows); the rows
+                             // reach the selection through the leader's shared memory
   // fp32 state step folded into the selection (the head call wrote U = A S
   // for its rows): the request's next rows S_next[m] = tanh(U[slot_next[m]]
   // + E[tok_next[m]])
@@ -200,6 +203,10 @@ cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t st);
 // partials per row; merge_bound_fits says which).
 bool merge_bound_fits(const MergeParams& p);
 cudaError_t launch_merge_bound(const MergeParams& p, cudaStream_t st);
+// Largest cluster of k_merge_bound blocks the device schedules (at most
+// kClusterRows; 0 when clusters cannot be used).
+constexpr int kClusterRows = 16;
+int merge_cluster_limit();
 
 // Deferred Top-B, compaction and the ancestor mask.
 struct PruneParams {

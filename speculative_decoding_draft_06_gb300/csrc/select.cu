@@ -34,6 +34,36 @@ __device__ __forceinline__ double log_f32_exp(float x) {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
+// thread-block cluster access (the row blocks of a request, k_merge_bound)
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The cluster address of `p` (this CTA's shared memory) in the CTA of rank 0.
+__device__ __forceinline__ uint32_t cl_leader_addr(const void* p) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;"
+               : "=r"(a)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+  return a;
+}
+__device__ __forceinline__ void cl_store_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cl_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Split form for the start: every CTA of the cluster has begun (and its
+// shared memory exists) once the wait returns.
+__device__ __forceinline__ void cl_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Global top-W of one request's candidates (run by the last merge block of
 // the request).  Candidate (i, j) = child j of frontier slot i, score
 // c = score_i + logp_ij (one fp32 add), index i*K + j; the best |F_d| by
@@ -266,6 +296,20 @@ __device__ void select_frontier_rank(const MergeParams& p, int r, uint64_t* keys
   for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, out[q], sh_tok);
 }
 
+// The same selection from the rows' log-probs and tokens and the frontier
+// scores in this CTA's shared memory (the cluster leader's): no loads.
+__device__ void select_frontier_smem(const MergeParams& p, int r, uint64_t* keys,
+                                     const float* logp, const int32_t* tok, const float* score) {
+  const int n = p.F * p.K;
+  uint64_t* out = keys + n;
+  for (int e = threadIdx.x; e < n; e += blockDim.x)
+    keys[e] = make_key(__fadd_rn(score[e / p.K], logp[e]), static_cast<uint32_t>(e));
+  __syncthreads();
+  block_rank_select(keys, n, p.Fd, out);
+  __syncthreads();
+  for (int q = threadIdx.x; q < p.Fd; q += blockDim.x) write_frontier(p, r, q, out[q], tok);
+}
+
 __device__ void select_frontier(const MergeParams& p, int r, uint64_t* keys,
                                 uint64_t (*wl)[32]) {
   if (p.radix) {
@@ -478,18 +522,29 @@ constexpr int kSurvCap = 512;     // keys at or above the bound staged in shared
 // n_cta K), and sorts them.  The log-sum-exp pairs merge in fp32 in a fixed
 // order (thread, lanes, warps).  With p.select set, the last row of each
 // request then runs the request's top-W selection.  Shared memory stays
-// small (the selection's, the survivors' 4 KB and a few more).
+// small (the selection's, the survivors' 4 KB and a few more).  With
+// p.cluster the F row blocks of a request are one cluster: each row's
+// results also go to the leader's shared memory (distributed shared
+// memory), and after one cluster barrier the leader selects -- in place of
+// the global hand-over (fence, arrival count) and the selection's loads.
 __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams p) {
   extern __shared__ uint64_t dyn[];  // the selection's keys
   __shared__ uint64_t wl[kMergeWarps][32];
   __shared__ float2 wls[kMergeWarps];
   __shared__ uint64_t sv[kSurvCap];
   __shared__ int n_sv, last_flag;
+  __shared__ float cl_logp[kClusterRows * 32];  // cluster leader: the rows' results
+  __shared__ int32_t cl_tok[kClusterRows * 32];
+  __shared__ float cl_score[kClusterRows];
   const int row = blockIdx.x, K = p.K, p2 = pow2_ceil32(K), n = p.n_cta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) n_sv = 0;
+  if (p.cluster) cl_arrive_relaxed();  // (waited on before the first remote store)
   pdl_wait();
   pdl_trigger();
+  const int i_req = row % (p.F > 0 ? p.F : 1);  // this row within its request
+  if (p.cluster && i_req == 0 && threadIdx.x < p.F)  // the leader: frontier scores
+    cl_score[threadIdx.x] = __ldcg(p.score_in + row + threadIdx.x);
   const uint64_t th = p.gth ? __ldcg(p.gth + row) : 0ull;
   const float* pmr = p.pm + static_cast<size_t>(row) * p.cta_stride;
   const float* psr = p.ps + static_cast<size_t>(row) * p.cta_stride;
@@ -555,6 +610,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
     }
     v = block_tree_merge(v, wl, p2);
   }
+  if (p.cluster) cl_wait();  // the leader has started: its shared memory may be written
   if (warp == 0) {
     // the warps' pairs: lanes 0..7, a fixed shuffle tree, lane 0's result to all
     float mm = lane < kMergeWarps ? wls[lane].x : -INFINITY;
@@ -572,18 +628,34 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
     if (lane == 0 && mm == -INFINITY) atomicOr(p.err, DT_ERR_EMPTY_ROW);
     if (lane < K) {
       if (v == 0ull) atomicOr(p.err, DT_ERR_BAD_INDEX);  // fewer than K real entries
-      p.row_tok[static_cast<size_t>(row) * K + lane] = static_cast<int32_t>(key_index(v));
-      p.row_logp[static_cast<size_t>(row) * K + lane] =
-          static_cast<float>(static_cast<double>(key_value(v)) - lse);
+      const int32_t tk = static_cast<int32_t>(key_index(v));
+      const float lp = static_cast<float>(static_cast<double>(key_value(v)) - lse);
+      p.row_tok[static_cast<size_t>(row) * K + lane] = tk;
+      p.row_logp[static_cast<size_t>(row) * K + lane] = lp;
+      if (p.cluster) {  // the leader's copy, for its selection
+        const int e = i_req * K + lane;
+        cl_store_u32(cl_leader_addr(cl_tok + e), static_cast<uint32_t>(tk));
+        cl_store_u32(cl_leader_addr(cl_logp + e), __float_as_uint(lp));
+      }
     }
     if (lane == 0) p.row_lse[row] = lse;
     if (lane == 0 && p.gth) p.gth[row] = 0ull;  // the head call's bounds, ready for the next call
     if (p.gmx) p.gmx[static_cast<size_t>(row) * 32 + lane] = 0ull;
   }
   if (!p.select) return;
+  const int r = row / p.F;
+  if (p.cluster) {  // ---- one cluster per request: its leader selects
+    cl_barrier();
+    if (i_req != 0) return;
+    select_frontier_smem(p, r, dyn, cl_logp, cl_tok, cl_score);
+    if (p.U_f32) {
+      __syncthreads();
+      state_from_u(p, r);
+    }
+    return;
+  }
 
   // ---- the last row of request r runs its top-W selection
-  const int r = row / p.F;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) last_flag = (atomicAdd(p.counters + r, 1) == p.F - 1);
@@ -599,6 +671,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_bound(const MergeParams
 }
 
 static size_t select_smem(const MergeParams& p) {
+  if (p.select && p.cluster) return static_cast<size_t>(p.F * p.K + p.Fd) * 8;
   if (p.select && p.radix) {
     int kp2 = 1;
     while (kp2 < p.Fd) kp2 <<= 1;
@@ -621,8 +694,32 @@ bool merge_bound_fits(const MergeParams& p) {
 
 cudaError_t launch_merge_bound(const MergeParams& p, cudaStream_t st) {
   if (!merge_bound_fits(p)) return cudaErrorInvalidValue;
+  if (p.cluster) {
+    if (!p.select || p.F < 1 || p.F > kClusterRows || p.M % p.F != 0 || p.K > 32)
+      return cudaErrorInvalidValue;
+    return launch_kernel_cluster(k_merge_bound, dim3(p.M), dim3(kMergeThreads), select_smem(p),
+                                 st, p.pdl != 0, p.F, p);
+  }
   return launch_kernel(k_merge_bound, dim3(p.M), dim3(kMergeThreads), select_smem(p), st,
                        p.pdl != 0, p);
+}
+
+int merge_cluster_limit() {
+  if (cudaFuncSetAttribute(k_merge_bound, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kClusterRows);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(kClusterRows * 32 + 256) * 8;
+  int size = 0;
+  if (cudaOccupancyMaxPotentialClusterSize(&size, k_merge_bound, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return size < kClusterRows ? size : kClusterRows;
 }
 
 // ------------------------------------------------- Top-B, compaction, mask

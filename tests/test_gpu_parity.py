@@ -76,6 +76,16 @@ def test_build_with_the_row_group_merge_matches_oracle(monkeypatch, name):
     test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
 
 
+@pytest.mark.parametrize("name", ["bf16-n16", "bf16-batch", "bf16-k1w1", "f32-ragged",
+                                  "f32-multi"])
+def test_build_with_the_global_row_hand_over_matches_oracle(monkeypatch, name):
+    """The row blocks of a request handing their results to the selection
+    through global memory and an arrival count (instead of a thread-block
+    cluster and the leader's shared memory) give the same trees."""
+    monkeypatch.setenv("DARTREE_MERGE_CLUSTER", "0")
+    test_build_matches_oracle_small([s[0] for s in SMALL].index(name))
+
+
 @pytest.mark.parametrize("name", ["bf16-n16", "bf16-n32", "bf16-batch", "f32-ragged",
                                   "f32-multi"])
 def test_build_with_the_merge_fold_top_w_matches_oracle(monkeypatch, name):
