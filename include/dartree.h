@@ -199,8 +199,11 @@ dartree_status dartree_build_ex(dartree_ctx *ctx, const float *base_logits, cons
 
 /* Same as dartree_build with HOST base_logits, state0 and outputs (weights
  * stay on the device): copies the inputs into the context's staging buffers,
- * builds, copies the tree back and synchronises the stream.  Returns the
- * folded device status like dartree_sync_status. */
+ * builds, copies the tree back and synchronises the stream.  Depth 1's base
+ * logits and state0 are copied on `stream`; the later depths' on a context
+ * stream, overlapping the first head call (the head call of depth 2 waits
+ * for them).  The host buffers should be pinned (page-locked) for the copies
+ * to overlap.  Returns the folded device status like dartree_sync_status. */
 dartree_status dartree_build_host(dartree_ctx *ctx, const float *base_logits_host,
                                   const float *state0_host, const dartree_head *head, int32_t R,
                                   int32_t D, int32_t W, int32_t K, int32_t B, float beta,

@@ -92,7 +92,7 @@ struct dartree_ctx {
     int R, D, W, K, B;
     float beta;
     dartree_options opt;
-    int32_t unused;  // keeps the layout free of padding (the key is compared bytewise)
+    int32_t z_late;  // base logits of depth >= 2 arrive on the copy stream (dartree_build_host)
     dartree_tree out;
     cudaStream_t st;
     bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof o) == 0; }
@@ -139,15 +139,19 @@ struct dartree_ctx {
   float* bf_rlogp = nullptr;
   int last_expansion = DARTREE_EXPAND_DEPTHWISE;
   int last_B = 0;
-  // staging for dartree_build_host
+  // staging for dartree_build_host; its base logits past depth 1 are copied
+  // on copy_st while the first head call runs (z_ready: done, z_order: the
+  // previous work on the build stream is done with the staging)
+  cudaStream_t copy_st = nullptr;
+  cudaEvent_t z_ready = nullptr, z_order = nullptr;
   float* z_stage = nullptr;
   float* s0_stage = nullptr;
-  int32_t* o_parent = nullptr;
-  int32_t* o_token = nullptr;
-  int32_t* o_depth = nullptr;
-  float* o_score = nullptr;
-  uint32_t* o_mask = nullptr;
-  int32_t* o_nout = nullptr;
+  // the tree of a host build, laid out contiguously for its (R, B) so that
+  // one copy brings it back (o_all), and its pinned host image with the
+  // device check word after it (h_stage)
+  uint8_t* o_all = nullptr;
+  uint8_t* h_stage = nullptr;
+  size_t o_bytes = 0;
 
   std::vector<CUtensorMap> tm_S;  // [n_slots * kNumPads]
   void* S(int slot) const {
@@ -245,6 +249,20 @@ void flush_timing(dartree_ctx* c) {
   }
   c->ev_marks.clear();
   c->ev_used = 0;
+}
+
+// Offsets of the six tree arrays of R requests of B nodes in one region
+// (each 16-byte aligned): parent, token, depth, score, mask, n_out.  Returns
+// the region's size.
+size_t tree_layout(size_t R, size_t B, size_t* off) {
+  const size_t nb = R * B, nw = nb * ((B + 31) / 32);
+  const size_t sz[6] = {nb * 4, nb * 4, nb * 4, nb * 4, nw * 4, R * 4};
+  size_t at = 0;
+  for (int i = 0; i < 6; ++i) {
+    if (off) off[i] = at;
+    at += (sz[i] + 15) & ~static_cast<size_t>(15);
+  }
+  return at;
 }
 
 template <typename T>
@@ -573,9 +591,11 @@ dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
                              const dartree_head* head, int R, int D, int K, int B, float beta,
                              const dartree_options& o, const dartree_tree* out, cudaStream_t st);
 
+// z_wait: the base logits of depths >= 2 are complete once this event is
+// (the head call of depth 2 waits for it; depth 1's are complete on st).
 dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const dartree_head* head,
                          int R, int D, int W, int K, int B, float beta, const dartree_options& o,
-                         const dartree_tree* out, cudaStream_t st) {
+                         const dartree_tree* out, cudaStream_t st, cudaEvent_t z_wait = nullptr) {
   if (o.expansion == DARTREE_EXPAND_BESTFIRST)
     return run_bestfirst(c, z, s0, head, R, D, K, B, beta, o, out, st);
   const bool markov = o.head_kind == DARTREE_HEAD_MARKOV;
@@ -672,10 +692,18 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
                    c->cand + static_cast<size_t>(d - 1) * K, static_cast<long long>(D) * K, F, M,
                    K, head->Wout, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K,
                    &sel, st);
-    else
+    else {
+      if (z_wait && d == 2) {  // the first head call that reads the late base logits
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+        const cudaError_t ew = cudaStreamWaitEvent(
+            st, z_wait, cs == cudaStreamCaptureStatusActive ? cudaEventWaitExternal : 0);
+        if (ew != cudaSuccess) return c->cuda_fail(ew, "base-logit copy wait");
+      }
       s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
                    F, M, K, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K, &sel,
                    st, fold ? static_cast<const float*>(head->A) : nullptr);
+    }
     if (s != DARTREE_OK) return s;
     folded = fold;
     ++calls;
@@ -826,12 +854,13 @@ dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
 dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
                               const dartree_head* head, int R, int D, int W, int K, int B,
                               float beta, const dartree_options& o, const dartree_tree* out,
-                              cudaStream_t st) {
+                              cudaStream_t st, cudaEvent_t z_wait = nullptr) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (st != nullptr && cudaStreamIsCapturing(st, &cap) != cudaSuccess) cap = cudaStreamCaptureStatusNone;
   if (!c->use_graph || c->timing || st == nullptr || cap != cudaStreamCaptureStatusNone)
-    return run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st);
+    return run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st, z_wait);
   dartree_ctx::GraphKey key{};
+  key.z_late = z_wait != nullptr;
   key.opt = o;
   key.z = z;
   key.s0 = s0;
@@ -853,7 +882,7 @@ dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
     }
     cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return c->cuda_fail(e, "begin capture");
-    dartree_status s = run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st);
+    dartree_status s = run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st, z_wait);
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(st, &g);
     if (s != DARTREE_OK) {
@@ -895,13 +924,19 @@ void free_all(dartree_ctx* c) {
   free_events(c);
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   c->gexec = nullptr;
+  if (c->z_ready) cudaEventDestroy(c->z_ready);
+  if (c->z_order) cudaEventDestroy(c->z_order);
+  if (c->copy_st) cudaStreamDestroy(c->copy_st);
+  c->z_ready = c->z_order = nullptr;
+  c->copy_st = nullptr;
+  if (c->h_stage) cudaFreeHost(c->h_stage);
+  c->h_stage = nullptr;
   void* ptrs[] = {c->S_all,     c->score[0],    c->score[1],   c->tok_next,
                   c->slot_next, c->iota,       c->counters,    c->part,
                   c->row_cnt,   c->gpl,        c->gls,         c->gth,
                   c->pm,        c->ps,         c->ptop,        c->rows_lse,   c->rows_tok,
                   c->rows_logp, c->pool_parent, c->pool_token, c->pool_depth, c->pool_score,
-                  c->d_err,     c->z_stage,    c->s0_stage,    c->o_parent,   c->o_token,
-                  c->o_depth,   c->o_score,    c->o_mask,      c->o_nout,     c->cand,
+                  c->d_err,     c->z_stage,    c->s0_stage,    c->o_all,      c->cand,
                   c->base_part, c->base_cnt,   c->bf_par,      c->bf_tok,     c->bf_dep,
                   c->bf_rank,   c->bf_score,   c->bf_st,       c->bf_tok_next, c->bf_zrow,
                   c->bf_S,      c->bf_lse,     c->bf_rtok,     c->bf_rlogp,   c->bf_z};
@@ -1004,6 +1039,7 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
   const size_t RD = Rc * g.max_D;
   const size_t bfn = Rc * c->bf_nodes;
   const size_t slot_bytes = rows * g.H * c->elem;
+  c->o_bytes = tree_layout(Rc, B, nullptr);
   bool ok = alloc(reinterpret_cast<uint8_t**>(&c->S_all), c->n_slots * slot_bytes) == cudaSuccess &&
             alloc(&c->score[0], rows) == cudaSuccess && alloc(&c->score[1], rows) == cudaSuccess &&
             alloc(&c->tok_next, rows) == cudaSuccess && alloc(&c->slot_next, rows) == cudaSuccess &&
@@ -1025,10 +1061,8 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
             alloc(&c->d_err, 1) == cudaSuccess &&
             alloc(&c->z_stage, Rc * g.max_D * static_cast<size_t>(g.V)) == cudaSuccess &&
             alloc(&c->s0_stage, Rc * g.H) == cudaSuccess &&
-            alloc(&c->o_parent, Rc * B) == cudaSuccess && alloc(&c->o_token, Rc * B) == cudaSuccess &&
-            alloc(&c->o_depth, Rc * B) == cudaSuccess && alloc(&c->o_score, Rc * B) == cudaSuccess &&
-            alloc(&c->o_mask, Rc * B * words) == cudaSuccess &&
-            alloc(&c->o_nout, Rc) == cudaSuccess &&
+            alloc(&c->o_all, c->o_bytes) == cudaSuccess &&
+            cudaMallocHost(reinterpret_cast<void**>(&c->h_stage), c->o_bytes + 16) == cudaSuccess &&
             alloc(&c->cand, RD * g.max_K) == cudaSuccess &&
             alloc(&c->base_part, RD * c->base_chunks * g.max_K) == cudaSuccess &&
             alloc(&c->base_cnt, RD) == cudaSuccess &&
@@ -1060,6 +1094,9 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
     for (int i = 0; i < dt::kMaxRows; ++i) h_iota[i] = i;
     e = cudaMemcpy(c->iota, h_iota, sizeof h_iota, cudaMemcpyHostToDevice);
   }
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->copy_st, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->z_ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->z_order, cudaEventDisableTiming);
   if (e == cudaSuccess) e = dt::init_head_attrs();
   if (e == cudaSuccess) e = dt::init_select_attrs();
   if (e == cudaSuccess) c->cluster_limit = dt::merge_cluster_limit();
@@ -1112,6 +1149,10 @@ dartree_status dartree_build_ex(dartree_ctx* ctx, const float* base_logits, cons
                         static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+dartree_status status_from_word(dartree_ctx* ctx, int h);
+}  // namespace
+
 dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!ctx) {  // the context-free state step's check word on this device
@@ -1139,9 +1180,19 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
   flush_timing(ctx);
   int h = 0;
   e = cudaMemcpy(&h, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && h != 0) {
-    // a failed launch may have left arrival counters part-way: clear them so
-    // the next build starts from a clean workspace
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "error word read");
+  return status_from_word(ctx, h);
+}
+
+namespace {
+
+// The status a device check word stands for (after the stream's work is
+// complete).  A failed launch may have left arrival counters part-way: a
+// nonzero word also clears them and the word, so the next build starts from
+// a clean workspace.
+dartree_status status_from_word(dartree_ctx* ctx, int h) {
+  cudaError_t e = cudaSuccess;
+  if (h != 0) {
     e = cudaMemset(ctx->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->counters, 0, dt::kMaxRows * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->row_cnt, 0, dt::kMaxRows * sizeof(int));
@@ -1158,6 +1209,8 @@ dartree_status dartree_sync_status(dartree_ctx* ctx, void* stream) {
   return DARTREE_OK;
 }
 
+}  // namespace
+
 dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float* s0h,
                                   const dartree_head* head, int32_t R, int32_t D, int32_t W,
                                   int32_t K, int32_t B, float beta, const dartree_tree* out_host,
@@ -1166,27 +1219,47 @@ dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float
   dartree_status s = check_build_args(ctx, zh, s0h, head, R, D, W, K, B, beta, out_host);
   if (s != DARTREE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t zn = static_cast<size_t>(R) * D * ctx->cfg.V, sn = static_cast<size_t>(R) * ctx->cfg.H;
-  cudaError_t e = cudaMemcpyAsync(ctx->z_stage, zh, zn * 4, cudaMemcpyHostToDevice, st);
+  const size_t V = ctx->cfg.V, sn = static_cast<size_t>(R) * ctx->cfg.H;
+  const size_t pitch = static_cast<size_t>(D) * V * 4;  // one request's [D, V] rows
+  // depth 1's base logits of every request (and the root states) on the
+  // build stream; the later depths' on the copy stream, which the head call
+  // of depth 2 waits for -- the copy runs under the first head call
+  cudaError_t e = cudaMemcpy2DAsync(ctx->z_stage, pitch, zh, pitch, V * 4, R,
+                                    cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->s0_stage, s0h, sn * 4, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return ctx->cuda_fail(e, "input copy");
-  dartree_tree dev{ctx->o_parent, ctx->o_token, ctx->o_depth, ctx->o_score, ctx->o_mask, ctx->o_nout};
-  s = build_dispatch(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta,
-                     dartree_options{}, &dev, st);
-  if (s != DARTREE_OK) return s;
-  const size_t nb = static_cast<size_t>(R) * B, nw = nb * ((B + 31) / 32);
-  struct {
-    void* dst;
-    const void* src;
-    size_t bytes;
-  } cp[] = {{out_host->parent, ctx->o_parent, nb * 4}, {out_host->token, ctx->o_token, nb * 4},
-            {out_host->depth, ctx->o_depth, nb * 4},   {out_host->score, ctx->o_score, nb * 4},
-            {out_host->mask, ctx->o_mask, nw * 4},     {out_host->n_out, ctx->o_nout, static_cast<size_t>(R) * 4}};
-  for (auto& x : cp) {
-    e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return ctx->cuda_fail(e, "output copy");
+  const bool late = D > 1;
+  if (late) {
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->z_order, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->copy_st, ctx->z_order, 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(ctx->z_stage + V, pitch, zh + V, pitch, (D - 1) * V * 4, R,
+                            cudaMemcpyHostToDevice, ctx->copy_st);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->z_ready, ctx->copy_st);
   }
-  return dartree_sync_status(ctx, stream);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "input copy");
+  size_t off[6];
+  const size_t bytes = tree_layout(R, B, off);
+  uint8_t* o = ctx->o_all;
+  dartree_tree dev{reinterpret_cast<int32_t*>(o + off[0]), reinterpret_cast<int32_t*>(o + off[1]),
+                   reinterpret_cast<int32_t*>(o + off[2]), reinterpret_cast<float*>(o + off[3]),
+                   reinterpret_cast<uint32_t*>(o + off[4]), reinterpret_cast<int32_t*>(o + off[5])};
+  s = build_dispatch(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta,
+                     dartree_options{}, &dev, st, late ? ctx->z_ready : nullptr);
+  if (s != DARTREE_OK) return s;
+  // the tree in one copy, the check word in another, one synchronisation
+  int* h_err = reinterpret_cast<int*>(ctx->h_stage + ctx->o_bytes);
+  e = cudaMemcpyAsync(ctx->h_stage, o, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h_err, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "output copy");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return ctx->cuda_fail(e, "stream synchronize");
+  flush_timing(ctx);
+  const size_t nb = static_cast<size_t>(R) * B, nw = nb * ((B + 31) / 32);
+  void* dst[6] = {out_host->parent, out_host->token, out_host->depth,
+                  out_host->score,  out_host->mask,  out_host->n_out};
+  const size_t n[6] = {nb * 4, nb * 4, nb * 4, nb * 4, nw * 4, static_cast<size_t>(R) * 4};
+  for (int i = 0; i < 6; ++i) std::memcpy(dst[i], ctx->h_stage + off[i], n[i]);
+  return status_from_word(ctx, *h_err);
 }
 
 dartree_status dartree_set_timing(dartree_ctx* ctx, int32_t enable) {
