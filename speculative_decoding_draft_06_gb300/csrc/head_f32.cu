@@ -10,12 +10,10 @@
 // With fp32 weights the output projection is small (33 MB at V = 32000,
 // H = 256) and the call is bound by latency, not by a pipe.  A CTA of 640
 // threads owns 128-row tiles.  Warps 4-19 compute the dot products: four
-// threads share a weight row, thread (row, part) reading the row's float4
-// granules part, part + 4, part + 8, ... of each 256-column chunk -- its 16
-// loads issued before any is used, the four threads of a row together
-// reading 64 contiguous bytes per load -- and multiplying them with the head
-// rows (staged in shared memory); the four partial sums meet by two
-// shuffles.  Warps 0-3 run the epilogue only (thread t = vocabulary entry t
+// threads share a weight row (dot_tiles: the row's four threads read 64
+// contiguous bytes per load, the loads software-pipelined over the CTA's
+// tiles) and multiply them with the head rows (staged in shared memory);
+// the four partial sums meet by two shuffles.  Warps 0-3 run the epilogue only (thread t = vocabulary entry t
 // of the tile): the tile sums pass through a double buffer in shared memory
 // with named barriers (full: the dot warps arrive, the epilogue warps wait;
 // empty: the reverse), so the epilogue of tile i, which is longest on a
@@ -51,21 +49,41 @@ __device__ __forceinline__ void nb_arrive(int id) {
 constexpr int kBarFull = 4;   // + buffer: the tile sums are written
 constexpr int kBarEmpty = 6;  // + buffer: the epilogue has read them
 
-// granules g = part + 4 k of a 256-column chunk (columns c0 + 4 g .. + 3),
-// in batches of NB loads issued together (16 for up to 8 head rows; two
-// batches of 8 for 16 rows, to stay within the registers of 640 threads)
+// The dot-product warps' loop over this CTA's tiles for J live head rows.
+// Thread (row r_in, quarter part) reads the row's float4 granules part,
+// part + 4, ... of each 256-column chunk, in batches of NB (8 for up to 4
+// head rows, else 4: two batches' registers beside J accumulators).
+// The batches of all the CTA's tiles form one stream, software-pipelined:
+// the loads of batch b + 1 are issued before batch b is multiplied (also
+// across a tile's end, so the next tile's first loads are in flight during
+// the tile's reduction and hand-over), and the memory system does not wait
+// for the FFMAs.  A tile's four partial sums per row meet by two shuffles and
+// go to the tile-sum buffer (double-buffered with the epilogue warps).
 template <int J, int NB>
-__device__ __forceinline__ void chunk_dot(const float* wrow, bool valid, int part, int hn,
-                                          const float* sS, int ldS, int c0, float (&acc)[16]) {
-#pragma unroll
-  for (int k0 = 0; k0 < 16; k0 += NB) {
-    float4 w[NB];
+__device__ __forceinline__ void dot_tiles(const TcParams& p, const float* sS, int ldS, float* sX,
+                                          int t_begin, int n_t, int r_in, int part) {
+  constexpr int kPer = 16 / NB;  // batches per chunk
+  const int per_tile = kPer * ((p.H + kF32Chunk - 1) / kF32Chunk);  // batches per tile (even)
+  const int total = n_t * per_tile;
+  auto load = [&](int bt, float4 (&w)[NB]) {
+    const int i = bt / per_tile, rem = bt - i * per_tile;
+    const int c0 = (rem / kPer) * kF32Chunk, k0 = (rem % kPer) * NB;
+    const int t = t_begin + i;
+    const bool st = t >= p.n_tiles;  // a tile of A's rows
+    const int row = (st ? t - p.n_tiles : t) * kTileV + r_in;
+    const bool valid = row < (st ? p.H : p.rows);
+    const float4* wrow = reinterpret_cast<const float4*>(
+        (st ? p.A_f32 : p.W_f32) + static_cast<size_t>(valid ? row : 0) * p.H + c0);
+    const int hn = p.H - c0 < kF32Chunk ? p.H - c0 : kF32Chunk;
 #pragma unroll
     for (int k = 0; k < NB; ++k) {
       const int g = part + 4 * (k0 + k);
-      w[k] = (valid && 4 * g < hn) ? __ldg(reinterpret_cast<const float4*>(wrow + c0) + g)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[k] = (valid && 4 * g < hn) ? __ldg(wrow + g) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  auto fma = [&](int bt, const float4 (&w)[NB], float (&acc)[J]) {
+    const int rem = bt % per_tile;
+    const int c0 = (rem / kPer) * kF32Chunk, k0 = (rem % kPer) * NB;
 #pragma unroll
     for (int k = 0; k < NB; ++k) {
       const int col = c0 + 4 * (part + 4 * (k0 + k));
@@ -77,6 +95,34 @@ __device__ __forceinline__ void chunk_dot(const float* wrow, bool valid, int par
         acc[j] = fmaf(w[k].z, s.z, acc[j]);
         acc[j] = fmaf(w[k].w, s.w, acc[j]);
       }
+    }
+  };
+  float acc[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) acc[j] = 0.f;
+  float4 wa[NB], wb[NB];
+  if (total > 0) load(0, wa);
+  for (int bt = 0; bt < total; bt += 2) {  // a pair of batches of one tile
+    load(bt + 1, wb);
+    fma(bt, wa, acc);
+    if (bt + 2 < total) load(bt + 2, wa);
+    fma(bt + 1, wb, acc);
+    if ((bt + 2) % per_tile == 0) {  // the tile's end
+      const int i = bt / per_tile, b = i & 1;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        acc[j] += __shfl_xor_sync(kFullMask, acc[j], 1);
+        acc[j] += __shfl_xor_sync(kFullMask, acc[j], 2);
+      }
+      if (i >= 2) nb_sync(kBarEmpty + b);  // the epilogue has read tile i - 2
+      if (part == 0) {
+        float* X = sX + b * kTileV * 17;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) X[r_in * 17 + j] = j < J ? acc[j] : 0.f;
+      }
+      nb_arrive(kBarFull + b);
+#pragma unroll
+      for (int j = 0; j < J; ++j) acc[j] = 0.f;
     }
   }
 }
@@ -109,39 +155,12 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
     // ---- dot-product warps: 128 weight rows x 4 quarters
     const int dt = tid - kF32Epi;
     const int r_in = dt >> 2, part = dt & 3;
-    const int J = p.M;  // live head rows (1..16)
-    for (int i = 0; i < n_t; ++i) {
-      const int b = i & 1, t = t_begin + i;
-      const bool st_tile = t >= p.n_tiles;  // a tile of A's rows
-      const int row = (st_tile ? t - p.n_tiles : t) * kTileV + r_in;
-      const bool valid = row < (st_tile ? p.H : p.rows);
-      const float* wrow =
-          (st_tile ? p.A_f32 : p.W_f32) + static_cast<size_t>(valid ? row : 0) * p.H;
-      float acc[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-      for (int c0 = 0; c0 < p.H; c0 += kF32Chunk) {
-        const int hn = p.H - c0 < kF32Chunk ? p.H - c0 : kF32Chunk;
-        if (J <= 4)
-          chunk_dot<4, 16>(wrow, valid, part, hn, sS, ldS, c0, acc);
-        else if (J <= 8)
-          chunk_dot<8, 16>(wrow, valid, part, hn, sS, ldS, c0, acc);
-        else
-          chunk_dot<16, 8>(wrow, valid, part, hn, sS, ldS, c0, acc);
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        acc[j] += __shfl_xor_sync(kFullMask, acc[j], 1);
-        acc[j] += __shfl_xor_sync(kFullMask, acc[j], 2);
-      }
-      if (i >= 2) nb_sync(kBarEmpty + b);  // the epilogue has read tile i - 2
-      if (part == 0) {
-        float* X = sX + b * kTileV * 17;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) X[r_in * 17 + j] = acc[j];
-      }
-      nb_arrive(kBarFull + b);
-    }
+    if (p.M <= 4)
+      dot_tiles<4, 8>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
+    else if (p.M <= 8)
+      dot_tiles<8, 4>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
+    else
+      dot_tiles<16, 4>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
     return;
   }
 
