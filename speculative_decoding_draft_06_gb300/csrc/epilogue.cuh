@@ -172,23 +172,30 @@ static __device__ __forceinline__ void list_update(uint64_t* L, int K, uint64_t*
 }
 
 // This CTA's best key of a row improved: raise its group's maximum (group =
-// CTA % K), then the row's bound gth to the least of the K group maxima (K
-// distinct keys at or above it; the new value stands in for this CTA's
-// group).  Warp-collective.
-static __device__ __noinline__ void publish_group_best(unsigned long long* gth,
-                                                       unsigned long long* gm, int K,
-                                                       uint64_t best) {
-  const int lane = threadIdx.x & 31;
+// CTA % K), then the row's bound gth to the least of K keys of K groups --
+// this CTA's best and the other groups' maxima as read at the start of the
+// tile (others_min; a group's maximum only grows, so an earlier value is
+// still one of its CTAs' keys).  Keys of different CTAs are different
+// vocabulary entries, so these are K distinct keys of the row and their
+// least bounds its K-th key from below.  Nothing waits for a result.
+__device__ __forceinline__ void publish_group_best(unsigned long long* gth,
+                                                   unsigned long long* gm, int K,
+                                                   uint64_t best, uint64_t others_min) {
+  atomicMax(gm + blockIdx.x % K, best);
+  const uint64_t v = others_min < best ? others_min : best;
+  if (v > 0ull) atomicMax(gth, v);
+}
+
+// The least of the other K - 1 groups' maxima of a row (all ones for K = 1).
+__device__ __forceinline__ uint64_t others_min(const unsigned long long* gm, int K) {
   const int mine = blockIdx.x % K;
-  if (lane == 0) atomicMax(gm + mine, best);
-  uint64_t v = lane < K ? __ldcg(gm + lane) : ~0ull;
-  if (lane == mine) v = v > best ? v : best;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t w = shfl_xor_u64(v, o);
-    v = w < v ? w : v;
+  uint64_t v = ~0ull;
+#pragma unroll 8
+  for (int g = 0; g < K; ++g) {
+    const uint64_t x = g == mine ? ~0ull : __ldcg(gm + g);
+    v = x < v ? x : v;
   }
-  if (lane == 0 && v != ~0ull && v > 0ull) atomicMax(gth, v);
+  return v;
 }
 
 // Shared-memory footprint of the epilogue (bytes) for N rows, top-K and NG
@@ -199,6 +206,7 @@ __host__ __device__ constexpr size_t epi_smem_bytes(int N, int K, int NG = 1) {
          + static_cast<size_t>(N) * 8                       // running (max, sum) per row
          + static_cast<size_t>(N) * 8                       // per-tile copy of the row bounds
          + static_cast<size_t>(N) * 8                       // best keys as last published
+         + static_cast<size_t>(N) * 8                       // other groups' least maximum
          + static_cast<size_t>(NG) * 4 * 32 * 8;            // entrant staging, 32 keys per warp
 }
 
@@ -221,6 +229,7 @@ struct LogitsEpilogue {
   unsigned long long* gmx;  // [N][32] per-row best key of each CTA group (or null)
   uint64_t* gcache;         // [N] this tile's copy of gth
   uint64_t* gpub;           // [N] this CTA's best key per row as last published
+  uint64_t* gomin;          // [N] the other CTA groups' least best key, per tile
   uint64_t* stg;            // [32] entrant staging of this warp
   float* T;                 // [2][16][kTPitch] of this group
   float2* run;              // [N] (N > 64)
@@ -255,7 +264,8 @@ struct LogitsEpilogue {
     w4 = t >> 5;
     T = T0 + g * 2 * 16 * kTPitch;
     gpub = gcache + N;
-    stg = gpub + N + (tt >> 5) * 32;
+    gomin = gpub + N;
+    stg = gomin + N + (tt >> 5) * 32;
     nchunk = 0;
     bad = false;
 #pragma unroll
@@ -268,18 +278,21 @@ struct LogitsEpilogue {
       run[c] = make_float2(-INFINITY, 0.f);
       gcache[c] = 0ull;
       gpub[c] = 0ull;
+      gomin[c] = 0ull;
     }
     asm volatile("bar.sync 3, %0;" ::"r"(kThreads) : "memory");
   }
 
-  // At the start of a tile: this warp's rows' global bounds, all loads in
-  // flight together (the list update then reads shared memory only).
+  // At the start of a tile: this warp's rows' global bounds and the other
+  // CTA groups' least best key, all loads in flight together (the list
+  // update and the bound publishing then read shared memory only).
   __device__ __forceinline__ void tile_begin() {
     if (!gth) return;
     for (int i = lane;; i += 32) {
       const int c = ((i >> 2) * NG + g) * 16 + w4 + 4 * (i & 3);
       if (c >= M) break;
       gcache[c] = __ldcg(gth + c);
+      if (gmx) gomin[c] = others_min(gmx + static_cast<size_t>(c) * 32, K);
     }
     __syncwarp();
   }
@@ -316,9 +329,10 @@ struct LogitsEpilogue {
     const uint64_t k_after = L[K - 1], best = L[0];
     if (gth && lane == 0 && k_after > th) atomicMax(gth + c, k_after);
     if (gmx && best > gpub[c]) {
-      publish_group_best(gth + c, gmx + static_cast<size_t>(c) * 32, K, best);
-      __syncwarp();
-      if (lane == 0) gpub[c] = best;
+      if (lane == 0) {
+        publish_group_best(gth + c, gmx + static_cast<size_t>(c) * 32, K, best, gomin[c]);
+        gpub[c] = best;
+      }
       __syncwarp();
     }
   }
