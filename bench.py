@@ -533,7 +533,11 @@ def run_gpu(args) -> None:
     big = [m for m in w.head_rows() if m >= ROWS_MIN]
     kernel_name = {
         "head": ("k_cand_logits (candidate logits)" if opt.get("candidates") == "base" else
-                 "k_head_simt" if not w.bf16 else
+                 ("k_head_f32 (fp32 head call, at most 16 rows: 16 dot-product warps, 4 epilogue "
+                  "warps; also the next state contraction)"
+                  if not w.bf16 and max(w.head_rows()) <= 16 and w.H % 4 == 0
+                  and f32_head_fits(w.H, w.K) else "k_head_simt (fp32 head call)")
+                 if not w.bf16 else
                  "k_head_tc (head call: Wout stream, fused log-softmax + top-K)" if not big else
                  f"k_head_rows (head call, {max(big)} head rows on the MMA M side: Wout stream, "
                  f"fused log-softmax + top-K; calls with fewer than {ROWS_MIN} rows: k_head_tc)"),
