@@ -106,6 +106,11 @@ def kernel_bytes_per_launch(w: I.Workload, variant: str, kind: str) -> float | N
             per = [w.R * w.K * w.H * wb + m * w.H * wb + w.R * w.K * 4 for m in rows]
         else:
             per = [w.V * w.H * wb + w.R * w.V * 4 + m * w.H * wb for m in rows]
+            if not w.bf16 and not opt and w.H % 4 == 0 and f32_head_fits(w.H, w.K):
+                # fp32 head calls of at most 16 rows with a next depth also
+                # stream A (the folded state contraction)
+                per = [b + (w.H * w.H * 4 if m <= 16 and d < w.D else 0)
+                       for d, (b, m) in enumerate(zip(per, rows), start=1)]
         return sum(per) / len(per)
     if kind == "state":
         # parent states in, the tokens' embedding rows, new states out (+ A)
