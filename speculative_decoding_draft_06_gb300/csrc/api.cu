@@ -92,7 +92,8 @@ struct dartree_ctx {
     int R, D, W, K, B;
     float beta;
     dartree_options opt;
-    int32_t z_late;  // base logits of depth >= 2 arrive on the copy stream (dartree_build_host)
+    int32_t z_late;  // base logits of depth >= 2 arrive on the copy stream (dartree_build_host):
+                     // 1 all before head call 2, 2 each before its own head call
     dartree_tree out;
     cudaStream_t st;
     bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof o) == 0; }
@@ -143,7 +144,8 @@ struct dartree_ctx {
   // on copy_st while the first head call runs (z_ready: done, z_order: the
   // previous work on the build stream is done with the staging)
   cudaStream_t copy_st = nullptr;
-  cudaEvent_t z_ready = nullptr, z_order = nullptr;
+  cudaEvent_t z_order = nullptr;
+  std::vector<cudaEvent_t> z_ready;  // [max_D + 1]: depth d's base logits are complete
   float* z_stage = nullptr;
   float* s0_stage = nullptr;
   // the tree of a host build, laid out contiguously for its (R, B) so that
@@ -591,11 +593,12 @@ dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
                              const dartree_head* head, int R, int D, int K, int B, float beta,
                              const dartree_options& o, const dartree_tree* out, cudaStream_t st);
 
-// z_wait: the base logits of depths >= 2 are complete once this event is
-// (the head call of depth 2 waits for it; depth 1's are complete on st).
+// z_wait (or null): z_wait[d], where not null, is complete once the base
+// logits the head call of depth d reads are (depth 1's are complete on st).
 dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const dartree_head* head,
                          int R, int D, int W, int K, int B, float beta, const dartree_options& o,
-                         const dartree_tree* out, cudaStream_t st, cudaEvent_t z_wait = nullptr) {
+                         const dartree_tree* out, cudaStream_t st,
+                         const cudaEvent_t* z_wait = nullptr) {
   if (o.expansion == DARTREE_EXPAND_BESTFIRST)
     return run_bestfirst(c, z, s0, head, R, D, K, B, beta, o, out, st);
   const bool markov = o.head_kind == DARTREE_HEAD_MARKOV;
@@ -693,11 +696,11 @@ dartree_status run_build(dartree_ctx* c, const float* z, const float* s0, const 
                    K, head->Wout, c->rows_lse + ro, c->rows_tok + ro * K, c->rows_logp + ro * K,
                    &sel, st);
     else {
-      if (z_wait && d == 2) {  // the first head call that reads the late base logits
+      if (z_wait && z_wait[d]) {  // this depth's base logits come from the copy stream
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
         const cudaError_t ew = cudaStreamWaitEvent(
-            st, z_wait, cs == cudaStreamCaptureStatusActive ? cudaEventWaitExternal : 0);
+            st, z_wait[d], cs == cudaStreamCaptureStatusActive ? cudaEventWaitExternal : 0);
         if (ew != cudaSuccess) return c->cuda_fail(ew, "base-logit copy wait");
       }
       s = run_head(c, sbuf, z + static_cast<size_t>(d - 1) * V, static_cast<long long>(D) * V,
@@ -854,13 +857,14 @@ dartree_status run_bestfirst(dartree_ctx* c, const float* z, const float* s0,
 dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
                               const dartree_head* head, int R, int D, int W, int K, int B,
                               float beta, const dartree_options& o, const dartree_tree* out,
-                              cudaStream_t st, cudaEvent_t z_wait = nullptr) {
+                              cudaStream_t st, const cudaEvent_t* z_wait = nullptr,
+                              int z_late = 0) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (st != nullptr && cudaStreamIsCapturing(st, &cap) != cudaSuccess) cap = cudaStreamCaptureStatusNone;
   if (!c->use_graph || c->timing || st == nullptr || cap != cudaStreamCaptureStatusNone)
     return run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st, z_wait);
   dartree_ctx::GraphKey key{};
-  key.z_late = z_wait != nullptr;
+  key.z_late = z_late;
   key.opt = o;
   key.z = z;
   key.s0 = s0;
@@ -924,10 +928,12 @@ void free_all(dartree_ctx* c) {
   free_events(c);
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
   c->gexec = nullptr;
-  if (c->z_ready) cudaEventDestroy(c->z_ready);
+  for (cudaEvent_t ev : c->z_ready)
+    if (ev) cudaEventDestroy(ev);
+  c->z_ready.clear();
   if (c->z_order) cudaEventDestroy(c->z_order);
   if (c->copy_st) cudaStreamDestroy(c->copy_st);
-  c->z_ready = c->z_order = nullptr;
+  c->z_order = nullptr;
   c->copy_st = nullptr;
   if (c->h_stage) cudaFreeHost(c->h_stage);
   c->h_stage = nullptr;
@@ -1095,7 +1101,9 @@ dartree_status dartree_create(const dartree_config* cfg, dartree_ctx** out) {
     e = cudaMemcpy(c->iota, h_iota, sizeof h_iota, cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->copy_st, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->z_ready, cudaEventDisableTiming);
+  c->z_ready.assign(static_cast<size_t>(g.max_D) + 1, nullptr);
+  for (size_t d = 2; d < c->z_ready.size() && e == cudaSuccess; ++d)
+    e = cudaEventCreateWithFlags(&c->z_ready[d], cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->z_order, cudaEventDisableTiming);
   if (e == cudaSuccess) e = dt::init_head_attrs();
   if (e == cudaSuccess) e = dt::init_select_attrs();
@@ -1227,14 +1235,23 @@ dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float
   cudaError_t e = cudaMemcpy2DAsync(ctx->z_stage, pitch, zh, pitch, V * 4, R,
                                     cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->s0_stage, s0h, sn * 4, cudaMemcpyHostToDevice, st);
-  const bool late = D > 1;
-  if (late) {
+  // small per-depth slices: one copy, which the head call of depth 2
+  // waits for; large ones (many requests): one copy and one event per
+  // depth, so that each head call waits only for its own
+  cudaEvent_t ev[DARTREE_MAX_D + 1] = {};
+  const bool each = static_cast<size_t>(R) * V * 4 >= (size_t(4) << 20);
+  const int z_late = D > 1 ? (each ? 2 : 1) : 0;
+  if (z_late) {
     if (e == cudaSuccess) e = cudaEventRecord(ctx->z_order, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->copy_st, ctx->z_order, 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(ctx->z_stage + V, pitch, zh + V, pitch, (D - 1) * V * 4, R,
-                            cudaMemcpyHostToDevice, ctx->copy_st);
-    if (e == cudaSuccess) e = cudaEventRecord(ctx->z_ready, ctx->copy_st);
+    for (int d = 2; d <= D && e == cudaSuccess; ++d) {
+      const int n = each ? 1 : D - 1;  // depths in this copy
+      e = cudaMemcpy2DAsync(ctx->z_stage + (d - 1) * V, pitch, zh + (d - 1) * V, pitch,
+                            n * V * 4, R, cudaMemcpyHostToDevice, ctx->copy_st);
+      if (e == cudaSuccess) e = cudaEventRecord(ctx->z_ready[d], ctx->copy_st);
+      ev[d] = ctx->z_ready[d];
+      if (!each) break;
+    }
   }
   if (e != cudaSuccess) return ctx->cuda_fail(e, "input copy");
   size_t off[6];
@@ -1244,7 +1261,7 @@ dartree_status dartree_build_host(dartree_ctx* ctx, const float* zh, const float
                    reinterpret_cast<int32_t*>(o + off[2]), reinterpret_cast<float*>(o + off[3]),
                    reinterpret_cast<uint32_t*>(o + off[4]), reinterpret_cast<int32_t*>(o + off[5])};
   s = build_dispatch(ctx, ctx->z_stage, ctx->s0_stage, head, R, D, W, K, B, beta,
-                     dartree_options{}, &dev, st, late ? ctx->z_ready : nullptr);
+                     dartree_options{}, &dev, st, z_late ? ev : nullptr, z_late);
   if (s != DARTREE_OK) return s;
   // the tree in one copy, the check word in another, one synchronisation
   int* h_err = reinterpret_cast<int*>(ctx->h_stage + ctx->o_bytes);

@@ -1,7 +1,8 @@
 """The host-buffer build (inputs copied in, the later depths' base logits on a
-second stream under the first head call, the tree copied out) gives the same
-trees as the device-buffer build on the same inputs, bit for bit -- with and
-without graph capture, and on repeated calls (graph replay)."""
+second stream under the head calls -- in one copy, or per depth when they
+are large -- the tree copied out) gives the same trees as the device-buffer
+build on the same inputs, bit for bit: with and without graph capture, and
+on repeated calls (graph replay)."""
 from __future__ import annotations
 
 import numpy as np
@@ -18,6 +19,8 @@ CASES = [
     ("bf16-r3", dict(V=2100, H=128, D=4, W=8, K=6, B=24, beta=-0.1, bf16=True, R=3)),
     ("f32-r1", dict(V=1000, H=64, D=5, W=4, K=4, B=12, beta=0.0, bf16=False)),
     ("bf16-d1", dict(V=900, H=64, D=1, W=4, K=4, B=4, beta=0.0, bf16=True, R=2)),
+    # 4 MB of base logits per depth: one copy and one event per depth
+    ("bf16-big-z", dict(V=131072, H=64, D=4, W=4, K=4, B=12, beta=0.0, bf16=True, R=8)),
 ]
 
 
