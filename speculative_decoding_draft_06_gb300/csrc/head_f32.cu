@@ -46,8 +46,22 @@ __device__ __forceinline__ void nb_sync(int id) {
 __device__ __forceinline__ void nb_arrive(int id) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(kF32Threads) : "memory");
 }
+constexpr int kBarStage = 2;  // the head rows are staged
 constexpr int kBarFull = 4;   // + buffer: the tile sums are written
 constexpr int kBarEmpty = 6;  // + buffer: the epilogue has read them
+
+// The head rows (written by the previous kernel) into shared memory, every
+// thread's share, after the wait for that kernel; then all 640 threads meet
+// (a named barrier: the two warp groups reach it from different code).
+__device__ __forceinline__ void stage_head_rows(const TcParams& p, float* sS, int ldS) {
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < 16 * ldS; e += kF32Threads) {
+    const int j = e / ldS, c = e % ldS;
+    sS[e] = (j < p.M && c < p.H) ? __ldcg(p.S_f32 + static_cast<size_t>(j) * p.H + c) : 0.f;
+  }
+  nb_sync(kBarStage);
+}
 
 // The dot-product warps' loop over this CTA's tiles for J live head rows.
 // Thread (row r_in, quarter part) reads the row's float4 granules part,
@@ -60,7 +74,7 @@ constexpr int kBarEmpty = 6;  // + buffer: the epilogue has read them
 // for the FFMAs.  A tile's four partial sums per row meet by two shuffles and
 // go to the tile-sum buffer (double-buffered with the epilogue warps).
 template <int J, int NB>
-__device__ __forceinline__ void dot_tiles(const TcParams& p, const float* sS, int ldS, float* sX,
+__device__ __forceinline__ void dot_tiles(const TcParams& p, float* sS, int ldS, float* sX,
                                           int t_begin, int n_t, int r_in, int part) {
   constexpr int kPer = 16 / NB;  // batches per chunk
   const int per_tile = kPer * ((p.H + kF32Chunk - 1) / kF32Chunk);  // batches per tile (even)
@@ -101,7 +115,10 @@ __device__ __forceinline__ void dot_tiles(const TcParams& p, const float* sS, in
 #pragma unroll
   for (int j = 0; j < J; ++j) acc[j] = 0.f;
   float4 wa[NB], wb[NB];
+  // the weights are constant: the first batch goes out before the wait for
+  // the previous kernel, and lands while the head rows are staged
   if (total > 0) load(0, wa);
+  stage_head_rows(p, sS, ldS);
   for (int bt = 0; bt < total; bt += 2) {  // a pair of batches of one tile
     load(bt + 1, wb);
     fma(bt, wa, acc);
@@ -143,13 +160,6 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
 
   LogitsEpilogue<16> epi;
   if (warp < 4) epi.init(epi_smem, p.K, p.M, p.gth, p.gmx);
-  pdl_wait();  // the head rows come from the previous kernel
-  pdl_trigger();
-  for (int e = tid; e < 16 * ldS; e += kF32Threads) {
-    const int j = e / ldS, c = e % ldS;
-    sS[e] = (j < p.M && c < p.H) ? __ldcg(p.S_f32 + static_cast<size_t>(j) * p.H + c) : 0.f;
-  }
-  __syncthreads();
 
   if (warp >= 4) {
     // ---- dot-product warps: 128 weight rows x 4 quarters
@@ -165,6 +175,7 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
   }
 
   // ---- epilogue warps: thread tid = vocabulary entry tid of the tile
+  stage_head_rows(p, sS, ldS);
   const bool one_req = p.rows_per_req >= p.M;
   for (int i = 0; i < n_t; ++i) {
     const int b = i & 1, t = t_begin + i;
