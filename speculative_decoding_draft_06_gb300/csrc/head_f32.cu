@@ -68,10 +68,10 @@ __device__ __forceinline__ void stage_head_rows(const TcParams& p, float* sS, in
 // part + 4, ... of each 256-column chunk, in batches of NB (8 for up to 4
 // head rows, else 4: two batches' registers beside J accumulators).
 // The batches of all the CTA's tiles form one stream, software-pipelined:
-// the loads of batch b + 1 are issued before batch b is multiplied (also
-// across a tile's end, so the next tile's first loads are in flight during
-// the tile's reduction and hand-over), and the memory system does not wait
-// for the FFMAs.  A tile's four partial sums per row meet by two shuffles and
+// the loads of batch b + 2 are issued once batch b is multiplied (also
+// across a tile's end, so the next tile's loads are in flight during the
+// tile's reduction and hand-over), and the memory system does not wait for
+// the FFMAs.  A tile's four partial sums per row meet by two shuffles and
 // go to the tile-sum buffer (double-buffered with the epilogue warps).
 template <int J, int NB>
 __device__ __forceinline__ void dot_tiles(const TcParams& p, float* sS, int ldS, float* sX,
@@ -115,15 +115,18 @@ __device__ __forceinline__ void dot_tiles(const TcParams& p, float* sS, int ldS,
 #pragma unroll
   for (int j = 0; j < J; ++j) acc[j] = 0.f;
   float4 wa[NB], wb[NB];
-  // the weights are constant: the first batch goes out before the wait for
-  // the previous kernel, and lands while the head rows are staged
-  if (total > 0) load(0, wa);
+  // the weights are constant: the first two batches go out before the wait
+  // for the previous kernel, and land while the head rows are staged
+  if (total > 0) {
+    load(0, wa);
+    load(1, wb);
+  }
   stage_head_rows(p, sS, ldS);
   for (int bt = 0; bt < total; bt += 2) {  // a pair of batches of one tile
-    load(bt + 1, wb);
     fma(bt, wa, acc);
     if (bt + 2 < total) load(bt + 2, wa);
     fma(bt + 1, wb, acc);
+    if (bt + 3 < total) load(bt + 3, wb);
     if ((bt + 2) % per_tile == 0) {  // the tile's end
       const int i = bt / per_tile, b = i & 1;
 #pragma unroll
