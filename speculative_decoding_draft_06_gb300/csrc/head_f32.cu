@@ -147,6 +147,9 @@ __device__ __forceinline__ void dot_tiles(const TcParams& p, float* sS, int ldS,
   }
 }
 
+// J: at least the live head rows (4, 8 or 16), NB: the dot-product batch;
+// one instantiation per row count keeps each kernel's code to its own loop.
+template <int J, int NB>
 __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int ldS = (p.H + kF32Chunk - 1) / kF32Chunk * kF32Chunk;  // padded row pitch
@@ -168,12 +171,7 @@ __global__ void __launch_bounds__(kF32Threads, 1) k_head_f32(const TcParams p) {
     // ---- dot-product warps: 128 weight rows x 4 quarters
     const int dt = tid - kF32Epi;
     const int r_in = dt >> 2, part = dt & 3;
-    if (p.M <= 4)
-      dot_tiles<4, 8>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
-    else if (p.M <= 8)
-      dot_tiles<8, 4>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
-    else
-      dot_tiles<16, 4>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
+    dot_tiles<J, NB>(p, sS, ldS, sX, t_begin, n_t, r_in, part);
     return;
   }
 
@@ -236,13 +234,18 @@ bool head_f32_fits(int M, int H, int K) {
   return M >= 1 && M <= 16 && H % 4 == 0 && f32_smem(H, K) <= 200 * 1024;
 }
 
-cudaError_t init_head_f32_attrs() { return set_max_dynamic_smem(k_head_f32); }
+cudaError_t init_head_f32_attrs() {
+  cudaError_t e = set_max_dynamic_smem(k_head_f32<4, 8>);
+  if (e == cudaSuccess) e = set_max_dynamic_smem(k_head_f32<8, 4>);
+  return e != cudaSuccess ? e : set_max_dynamic_smem(k_head_f32<16, 4>);
+}
 
 cudaError_t launch_head_f32(const TcParams& p, int grid, cudaStream_t st) {
   if (!head_f32_fits(p.M, p.H, p.K) || (reinterpret_cast<uintptr_t>(p.W_f32) & 15) ||
       (p.A_f32 && ((reinterpret_cast<uintptr_t>(p.A_f32) & 15) || !p.U_f32)))
     return cudaErrorInvalidValue;
-  return launch_kernel(k_head_f32, dim3(grid), dim3(kF32Threads), f32_smem(p.H, p.K), st,
+  auto k = p.M <= 4 ? k_head_f32<4, 8> : p.M <= 8 ? k_head_f32<8, 4> : k_head_f32<16, 4>;
+  return launch_kernel(k, dim3(grid), dim3(kF32Threads), f32_smem(p.H, p.K), st,
                        p.pdl != 0, p);
 }
 
