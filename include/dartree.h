@@ -354,11 +354,10 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
  * product and its normaliser.  A row with no visible key gives 0.  dh must
  * be 128 (UNSUPPORTED otherwise); Hq % Hkv == 0, B <= 1024; Q, K, Vt, O
  * 16-byte aligned.
- * work / work_bytes: optional caller-owned device scratch (16-byte aligned)
- * for splitting the keys over more CTAs when a launch would leave SMs idle;
- * dartree_tree_attention_workspace() gives the size that allows the largest
- * split.  NULL or too small: fewer or no splits, same results up to
- * rounding.  Calls sharing one workspace must not overlap on the GPU.
+ * When a launch would leave SMs idle the keys are split over up to 8 CTAs
+ * per query tile (a thread-block cluster that combines its partial rows in
+ * distributed shared memory).  work / work_bytes: unused (the splits need
+ * no scratch; kept for the interface, may be NULL).
  * err: optional device word; a bounded pipeline wait that runs out ORs
  * 2 (timeout) into it (NULL: a library-internal word). */
 dartree_status dartree_tree_attention(const void *Q, const void *K, const void *Vt,
@@ -367,8 +366,8 @@ dartree_status dartree_tree_attention(const void *Q, const void *K, const void *
                                       void *O_bf16, void *work, size_t work_bytes, int32_t *err,
                                       void *stream);
 
-/* Workspace bytes for the largest key split of dartree_tree_attention (0 on
- * bad sizes). */
+/* Scratch bytes dartree_tree_attention needs: 0 (the key splits combine in
+ * distributed shared memory). */
 size_t dartree_tree_attention_workspace(int32_t R, int32_t Lp, int32_t B, int32_t Hq,
                                         int32_t Hkv);
 

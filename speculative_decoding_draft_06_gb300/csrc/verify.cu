@@ -70,11 +70,36 @@ struct AttnParams {
   uint16_t* O16;                          // same, bf16 bits, or null
   int* err;
   long long wait_limit;
-  int n_split, q_tiles;
-  float* part_O;                          // [tiles][n_split][128][dh] unnormalised
-  float2* part_ml;                        // [tiles][n_split][128] (max, sum) in base 2
-  int* cnt;                               // [tiles] arrivals, zero before the launch
+  int n_split, q_tiles;                   // n_split > 1: a cluster of n_split CTAs per query tile
 };
+
+// Thread-block cluster access (the key splits of a query tile).
+__device__ __forceinline__ uint32_t cl_addr(const void* p, int rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(a)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ void cl_st_f4(uint32_t a, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void cl_st_f2(uint32_t a, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+__device__ __forceinline__ void cl_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // 2^x (approximate hardware exp2; -inf -> +0).
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -128,116 +153,109 @@ __device__ __forceinline__ void store_row(const AttnParams& p, size_t base, floa
         make_uint2(cvt_bf16x2(v.x, v.y), cvt_bf16x2(v.z, v.w));
 }
 
-// The end of a query tile (the 256 softmax threads; thread = (row, half of
-// the head dims), holding its unnormalised O half, the row's max m and sum l
-// in base 2).  The rows are staged in shared memory (sO, the pipeline's
-// stage buffers, free once the last product has landed) so that each warp
-// then moves whole rows with 512-byte accesses.  One split: O = O_row / l.
-// Several: each split publishes its rows and (m, l); the last split of the
-// query tile to arrive combines them,
-//   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L,
-// in split order (deterministic).
-__device__ __forceinline__ void finish_tile(const AttnParams& p, int r, int hk, int qt, int split,
-                                            int row, int half, const float (&o)[kDh / 2],
-                                            float m, float l, float* sO) {
+// Each query row's base-2 (max, sum) of this CTA's keys, as finish_tile
+// staged it.
+__shared__ float2 sh_ml[kQRows];
+
+// The end of a query tile's keys in this CTA (the 256 softmax threads;
+// thread = (row, half of the head dims), holding its unnormalised O half
+// and the row's max m and sum l in base 2).  The rows are staged in shared
+// memory (sO, the pipeline's stage buffers, free once the last product has
+// landed) so that each warp then moves whole rows with 512-byte accesses.
+// One split: O = O_row / l, stored here.  Several: the cluster's exchange
+// and combine follow (split_exchange, split_combine).
+__device__ __forceinline__ void finish_tile(const AttnParams& p, int r, int hk, int qt, int row,
+                                            int half, const float (&o)[kDh / 2], float m, float l,
+                                            float* sO) {
   constexpr int kOH = kDh / 2;
-  __shared__ float2 s_ml[kQRows];
-  __shared__ int last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* dst = sO + row * kOPitch + half * kOH;
 #pragma unroll
   for (int i = 0; i < kOH; i += 4)
     *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
-  if (half == 0) s_ml[row] = make_float2(m, l);
+  if (half == 0) sh_ml[row] = make_float2(m, l);
   asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (p.n_split > 1) return;
   const int q0 = qt * kQRows;
-  if (p.n_split == 1) {
-    for (int rr = warp; rr < kQRows; rr += 8) {
-      if (q0 + rr >= p.rows) break;
-      const float lr = s_ml[rr].y;
-      const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      float4 v = *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
-      v.x *= inv;
-      v.y *= inv;
-      v.z *= inv;
-      v.w *= inv;
-      store_row(p, out_row(p, r, hk, q0 + rr), v);
-    }
-    return;
-  }
-  const size_t tile = (static_cast<size_t>(r) * p.Hkv + hk) * p.q_tiles + qt;
-  float* po = p.part_O + (tile * p.n_split + split) * kQRows * kDh;
-  float2* pml = p.part_ml + (tile * p.n_split + split) * kQRows;
   for (int rr = warp; rr < kQRows; rr += 8) {
     if (q0 + rr >= p.rows) break;
-    *reinterpret_cast<float4*>(po + rr * kDh + 4 * lane) =
-        *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
-    if (lane == 0) pml[rr] = s_ml[rr];
+    const float lr = sh_ml[rr].y;
+    const float inv = lr > 0.f ? 1.f / lr : 0.f;
+    float4 v = *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
+    v.x *= inv;
+    v.y *= inv;
+    v.z *= inv;
+    v.w *= inv;
+    store_row(p, out_row(p, r, hk, q0 + rr), v);
   }
-  __threadfence();
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  if (threadIdx.x == 0) last = (atomicAdd(p.cnt + tile, 1) == p.n_split - 1);
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  if (!last) return;
-  __threadfence();
-  const float* all_o = p.part_O + tile * p.n_split * kQRows * kDh;
-  const float2* all_ml = p.part_ml + tile * p.n_split * kQRows;
-  const int ns = p.n_split;  // <= 32: lane s holds split s's (m, l)
-  // the (m, l) of this warp's 16 rows, all loads in flight together
-  constexpr int kRows = kQRows / 8;
-  float2 ml[kRows];
-#pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const int rr = warp + 8 * i;
-    ml[i] = (lane < ns && q0 + rr < p.rows) ? __ldcg(&all_ml[lane * kQRows + rr])
-                                            : make_float2(-INFINITY, 0.f);
-  }
-  // four rows at a time: every split's partial row loaded before any is summed
-#pragma unroll
-  for (int i0 = 0; i0 < kRows; i0 += 4) {
-    float f[4], L[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float M = ml[i0 + i].x;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
-      f[i] = ml[i0 + i].x == -INFINITY ? 0.f : fast_ex2(ml[i0 + i].x - M);
-      float ls = ml[i0 + i].y * f[i];
-      // the sum over the splits in split order (lane order), deterministic
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(kFullMask, ls, o);
-        if (lane >= o) ls += y;
-      }
-      L[i] = __shfl_sync(kFullMask, ls, 31);
-    }
-    float4 acc[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int sp = 0; sp < ns; ++sp) {  // fixed order: deterministic
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rr = warp + 8 * (i0 + i);
-        const float fs = __shfl_sync(kFullMask, f[i], sp);
-        const float4 v =
-            __ldcg(reinterpret_cast<const float4*>(all_o + (sp * kQRows + rr) * kDh) + lane);
-        acc[i].x += v.x * fs;
-        acc[i].y += v.y * fs;
-        acc[i].z += v.z * fs;
-        acc[i].w += v.w * fs;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int rr = warp + 8 * (i0 + i);
-      if (q0 + rr >= p.rows) continue;
-      const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
-      store_row(p, out_row(p, r, hk, q0 + rr),
-                make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv));
+}
+
+// Several splits: split s owns rows [s RS, (s + 1) RS) of the query tile
+// (RS = ceil(128 / n)).  Every split sends the rows the others own -- its
+// unnormalised O row and (m, l) -- into the owner's receive buffer in
+// shared memory (distributed shared memory; slot s of the owner's n - 1
+// slots, the owner's own split skipped).  The 256 softmax threads, after
+// the cluster has started.
+__device__ __forceinline__ void split_exchange(const AttnParams& p, int qt, int split,
+                                               const float* sO, float* recv) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.n_split, rs = (kQRows + n - 1) / n;
+  const int q0 = qt * kQRows;
+  float2* recv_ml = reinterpret_cast<float2*>(recv + static_cast<size_t>(n - 1) * rs * kDh);
+  for (int d = 0; d < n; ++d) {
+    if (d == split) continue;
+    const int slot = split < d ? split : split - 1;
+    const int b = d * rs, e = b + rs < kQRows ? b + rs : kQRows;
+    for (int rr = b + warp; rr < e; rr += 8) {
+      if (q0 + rr >= p.rows) break;
+      const float4 v = *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
+      cl_st_f4(cl_addr(recv + (static_cast<size_t>(slot) * rs + (rr - b)) * kDh + 4 * lane, d), v);
+      if (lane == 0) cl_st_f2(cl_addr(recv_ml + slot * rs + (rr - b), d), sh_ml[rr]);
     }
   }
-  if (threadIdx.x == 0) p.cnt[tile] = 0;
+}
+
+// The rows this split owns, from every split's (m, l, O) in split order
+// (deterministic):
+//   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
+// After the cluster barrier that follows every split's exchange.
+__device__ __forceinline__ void split_combine(const AttnParams& p, int r, int hk, int qt,
+                                              int split, const float* sO, const float* recv) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.n_split, rs = (kQRows + n - 1) / n;
+  const int q0 = qt * kQRows;
+  const float2* recv_ml =
+      reinterpret_cast<const float2*>(recv + static_cast<size_t>(n - 1) * rs * kDh);
+  const int b = split * rs, e = b + rs < kQRows ? b + rs : kQRows;
+  for (int rr = b + warp; rr < e; rr += 8) {
+    if (q0 + rr >= p.rows) break;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < n; ++s2) {
+      const float2 ml = s2 == split ? sh_ml[rr] : recv_ml[(s2 < split ? s2 : s2 - 1) * rs + (rr - b)];
+      M = fmaxf(M, ml.x);
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s2 = 0; s2 < n; ++s2) {
+      const int slot = s2 < split ? s2 : s2 - 1;
+      const float2 ml = s2 == split ? sh_ml[rr] : recv_ml[slot * rs + (rr - b)];
+      const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
+      L += ml.y * f;
+      const float4 v =
+          s2 == split
+              ? *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane)
+              : *reinterpret_cast<const float4*>(recv + (static_cast<size_t>(slot) * rs + (rr - b)) *
+                                                            kDh +
+                                                 4 * lane);
+      acc.x += v.x * f;
+      acc.y += v.y * f;
+      acc.z += v.z * f;
+      acc.w += v.w * f;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    store_row(p, out_row(p, r, hk, q0 + rr),
+              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  }
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -258,8 +276,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* o_done = p_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // several key splits: the rows this split owns, as the others send them
+  float* recv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.n_split > 1) cl_arrive_relaxed();  // (waited on before the first remote store)
   const int r = blockIdx.z, hk = blockIdx.y;
   const int qt = blockIdx.x / p.n_split, split = blockIdx.x % p.n_split;
   const int q0 = qt * kQRows;
@@ -564,7 +585,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (nt > 0) l = 0.f;
     }
     // the stage buffers are free: every product (the last reader) has landed
-    finish_tile(p, r, hk, qt, split, row, wg, o, m, l, reinterpret_cast<float*>(sStage));
+    finish_tile(p, r, hk, qt, row, wg, o, m, l, reinterpret_cast<float*>(sStage));
+  }
+
+  // several splits: every CTA of the query tile's cluster sends the rows the
+  // others own and combines its own (every thread of every CTA meets both
+  // cluster barriers, whatever path it took above)
+  if (p.n_split > 1) {
+    cl_wait();  // every CTA of the cluster runs: its receive buffer exists
+    if (warp < kSoftmaxThreads / 32)
+      split_exchange(p, qt, split, reinterpret_cast<const float*>(sStage), recv);
+    cl_sync();  // every row delivered
+    if (warp < kSoftmaxThreads / 32)
+      split_combine(p, r, hk, qt, split, reinterpret_cast<const float*>(sStage), recv);
   }
 
   tc_fence_before();
@@ -653,14 +686,7 @@ bool encode_4d(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4],
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kMaxSplit = 16;
-
-size_t split_bytes(int R, int B, int Hq, int Hkv, int n_split) {
-  const size_t q_tiles = (static_cast<size_t>(B + 1) * (Hq / Hkv) + kQRows - 1) / kQRows;
-  const size_t tiles = static_cast<size_t>(R) * Hkv * q_tiles;
-  const size_t o = tiles * n_split * kQRows * kDh * 4, ml = tiles * n_split * kQRows * 8;
-  return o + ml + tiles * 4 + 64;
-}
+constexpr int kMaxSplit = 8;  // key splits of a query tile: one (portable) cluster
 
 __device__ int g_attn_err;  // error word when the caller passes none
 
@@ -669,9 +695,14 @@ __device__ int g_attn_err;  // error word when the caller passes none
 
 extern "C" size_t dartree_tree_attention_workspace(int32_t R, int32_t Lp, int32_t B, int32_t Hq,
                                                    int32_t Hkv) {
+  // the key splits exchange their rows in distributed shared memory: no
+  // device scratch is needed
+  (void)R;
   (void)Lp;
-  if (R < 1 || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return 0;
-  return dt::split_bytes(R, B, Hq, Hkv, dt::kMaxSplit);
+  (void)B;
+  (void)Hq;
+  (void)Hkv;
+  return 0;
 }
 
 extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, const void* Vt,
@@ -681,6 +712,8 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
                                                  void* work, size_t work_bytes, int32_t* err,
                                                  void* stream) {
   using namespace dt;
+  (void)work;  // (the key splits need no scratch: kept for the interface)
+  (void)work_bytes;
   if (!Q || !K || !Vt || !O || (B > 0 && !mask))
     return fail(DARTREE_ERR_INVALID_ARG, "null pointer argument");
   if (R < 1 || Lp < 0 || B < 0 || B > DARTREE_MAX_B || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
@@ -734,12 +767,10 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p.err), g_attn_err);
     if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   }
-  const size_t smem =
+  const size_t smem0 =
       1024 + kQBytes + static_cast<size_t>(kStages) * kStageBytes + 256;
-  e = cudaFuncSetAttribute(k_tree_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-  if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
-  // split the keys so that one wave of CTAs fills the GPU, as the workspace allows
+  // split the keys so that one wave of CTAs fills the GPU: the splits of a
+  // query tile are one cluster (at most kMaxSplit CTAs)
   p.q_tiles = (p.rows + kQRows - 1) / kQRows;
   const int tiles = R * Hkv * p.q_tiles;
   const int key_tiles = (L + kKeys - 1) / kKeys;
@@ -749,30 +780,30 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
   int n_split = sms / tiles;  // one CTA per SM
   n_split = n_split < kMaxSplit ? n_split : kMaxSplit;
   // a split keeps at least 5 key tiles (tuning: DARTREE_ATTN_SPLIT_MIN): with
-  // fewer, the partials' round trip and the combine cost more than the tiles
-  // they save
+  // fewer, the exchange and the combine cost more than the tiles they save
   int min_tiles = 5;
   if (const char* v = getenv("DARTREE_ATTN_SPLIT_MIN")) min_tiles = atoi(v) > 0 ? atoi(v) : 1;
   const int by_keys = key_tiles / min_tiles;
   n_split = n_split < by_keys ? n_split : by_keys;
+  if (const char* v = getenv("DARTREE_ATTN_MAX_SPLIT"))  // (test knob)
+    if (atoi(v) >= 1 && atoi(v) < n_split) n_split = atoi(v);
   if (n_split < 1) n_split = 1;
-  if ((reinterpret_cast<uintptr_t>(work) & 15) != 0) work = nullptr;
-  while (n_split > 1 && (work == nullptr || split_bytes(R, B, Hq, Hkv, n_split) > work_bytes))
-    --n_split;
   p.n_split = n_split;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (n_split > 1) {
-    const size_t ot = static_cast<size_t>(tiles) * n_split * kQRows * kDh * 4;
-    const size_t mt = static_cast<size_t>(tiles) * n_split * kQRows * 8;
-    uint8_t* wb = static_cast<uint8_t*>(work);
-    p.part_O = reinterpret_cast<float*>(wb);
-    p.part_ml = reinterpret_cast<float2*>(wb + ot);
-    p.cnt = reinterpret_cast<int*>(wb + ot + mt);
-    e = cudaMemsetAsync(p.cnt, 0, sizeof(int) * tiles, st);
-    if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
-  }
+  const int rs = (kQRows + n_split - 1) / n_split;
+  const size_t recv_bytes =
+      n_split > 1 ? static_cast<size_t>(n_split - 1) * rs * (kDh * 4 + 8) : 0;
+  const size_t smem = smem0 + recv_bytes;
+  e = cudaFuncSetAttribute(k_tree_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem0 + static_cast<size_t>(kMaxSplit - 1) *
+                                                        ((kQRows + kMaxSplit - 1) / kMaxSplit) *
+                                                        (kDh * 4 + 8)));
+  if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   const dim3 grid(p.q_tiles * n_split, Hkv, R);
-  e = launch_kernel(k_tree_attention, grid, dim3(kAttnThreads), smem, st, false, tm_k, tm_vt, p);
+  e = n_split > 1 ? launch_kernel_cluster(k_tree_attention, grid, dim3(kAttnThreads), smem, st,
+                                          false, n_split, tm_k, tm_vt, p)
+                  : launch_kernel(k_tree_attention, grid, dim3(kAttnThreads), smem, st, false,
+                                  tm_k, tm_vt, p);
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   return DARTREE_OK;
 }

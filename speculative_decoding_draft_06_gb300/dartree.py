@@ -400,8 +400,8 @@ def tree_attention(Q, K, Vt, mask, *, Lp: int, scale: float | None = None,
     Q [R,B+1,Hq,dh], key cache K [R,Hkv,Lp+B,dh] (prefix keys, then the tree
     nodes'), blocked transposed value cache Vt [R,Hkv,ceil(L/64),dh,64] (bf16
     CUDA tensors; see kv_cache),
-    mask [R,B,words] int32 -> {"O": fp32, "O16": bf16 bits}.  ``work`` is
-    the key-split scratch (allocated here when None and ``split``)."""
+    mask [R,B,words] int32 -> {"O": fp32, "O16": bf16 bits}.  ``work`` and
+    ``split`` are kept for the interface: the key splits need no scratch."""
     for n, t in (("Q", Q), ("K", K), ("Vt", Vt)):
         _dev(t, n, _W16)
     _dev(mask, "mask", (torch.int32,))
@@ -410,9 +410,6 @@ def tree_attention(Q, K, Vt, mask, *, Lp: int, scale: float | None = None,
     O = torch.empty(R, Bp1, Hq, dh, dtype=torch.float32, device=Q.device)
     O16 = torch.empty(R, Bp1, Hq, dh, dtype=torch.int16, device=Q.device) if want_bf16 else None
     sc = float(scale) if scale is not None else dh ** -0.5
-    if work is None and split:
-        n = int(load().dartree_tree_attention_workspace(R, Lp, Bp1 - 1, Hq, Hkv))
-        work = torch.empty(max(n, 16), dtype=torch.uint8, device=Q.device)
     wb = 0 if work is None else work.numel() * work.element_size()
     _check_free(load().dartree_tree_attention(
         _ptr(Q), _ptr(K), _ptr(Vt), _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh,

@@ -55,9 +55,17 @@ ATTN_CASES = [  # R, B, Lp, Hq, Hkv
 ]
 
 
-@pytest.mark.parametrize("split", [True, False])
+@pytest.mark.parametrize("split", ["auto", "none", "2", "8"])
 @pytest.mark.parametrize("case", range(len(ATTN_CASES)))
-def test_tree_attention_parity(case, split):
+def test_tree_attention_parity(monkeypatch, case, split):
+    """The key splits: as the launch chooses them, none, or forced small
+    split sizes (DARTREE_ATTN_SPLIT_MIN: key tiles per split at least), so
+    that clusters of 2 to 8 CTAs exchange and combine their rows."""
+    if split == "none":
+        monkeypatch.setenv("DARTREE_ATTN_SPLIT_MIN", "100000")
+    elif split != "auto":
+        monkeypatch.setenv("DARTREE_ATTN_SPLIT_MIN", "1")
+        monkeypatch.setenv("DARTREE_ATTN_MAX_SPLIT", split)
     R, B, Lp, Hq, Hkv = ATTN_CASES[case]
     shape = I.VerifyShape(Lp=Lp, Hq=Hq, Hkv=Hkv, dh=128, seed=4000 + case)
     x = I.make_verify_inputs(R, B, shape)
@@ -69,7 +77,7 @@ def test_tree_attention_parity(case, split):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = dtl.tree_attention(_cuda16(x["Q"]), K, VT,
                              torch.from_numpy(masks.view(np.int32)).cuda(), Lp=Lp, scale=scale,
-                             split=split, err=err)
+                             err=err)
     assert int(err.item()) == 0                       # no pipeline wait ran out
     O = out["O"].cpu().numpy()
     O16 = out["O16"].cpu().numpy().view(np.uint16)
