@@ -8,8 +8,9 @@
 // Tree attention on the 5th-generation tensor cores.  A CTA owns 128 query
 // rows (one TMEM lane each) of one request and one key/value head, and a
 // share of the key range (the keys are split over CTAs until one wave fills
-// the GPU; the last split to finish a query tile combines the partials,
-// whole rows per warp with coalesced 512-byte accesses).
+// the GPU; the splits of a query tile are one thread-block cluster, which
+// exchanges the partial rows in distributed shared memory, each split
+// combining the rows it owns).
 // Query row q of a key/value head is (node q / g, query head hk * g + q % g),
 // g = Hq / Hkv.  Row 0 (the root) sees the prefix; node i >= 1 sees the
 // prefix and the tree nodes of mask row i - 1.
@@ -53,6 +54,7 @@ constexpr int kSoftmaxThreads = 256;   // two warpgroups, one per half of each k
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kHalf = kKeys / 2;       // keys of a tile per warpgroup
 constexpr int kStages = 2;
+constexpr int kMaxSplit = 8;  // key splits of a query tile: one (portable) cluster
 constexpr int kQBytes = kQRows * kDh * 2;        // 32 KB: 2 swizzle atoms of 64 head dims
 constexpr int kKBytes = kKeys * kDh * 2;         // 32 KB: 2 atoms of 64 head dims
 constexpr int kVBytes = kDh * kKeys * 2;         // 32 KB: 2 blocks of 128 head dims x 64 keys
@@ -215,7 +217,7 @@ __device__ __forceinline__ void split_exchange(const AttnParams& p, int qt, int 
   }
 }
 
-// The rows this split owns, from every split's (m, l, O) in split order
+// The rows this split owns, from every split's (m, l, O) in a fixed order
 // (deterministic):
 //   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
 // After the cluster barrier that follows every split's exchange.
@@ -229,28 +231,40 @@ __device__ __forceinline__ void split_combine(const AttnParams& p, int r, int hk
   const int b = split * rs, e = b + rs < kQRows ? b + rs : kQRows;
   for (int rr = b + warp; rr < e; rr += 8) {
     if (q0 + rr >= p.rows) break;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < n; ++s2) {
-      const float2 ml = s2 == split ? sh_ml[rr] : recv_ml[(s2 < split ? s2 : s2 - 1) * rs + (rr - b)];
-      M = fmaxf(M, ml.x);
+    // lane s2 < n holds split s2's (m, l) of the row
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < n) ml = lane == split ? sh_ml[rr] : recv_ml[(lane < split ? lane : lane - 1) * rs + (rr - b)];
+    float M = ml.x;
+#pragma unroll
+    for (int o = kMaxSplit / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+    M = __shfl_sync(kFullMask, M, 0);
+    const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
+    float L = ml.y * f;
+#pragma unroll
+    for (int o = kMaxSplit / 2; o > 0; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
+    L = __shfl_sync(kFullMask, L, 0);
+    // every split's partial row first, then the sum in split order
+    float4 v[kMaxSplit];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+      if (s2 < n) {
+        const int slot = s2 < split ? s2 : s2 - 1;
+        v[s2] = s2 == split
+                    ? *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane)
+                    : *reinterpret_cast<const float4*>(
+                          recv + (static_cast<size_t>(slot) * rs + (rr - b)) * kDh + 4 * lane);
+      }
     }
-    float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s2 = 0; s2 < n; ++s2) {
-      const int slot = s2 < split ? s2 : s2 - 1;
-      const float2 ml = s2 == split ? sh_ml[rr] : recv_ml[slot * rs + (rr - b)];
-      const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
-      L += ml.y * f;
-      const float4 v =
-          s2 == split
-              ? *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane)
-              : *reinterpret_cast<const float4*>(recv + (static_cast<size_t>(slot) * rs + (rr - b)) *
-                                                            kDh +
-                                                 4 * lane);
-      acc.x += v.x * f;
-      acc.y += v.y * f;
-      acc.z += v.z * f;
-      acc.w += v.w * f;
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+      const float fs = __shfl_sync(kFullMask, f, s2);
+      if (s2 < n) {
+        acc.x += v[s2].x * fs;
+        acc.y += v[s2].y * fs;
+        acc.z += v[s2].z * fs;
+        acc.w += v[s2].w * fs;
+      }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     store_row(p, out_row(p, r, hk, q0 + rr),
@@ -291,12 +305,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int t_beg = split * t_all / p.n_split, t_end = (split + 1) * t_all / p.n_split;
   const int nt = t_end - t_beg;
 
+  // the keys and values of the CTA's key tile f into its stage
+  auto issue_kv = [&](int f) {
+    const int t = t_beg + f;
+    const int stage = f % kStages;
+    uint8_t* k_dst = sStage + stage * kStageBytes;
+    mbar_arrive_expect_tx(&kv_full[stage], kStageBytes);
+    tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, t * kKeys, hk, r);
+    tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, t * kKeys, hk, r);
+    tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], 0, 0, 2 * t, hk + p.Hkv * r);
+    tma_load_4d(k_dst + kKBytes + kVBytes / 2, &tm_vt, &kv_full[stage], 0, 0, 2 * t + 1,
+                hk + p.Hkv * r);
+  };
+  const int n_pre = nt < kStages ? nt : kStages;  // tiles loaded during the setup
+
   if (warp == kMmaWarp) tmem_alloc<kTmemCols>(tmem_slot);
-  if (threadIdx.x == 0) {
+  if (warp == kProducerWarp && lane == 0) {
+    // the producer's own barriers, and the first stages' copies while the
+    // query tile is staged (the stages start empty)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_vt);
+    for (int f = 0; f < n_pre; ++f) issue_kv(f);
+  }
+  if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], 8);  // one arrival per softmax warp
@@ -308,10 +345,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(o_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_vt);
   }
   // the query tile, written by the softmax threads in the swizzled layout
   if (threadIdx.x < kQRows) {
@@ -338,22 +371,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      long long issued = 0;
-      for (int f = 0; f < nt && !*abort_flag; ++f) {
-        const int t = t_beg + f;
+      long long issued = n_pre;
+      for (int f = n_pre; f < nt && !*abort_flag; ++f) {
         const int stage = f % kStages;
         const uint32_t ph = static_cast<uint32_t>((f / kStages) & 1);
         if (!mbar_wait(&kv_empty[stage], ph ^ 1u, p.err, p.wait_limit)) {
           *abort_flag = 1;
           break;
         }
-        uint8_t* k_dst = sStage + stage * kStageBytes;
-        mbar_arrive_expect_tx(&kv_full[stage], kStageBytes);
-        tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, t * kKeys, hk, r);
-        tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, t * kKeys, hk, r);
-        tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], 0, 0, 2 * t, hk + p.Hkv * r);
-        tma_load_4d(k_dst + kKBytes + kVBytes / 2, &tm_vt, &kv_full[stage], 0, 0, 2 * t + 1,
-                    hk + p.Hkv * r);
+        issue_kv(f);
         ++issued;
       }
       // drain: every issued copy must have landed before the CTA may exit
@@ -435,8 +461,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                   : nullptr;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const int col0 = wg * kHalf;  // this group's keys within a tile
+    // the row's mask words covering this group's half of tile t (three
+    // words from the one holding the half's first tree key; zero for the
+    // root row and beyond the row)
+    auto mask_words = [&](int t, uint32_t (&w)[3]) {
+      w[0] = w[1] = w[2] = 0u;
+      const int j0 = t * kKeys + col0;
+      if (mrow && j0 + kHalf > p.Lp) {
+        const int wb = (j0 > p.Lp ? j0 - p.Lp : 0) >> 5;
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          if (wb + k < p.words) w[k] = __ldg(mrow + wb + k);
+      }
+    };
     // scaled scores of this group's half of tile t, -inf where not visible
-    auto load_s = [&](int u, int t, float (&s)[kHalf]) {
+    auto load_s = [&](int u, int t, const uint32_t (&w)[3], float (&s)[kHalf]) {
       const int b = u & 1;
       const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * kKeys + col0);
 #pragma unroll
@@ -454,23 +493,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) s[c] *= p.scale_log2;
       } else {
-        uint32_t w[3] = {0u, 0u, 0u};  // mask words covering the half tile's tree keys
-        const int tt0 = j0 - p.Lp;  // tree index of the first key
-        const int wb = tt0 >= 0 ? tt0 >> 5 : 0;
-        if (mrow) {
-#pragma unroll
-          for (int k = 0; k < 3; ++k)
-            if (wb + k < p.words) w[k] = __ldg(mrow + wb + k);
-        }
+        // visibility of keys j0 .. j0 + 63 as one 64-bit word: the np prefix
+        // keys, then the mask bits from tree index tf on, cut at L
+        const int np = p.Lp > j0 ? p.Lp - j0 : 0;  // < 64 here
+        const int tf = j0 > p.Lp ? j0 - p.Lp : 0;
+        const uint32_t lo = __funnelshift_r(w[0], w[1], tf & 31);
+        const uint32_t hi = __funnelshift_r(w[1], w[2], tf & 31);
+        uint64_t vis = ((static_cast<uint64_t>(hi) << 32) | lo) << np;
+        if (np > 0) vis |= (1ull << np) - 1;
+        const int nv = p.L - j0;  // keys of the window below L
+        if (nv < kHalf) vis &= nv > 0 ? (1ull << nv) - 1 : 0ull;
+        const uint32_t v0 = static_cast<uint32_t>(vis), v1 = static_cast<uint32_t>(vis >> 32);
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) {
-          const int j = j0 + c;
-          bool vis = j < p.Lp;
-          if (!vis && j < p.L) {
-            const int tt = j - p.Lp - wb * 32;  // within the loaded words
-            vis = (w[tt >> 5] >> (tt & 31)) & 1u;
-          }
-          s[c] = vis ? s[c] * p.scale_log2 : -INFINITY;
+          const bool seen = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0u;
+          s[c] = seen ? s[c] * p.scale_log2 : -INFINITY;
         }
       }
     };
@@ -491,12 +528,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       return __shfl_sync(kFullMask, okl, 0) != 0;
     };
     for (int j = 0; j < nt; ++j) {
+      uint32_t mw[3];
+      mask_words(t_beg + j, mw);  // (in flight during the wait)
       const bool okw = go && !*abort_flag && wait_w(&s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u);
       float s[kHalf];
       float mh = -INFINITY;
       if (okw) {
         tc_fence_after();
-        load_s(j, t_beg + j, s);
+        load_s(j, t_beg + j, mw, s);
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) mh = fmaxf(mh, s[c]);
       }
@@ -686,7 +725,6 @@ bool encode_4d(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4],
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kMaxSplit = 8;  // key splits of a query tile: one (portable) cluster
 
 __device__ int g_attn_err;  // error word when the caller passes none
 
