@@ -217,7 +217,7 @@ __device__ __forceinline__ void split_exchange(const AttnParams& p, int qt, int 
   }
 }
 
-// The rows this split owns, from every split's (m, l, O) in a fixed order
+// The rows this split owns, from every split's (m, l, O) in split order
 // (deterministic):
 //   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
 // After the cluster barrier that follows every split's exchange.
@@ -231,39 +231,36 @@ __device__ __forceinline__ void split_combine(const AttnParams& p, int r, int hk
   const int b = split * rs, e = b + rs < kQRows ? b + rs : kQRows;
   for (int rr = b + warp; rr < e; rr += 8) {
     if (q0 + rr >= p.rows) break;
-    // lane s2 < n holds split s2's (m, l) of the row
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (lane < n) ml = lane == split ? sh_ml[rr] : recv_ml[(lane < split ? lane : lane - 1) * rs + (rr - b)];
-    float M = ml.x;
-#pragma unroll
-    for (int o = kMaxSplit / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
-    M = __shfl_sync(kFullMask, M, 0);
-    const float f = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
-    float L = ml.y * f;
-#pragma unroll
-    for (int o = kMaxSplit / 2; o > 0; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
-    L = __shfl_sync(kFullMask, L, 0);
-    // every split's partial row first, then the sum in split order
+    // every split's (m, l) and partial row of this row, all loads at once
+    // (each lane reads the (m, l) pairs itself: broadcast reads, no shuffles)
+    float2 ml[kMaxSplit];
     float4 v[kMaxSplit];
 #pragma unroll
     for (int s2 = 0; s2 < kMaxSplit; ++s2) {
       if (s2 < n) {
         const int slot = s2 < split ? s2 : s2 - 1;
-        v[s2] = s2 == split
-                    ? *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane)
+        const bool own = s2 == split;
+        ml[s2] = own ? sh_ml[rr] : recv_ml[slot * rs + (rr - b)];
+        v[s2] = own ? *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane)
                     : *reinterpret_cast<const float4*>(
                           recv + (static_cast<size_t>(slot) * rs + (rr - b)) * kDh + 4 * lane);
       }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplit; ++s2)
+      if (s2 < n) M = fmaxf(M, ml[s2].x);
+    float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-      const float fs = __shfl_sync(kFullMask, f, s2);
       if (s2 < n) {
-        acc.x += v[s2].x * fs;
-        acc.y += v[s2].y * fs;
-        acc.z += v[s2].z * fs;
-        acc.w += v[s2].w * fs;
+        const float f = ml[s2].x == -INFINITY ? 0.f : fast_ex2(ml[s2].x - M);
+        L += ml[s2].y * f;
+        acc.x += v[s2].x * f;
+        acc.y += v[s2].y * f;
+        acc.z += v[s2].z * f;
+        acc.w += v[s2].w * f;
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -817,9 +814,9 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int n_split = sms / tiles;  // one CTA per SM
   n_split = n_split < kMaxSplit ? n_split : kMaxSplit;
-  // a split keeps at least 5 key tiles (tuning: DARTREE_ATTN_SPLIT_MIN): with
+  // a split keeps at least 3 key tiles (tuning: DARTREE_ATTN_SPLIT_MIN): with
   // fewer, the exchange and the combine cost more than the tiles they save
-  int min_tiles = 5;
+  int min_tiles = 3;
   if (const char* v = getenv("DARTREE_ATTN_SPLIT_MIN")) min_tiles = atoi(v) > 0 ? atoi(v) : 1;
   const int by_keys = key_tiles / min_tiles;
   n_split = n_split < by_keys ? n_split : by_keys;
