@@ -73,6 +73,7 @@ struct AttnParams {
   int* err;
   long long wait_limit;
   int n_split, q_tiles;                   // n_split > 1: a cluster of n_split CTAs per query tile
+  int q_tma;                              // the query tile by TMA (128 % g == 0), else by the threads
 };
 
 // Thread-block cluster access (the key splits of a query tile).
@@ -270,7 +271,8 @@ __device__ __forceinline__ void split_combine(const AttnParams& p, int r, int hk
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    k_tree_attention(const __grid_constant__ CUtensorMap tm_k,
+    k_tree_attention(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -285,7 +287,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* p_full = s_empty + 2;   // [2]
   uint64_t* p_empty = p_full + 2;   // [2]
   uint64_t* o_done = p_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  uint64_t* q_full = o_done + 1;    // the query tile's copies (q_tma)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // several key splits: the rows this split owns, as the others send them
   float* recv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
@@ -324,8 +327,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
+    mbar_init(q_full, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
+    if (p.q_tma) {
+      // rows (node, query head) of the tile: a box of 128 / g nodes by the
+      // g query heads of this key/value head, per 64 head dims
+      const int nodes = kQRows / p.g;
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      tma_load_4d(sQ, &tm_q, q_full, 0, hk * p.g, qt * nodes, r);
+      tma_load_4d(sQ + kQRows * 128, &tm_q, q_full, 64, hk * p.g, qt * nodes, r);
+    }
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_vt);
     for (int f = 0; f < n_pre; ++f) issue_kv(f);
@@ -343,8 +355,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // the query tile, written by the softmax threads in the swizzled layout
-  if (threadIdx.x < kQRows) {
+  // otherwise the query tile, written by the softmax threads in the
+  // swizzled layout
+  if (!p.q_tma && threadIdx.x < kQRows) {
     const int row = threadIdx.x, q = q0 + row;
     const bool valid = q < p.rows;
     const uint4* src = nullptr;
@@ -385,6 +398,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int s = static_cast<int>(n % kStages);
         if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((n / kStages) & 1), p.err)) break;
       }
+      if (p.q_tma) mbar_wait(q_full, 0, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer
@@ -436,6 +450,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_commit(&kv_empty[stage]);
         return true;
       };
+      if (p.q_tma && nt > 0) wait(q_full, 0);
       // scores of tile j, then the product of tile j - 1
       for (int j = 0; j < nt && ok; ++j) {
         if (!issue_s(j, j % kStages)) break;
@@ -760,7 +775,8 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
                        reinterpret_cast<uintptr_t>(O_bf16);
   if (al & 15) return fail(DARTREE_ERR_INVALID_ARG, "Q, K, Vt and O must be 16-byte aligned");
   const int L = Lp + B;
-  CUtensorMap tm_k, tm_vt;
+  const int g = Hq / Hkv;
+  CUtensorMap tm_q, tm_k, tm_vt;
   const int nblk = (L + kVBlock - 1) / kVBlock;
   {  // keys [R][Hkv][L][dh]: a tile is 64 consecutive rows of one head
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDh), static_cast<cuuint64_t>(L),
@@ -782,13 +798,27 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
                                1};
     if (!encode_4d(&tm_vt, Vt, dims, str, box)) return fail(DARTREE_ERR_CUDA, "value tensor map");
   }
+  const bool q_tma = kQRows % g == 0;
+  if (q_tma) {  // queries [R][B+1][Hq][dh]: a tile is 128 / g nodes x g heads
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDh), static_cast<cuuint64_t>(Hq),
+                                static_cast<cuuint64_t>(B) + 1, static_cast<cuuint64_t>(R)};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(kDh) * 2,
+                               static_cast<cuuint64_t>(Hq) * kDh * 2,
+                               static_cast<cuuint64_t>(B + 1) * Hq * kDh * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g),
+                               static_cast<cuuint32_t>(kQRows / g), 1};
+    if (!encode_4d(&tm_q, Q, dims, str, box)) return fail(DARTREE_ERR_CUDA, "query tensor map");
+  } else {
+    tm_q = tm_k;  // (not read: the threads stage the query tile)
+  }
   AttnParams p{};
   p.Lp = Lp;
   p.B = B;
   p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.g = Hq / Hkv;
+  p.g = g;
+  p.q_tma = q_tma ? 1 : 0;
   p.words = (B + 31) / 32;
   p.rows = (B + 1) * p.g;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -836,9 +866,9 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   const dim3 grid(p.q_tiles * n_split, Hkv, R);
   e = n_split > 1 ? launch_kernel_cluster(k_tree_attention, grid, dim3(kAttnThreads), smem, st,
-                                          false, n_split, tm_k, tm_vt, p)
+                                          false, n_split, tm_q, tm_k, tm_vt, p)
                   : launch_kernel(k_tree_attention, grid, dim3(kAttnThreads), smem, st, false,
-                                  tm_k, tm_vt, p);
+                                  tm_q, tm_k, tm_vt, p);
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   return DARTREE_OK;
 }

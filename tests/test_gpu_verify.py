@@ -52,6 +52,8 @@ ATTN_CASES = [  # R, B, Lp, Hq, Hkv
     (1, 40, 3000, 2, 1),      # long key ranges: the keys are split over CTAs
     (1, 130, 4000, 8, 2),
     (2, 16, 8000, 4, 2),
+    (1, 50, 700, 12, 4),      # g = 3 and 6 do not divide a tile's 128 rows: the
+    (1, 30, 2500, 6, 1),      # threads stage the query tile (else TMA boxes of nodes x heads)
 ]
 
 
