@@ -280,9 +280,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sStage = sQ + kQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + kStages * kStageBytes);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + kStages;
-  uint64_t* s_full = kv_empty + kStages;
+  // keys and values of a stage have their own barriers: the keys are free
+  // once QK^T has read them, two tiles before the values
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = k_full + kStages;
+  uint64_t* v_full = k_empty + kStages;
+  uint64_t* v_empty = v_full + kStages;
+  uint64_t* s_full = v_empty + kStages;
   uint64_t* s_empty = s_full + 2;
   uint64_t* p_full = s_empty + 2;   // [2]
   uint64_t* p_empty = p_full + 2;   // [2]
@@ -305,17 +309,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int t_beg = split * t_all / p.n_split, t_end = (split + 1) * t_all / p.n_split;
   const int nt = t_end - t_beg;
 
-  // the keys and values of the CTA's key tile f into its stage
-  auto issue_kv = [&](int f) {
+  // the keys, and the values, of the CTA's key tile f into its stage
+  auto issue_k = [&](int f) {
     const int t = t_beg + f;
     const int stage = f % kStages;
     uint8_t* k_dst = sStage + stage * kStageBytes;
-    mbar_arrive_expect_tx(&kv_full[stage], kStageBytes);
-    tma_load_4d(k_dst, &tm_k, &kv_full[stage], 0, t * kKeys, hk, r);
-    tma_load_4d(k_dst + kKBytes / 2, &tm_k, &kv_full[stage], 64, t * kKeys, hk, r);
-    tma_load_4d(k_dst + kKBytes, &tm_vt, &kv_full[stage], 0, 0, 2 * t, hk + p.Hkv * r);
-    tma_load_4d(k_dst + kKBytes + kVBytes / 2, &tm_vt, &kv_full[stage], 0, 0, 2 * t + 1,
-                hk + p.Hkv * r);
+    mbar_arrive_expect_tx(&k_full[stage], kKBytes);
+    tma_load_4d(k_dst, &tm_k, &k_full[stage], 0, t * kKeys, hk, r);
+    tma_load_4d(k_dst + kKBytes / 2, &tm_k, &k_full[stage], 64, t * kKeys, hk, r);
+  };
+  auto issue_v = [&](int f) {
+    const int t = t_beg + f;
+    const int stage = f % kStages;
+    uint8_t* v_dst = sStage + stage * kStageBytes + kKBytes;
+    mbar_arrive_expect_tx(&v_full[stage], kVBytes);
+    tma_load_4d(v_dst, &tm_vt, &v_full[stage], 0, 0, 2 * t, hk + p.Hkv * r);
+    tma_load_4d(v_dst + kVBytes / 2, &tm_vt, &v_full[stage], 0, 0, 2 * t + 1, hk + p.Hkv * r);
   };
   const int n_pre = nt < kStages ? nt : kStages;  // tiles loaded during the setup
 
@@ -324,8 +333,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the producer's own barriers, and the first stages' copies while the
     // query tile is staged (the stages start empty)
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(q_full, 1);
     fence_mbar_init();
@@ -340,7 +351,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_vt);
-    for (int f = 0; f < n_pre; ++f) issue_kv(f);
+    for (int f = 0; f < n_pre; ++f) {
+      issue_k(f);
+      issue_v(f);
+    }
   }
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -381,22 +395,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      long long issued = n_pre;
+      long long k_issued = n_pre, v_issued = n_pre;
       for (int f = n_pre; f < nt && !*abort_flag; ++f) {
         const int stage = f % kStages;
         const uint32_t ph = static_cast<uint32_t>((f / kStages) & 1);
-        if (!mbar_wait(&kv_empty[stage], ph ^ 1u, p.err, p.wait_limit)) {
+        // the keys once QK^T of tile f - 2 has read its stage's, then the
+        // values once the product of tile f - 2 has
+        if (!mbar_wait(&k_empty[stage], ph ^ 1u, p.err, p.wait_limit)) {
           *abort_flag = 1;
           break;
         }
-        issue_kv(f);
-        ++issued;
+        issue_k(f);
+        ++k_issued;
+        if (!mbar_wait(&v_empty[stage], ph ^ 1u, p.err, p.wait_limit)) {
+          *abort_flag = 1;
+          break;
+        }
+        issue_v(f);
+        ++v_issued;
       }
       // drain: every issued copy must have landed before the CTA may exit
-      const long long first = issued > kStages ? issued - kStages : 0;
-      for (long long n = first; n < issued; ++n) {
-        const int s = static_cast<int>(n % kStages);
-        if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((n / kStages) & 1), p.err)) break;
+      for (int kv = 0; kv < 2; ++kv) {
+        const long long issued = kv == 0 ? k_issued : v_issued;
+        uint64_t* full = kv == 0 ? k_full : v_full;
+        const long long first = issued > kStages ? issued - kStages : 0;
+        for (long long n = first; n < issued; ++n) {
+          const int s = static_cast<int>(n % kStages);
+          if (!mbar_wait(&full[s], static_cast<uint32_t>((n / kStages) & 1), p.err)) break;
+        }
       }
       if (p.q_tma) mbar_wait(q_full, 0, p.err);
     }
@@ -417,7 +443,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       auto issue_s = [&](int u, int stage) {
         const int b = u & 1;
         if (!wait(&s_empty[b], (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u)) return false;
-        if (!wait(&kv_full[stage], static_cast<uint32_t>((u / kStages) & 1))) return false;
+        if (!wait(&k_full[stage], static_cast<uint32_t>((u / kStages) & 1))) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sStage + stage * kStageBytes);
 #pragma unroll
@@ -429,12 +455,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                       kk != 0 ? 1u : 0u);
         }
         tc_commit(&s_full[b]);
+        tc_commit(&k_empty[stage]);  // the keys are read once the scores are done
         return true;
       };
       // O += P V for tile j (its stage), then release P and the stage
       auto issue_o = [&](int j) {
         const int stage = j % kStages, pb = j % kPBufs;
         if (!wait(&p_full[pb], static_cast<uint32_t>(j / kPBufs) & 1u)) return false;
+        if (!wait(&v_full[stage], static_cast<uint32_t>((j / kStages) & 1))) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sStage + stage * kStageBytes + kKBytes);
         const uint32_t pa = tmem_base + kColP + static_cast<uint32_t>(pb * (kKeys / 2));
@@ -447,7 +475,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                          (j != 0 || kk != 0) ? 1u : 0u);
         }
         tc_commit(&p_empty[pb]);
-        tc_commit(&kv_empty[stage]);
+        tc_commit(&v_empty[stage]);
         return true;
       };
       if (p.q_tma && nt > 0) wait(q_full, 0);
