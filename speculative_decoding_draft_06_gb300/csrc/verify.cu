@@ -74,6 +74,7 @@ struct AttnParams {
   long long wait_limit;
   int n_split, q_tiles;                   // n_split > 1: a cluster of n_split CTAs per query tile
   int q_tma;                              // the query tile by TMA (128 % g == 0), else by the threads
+  unsigned long long g_magic;             // ceil(2^32 / g): q / g = (q g_magic) >> 32 for every row q
 };
 
 // Thread-block cluster access (the key splits of a query tile).
@@ -140,9 +141,12 @@ __device__ __forceinline__ uint32_t sw128(int r, int gr) {
 
 constexpr int kOPitch = kDh + 4;  // floats per staged O row (16-byte rows spread over the banks)
 
-// Output row q of a query tile (node q / g, query head hk g + q % g).
+// Output row q of a query tile (node q / g, query head hk g + q % g; the
+// quotient by a multiply with the rounded-up reciprocal, exact for the
+// row counts the host admits).
 __device__ __forceinline__ size_t out_row(const AttnParams& p, int r, int hk, int q) {
-  const int node = q / p.g, h = hk * p.g + q % p.g;
+  const int node = static_cast<int>((static_cast<unsigned long long>(q) * p.g_magic) >> 32);
+  const int h = hk * p.g + (q - node * p.g);
   return ((static_cast<size_t>(r) * (p.B + 1) + node) * p.Hq + h) * kDh;
 }
 
@@ -204,16 +208,20 @@ __device__ __forceinline__ void split_exchange(const AttnParams& p, int qt, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.n_split, rs = (kQRows + n - 1) / n;
   const int q0 = qt * kQRows;
+  const int live = p.rows - q0 < kQRows ? p.rows - q0 : kQRows;  // rows of the tile that exist
   float2* recv_ml = reinterpret_cast<float2*>(recv + static_cast<size_t>(n - 1) * rs * kDh);
   for (int d = 0; d < n; ++d) {
     if (d == split) continue;
     const int slot = split < d ? split : split - 1;
-    const int b = d * rs, e = b + rs < kQRows ? b + rs : kQRows;
-    for (int rr = b + warp; rr < e; rr += 8) {
-      if (q0 + rr >= p.rows) break;
-      const float4 v = *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane);
-      cl_st_f4(cl_addr(recv + (static_cast<size_t>(slot) * rs + (rr - b)) * kDh + 4 * lane, d), v);
-      if (lane == 0) cl_st_f2(cl_addr(recv_ml + slot * rs + (rr - b), d), sh_ml[rr]);
+    const int b = d * rs;
+    const int cnt = (b + rs < live ? b + rs : live) - b;
+    // the slot's rows in rank d's receive buffer (one address map per rank)
+    const uint32_t dst = cl_addr(recv + static_cast<size_t>(slot) * rs * kDh + 4 * lane, d);
+    const uint32_t dst_ml = cl_addr(recv_ml + slot * rs, d);
+    for (int i = warp; i < cnt; i += 8) {
+      const float4 v = *reinterpret_cast<const float4*>(sO + (b + i) * kOPitch + 4 * lane);
+      cl_st_f4(dst + static_cast<uint32_t>(i * kDh * 4), v);
+      if (lane == 0) cl_st_f2(dst_ml + static_cast<uint32_t>(i * 8), sh_ml[b + i]);
     }
   }
 }
@@ -221,52 +229,69 @@ __device__ __forceinline__ void split_exchange(const AttnParams& p, int qt, int 
 // The rows this split owns, from every split's (m, l, O) in split order
 // (deterministic):
 //   M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L.
-// After the cluster barrier that follows every split's exchange.
-__device__ __forceinline__ void split_combine(const AttnParams& p, int r, int hk, int qt,
-                                              int split, const float* sO, const float* recv) {
+// After the cluster barrier that follows every split's exchange.  N = the
+// split count, so that the per-row work is straight-line code: every
+// split's rows are a base and a row stride (the own split's in sO and
+// sh_ml, the others' in the receive buffer).
+template <int N>
+__device__ __forceinline__ void combine_rows(const AttnParams& p, int r, int hk, int qt, int split,
+                                             const float* sO, const float* recv) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = p.n_split, rs = (kQRows + n - 1) / n;
+  constexpr int rs = (kQRows + N - 1) / N;
   const int q0 = qt * kQRows;
-  const float2* recv_ml =
-      reinterpret_cast<const float2*>(recv + static_cast<size_t>(n - 1) * rs * kDh);
-  const int b = split * rs, e = b + rs < kQRows ? b + rs : kQRows;
-  for (int rr = b + warp; rr < e; rr += 8) {
-    if (q0 + rr >= p.rows) break;
-    // every split's (m, l) and partial row of this row, all loads at once
-    // (each lane reads the (m, l) pairs itself: broadcast reads, no shuffles)
-    float2 ml[kMaxSplit];
-    float4 v[kMaxSplit];
+  const int live = p.rows - q0 < kQRows ? p.rows - q0 : kQRows;
+  const int b = split * rs;
+  const int cnt = (b + rs < live ? b + rs : live) - b;
+  const float2* recv_ml = reinterpret_cast<const float2*>(recv + static_cast<size_t>(N - 1) * rs * kDh);
+  const float* vb[N];
+  int vs[N];
+  const float2* mb[N];
 #pragma unroll
-    for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-      if (s2 < n) {
-        const int slot = s2 < split ? s2 : s2 - 1;
-        const bool own = s2 == split;
-        ml[s2] = own ? sh_ml[rr] : recv_ml[slot * rs + (rr - b)];
-        v[s2] = own ? *reinterpret_cast<const float4*>(sO + rr * kOPitch + 4 * lane)
-                    : *reinterpret_cast<const float4*>(
-                          recv + (static_cast<size_t>(slot) * rs + (rr - b)) * kDh + 4 * lane);
-      }
+  for (int s2 = 0; s2 < N; ++s2) {
+    const bool own = s2 == split;
+    const int slot = s2 < split ? s2 : s2 - 1;
+    vb[s2] = own ? sO + b * kOPitch + 4 * lane : recv + static_cast<size_t>(slot) * rs * kDh + 4 * lane;
+    vs[s2] = own ? kOPitch : kDh;
+    mb[s2] = own ? sh_ml + b : recv_ml + slot * rs;
+  }
+  for (int i = warp; i < cnt; i += 8) {
+    float2 ml[N];
+    float4 v[N];
+#pragma unroll
+    for (int s2 = 0; s2 < N; ++s2) {
+      ml[s2] = mb[s2][i];
+      v[s2] = *reinterpret_cast<const float4*>(vb[s2] + i * vs[s2]);
     }
-    float M = -INFINITY;
+    float M = ml[0].x;
 #pragma unroll
-    for (int s2 = 0; s2 < kMaxSplit; ++s2)
-      if (s2 < n) M = fmaxf(M, ml[s2].x);
+    for (int s2 = 1; s2 < N; ++s2) M = fmaxf(M, ml[s2].x);
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-      if (s2 < n) {
-        const float f = ml[s2].x == -INFINITY ? 0.f : fast_ex2(ml[s2].x - M);
-        L += ml[s2].y * f;
-        acc.x += v[s2].x * f;
-        acc.y += v[s2].y * f;
-        acc.z += v[s2].z * f;
-        acc.w += v[s2].w * f;
-      }
+    for (int s2 = 0; s2 < N; ++s2) {
+      const float f = ml[s2].x == -INFINITY ? 0.f : fast_ex2(ml[s2].x - M);
+      L += ml[s2].y * f;
+      acc.x += v[s2].x * f;
+      acc.y += v[s2].y * f;
+      acc.z += v[s2].z * f;
+      acc.w += v[s2].w * f;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    store_row(p, out_row(p, r, hk, q0 + rr),
+    store_row(p, out_row(p, r, hk, q0 + b + i),
               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  }
+}
+
+__device__ __forceinline__ void split_combine(const AttnParams& p, int r, int hk, int qt,
+                                              int split, const float* sO, const float* recv) {
+  switch (p.n_split) {
+    case 2: combine_rows<2>(p, r, hk, qt, split, sO, recv); break;
+    case 3: combine_rows<3>(p, r, hk, qt, split, sO, recv); break;
+    case 4: combine_rows<4>(p, r, hk, qt, split, sO, recv); break;
+    case 5: combine_rows<5>(p, r, hk, qt, split, sO, recv); break;
+    case 6: combine_rows<6>(p, r, hk, qt, split, sO, recv); break;
+    case 7: combine_rows<7>(p, r, hk, qt, split, sO, recv); break;
+    default: combine_rows<8>(p, r, hk, qt, split, sO, recv); break;
   }
 }
 
@@ -847,6 +872,12 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
   p.Hkv = Hkv;
   p.g = g;
   p.q_tma = q_tma ? 1 : 0;
+  // q / g by a multiply: with m = ceil(2^32 / g) = (2^32 + e) / g, e < g,
+  // (q m) >> 32 = floor(q / g + q e / (g 2^32)) = q / g while q e < 2^32;
+  // here q < (B + 1) g <= 1025 g and e < g
+  p.g_magic = ((1ull << 32) + static_cast<unsigned long long>(g) - 1) / static_cast<unsigned long long>(g);
+  if (static_cast<unsigned long long>(B + 1) * g * g >= (1ull << 32))
+    return fail(DARTREE_ERR_UNSUPPORTED, "too many query heads per key/value head");
   p.words = (B + 31) / 32;
   p.rows = (B + 1) * p.g;
   p.scale_log2 = scale * 1.4426950408889634f;
