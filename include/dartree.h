@@ -352,8 +352,9 @@ dartree_status dartree_state_step_noalloc(const void *S_par, const int32_t *tok,
  * h / (Hq/Hkv).  O = softmax(scale * q.k) v with fp32 accumulation on the
  * tensor cores; the softmax weights are rounded to bf16 for the P.V
  * product and its normaliser.  A row with no visible key gives 0.  dh must
- * be 128 (UNSUPPORTED otherwise); Hq % Hkv == 0, B <= 1024; Q, K, Vt, O
- * 16-byte aligned.
+ * be 128 (UNSUPPORTED otherwise); Hq % Hkv == 0, B <= 1024,
+ * (B+1) (Hq/Hkv)^2 < 2^32 (UNSUPPORTED otherwise); Q, K, Vt, O 16-byte
+ * aligned.
  * When a launch would leave SMs idle the keys are split over up to 8 CTAs
  * per query tile (a thread-block cluster that combines its partial rows in
  * distributed shared memory).  work / work_bytes: unused (the splits need
