@@ -730,8 +730,6 @@ def run_verify(args) -> None:
     if U is None:
         raise SystemExit("verify: the stand-in projection needs H == Hq * dh")
     zero = torch.zeros(w.V, dtype=torch.float32, device="cuda")
-    work = torch.empty(max(16, dtl.load().dartree_tree_attention_workspace(
-        w.R, vs.Lp, w.B, vs.Hq, vs.Hkv)), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
     out = ctx.alloc_tree(w.R, w.B)
     kw = dict(D=w.D, W=w.W, K=w.K, B=w.B, beta=w.beta, out=out, stream=stream)
@@ -743,8 +741,7 @@ def run_verify(args) -> None:
         with torch.cuda.stream(stream):
             if timed:
                 ev["a0"].record(stream)
-            att = dtl.tree_attention(xd["Q"], Kc, VTc, out["mask"], Lp=vs.Lp, work=work,
-                                     stream=stream)
+            att = dtl.tree_attention(xd["Q"], Kc, VTc, out["mask"], Lp=vs.Lp, stream=stream)
             if timed:
                 ev["a1"].record(stream)
             S = att["O16"].view(rows, H2)
@@ -782,6 +779,24 @@ def run_verify(args) -> None:
         t_proj += ev["a1"].elapsed_time(ev["p1"])
     t_att /= n_t
     t_proj /= n_t
+    # the attention alone, back to back: 20 launches captured in a CUDA graph
+    # and replayed (no launch latency or host time between them)
+    n_bb, n_rep = 20, 5
+    g_att = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_att, stream=stream):
+        for _ in range(n_bb):
+            dtl.tree_attention(xd["Q"], Kc, VTc, out["mask"], Lp=vs.Lp)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g_att.replay()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_rep):
+            g_att.replay()
+        e1.record(stream)
+    e1.synchronize()
+    t_att_bb = e0.elapsed_time(e1) / (n_bb * n_rep)
     acc_len = acc["len"].cpu().numpy()
     depth = out["depth"].cpu().numpy()
     n_out = out["n_out"].cpu().numpy()
@@ -813,7 +828,9 @@ def run_verify(args) -> None:
                           "bound": "tensor", "launch_ms": t_att,
                           "achieved": att_flops / (t_att * 1e-3) / 1e12, "peak": tfl,
                           "unit": "TFLOP/s", "frac": att_flops / (t_att * 1e-3) / 1e12 / tfl,
-                          "peak_source": tfl_kind, "flops_per_launch": att_flops},
+                          "peak_source": tfl_kind, "flops_per_launch": att_flops,
+                          "launch_ms_back_to_back": t_att_bb,
+                          "achieved_back_to_back": att_flops / (t_att_bb * 1e-3) / 1e12},
             "accept_len_mean": float(acc_len.mean()),
             "cpu_baseline": None, "e2e": None,
             "gpu_launches": (kernels_per_build(w) + 4) * args.steps,
