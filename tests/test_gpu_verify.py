@@ -57,12 +57,13 @@ ATTN_CASES = [  # R, B, Lp, Hq, Hkv
 ]
 
 
-@pytest.mark.parametrize("split", ["auto", "none", "2", "8"])
+@pytest.mark.parametrize("split", ["auto", "none", "2", "4", "5", "7", "8"])
 @pytest.mark.parametrize("case", range(len(ATTN_CASES)))
 def test_tree_attention_parity(monkeypatch, case, split):
     """The key splits: as the launch chooses them, none, or forced small
     split sizes (DARTREE_ATTN_SPLIT_MIN: key tiles per split at least), so
-    that clusters of 2 to 8 CTAs exchange and combine their rows."""
+    that clusters of 2 to 8 CTAs exchange and combine their rows (the
+    combine is instantiated per split count)."""
     if split == "none":
         monkeypatch.setenv("DARTREE_ATTN_SPLIT_MIN", "100000")
     elif split != "auto":
