@@ -918,9 +918,15 @@ extern "C" dartree_status dartree_tree_attention(const void* Q, const void* K, c
   const size_t recv_bytes =
       n_split > 1 ? static_cast<size_t>(n_split - 1) * rs * (kDh * 4 + 8) : 0;
   const size_t smem = smem0 + recv_bytes;
+  // the receive buffer is largest for the split count that maximises
+  // (n - 1) ceil(128 / n) (7: 114 rows), not for the largest count
+  int recv_rows_max = 0;
+  for (int n = 2; n <= kMaxSplit; ++n) {
+    const int rows_n = (n - 1) * ((kQRows + n - 1) / n);
+    recv_rows_max = rows_n > recv_rows_max ? rows_n : recv_rows_max;
+  }
   e = cudaFuncSetAttribute(k_tree_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem0 + static_cast<size_t>(kMaxSplit - 1) *
-                                                        ((kQRows + kMaxSplit - 1) / kMaxSplit) *
+                           static_cast<int>(smem0 + static_cast<size_t>(recv_rows_max) *
                                                         (kDh * 4 + 8)));
   if (e != cudaSuccess) return fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
   const dim3 grid(p.q_tiles * n_split, Hkv, R);
