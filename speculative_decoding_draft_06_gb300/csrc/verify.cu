@@ -17,9 +17,10 @@
 //
 // Warp roles (320 threads): warps 0-7 softmax (two warpgroups; a thread
 // owns a query row = TMEM lane, its group half of each key tile and half of
-// the head dimensions of O), warp 8 TMA producer (128-key tiles of K and of
-// the blocked, transposed value cache, 128-byte swizzle), warp 9 TMEM
-// allocator + single-thread MMA issuer.
+// the head dimensions of O), warp 8 TMA producer (the query tile, and
+// 128-key tiles of K and of the blocked, transposed value cache, 128-byte
+// swizzle, two stages whose keys and values have separate barriers), warp 9
+// TMEM allocator + single-thread MMA issuer.
 // One pass over the CTA's keys with an online softmax: S = Q K^T (M = 128
 // rows, N = 128 keys, K = 128 head dims) into double-buffered TMEM, P =
 // 2^(s - m) rounded to bf16 and stored to tensor memory (double-buffered;
