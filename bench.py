@@ -59,7 +59,24 @@ def parse_args(argv=None):
     ap.add_argument("--vocab", type=int, default=0,
                     help="override V (profiling aid for small ncu captures)")
     ap.add_argument("--variant", choices=sorted(VARIANTS), default="dartree")
+    ap.add_argument("--wout-layout", choices=("blocks", "rows"), default="blocks",
+                    help="layout of the output projection in HBM (bf16): blocks of 128 x 64 "
+                         "(converted once before timing) or row-major")
     return ap.parse_args(argv)
+
+
+def prepare_wout(ctx, dev: dict, bf16: bool, layout: str) -> str:
+    """Puts the output projection in the layout the context will read:
+    converted once, before any timing (the weights do not change between
+    builds).  Returns the layout used."""
+    from speculative_decoding_draft_06_gb300 import dartree as dtl
+    if not bf16 or layout == "rows":
+        return "rows"
+    if not dev.get("wout_blocked"):
+        dev["Wout"] = dtl.block_weights(dev["Wout"])
+        dev["wout_blocked"] = True
+    ctx.set_weight_layout("blocks")
+    return "blocks of 128 x 64 (converted once before timing)"
 
 
 # build variants: options of DARTree.build
@@ -476,6 +493,8 @@ def run_gpu(args) -> None:
     dev = dtl.weights_to_device(inp, w.bf16)
     ctx = dtl.DARTree(w.V, w.H, max_D=w.D, max_W=w.W, max_K=w.K, max_B=w.B,
                       max_requests=w.R, bf16=w.bf16)
+    layout = prepare_wout(ctx, dev, w.bf16, args.wout_layout)
+    torch.cuda.synchronize()
     stream = torch.cuda.Stream()
     out = ctx.alloc_tree(w.R, w.B)
     opt = VARIANTS[args.variant]
@@ -645,7 +664,7 @@ def run_gpu(args) -> None:
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.bf16 else "f32", "data": "synthetic",
-            "config": workload_config(w),
+            "config": dict(workload_config(w), wout_layout=layout),
             "variant": args.variant,
             "head_calls_per_build": ctx.head_calls(),
             "nodes_scored_per_s": (value / w.R * w.candidates_per_build()
@@ -726,6 +745,9 @@ def run_verify(args) -> None:
     H2 = vs.Hq * vs.dh
     rows = w.R * (w.B + 1)
     tgt = dtl.DARTree(w.V, H2, max_D=1, max_W=rows, max_K=1, max_B=1, bf16=True)
+    layout = prepare_wout(ctx, dev, w.bf16, args.wout_layout)
+    if layout != "rows":
+        tgt.set_weight_layout("blocks")
     U = dev["Wout"] if H2 == w.H else None
     if U is None:
         raise SystemExit("verify: the stand-in projection needs H == Hq * dh")
@@ -814,7 +836,7 @@ def run_verify(args) -> None:
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "variant": "verify",
-            "config": dict(workload_config(w), verify=(
+            "config": dict(workload_config(w), wout_layout=layout, verify=(
                 f"target layer: prefix {vs.Lp}, {vs.Hq} query heads, {vs.Hkv} kv heads, head "
                 f"dim {vs.dh}; projection [V, {H2}] (the head's Wout as stand-in)")),
             "roofline": {"bound": "hbm", "kernel": (
@@ -864,6 +886,7 @@ def run_profile_head(args) -> None:
         torch.from_numpy(S).cuda()
     ctx = dtl.DARTree(w.V, w.H, max_D=1, max_W=w.W, max_K=w.K, max_B=w.B, max_requests=w.R,
                       bf16=w.bf16)
+    prepare_wout(ctx, dev, w.bf16, args.wout_layout)
     z = dev["z"][:, 0].contiguous()
     for _ in range(args.profile_head):
         ctx.head_topk(S, z, dev["Wout"], K=w.K, rows_per_req=M // w.R, z_req_stride=w.V)

@@ -94,6 +94,7 @@ struct dartree_ctx {
     dartree_options opt;
     int32_t z_late;  // base logits of depth >= 2 arrive on the copy stream (dartree_build_host):
                      // 1 all before head call 2, 2 each before its own head call
+    int32_t w_layout;  // the layout Wout's tensor map was encoded for
     dartree_tree out;
     cudaStream_t st;
     bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof o) == 0; }
@@ -106,6 +107,7 @@ struct dartree_ctx {
   bool rows_pair = true;   // ... and with more than 128 rows on CTA pairs (two-CTA MMA)
   bool rows_half_s = true;  // ... and with at most 64 rows on one CTA, 64-row state boxes
   bool merge_bound = true;  // row merge through the head call's row bound (k_merge_bound)
+  bool w_tiled = false;     // Wout in blocks of 128 x 64 (dartree_set_weight_layout)
   int merge_surv_cap = 512;  // ... staging at most this many keys (test knob)
   float* pm = nullptr;
   float* ps = nullptr;
@@ -297,6 +299,8 @@ dartree_status run_head(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.H = H;
   p.M = M;
   p.n_tiles = (V + dt::kTileV - 1) / dt::kTileV;
+  p.w_tiled = c->bf16 && c->w_tiled;
+  p.w_nk = H / dt::kTileH;
   p.err = c->d_err;
   p.z = z;
   p.z_req_stride = z_req_stride;
@@ -515,6 +519,8 @@ dartree_status run_cand(dartree_ctx* c, int sbuf, const float* z, long long z_re
   p.cand_req_stride = cand_req_stride;
   p.S = c->S(sbuf);
   p.Wout = Wout;
+  p.w_tiled = c->bf16 && c->w_tiled;
+  p.w_nk = c->cfg.H / dt::kTileH;
   p.pm = c->pm;
   p.ps = c->ps;
   p.ptop = c->ptop;
@@ -545,7 +551,12 @@ dartree_status bind_weights(dartree_ctx* c, const void* A, const void* Wout) {
     c->tm_A_ptr = A;
   }
   if (Wout != nullptr && Wout != c->tm_Wout_ptr) {
-    if ((s = encode_2d(c, &c->tm_Wout, Wout, c->cfg.V, c->cfg.H, dt::kTileV)) != DARTREE_OK)
+    const uint64_t vt = (static_cast<uint64_t>(c->cfg.V) + dt::kTileV - 1) / dt::kTileV;
+    if ((s = c->w_tiled ? encode_2d(c, &c->tm_Wout, Wout,
+                                    vt * (c->cfg.H / dt::kTileH) * dt::kTileV, dt::kTileH,
+                                    dt::kTileV)
+                        : encode_2d(c, &c->tm_Wout, Wout, c->cfg.V, c->cfg.H, dt::kTileV)) !=
+        DARTREE_OK)
       return s;
     c->tm_Wout_ptr = Wout;
   }
@@ -865,6 +876,7 @@ dartree_status build_dispatch(dartree_ctx* c, const float* z, const float* s0,
     return run_build(c, z, s0, head, R, D, W, K, B, beta, o, out, st, z_wait);
   dartree_ctx::GraphKey key{};
   key.z_late = z_late;
+  key.w_layout = c->w_tiled ? DARTREE_LAYOUT_BLOCKS : DARTREE_LAYOUT_ROWS;
   key.opt = o;
   key.z = z;
   key.s0 = s0;
@@ -1322,6 +1334,51 @@ dartree_status dartree_reset_timing(dartree_ctx* ctx) {
 }
 
 int64_t dartree_head_calls(const dartree_ctx* ctx) { return ctx ? ctx->head_calls : -1; }
+
+namespace {
+// Context-free failure: the text goes to dartree_last_error(NULL).
+dartree_status free_fail(dartree_status s, const char* why) {
+  dt::set_context_free_error(why);
+  return s;
+}
+}  // namespace
+
+dartree_status dartree_set_weight_layout(dartree_ctx* ctx, int32_t layout) {
+  if (!ctx) return free_fail(DARTREE_ERR_INVALID_ARG, "null context");
+  if (layout != DARTREE_LAYOUT_ROWS && layout != DARTREE_LAYOUT_BLOCKS)
+    return ctx->fail(DARTREE_ERR_INVALID_ARG, "unknown weight layout %d", layout);
+  if (layout == DARTREE_LAYOUT_BLOCKS && !ctx->bf16)
+    return ctx->fail(DARTREE_ERR_UNSUPPORTED, "the blocked layout needs bf16 weights");
+  const bool tiled = layout == DARTREE_LAYOUT_BLOCKS;
+  if (tiled != ctx->w_tiled) {
+    ctx->w_tiled = tiled;
+    ctx->tm_Wout_ptr = nullptr;  // the next call re-encodes Wout's tensor map
+  }
+  return DARTREE_OK;
+}
+
+size_t dartree_blocked_weight_bytes(int32_t V, int32_t H) {
+  if (V < 1 || H < 1 || H % 64 != 0) return 0;
+  return (static_cast<size_t>(V) + 127) / 128 * 128 * static_cast<size_t>(H) * 2;
+}
+
+dartree_status dartree_block_weights(const void* W, int32_t V, int32_t H, void* W_blocked,
+                                     void* stream) {
+  const size_t bytes = dartree_blocked_weight_bytes(V, H);
+  if (!W || !W_blocked || bytes == 0)
+    return free_fail(DARTREE_ERR_INVALID_ARG, "bad W, W_blocked, V or H");
+  if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(W_blocked)) & 15)
+    return free_fail(DARTREE_ERR_INVALID_ARG, "W and W_blocked must be 16-byte aligned");
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(W), b0 = reinterpret_cast<uintptr_t>(W_blocked);
+  const size_t src_bytes = static_cast<size_t>(V) * H * 2;
+  if (a0 < b0 + bytes && b0 < a0 + src_bytes)
+    return free_fail(DARTREE_ERR_INVALID_ARG, "W and W_blocked overlap");
+  const cudaError_t e =
+      dt::launch_block_weights(static_cast<const uint16_t*>(W), V, H,
+                               static_cast<uint16_t*>(W_blocked), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return free_fail(DARTREE_ERR_CUDA, cudaGetErrorString(e));
+  return DARTREE_OK;
+}
 
 const char* dartree_last_error(const dartree_ctx* ctx) {
   return ctx ? ctx->last_error.c_str() : g_create_error.c_str();

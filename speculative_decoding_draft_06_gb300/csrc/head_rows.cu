@@ -388,8 +388,12 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
             const uint32_t fb = map_to_rank(&full[stage], 0);
             tma_load_2d_pair(dst, &tmap_s, fb, kb * kTileH, static_cast<int>(rank) * 128, pol_s);
-            tma_load_2d_pair(dst + C::kABytes, &tmap_w, fb, kb * kTileH,
-                             t * NV + static_cast<int>(rank) * 128, pol_w);
+            const int wr = t * NV + static_cast<int>(rank) * 128;  // first weight row
+            if (p.w_tiled)
+              tma_load_2d_pair(dst + C::kABytes, &tmap_w, fb, 0, (wr / 128 * p.w_nk + kb) * 128,
+                               pol_w);
+            else
+              tma_load_2d_pair(dst + C::kABytes, &tmap_w, fb, kb * kTileH, wr, pol_w);
           } else {
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
 #pragma unroll
@@ -397,9 +401,15 @@ __global__ void __launch_bounds__(RowsCfg<MH, NV, kPair, kHalfS>::kThreads, 1)
               tma_load_2d(dst + h * (128 * 128), &tmap_s, &full[stage], kb * kTileH, h * 128,
                           pol_s);
 #pragma unroll
-            for (int j = 0; j < NV / 128; ++j)
-              tma_load_2d(dst + C::kABytes + j * (128 * 128), &tmap_w, &full[stage], kb * kTileH,
-                          t * NV + j * 128, pol_w);
+            for (int j = 0; j < NV / 128; ++j) {
+              const int wr = t * NV + j * 128;  // first weight row of the box
+              if (p.w_tiled)
+                tma_load_2d(dst + C::kABytes + j * (128 * 128), &tmap_w, &full[stage], 0,
+                            (wr / 128 * p.w_nk + kb) * 128, pol_w);
+              else
+                tma_load_2d(dst + C::kABytes + j * (128 * 128), &tmap_w, &full[stage],
+                            kb * kTileH, wr, pol_w);
+            }
           }
           ++issued;
           if (++stage == S) {

@@ -235,7 +235,10 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
           uint8_t* a_dst = stage_base + static_cast<size_t>(stage) * L::kStageBytes;
           uint8_t* b_dst = a_dst + L::kABytes;
           mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-          tma_load_2d(a_dst, &tmap_w, &full[stage], kb * kTileH, t * kTileV, pol_w);
+          if (kLogits && p.w_tiled)
+            tma_load_2d(a_dst, &tmap_w, &full[stage], 0, (t * p.w_nk + kb) * kTileV, pol_w);
+          else
+            tma_load_2d(a_dst, &tmap_w, &full[stage], kb * kTileH, t * kTileV, pol_w);
           tma_load_2d(b_dst, &tmap_s, &full[stage], kb * kTileH, 0, pol_s);
           ++issued;
           if (++stage == S) {

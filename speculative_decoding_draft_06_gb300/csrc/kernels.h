@@ -21,6 +21,10 @@ struct TcParams {
   int* err;            // device error word
   long long wait_limit;  // pipeline wait limit in cycles (0: the full ~2 s)
   int V_tok;           // vocabulary size (bound of state-step tokens)
+  int w_tiled;         // logits: the weights in blocks of 128 rows x 64 columns
+                       // (DARTREE_LAYOUT_BLOCKS), block (tile, k step) at row
+                       // (tile * w_nk + k step) * 128 of a [rows][64] tensor map
+  int w_nk;            // k steps of 64 per weight row (H / 64)
   int s_rows;          // row-major head kernel: state rows per TMA box of tmap_s (64: one
                        // CTA with at most 64 live rows and 256-entry tiles; else 128)
   // logits epilogue
@@ -276,7 +280,8 @@ struct CandParams {
   const int32_t* cand;      // this depth's candidates, request 0
   long long cand_req_stride;
   const void* S;            // [M][H] head states (bf16 bits or fp32)
-  const void* Wout;         // [V][H]
+  const void* Wout;         // [V][H], or blocks of 128 x 64 (w_tiled, bf16)
+  int w_tiled, w_nk;        // (w_nk = H / 64)
   float* pm;
   float* ps;
   uint64_t* ptop;
@@ -284,6 +289,11 @@ struct CandParams {
   int* err;
 };
 cudaError_t launch_cand_logits(const CandParams& p, cudaStream_t st);
+
+// Row-major bf16 W [V][H] (H a multiple of 64) -> blocks of 128 rows x 64
+// columns (DARTREE_LAYOUT_BLOCKS), rows past V zero.
+cudaError_t launch_block_weights(const uint16_t* W, int V, int H, uint16_t* out,
+                                 cudaStream_t st);
 
 // Sequential best-first baseline: requests advance in lockstep, one head
 // call (one row per request) per step.  Per request a node table holds every

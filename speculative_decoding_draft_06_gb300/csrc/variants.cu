@@ -142,15 +142,18 @@ constexpr int kCandThreads = 256;
 constexpr int kCandWarps = kCandThreads / 32;
 
 // Dot product of a state row and a weight row (H a multiple of 8 for bf16),
-// lanes striding over 16-byte pieces; fp32 accumulation, warp-reduced.
-__device__ __forceinline__ float warp_dot(const void* s, const void* w, int H, bool bf16) {
+// lanes striding over 16-byte pieces; fp32 accumulation, warp-reduced.  A
+// blocked bf16 row (blocks of 128 rows x 64 columns) has its 16-byte piece i
+// at piece (i / 8) * 1024 + i % 8 from the row's start in its first block.
+__device__ __forceinline__ float warp_dot(const void* s, const void* w, int H, bool bf16,
+                                          bool blocked = false) {
   const int lane = threadIdx.x & 31;
   float acc = 0.f;
   if (bf16) {
     const uint4* a = static_cast<const uint4*>(s);
     const uint4* b = static_cast<const uint4*>(w);
     for (int i = lane; i < H / 8; i += 32) {
-      const uint4 x = __ldg(a + i), y = __ldg(b + i);
+      const uint4 x = __ldg(a + i), y = __ldg(b + (blocked ? (i >> 3) * 1024 + (i & 7) : i));
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -184,8 +187,13 @@ __global__ void __launch_bounds__(kCandThreads) k_cand_logits(const CandParams p
   const uint8_t* srow = static_cast<const uint8_t*>(p.S) + static_cast<size_t>(m) * p.H * eb;
   for (int j = warp; j < p.K; j += kCandWarps) {
     const int c = __ldg(cand + j);
-    const uint8_t* wrow = static_cast<const uint8_t*>(p.Wout) + static_cast<size_t>(c) * p.H * eb;
-    const float dot = warp_dot(srow, wrow, p.H, p.bf16 != 0);
+    const bool blocked = p.bf16 && p.w_tiled;
+    // row c: row-major, or row c % 128 of its first 128 x 64 block
+    const size_t w_off = blocked ? (static_cast<size_t>(c >> 7) * p.w_nk * 8192 +
+                                    static_cast<size_t>(c & 127) * 64) * 2
+                                 : static_cast<size_t>(c) * p.H * eb;
+    const uint8_t* wrow = static_cast<const uint8_t*>(p.Wout) + w_off;
+    const float dot = warp_dot(srow, wrow, p.H, p.bf16 != 0, blocked);
     if (lane == 0) {
       const float e = dot + __ldg(z + c);
       if (e != e || e == INFINITY) atomicOr(p.err, DT_ERR_NONFINITE);
@@ -208,6 +216,37 @@ __global__ void __launch_bounds__(kCandThreads) k_cand_logits(const CandParams p
 
 cudaError_t launch_cand_logits(const CandParams& p, cudaStream_t st) {
   return launch_kernel(k_cand_logits, dim3(p.M), dim3(kCandThreads), 0, st, p.pdl != 0, p);
+}
+
+// The blocked layout of a row-major bf16 matrix: output 16-byte piece o is
+// piece o % 8 of row o / 8 % 128 of block o / 1024 = (b, k) = (block / nk,
+// block % nk), i.e. columns 64 k + 8 (o % 8) .. of row 128 b + o / 8 % 128
+// (zero past V).  Grid-stride; one 16-byte load and store per piece.
+__global__ void k_block_weights(const uint4* __restrict__ W, int V, int H, uint4* __restrict__ out,
+                                long long n_pieces) {
+  const int nk = H / 64;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long o = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; o < n_pieces;
+       o += step) {
+    const long long block = o >> 10;
+    const int within = static_cast<int>(o & 1023);
+    const long long row = (block / nk) * 128 + (within >> 3);
+    const int k = static_cast<int>(block % nk);
+    out[o] = row < V ? __ldg(W + row * (H / 8) + k * 8 + (within & 7)) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_block_weights(const uint16_t* W, int V, int H, uint16_t* out,
+                                 cudaStream_t st) {
+  const long long n_pieces = (static_cast<long long>(V) + 127) / 128 * 128 * (H / 8);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long want = (n_pieces + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+  k_block_weights<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(W), V, H,
+                                        reinterpret_cast<uint4*>(out), n_pieces);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------ best-first baseline

@@ -25,6 +25,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "dartree.h")
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "DEVICE_CHECK",
           5: "TIMEOUT", 6: "OOM"}
 W_F32, W_BF16 = 0, 1
+WEIGHT_LAYOUTS = {"rows": 0, "blocks": 1}
 HEAD_KINDS = {"recurrent": 0, "markov": 1}
 CAND_KINDS = {"corrected": 0, "base": 1}
 EXPANSIONS = {"depthwise": 0, "bestfirst": 1}
@@ -90,6 +91,9 @@ def load():
                                     _i32, _i32, _i32, ctypes.c_float, ctypes.POINTER(Tree), _vp]),
         "dartree_sync_status": (st, [_vp, _vp]),
         "dartree_head_calls": (ctypes.c_int64, [_vp]),
+        "dartree_set_weight_layout": (st, [_vp, _i32]),
+        "dartree_blocked_weight_bytes": (ctypes.c_size_t, [_i32, _i32]),
+        "dartree_block_weights": (st, [_vp, _i32, _i32, _vp, _vp]),
         "dartree_last_error": (ctypes.c_char_p, [_vp]),
         "dartree_get_pool": (st, [_vp, _vp, _vp, _vp, _vp, _vp]),
         "dartree_get_rows": (st, [_vp, _i32, _vp, _vp, _vp, _vp]),
@@ -283,6 +287,12 @@ class DARTree:
             out[k] = (ms.value, n.value)
         return out
 
+    def set_weight_layout(self, layout: str) -> None:
+        """Layout of the Wout passed to later calls: "rows" ([V, H]
+        row-major) or "blocks" (128 x 64 blocks, see block_weights;
+        dartree_set_weight_layout)."""
+        self._check(self._lib.dartree_set_weight_layout(self._h, WEIGHT_LAYOUTS[layout]))
+
     def head_calls(self) -> int:
         return int(self._lib.dartree_head_calls(self._h))
 
@@ -415,6 +425,20 @@ def tree_attention(Q, K, Vt, mask, *, Lp: int, scale: float | None = None,
         _ptr(Q), _ptr(K), _ptr(Vt), _ptr(mask), R, Lp, Bp1 - 1, Hq, Hkv, dh,
         ctypes.c_float(sc), _ptr(O), _ptr(O16), _ptr(work), wb, _ptr(err), _stream(stream)))
     return {"O": O, "O16": O16}
+
+
+def block_weights(W: torch.Tensor, stream=None) -> torch.Tensor:
+    """The blocked layout (blocks of 128 rows x 64 columns, rows past V
+    zero; dartree_block_weights) of a row-major bf16 CUDA matrix [V, H],
+    as a [ceil(V/128) * 128, H] tensor of the same dtype."""
+    _dev(W, "W", _W16)
+    V, H = W.shape
+    n = int(load().dartree_blocked_weight_bytes(V, H))
+    if n == 0:
+        raise ValueError("H must be a multiple of 64")
+    out = torch.empty(n // (2 * H), H, dtype=W.dtype, device=W.device)
+    _check_free(load().dartree_block_weights(_ptr(W), V, H, _ptr(out), _stream(stream)))
+    return out
 
 
 def kv_cache(Kp, Vp, Kt, Vt) -> tuple[torch.Tensor, torch.Tensor]:
