@@ -70,3 +70,24 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(dtl, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         dtl.load()
+
+
+def test_blocked_weight_layout_host_checks(lib):
+    """The blocked layout's size (ceil(V/128) 128 H bf16 elements) and the
+    argument checks of dartree_block_weights / dartree_set_weight_layout,
+    which return before any device call."""
+    assert lib.dartree_blocked_weight_bytes(151936, 4096) == 151936 * 4096 * 2
+    assert lib.dartree_blocked_weight_bytes(1000, 64) == 1024 * 64 * 2
+    assert lib.dartree_blocked_weight_bytes(129, 128) == 256 * 128 * 2
+    for V, H in ((0, 64), (100, 0), (100, 100), (-1, 64)):
+        assert lib.dartree_blocked_weight_bytes(V, H) == 0
+    a, b = ctypes.c_void_p(0x10000000), ctypes.c_void_p(0x20000000)
+    bad = [(None, 100, 64, b),                              # null source
+           (a, 100, 64, None),                              # null destination
+           (a, 100, 100, b),                                # H not a multiple of 64
+           (ctypes.c_void_p(0x10000008), 100, 64, b),       # misaligned
+           (a, 1000, 64, ctypes.c_void_p(0x10000000 + 4096))]  # overlapping
+    for W, V, H, out in bad:
+        assert lib.dartree_block_weights(W, V, H, out, None) == 1  # INVALID_ARG
+        assert lib.dartree_last_error(None)
+    assert lib.dartree_set_weight_layout(None, 1) == 1
