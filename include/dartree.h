@@ -240,8 +240,8 @@ int64_t dartree_head_calls(const dartree_ctx *ctx);
  * strided 128-byte pieces (measured: q8b 3.151 -> 3.088 ms per build, q4b
  * 2.057 -> 1.965).  Results are bit-identical in both layouts.  Convert once
  * with dartree_block_weights (the weights do not change between builds).
- * Returns INVALID_ARG for an unknown layout and UNSUPPORTED for BLOCKS on an
- * fp32 context. */
+ * Returns INVALID_ARG for a NULL context or an unknown layout and
+ * UNSUPPORTED for BLOCKS on an fp32 context. */
 #define DARTREE_LAYOUT_ROWS 0
 #define DARTREE_LAYOUT_BLOCKS 1
 dartree_status dartree_set_weight_layout(dartree_ctx *ctx, int32_t layout);
