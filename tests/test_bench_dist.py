@@ -77,3 +77,28 @@ def test_build_bytes_match_the_closed_forms():
     assert bench.kernels_per_build(I.CONFIGS["tiny"]) == 1 + 8 + 8 + 0 + 1
     wide32 = I.CONFIGS["tiny"].replace(W=20)  # rows 1, 4, 16, 20, ...: depths 1-3 fold
     assert bench.kernels_per_build(wide32) == 1 + 8 + 8 + 4 + 1
+
+
+def test_wout_layout_choice(monkeypatch):
+    """bench.prepare_wout: auto takes the blocked layout except for the
+    base-logit candidate variants (their gathered rows are contiguous only
+    row-major); fp32 weights and `rows` keep the row-major matrix; the
+    conversion runs once per weight set."""
+    from speculative_decoding_draft_06_gb300 import dartree as dtl
+    calls = []
+
+    class Ctx:
+        def set_weight_layout(self, layout):
+            calls.append(layout)
+
+    monkeypatch.setattr(dtl, "block_weights", lambda W: ("blocked", W))
+    dev = {"Wout": "W"}
+    assert bench.prepare_wout(Ctx(), dev, True, "auto", "dartree").startswith("blocks")
+    assert dev["Wout"] == ("blocked", "W") and calls == ["blocks"]
+    bench.prepare_wout(Ctx(), dev, True, "auto", "markov")
+    assert dev["Wout"] == ("blocked", "W")          # not converted twice
+    for bf16, layout, variant in ((True, "auto", "base"), (True, "auto", "markov-base"),
+                                  (False, "blocks", "dartree"), (True, "rows", "dartree")):
+        d = {"Wout": "W"}
+        assert bench.prepare_wout(Ctx(), d, bf16, layout, variant) == "rows"
+        assert d["Wout"] == "W"
