@@ -154,14 +154,17 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // work of this CTA: logits -- a contiguous, balanced range of tiles over
-  // the whole contraction; state -- one tile and one slice of the
-  // contraction (split-K, reduced through global scratch)
+  // work of this CTA: logits -- tiles blockIdx.x, blockIdx.x + gridDim.x,
+  // ... over the whole contraction (the CTAs stream neighbouring tiles at
+  // the same time); state -- one tile and one slice of the contraction
+  // (split-K, reduced through global scratch).  tile_of maps the CTA's
+  // i-th tile to its index.
   const int nk_all = p.H / kTileH;
   int t_begin, t_end, kb_begin = 0, kb_end = nk_all, split = 0;
   if constexpr (kLogits) {
-    t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
-    t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
+    t_begin = 0;
+    t_end = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+            static_cast<int>(gridDim.x);
   } else {
     t_begin = blockIdx.x / p.n_split;
     t_end = t_begin + 1;
@@ -176,6 +179,9 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
   // concentrates the stream on a few DRAM channels.  Rotating the start
   // spreads concurrent CTAs over different offsets.
   const int kb_span = kb_end - kb_begin;
+  auto tile_of = [&](int ti) {
+    return kLogits ? static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x) : ti;
+  };
   auto kb_at = [&](int t, int i) {
     int j = i + (t * 5) % kb_span;
     if (j >= kb_span) j -= kb_span;
@@ -225,7 +231,8 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (int t = t_begin; t < t_end && !*abort_flag; ++t) {
+      for (int ti = t_begin; ti < t_end && !*abort_flag; ++ti) {
+        const int t = tile_of(ti);
         for (int i = 0; i < kb_span; ++i) {
           const int kb = kb_at(t, i);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.wait_limit)) {
@@ -262,7 +269,8 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = t_begin; t < t_end && !*abort_flag; ++t, ++it) {
+      for (int ti = t_begin; ti < t_end && !*abort_flag; ++ti, ++it) {
+        const int t = tile_of(ti);
         const int a = it & 1;
         if (!mbar_wait(&tempty[a], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.err,
                        p.wait_limit)) {
@@ -320,7 +328,8 @@ __global__ void __launch_bounds__(TcRoles<N, kLogits>::kThreads, 1)
     // all rows of one request (the usual case): one base logit per thread
     // and tile, loaded before the accumulator wait
     const bool one_req = kLogits && p.rows_per_req >= p.M;
-    for (int t = t_begin; t < t_end; ++t, ++it) {
+    for (int ti = t_begin; ti < t_end; ++ti, ++it) {
+      const int t = tile_of(ti);
       const int a = it & 1;
       const int row = t * kTileV + wq * 32 + lane;  // vocabulary (or hidden) index
       const bool valid = row < p.rows;
