@@ -240,6 +240,9 @@ int64_t dartree_head_calls(const dartree_ctx *ctx);
  * strided 128-byte pieces (measured: q8b 3.151 -> 3.088 ms per build, q4b
  * 2.057 -> 1.965).  Results are bit-identical in both layouts.  Convert once
  * with dartree_block_weights (the weights do not change between builds).
+ * Base-logit candidates (DARTREE_CAND_BASE) gather K whole rows per head
+ * row, which only the row-major layout keeps contiguous: that variant runs
+ * about 5 % slower blocked.
  * Returns INVALID_ARG for a NULL context or an unknown layout and
  * UNSUPPORTED for BLOCKS on an fp32 context. */
 #define DARTREE_LAYOUT_ROWS 0
